@@ -1,0 +1,254 @@
+"""GB300 (sm_103a) varlen / paged attention: thin Python binding of the C ABI.
+
+Every computation runs in the CUDA kernels of ``libattn_varlen.so`` (built
+in-tree from ``csrc/`` by :func:`build`).  This module only checks and
+marshals arguments: it takes torch CUDA tensors (PyTorch supplies device
+memory and streams) and calls the C entry points of ``include/attn_varlen.h``
+with their raw pointers on the current stream.  There is no fallback: if the
+library is missing or the device is not sm_103 the calls raise.
+
+Entry points (same names as the C ABI):
+    attn_varlen_fwd     varlen prefill, contiguous or paged K/V
+    attn_decode_paged   single-token decode through the paged cache
+    store_kvcache       slot_mapping scatter into the caches
+and the article-shaped wrappers in :mod:`attention_attn_varlen_gb300.attention`.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import re
+
+import torch
+
+from ._build import LIB as _LIB_PATH
+from ._build import build
+
+__all__ = ["attn_varlen_fwd", "attn_decode_paged", "store_kvcache", "get_last_device_error", "lib",
+           "build", "AttnError", "exported_symbols", "decode_num_splits", "decode_workspace_size"]
+
+ATTN_OK = 0
+_STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "workspace too small", 4: "launch failed",
+           5: "device timeout", 6: "device index out of range", 7: "no device"}
+
+
+class AttnError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {_STATUS.get(status, status)} (status {status})")
+
+
+_lib = None
+_c = ctypes
+_vp, _i32, _i64, _f32, _sz = _c.c_void_p, _c.c_int, _c.c_int64, _c.c_float, _c.c_size_t
+
+
+def lib():
+    """The loaded CUDA library (ctypes.CDLL); raises if it was never built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(_LIB_PATH):
+        raise RuntimeError(f"CUDA attention library not built ({_LIB_PATH} missing); "
+                           "run attention_attn_varlen_gb300.build() on a machine with nvcc")
+    L = ctypes.CDLL(_LIB_PATH)
+    L.attn_varlen_fwd.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i64, _i64, _i32, _i32, _i32, _i32, _i32,
+                                  _f32, _i32, _vp, _i32, _i32, _i64, _i64, _i64, _i64, _i64, _vp, _sz, _vp]
+    L.attn_varlen_fwd.restype = _i32
+    L.attn_varlen_workspace_size.argtypes = [_i32, _i32, _i32, _i32]
+    L.attn_varlen_workspace_size.restype = _sz
+    L.attn_decode_paged.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _i64, _i32,
+                                    _f32, _i32, _i64, _i64, _vp, _sz, _vp]
+    L.attn_decode_paged.restype = _i32
+    L.attn_decode_workspace_size.argtypes = [_i32, _i32, _i32, _i32, _i32, _i32]
+    L.attn_decode_workspace_size.restype = _sz
+    L.attn_decode_num_splits.argtypes = [_i32, _i32, _i32, _i32]
+    L.attn_decode_num_splits.restype = _i32
+    L.store_kvcache.argtypes = [_vp, _vp, _vp, _vp, _vp, _i64, _i32, _i32, _i64, _i64, _i64, _vp]
+    L.store_kvcache.restype = _i32
+    L.attn_status_string.argtypes = [_i32]
+    L.attn_status_string.restype = _c.c_char_p
+    L.attn_get_last_device_error.argtypes = [_vp, _c.POINTER(_c.c_uint32)]
+    L.attn_get_last_device_error.restype = _i32
+    L.attn_abi_version.argtypes = []
+    L.attn_abi_version.restype = _i32
+    _lib = L
+    return L
+
+
+def exported_symbols() -> list[str]:
+    """Function names declared in include/attn_varlen.h."""
+    hdr = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "attn_varlen.h")
+    src = open(hdr).read()
+    return re.findall(r"ATTN_API\s+[\w\s\*]+?\b(\w+)\s*\(", src)
+
+
+# --------------------------------------------------------------------------
+# marshalling helpers
+# --------------------------------------------------------------------------
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check(status: int, where: str):
+    if status != ATTN_OK:
+        raise AttnError(status, where)
+
+
+def _rows(t: torch.Tensor, name: str, heads: int, dim: int) -> int:
+    """Row stride (elements) of a [rows, heads, dim] view whose heads and dim are packed."""
+    if t.dim() != 3 or t.shape[1] != heads or t.shape[2] != dim:
+        raise ValueError(f"{name}: expected [rows, {heads}, {dim}], got {tuple(t.shape)}")
+    if t.stride(2) != 1 or t.stride(1) != dim:
+        raise ValueError(f"{name}: heads and head_dim must be packed (strides {t.stride()})")
+    return t.stride(0) if t.shape[0] > 1 else heads * dim
+
+
+def _bf16_cuda(*named):
+    for name, t in named:
+        if t is None:
+            continue
+        if not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor")
+        if t.dtype != torch.bfloat16:
+            raise ValueError(f"{name} must be bfloat16")
+
+
+def _int_cuda(name, t, dtype):
+    if not t.is_cuda or t.dtype != dtype or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous CUDA {dtype} tensor")
+
+
+# --------------------------------------------------------------------------
+# C-ABI bindings
+# --------------------------------------------------------------------------
+
+def attn_varlen_fwd(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, max_seqlen_k: int,
+                    softmax_scale: float | None = None, causal: bool = True, block_table=None,
+                    out=None, lse=None, return_lse: bool = False, stream=None):
+    """Varlen prefill.  q [total_q, Hq, D]; k/v [total_k, Hkv, D] or, with
+    block_table [B, max_blocks] int32, caches [num_blocks, block_size, Hkv, D].
+    Returns out [total_q, Hq, D] (and lse [Hq, total_q] float32 if asked)."""
+    _bf16_cuda(("q", q), ("k", k), ("v", v), ("out", out))
+    _int_cuda("cu_seqlens_q", cu_seqlens_q, torch.int32)
+    _int_cuda("cu_seqlens_k", cu_seqlens_k, torch.int32)
+    total_q, Hq, D = q.shape
+    paged = block_table is not None
+    if paged:
+        _int_cuda("block_table", block_table, torch.int32)
+        if k.dim() != 4 or v.shape != k.shape or not k.is_contiguous() or not v.is_contiguous():
+            raise ValueError("paged k/v must be contiguous [num_blocks, block_size, Hkv, D]")
+        num_blocks, block_size, Hkv, _ = k.shape
+        k_stride = v_stride = Hkv * D
+        total_k = num_blocks * block_size
+        bt_stride = block_table.shape[1]
+    else:
+        Hkv = k.shape[1]
+        k_stride = _rows(k, "k", Hkv, D)
+        v_stride = _rows(v, "v", Hkv, D)
+        total_k = k.shape[0]
+        num_blocks = block_size = bt_stride = 0
+    q_stride = _rows(q, "q", Hq, D)
+    B = cu_seqlens_q.numel() - 1
+    if cu_seqlens_k.numel() != B + 1:
+        raise ValueError("cu_seqlens_q and cu_seqlens_k must have the same length")
+    if out is None:
+        out = torch.empty_like(q, memory_format=torch.contiguous_format)
+    out_stride = _rows(out, "out", Hq, D)
+    if return_lse and lse is None:
+        lse = torch.empty((Hq, total_q), dtype=torch.float32, device=q.device)
+    scale = 1.0 / math.sqrt(D) if softmax_scale is None else float(softmax_scale)
+    L = lib()
+    ws_bytes = L.attn_varlen_workspace_size(B, Hq, Hkv, int(max_seqlen_q))
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device) if ws_bytes else None
+    st = L.attn_varlen_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(cu_seqlens_q), _ptr(cu_seqlens_k),
+                           B, total_q, total_k, int(max_seqlen_q), int(max_seqlen_k), Hq, Hkv, D, scale,
+                           1 if causal else 0, _ptr(block_table), bt_stride, block_size, num_blocks, q_stride,
+                           k_stride, v_stride, out_stride, _ptr(ws), ws_bytes, _stream(stream))
+    _check(st, "attn_varlen_fwd")
+    return (out, lse) if return_lse else out
+
+
+def decode_num_splits(batch: int, num_heads_kv: int, max_cache_seqlen: int, num_splits: int = 0) -> int:
+    return lib().attn_decode_num_splits(batch, num_heads_kv, max_cache_seqlen, num_splits)
+
+
+def decode_workspace_size(batch, num_heads_q, num_heads_kv, head_dim, max_cache_seqlen, num_splits=0) -> int:
+    return lib().attn_decode_workspace_size(batch, num_heads_q, num_heads_kv, head_dim, max_cache_seqlen,
+                                            num_splits)
+
+
+def attn_decode_paged(q, k_cache, v_cache, cache_seqlens, block_table, softmax_scale: float | None = None,
+                      max_cache_seqlen: int | None = None, num_splits: int = 0, out=None, lse=None,
+                      return_lse: bool = False, workspace=None, stream=None):
+    """Decode: q [B, Hq, D] (or [B, 1, Hq, D]); caches [num_blocks, block_size,
+    Hkv, D]; cache_seqlens int32 [B]; block_table int32 [B, max_blocks].
+    max_cache_seqlen defaults to the block table's capacity (no device sync)."""
+    if q.dim() == 4:
+        if q.shape[1] != 1:
+            raise ValueError("attn_decode_paged takes one query token per sequence")
+        q = q[:, 0]
+    _bf16_cuda(("q", q), ("k_cache", k_cache), ("v_cache", v_cache), ("out", out))
+    _int_cuda("cache_seqlens", cache_seqlens, torch.int32)
+    _int_cuda("block_table", block_table, torch.int32)
+    if k_cache.dim() != 4 or v_cache.shape != k_cache.shape or not k_cache.is_contiguous() \
+            or not v_cache.is_contiguous():
+        raise ValueError("caches must be contiguous [num_blocks, block_size, Hkv, D]")
+    B, Hq, D = q.shape
+    num_blocks, block_size, Hkv, _ = k_cache.shape
+    q_stride = _rows(q, "q", Hq, D)
+    if out is None:
+        out = torch.empty((B, Hq, D), dtype=torch.bfloat16, device=q.device)
+    out_stride = _rows(out, "out", Hq, D)
+    if return_lse and lse is None:
+        lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+    if max_cache_seqlen is None:
+        max_cache_seqlen = block_table.shape[1] * block_size
+    scale = 1.0 / math.sqrt(D) if softmax_scale is None else float(softmax_scale)
+    L = lib()
+    ws_bytes = L.attn_decode_workspace_size(B, Hq, Hkv, D, int(max_cache_seqlen), int(num_splits))
+    if workspace is None and ws_bytes:
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device)
+    ws_have = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = L.attn_decode_paged(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(out), _ptr(lse), _ptr(cache_seqlens),
+                             _ptr(block_table), block_table.shape[1], B, Hq, Hkv, D, block_size, num_blocks,
+                             int(max_cache_seqlen), scale, int(num_splits), q_stride, out_stride, _ptr(workspace),
+                             ws_have, _stream(stream))
+    _check(st, "attn_decode_paged")
+    return (out, lse) if return_lse else out
+
+
+def store_kvcache(k, v, k_cache, v_cache, slot_mapping, stream=None):
+    """Scatter k/v [N, Hkv, D] into caches [num_blocks, block_size, Hkv, D] (or
+    any [num_slots, Hkv, D] view) at the flat slots slot_mapping (int64 [N])."""
+    _bf16_cuda(("k", k), ("v", v), ("k_cache", k_cache), ("v_cache", v_cache))
+    _int_cuda("slot_mapping", slot_mapping, torch.int64)
+    N, Hkv, D = k.shape
+    if not k_cache.is_contiguous() or not v_cache.is_contiguous() or k_cache.shape != v_cache.shape:
+        raise ValueError("caches must be contiguous and of the same shape")
+    if k_cache.shape[-2:] != (Hkv, D):
+        raise ValueError("cache head layout does not match k")
+    num_slots = k_cache.numel() // (Hkv * D)
+    ks = _rows(k, "k", Hkv, D)
+    vs = _rows(v, "v", Hkv, D)
+    if slot_mapping.numel() != N:
+        raise ValueError("slot_mapping must have one entry per token")
+    st = lib().store_kvcache(_ptr(k), _ptr(v), _ptr(k_cache), _ptr(v_cache), _ptr(slot_mapping), N, Hkv, D, ks, vs,
+                             num_slots, _stream(stream))
+    _check(st, "store_kvcache")
+
+
+def get_last_device_error(stream=None) -> tuple[int, int]:
+    """Synchronise the stream and read / clear the device error word.
+    Returns (status, raw word)."""
+    word = ctypes.c_uint32(0)
+    st = lib().attn_get_last_device_error(_stream(stream), ctypes.byref(word))
+    return st, word.value

@@ -1,0 +1,390 @@
+// api.cu -- the C ABI (include/attn_varlen.h): argument checks, TMA tensor-map
+// encoding, launch sizing, and the device error word.
+//
+// Call shapes follow "从零实现 vLLM (1.3)：如何加速 Attention 计算", section
+// "Attention 源码分析": store_kvcache(k, v, k_cache, v_cache, slot_mapping),
+// flash_attn_varlen_func(q, k, v, max_seqlen_q, cu_seqlens_q, max_seqlen_k,
+// cu_seqlens_k, softmax_scale, causal, block_table) and
+// flash_attn_with_kvcache(q.unsqueeze(1), k_cache, v_cache, cache_seqlens,
+// block_table, softmax_scale, causal).
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+#include "../../include/attn_varlen.h"
+#include "common.cuh"
+#include "kernels.h"
+
+using namespace attn;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+// one error word per device; kernels get its address
+__device__ uint32_t g_attn_error_word;
+
+struct DevInfo {
+    bool ready = false;
+    int num_sms = 0;
+    int cc_major = 0, cc_minor = 0;
+    uint32_t *err = nullptr;
+};
+DevInfo g_dev[kMaxDevices];
+
+attn_status dev_info(DevInfo **out) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        cudaGetLastError();
+        return ATTN_ERR_NO_DEVICE;
+    }
+    DevInfo &d = g_dev[dev];
+    if (!d.ready) {
+        if (cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&d.cc_major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&d.cc_minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaGetSymbolAddress(reinterpret_cast<void **>(&d.err), g_attn_error_word) != cudaSuccess) {
+            cudaGetLastError();
+            return ATTN_ERR_NO_DEVICE;
+        }
+        d.ready = true;
+    }
+    *out = &d;
+    return ATTN_OK;
+}
+
+// the kernels are built for sm_103a only
+attn_status check_arch(const DevInfo *d) {
+    return (d->cc_major == 10 && d->cc_minor == 3) ? ATTN_OK : ATTN_ERR_UNSUPPORTED;
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    if (!fn) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+        else
+            cudaGetLastError();
+    }
+    return fn;
+}
+
+// bf16 tensor [rows, heads, dim] with a row stride (elements) viewed as a 3-D
+// TMA map (dim, heads, rows), 128-byte swizzle, box (64, box_heads, box_rows).
+bool make_map(CUtensorMap *map, const void *base, int64_t rows, int heads, int dim, int64_t row_stride,
+              int box_heads, int box_rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t gdim[3] = {(cuuint64_t)dim, (cuuint64_t)heads, (cuuint64_t)(rows > 0 ? rows : 1)};
+    cuuint64_t gstride[2] = {(cuuint64_t)dim * 2, (cuuint64_t)row_stride * 2};
+    cuuint32_t box[3] = {64u, (cuuint32_t)box_heads, (cuuint32_t)box_rows};
+    cuuint32_t estr[3] = {1u, 1u, 1u};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), gdim, gstride, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
+
+// Row stride in elements: 0 selects the packed default; otherwise it must
+// cover a row and keep rows 16-byte aligned.
+bool fix_stride(int64_t *stride, int64_t packed) {
+    if (*stride == 0) *stride = packed;
+    return *stride >= packed && (*stride % 8) == 0;
+}
+
+constexpr int kMaxSplits = 64;
+constexpr int kDecodeTile = 64;
+
+int choose_splits(int num_sms, int batch, int num_heads_kv, int max_len, int requested) {
+    if (max_len <= 0) return 1;
+    const int max_tiles = (max_len + kDecodeTile - 1) / kDecodeTile;
+    int s;
+    if (requested > 0) {
+        s = requested;
+    } else {
+        // each split streams at most ~2048 tokens (load balance across very
+        // different lengths), and there are at least ~2 CTAs per SM in total
+        const int s_balance = (max_len + 2047) / 2048;
+        const int64_t units = (int64_t)batch * num_heads_kv;
+        const int s_par = (int)((2LL * 2 * num_sms + units - 1) / units);
+        s = s_balance > s_par ? s_balance : s_par;
+    }
+    if (s > kMaxSplits) s = kMaxSplits;
+    if (s > max_tiles) s = max_tiles;
+    if (s < 1) s = 1;
+    return s;
+}
+
+int split_tokens_for(int max_len, int splits) {
+    int per = (max_len + splits - 1) / splits;
+    return ((per + kDecodeTile - 1) / kDecodeTile) * kDecodeTile;
+}
+
+}  // namespace
+
+extern "C" {
+
+int attn_abi_version(void) { return ATTN_ABI_VERSION; }
+
+const char *attn_status_string(attn_status s) {
+    switch (s) {
+        case ATTN_OK: return "ok";
+        case ATTN_ERR_INVALID_ARG: return "invalid argument";
+        case ATTN_ERR_UNSUPPORTED: return "unsupported configuration or device";
+        case ATTN_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+        case ATTN_ERR_LAUNCH_FAILED: return "CUDA launch or runtime call failed";
+        case ATTN_ERR_DEVICE_TIMEOUT: return "a kernel's bounded wait ran out";
+        case ATTN_ERR_DEVICE_INDEX: return "a device-side index was out of range";
+        case ATTN_ERR_NO_DEVICE: return "no usable CUDA device";
+    }
+    return "unknown status";
+}
+
+attn_status attn_get_last_device_error(void *stream, uint32_t *detail) {
+    DevInfo *d = nullptr;
+    attn_status st = dev_info(&d);
+    if (st != ATTN_OK) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(s) != cudaSuccess) {
+        cudaGetLastError();
+        return ATTN_ERR_LAUNCH_FAILED;
+    }
+    uint32_t word = 0;
+    if (cudaMemcpy(&word, d->err, sizeof word, cudaMemcpyDeviceToHost) != cudaSuccess) {
+        cudaGetLastError();
+        return ATTN_ERR_LAUNCH_FAILED;
+    }
+    if (word) {
+        const uint32_t zero = 0;
+        if (cudaMemcpy(d->err, &zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess) {
+            cudaGetLastError();
+            return ATTN_ERR_LAUNCH_FAILED;
+        }
+    }
+    if (detail) *detail = word;
+    if (word & ERR_INDEX) return ATTN_ERR_DEVICE_INDEX;
+    if (word & ERR_TIMEOUT) return ATTN_ERR_DEVICE_TIMEOUT;
+    return ATTN_OK;
+}
+
+// ---------------------------------------------------------------------------
+size_t attn_varlen_workspace_size(int batch, int num_heads_q, int num_heads_kv, int max_seqlen_q) {
+    (void)batch;
+    (void)num_heads_q;
+    (void)num_heads_kv;
+    (void)max_seqlen_q;
+    return 0;   // the launch needs no scheduler metadata at present
+}
+
+attn_status attn_varlen_fwd(const void *q, const void *k, const void *v, void *out, float *lse,
+                            const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k, int batch, int64_t total_q,
+                            int64_t total_k, int max_seqlen_q, int max_seqlen_k, int num_heads_q, int num_heads_kv,
+                            int head_dim, float softmax_scale, int causal, const int32_t *block_table,
+                            int block_table_stride, int block_size, int64_t num_blocks, int64_t q_row_stride,
+                            int64_t k_row_stride, int64_t v_row_stride, int64_t out_row_stride, void *workspace,
+                            size_t workspace_bytes, void *stream) {
+    (void)workspace;
+    (void)workspace_bytes;
+    (void)max_seqlen_k;
+    if (!q || !k || !v || !out || !cu_seqlens_q || !cu_seqlens_k) return ATTN_ERR_INVALID_ARG;
+    if (batch <= 0 || num_heads_q <= 0 || num_heads_kv <= 0 || num_heads_q % num_heads_kv != 0)
+        return ATTN_ERR_INVALID_ARG;
+    if (total_q < 0 || total_k < 0 || max_seqlen_q < 0 || max_seqlen_k < 0) return ATTN_ERR_INVALID_ARG;
+    if (!(softmax_scale > 0.f) || !isfinite(softmax_scale)) return ATTN_ERR_INVALID_ARG;
+    if (head_dim != 64 && head_dim != 128) return ATTN_ERR_UNSUPPORTED;
+    const int G = num_heads_q / num_heads_kv;
+    if (kPrefillSlotRows % G != 0) return ATTN_ERR_UNSUPPORTED;
+    if (batch > 65535 || num_heads_kv > 65535) return ATTN_ERR_UNSUPPORTED;
+    const bool paged = block_table != nullptr;
+    if (paged) {
+        if (!pow2(block_size) || block_size < 16 || num_blocks <= 0 || block_table_stride <= 0)
+            return ATTN_ERR_INVALID_ARG;
+        if (num_blocks * (int64_t)block_size >= (int64_t)INT32_MAX) return ATTN_ERR_UNSUPPORTED;
+    } else if (total_k >= (int64_t)INT32_MAX) {
+        return ATTN_ERR_UNSUPPORTED;
+    }
+    if (total_q >= (int64_t)INT32_MAX) return ATTN_ERR_UNSUPPORTED;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return ATTN_ERR_INVALID_ARG;
+    if (!fix_stride(&q_row_stride, (int64_t)num_heads_q * head_dim) ||
+        !fix_stride(&out_row_stride, (int64_t)num_heads_q * head_dim) ||
+        !fix_stride(&k_row_stride, (int64_t)num_heads_kv * head_dim) ||
+        !fix_stride(&v_row_stride, (int64_t)num_heads_kv * head_dim))
+        return ATTN_ERR_INVALID_ARG;
+    if (paged && (k_row_stride != (int64_t)num_heads_kv * head_dim || v_row_stride != k_row_stride))
+        return ATTN_ERR_INVALID_ARG;   // caches are packed [num_blocks, block_size, Hkv, D]
+
+    DevInfo *d = nullptr;
+    attn_status st = dev_info(&d);
+    if (st != ATTN_OK) return st;
+    if ((st = check_arch(d)) != ATTN_OK) return st;
+    if (total_q == 0 || max_seqlen_q == 0) return ATTN_OK;
+
+    const int tps = kPrefillSlotRows / G;
+    const int64_t kv_rows = paged ? num_blocks * (int64_t)block_size : total_k;
+    const int kv_box = paged ? (block_size < kPrefillKeyTile ? block_size : kPrefillKeyTile) : kPrefillKeyTile;
+    CUtensorMap qmap, kmap, vmap;
+    if (!make_map(&qmap, q, total_q, num_heads_q, head_dim, q_row_stride, G, tps) ||
+        !make_map(&kmap, k, kv_rows, num_heads_kv, head_dim, k_row_stride, 1, kv_box) ||
+        !make_map(&vmap, v, kv_rows, num_heads_kv, head_dim, v_row_stride, 1, kv_box))
+        return ATTN_ERR_LAUNCH_FAILED;
+
+    PrefillParams p;
+    memset(&p, 0, sizeof p);
+    p.out = reinterpret_cast<__nv_bfloat16 *>(out);
+    p.lse = lse;
+    p.cu_q = cu_seqlens_q;
+    p.cu_k = cu_seqlens_k;
+    p.block_table = block_table;
+    p.total_q = total_q;
+    p.out_row_stride = out_row_stride;
+    p.num_blocks = num_blocks;
+    p.bt_stride = block_table_stride;
+    p.block_size = block_size;
+    p.rows_per_box = kv_box;
+    p.batch = batch;
+    p.Hq = num_heads_q;
+    p.Hkv = num_heads_kv;
+    p.G = G;
+    p.causal = causal ? 1 : 0;
+    p.num_pairs = (max_seqlen_q + 2 * tps - 1) / (2 * tps);
+    p.scale_log2 = softmax_scale * 1.4426950408889634f;
+    p.err = d->err;
+    cudaError_t e = launch_prefill(qmap, kmap, vmap, p, head_dim, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return ATTN_ERR_LAUNCH_FAILED;
+    }
+    return ATTN_OK;
+}
+
+// ---------------------------------------------------------------------------
+int attn_decode_num_splits(int batch, int num_heads_kv, int max_cache_seqlen, int num_splits) {
+    DevInfo *d = nullptr;
+    int sms = 148;
+    if (dev_info(&d) == ATTN_OK) sms = d->num_sms;
+    return choose_splits(sms, batch, num_heads_kv, max_cache_seqlen, num_splits);
+}
+
+size_t attn_decode_workspace_size(int batch, int num_heads_q, int num_heads_kv, int head_dim, int max_cache_seqlen,
+                                  int num_splits) {
+    if (batch <= 0 || num_heads_q <= 0 || num_heads_kv <= 0 || head_dim <= 0) return 0;
+    const int s = attn_decode_num_splits(batch, num_heads_kv, max_cache_seqlen, num_splits);
+    if (s <= 1) return 0;
+    const int splits = (max_cache_seqlen + split_tokens_for(max_cache_seqlen, s) - 1) /
+                       split_tokens_for(max_cache_seqlen, s);
+    if (splits <= 1) return 0;
+    return (size_t)batch * num_heads_q * splits * (head_dim + 1) * sizeof(float) + 256;
+}
+
+attn_status attn_decode_paged(const void *q, const void *k_cache, const void *v_cache, void *out, float *lse,
+                              const int32_t *cache_seqlens, const int32_t *block_table, int block_table_stride,
+                              int batch, int num_heads_q, int num_heads_kv, int head_dim, int block_size,
+                              int64_t num_blocks, int max_cache_seqlen, float softmax_scale, int num_splits,
+                              int64_t q_row_stride, int64_t out_row_stride, void *workspace, size_t workspace_bytes,
+                              void *stream) {
+    if (!q || !k_cache || !v_cache || !out || !cache_seqlens || !block_table) return ATTN_ERR_INVALID_ARG;
+    if (batch <= 0 || num_heads_q <= 0 || num_heads_kv <= 0 || num_heads_q % num_heads_kv != 0)
+        return ATTN_ERR_INVALID_ARG;
+    if (max_cache_seqlen < 0 || num_splits < 0 || block_table_stride <= 0) return ATTN_ERR_INVALID_ARG;
+    if (!(softmax_scale > 0.f) || !isfinite(softmax_scale)) return ATTN_ERR_INVALID_ARG;
+    if (!pow2(block_size) || block_size < 16 || num_blocks <= 0) return ATTN_ERR_INVALID_ARG;
+    if (head_dim != 64 && head_dim != 128) return ATTN_ERR_UNSUPPORTED;
+    const int G = num_heads_q / num_heads_kv;
+    if (G > 8) return ATTN_ERR_UNSUPPORTED;
+    if (batch > 65535 || num_heads_kv > 65535) return ATTN_ERR_UNSUPPORTED;
+    if (num_blocks * (int64_t)block_size >= (int64_t)INT32_MAX) return ATTN_ERR_UNSUPPORTED;
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out)) return ATTN_ERR_INVALID_ARG;
+    if (!fix_stride(&q_row_stride, (int64_t)num_heads_q * head_dim) ||
+        !fix_stride(&out_row_stride, (int64_t)num_heads_q * head_dim))
+        return ATTN_ERR_INVALID_ARG;
+
+    DevInfo *d = nullptr;
+    attn_status st = dev_info(&d);
+    if (st != ATTN_OK) return st;
+    if ((st = check_arch(d)) != ATTN_OK) return st;
+
+    int splits = choose_splits(d->num_sms, batch, num_heads_kv, max_cache_seqlen, num_splits);
+    const int split_tok = split_tokens_for(max_cache_seqlen > 0 ? max_cache_seqlen : 1, splits);
+    splits = max_cache_seqlen > 0 ? (max_cache_seqlen + split_tok - 1) / split_tok : 1;
+    if (splits < 1) splits = 1;
+
+    DecodeParams p;
+    memset(&p, 0, sizeof p);
+    if (splits > 1) {
+        const size_t need = (size_t)batch * num_heads_q * splits * (head_dim + 1) * sizeof(float);
+        if (!workspace || workspace_bytes < need) return ATTN_ERR_WORKSPACE_TOO_SMALL;
+        if ((reinterpret_cast<uintptr_t>(workspace) & 15u) != 0) return ATTN_ERR_INVALID_ARG;
+        p.o_part = reinterpret_cast<float *>(workspace);
+        p.lse_part = p.o_part + (size_t)batch * num_heads_q * splits * head_dim;
+    }
+    const int rpb = block_size < kDecodeTile ? block_size : kDecodeTile;
+    const int64_t rows = num_blocks * (int64_t)block_size;
+    const int64_t row_stride = (int64_t)num_heads_kv * head_dim;
+    CUtensorMap kmap, vmap;
+    if (!make_map(&kmap, k_cache, rows, num_heads_kv, head_dim, row_stride, 1, rpb) ||
+        !make_map(&vmap, v_cache, rows, num_heads_kv, head_dim, row_stride, 1, rpb))
+        return ATTN_ERR_LAUNCH_FAILED;
+    p.q = reinterpret_cast<const __nv_bfloat16 *>(q);
+    p.out = reinterpret_cast<__nv_bfloat16 *>(out);
+    p.lse = lse;
+    p.cache_seqlens = cache_seqlens;
+    p.block_table = block_table;
+    p.q_row_stride = q_row_stride;
+    p.out_row_stride = out_row_stride;
+    p.bt_stride = block_table_stride;
+    p.block_size = block_size;
+    p.rows_per_box = rpb;
+    p.num_splits = splits;
+    p.split_tokens = split_tok;
+    p.num_blocks = num_blocks;
+    p.Hq = num_heads_q;
+    p.Hkv = num_heads_kv;
+    p.G = G;
+    p.scale_log2 = softmax_scale * 1.4426950408889634f;
+    p.err = d->err;
+    cudaError_t e = launch_decode(kmap, vmap, p, batch, head_dim, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return ATTN_ERR_LAUNCH_FAILED;
+    }
+    return ATTN_OK;
+}
+
+// ---------------------------------------------------------------------------
+attn_status store_kvcache(const void *k, const void *v, void *k_cache, void *v_cache, const int64_t *slot_mapping,
+                          int64_t num_tokens, int num_heads_kv, int head_dim, int64_t k_row_stride,
+                          int64_t v_row_stride, int64_t num_slots, void *stream) {
+    if (num_tokens < 0 || num_heads_kv <= 0 || head_dim <= 0 || num_slots < 0) return ATTN_ERR_INVALID_ARG;
+    if (num_tokens == 0) return ATTN_OK;
+    if (!k || !v || !k_cache || !v_cache || !slot_mapping) return ATTN_ERR_INVALID_ARG;
+    const int64_t row = (int64_t)num_heads_kv * head_dim;
+    if (k_row_stride == 0) k_row_stride = row;
+    if (v_row_stride == 0) v_row_stride = row;
+    if (k_row_stride < row || v_row_stride < row) return ATTN_ERR_INVALID_ARG;
+    if (row > (int64_t)INT32_MAX) return ATTN_ERR_UNSUPPORTED;
+    DevInfo *d = nullptr;
+    attn_status st = dev_info(&d);
+    if (st != ATTN_OK) return st;
+    if ((st = check_arch(d)) != ATTN_OK) return st;
+    cudaError_t e = launch_store_kvcache(k, v, k_cache, v_cache, slot_mapping, num_tokens, (int)row, k_row_stride,
+                                         v_row_stride, num_slots, d->num_sms, d->err,
+                                         reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return ATTN_ERR_LAUNCH_FAILED;
+    }
+    return ATTN_OK;
+}
+
+}  // extern "C"

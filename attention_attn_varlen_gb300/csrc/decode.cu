@@ -1,0 +1,379 @@
+// decode.cu -- single-token decode through the paged KV cache
+// ("从零实现 vLLM (1.3)：如何加速 Attention 计算", section "Decode":
+// flash_attn_with_kvcache(q.unsqueeze(1), k_cache, v_cache, cache_seqlens,
+// block_table, softmax_scale, causal=True)), as a split-KV pass plus an exact
+// log-sum-exp combine.
+//
+// The work is HBM-bound: every cached K/V byte of a (sequence, KV head) is read
+// once and serves all G = Hq/Hkv query heads of the group.
+//
+// attn_decode_split_kernel: one CTA per (split, KV head, sequence).
+//   warp 4 (lane 0)   TMA producer: 64-token K and V tiles of the split,
+//                     addressed through the block table, into a 3-stage ring
+//                     of 128-byte-swizzled shared-memory panels.
+//   warps 0-3         consumers: each takes 16 of the 64 tokens of every tile
+//                     and keeps its own online-softmax state (m, d', o') for
+//                     its tokens ("减少遍历次数的“在线 Softmax”" and
+//                     "FlashAttention 的最终实现": running max, proxy
+//                     denominator, proxy output rescaled by 2^(m_old - m_new)).
+//                     S^T = K Q^T and O^T += V^T P^T run on mma.sync m16n8k16
+//                     with the tokens (then head_dim) in M and the G query
+//                     heads (padded to 8) in N; P^T is moved into the
+//                     B-operand layout with movmatrix.  The four warps' states
+//                     are merged exactly at the end.
+// attn_decode_combine_kernel: one warp per (sequence, query head) merges the
+//   split partials: lse = log2 sum_s 2^lse_s, O = sum_s 2^(lse_s - lse) O_s.
+//   This merge is exact because the update is associative ("计算流程（1-Pass
+//   算法与分块）": tiles may be folded in any grouping).
+#include "common.cuh"
+#include "kernels.h"
+
+namespace attn {
+
+constexpr int kDecThreads = 160;   // 4 consumer warps + 1 producer warp
+constexpr int kDecTile = 64;       // tokens per ring stage
+constexpr int kDecStages = 3;
+
+template <int D>
+struct DecSmem {
+    static constexpr int kPanels = D / 64;
+    static constexpr int kPanelBytes = kDecTile * 128;             // 64 rows x 128 B
+    static constexpr int kStageBytes = 2 * kPanels * kPanelBytes;  // K then V
+    static constexpr int kRingBytes = kDecStages * kStageBytes;
+    static constexpr int kBytes = kRingBytes + 1024 /*align slack*/ + 64 /*barriers*/;
+};
+
+
+template <int D>
+__global__ void __launch_bounds__(kDecThreads) attn_decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
+                                                                       const __grid_constant__ CUtensorMap vmap,
+                                                                       const DecodeParams p) {
+    using S = DecSmem<D>;
+    constexpr int KS = D / 16;       // k-steps of the QK^T product
+    extern __shared__ uint8_t dsmem_raw[];
+    uint8_t *ring = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(dsmem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t *full = reinterpret_cast<uint64_t *>(ring + S::kRingBytes);
+    uint64_t *empty = full + kDecStages;
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(empty + kDecStages);
+
+    const int split = blockIdx.x, hkv = blockIdx.y, b = blockIdx.z;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int L = __ldg(p.cache_seqlens + b);
+    const int s0 = split * p.split_tokens;
+    if (L < 0) {
+        if (threadIdx.x == 0) record_error(p.err, ERR_INDEX | SRC_DECODE);
+        return;
+    }
+    if (split == 0 && threadIdx.x == 0 && (int64_t)L > (int64_t)p.num_splits * p.split_tokens)
+        record_error(p.err, ERR_INDEX | SRC_DECODE);   // longer than the stated max_cache_seqlen
+    if (s0 >= L) {
+        // no tokens for this split.  With one split the output is written here.
+        if (p.num_splits == 1 && split == 0 && threadIdx.x < 32 * 4) {
+            for (int i = threadIdx.x; i < p.G * D; i += 128) {
+                const int n = i / D, d = i % D;
+                const int h = hkv * p.G + n;
+                p.out[(int64_t)b * p.out_row_stride + (int64_t)h * D + d] = __float2bfloat16(0.f);
+                if (p.lse && d == 0) p.lse[(int64_t)b * p.Hq + h] = -INFINITY;
+            }
+        }
+        return;
+    }
+    const int s1 = min(L, s0 + p.split_tokens);
+    const int n_tiles = (s1 - s0 + kDecTile - 1) / kDecTile;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kDecStages; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], 4);
+        }
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    if (warp == 4) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            tma_prefetch_desc(&kmap);
+            tma_prefetch_desc(&vmap);
+            const int rpb = p.rows_per_box;
+            const int boxes = kDecTile / rpb;
+            const uint32_t box_bytes = (uint32_t)rpb * 128u;
+            const int32_t *bt = p.block_table + (int64_t)b * p.bt_stride;
+            const int oob_row = (int)(p.num_blocks * p.block_size);   // one past the last row: zero-filled
+            int issued = 0;
+            for (int t = 0; t < n_tiles; ++t) {
+                const int st = t % kDecStages;
+                const uint32_t ph = (uint32_t)(t / kDecStages) & 1u;
+                if (!mbar_wait(&empty[st], ph ^ 1u, abort_flag, p.err, SRC_DECODE)) break;
+                issued = t + 1;
+                const int tok0 = s0 + t * kDecTile;
+                int nb = 0;
+                for (int i = 0; i < boxes; ++i)
+                    if (tok0 + i * rpb < s1) ++nb;
+                mbar_arrive_expect_tx(&full[st], (uint32_t)nb * box_bytes * 2u * S::kPanels);
+                uint8_t *kbase = ring + st * S::kStageBytes;
+                uint8_t *vbase = kbase + S::kPanels * S::kPanelBytes;
+                for (int i = 0; i < nb; ++i) {
+                    const int tok = tok0 + i * rpb;
+                    int blk = __ldg(bt + tok / p.block_size);
+                    int row;
+                    if (blk < 0 || (int64_t)blk >= p.num_blocks) {
+                        record_error(p.err, ERR_INDEX | SRC_DECODE);
+                        row = oob_row;
+                    } else {
+                        row = blk * p.block_size + tok % p.block_size;
+                    }
+#pragma unroll
+                    for (int pn = 0; pn < S::kPanels; ++pn) {
+                        tma_load_3d(kbase + pn * S::kPanelBytes + i * box_bytes, &kmap, &full[st], pn * 64, hkv, row);
+                        tma_load_3d(vbase + pn * S::kPanelBytes + i * box_bytes, &vmap, &full[st], pn * 64, hkv, row);
+                    }
+                }
+            }
+            // keep the CTA (and its shared memory) alive until every copy this
+            // thread issued has landed, even if the consumers gave up
+            for (int t = issued - kDecStages < 0 ? 0 : issued - kDecStages; t < issued; ++t)
+                mbar_wait(&full[t % kDecStages], (uint32_t)(t / kDecStages) & 1u, nullptr, p.err, SRC_DECODE);
+        }
+        return;
+    }
+
+    // ---------------------------------------------------------------- consumers
+    const int g = lane >> 2, c = lane & 3;
+    // Q^T as B fragments: b0 = Q[n=g][16ks + 2c .. +1], b1 = Q[g][16ks + 2c + 8 .. +9]
+    uint32_t qf[KS][2];
+    {
+        const bool valid = g < p.G;
+        const uint32_t *qrow = reinterpret_cast<const uint32_t *>(p.q + (int64_t)b * p.q_row_stride +
+                                                                  (int64_t)(hkv * p.G + (valid ? g : 0)) * D);
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+            qf[ks][0] = valid ? __ldg(qrow + ks * 8 + c) : 0u;
+            qf[ks][1] = valid ? __ldg(qrow + ks * 8 + 4 + c) : 0u;
+        }
+    }
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+    float o[KS][4];
+#pragma unroll
+    for (int i = 0; i < KS; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+
+    const float sl2 = p.scale_log2;
+    bool ok = true;
+    for (int t = 0; t < n_tiles; ++t) {
+        const int st = t % kDecStages;
+        const uint32_t ph = (uint32_t)(t / kDecStages) & 1u;
+        if (!mbar_wait(&full[st], ph, abort_flag, p.err, SRC_DECODE)) { ok = false; break; }
+        const int tok0 = s0 + t * kDecTile;
+        const int nvalid = s1 - tok0;   // >= 1
+        const uint32_t kb = smem_u32(ring + st * S::kStageBytes);
+        const uint32_t vb = kb + S::kPanels * S::kPanelBytes;
+        const int r0 = warp * 16;
+        if (r0 < nvalid) {
+            const bool tail = r0 + 16 > nvalid;
+            if (tail) {
+                // rows past the sequence may hold anything (even NaN): zero this
+                // warp's V rows there so P = 0 never meets a non-finite value
+                uint8_t *vgen = ring + st * S::kStageBytes + S::kPanels * S::kPanelBytes;
+                for (int i = lane; i < 16 * (D / 8); i += 32) {
+                    const int r = r0 + i / (D / 8);
+                    const int ch = i % (D / 8);
+                    if (r >= nvalid)
+                        *reinterpret_cast<uint4 *>(vgen + (ch / 8) * S::kPanelBytes + sw128_off(r, ch % 8)) =
+                            make_uint4(0, 0, 0, 0);
+                }
+                __syncwarp();
+            }
+            // S^T[16 tokens x 8 heads] = K[16 x D] * Q^T[D x 8]
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+            const int arow = r0 + (lane & 7) + ((lane >> 3) & 1) * 8;
+#pragma unroll
+            for (int ks = 0; ks < KS; ++ks) {
+                uint32_t a0, a1, a2, a3;
+                const uint32_t addr = kb + (ks / 4) * S::kPanelBytes + sw128_off(arow, (ks % 4) * 2 + (lane >> 4));
+                ldsm_x4(addr, a0, a1, a2, a3);
+                mma_bf16_16816(acc, a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
+            }
+            // scale into the log2 domain, mask tokens past the sequence
+            float s_0 = acc[0] * sl2, s_1 = acc[1] * sl2, s_2 = acc[2] * sl2, s_3 = acc[3] * sl2;
+            if (r0 + g >= nvalid) s_0 = s_1 = -INFINITY;
+            if (r0 + g + 8 >= nvalid) s_2 = s_3 = -INFINITY;
+            float mx0 = fmaxf(s_0, s_2), mx1 = fmaxf(s_1, s_3);
+#pragma unroll
+            for (int sh = 4; sh < 32; sh <<= 1) {
+                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, sh));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, sh));
+            }
+            const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+            const float a_0 = (m0 == -INFINITY) ? 0.f : ex2(m0 - mn0);
+            const float a_1 = (m1 == -INFINITY) ? 0.f : ex2(m1 - mn1);
+            const float ref0 = (mn0 == -INFINITY) ? 0.f : mn0;
+            const float ref1 = (mn1 == -INFINITY) ? 0.f : mn1;
+            const float p0 = ex2(s_0 - ref0), p2 = ex2(s_2 - ref0);
+            const float p1 = ex2(s_1 - ref1), p3 = ex2(s_3 - ref1);
+            l0 = l0 * a_0 + (p0 + p2);
+            l1 = l1 * a_1 + (p1 + p3);
+            m0 = mn0;
+            m1 = mn1;
+#pragma unroll
+            for (int i = 0; i < KS; ++i) {
+                o[i][0] *= a_0;
+                o[i][1] *= a_1;
+                o[i][2] *= a_0;
+                o[i][3] *= a_1;
+            }
+            // P^T into the B layout: rows = tokens, cols = heads -> transpose
+            const uint32_t bp0 = movmatrix_t(pack_bf16x2(p0, p1));
+            const uint32_t bp1 = movmatrix_t(pack_bf16x2(p2, p3));
+            // O^T[D x 8] += V^T[D x 16 tokens] * P^T[16 x 8]
+            const int mi = lane >> 3;
+            const int vrow = r0 + (lane & 7) + (mi >> 1) * 8;
+#pragma unroll
+            for (int mt = 0; mt < KS; ++mt) {
+                const int ch = 2 * mt + (mi & 1);
+                uint32_t a0, a1, a2, a3;
+                ldsm_x4_t(vb + (ch / 8) * S::kPanelBytes + sw128_off(vrow, ch % 8), a0, a1, a2, a3);
+                mma_bf16_16816(o[mt], a0, a1, a2, a3, bp0, bp1);
+            }
+            if (tail) fence_proxy_async_smem();
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[st]);
+    }
+
+    // ---------------------------------------------------------------- merge the four warps
+    // full per-warp denominators
+#pragma unroll
+    for (int sh = 4; sh < 32; sh <<= 1) {
+        l0 += __shfl_xor_sync(0xffffffffu, l0, sh);
+        l1 += __shfl_xor_sync(0xffffffffu, l1, sh);
+    }
+    // all consumer warps are past the ring: reuse stage memory for the merge
+    asm volatile("bar.sync 1, 128;" ::: "memory");
+    if (*abort_flag) ok = false;
+    float *mo = reinterpret_cast<float *>(ring);          // [4][D][8]
+    float *mm = mo + 4 * D * 8;                           // [4][8]
+    float *ml = mm + 4 * 8;                               // [4][8]
+    if (ok) {
+#pragma unroll
+        for (int mt = 0; mt < KS; ++mt) {
+            const int d = mt * 16 + g;
+            mo[(warp * D + d) * 8 + 2 * c] = o[mt][0];
+            mo[(warp * D + d) * 8 + 2 * c + 1] = o[mt][1];
+            mo[(warp * D + d + 8) * 8 + 2 * c] = o[mt][2];
+            mo[(warp * D + d + 8) * 8 + 2 * c + 1] = o[mt][3];
+        }
+        if (g == 0) {
+            mm[warp * 8 + 2 * c] = m0;
+            mm[warp * 8 + 2 * c + 1] = m1;
+            ml[warp * 8 + 2 * c] = l0;
+            ml[warp * 8 + 2 * c + 1] = l1;
+        }
+    }
+    asm volatile("bar.sync 1, 128;" ::: "memory");
+    if (!ok) return;
+    for (int i = threadIdx.x; i < p.G * D; i += 128) {
+        const int n = i / D, d = i % D;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < 4; ++w) M = fmaxf(M, mm[w * 8 + n]);
+        float Ls = 0.f, O = 0.f;
+        if (M != -INFINITY) {
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
+                const float mw = mm[w * 8 + n];
+                const float f = (mw == -INFINITY) ? 0.f : ex2(mw - M);
+                Ls += ml[w * 8 + n] * f;
+                O += mo[(w * D + d) * 8 + n] * f;
+            }
+        }
+        const int h = hkv * p.G + n;
+        const float on = Ls > 0.f ? O / Ls : 0.f;
+        const float l2 = Ls > 0.f ? M + __log2f(Ls) : -INFINITY;
+        if (p.num_splits == 1) {
+            p.out[(int64_t)b * p.out_row_stride + (int64_t)h * D + d] = __float2bfloat16(on);
+            if (p.lse && d == 0) p.lse[(int64_t)b * p.Hq + h] = l2 * 0.69314718055994531f;
+        } else {
+            const int64_t row = ((int64_t)b * p.Hq + h) * p.num_splits + split;
+            p.o_part[row * D + d] = on;
+            if (d == 0) p.lse_part[row] = l2;
+        }
+    }
+}
+
+// One warp per (sequence, query head): exact merge of the split partials.
+template <int D>
+__global__ void __launch_bounds__(128) attn_decode_combine_kernel(const DecodeParams p, int total_rows) {
+    const int w = blockIdx.x * 4 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (w >= total_rows) return;
+    const int b = w / p.Hq, h = w % p.Hq;
+    const int L = __ldg(p.cache_seqlens + b);
+    int ns = L <= 0 ? 0 : (L + p.split_tokens - 1) / p.split_tokens;
+    if (ns > p.num_splits) ns = p.num_splits;
+    const int64_t row0 = (int64_t)w * p.num_splits;
+    float la = lane < ns ? p.lse_part[row0 + lane] : -INFINITY;
+    float lb = lane + 32 < ns ? p.lse_part[row0 + lane + 32] : -INFINITY;
+    float M = fmaxf(la, lb);
+#pragma unroll
+    for (int sh = 16; sh > 0; sh >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, sh));
+    const float wa = (la == -INFINITY) ? 0.f : ex2(la - M);
+    const float wb = (lb == -INFINITY) ? 0.f : ex2(lb - M);
+    float Ls = wa + wb;
+#pragma unroll
+    for (int sh = 16; sh > 0; sh >>= 1) Ls += __shfl_xor_sync(0xffffffffu, Ls, sh);
+    constexpr int PER = D / 32;
+    float acc[PER];
+#pragma unroll
+    for (int i = 0; i < PER; ++i) acc[i] = 0.f;
+    for (int s = 0; s < ns; ++s) {
+        const float ws = __shfl_sync(0xffffffffu, s < 32 ? wa : wb, s & 31);
+        const float *src = p.o_part + (row0 + s) * D + lane * PER;
+        if (PER == 4) {
+            const float4 v4 = *reinterpret_cast<const float4 *>(src);
+            acc[0] += ws * v4.x;
+            acc[1] += ws * v4.y;
+            acc[2] += ws * v4.z;
+            acc[3] += ws * v4.w;
+        } else {
+#pragma unroll
+            for (int i = 0; i < PER; ++i) acc[i] += ws * src[i];
+        }
+    }
+    const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
+    __nv_bfloat16 *dst = p.out + (int64_t)b * p.out_row_stride + (int64_t)h * D + lane * PER;
+#pragma unroll
+    for (int i = 0; i < PER; ++i) dst[i] = __float2bfloat16(acc[i] * inv);
+    if (p.lse && lane == 0)
+        p.lse[(int64_t)b * p.Hq + h] = Ls > 0.f ? (M + __log2f(Ls)) * 0.69314718055994531f : -INFINITY;
+}
+
+template <int D>
+static cudaError_t launch_decode_t(const CUtensorMap &kmap, const CUtensorMap &vmap, const DecodeParams &p,
+                                   int batch, cudaStream_t stream) {
+    using S = DecSmem<D>;
+    static bool attr_done[64] = {false};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 64 && !attr_done[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(attn_decode_split_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             S::kBytes);
+        if (e != cudaSuccess) return e;
+        attr_done[dev] = true;
+    }
+    dim3 grid(p.num_splits, p.Hkv, batch);
+    attn_decode_split_kernel<D><<<grid, kDecThreads, S::kBytes, stream>>>(kmap, vmap, p);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess || p.num_splits == 1) return e;
+    const int rows = batch * p.Hq;
+    attn_decode_combine_kernel<D><<<(rows + 3) / 4, 128, 0, stream>>>(p, rows);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_decode(const CUtensorMap &kmap, const CUtensorMap &vmap, const DecodeParams &p, int batch,
+                          int head_dim, cudaStream_t stream) {
+    if (head_dim == 128) return launch_decode_t<128>(kmap, vmap, p, batch, stream);
+    return launch_decode_t<64>(kmap, vmap, p, batch, stream);
+}
+
+}  // namespace attn

@@ -1,0 +1,58 @@
+// kernels.h -- host-side declarations shared by the C-ABI layer (api.cu) and
+// the kernel translation units.  Parameter blocks are plain structs passed by
+// value to the kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace attn {
+
+struct DecodeParams {
+    const __nv_bfloat16 *q;      // [B, Hq, D], row stride q_row_stride
+    __nv_bfloat16 *out;          // [B, Hq, D], row stride out_row_stride
+    float *lse;                  // [B, Hq] or null
+    float *o_part;               // [B, Hq, S, D]  split partial outputs (normalised)
+    float *lse_part;             // [B, Hq, S]     split partial log2-sum-exp
+    const int32_t *cache_seqlens;
+    const int32_t *block_table;
+    int64_t q_row_stride, out_row_stride;
+    int bt_stride, block_size, rows_per_box, num_splits, split_tokens;
+    int64_t num_blocks;
+    int Hq, Hkv, G;
+    float scale_log2;            // softmax_scale * log2(e)
+    uint32_t *err;
+};
+
+struct PrefillParams {
+    __nv_bfloat16 *out;          // [total_q, Hq, D], row stride out_row_stride
+    float *lse;                  // [Hq, total_q] or null
+    const int32_t *cu_q, *cu_k;
+    const int32_t *block_table;  // null: contiguous K/V
+    int64_t total_q, out_row_stride;
+    int64_t num_blocks;
+    int bt_stride, block_size, rows_per_box;
+    int batch, Hq, Hkv, G, causal;
+    int num_pairs;               // grid.x: slot pairs per (sequence, KV head) at max_seqlen_q
+    float scale_log2;            // softmax_scale * log2(e), > 0
+    uint32_t *err;
+};
+
+cudaError_t launch_store_kvcache(const void *k, const void *v, void *k_cache, void *v_cache,
+                                 const int64_t *slot_mapping, int64_t num_tokens, int row_elems,
+                                 int64_t k_stride, int64_t v_stride, int64_t num_slots, int num_sms,
+                                 uint32_t *err, cudaStream_t stream);
+
+cudaError_t launch_decode(const CUtensorMap &kmap, const CUtensorMap &vmap, const DecodeParams &p, int batch,
+                          int head_dim, cudaStream_t stream);
+
+// rows per query slot of the prefill kernel (a slot packs 128 / G tokens x G heads)
+constexpr int kPrefillSlotRows = 128;
+constexpr int kPrefillKeyTile = 128;
+
+cudaError_t launch_prefill(const CUtensorMap &qmap, const CUtensorMap &kmap, const CUtensorMap &vmap,
+                           const PrefillParams &p, int head_dim, cudaStream_t stream);
+
+}  // namespace attn

@@ -1,0 +1,520 @@
+"""Throughput of the attention hot path on GB300, one JSON line on stdout.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Main line: varlen causal prefill, 16 sequences with L ~ U{256..4096} (Lq = Lk),
+GQA 32/8, head_dim 128, bf16 (the prefill half of the metric), in TFLOP/s of
+algorithmic work (4 * D * Hq * visible pairs).  One step = one attn_varlen_fwd
+call over the batch.  L2 is flushed (a 512 MB write) between timed steps,
+outside the timed events.  The same line carries the decode half of the metric
+(256-sequence paged decode, KV GB/s) and the other workloads as extra objects,
+each with its roofline, plus:
+  roofline      dominant kernel: algorithmic FLOPs per launch / event time,
+                against MEASURED_PEAKS.json
+  cpu_baseline  the float64 oracle on a bounded sample of the same workload,
+                timed on this host's cores (rank 0, N = 1 only)
+  e2e           the same metric through the public call with host buffers:
+                pinned host -> device copies of q, k, v, cu_seqlens, the kernel,
+                and the device -> host copy of the output, all inside the events
+  clocks        nvidia-smi samples taken while the measurements ran
+
+Under torchrun (N > 1) every rank runs its own independent batch (replicas,
+weak scaling: the units never need another rank's data); the timing is
+bracketed by barriers and the maximum over ranks is reported.
+
+--impl reference times the oracle itself as the reference arm (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+METRIC = "prefill TFLOP/s & decode KV GB/s at 1 GB300; % of tensor/HBM roofline"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_FLUSH_BYTES = 512 << 20
+
+
+# --------------------------------------------------------------------------
+# distributed plumbing (host side only; no collective on the data path)
+# --------------------------------------------------------------------------
+
+def dist_env():
+    return int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0")), int(
+        os.environ.get("WORLD_SIZE", "1"))
+
+
+def dist_init(backend: str):
+    import torch.distributed as dist
+    if dist.is_available() and not dist.is_initialized():
+        dist.init_process_group(backend=backend)
+
+
+def dist_barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+def dist_max(x: float, device=None) -> float:
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate(units_per_rank: float, max_seconds: float, world: int) -> float:
+    """Whole-job throughput: the units all ranks processed / the slowest rank's time."""
+    return units_per_rank * world / max_seconds
+
+
+# --------------------------------------------------------------------------
+# peaks, clocks, profile data
+# --------------------------------------------------------------------------
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {k: float(d[k]) for k in ("hbm_gbs", "bf16_tflops", "bf16_tflops_sustained")}, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi -lms sampling in the background while measurements run."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.file = None
+
+    def start(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile(mode="w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=self.file, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.file.flush()
+        rows = []
+        with open(self.file.name) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    rows.append((float(parts[1]), float(parts[2]), float(parts[3]), parts[5:9]))
+                except ValueError:
+                    continue
+        os.unlink(self.file.name)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        pw = np.array([r[2] for r in rows])
+        loaded = [r for r in rows if r[2] >= 0.5 * pw.max()] or rows
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in loaded for i, v in enumerate(r[3]) if v.lower() == "active"})
+        return {"sm_mhz": float(np.median([r[0] for r in loaded])), "sm_max_mhz": float(max(r[1] for r in rows)),
+                "reasons": reasons, "samples": len(loaded), "power_w_max": float(pw.max())}
+
+
+def src_digest(files) -> str:
+    h = hashlib.sha256()
+    for f in files:
+        h.update(open(os.path.join(ROOT, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+KERNEL_SOURCES = {
+    "prefill": ["attention_attn_varlen_gb300/csrc/prefill.cu", "attention_attn_varlen_gb300/csrc/common.cuh"],
+    "decode": ["attention_attn_varlen_gb300/csrc/decode.cu", "attention_attn_varlen_gb300/csrc/common.cuh"],
+    "store": ["attention_attn_varlen_gb300/csrc/store_kvcache.cu"],
+}
+
+
+def ncu_traffic(kernel: str, units: float):
+    """DRAM bytes per launch from the committed ncu summary, scaled to `units`
+    (the summary stores bytes per unit of work and the source digest of the
+    kernel it was taken on); None if absent or the kernel changed since."""
+    p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p)).get(kernel)
+    if not d or d.get("src_digest") != src_digest(KERNEL_SOURCES[kernel]):
+        return None
+    return float(d["dram_bytes_per_unit"]) * units
+
+
+# --------------------------------------------------------------------------
+# timing helpers
+# --------------------------------------------------------------------------
+
+def time_steps(fn, steps: int, flush=None):
+    """Per-step CUDA-event times (ms) on the current stream; `flush` runs
+    between steps outside the events."""
+    import torch
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for a, b in evs:
+        if flush is not None:
+            flush()
+        a.record()
+        fn()
+        b.record()
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in evs]
+
+
+# --------------------------------------------------------------------------
+# workloads on the device
+# --------------------------------------------------------------------------
+
+def varlen_inputs(cfg, device):
+    import torch
+    return dict(q=cfg.q().to(device), k=cfg.k().to(device), v=cfg.v().to(device),
+                cu_q=torch.from_numpy(cfg.cu_q).to(device), cu_k=torch.from_numpy(cfg.cu_k).to(device),
+                mq=int(cfg.lens_q.max()), mk=int(cfg.lens_k.max()))
+
+
+def bench_varlen(av, cfg, inp, steps, warmup, flush):
+    import torch
+    out = torch.empty_like(inp["q"])
+
+    def step():
+        av.attn_varlen_fwd(inp["q"], inp["k"], inp["v"], inp["cu_q"], inp["cu_k"], inp["mq"], inp["mk"], cfg.scale,
+                           out=out)
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    dist_barrier()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    ms = time_steps(step, steps, flush)
+    torch.cuda.synchronize()
+    dist_barrier()
+    wall = time.perf_counter() - t0
+    return ms, wall
+
+
+def bench_varlen_e2e(av, cfg, inp, steps, warmup, flush):
+    """Host buffers in, host buffer out, through the public call."""
+    import torch
+    hq, hk, hv = (inp[n].cpu().pin_memory() for n in ("q", "k", "v"))
+    hcq, hck = inp["cu_q"].cpu().pin_memory(), inp["cu_k"].cpu().pin_memory()
+    hout = torch.empty(hq.shape, dtype=hq.dtype).pin_memory()
+    dq, dk, dv = torch.empty_like(inp["q"]), torch.empty_like(inp["k"]), torch.empty_like(inp["v"])
+    dcq, dck = torch.empty_like(inp["cu_q"]), torch.empty_like(inp["cu_k"])
+    dout = torch.empty_like(inp["q"])
+
+    def step():
+        dq.copy_(hq, non_blocking=True)
+        dk.copy_(hk, non_blocking=True)
+        dv.copy_(hv, non_blocking=True)
+        dcq.copy_(hcq, non_blocking=True)
+        dck.copy_(hck, non_blocking=True)
+        av.attn_varlen_fwd(dq, dk, dv, dcq, dck, inp["mq"], inp["mk"], cfg.scale, out=dout)
+        hout.copy_(dout, non_blocking=True)
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    ms = time_steps(step, steps, flush)
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hcq, hck))
+    d2h = hout.numel() * hout.element_size()
+    return ms, h2d, d2h
+
+
+def bench_decode(av, device, steps, warmup, flush, peaks):
+    import torch
+    cfg = workloads.make("c4_decode")
+    kc = torch.empty((cfg.num_blocks, cfg.block_size, cfg.Hkv, cfg.D), dtype=torch.bfloat16, device=device)
+    vc = torch.empty_like(kc)
+    workloads.fill_paged_cache(cfg, kc, vc)
+    q = cfg.q().to(device)
+    cs = torch.from_numpy(cfg.ctx.astype(np.int32)).to(device)
+    bt = torch.from_numpy(cfg.block_table).to(device)
+    out = torch.empty_like(q)
+    mx = int(cfg.ctx.max())
+    ws_bytes = av.decode_workspace_size(cfg.batch, cfg.Hq, cfg.Hkv, cfg.D, mx, 0)
+    ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=device)
+    splits = av.decode_num_splits(cfg.batch, cfg.Hkv, mx, 0)
+
+    def step():
+        av.attn_decode_paged(q, kc, vc, cs, bt, cfg.scale, max_cache_seqlen=mx, out=out, workspace=ws)
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    ms = time_steps(step, steps, flush)
+    t = float(np.mean(ms)) / 1e3
+    nbytes = workloads.decode_bytes(cfg.ctx, cfg.Hq, cfg.Hkv, cfg.D, cfg.block_size)
+    gbs = nbytes / t / 1e9
+    res = {"workload": "c4_decode: 256 seqs x 1 token, cache_seqlens U{128..16384}, GQA 32/8, D128, "
+                       "block_size 256, random block table",
+           "value": gbs, "unit": "GB/s", "ms_per_step": t * 1e3, "num_splits": splits,
+           "algorithmic_bytes": nbytes,
+           "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                        "frac": gbs / peaks["hbm_gbs"],
+                        "traffic": ncu_traffic("decode", float(cfg.ctx.sum()) * cfg.Hkv)},
+           "launches_per_step": 2 if splits > 1 else 1}
+    del kc, vc
+    torch.cuda.empty_cache()
+    return res
+
+
+def bench_prefix(av, device, steps, warmup, flush, peaks):
+    import torch
+    cfg = workloads.make("c3_prefix_paged")
+    kc = torch.empty((cfg.num_blocks, cfg.block_size, cfg.Hkv, cfg.D), dtype=torch.bfloat16, device=device)
+    vc = torch.empty_like(kc)
+    workloads.fill_paged_cache(cfg, kc, vc)
+    q = cfg.q().to(device)
+    k_new, v_new = cfg.k_new().to(device), cfg.v_new().to(device)
+    slots = torch.from_numpy(cfg.slot_mapping()).to(device)
+    cu_q = torch.from_numpy(workloads.cu_from_lens(cfg.new)).to(device)
+    cu_k = torch.from_numpy(workloads.cu_from_lens(cfg.lens_k)).to(device)
+    bt = torch.from_numpy(cfg.block_table).to(device)
+    out = torch.empty_like(q)
+    mq, mk = int(cfg.new.max()), int(cfg.lens_k.max())
+
+    def store():
+        av.store_kvcache(k_new, v_new, kc, vc, slots)
+
+    def attn():
+        av.attn_varlen_fwd(q, kc, vc, cu_q, cu_k, mq, mk, cfg.scale, block_table=bt, out=out)
+
+    def step():
+        store()
+        attn()
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    ms = time_steps(step, steps, flush)
+    ms_attn = time_steps(attn, steps, flush)
+    ms_store = time_steps(store, steps, flush)
+    flops = workloads.prefill_flops(cfg.new, cfg.lens_k, cfg.Hq, cfg.D)
+    sbytes = workloads.store_bytes(int(cfg.new.sum()), cfg.Hkv, cfg.D)
+    t = float(np.mean(ms)) / 1e3
+    ta = float(np.mean(ms_attn)) / 1e3
+    ts = float(np.mean(ms_store)) / 1e3
+    res = {"workload": "c3_prefix_paged: 32 seqs, context U{512..8192} + 1..512 new tokens, GQA 32/8, D128, "
+                       "block_size 256, 65536-block pool, 8 seqs share prefix blocks; step = store_kvcache + "
+                       "paged prefill",
+           "value": flops / t / 1e12, "unit": "TFLOP/s", "ms_per_step": t * 1e3,
+           "attn_ms": ta * 1e3, "store_ms": ts * 1e3,
+           "roofline": {"bound": "tensor", "achieved": flops / ta / 1e12, "peak": peaks["bf16_tflops"],
+                        "unit": "TFLOP/s", "frac": flops / ta / 1e12 / peaks["bf16_tflops"], "traffic": None},
+           "store_kvcache": {"value": sbytes / ts / 1e9, "unit": "GB/s", "frac": sbytes / ts / 1e9 / peaks["hbm_gbs"],
+                             "tokens": int(cfg.new.sum())},
+           "launches_per_step": 2}
+    del kc, vc
+    torch.cuda.empty_cache()
+    return res
+
+
+def bench_long(av, device, steps, warmup, flush, peaks):
+    import torch
+    cfg = workloads.make("c5_long")
+    inp = varlen_inputs(cfg, device)
+    ms, _ = bench_varlen(av, cfg, inp, steps, warmup, flush)
+    flops = workloads.prefill_flops(cfg.lens_q, cfg.lens_k, cfg.Hq, cfg.D)
+    t = float(np.mean(ms)) / 1e3
+    res = {"workload": "c5_long: 2 x 32768 tokens, MHA 32 heads, D128, heads 0-15 with Q x160 (logits ~700)",
+           "value": flops / t / 1e12, "unit": "TFLOP/s", "ms_per_step": t * 1e3,
+           "roofline": {"bound": "tensor", "achieved": flops / t / 1e12, "peak": peaks["bf16_tflops_sustained"],
+                        "unit": "TFLOP/s", "frac": flops / t / 1e12 / peaks["bf16_tflops_sustained"],
+                        "traffic": None}}
+    del inp
+    torch.cuda.empty_cache()
+    return res
+
+
+# --------------------------------------------------------------------------
+# the oracle on this host (CPU baseline / reference arm)
+# --------------------------------------------------------------------------
+
+def oracle_sample_run(cfg, q, k, v, rows):
+    import oracle
+    t0 = time.perf_counter()
+    oracle.attn_varlen(q, k, v, cfg.cu_q, cfg.cu_k, cfg.Hq, cfg.Hkv, cfg.D, cfg.scale, True, rows=rows)
+    return time.perf_counter() - t0
+
+
+def rows_flops(cfg, rows):
+    """Algorithmic flops of the sampled query rows (4 * D * visible keys each)."""
+    t = rows // cfg.Hq
+    b = np.searchsorted(cfg.cu_q, t, side="right") - 1
+    i = t - cfg.cu_q[b]
+    Lq = cfg.lens_q[b]
+    Lk = cfg.lens_k[b]
+    vis = np.clip(Lk - Lq + i + 1, 0, Lk)
+    return float(4 * cfg.D * vis.sum())
+
+
+def cpu_baseline(cfg, q, k, v, target_s: float = 12.0):
+    import oracle
+    oracle.build()
+    n_rows = q.shape[0] * cfg.Hq
+    cal = workloads.sample_rows(cfg.seed + 77, n_rows, 1.0, cap=2000)
+    t_cal = oracle_sample_run(cfg, q, k, v, cal)
+    rate = rows_flops(cfg, cal) / max(t_cal, 1e-6)
+    per_row = rows_flops(cfg, cal) / len(cal)
+    n = int(min(n_rows, max(2000, target_s * rate / per_row)))
+    rows = workloads.sample_rows(cfg.seed + 78, n_rows, 1.0, cap=n)
+    t = oracle_sample_run(cfg, q, k, v, rows)
+    fl = rows_flops(cfg, rows)
+    return {"value": fl / t / 1e12, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"{len(rows)} of {n_rows} query rows (uniform over sequence, head, position) of "
+                      f"{cfg.name}; {fl / 1e9:.1f} GFLOP in {t:.1f} s; float64 three-step attention, OpenMP",
+            "seconds": t}
+
+
+def run_reference(args):
+    rank, _, world = dist_env()
+    if rank != 0:
+        return
+    cfg = workloads.make("c2_varlen_gqa")
+    q, k, v = cfg.q(), cfg.k(), cfg.v()
+    import oracle
+    oracle.build()
+    n_rows = q.shape[0] * cfg.Hq
+    # each step: a bounded sample (about 2 s of host time)
+    cal = workloads.sample_rows(cfg.seed + 90, n_rows, 1.0, cap=1000)
+    t_cal = oracle_sample_run(cfg, q, k, v, cal)
+    n = int(min(n_rows, max(500, 2.0 / max(t_cal, 1e-6) * len(cal))))
+    for w in range(args.warmup):
+        oracle_sample_run(cfg, q, k, v, workloads.sample_rows(cfg.seed + 100 + w, n_rows, 1.0, cap=n))
+    times, flops = [], []
+    for s in range(args.steps):
+        rows = workloads.sample_rows(cfg.seed + 200 + s, n_rows, 1.0, cap=n)
+        times.append(oracle_sample_run(cfg, q, k, v, rows))
+        flops.append(rows_flops(cfg, rows))
+    value = sum(flops) / sum(times) / 1e12
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * float(np.mean(times)),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
+            "config": {"workload": "c2_varlen_gqa", "global_batch": 16, "seq_len": "U{256..4096}",
+                       "sample_rows_per_step": n},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
+                             "sample": f"{n} query rows per step of c2_varlen_gqa"},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------------------
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--only-main", action="store_true", help="skip the extra workloads")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+
+    if args.impl == "reference":
+        run_reference(args)
+        return
+
+    import torch
+    rank, local_rank, world = dist_env()
+    if world > 1:
+        torch.cuda.set_device(local_rank)
+        dist_init("nccl")
+    device = torch.device("cuda", torch.cuda.current_device())
+    import attention_attn_varlen_gb300 as av
+    av.build()
+    av.lib()
+    peaks, peak_src = load_peaks()
+
+    flush_buf = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=device)
+
+    def flush():
+        flush_buf.zero_()
+
+    sampler = ClockSampler(torch.cuda.current_device())
+    sampler.start()
+
+    cfg = workloads.make("c2_varlen_gqa")
+    if rank:
+        # an independent batch per rank (same shapes, other values)
+        cfg.seed += 1000 * rank
+    inp = varlen_inputs(cfg, device)
+    flops = workloads.prefill_flops(cfg.lens_q, cfg.lens_k, cfg.Hq, cfg.D)
+    ms, wall = bench_varlen(av, cfg, inp, args.steps, args.warmup, flush)
+    ms_mean = float(np.mean(ms))
+    ms_max = dist_max(ms_mean, device)
+    value = aggregate(flops, ms_max / 1e3, world) / 1e12
+    achieved = flops / (ms_mean / 1e3) / 1e12
+    e2e_ms, h2d, d2h = bench_varlen_e2e(av, cfg, inp, args.steps, args.warmup, flush)
+    e2e_max = dist_max(float(np.mean(e2e_ms)), device)
+
+    extras = {}
+    if not args.only_main:
+        extras["decode"] = bench_decode(av, device, args.steps, args.warmup, flush, peaks)
+        extras["prefix_prefill"] = bench_prefix(av, device, args.steps, args.warmup, flush, peaks)
+        extras["long_prefill"] = bench_long(av, device, max(3, args.steps // 3), args.warmup, flush, peaks)
+    clocks = sampler.stop()
+
+    status, word = av.get_last_device_error()
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "c2_varlen_gqa: varlen causal prefill, 16 seqs, L ~ U{256..4096} (Lq = Lk), "
+                               "GQA 32/8, head_dim 128, bf16, packed by cu_seqlens",
+                   "global_batch": 16 * world, "seq_len": "U{256..4096}", "total_tokens": int(cfg.lens_q.sum()),
+                   "algorithmic_flops": flops, "l2": "flushed between timed steps (512 MB write)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                     "frac": achieved / peaks["bf16_tflops"],
+                     "traffic": ncu_traffic("prefill", float(cfg.lens_q.sum())),
+                     "peak_source": f"{peak_src} bf16 burst (MEASURED_PEAKS.json)" if peak_src == "measured"
+                     else "fallback 1.9 PFLOP/s"},
+        "e2e": {"value": aggregate(flops, e2e_max / 1e3, world) / 1e12, "unit": "TFLOP/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_max},
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+        "wall_s_timed": wall,
+        "device_status": status,
+    }
+    line.update(extras)
+    if rank == 0 and world == 1:
+        line["cpu_baseline"] = cpu_baseline(cfg, cfg.q(), cfg.k(), cfg.v())
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist_barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

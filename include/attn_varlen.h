@@ -1,0 +1,189 @@
+/*
+ * attn_varlen.h -- C ABI of the GB300 (sm_103a) attention library.
+ *
+ * Exact scaled-dot-product attention O = softmax(scale * Q K^T) V computed in
+ * one pass per query tile with the online-softmax recurrence (running max m,
+ * proxy denominator d', proxy output o' rescaled by e^(m_old - m_new)), so the
+ * logits X and probabilities A never reach device memory.  Source of the
+ * method and of the call shapes: "从零实现 vLLM (1.3)：如何加速 Attention 计算"
+ * (blog.xiaohansong.com), sections "减少遍历次数的“在线 Softmax”",
+ * "FlashAttention 的最终实现", "计算流程（1-Pass 算法与分块）",
+ * "Attention 源码分析", "Prefill" and "Decode".
+ *
+ * Conventions shared by every entry point
+ *  - Tensors are bf16 (IEEE bfloat16 bit patterns), row-major, the head_dim
+ *    axis contiguous and the head axis packed right above it.  Only the token
+ *    ("row") stride may be chosen; it is given in ELEMENTS and must keep every
+ *    row 16-byte aligned (stride * 2 % 16 == 0).  A row stride of 0 means the
+ *    packed default (num_heads * head_dim).
+ *  - Every pointer is a DEVICE pointer unless stated otherwise.  The caller
+ *    owns all memory (inputs, outputs, lse, workspace); the library allocates
+ *    nothing and keeps no state besides cached device attributes and one
+ *    device-side error word.
+ *  - Calls are asynchronous on `stream` (a cudaStream_t passed as void*; NULL
+ *    = the legacy default stream).  A returned ATTN_OK means the arguments were
+ *    accepted and the kernels were launched.
+ *  - Index data that lives on the device (cu_seqlens, block_table,
+ *    cache_seqlens, slot_mapping) is not read on the host.  Kernels never
+ *    access memory outside the sizes given here: a bad index is skipped and
+ *    recorded in the device error word (attn_get_last_device_error).
+ *  - head_dim must be 64 or 128; num_heads_q must be a multiple of
+ *    num_heads_kv (GQA: query head h reads KV head h / (num_heads_q /
+ *    num_heads_kv)).
+ *  - No function aborts, throws or prints.
+ */
+#ifndef ATTN_VARLEN_H
+#define ATTN_VARLEN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define ATTN_API __attribute__((visibility("default")))
+#else
+#define ATTN_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define ATTN_ABI_VERSION 1
+
+typedef enum attn_status {
+    ATTN_OK = 0,
+    ATTN_ERR_INVALID_ARG = 1,        /* null pointer, negative size, Hq % Hkv != 0, misaligned stride */
+    ATTN_ERR_UNSUPPORTED = 2,        /* head_dim, GQA group or block_size outside what is built;
+                                        device older than sm_103 */
+    ATTN_ERR_WORKSPACE_TOO_SMALL = 3,
+    ATTN_ERR_LAUNCH_FAILED = 4,      /* a CUDA runtime or driver call failed */
+    ATTN_ERR_DEVICE_TIMEOUT = 5,     /* a kernel's bounded wait ran out (reported by the error word) */
+    ATTN_ERR_DEVICE_INDEX = 6,       /* a device-side index was out of range (reported by the error word) */
+    ATTN_ERR_NO_DEVICE = 7           /* no CUDA device, or the device query failed */
+} attn_status;
+
+/* ------------------------------------------------------------------------
+ * attn_varlen_fwd -- varlen prefill ("flash_attn_varlen_func" in the article's
+ * Prefill section), causal or not, with contiguous or paged K/V.
+ *
+ *   q            [total_q, num_heads_q, head_dim]; sequence b owns query rows
+ *                [cu_seqlens_q[b], cu_seqlens_q[b+1])
+ *   k, v         contiguous (block_table == NULL): [total_k, num_heads_kv,
+ *                head_dim], sequence b owns key rows [cu_seqlens_k[b],
+ *                cu_seqlens_k[b+1]);
+ *                paged (block_table != NULL, the article's prefix cache): the
+ *                caches [num_blocks, block_size, num_heads_kv, head_dim];
+ *                logical key j of sequence b is cache row
+ *                block_table[b * block_table_stride + j / block_size] *
+ *                block_size + j % block_size, and cu_seqlens_k counts each
+ *                sequence's whole context (cached + new)
+ *   out          [total_q, num_heads_q, head_dim] bf16, written
+ *   lse          nullable; [num_heads_q, total_q] float32, natural-log
+ *                log-sum-exp of the scaled logits of each row (-inf for a row
+ *                that sees no key, whose output is 0)
+ *   cu_seqlens_q/_k  int32 [batch + 1], non-decreasing, starting at 0
+ *   total_q, total_k row counts of q/out and of contiguous k/v (total_k is
+ *                ignored when paged); kernels never touch rows beyond them
+ *   max_seqlen_q/_k  host-side upper bounds of the per-sequence lengths
+ *   causal       nonzero: bottom-right aligned mask, query i of a sequence
+ *                with Lq queries and Lk keys sees keys j <= Lk - Lq + i
+ *   block_size   paged only: a power of two >= 16; num_blocks > 0
+ *   workspace    device scratch of at least attn_varlen_workspace_size(...)
+ *                bytes (scheduler metadata); may be NULL when that size is 0
+ * Returns ATTN_OK, ATTN_ERR_INVALID_ARG, ATTN_ERR_UNSUPPORTED,
+ * ATTN_ERR_WORKSPACE_TOO_SMALL, ATTN_ERR_LAUNCH_FAILED or ATTN_ERR_NO_DEVICE.
+ * ------------------------------------------------------------------------ */
+ATTN_API attn_status attn_varlen_fwd(const void *q, const void *k, const void *v, void *out, float *lse,
+                            const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k,
+                            int batch, int64_t total_q, int64_t total_k,
+                            int max_seqlen_q, int max_seqlen_k,
+                            int num_heads_q, int num_heads_kv, int head_dim,
+                            float softmax_scale, int causal,
+                            const int32_t *block_table, int block_table_stride,
+                            int block_size, int64_t num_blocks,
+                            int64_t q_row_stride, int64_t k_row_stride, int64_t v_row_stride,
+                            int64_t out_row_stride,
+                            void *workspace, size_t workspace_bytes, void *stream);
+
+/* Bytes of device workspace attn_varlen_fwd needs for these sizes. */
+ATTN_API size_t attn_varlen_workspace_size(int batch, int num_heads_q, int num_heads_kv, int max_seqlen_q);
+
+/* ------------------------------------------------------------------------
+ * attn_decode_paged -- one new query token per sequence against its paged
+ * cache ("flash_attn_with_kvcache(q.unsqueeze(1), k_cache, v_cache,
+ * cache_seqlens, block_table, softmax_scale, causal=True)" in the article's
+ * Decode section).  With one query the bottom-right causal mask lets it see
+ * every cached key, so causality needs no argument.
+ *
+ *   q            [batch, num_heads_q, head_dim] (the article's [B, 1, H, D]
+ *                with the unit axis dropped); row stride q_row_stride
+ *   k_cache, v_cache  [num_blocks, block_size, num_heads_kv, head_dim]
+ *   out          [batch, num_heads_q, head_dim] bf16; row stride out_row_stride
+ *   lse          nullable; [batch, num_heads_q] float32
+ *   cache_seqlens int32 [batch]: keys 0 .. cache_seqlens[b]-1 are attended
+ *                (they include the current token, stored beforehand)
+ *   block_table  int32 [batch, block_table_stride]
+ *   max_cache_seqlen host-side upper bound of cache_seqlens
+ *   num_splits   0 = chosen by the library; otherwise the number of KV splits
+ *                per sequence (1..64).  Split partials are merged exactly by a
+ *                log-sum-exp combine.
+ *   workspace    at least attn_decode_workspace_size(...) bytes
+ * ------------------------------------------------------------------------ */
+ATTN_API attn_status attn_decode_paged(const void *q, const void *k_cache, const void *v_cache, void *out,
+                              float *lse, const int32_t *cache_seqlens, const int32_t *block_table,
+                              int block_table_stride, int batch, int num_heads_q, int num_heads_kv,
+                              int head_dim, int block_size, int64_t num_blocks, int max_cache_seqlen,
+                              float softmax_scale, int num_splits,
+                              int64_t q_row_stride, int64_t out_row_stride,
+                              void *workspace, size_t workspace_bytes, void *stream);
+
+/* Bytes of device workspace attn_decode_paged needs for these sizes
+ * (the same num_splits rule as attn_decode_paged, 0 = the library's choice). */
+ATTN_API size_t attn_decode_workspace_size(int batch, int num_heads_q, int num_heads_kv, int head_dim,
+                                  int max_cache_seqlen, int num_splits);
+
+/* The split count attn_decode_paged uses for these sizes (num_splits as passed). */
+ATTN_API int attn_decode_num_splits(int batch, int num_heads_kv, int max_cache_seqlen, int num_splits);
+
+/* ------------------------------------------------------------------------
+ * store_kvcache -- scatter this step's K/V rows into the paged caches before
+ * attention (the article's Prefill section: store_kvcache(k, v, k_cache,
+ * v_cache, slot_mapping)).
+ *
+ *   k, v          [num_tokens, num_heads_kv, head_dim], row strides
+ *                 k_row_stride / v_row_stride (elements, 0 = packed)
+ *   k_cache, v_cache  viewed as [num_slots, num_heads_kv, head_dim]
+ *                 (num_slots = num_blocks * block_size)
+ *   slot_mapping  int64 [num_tokens]: flat slot block_id * block_size +
+ *                 offset; a negative slot skips the token; a slot >=
+ *                 num_slots is skipped and flagged in the error word.
+ *                 Duplicate slots are a caller error (last writer undefined).
+ * head_dim may be any even value here (the copy is type-agnostic).
+ * ------------------------------------------------------------------------ */
+ATTN_API attn_status store_kvcache(const void *k, const void *v, void *k_cache, void *v_cache,
+                          const int64_t *slot_mapping, int64_t num_tokens, int num_heads_kv,
+                          int head_dim, int64_t k_row_stride, int64_t v_row_stride,
+                          int64_t num_slots, void *stream);
+
+/* ------------------------------------------------------------------------
+ * Diagnostics
+ * ------------------------------------------------------------------------ */
+
+/* Static text for a status code. */
+ATTN_API const char *attn_status_string(attn_status status);
+
+/* Synchronises `stream`, then reads and clears the device error word of the
+ * current device.  Returns ATTN_OK if no kernel recorded a problem since the
+ * last call, else ATTN_ERR_DEVICE_INDEX or ATTN_ERR_DEVICE_TIMEOUT (the first
+ * kind recorded), or ATTN_ERR_LAUNCH_FAILED if the stream itself reports a
+ * CUDA error.  *detail (nullable) receives the raw error word. */
+ATTN_API attn_status attn_get_last_device_error(void *stream, uint32_t *detail);
+
+/* ATTN_ABI_VERSION of the loaded library. */
+ATTN_API int attn_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_VARLEN_H */

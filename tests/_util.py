@@ -1,0 +1,48 @@
+"""Shared helpers for the parity tests (comparison metrics, device placement)."""
+import numpy as np
+import torch
+
+# Tolerance for bf16 inputs / fp32 accumulation / bf16 output against the
+# float64 oracle: max |err| <= 1e-2 and relative RMS <= 2e-3 over the
+# compared outputs.  lse (float32) is compared with an absolute bound.
+MAX_ABS = 1e-2
+REL_RMS = 2e-3
+LSE_ABS = 2e-3
+
+
+def errors(got, ref):
+    """(max |err|, relative RMS) of got (bf16/float tensor or array) vs ref (float64)."""
+    g = got.float().cpu().double().numpy() if isinstance(got, torch.Tensor) else np.asarray(got, np.float64)
+    r = np.asarray(ref, dtype=np.float64)
+    g = g.reshape(r.shape)
+    d = g - r
+    max_abs = float(np.max(np.abs(d))) if d.size else 0.0
+    den = float(np.sqrt(np.sum(r * r)))
+    rel = float(np.sqrt(np.sum(d * d)) / den) if den > 0 else float(np.sqrt(np.sum(d * d)))
+    return max_abs, rel
+
+
+def assert_close(got, ref, what=""):
+    g = got.float().cpu().double().numpy() if isinstance(got, torch.Tensor) else np.asarray(got, np.float64)
+    assert np.all(np.isfinite(g)), f"{what}: non-finite output"
+    max_abs, rel = errors(got, ref)
+    assert max_abs <= MAX_ABS and rel <= REL_RMS, f"{what}: max|err|={max_abs:.3e} relRMS={rel:.3e}"
+    return max_abs, rel
+
+
+def assert_lse_close(got, ref, what=""):
+    g = got.float().cpu().double().numpy() if isinstance(got, torch.Tensor) else np.asarray(got)
+    r = np.asarray(ref, dtype=np.float64).reshape(g.shape)
+    fin = np.isfinite(r)
+    assert np.array_equal(np.isfinite(g), fin), f"{what}: lse finiteness differs"
+    assert np.array_equal(np.isneginf(g), np.isneginf(r)), f"{what}: lse -inf pattern differs"
+    if fin.any():
+        err = np.max(np.abs(g[fin] - r[fin]) / np.maximum(1.0, np.abs(r[fin])))
+        assert err <= LSE_ABS, f"{what}: lse err {err:.3e}"
+
+
+def cuda(x, dtype=None):
+    t = torch.as_tensor(x)
+    if dtype is not None:
+        t = t.to(dtype)
+    return t.cuda()

@@ -1,0 +1,258 @@
+"""Varlen prefill (contiguous and paged) on the GPU against the float64 oracle."""
+import numpy as np
+import pytest
+import torch
+
+import attention_attn_varlen_gb300 as av
+import oracle
+import workloads
+from _util import assert_close, assert_lse_close
+from test_gpu_decode import device_cache, poison_tail
+
+pytestmark = pytest.mark.gpu
+
+
+def run_contig(cfg, q, k, v, causal=True):
+    cu_q = torch.from_numpy(cfg.cu_q).cuda()
+    cu_k = torch.from_numpy(cfg.cu_k).cuda()
+    return av.attn_varlen_fwd(q.cuda() if not q.is_cuda else q, k.cuda() if not k.is_cuda else k,
+                              v.cuda() if not v.is_cuda else v, cu_q, cu_k, int(cfg.lens_q.max(initial=0)),
+                              int(cfg.lens_k.max(initial=0)), cfg.scale, causal=causal, return_lse=True)
+
+
+def check_rows(out, lse, ref, ref_lse, rows, Hq, what):
+    D = out.shape[-1]
+    got = out.reshape(-1, D)[torch.from_numpy(rows).cuda()]
+    assert_close(got, ref, what)
+    t, h = rows // Hq, rows % Hq
+    assert_lse_close(lse[torch.from_numpy(h).cuda(), torch.from_numpy(t).cuda()], ref_lse, what + " lse")
+
+
+def test_c1_article_example_full():
+    cfg = workloads.make("c1_tiny")
+    q, k, v = cfg.q(), cfg.k(), cfg.v()
+    av.get_last_device_error()
+    out, lse = run_contig(cfg, q, k, v)
+    torch.cuda.synchronize()
+    assert av.get_last_device_error()[0] == 0
+    ref, ref_lse = oracle.attn_varlen(q, k, v, cfg.cu_q, cfg.cu_k, 4, 4, 64, cfg.scale, True)
+    assert_close(out, ref.reshape(out.shape), "c1")
+    assert_lse_close(lse.t().contiguous(), ref_lse.reshape(-1, 4), "c1 lse")
+
+
+VARLEN_CASES = [
+    # seed, lens_q, lens_k, Hq, Hkv, D, causal
+    (1, [5, 2, 1], [9, 7, 3], 4, 4, 64, True),
+    (2, [1, 17, 128, 129, 300], [1, 17, 128, 129, 300], 8, 2, 128, True),
+    (3, [200, 33], [500, 40], 32, 8, 128, True),
+    (4, [64, 257], [30, 100], 4, 4, 64, True),
+    (5, [0, 100, 0, 3], [5, 100, 0, 3], 16, 2, 128, True),
+    (6, [130, 77], [130, 300], 8, 1, 128, False),
+    (7, [512, 1000], [512, 1000], 2, 2, 128, True),
+    (8, [256], [256], 32, 2, 128, True),
+    (9, [700, 45], [700, 45], 32, 8, 64, True),
+    (10, [1, 1, 1], [1, 2, 1000], 8, 8, 128, True),
+]
+
+
+@pytest.mark.parametrize("seed,lq,lk,Hq,Hkv,D,causal", VARLEN_CASES)
+def test_varlen_matches_oracle(seed, lq, lk, Hq, Hkv, D, causal):
+    cfg = workloads.small_varlen(seed, lq, lk, Hq, Hkv, D, causal)
+    q, k, v = cfg.q(), cfg.k(), cfg.v()
+    av.get_last_device_error()
+    out, lse = run_contig(cfg, q, k, v, causal)
+    torch.cuda.synchronize()
+    assert av.get_last_device_error()[0] == 0
+    ref, ref_lse = oracle.attn_varlen(q, k, v, cfg.cu_q, cfg.cu_k, Hq, Hkv, D, cfg.scale, causal)
+    if ref.size:
+        assert_close(out, ref.reshape(out.shape), f"varlen {lq}/{lk}")
+        assert_lse_close(lse.t().contiguous(), ref_lse.reshape(-1, Hq), "varlen lse")
+
+
+def test_varlen_strided_qkv_views():
+    """q, k, v as views of one packed [tokens, Hq + 2 Hkv, D] projection."""
+    lens = np.array([300, 129])
+    Hq, Hkv, D = 16, 4, 128
+    T = int(lens.sum())
+    qkv = workloads.normal_bf16((21, 1), T, (Hq + 2 * Hkv) * D).view(T, Hq + 2 * Hkv, D)
+    q, k, v = qkv[:, :Hq], qkv[:, Hq:Hq + Hkv], qkv[:, Hq + Hkv:]
+    cfg = workloads.small_varlen(21, lens, lens, Hq, Hkv, D)
+    qkv_d = qkv.cuda()
+    out, lse = run_contig(cfg, qkv_d[:, :Hq], qkv_d[:, Hq:Hq + Hkv], qkv_d[:, Hq + Hkv:])
+    ref, _ = oracle.attn_varlen(q.contiguous(), k.contiguous(), v.contiguous(), cfg.cu_q, cfg.cu_k, Hq, Hkv, D,
+                                cfg.scale, True)
+    assert_close(out, ref.reshape(out.shape), "strided")
+
+
+def test_varlen_overflow_scaled_heads():
+    """Half the heads have Q scaled by 160: logits reach hundreds."""
+    hs = np.ones(8, dtype=np.float32)
+    hs[:4] = 160.0
+    cfg = workloads.small_varlen(22, [1000, 300], [1000, 300], 8, 8, 128, q_head_scale=hs)
+    q, k, v = cfg.q(), cfg.k(), cfg.v()
+    out, lse = run_contig(cfg, q, k, v)
+    ref, ref_lse = oracle.attn_varlen(q, k, v, cfg.cu_q, cfg.cu_k, 8, 8, 128, cfg.scale, True)
+    assert np.max(ref_lse) > 300
+    assert_close(out, ref.reshape(out.shape), "overflow heads")
+    assert_lse_close(lse.t().contiguous(), ref_lse.reshape(-1, 8), "overflow lse")
+
+
+def _paged_device(cfg):
+    """Caches with drawn context blocks, new tokens stored by store_kvcache,
+    rows past each sequence poisoned with NaN."""
+    kc, vc = device_cache(cfg, poison=False)
+    k_new, v_new = cfg.k_new(), cfg.v_new()
+    av.store_kvcache(k_new.cuda(), v_new.cuda(), kc, vc, torch.from_numpy(cfg.slot_mapping()).cuda())
+    poison_tail(cfg, kc, vc)
+    return kc, vc, k_new, v_new
+
+
+def _paged_oracle(cfg, q, k_new, v_new, seqs, rows_local=None):
+    """Oracle on a compact pool of `seqs` after its own store of the new tokens."""
+    kp, vp, bt = workloads.compact_paged(cfg, seqs)
+    # slots of the new tokens of `seqs` in the compact pool
+    bs = cfg.block_size
+    slots, tok_idx = [], []
+    cu_new = workloads.cu_from_lens(cfg.new)
+    for r, b in enumerate(seqs):
+        j = np.arange(int(cfg.ctx[b]), int(cfg.ctx[b] + cfg.new[b]))
+        slots.append(bt[r, j // bs].astype(np.int64) * bs + j % bs)
+        tok_idx.append(np.arange(cu_new[b], cu_new[b + 1]))
+    slots = np.concatenate(slots)
+    tok_idx = np.concatenate(tok_idx)
+    kb, vb = oracle.store_kvcache(k_new[tok_idx], v_new[tok_idx], kp, vp, slots)
+    qs = q[torch.from_numpy(tok_idx)]
+    cu_q = workloads.cu_from_lens(cfg.new[seqs])
+    cu_k = workloads.cu_from_lens(cfg.lens_k[seqs])
+    ref, ref_lse = oracle.attn_varlen(qs, kb.reshape(kp.shape), vb.reshape(vp.shape), cu_q, cu_k, cfg.Hq, cfg.Hkv,
+                                      cfg.D, cfg.scale, True, block_table=bt, block_size=bs,
+                                      num_blocks=kp.shape[0], rows=rows_local)
+    return ref, ref_lse, tok_idx
+
+
+def _run_paged(cfg, q, kc, vc):
+    cu_q = torch.from_numpy(workloads.cu_from_lens(cfg.new)).cuda()
+    cu_k = torch.from_numpy(workloads.cu_from_lens(cfg.lens_k)).cuda()
+    return av.attn_varlen_fwd(q.cuda(), kc, vc, cu_q, cu_k, int(cfg.new.max()), int(cfg.lens_k.max()), cfg.scale,
+                              causal=True, block_table=torch.from_numpy(cfg.block_table).cuda(), return_lse=True)
+
+
+PAGED_CASES = [
+    # seed, ctx, new, Hq, Hkv, D, block_size
+    (31, [37, 5, 300], [6, 1, 90], 32, 8, 128, 16),
+    (32, [1000, 257, 0], [200, 1, 64], 32, 8, 128, 256),
+    (33, [511, 2048], [129, 3], 8, 8, 128, 64),
+    (34, [90, 700], [40, 333], 16, 2, 64, 32),
+]
+
+
+@pytest.mark.parametrize("seed,ctx,new,Hq,Hkv,D,bs", PAGED_CASES)
+def test_paged_prefill_matches_oracle(seed, ctx, new, Hq, Hkv, D, bs):
+    cfg = workloads.small_paged(seed, ctx=ctx, new=new, Hq=Hq, Hkv=Hkv, D=D, block_size=bs)
+    q = cfg.q()
+    av.get_last_device_error()
+    kc, vc, k_new, v_new = _paged_device(cfg)
+    out, lse = _run_paged(cfg, q, kc, vc)
+    torch.cuda.synchronize()
+    assert av.get_last_device_error()[0] == 0
+    ref, ref_lse, _ = _paged_oracle(cfg, q, k_new, v_new, list(range(cfg.batch)))
+    assert_close(out, ref.reshape(out.shape), f"paged {ctx}+{new}")
+    assert_lse_close(lse.t().contiguous(), ref_lse.reshape(-1, Hq), "paged lse")
+
+
+def test_paged_equals_contiguous_bitexact():
+    """Paging is pure addressing: the same K/V, paged or packed, gives the same bits."""
+    cfg = workloads.small_paged(41, ctx=[700, 90], new=[300, 60], Hq=32, Hkv=8, D=128, block_size=128)
+    q = cfg.q()
+    kc, vc, k_new, v_new = _paged_device(cfg)
+    out_p, lse_p = _run_paged(cfg, q, kc, vc)
+    # gather the logical K/V rows into packed tensors (torch indexing on the device)
+    bs = cfg.block_size
+    rows = []
+    for b in range(cfg.batch):
+        j = np.arange(int(cfg.lens_k[b]))
+        rows.append(cfg.block_table[b, j // bs].astype(np.int64) * bs + j % bs)
+    rows = torch.from_numpy(np.concatenate(rows)).cuda()
+    kk = kc.view(-1, cfg.Hkv, cfg.D)[rows].contiguous()
+    vv = vc.view(-1, cfg.Hkv, cfg.D)[rows].contiguous()
+    cu_q = torch.from_numpy(workloads.cu_from_lens(cfg.new)).cuda()
+    cu_k = torch.from_numpy(workloads.cu_from_lens(cfg.lens_k)).cuda()
+    out_c, lse_c = av.attn_varlen_fwd(q.cuda(), kk, vv, cu_q, cu_k, int(cfg.new.max()), int(cfg.lens_k.max()),
+                                      cfg.scale, return_lse=True)
+    torch.cuda.synchronize()
+    assert torch.equal(out_p.view(torch.int16), out_c.view(torch.int16))
+    assert torch.equal(lse_p, lse_c)
+
+
+def test_decode_equals_last_row_of_paged_prefill():
+    cfg = workloads.small_paged(42, ctx=[500, 1200], new=[40, 1], Hq=32, Hkv=8, D=128, block_size=256)
+    q = cfg.q()
+    kc, vc, _, _ = _paged_device(cfg)
+    out, _ = _run_paged(cfg, q, kc, vc)
+    cu_new = workloads.cu_from_lens(cfg.new)
+    last = torch.from_numpy(cu_new[1:] - 1).cuda()
+    dec = av.attn_decode_paged(q.cuda()[last], kc, vc, torch.from_numpy(cfg.lens_k.astype(np.int32)).cuda(),
+                               torch.from_numpy(cfg.block_table).cuda(), cfg.scale)
+    d = (dec.float() - out[last].float()).abs().max().item()
+    assert d <= 1e-2
+
+
+@pytest.mark.slow
+def test_c2_full_size_sampled():
+    cfg = workloads.make("c2_varlen_gqa")
+    q, k, v = cfg.q(), cfg.k(), cfg.v()
+    av.get_last_device_error()
+    out, lse = run_contig(cfg, q, k, v)
+    torch.cuda.synchronize()
+    assert av.get_last_device_error()[0] == 0
+    rows = workloads.sample_rows(cfg.seed, q.shape[0] * cfg.Hq)
+    ref, ref_lse = oracle.attn_varlen(q, k, v, cfg.cu_q, cfg.cu_k, cfg.Hq, cfg.Hkv, cfg.D, cfg.scale, True,
+                                      rows=rows)
+    check_rows(out, lse, ref, ref_lse, rows, cfg.Hq, "c2")
+
+
+@pytest.mark.slow
+def test_c5_long_overflow_sampled():
+    cfg = workloads.make("c5_long")
+    q, k, v = cfg.q(), cfg.k(), cfg.v()
+    out, lse = run_contig(cfg, q, k, v)
+    torch.cuda.synchronize()
+    assert av.get_last_device_error()[0] == 0
+    assert torch.isfinite(out.float()).all()
+    # 4 (sequence, head) pairs: two overflow-stress heads, two plain ones; 1/64 of their rows
+    rng = np.random.default_rng(cfg.seed + 5)
+    rows = []
+    for b, h in [(0, 3), (1, 12), (0, 20), (1, 31)]:
+        i = np.sort(rng.choice(32768, 512, replace=False))
+        rows.append((int(cfg.cu_q[b]) + i) * cfg.Hq + h)
+    rows = np.concatenate(rows).astype(np.int64)
+    ref, ref_lse = oracle.attn_varlen(q, k, v, cfg.cu_q, cfg.cu_k, cfg.Hq, cfg.Hkv, cfg.D, cfg.scale, True,
+                                      rows=rows)
+    assert np.max(ref_lse) > 500
+    check_rows(out, lse, ref, ref_lse, rows, cfg.Hq, "c5")
+
+
+@pytest.mark.slow
+def test_c3_prefix_paged_full_size_sampled():
+    cfg = workloads.make("c3_prefix_paged")
+    q = cfg.q()
+    av.get_last_device_error()
+    kc = torch.empty((cfg.num_blocks, cfg.block_size, cfg.Hkv, cfg.D), dtype=torch.bfloat16, device="cuda")
+    vc = torch.empty_like(kc)
+    workloads.fill_paged_cache(cfg, kc, vc)
+    k_new, v_new = cfg.k_new(), cfg.v_new()
+    av.store_kvcache(k_new.cuda(), v_new.cuda(), kc, vc, torch.from_numpy(cfg.slot_mapping()).cuda())
+    poison_tail(cfg, kc, vc)
+    out, lse = _run_paged(cfg, q, kc, vc)
+    torch.cuda.synchronize()
+    assert av.get_last_device_error()[0] == 0
+    # oracle: 6 sequences (3 of them sharing the prefix), 1/16 of their rows
+    seqs = [0, 3, 7, 12, 20, 31]
+    Hq = cfg.Hq
+    n_local = int(cfg.new[seqs].sum()) * Hq
+    rows_local = workloads.sample_rows(cfg.seed, n_local, 1 / 16)
+    ref, ref_lse, tok_idx = _paged_oracle(cfg, q, k_new, v_new, seqs, rows_local)
+    rows = tok_idx[rows_local // Hq] * Hq + rows_local % Hq
+    check_rows(out, lse, ref, ref_lse, rows, Hq, "c3")
+    del kc, vc
+    torch.cuda.empty_cache()

@@ -341,3 +341,84 @@ def sample_rows(seed: int, n_rows: int, fraction: float = 1 / 64, cap: int | Non
         k = min(k, cap)
     rng = np.random.default_rng([seed, TAG_SAMPLE])
     return np.sort(rng.choice(n_rows, size=k, replace=False)).astype(np.int64)
+
+
+# --------------------------------------------------------------------------
+# materialising paged caches (device placement is plain copying)
+# --------------------------------------------------------------------------
+
+def _ctx_block_items(cfg: Paged, seqs=None):
+    seen, items = set(), []
+    for b in (range(cfg.batch) if seqs is None else seqs):
+        for i in range(cfg.n_ctx_blocks(b)):
+            pb = int(cfg.block_table[b, i])
+            if pb not in seen:
+                seen.add(pb)
+                items.append((pb, b, i))
+    return items
+
+
+def _draw_blocks(cfg: Paged, items):
+    """Host tensors [n, bs, Hkv*D] (K and V) for the listed context blocks."""
+    n = len(items)
+    row = cfg.Hkv * cfg.D
+    kh = torch.empty((n, cfg.block_size, row), dtype=torch.bfloat16)
+    vh = torch.empty_like(kh)
+
+    def job(t):
+        _, b, i = items[t]
+        kh[t] = cfg.block_content(TAG_K, b, i)
+        vh[t] = cfg.block_content(TAG_V, b, i)
+
+    with ThreadPoolExecutor(_nthreads()) as ex:
+        list(ex.map(job, range(n)))
+    return kh, vh
+
+
+def fill_paged_cache(cfg: Paged, k_cache: torch.Tensor, v_cache: torch.Tensor, seqs=None, batch_blocks: int = 512):
+    """Write every drawn context block of the chosen sequences into the caches
+    ([num_blocks, block_size, Hkv, D], any device) at its physical block id.
+    Other blocks are left as they are."""
+    items = _ctx_block_items(cfg, seqs)
+    kf = k_cache.view(cfg.num_blocks, -1)
+    vf = v_cache.view(cfg.num_blocks, -1)
+    for s in range(0, len(items), batch_blocks):
+        chunk = items[s:s + batch_blocks]
+        kh, vh = _draw_blocks(cfg, chunk)
+        idx = torch.tensor([pb for pb, _, _ in chunk], dtype=torch.int64, device=k_cache.device)
+        if k_cache.is_cuda:
+            kh, vh = kh.pin_memory(), vh.pin_memory()
+        kf.index_copy_(0, idx, kh.view(len(chunk), -1).to(k_cache.device, non_blocking=True))
+        vf.index_copy_(0, idx, vh.view(len(chunk), -1).to(v_cache.device, non_blocking=True))
+
+
+def compact_paged(cfg: Paged, seqs):
+    """A small host-side pool holding only the blocks of `seqs`.
+
+    Returns (k_pool, v_pool, block_table) with pools [n_blocks, bs, Hkv, D]
+    bf16 (context blocks drawn, blocks for new tokens zero) and the block
+    table of `seqs` renumbered into the pool.  Paging is a pure copy, so
+    attention over it equals attention over the full pool."""
+    remap = {}
+    for b in seqs:
+        nb = (int(cfg.lens_k[b]) + cfg.block_size - 1) // cfg.block_size
+        for i in range(nb):
+            pb = int(cfg.block_table[b, i])
+            if pb not in remap:
+                remap[pb] = len(remap)
+    n = len(remap)
+    kp = torch.zeros((n, cfg.block_size, cfg.Hkv, cfg.D), dtype=torch.bfloat16)
+    vp = torch.zeros_like(kp)
+    items = _ctx_block_items(cfg, seqs)
+    if items:
+        kh, vh = _draw_blocks(cfg, items)
+        for t, (pb, _, _) in enumerate(items):
+            kp[remap[pb]] = kh[t].view(cfg.block_size, cfg.Hkv, cfg.D)
+            vp[remap[pb]] = vh[t].view(cfg.block_size, cfg.Hkv, cfg.D)
+    width = cfg.block_table.shape[1]
+    bt = np.full((len(seqs), width), -1, dtype=np.int32)
+    for r, b in enumerate(seqs):
+        nb = (int(cfg.lens_k[b]) + cfg.block_size - 1) // cfg.block_size
+        for i in range(nb):
+            bt[r, i] = remap[int(cfg.block_table[b, i])]
+    return kp, vp, bt
