@@ -222,9 +222,15 @@ __global__ void __launch_bounds__(kDecThreads) attn_decode_split_kernel(const __
                 o[i][2] *= a_0;
                 o[i][3] *= a_1;
             }
-            // P^T into the B layout: rows = tokens, cols = heads -> transpose
-            const uint32_t bp0 = movmatrix_t(pack_bf16x2(p0, p1));
-            const uint32_t bp1 = movmatrix_t(pack_bf16x2(p2, p3));
+            // P^T into the B layout: rows = tokens, cols = heads -> transpose.
+            // P is carried as bf16 hi + lo terms (about 16 significant bits).
+            const uint32_t h01 = pack_bf16x2(p0, p1), h23 = pack_bf16x2(p2, p3);
+            const uint32_t bp0 = movmatrix_t(h01);
+            const uint32_t bp1 = movmatrix_t(h23);
+            const uint32_t bl0 = movmatrix_t(
+                pack_bf16x2(p0 - __uint_as_float(h01 << 16), p1 - __uint_as_float(h01 & 0xFFFF0000u)));
+            const uint32_t bl1 = movmatrix_t(
+                pack_bf16x2(p2 - __uint_as_float(h23 << 16), p3 - __uint_as_float(h23 & 0xFFFF0000u)));
             // O^T[D x 8] += V^T[D x 16 tokens] * P^T[16 x 8]
             const int mi = lane >> 3;
             const int vrow = r0 + (lane & 7) + (mi >> 1) * 8;
@@ -234,6 +240,7 @@ __global__ void __launch_bounds__(kDecThreads) attn_decode_split_kernel(const __
                 uint32_t a0, a1, a2, a3;
                 ldsm_x4_t(vb + (ch / 8) * S::kPanelBytes + sw128_off(vrow, ch % 8), a0, a1, a2, a3);
                 mma_bf16_16816(o[mt], a0, a1, a2, a3, bp0, bp1);
+                mma_bf16_16816(o[mt], a0, a1, a2, a3, bl0, bl1);
             }
             if (tail) fence_proxy_async_smem();
         }

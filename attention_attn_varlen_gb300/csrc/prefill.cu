@@ -25,7 +25,8 @@
 //              4-stage ring (128 keys x head_dim, 128-byte swizzle)
 //   warp 9     TMEM allocator and single-thread MMA issuer
 // TMEM (512 columns): S_A [0,128), S_B [128,256) fp32; O_A, O_B after them.
-// P (bf16) is written by the softmax threads over the first 64 columns of S.
+// P is written back by the softmax threads over S: P_hi = bf16(P) in columns
+// 0-63, P_lo = bf16(P - P_hi) in columns 64-127; PV runs on both terms.
 //
 // MMA order per key tile j:  S_A(j), PV_B(j-1), S_B(j), PV_A(j)
 // so the tensor core works on one slot while the other slot's softmax runs.
@@ -69,14 +70,19 @@ __device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t q_base, uint3
     }
 }
 
+// O (+)= P_hi V + P_lo V.  P is carried as two bf16 terms (P_hi = bf16(P),
+// P_lo = bf16(P - P_hi)) so the weights keep about 16 significant bits; a
+// single bf16 P adds a weight-rounding error comparable to the bf16 output
+// rounding itself.
 template <int D>
 __device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint32_t v_base, bool accumulate) {
     using S = PfSmem<D>;
     constexpr uint32_t idesc = idesc_bf16_f32(BM, D, 1);
 #pragma unroll
     for (int kk = 0; kk < BN / 16; ++kk) {
-        tc_mma_ts(d_tmem, p_tmem + kk * 8, sw128_desc(v_base + kk * 16 * 128, S::kPanelBytes, 1024), idesc,
-                  (accumulate || kk > 0) ? 1u : 0u);
+        const uint64_t vd = sw128_desc(v_base + kk * 16 * 128, S::kPanelBytes, 1024);
+        tc_mma_ts(d_tmem, p_tmem + kk * 8, vd, idesc, (accumulate || kk > 0) ? 1u : 0u);
+        tc_mma_ts(d_tmem, p_tmem + BN / 2 + kk * 8, vd, idesc, 1u);
     }
 }
 
@@ -343,18 +349,22 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             }
             l *= alpha;
             const float nref = (m_ref == -INFINITY) ? 0.f : -m_ref;
-            // P = 2^(s*scale*log2e - m_ref) -> bf16, over the first 64 columns of S
+            // P = 2^(s*scale*log2e - m_ref) as P_hi (columns 0-63 of S) and
+            // P_lo = P - P_hi (columns 64-127), both bf16
 #pragma unroll
             for (int c4 = 0; c4 < BN / 32; ++c4) {
-                uint32_t pk[16];
+                uint32_t pk[16], pl[16];
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
                     const float x0 = ex2(fmaf(s[c4 * 32 + 2 * i], sl2, nref));
                     const float x1 = ex2(fmaf(s[c4 * 32 + 2 * i + 1], sl2, nref));
                     l += x0 + x1;
-                    pk[i] = pack_bf16x2(x0, x1);
+                    const uint32_t h = pack_bf16x2(x0, x1);
+                    pk[i] = h;
+                    pl[i] = pack_bf16x2(x0 - __uint_as_float(h << 16), x1 - __uint_as_float(h & 0xFFFF0000u));
                 }
                 tmem_st16(tS + (uint32_t)(c4 * 16), pk);
+                tmem_st16(tS + (uint32_t)(BN / 2 + c4 * 16), pl);
             }
             // O *= alpha where the reference moved (O of tile 0 is written, not accumulated)
             if (j > 0 && __any_sync(0xffffffffu, need)) {

@@ -3,20 +3,25 @@ import numpy as np
 import torch
 
 # Tolerance for bf16 inputs / fp32 accumulation / bf16 output against the
-# float64 oracle: max |err| <= 1e-2 and relative RMS <= 2e-3 over the
-# compared outputs.  lse (float32) is compared with an absolute bound.
+# float64 oracle: relative RMS <= 2e-3 over the compared outputs, and per
+# element |err| <= 1e-2 + 2^-8 |ref|.  The second term is the bf16 output's own
+# rounding bound (8 significant bits, round-to-nearest: half an ulp is at most
+# 2^-8 of the value); without it no bf16 result could meet 1e-2 once |ref| >= 4.
+# lse (float32) is compared with a relative bound.
 MAX_ABS = 1e-2
+OUT_ROUND = 2.0 ** -8
 REL_RMS = 2e-3
 LSE_ABS = 2e-3
 
 
 def errors(got, ref):
-    """(max |err|, relative RMS) of got (bf16/float tensor or array) vs ref (float64)."""
+    """(max over elements of |err| - 2^-8 |ref|, relative RMS) of got
+    (bf16/float tensor or array) vs ref (float64)."""
     g = got.float().cpu().double().numpy() if isinstance(got, torch.Tensor) else np.asarray(got, np.float64)
     r = np.asarray(ref, dtype=np.float64)
     g = g.reshape(r.shape)
     d = g - r
-    max_abs = float(np.max(np.abs(d))) if d.size else 0.0
+    max_abs = float(np.max(np.abs(d) - OUT_ROUND * np.abs(r))) if d.size else 0.0
     den = float(np.sqrt(np.sum(r * r)))
     rel = float(np.sqrt(np.sum(d * d)) / den) if den > 0 else float(np.sqrt(np.sum(d * d)))
     return max_abs, rel
