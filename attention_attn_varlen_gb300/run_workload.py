@@ -1,0 +1,89 @@
+"""Run one operation of the attention path on a named synthetic workload.
+
+    python -m attention_attn_varlen_gb300.run_workload --workload c2_varlen_gqa --op prefill --iters 3
+
+A plain driver for profilers and quick checks: it builds the inputs on the
+device, runs the chosen call `--iters` times on the current stream and exits
+with the device error status.  No timing, no comparison.
+
+  --op prefill  attn_varlen_fwd (contiguous workloads c1, c2, c5; paged c3)
+  --op store    store_kvcache of the new tokens (c3)
+  --op decode   attn_decode_paged (c4)
+  --seqs N      keep only the first N sequences (smaller captures)
+"""
+from __future__ import annotations
+
+import argparse
+import os
+import sys
+
+import numpy as np
+import torch
+
+sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+
+import attention_attn_varlen_gb300 as av  # noqa: E402
+import workloads  # noqa: E402
+
+
+def _trim(cfg, n):
+    if n is None or n >= cfg.batch:
+        return cfg
+    if isinstance(cfg, workloads.Varlen):
+        cfg.lens_q = cfg.lens_q[:n]
+        cfg.lens_k = cfg.lens_k[:n]
+        return cfg
+    cfg.ctx = cfg.ctx[:n]
+    cfg.new = cfg.new[:n]
+    cfg.block_table = cfg.block_table[:n]
+    return cfg
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--workload", required=True, choices=workloads.CONFIG_NAMES)
+    ap.add_argument("--op", required=True, choices=["prefill", "store", "decode"])
+    ap.add_argument("--iters", type=int, default=3)
+    ap.add_argument("--seqs", type=int, default=None)
+    a = ap.parse_args(argv)
+    av.lib()
+    dev = torch.device("cuda", 0)
+    cfg = _trim(workloads.make(a.workload), a.seqs)
+    if isinstance(cfg, workloads.Varlen):
+        if a.op != "prefill":
+            raise SystemExit("contiguous workloads only have --op prefill")
+        q, k, v = cfg.q().to(dev), cfg.k().to(dev), cfg.v().to(dev)
+        cu_q = torch.from_numpy(cfg.cu_q).to(dev)
+        cu_k = torch.from_numpy(cfg.cu_k).to(dev)
+        out = torch.empty_like(q)
+        for _ in range(a.iters):
+            av.attn_varlen_fwd(q, k, v, cu_q, cu_k, int(cfg.lens_q.max()), int(cfg.lens_k.max()), cfg.scale, out=out)
+    else:
+        kc = torch.empty((cfg.num_blocks, cfg.block_size, cfg.Hkv, cfg.D), dtype=torch.bfloat16, device=dev)
+        vc = torch.empty_like(kc)
+        workloads.fill_paged_cache(cfg, kc, vc)
+        bt = torch.from_numpy(np.ascontiguousarray(cfg.block_table)).to(dev)
+        q = cfg.q().to(dev)
+        if a.op == "decode":
+            cs = torch.from_numpy(cfg.ctx.astype(np.int32)).to(dev)
+            out = torch.empty_like(q)
+            for _ in range(a.iters):
+                av.attn_decode_paged(q, kc, vc, cs, bt, cfg.scale, max_cache_seqlen=int(cfg.ctx.max()), out=out)
+        else:
+            k_new, v_new = cfg.k_new().to(dev), cfg.v_new().to(dev)
+            slots = torch.from_numpy(cfg.slot_mapping()).to(dev)
+            cu_q = torch.from_numpy(workloads.cu_from_lens(cfg.new)).to(dev)
+            cu_k = torch.from_numpy(workloads.cu_from_lens(cfg.lens_k)).to(dev)
+            out = torch.empty_like(q)
+            for _ in range(a.iters):
+                av.store_kvcache(k_new, v_new, kc, vc, slots)
+                if a.op == "prefill":
+                    av.attn_varlen_fwd(q, kc, vc, cu_q, cu_k, int(cfg.new.max()), int(cfg.lens_k.max()), cfg.scale,
+                                       block_table=bt, out=out)
+    st, word = av.get_last_device_error()
+    print(f"{a.workload} {a.op} x{a.iters}: device status {st} word {word:#x}")
+    return 0 if st == 0 else 1
+
+
+if __name__ == "__main__":
+    sys.exit(main())

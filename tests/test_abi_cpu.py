@@ -1,0 +1,61 @@
+"""The C ABI on a machine without a GPU: the library loads, exports every
+function include/attn_varlen.h declares, and rejects bad arguments on the host
+before touching a device."""
+import ctypes
+
+import pytest
+
+import attention_attn_varlen_gb300 as av
+
+
+@pytest.fixture(scope="module")
+def L():
+    av.build()
+    return av.lib()
+
+
+def test_every_declared_symbol_is_exported(L):
+    names = av.exported_symbols()
+    assert {"attn_varlen_fwd", "attn_decode_paged", "store_kvcache"} <= set(names)
+    for n in names:
+        assert hasattr(L, n), n
+
+
+def test_abi_version_and_status_strings(L):
+    assert L.attn_abi_version() == 1
+    for s in range(8):
+        assert L.attn_status_string(s)
+    assert L.attn_status_string(99) == b"unknown status"
+
+
+def test_host_validation_without_device(L):
+    null = None
+    # store_kvcache: null pointers / negative sizes
+    assert L.store_kvcache(null, null, null, null, null, 5, 8, 128, 0, 0, 10, null) == 1
+    assert L.store_kvcache(null, null, null, null, null, -1, 8, 128, 0, 0, 10, null) == 1
+    assert L.store_kvcache(null, null, null, null, null, 0, 8, 128, 0, 0, 10, null) == 0   # nothing to do
+    fake = ctypes.c_void_p(0x1000)
+    # varlen: Hq not a multiple of Hkv, bad scale, unsupported head_dim, misaligned stride
+    args = lambda **kw: [fake, fake, fake, fake, null, fake, fake, kw.get("B", 2), 8, 8, 4, 4, kw.get("Hq", 4),
+                         kw.get("Hkv", 4), kw.get("D", 64), kw.get("scale", 0.125), 1, null, 0, 0, 0,
+                         kw.get("qs", 0), 0, 0, 0, null, 0, null]
+    assert L.attn_varlen_fwd(*args(Hq=6, Hkv=4)) == 1
+    assert L.attn_varlen_fwd(*args(scale=0.0)) == 1
+    assert L.attn_varlen_fwd(*args(scale=float("nan"))) == 1
+    assert L.attn_varlen_fwd(*args(D=96)) == 2
+    assert L.attn_varlen_fwd(*args(Hq=12, Hkv=4)) == 2       # group of 3 does not divide the 128-row slot
+    assert L.attn_varlen_fwd(*args(qs=4 * 64 + 3)) == 1        # row stride not 16-byte aligned
+    assert L.attn_varlen_fwd(*args(B=0)) == 1
+    # decode: block size must be a power of two >= 16; group <= 8
+    dec = lambda **kw: [fake, fake, fake, fake, null, fake, fake, 4, 2, kw.get("Hq", 8), kw.get("Hkv", 8), 128,
+                        kw.get("bs", 16), 10, 64, 0.1, 0, 0, 0, null, 0, null]
+    assert L.attn_decode_paged(*dec(bs=24)) == 1
+    assert L.attn_decode_paged(*dec(Hq=32, Hkv=2)) == 2
+
+
+def test_decode_split_rule_is_host_side(L):
+    # no device: the rule falls back to a default SM count but stays well defined
+    assert L.attn_decode_num_splits(256, 8, 16384, 0) == 8
+    assert L.attn_decode_num_splits(1, 8, 16384, 0) >= 8
+    assert L.attn_decode_num_splits(4, 8, 100, 5) == 2          # capped by 64-token tiles
+    assert L.attn_decode_workspace_size(256, 32, 8, 128, 16384, 1) == 0
