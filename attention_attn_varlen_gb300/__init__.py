@@ -61,6 +61,9 @@ def lib():
     L.attn_decode_paged.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _i64, _i32,
                                     _f32, _i32, _i64, _i64, _vp, _sz, _vp]
     L.attn_decode_paged.restype = _i32
+    L.attn_decode_paged_noalloc.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32,
+                                            _i64, _i32, _f32, _i32, _i64, _i64, _vp]
+    L.attn_decode_paged_noalloc.restype = _i32
     L.attn_decode_workspace_size.argtypes = [_i32, _i32, _i32, _i32, _i32, _i32]
     L.attn_decode_workspace_size.restype = _sz
     L.attn_decode_num_splits.argtypes = [_i32, _i32, _i32, _i32]

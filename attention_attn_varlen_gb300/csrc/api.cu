@@ -362,6 +362,94 @@ attn_status attn_decode_paged(const void *q, const void *k_cache, const void *v_
 }
 
 // ---------------------------------------------------------------------------
+attn_status attn_decode_paged_noalloc(const void *q, const void *k_cache, const void *v_cache, void *out,
+                                      float *lse, const int32_t *cache_seqlens, const int32_t *block_table,
+                                      int block_table_stride, int batch, int num_heads_q, int num_heads_kv,
+                                      int head_dim, int block_size, int64_t num_blocks, int max_cache_seqlen,
+                                      float softmax_scale, int num_splits, int64_t q_row_stride,
+                                      int64_t out_row_stride, void *stream) {
+    if (!q || !k_cache || !v_cache || !out || !cache_seqlens || !block_table) return ATTN_ERR_INVALID_ARG;
+    if (batch <= 0 || num_heads_q <= 0 || num_heads_kv <= 0 || num_heads_q % num_heads_kv != 0)
+        return ATTN_ERR_INVALID_ARG;
+    if (max_cache_seqlen < 0 || num_splits < 0 || block_table_stride <= 0) return ATTN_ERR_INVALID_ARG;
+    if (!(softmax_scale > 0.f) || !isfinite(softmax_scale)) return ATTN_ERR_INVALID_ARG;
+    if (!pow2(block_size) || block_size < 16 || num_blocks <= 0) return ATTN_ERR_INVALID_ARG;
+    if (head_dim != 64 && head_dim != 128) return ATTN_ERR_UNSUPPORTED;
+    const int G = num_heads_q / num_heads_kv;
+    if (G > 8) return ATTN_ERR_UNSUPPORTED;
+    if (batch > 65535 || num_heads_kv > 65535) return ATTN_ERR_UNSUPPORTED;
+    if (num_blocks * (int64_t)block_size >= (int64_t)INT32_MAX) return ATTN_ERR_UNSUPPORTED;
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out)) return ATTN_ERR_INVALID_ARG;
+    if (!fix_stride(&q_row_stride, (int64_t)num_heads_q * head_dim) ||
+        !fix_stride(&out_row_stride, (int64_t)num_heads_q * head_dim))
+        return ATTN_ERR_INVALID_ARG;
+
+    DevInfo *d = nullptr;
+    attn_status st = dev_info(&d);
+    if (st != ATTN_OK) return st;
+    if ((st = check_arch(d)) != ATTN_OK) return st;
+    float *scratch = nullptr;
+    size_t scratch_bytes = 0;
+    if (decode_noalloc_scratch(&scratch, &scratch_bytes) != cudaSuccess) {
+        cudaGetLastError();
+        return ATTN_ERR_LAUNCH_FAILED;
+    }
+
+    // split partials: [batch, Hq, splits, head_dim] outputs + [batch, Hq, splits] lse
+    const size_t per_split = (size_t)batch * num_heads_q * (head_dim + 1) * sizeof(float);
+    int splits = choose_splits(d->num_sms, batch, num_heads_kv, max_cache_seqlen, num_splits);
+    int split_tok = split_tokens_for(max_cache_seqlen > 0 ? max_cache_seqlen : 1, splits);
+    splits = max_cache_seqlen > 0 ? (max_cache_seqlen + split_tok - 1) / split_tok : 1;
+    if (splits < 1) splits = 1;
+    if (splits > 1 && (size_t)splits * per_split > scratch_bytes) {
+        if (num_splits > 0) return ATTN_ERR_WORKSPACE_TOO_SMALL;   // the asked split count does not fit
+        // library's choice: the largest split count whose partials fit (1 needs none)
+        int fit = (int)(scratch_bytes / per_split);
+        if (fit < 2) fit = 1;
+        split_tok = split_tokens_for(max_cache_seqlen, fit);
+        splits = (max_cache_seqlen + split_tok - 1) / split_tok;
+    }
+
+    DecodeParams p;
+    memset(&p, 0, sizeof p);
+    if (splits > 1) {
+        p.o_part = scratch;
+        p.lse_part = scratch + (size_t)batch * num_heads_q * splits * head_dim;
+    }
+    const int rpb = block_size < kDecodeTile ? block_size : kDecodeTile;
+    const int64_t rows = num_blocks * (int64_t)block_size;
+    const int64_t row_stride = (int64_t)num_heads_kv * head_dim;
+    CUtensorMap kmap, vmap;
+    if (!make_map(&kmap, k_cache, rows, num_heads_kv, head_dim, row_stride, 1, rpb) ||
+        !make_map(&vmap, v_cache, rows, num_heads_kv, head_dim, row_stride, 1, rpb))
+        return ATTN_ERR_LAUNCH_FAILED;
+    p.q = reinterpret_cast<const __nv_bfloat16 *>(q);
+    p.out = reinterpret_cast<__nv_bfloat16 *>(out);
+    p.lse = lse;
+    p.cache_seqlens = cache_seqlens;
+    p.block_table = block_table;
+    p.q_row_stride = q_row_stride;
+    p.out_row_stride = out_row_stride;
+    p.bt_stride = block_table_stride;
+    p.block_size = block_size;
+    p.rows_per_box = rpb;
+    p.num_splits = splits;
+    p.split_tokens = split_tok;
+    p.num_blocks = num_blocks;
+    p.Hq = num_heads_q;
+    p.Hkv = num_heads_kv;
+    p.G = G;
+    p.scale_log2 = softmax_scale * 1.4426950408889634f;
+    p.err = d->err;
+    cudaError_t e = launch_decode(kmap, vmap, p, batch, head_dim, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return ATTN_ERR_LAUNCH_FAILED;
+    }
+    return ATTN_OK;
+}
+
+// ---------------------------------------------------------------------------
 attn_status store_kvcache(const void *k, const void *v, void *k_cache, void *v_cache, const int64_t *slot_mapping,
                           int64_t num_tokens, int num_heads_kv, int head_dim, int64_t k_row_stride,
                           int64_t v_row_stride, int64_t num_slots, void *stream) {

@@ -384,3 +384,53 @@ cudaError_t launch_decode(const CUtensorMap &kmap, const CUtensorMap &vmap, cons
 }
 
 }  // namespace attn
+
+namespace attn {
+
+// ---------------------------------------------------------------------------
+// Statically reserved scratch for attn_decode_paged_noalloc.
+//
+// Some callers cannot allocate device memory when they decode: a serving
+// loop that has handed all free memory to its paged KV-cache pool at start-up,
+// or code that must not call cudaMalloc on its hot path because it may
+// synchronise the device and stall other streams.  For them the split
+// partials live in this fixed array instead of a caller workspace.  It is
+// part of the module image, so every GPU that loads the library holds these
+// bytes until the process exits.  All calls share it: two calls that overlap
+// on the GPU (different streams, no ordering between them) race on it.
+// Nothing in it needs clearing between calls: every partial the combine
+// kernel reads is written earlier by the same call.
+// ---------------------------------------------------------------------------
+namespace {
+constexpr size_t kNoAllocScratchBytes = 32ull << 20;   // 32 MiB
+static __device__ __align__(256) float g_decode_noalloc_scratch[kNoAllocScratchBytes / sizeof(float)];
+
+struct ScratchAddr {
+    bool ready = false;
+    float *ptr = nullptr;
+};
+ScratchAddr g_scratch_addr[64];
+}  // namespace
+
+// Device address of the static scratch on the current device.  The first call
+// on a device looks it up (cudaGetSymbolAddress, with that device current);
+// later calls reuse the cached address.
+cudaError_t decode_noalloc_scratch(float **ptr, size_t *bytes) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    ScratchAddr &s = g_scratch_addr[dev];
+    if (!s.ready) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_decode_noalloc_scratch);
+        if (e != cudaSuccess) return e;
+        s.ptr = reinterpret_cast<float *>(p);
+        s.ready = true;
+    }
+    *ptr = s.ptr;
+    *bytes = kNoAllocScratchBytes;
+    return cudaSuccess;
+}
+
+}  // namespace attn

@@ -48,6 +48,10 @@ cudaError_t launch_store_kvcache(const void *k, const void *v, void *k_cache, vo
 cudaError_t launch_decode(const CUtensorMap &kmap, const CUtensorMap &vmap, const DecodeParams &p, int batch,
                           int head_dim, cudaStream_t stream);
 
+// static scratch of the allocation-free decode entry point (device address on
+// the current device, looked up on first use)
+cudaError_t decode_noalloc_scratch(float **ptr, size_t *bytes);
+
 // rows per query slot of the prefill kernel (a slot packs 128 / G tokens x G heads)
 constexpr int kPrefillSlotRows = 128;
 constexpr int kPrefillKeyTile = 128;

@@ -146,6 +146,38 @@ ATTN_API size_t attn_decode_workspace_size(int batch, int num_heads_q, int num_h
 ATTN_API int attn_decode_num_splits(int batch, int num_heads_kv, int max_cache_seqlen, int num_splits);
 
 /* ------------------------------------------------------------------------
+ * attn_decode_paged_noalloc -- attn_decode_paged for callers that cannot
+ * allocate device memory when they decode.  The article has no counterpart:
+ * this entry point exists for deployments such as a serving loop that gave
+ * all free device memory to its paged KV-cache pool at start-up, or a hot
+ * path that must not call cudaMalloc because it can synchronise the device.
+ *
+ * Arguments and results are those of attn_decode_paged without the
+ * workspace: the split partials go to a scratch array reserved statically in
+ * the library (ATTN_DECODE_NOALLOC_SCRATCH_BYTES, 32 MiB, held on every GPU
+ * that loads the library until the process exits).  The call allocates
+ * nothing.
+ *  - The first call on a device looks up the scratch address on that device
+ *    (with it current); make that first call before any stream capture.
+ *  - Every call shares the one array: calls that overlap on the GPU (on
+ *    streams with no ordering between them) race and give wrong results.
+ *    Nothing in the array needs clearing between calls.
+ *  - num_splits = 0 picks the library's split count, lowered until the
+ *    partials fit the scratch (one split needs none).  An explicit num_splits
+ *    whose partials (batch * num_heads_q * num_splits * (head_dim + 1) floats)
+ *    do not fit is rejected with ATTN_ERR_WORKSPACE_TOO_SMALL.
+ * ------------------------------------------------------------------------ */
+#define ATTN_DECODE_NOALLOC_SCRATCH_BYTES (32u << 20)
+
+ATTN_API attn_status attn_decode_paged_noalloc(const void *q, const void *k_cache, const void *v_cache, void *out,
+                                               float *lse, const int32_t *cache_seqlens,
+                                               const int32_t *block_table, int block_table_stride, int batch,
+                                               int num_heads_q, int num_heads_kv, int head_dim, int block_size,
+                                               int64_t num_blocks, int max_cache_seqlen, float softmax_scale,
+                                               int num_splits, int64_t q_row_stride, int64_t out_row_stride,
+                                               void *stream);
+
+/* ------------------------------------------------------------------------
  * store_kvcache -- scatter this step's K/V rows into the paged caches before
  * attention (the article's Prefill section: store_kvcache(k, v, k_cache,
  * v_cache, slot_mapping)).
