@@ -163,15 +163,19 @@ KERNEL_SOURCES = {
 
 def ncu_traffic(kernel: str, units: float):
     """DRAM bytes per launch from the committed ncu summary, scaled to `units`
-    (the summary stores bytes per unit of work and the source digest of the
-    kernel it was taken on); None if absent or the kernel changed since."""
-    p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    (profiles/dram_traffic.txt stores bytes per unit of work and the source
+    digest of the kernel it was taken on); None if absent or the kernel
+    changed since."""
+    p = os.path.join(ROOT, "profiles", "dram_traffic.txt")
     if not os.path.exists(p):
         return None
-    d = json.load(open(p)).get(kernel)
-    if not d or d.get("src_digest") != src_digest(KERNEL_SOURCES[kernel]):
-        return None
-    return float(d["dram_bytes_per_unit"]) * units
+    for line in open(p):
+        f = line.split()
+        if len(f) >= 3 and not line.startswith("#") and f[0] == kernel:
+            if f[1] != src_digest(KERNEL_SOURCES[kernel]):
+                return None
+            return float(f[2]) * units
+    return None
 
 
 # --------------------------------------------------------------------------
