@@ -30,7 +30,7 @@ __all__ = ["attn_varlen_fwd", "attn_decode_paged", "store_kvcache", "get_last_de
 
 ATTN_OK = 0
 _STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "workspace too small", 4: "launch failed",
-           5: "device timeout", 6: "device index out of range", 7: "no device"}
+           5: "device timeout", 6: "device index out of range", 7: "no device", 8: "input value out of range"}
 
 
 class AttnError(RuntimeError):
@@ -56,7 +56,7 @@ def lib():
     L.attn_varlen_fwd.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i64, _i64, _i32, _i32, _i32, _i32, _i32,
                                   _f32, _i32, _vp, _i32, _i32, _i64, _i64, _i64, _i64, _i64, _vp, _sz, _vp]
     L.attn_varlen_fwd.restype = _i32
-    L.attn_varlen_workspace_size.argtypes = [_i32, _i32, _i32, _i32]
+    L.attn_varlen_workspace_size.argtypes = [_i32, _i32, _i32, _i32, _i32, _i64]
     L.attn_varlen_workspace_size.restype = _sz
     L.attn_decode_paged.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _i64, _i32,
                                     _f32, _i32, _i64, _i64, _vp, _sz, _vp]
@@ -136,9 +136,12 @@ def _int_cuda(name, t, dtype):
 
 def attn_varlen_fwd(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, max_seqlen_k: int,
                     softmax_scale: float | None = None, causal: bool = True, block_table=None,
-                    out=None, lse=None, return_lse: bool = False, stream=None):
+                    out=None, lse=None, return_lse: bool = False, total_k: int | None = None,
+                    workspace=None, stream=None):
     """Varlen prefill.  q [total_q, Hq, D]; k/v [total_k, Hkv, D] or, with
     block_table [B, max_blocks] int32, caches [num_blocks, block_size, Hkv, D].
+    total_k (paged only): an upper bound of cu_seqlens_k[-1]; defaults to
+    B * max_seqlen_k (no device sync).
     Returns out [total_q, Hq, D] (and lse [Hq, total_q] float32 if asked)."""
     _bf16_cuda(("q", q), ("k", k), ("v", v), ("out", out))
     _int_cuda("cu_seqlens_q", cu_seqlens_q, torch.int32)
@@ -151,7 +154,6 @@ def attn_varlen_fwd(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, max_
             raise ValueError("paged k/v must be contiguous [num_blocks, block_size, Hkv, D]")
         num_blocks, block_size, Hkv, _ = k.shape
         k_stride = v_stride = Hkv * D
-        total_k = num_blocks * block_size
         bt_stride = block_table.shape[1]
     else:
         Hkv = k.shape[1]
@@ -161,6 +163,8 @@ def attn_varlen_fwd(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, max_
         num_blocks = block_size = bt_stride = 0
     q_stride = _rows(q, "q", Hq, D)
     B = cu_seqlens_q.numel() - 1
+    if paged and total_k is None:
+        total_k = B * int(max_seqlen_k)
     if cu_seqlens_k.numel() != B + 1:
         raise ValueError("cu_seqlens_q and cu_seqlens_k must have the same length")
     if out is None:
@@ -170,12 +174,14 @@ def attn_varlen_fwd(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, max_
         lse = torch.empty((Hq, total_q), dtype=torch.float32, device=q.device)
     scale = 1.0 / math.sqrt(D) if softmax_scale is None else float(softmax_scale)
     L = lib()
-    ws_bytes = L.attn_varlen_workspace_size(B, Hq, Hkv, int(max_seqlen_q))
-    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device) if ws_bytes else None
+    ws_bytes = L.attn_varlen_workspace_size(B, Hq, Hkv, D, int(max_seqlen_q), int(total_k))
+    if workspace is None or workspace.numel() * workspace.element_size() < ws_bytes:
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device)
+    ws = workspace
     st = L.attn_varlen_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(cu_seqlens_q), _ptr(cu_seqlens_k),
                            B, total_q, total_k, int(max_seqlen_q), int(max_seqlen_k), Hq, Hkv, D, scale,
                            1 if causal else 0, _ptr(block_table), bt_stride, block_size, num_blocks, q_stride,
-                           k_stride, v_stride, out_stride, _ptr(ws), ws_bytes, _stream(stream))
+                           k_stride, v_stride, out_stride, _ptr(ws), ws.numel() * ws.element_size(), _stream(stream))
     _check(st, "attn_varlen_fwd")
     return (out, lse) if return_lse else out
 

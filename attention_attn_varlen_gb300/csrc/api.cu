@@ -80,14 +80,14 @@ EncodeTiledFn encode_fn() {
 // bf16 tensor [rows, heads, dim] with a row stride (elements) viewed as a 3-D
 // TMA map (dim, heads, rows), 128-byte swizzle, box (64, box_heads, box_rows).
 bool make_map(CUtensorMap *map, const void *base, int64_t rows, int heads, int dim, int64_t row_stride,
-              int box_heads, int box_rows) {
+              int box_heads, int box_rows, CUtensorMapDataType dtype = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
     cuuint64_t gdim[3] = {(cuuint64_t)dim, (cuuint64_t)heads, (cuuint64_t)(rows > 0 ? rows : 1)};
     cuuint64_t gstride[2] = {(cuuint64_t)dim * 2, (cuuint64_t)row_stride * 2};
     cuuint32_t box[3] = {64u, (cuuint32_t)box_heads, (cuuint32_t)box_rows};
     cuuint32_t estr[3] = {1u, 1u, 1u};
-    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), gdim, gstride, box, estr,
+    CUresult r = fn(map, dtype, 3, const_cast<void *>(base), gdim, gstride, box, estr,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
@@ -147,6 +147,7 @@ const char *attn_status_string(attn_status s) {
         case ATTN_ERR_DEVICE_TIMEOUT: return "a kernel's bounded wait ran out";
         case ATTN_ERR_DEVICE_INDEX: return "a device-side index was out of range";
         case ATTN_ERR_NO_DEVICE: return "no usable CUDA device";
+        case ATTN_ERR_DEVICE_RANGE: return "an input value was outside the range a kernel handles";
     }
     return "unknown status";
 }
@@ -175,16 +176,22 @@ attn_status attn_get_last_device_error(void *stream, uint32_t *detail) {
     if (detail) *detail = word;
     if (word & ERR_INDEX) return ATTN_ERR_DEVICE_INDEX;
     if (word & ERR_TIMEOUT) return ATTN_ERR_DEVICE_TIMEOUT;
+    if (word & ERR_RANGE) return ATTN_ERR_DEVICE_RANGE;
     return ATTN_OK;
 }
 
 // ---------------------------------------------------------------------------
-size_t attn_varlen_workspace_size(int batch, int num_heads_q, int num_heads_kv, int max_seqlen_q) {
+// Workspace: the fp16 copy of V (V / 16), [total_k, Hkv, D] by logical key,
+// after a 256-byte header.
+static const size_t kWsHeader = 256;
+
+size_t attn_varlen_workspace_size(int batch, int num_heads_q, int num_heads_kv, int head_dim, int max_seqlen_q,
+                                  int64_t total_k) {
     (void)batch;
     (void)num_heads_q;
-    (void)num_heads_kv;
     (void)max_seqlen_q;
-    return 0;   // the launch needs no scheduler metadata at present
+    if (num_heads_kv <= 0 || head_dim <= 0 || total_k < 0) return 0;
+    return kWsHeader + (size_t)total_k * (size_t)num_heads_kv * (size_t)head_dim * 2;
 }
 
 attn_status attn_varlen_fwd(const void *q, const void *k, const void *v, void *out, float *lse,
@@ -194,9 +201,7 @@ attn_status attn_varlen_fwd(const void *q, const void *k, const void *v, void *o
                             int block_table_stride, int block_size, int64_t num_blocks, int64_t q_row_stride,
                             int64_t k_row_stride, int64_t v_row_stride, int64_t out_row_stride, void *workspace,
                             size_t workspace_bytes, void *stream) {
-    (void)workspace;
-    (void)workspace_bytes;
-    (void)max_seqlen_k;
+
     if (!q || !k || !v || !out || !cu_seqlens_q || !cu_seqlens_k) return ATTN_ERR_INVALID_ARG;
     if (batch <= 0 || num_heads_q <= 0 || num_heads_kv <= 0 || num_heads_q % num_heads_kv != 0)
         return ATTN_ERR_INVALID_ARG;
@@ -211,9 +216,8 @@ attn_status attn_varlen_fwd(const void *q, const void *k, const void *v, void *o
         if (!pow2(block_size) || block_size < 16 || num_blocks <= 0 || block_table_stride <= 0)
             return ATTN_ERR_INVALID_ARG;
         if (num_blocks * (int64_t)block_size >= (int64_t)INT32_MAX) return ATTN_ERR_UNSUPPORTED;
-    } else if (total_k >= (int64_t)INT32_MAX) {
-        return ATTN_ERR_UNSUPPORTED;
     }
+    if (total_k >= (int64_t)INT32_MAX) return ATTN_ERR_UNSUPPORTED;
     if (total_q >= (int64_t)INT32_MAX) return ATTN_ERR_UNSUPPORTED;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return ATTN_ERR_INVALID_ARG;
     if (!fix_stride(&q_row_stride, (int64_t)num_heads_q * head_dim) ||
@@ -231,23 +235,36 @@ attn_status attn_varlen_fwd(const void *q, const void *k, const void *v, void *o
     if (total_q == 0 || max_seqlen_q == 0) return ATTN_OK;
 
     const int tps = kPrefillSlotRows / G;
+    const size_t ws_need = attn_varlen_workspace_size(batch, num_heads_q, num_heads_kv, head_dim, max_seqlen_q, total_k);
+    if (!workspace || workspace_bytes < ws_need) return ATTN_ERR_WORKSPACE_TOO_SMALL;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return ATTN_ERR_INVALID_ARG;
+    void *v16 = reinterpret_cast<uint8_t *>(workspace) + kWsHeader;
     const int64_t kv_rows = paged ? num_blocks * (int64_t)block_size : total_k;
     const int kv_box = paged ? (block_size < kPrefillKeyTile ? block_size : kPrefillKeyTile) : kPrefillKeyTile;
     CUtensorMap qmap, kmap, vmap;
     if (!make_map(&qmap, q, total_q, num_heads_q, head_dim, q_row_stride, G, tps) ||
         !make_map(&kmap, k, kv_rows, num_heads_kv, head_dim, k_row_stride, 1, kv_box) ||
-        !make_map(&vmap, v, kv_rows, num_heads_kv, head_dim, v_row_stride, 1, kv_box))
+        !make_map(&vmap, v16, total_k, num_heads_kv, head_dim, (int64_t)num_heads_kv * head_dim, 1,
+                  kPrefillKeyTile, CU_TENSOR_MAP_DATA_TYPE_FLOAT16))
         return ATTN_ERR_LAUNCH_FAILED;
 
     PrefillParams p;
     memset(&p, 0, sizeof p);
+    p.v = reinterpret_cast<const __nv_bfloat16 *>(v);
+    p.v = reinterpret_cast<const __nv_bfloat16 *>(v);
+    p.v16 = reinterpret_cast<__half *>(v16);
     p.out = reinterpret_cast<__nv_bfloat16 *>(out);
     p.lse = lse;
     p.cu_q = cu_seqlens_q;
     p.cu_k = cu_seqlens_k;
     p.block_table = block_table;
     p.total_q = total_q;
+    p.total_k = total_k;
     p.out_row_stride = out_row_stride;
+    p.v_row_stride = v_row_stride;
+    p.head_dim = head_dim;
+    p.max_seqlen_k = max_seqlen_k;
+    p.v_row_stride = v_row_stride;
     p.num_blocks = num_blocks;
     p.bt_stride = block_table_stride;
     p.block_size = block_size;

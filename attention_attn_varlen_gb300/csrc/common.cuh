@@ -17,6 +17,7 @@ namespace attn {
 enum : uint32_t {
     ERR_INDEX = 1u << 0,      // an index read from device memory was out of range
     ERR_TIMEOUT = 1u << 1,    // a bounded wait ran out
+    ERR_RANGE = 1u << 2,      // an input value outside the range the kernel handles (clamped)
     SRC_STORE = 1u << 8,
     SRC_DECODE = 1u << 9,
     SRC_COMBINE = 1u << 10,
@@ -239,6 +240,11 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, int b_mn_maj
            ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
+// Instruction descriptor of tcgen05.mma kind::f16, f16 x f16 -> f32.
+__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N, int b_mn_major) {
+    return (1u << 4) | ((uint32_t)(b_mn_major & 1) << 16) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
 // ---------------------------------------------------------------------------
 // numerics helpers
 // ---------------------------------------------------------------------------
@@ -253,6 +259,34 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     uint32_t r;
     asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
     return r;
+}
+
+// two floats -> packed f16x2 (round to nearest even); lo in the low half
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// packed bf16x2 -> packed f16x2 of the values divided by 16 (exact for
+// |v| in [2^-10, 2^20); smaller values become fp16 subnormals, larger ones
+// saturate at the largest finite fp16)
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2_div16(uint32_t w) {
+    const float lo = __uint_as_float(w << 16) * 0.0625f;
+    const float hi = __uint_as_float(w & 0xFFFF0000u) * 0.0625f;
+    uint32_t r;
+    asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// 16-byte global load through the non-coherent path without L1 allocation
+// (data read once)
+__device__ __forceinline__ uint4 ldg_stream16(const void *ptr) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(ptr));
+    return v;
 }
 
 // ---------------------------------------------------------------------------

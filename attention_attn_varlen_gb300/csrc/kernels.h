@@ -5,6 +5,7 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -27,14 +28,16 @@ struct DecodeParams {
 };
 
 struct PrefillParams {
+    const __nv_bfloat16 *v;      // contiguous [total_k, Hkv, D] (row stride v_row_stride) or the V cache
+    __half *v16;                 // workspace: V / 16 in fp16, [total_k, Hkv, D] by logical key
     __nv_bfloat16 *out;          // [total_q, Hq, D], row stride out_row_stride
     float *lse;                  // [Hq, total_q] or null
     const int32_t *cu_q, *cu_k;
     const int32_t *block_table;  // null: contiguous K/V
-    int64_t total_q, out_row_stride;
+    int64_t total_q, total_k, out_row_stride, v_row_stride;
     int64_t num_blocks;
     int bt_stride, block_size, rows_per_box;
-    int batch, Hq, Hkv, G, causal;
+    int batch, Hq, Hkv, G, causal, head_dim, max_seqlen_k;
     int num_pairs;               // grid.x: slot pairs per (sequence, KV head) at max_seqlen_q
     float scale_log2;            // softmax_scale * log2(e), > 0
     uint32_t *err;

@@ -25,8 +25,15 @@
 //              4-stage ring (128 keys x head_dim, 128-byte swizzle)
 //   warp 9     TMEM allocator and single-thread MMA issuer
 // TMEM (512 columns): S_A [0,128), S_B [128,256) fp32; O_A, O_B after them.
-// P is written back by the softmax threads over S: P_hi = bf16(P) in columns
-// 0-63, P_lo = bf16(P - P_hi) in columns 64-127; PV runs on both terms.
+//
+// PV runs in fp16: the softmax threads write P' = 16 P as fp16 over the first
+// 64 columns of S, and V comes from an fp16 copy V' = V / 16 made by
+// attn_v_to_f16_kernel before the attention kernel (laid out contiguously by
+// sequence, also for a paged cache).  The product P' V' equals P V, and the
+// weights keep 11 significant bits: with bf16 weights (8 bits) the weight
+// rounding adds about as much error as the bf16 output rounding and the result
+// exceeds a 2e-3 relative RMS error.  One MMA takes A and B of the same type,
+// hence the fp16 copy of V.
 //
 // MMA order per key tile j:  S_A(j), PV_B(j-1), S_B(j), PV_A(j)
 // so the tensor core works on one slot while the other slot's softmax runs.
@@ -55,7 +62,7 @@ struct PfSmem {
     static constexpr int kTileBytes = kPanels * kPanelBytes; // one Q slot, K tile or V tile
     static constexpr int kRingOff = 2 * kTileBytes;
     static constexpr int kBarOff = kRingOff + kPfStages * kTileBytes;
-    static constexpr int kNumBars = 17;
+    static constexpr int kNumBars = 16;
     static constexpr int kBytes = kBarOff + kNumBars * 8 + 16 + 1024 /*align slack*/;
 };
 
@@ -70,20 +77,68 @@ __device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t q_base, uint3
     }
 }
 
-// O (+)= P_hi V + P_lo V.  P is carried as two bf16 terms (P_hi = bf16(P),
-// P_lo = bf16(P - P_hi)) so the weights keep about 16 significant bits; a
-// single bf16 P adds a weight-rounding error comparable to the bf16 output
-// rounding itself.
+// O (+)= P' V': fp16 operands, P' from TMEM, V' (MN-major) from shared memory
 template <int D>
 __device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint32_t v_base, bool accumulate) {
     using S = PfSmem<D>;
-    constexpr uint32_t idesc = idesc_bf16_f32(BM, D, 1);
+    constexpr uint32_t idesc = idesc_f16_f32(BM, D, 1);
 #pragma unroll
     for (int kk = 0; kk < BN / 16; ++kk) {
         const uint64_t vd = sw128_desc(v_base + kk * 16 * 128, S::kPanelBytes, 1024);
         tc_mma_ts(d_tmem, p_tmem + kk * 8, vd, idesc, (accumulate || kk > 0) ? 1u : 0u);
-        tc_mma_ts(d_tmem, p_tmem + BN / 2 + kk * 8, vd, idesc, 1u);
     }
+}
+
+// ---------------------------------------------------------------------------
+// V -> V' = fp16(V / 16), laid out [total_k, Hkv, D] by logical key
+// (cu_seqlens_k[b] + j), read contiguously or through the block table.
+// One CTA per (32 keys, sequence).  |v| >= 2^20 (or non-finite) does not fit
+// and is clamped and reported.
+// ---------------------------------------------------------------------------
+constexpr int kCvtThreads = 256;
+constexpr int kCvtKeys = 32;
+
+__global__ void __launch_bounds__(kCvtThreads) attn_v_to_f16_kernel(const PrefillParams p) {
+    const int b = blockIdx.y;
+    const int k0 = __ldg(p.cu_k + b), k1 = __ldg(p.cu_k + b + 1);
+    const int Lk = k1 - k0;
+    const int key0 = blockIdx.x * kCvtKeys;
+    if (blockIdx.x == gridDim.x - 1 && threadIdx.x == 0 && key0 + kCvtKeys < Lk)
+        record_error(p.err, ERR_INDEX | SRC_PREFILL);   // longer than the stated max_seqlen_k
+    if (Lk <= 0 || key0 >= Lk) return;
+    if (k0 < 0 || (int64_t)k1 > p.total_k) {
+        if (threadIdx.x == 0 && blockIdx.x == 0) record_error(p.err, ERR_INDEX | SRC_PREFILL);
+        return;
+    }
+    const int row_chunks = p.Hkv * p.head_dim / 8;   // 16-byte chunks per key row
+    const int nkeys = min(kCvtKeys, Lk - key0);
+    const int32_t *bt = p.block_table ? p.block_table + (int64_t)b * p.bt_stride : nullptr;
+    uint32_t big = 0;
+    for (int idx = threadIdx.x; idx < nkeys * row_chunks; idx += kCvtThreads) {
+        const int kk = idx / row_chunks, ch = idx % row_chunks;
+        const int key = key0 + kk;
+        int64_t src_row;
+        if (bt) {
+            const int blk = __ldg(bt + key / p.block_size);
+            if (blk < 0 || (int64_t)blk >= p.num_blocks) {
+                record_error(p.err, ERR_INDEX | SRC_PREFILL);
+                continue;
+            }
+            src_row = (int64_t)blk * p.block_size + key % p.block_size;
+        } else {
+            src_row = (int64_t)k0 + key;
+        }
+        uint4 v = ldg_stream16(p.v + src_row * p.v_row_stride + ch * 8);
+        big = __vmaxu2(big, __vmaxu2(v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu));
+        big = __vmaxu2(big, __vmaxu2(v.z & 0x7FFF7FFFu, v.w & 0x7FFF7FFFu));
+        v.x = bf16x2_to_f16x2_div16(v.x);
+        v.y = bf16x2_to_f16x2_div16(v.y);
+        v.z = bf16x2_to_f16x2_div16(v.z);
+        v.w = bf16x2_to_f16x2_div16(v.w);
+        *reinterpret_cast<uint4 *>(p.v16 + ((int64_t)k0 + key) * (row_chunks * 8) + ch * 8) = v;
+    }
+    if (__any_sync(0xffffffffu, (big & 0xFFFFu) >= 0x4980u || (big >> 16) >= 0x4980u) && (threadIdx.x & 31) == 0)
+        record_error(p.err, ERR_RANGE | SRC_PREFILL);
 }
 
 template <int D>
@@ -102,8 +157,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     uint64_t *s_full = bars + 1 + 2 * kPfStages;   // [2]
     uint64_t *p_ready = s_full + 2;                // [2]
     uint64_t *o_full = p_ready + 2;                // [2]
-    uint64_t *fix_bar = o_full + 2;
-    uint64_t *drain_bar = fix_bar + 1;
+    uint64_t *drain_bar = o_full + 2;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + S::kNumBars);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
@@ -146,7 +200,6 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             mbar_init(&p_ready[x], 128);
             mbar_init(&o_full[x], 1);
         }
-        mbar_init(fix_bar, 1);
         mbar_init(drain_bar, 1);
         *abort_flag = 0;
         fence_mbar_init();
@@ -182,7 +235,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         const bool paged = p.block_table != nullptr;
         const int32_t *bt = paged ? p.block_table + (int64_t)b * p.bt_stride : nullptr;
         const int oob_row = paged ? (int)(p.num_blocks * p.block_size) : 0;
-        int it = 0, fixc = 0;
+        int it = 0;
         bool ok = true;
         for (int j = 0; j < n && ok; ++j) {
             for (int w = 0; w < 2; ++w) {   // 0: K tile, 1: V tile
@@ -195,14 +248,12 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                 uint8_t *dst = sRing + st * S::kTileBytes;
                 const CUtensorMap *map = w ? &vmap : &kmap;
                 const int key0 = j * BN;
-                // paged V tile that runs past the sequence: rows past the end are
-                // cache slots of unknown content (possibly NaN).  Land it on a
-                // private barrier, zero those rows, then publish.
-                const bool fix = paged && w == 1 && key0 + BN > Lk;
-                uint64_t *bar = fix ? fix_bar : &full[st];
+                uint64_t *bar = &full[st];
                 if (lane == 0) {
                     mbar_arrive_expect_tx(bar, (uint32_t)S::kTileBytes);
-                    if (!paged) {
+                    // V' is contiguous by logical key (rows past the sequence hold the
+                    // next sequence's keys or lie past the end: finite, zero-filled)
+                    if (!paged || w == 1) {
 #pragma unroll
                         for (int pn = 0; pn < S::kPanels; ++pn)
                             tma_load_3d(dst + pn * S::kPanelBytes, map, bar, pn * 64, hkv, ks0 + key0);
@@ -223,22 +274,6 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                                 tma_load_3d(dst + pn * S::kPanelBytes + i * rpb * 128, map, bar, pn * 64, hkv, row);
                         }
                     }
-                }
-                if (fix) {
-                    int got2 = 1;
-                    if (lane == 0) got2 = mbar_wait(fix_bar, (uint32_t)fixc & 1u, abort_flag, p.err, SRC_PREFILL);
-                    got2 = __shfl_sync(0xffffffffu, got2, 0);
-                    ++fixc;
-                    if (!got2) { ok = false; break; }
-                    const int vr = Lk - key0;   // valid rows, >= 1
-                    for (int idx = lane; idx < (BN - vr) * (D / 8); idx += 32) {
-                        const int r = vr + idx / (D / 8), ch = idx % (D / 8);
-                        *reinterpret_cast<uint4 *>(dst + (ch / 8) * S::kPanelBytes + sw128_off(r, ch % 8)) =
-                            make_uint4(0, 0, 0, 0);
-                    }
-                    fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&full[st]);
                 }
                 ++it;
             }
@@ -348,23 +383,20 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                 m_ref = m_new;
             }
             l *= alpha;
-            const float nref = (m_ref == -INFINITY) ? 0.f : -m_ref;
-            // P = 2^(s*scale*log2e - m_ref) as P_hi (columns 0-63 of S) and
-            // P_lo = P - P_hi (columns 64-127), both bf16
+            // P' = 2^(s*scale*log2e - m_ref + 4) = 16 P
+            const float nref = ((m_ref == -INFINITY) ? 0.f : -m_ref) + 4.0f;
+            // P' (fp16) over the first 64 columns of S
 #pragma unroll
             for (int c4 = 0; c4 < BN / 32; ++c4) {
-                uint32_t pk[16], pl[16];
+                uint32_t pk[16];
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
                     const float x0 = ex2(fmaf(s[c4 * 32 + 2 * i], sl2, nref));
                     const float x1 = ex2(fmaf(s[c4 * 32 + 2 * i + 1], sl2, nref));
                     l += x0 + x1;
-                    const uint32_t h = pack_bf16x2(x0, x1);
-                    pk[i] = h;
-                    pl[i] = pack_bf16x2(x0 - __uint_as_float(h << 16), x1 - __uint_as_float(h & 0xFFFF0000u));
+                    pk[i] = pack_f16x2(x0, x1);
                 }
                 tmem_st16(tS + (uint32_t)(c4 * 16), pk);
-                tmem_st16(tS + (uint32_t)(BN / 2 + c4 * 16), pl);
             }
             // O *= alpha where the reference moved (O of tile 0 is written, not accumulated)
             if (j > 0 && __any_sync(0xffffffffu, need)) {
@@ -388,7 +420,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             tc_fence_after();
         }
         if (ok) {
-            const float inv = l > 0.f ? 1.f / l : 0.f;
+            const float inv = l > 0.f ? 16.f / l : 0.f;   // l accumulated P' = 16 P
             __nv_bfloat16 *orow = p.out + (int64_t)(qs + (row_valid ? tok : 0)) * p.out_row_stride + (int64_t)head * D;
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
@@ -412,7 +444,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             }
             if (row_valid && p.lse)
                 p.lse[(int64_t)head * p.total_q + qs + tok] =
-                    l > 0.f ? (m_ref + __log2f(l)) * 0.69314718055994531f : -INFINITY;
+                    l > 0.f ? (m_ref + __log2f(l) - 4.0f) * 0.69314718055994531f : -INFINITY;
         }
     }
 
@@ -437,6 +469,10 @@ static cudaError_t launch_prefill_t(const CUtensorMap &qmap, const CUtensorMap &
         if (e != cudaSuccess) return e;
         attr_done[dev] = true;
     }
+    dim3 cgrid((p.max_seqlen_k + kCvtKeys - 1) / kCvtKeys, p.batch);
+    attn_v_to_f16_kernel<<<cgrid, kCvtThreads, 0, stream>>>(p);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
     dim3 grid(p.num_pairs, p.Hkv, p.batch);
     attn_prefill_kernel<D><<<grid, kPfThreads, S::kBytes, stream>>>(qmap, kmap, vmap, p);
     return cudaGetLastError();

@@ -504,7 +504,7 @@ def main():
                      else "fallback 1.9 PFLOP/s"},
         "e2e": {"value": aggregate(flops, e2e_max / 1e3, world) / 1e12, "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_max},
-        "gpu_launches": args.steps,
+        "gpu_launches": 2 * args.steps,   # per step: the V fp16 pre-pass and the attention kernel
         "clocks": clocks,
         "wall_s_timed": wall,
         "device_status": status,

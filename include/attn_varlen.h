@@ -59,7 +59,9 @@ typedef enum attn_status {
     ATTN_ERR_LAUNCH_FAILED = 4,      /* a CUDA runtime or driver call failed */
     ATTN_ERR_DEVICE_TIMEOUT = 5,     /* a kernel's bounded wait ran out (reported by the error word) */
     ATTN_ERR_DEVICE_INDEX = 6,       /* a device-side index was out of range (reported by the error word) */
-    ATTN_ERR_NO_DEVICE = 7           /* no CUDA device, or the device query failed */
+    ATTN_ERR_NO_DEVICE = 7,          /* no CUDA device, or the device query failed */
+    ATTN_ERR_DEVICE_RANGE = 8        /* an input value outside the range a kernel handles (reported by the
+                                        error word; see attn_varlen_fwd) */
 } attn_status;
 
 /* ------------------------------------------------------------------------
@@ -82,14 +84,20 @@ typedef enum attn_status {
  *                log-sum-exp of the scaled logits of each row (-inf for a row
  *                that sees no key, whose output is 0)
  *   cu_seqlens_q/_k  int32 [batch + 1], non-decreasing, starting at 0
- *   total_q, total_k row counts of q/out and of contiguous k/v (total_k is
- *                ignored when paged); kernels never touch rows beyond them
+ *   total_q      rows of q / out; kernels never touch rows beyond them
+ *   total_k      contiguous: rows of k / v; paged: an upper bound of
+ *                cu_seqlens_k[batch] (all sequences' context lengths), e.g.
+ *                batch * max_seqlen_k.  It sizes the workspace.
  *   max_seqlen_q/_k  host-side upper bounds of the per-sequence lengths
  *   causal       nonzero: bottom-right aligned mask, query i of a sequence
  *                with Lq queries and Lk keys sees keys j <= Lk - Lq + i
  *   block_size   paged only: a power of two >= 16; num_blocks > 0
  *   workspace    device scratch of at least attn_varlen_workspace_size(...)
- *                bytes (scheduler metadata); may be NULL when that size is 0
+ *                bytes, 256-byte aligned: it receives an fp16 copy of V (V / 16)
+ *                laid out by logical key, which the P V product reads
+ * Value range: the P V product runs in fp16 on 16 P and V / 16, so V entries
+ * must satisfy |v| < 2^20; larger (or non-finite) entries are clamped and
+ * reported as ATTN_ERR_DEVICE_RANGE by attn_get_last_device_error.
  * Returns ATTN_OK, ATTN_ERR_INVALID_ARG, ATTN_ERR_UNSUPPORTED,
  * ATTN_ERR_WORKSPACE_TOO_SMALL, ATTN_ERR_LAUNCH_FAILED or ATTN_ERR_NO_DEVICE.
  * ------------------------------------------------------------------------ */
@@ -105,8 +113,10 @@ ATTN_API attn_status attn_varlen_fwd(const void *q, const void *k, const void *v
                             int64_t out_row_stride,
                             void *workspace, size_t workspace_bytes, void *stream);
 
-/* Bytes of device workspace attn_varlen_fwd needs for these sizes. */
-ATTN_API size_t attn_varlen_workspace_size(int batch, int num_heads_q, int num_heads_kv, int max_seqlen_q);
+/* Bytes of device workspace attn_varlen_fwd needs for these sizes (total_k as
+ * passed to attn_varlen_fwd). */
+ATTN_API size_t attn_varlen_workspace_size(int batch, int num_heads_q, int num_heads_kv, int head_dim,
+                                           int max_seqlen_q, int64_t total_k);
 
 /* ------------------------------------------------------------------------
  * attn_decode_paged -- one new query token per sequence against its paged
@@ -206,9 +216,9 @@ ATTN_API const char *attn_status_string(attn_status status);
 
 /* Synchronises `stream`, then reads and clears the device error word of the
  * current device.  Returns ATTN_OK if no kernel recorded a problem since the
- * last call, else ATTN_ERR_DEVICE_INDEX or ATTN_ERR_DEVICE_TIMEOUT (the first
- * kind recorded), or ATTN_ERR_LAUNCH_FAILED if the stream itself reports a
- * CUDA error.  *detail (nullable) receives the raw error word. */
+ * last call, else ATTN_ERR_DEVICE_INDEX, ATTN_ERR_DEVICE_TIMEOUT or
+ * ATTN_ERR_DEVICE_RANGE (in that order of precedence), or
+ * ATTN_ERR_LAUNCH_FAILED if the stream itself reports a CUDA error.  *detail (nullable) receives the raw error word. */
 ATTN_API attn_status attn_get_last_device_error(void *stream, uint32_t *detail);
 
 /* ATTN_ABI_VERSION of the loaded library. */

@@ -23,7 +23,7 @@ def test_every_declared_symbol_is_exported(L):
 
 def test_abi_version_and_status_strings(L):
     assert L.attn_abi_version() == 1
-    for s in range(8):
+    for s in range(9):
         assert L.attn_status_string(s)
     assert L.attn_status_string(99) == b"unknown status"
 

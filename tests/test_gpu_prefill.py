@@ -256,3 +256,30 @@ def test_c3_prefix_paged_full_size_sampled():
     check_rows(out, lse, ref, ref_lse, rows, Hq, "c3")
     del kc, vc
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("vscale", [1e5, 1e-3])
+def test_value_scale_of_v(vscale):
+    """PV runs in fp16 on 16 P and V / 16: large and small V keep their
+    relative accuracy (the metrics are scale-free)."""
+    cfg = workloads.small_varlen(52, [300, 77], [300, 77], 8, 2, 128)
+    q, k = cfg.q(), cfg.k()
+    v = (cfg.v().float() * vscale).to(torch.bfloat16)
+    out, lse = run_contig(cfg, q, k, v)
+    torch.cuda.synchronize()
+    assert av.get_last_device_error()[0] == 0
+    ref, _ = oracle.attn_varlen(q, k, v, cfg.cu_q, cfg.cu_k, 8, 2, 128, cfg.scale, True)
+    g = out.float().cpu().double().numpy().reshape(ref.shape)
+    rel = np.sqrt(((g - ref) ** 2).sum() / (ref ** 2).sum())
+    assert rel <= 2e-3, rel
+
+
+def test_v_beyond_fp16_range_is_reported():
+    cfg = workloads.small_varlen(53, [100], [100], 4, 4, 128)
+    q, k, v = cfg.q(), cfg.k(), cfg.v().clone()
+    v[5, 0, 3] = 3.0e6
+    av.get_last_device_error()
+    out, _ = run_contig(cfg, q, k, v)
+    st, word = av.get_last_device_error()
+    assert st == 8 and word & 4
+    assert torch.isfinite(out.float()).all()
