@@ -181,17 +181,30 @@ attn_status attn_get_last_device_error(void *stream, uint32_t *detail) {
 }
 
 // ---------------------------------------------------------------------------
-// Workspace: the fp16 copy of V (V / 16), [total_k, Hkv, D] by logical key,
-// after a 256-byte header.
+// Workspace: a 256-byte header (unit count), the fp16 copy of V (V / 16,
+// [total_k, Hkv, D] by logical key), then the unit list (one int2 per
+// (sequence, query pair, KV head)).
 static const size_t kWsHeader = 256;
+
+static int64_t varlen_max_pairs(int num_heads_q, int num_heads_kv, int max_seqlen_q) {
+    if (num_heads_kv <= 0 || num_heads_q <= 0 || num_heads_q % num_heads_kv || max_seqlen_q < 0) return -1;
+    const int G = num_heads_q / num_heads_kv;
+    if (kPrefillSlotRows % G) return -1;
+    const int64_t tps = kPrefillSlotRows / G;
+    return ((int64_t)max_seqlen_q + 2 * tps - 1) / (2 * tps);
+}
+
+static size_t v16_bytes(int num_heads_kv, int head_dim, int64_t total_k) {
+    const size_t b = (size_t)total_k * (size_t)num_heads_kv * (size_t)head_dim * 2;
+    return (b + 255) & ~(size_t)255;
+}
 
 size_t attn_varlen_workspace_size(int batch, int num_heads_q, int num_heads_kv, int head_dim, int max_seqlen_q,
                                   int64_t total_k) {
-    (void)batch;
-    (void)num_heads_q;
-    (void)max_seqlen_q;
-    if (num_heads_kv <= 0 || head_dim <= 0 || total_k < 0) return 0;
-    return kWsHeader + (size_t)total_k * (size_t)num_heads_kv * (size_t)head_dim * 2;
+    const int64_t mp = varlen_max_pairs(num_heads_q, num_heads_kv, max_seqlen_q);
+    if (batch <= 0 || mp < 0 || head_dim <= 0 || total_k < 0) return 0;
+    return kWsHeader + v16_bytes(num_heads_kv, head_dim, total_k) +
+           (size_t)batch * (size_t)mp * (size_t)num_heads_kv * sizeof(int2);
 }
 
 attn_status attn_varlen_fwd(const void *q, const void *k, const void *v, void *out, float *lse,
@@ -235,10 +248,15 @@ attn_status attn_varlen_fwd(const void *q, const void *k, const void *v, void *o
     if (total_q == 0 || max_seqlen_q == 0) return ATTN_OK;
 
     const int tps = kPrefillSlotRows / G;
+    const int64_t max_pairs = varlen_max_pairs(num_heads_q, num_heads_kv, max_seqlen_q);
+    if (max_pairs <= 0 || max_pairs > 0xFFFF || num_heads_kv > 0x7FFF ||
+        (int64_t)batch * max_pairs * num_heads_kv > (int64_t)INT32_MAX / 4)
+        return ATTN_ERR_UNSUPPORTED;
     const size_t ws_need = attn_varlen_workspace_size(batch, num_heads_q, num_heads_kv, head_dim, max_seqlen_q, total_k);
     if (!workspace || workspace_bytes < ws_need) return ATTN_ERR_WORKSPACE_TOO_SMALL;
     if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return ATTN_ERR_INVALID_ARG;
-    void *v16 = reinterpret_cast<uint8_t *>(workspace) + kWsHeader;
+    uint8_t *ws = reinterpret_cast<uint8_t *>(workspace);
+    void *v16 = ws + kWsHeader;
     const int64_t kv_rows = paged ? num_blocks * (int64_t)block_size : total_k;
     const int kv_box = paged ? (block_size < kPrefillKeyTile ? block_size : kPrefillKeyTile) : kPrefillKeyTile;
     CUtensorMap qmap, kmap, vmap;
@@ -274,7 +292,10 @@ attn_status attn_varlen_fwd(const void *q, const void *k, const void *v, void *o
     p.Hkv = num_heads_kv;
     p.G = G;
     p.causal = causal ? 1 : 0;
-    p.num_pairs = (max_seqlen_q + 2 * tps - 1) / (2 * tps);
+    p.max_pairs = (int)max_pairs;
+    p.num_ctas = (int)((int64_t)batch * max_pairs * num_heads_kv);
+    p.unit_count = reinterpret_cast<int *>(ws);
+    p.units = reinterpret_cast<int2 *>(ws + kWsHeader + v16_bytes(num_heads_kv, head_dim, total_k));
     p.scale_log2 = softmax_scale * 1.4426950408889634f;
     p.err = d->err;
     cudaError_t e = launch_prefill(qmap, kmap, vmap, p, head_dim, reinterpret_cast<cudaStream_t>(stream));

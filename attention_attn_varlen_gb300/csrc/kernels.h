@@ -38,7 +38,10 @@ struct PrefillParams {
     int64_t num_blocks;
     int bt_stride, block_size, rows_per_box;
     int batch, Hq, Hkv, G, causal, head_dim, max_seqlen_k;
-    int num_pairs;               // grid.x: slot pairs per (sequence, KV head) at max_seqlen_q
+    int max_pairs;               // slot pairs per sequence at max_seqlen_q
+    int num_ctas;                // grid size: the largest possible number of units
+    int2 *units;                 // workspace: (sequence, pair | kv_head << 16), scheduled order
+    int *unit_count;             // workspace: [0] number of units
     float scale_log2;            // softmax_scale * log2(e), > 0
     uint32_t *err;
 };

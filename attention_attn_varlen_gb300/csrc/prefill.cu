@@ -13,7 +13,8 @@
 //   * causal masking is bottom-right aligned: query i of a sequence with Lq
 //     queries and Lk keys sees keys j <= Lk - Lq + i.
 //
-// Work unit (one CTA): a sequence b, a KV head, and two query "slots" A and B
+// Work unit (one CTA, taken from the scheduler's list): a sequence b, a KV
+// head, and two query "slots" A and B
 // of 128 rows each.  A slot packs 128/G consecutive tokens x the G query heads
 // that share the KV head (row r = token_offset * G + g), so one K/V stream
 // feeds 256 query rows.  Slot B holds the 128/G tokens after slot A.
@@ -141,6 +142,90 @@ __global__ void __launch_bounds__(kCvtThreads) attn_v_to_f16_kernel(const Prefil
         record_error(p.err, ERR_RANGE | SRC_PREFILL);
 }
 
+// ---------------------------------------------------------------------------
+// Scheduler: one CTA writes the unit list; CTA i of the attention kernel
+// takes entry i (CTAs past the end exit at once, and they come last).
+// Sequences come longest first (counting sort on their pair count), so the
+// last units launched are short; inside a sequence units are grouped by KV
+// head and run from the last query pair (most key tiles) to the first, so
+// units running together share one K/V stream in L2.
+// Entry = (sequence, pair | kv_head << 16).  Also flags invalid offsets and
+// sequences longer than max_seqlen_q.
+// ---------------------------------------------------------------------------
+constexpr int kSchedThreads = 1024;
+constexpr int kSchedBuckets = 4096;
+
+__device__ __forceinline__ int pf_pairs(const PrefillParams &p, int b, bool report) {
+    const int tps = BM / p.G;
+    const int qs = __ldg(p.cu_q + b), qe = __ldg(p.cu_q + b + 1);
+    const int ks0 = __ldg(p.cu_k + b), ke = __ldg(p.cu_k + b + 1);
+    if (qs < 0 || qe < qs || ke < ks0 || (int64_t)qe > p.total_q) {
+        if (report) record_error(p.err, ERR_INDEX | SRC_PREFILL);
+        return 0;
+    }
+    int pairs = (qe - qs + 2 * tps - 1) / (2 * tps);
+    if (pairs > p.max_pairs) {   // longer than the stated max_seqlen_q
+        if (report) record_error(p.err, ERR_INDEX | SRC_PREFILL);
+        pairs = p.max_pairs;
+    }
+    return pairs;
+}
+
+__global__ void __launch_bounds__(kSchedThreads) attn_prefill_schedule_kernel(const PrefillParams p) {
+    __shared__ int units_in[kSchedBuckets];   // units per pair-count bucket, then running offsets
+    __shared__ int wsum[kSchedThreads / 32];
+    for (int i = threadIdx.x; i < kSchedBuckets; i += kSchedThreads) units_in[i] = 0;
+    __syncthreads();
+    for (int b = threadIdx.x; b < p.batch; b += kSchedThreads) {
+        const int pairs = pf_pairs(p, b, true);
+        if (pairs) atomicAdd(&units_in[min(pairs, kSchedBuckets - 1)], pairs * p.Hkv);
+    }
+    __syncthreads();
+    // descending exclusive scan: offset of a bucket = units of all larger buckets
+    constexpr int PER = kSchedBuckets / kSchedThreads;
+    int local[PER], sum = 0;
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+        local[i] = units_in[kSchedBuckets - 1 - (threadIdx.x * PER + i)];
+        sum += local[i];
+    }
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    int incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+    }
+    if (lane == 31) wsum[wid] = incl;
+    __syncthreads();
+    if (wid == 0) {
+        const int w = wsum[lane];
+        int wi = w;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, wi, o);
+            if (lane >= o) wi += y;
+        }
+        wsum[lane] = wi - w;   // exclusive
+    }
+    __syncthreads();
+    int run = wsum[wid] + incl - sum;
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+        units_in[kSchedBuckets - 1 - (threadIdx.x * PER + i)] = run;
+        run += local[i];
+    }
+    if (threadIdx.x == kSchedThreads - 1) p.unit_count[0] = run;
+    __syncthreads();
+    for (int b = threadIdx.x; b < p.batch; b += kSchedThreads) {
+        const int pairs = pf_pairs(p, b, false);
+        if (!pairs) continue;
+        int off = atomicAdd(&units_in[min(pairs, kSchedBuckets - 1)], pairs * p.Hkv);
+        for (int h = 0; h < p.Hkv; ++h)
+            for (int i = 0; i < pairs; ++i) p.units[off++] = make_int2(b, (pairs - 1 - i) | (h << 16));
+    }
+}
+
 template <int D>
 __global__ void __launch_bounds__(kPfThreads, 1)
     attn_prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
@@ -162,19 +247,15 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int pair = p.num_pairs - 1 - (int)blockIdx.x;   // longest pairs first
-    const int hkv = blockIdx.y, b = blockIdx.z;
+    if ((int)blockIdx.x >= p.unit_count[0]) return;
+    const int2 unit = p.units[blockIdx.x];
+    const int b = unit.x, pair = unit.y & 0xFFFF, hkv = unit.y >> 16;
     const int G = p.G, tps = BM / G;
 
     const int qs = __ldg(p.cu_q + b), qe = __ldg(p.cu_q + b + 1);
     const int ks0 = __ldg(p.cu_k + b), ke = __ldg(p.cu_k + b + 1);
     const int Lq = qe - qs, Lk = ke - ks0;
-    if (qs < 0 || Lq < 0 || Lk < 0 || (int64_t)qe > p.total_q) {
-        if (threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0) record_error(p.err, ERR_INDEX | SRC_PREFILL);
-        return;
-    }
-    if (blockIdx.x == 0 && threadIdx.x == 0 && (int64_t)Lq > (int64_t)p.num_pairs * 2 * tps)
-        record_error(p.err, ERR_INDEX | SRC_PREFILL);   // longer than the stated max_seqlen_q
+    if (qs < 0 || Lq < 0 || Lk < 0 || (int64_t)qe > p.total_q) return;   // reported by the scheduler
     const int t0A = pair * 2 * tps;
     if (t0A >= Lq) return;
     const int t0B = t0A + tps;
@@ -469,12 +550,12 @@ static cudaError_t launch_prefill_t(const CUtensorMap &qmap, const CUtensorMap &
         if (e != cudaSuccess) return e;
         attr_done[dev] = true;
     }
+    attn_prefill_schedule_kernel<<<1, kSchedThreads, 0, stream>>>(p);
     dim3 cgrid((p.max_seqlen_k + kCvtKeys - 1) / kCvtKeys, p.batch);
     attn_v_to_f16_kernel<<<cgrid, kCvtThreads, 0, stream>>>(p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    dim3 grid(p.num_pairs, p.Hkv, p.batch);
-    attn_prefill_kernel<D><<<grid, kPfThreads, S::kBytes, stream>>>(qmap, kmap, vmap, p);
+    attn_prefill_kernel<D><<<p.num_ctas, kPfThreads, S::kBytes, stream>>>(qmap, kmap, vmap, p);
     return cudaGetLastError();
 }
 
