@@ -453,9 +453,16 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                 for (int c = 0; c < BN; ++c)
                     if (key0 + c > lim) s[c] = -INFINITY;
             }
-            float mx = -INFINITY;
+            // row max: eight independent chains (chain q takes columns q, q + 8, ...)
+            float mx8[8];
 #pragma unroll
-            for (int c = 0; c < BN; ++c) mx = fmaxf(mx, s[c]);
+            for (int q = 0; q < 8; ++q) {
+                mx8[q] = max3f(s[q], s[q + 8], s[q + 16]);
+#pragma unroll
+                for (int k = 3; k < 15; k += 2) mx8[q] = max3f(mx8[q], s[q + 8 * k], s[q + 8 * k + 8]);
+                mx8[q] = fmaxf(mx8[q], s[q + 120]);
+            }
+            const float mx = max3f(max3f(mx8[0], mx8[1], mx8[2]), max3f(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]));
             const float m_new = fmaxf(m_ref, mx * sl2);
             const bool need = m_new > m_ref + 8.0f;
             float alpha = 1.f;
@@ -466,19 +473,23 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             l *= alpha;
             // P' = 2^(s*scale*log2e - m_ref + 4) = 16 P
             const float nref = ((m_ref == -INFINITY) ? 0.f : -m_ref) + 4.0f;
-            // P' (fp16) over the first 64 columns of S
+            // P' (fp16) over the first 64 columns of S; the row sum in four paired accumulators
+            float la[4] = {0.f, 0.f, 0.f, 0.f}, lb[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int c4 = 0; c4 < BN / 32; ++c4) {
                 uint32_t pk[16];
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
-                    const float x0 = ex2(fmaf(s[c4 * 32 + 2 * i], sl2, nref));
-                    const float x1 = ex2(fmaf(s[c4 * 32 + 2 * i + 1], sl2, nref));
-                    l += x0 + x1;
+                    float x0, x1;
+                    fma2(x0, x1, s[c4 * 32 + 2 * i], s[c4 * 32 + 2 * i + 1], sl2, sl2, nref, nref);
+                    x0 = ex2(x0);
+                    x1 = ex2(x1);
+                    add2(la[i & 3], lb[i & 3], x0, x1);
                     pk[i] = pack_f16x2(x0, x1);
                 }
                 tmem_st16(tS + (uint32_t)(c4 * 16), pk);
             }
+            l += ((la[0] + lb[0]) + (la[1] + lb[1])) + ((la[2] + lb[2]) + (la[3] + lb[3]));
             // O *= alpha where the reference moved (O of tile 0 is written, not accumulated)
             if (j > 0 && __any_sync(0xffffffffu, need)) {
 #pragma unroll
