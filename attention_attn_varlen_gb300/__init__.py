@@ -26,7 +26,7 @@ from ._build import LIB as _LIB_PATH
 from ._build import build
 
 __all__ = ["attn_varlen_fwd", "attn_decode_paged", "store_kvcache", "get_last_device_error", "lib",
-           "build", "AttnError", "exported_symbols", "decode_num_splits", "decode_workspace_size"]
+           "build", "AttnError", "exported_symbols", "set_kernel_events", "decode_num_splits", "decode_workspace_size"]
 
 ATTN_OK = 0
 _STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "workspace too small", 4: "launch failed",
@@ -76,6 +76,8 @@ def lib():
     L.attn_get_last_device_error.restype = _i32
     L.attn_abi_version.argtypes = []
     L.attn_abi_version.restype = _i32
+    L.attn_set_kernel_events.argtypes = [_vp, _vp]
+    L.attn_set_kernel_events.restype = None
     _lib = L
     return L
 
@@ -253,6 +255,25 @@ def store_kvcache(k, v, k_cache, v_cache, slot_mapping, stream=None):
     st = lib().store_kvcache(_ptr(k), _ptr(v), _ptr(k_cache), _ptr(v_cache), _ptr(slot_mapping), N, Hkv, D, ks, vs,
                              num_slots, _stream(stream))
     _check(st, "store_kvcache")
+
+
+def set_kernel_events(before=None, after=None) -> None:
+    """Record two torch.cuda.Event objects (created with enable_timing=True)
+    around the main kernel of every later attention call from this thread:
+    the prefill's attention kernel or the decode's split-KV kernel.  Call
+    with no arguments to switch it off.  Measurement aid for benchmarks."""
+    if (before is None) != (after is None):
+        raise ValueError("give both events or neither")
+    if before is None:
+        lib().attn_set_kernel_events(None, None)
+        return
+    # torch creates the CUDA event on its first record()
+    for e in (before, after):
+        if not e.cuda_event:
+            e.record()
+    if not before.cuda_event or not after.cuda_event:
+        raise ValueError("events have no CUDA event handle")
+    lib().attn_set_kernel_events(ctypes.c_void_p(before.cuda_event), ctypes.c_void_p(after.cuda_event))
 
 
 def get_last_device_error(stream=None) -> tuple[int, int]:

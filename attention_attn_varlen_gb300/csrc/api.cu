@@ -133,7 +133,25 @@ int split_tokens_for(int max_len, int splits) {
 
 }  // namespace
 
+// measurement hook (see attn_set_kernel_events)
+static thread_local cudaEvent_t g_ev_before = nullptr, g_ev_after = nullptr;
+
+namespace attn {
+void main_kernel_event_before(cudaStream_t stream) {
+    if (g_ev_before && g_ev_after) cudaEventRecord(g_ev_before, stream);
+}
+
+void main_kernel_event_after(cudaStream_t stream) {
+    if (g_ev_before && g_ev_after) cudaEventRecord(g_ev_after, stream);
+}
+}  // namespace attn
+
 extern "C" {
+
+void attn_set_kernel_events(void *before, void *after) {
+    g_ev_before = reinterpret_cast<cudaEvent_t>(before);
+    g_ev_after = reinterpret_cast<cudaEvent_t>(after);
+}
 
 int attn_abi_version(void) { return ATTN_ABI_VERSION; }
 

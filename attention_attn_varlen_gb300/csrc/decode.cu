@@ -369,7 +369,9 @@ static cudaError_t launch_decode_t(const CUtensorMap &kmap, const CUtensorMap &v
         attr_done[dev] = true;
     }
     dim3 grid(p.num_splits, p.Hkv, batch);
+    main_kernel_event_before(stream);
     attn_decode_split_kernel<D><<<grid, kDecThreads, S::kBytes, stream>>>(kmap, vmap, p);
+    main_kernel_event_after(stream);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess || p.num_splits == 1) return e;
     const int rows = batch * p.Hq;

@@ -62,6 +62,11 @@ cudaError_t decode_noalloc_scratch(float **ptr, size_t *bytes);
 constexpr int kPrefillSlotRows = 128;
 constexpr int kPrefillKeyTile = 128;
 
+// measurement hook: record the caller's events (if set on this thread) right
+// before and right after the main kernel of a call
+void main_kernel_event_before(cudaStream_t stream);
+void main_kernel_event_after(cudaStream_t stream);
+
 cudaError_t launch_prefill(const CUtensorMap &qmap, const CUtensorMap &kmap, const CUtensorMap &vmap,
                            const PrefillParams &p, int head_dim, cudaStream_t stream);
 

@@ -566,7 +566,9 @@ static cudaError_t launch_prefill_t(const CUtensorMap &qmap, const CUtensorMap &
     attn_v_to_f16_kernel<<<cgrid, kCvtThreads, 0, stream>>>(p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
+    main_kernel_event_before(stream);
     attn_prefill_kernel<D><<<p.num_ctas, kPfThreads, S::kBytes, stream>>>(qmap, kmap, vmap, p);
+    main_kernel_event_after(stream);
     return cudaGetLastError();
 }
 

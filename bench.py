@@ -182,19 +182,32 @@ def ncu_traffic(kernel: str, units: float):
 # timing helpers
 # --------------------------------------------------------------------------
 
-def time_steps(fn, steps: int, flush=None):
+def time_steps(fn, steps: int, flush=None, kernel: bool = False):
     """Per-step CUDA-event times (ms) on the current stream; `flush` runs
-    between steps outside the events."""
+    between steps outside the events.  With kernel=True also returns the
+    per-step device time of the call's main kernel alone (events the library
+    records around that launch on the same stream)."""
     import torch
+    import attention_attn_varlen_gb300 as av
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
-    for a, b in evs:
-        if flush is not None:
-            flush()
-        a.record()
-        fn()
-        b.record()
+    kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    try:
+        for (a, b), (ka, kb) in zip(evs, kev):
+            if flush is not None:
+                flush()
+            if kernel:
+                av.set_kernel_events(ka, kb)
+            a.record()
+            fn()
+            b.record()
+    finally:
+        if kernel:
+            av.set_kernel_events()
     torch.cuda.synchronize()
-    return [a.elapsed_time(b) for a, b in evs]
+    ms = [a.elapsed_time(b) for a, b in evs]
+    if not kernel:
+        return ms
+    return ms, [a.elapsed_time(b) for a, b in kev]
 
 
 # --------------------------------------------------------------------------
@@ -221,11 +234,11 @@ def bench_varlen(av, cfg, inp, steps, warmup, flush):
     dist_barrier()
     torch.cuda.synchronize()
     t0 = time.perf_counter()
-    ms = time_steps(step, steps, flush)
+    ms, kms = time_steps(step, steps, flush, kernel=True)
     torch.cuda.synchronize()
     dist_barrier()
     wall = time.perf_counter() - t0
-    return ms, wall
+    return ms, wall, kms
 
 
 def bench_varlen_e2e(av, cfg, inp, steps, warmup, flush):
@@ -275,16 +288,18 @@ def bench_decode(av, device, steps, warmup, flush, peaks):
     for _ in range(warmup):
         step()
     torch.cuda.synchronize()
-    ms = time_steps(step, steps, flush)
+    ms, kms = time_steps(step, steps, flush, kernel=True)
     t = float(np.mean(ms)) / 1e3
+    tk = float(np.mean(kms)) / 1e3
     nbytes = workloads.decode_bytes(cfg.ctx, cfg.Hq, cfg.Hkv, cfg.D, cfg.block_size)
     gbs = nbytes / t / 1e9
     res = {"workload": "c4_decode: 256 seqs x 1 token, cache_seqlens U{128..16384}, GQA 32/8, D128, "
                        "block_size 256, random block table",
            "value": gbs, "unit": "GB/s", "ms_per_step": t * 1e3, "num_splits": splits,
            "algorithmic_bytes": nbytes,
-           "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                        "frac": gbs / peaks["hbm_gbs"],
+           "roofline": {"bound": "hbm", "kernel": "attn_decode_split_kernel", "achieved": nbytes / tk / 1e9,
+                        "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": nbytes / tk / 1e9 / peaks["hbm_gbs"],
+                        "kernel_ms": tk * 1e3,
                         "traffic": ncu_traffic("decode", float(cfg.ctx.sum()) * cfg.Hkv)},
            "launches_per_step": 2 if splits > 1 else 1}
     del kc, vc
@@ -320,23 +335,25 @@ def bench_prefix(av, device, steps, warmup, flush, peaks):
         step()
     torch.cuda.synchronize()
     ms = time_steps(step, steps, flush)
-    ms_attn = time_steps(attn, steps, flush)
+    ms_attn, kms_attn = time_steps(attn, steps, flush, kernel=True)
     ms_store = time_steps(store, steps, flush)
     flops = workloads.prefill_flops(cfg.new, cfg.lens_k, cfg.Hq, cfg.D)
     sbytes = workloads.store_bytes(int(cfg.new.sum()), cfg.Hkv, cfg.D)
     t = float(np.mean(ms)) / 1e3
     ta = float(np.mean(ms_attn)) / 1e3
+    tk = float(np.mean(kms_attn)) / 1e3
     ts = float(np.mean(ms_store)) / 1e3
     res = {"workload": "c3_prefix_paged: 32 seqs, context U{512..8192} + 1..512 new tokens, GQA 32/8, D128, "
                        "block_size 256, 65536-block pool, 8 seqs share prefix blocks; step = store_kvcache + "
                        "paged prefill",
            "value": flops / t / 1e12, "unit": "TFLOP/s", "ms_per_step": t * 1e3,
            "attn_ms": ta * 1e3, "store_ms": ts * 1e3,
-           "roofline": {"bound": "tensor", "achieved": flops / ta / 1e12, "peak": peaks["bf16_tflops"],
-                        "unit": "TFLOP/s", "frac": flops / ta / 1e12 / peaks["bf16_tflops"], "traffic": None},
+           "roofline": {"bound": "tensor", "kernel": "attn_prefill_kernel", "achieved": flops / tk / 1e12,
+                        "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                        "frac": flops / tk / 1e12 / peaks["bf16_tflops"], "kernel_ms": tk * 1e3, "traffic": None},
            "store_kvcache": {"value": sbytes / ts / 1e9, "unit": "GB/s", "frac": sbytes / ts / 1e9 / peaks["hbm_gbs"],
                              "tokens": int(cfg.new.sum())},
-           "launches_per_step": 2}
+           "launches_per_step": 4}
     del kc, vc
     torch.cuda.empty_cache()
     return res
@@ -346,13 +363,15 @@ def bench_long(av, device, steps, warmup, flush, peaks):
     import torch
     cfg = workloads.make("c5_long")
     inp = varlen_inputs(cfg, device)
-    ms, _ = bench_varlen(av, cfg, inp, steps, warmup, flush)
+    ms, _, kms = bench_varlen(av, cfg, inp, steps, warmup, flush)
     flops = workloads.prefill_flops(cfg.lens_q, cfg.lens_k, cfg.Hq, cfg.D)
     t = float(np.mean(ms)) / 1e3
+    tk = float(np.mean(kms)) / 1e3
     res = {"workload": "c5_long: 2 x 32768 tokens, MHA 32 heads, D128, heads 0-15 with Q x160 (logits ~700)",
            "value": flops / t / 1e12, "unit": "TFLOP/s", "ms_per_step": t * 1e3,
-           "roofline": {"bound": "tensor", "achieved": flops / t / 1e12, "peak": peaks["bf16_tflops_sustained"],
-                        "unit": "TFLOP/s", "frac": flops / t / 1e12 / peaks["bf16_tflops_sustained"],
+           "roofline": {"bound": "tensor", "kernel": "attn_prefill_kernel", "achieved": flops / tk / 1e12,
+                        "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
+                        "frac": flops / tk / 1e12 / peaks["bf16_tflops_sustained"], "kernel_ms": tk * 1e3,
                         "traffic": None}}
     del inp
     torch.cuda.empty_cache()
@@ -472,11 +491,12 @@ def main():
         cfg.seed += 1000 * rank
     inp = varlen_inputs(cfg, device)
     flops = workloads.prefill_flops(cfg.lens_q, cfg.lens_k, cfg.Hq, cfg.D)
-    ms, wall = bench_varlen(av, cfg, inp, args.steps, args.warmup, flush)
+    ms, wall, kms = bench_varlen(av, cfg, inp, args.steps, args.warmup, flush)
     ms_mean = float(np.mean(ms))
     ms_max = dist_max(ms_mean, device)
     value = aggregate(flops, ms_max / 1e3, world) / 1e12
-    achieved = flops / (ms_mean / 1e3) / 1e12
+    kernel_ms = float(np.mean(kms))
+    achieved = flops / (kernel_ms / 1e3) / 1e12
     e2e_ms, h2d, d2h = bench_varlen_e2e(av, cfg, inp, args.steps, args.warmup, flush)
     e2e_max = dist_max(float(np.mean(e2e_ms)), device)
 
@@ -497,14 +517,16 @@ def main():
                    "global_batch": 16 * world, "seq_len": "U{256..4096}", "total_tokens": int(cfg.lens_q.sum()),
                    "algorithmic_flops": flops, "l2": "flushed between timed steps (512 MB write)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
-        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                     "frac": achieved / peaks["bf16_tflops"],
+        "roofline": {"bound": "tensor", "kernel": "attn_prefill_kernel", "achieved": achieved,
+                     "peak": peaks["bf16_tflops"], "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
+                     "kernel_ms": kernel_ms,
                      "traffic": ncu_traffic("prefill", float(cfg.lens_q.sum())),
                      "peak_source": f"{peak_src} bf16 burst (MEASURED_PEAKS.json)" if peak_src == "measured"
                      else "fallback 1.9 PFLOP/s"},
         "e2e": {"value": aggregate(flops, e2e_max / 1e3, world) / 1e12, "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_max},
-        "gpu_launches": 2 * args.steps,   # per step: the V fp16 pre-pass and the attention kernel
+        # per step: the unit scheduler, the V fp16 pre-pass and the attention kernel
+        "gpu_launches": 3 * args.steps,
         "clocks": clocks,
         "wall_s_timed": wall,
         "device_status": status,

@@ -283,3 +283,26 @@ def test_v_beyond_fp16_range_is_reported():
     st, word = av.get_last_device_error()
     assert st == 8 and word & 4
     assert torch.isfinite(out.float()).all()
+
+
+def test_kernel_event_hook_times_the_attention_kernel_only():
+    """attn_set_kernel_events: the span recorded around the attention kernel is
+    positive and lies inside the span of the whole call."""
+    cfg = workloads.small_varlen(5, [300, 900, 17], [300, 900, 17], 8, 2, 128)
+    q, k, v = cfg.q().cuda(), cfg.k().cuda(), cfg.v().cuda()
+    run_contig(cfg, q, k, v)   # warm-up
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ka, kb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    av.set_kernel_events(ka, kb)
+    try:
+        a.record()
+        out, _ = run_contig(cfg, q, k, v)
+        b.record()
+    finally:
+        av.set_kernel_events()
+    torch.cuda.synchronize()
+    call_ms, kern_ms = a.elapsed_time(b), ka.elapsed_time(kb)
+    assert 0.0 < kern_ms <= call_ms
+    assert a.elapsed_time(ka) >= 0.0 and kb.elapsed_time(b) >= 0.0
+    with pytest.raises(ValueError):
+        av.set_kernel_events(ka, None)
