@@ -73,13 +73,10 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     return ok != 0;
 }
 
-// Bounded wait for the phase with the given parity to complete.  Returns true
-// on success.  Returns false if *abort became nonzero (another role gave up)
-// or if about kWaitLimitNs passed; in the latter case it records a timeout in
-// the error word and raises *abort so the other roles stop too.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort,
-                                          uint32_t *err, uint32_t src) {
-    if (mbar_try_wait(bar, parity)) return true;
+// Slow path of mbar_wait, kept out of line so that the common case (phase
+// already complete) costs one try_wait in the caller.
+static __device__ __noinline__ bool mbar_wait_slow(uint64_t *bar, uint32_t parity, volatile int *abort, uint32_t *err,
+                                            uint32_t src) {
     uint64_t t0 = globaltimer_ns();
     for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
@@ -92,6 +89,16 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volati
             }
         }
     }
+}
+
+// Bounded wait for the phase with the given parity to complete.  Returns true
+// on success.  Returns false if *abort became nonzero (another role gave up)
+// or if about kWaitLimitNs passed; in the latter case it records a timeout in
+// the error word and raises *abort so the other roles stop too.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort, uint32_t *err,
+                                          uint32_t src) {
+    if (mbar_try_wait(bar, parity)) return true;
+    return mbar_wait_slow(bar, parity, abort, err, src);
 }
 
 // ---------------------------------------------------------------------------
