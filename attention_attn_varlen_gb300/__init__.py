@@ -25,7 +25,7 @@ import torch
 from ._build import LIB as _LIB_PATH
 from ._build import build
 
-__all__ = ["attn_varlen_fwd", "attn_decode_paged", "store_kvcache", "get_last_device_error", "lib",
+__all__ = ["attn_varlen_fwd", "attn_decode_paged", "attn_with_kvcache", "store_kvcache", "get_last_device_error", "lib",
            "build", "AttnError", "exported_symbols", "set_kernel_events", "decode_num_splits", "decode_workspace_size"]
 
 ATTN_OK = 0
@@ -76,6 +76,11 @@ def lib():
     L.attn_get_last_device_error.restype = _i32
     L.attn_abi_version.argtypes = []
     L.attn_abi_version.restype = _i32
+    L.attn_kvcache_fwd.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _i32,
+                                   _i64, _i32, _f32, _i32, _vp, _sz, _vp]
+    L.attn_kvcache_fwd.restype = _i32
+    L.attn_kvcache_workspace_size.argtypes = [_i32, _i32, _i32, _i32, _i32, _i32]
+    L.attn_kvcache_workspace_size.restype = _sz
     L.attn_set_kernel_events.argtypes = [_vp, _vp]
     L.attn_set_kernel_events.restype = None
     _lib = L
@@ -234,6 +239,49 @@ def attn_decode_paged(q, k_cache, v_cache, cache_seqlens, block_table, softmax_s
                              int(max_cache_seqlen), scale, int(num_splits), q_stride, out_stride, _ptr(workspace),
                              ws_have, _stream(stream))
     _check(st, "attn_decode_paged")
+    return (out, lse) if return_lse else out
+
+
+def attn_with_kvcache(q, k_cache, v_cache, cache_seqlens, block_table, softmax_scale: float | None = None,
+                      causal: bool = True, max_cache_seqlen: int | None = None, out=None, lse=None,
+                      return_lse: bool = False, workspace=None, stream=None):
+    """Several new tokens per sequence against the paged cache: q [B, Sq, Hq, D]
+    (Sq >= 1, all sequences the same Sq); caches [num_blocks, block_size, Hkv, D];
+    cache_seqlens int32 [B] counts the cached keys including the Sq new ones.
+    Returns out [B, Sq, Hq, D] (and lse [Hq, B*Sq])."""
+    if q.dim() != 4:
+        raise ValueError("q must be [B, seqlen_q, Hq, D]")
+    _bf16_cuda(("q", q), ("k_cache", k_cache), ("v_cache", v_cache), ("out", out))
+    _int_cuda("cache_seqlens", cache_seqlens, torch.int32)
+    _int_cuda("block_table", block_table, torch.int32)
+    if k_cache.dim() != 4 or v_cache.shape != k_cache.shape or not k_cache.is_contiguous() \
+            or not v_cache.is_contiguous():
+        raise ValueError("caches must be contiguous [num_blocks, block_size, Hkv, D]")
+    if not q.is_contiguous():
+        raise ValueError("q must be contiguous")
+    B, Sq, Hq, D = q.shape
+    num_blocks, block_size, Hkv, _ = k_cache.shape
+    if cache_seqlens.numel() != B or block_table.dim() != 2 or block_table.shape[0] != B:
+        raise ValueError("cache_seqlens / block_table do not match the batch")
+    if out is None:
+        out = torch.empty((B, Sq, Hq, D), dtype=torch.bfloat16, device=q.device)
+    elif out.shape != q.shape or not out.is_contiguous():
+        raise ValueError("out must be a contiguous tensor shaped like q")
+    if return_lse and lse is None:
+        lse = torch.empty((Hq, B * Sq), dtype=torch.float32, device=q.device)
+    if max_cache_seqlen is None:
+        max_cache_seqlen = block_table.shape[1] * block_size
+    scale = 1.0 / math.sqrt(D) if softmax_scale is None else float(softmax_scale)
+    L = lib()
+    ws_bytes = L.attn_kvcache_workspace_size(B, Sq, Hq, Hkv, D, int(max_cache_seqlen))
+    if workspace is None:
+        workspace = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=q.device)
+    ws_have = workspace.numel() * workspace.element_size()
+    st = L.attn_kvcache_fwd(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(out), _ptr(lse), _ptr(cache_seqlens),
+                            _ptr(block_table), block_table.shape[1], B, Sq, Hq, Hkv, D, block_size, num_blocks,
+                            int(max_cache_seqlen), scale, 1 if causal else 0, _ptr(workspace), ws_have,
+                            _stream(stream))
+    _check(st, "attn_kvcache_fwd")
     return (out, lse) if return_lse else out
 
 

@@ -325,6 +325,51 @@ attn_status attn_varlen_fwd(const void *q, const void *k, const void *v, void *o
 }
 
 // ---------------------------------------------------------------------------
+// kv-cache entry: [cu_seqlens_q | cu_seqlens_k] (256-byte aligned), then the
+// varlen workspace for total_k = batch * max_cache_seqlen.
+static size_t kvcache_cu_bytes(int batch) { return ((size_t)2 * (batch + 1) * sizeof(int32_t) + 255) & ~(size_t)255; }
+
+size_t attn_kvcache_workspace_size(int batch, int seqlen_q, int num_heads_q, int num_heads_kv, int head_dim,
+                                   int max_cache_seqlen) {
+    if (batch <= 0 || seqlen_q <= 0 || max_cache_seqlen < 0) return 0;
+    const size_t v = attn_varlen_workspace_size(batch, num_heads_q, num_heads_kv, head_dim, seqlen_q,
+                                                (int64_t)batch * max_cache_seqlen);
+    return v ? kvcache_cu_bytes(batch) + v : 0;
+}
+
+attn_status attn_kvcache_fwd(const void *q, const void *k_cache, const void *v_cache, void *out, float *lse,
+                             const int32_t *cache_seqlens, const int32_t *block_table, int block_table_stride,
+                             int batch, int seqlen_q, int num_heads_q, int num_heads_kv, int head_dim,
+                             int block_size, int64_t num_blocks, int max_cache_seqlen, float softmax_scale,
+                             int causal, void *workspace, size_t workspace_bytes, void *stream) {
+    if (!q || !k_cache || !v_cache || !out || !cache_seqlens || !block_table) return ATTN_ERR_INVALID_ARG;
+    if (batch <= 0 || seqlen_q <= 0 || max_cache_seqlen < 0) return ATTN_ERR_INVALID_ARG;
+    if ((int64_t)batch * max_cache_seqlen >= (int64_t)INT32_MAX || (int64_t)batch * seqlen_q >= (int64_t)INT32_MAX)
+        return ATTN_ERR_UNSUPPORTED;
+    const size_t need = attn_kvcache_workspace_size(batch, seqlen_q, num_heads_q, num_heads_kv, head_dim,
+                                                    max_cache_seqlen);
+    if (need == 0) return ATTN_ERR_INVALID_ARG;
+    if (!workspace || workspace_bytes < need) return ATTN_ERR_WORKSPACE_TOO_SMALL;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return ATTN_ERR_INVALID_ARG;
+    DevInfo *d = nullptr;
+    attn_status st = dev_info(&d);
+    if (st != ATTN_OK) return st;
+    if ((st = check_arch(d)) != ATTN_OK) return st;
+    int32_t *cu_q = reinterpret_cast<int32_t *>(workspace);
+    int32_t *cu_k = cu_q + (batch + 1);
+    const size_t cu_b = kvcache_cu_bytes(batch);
+    if (launch_kvcache_cu(cache_seqlens, batch, seqlen_q, max_cache_seqlen, cu_q, cu_k, d->err,
+                          reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) {
+        cudaGetLastError();
+        return ATTN_ERR_LAUNCH_FAILED;
+    }
+    return attn_varlen_fwd(q, k_cache, v_cache, out, lse, cu_q, cu_k, batch, (int64_t)batch * seqlen_q,
+                           (int64_t)batch * max_cache_seqlen, seqlen_q, max_cache_seqlen, num_heads_q, num_heads_kv,
+                           head_dim, softmax_scale, causal, block_table, block_table_stride, block_size, num_blocks,
+                           0, 0, 0, 0, reinterpret_cast<uint8_t *>(workspace) + cu_b, workspace_bytes - cu_b, stream);
+}
+
+// ---------------------------------------------------------------------------
 int attn_decode_num_splits(int batch, int num_heads_kv, int max_cache_seqlen, int num_splits) {
     DevInfo *d = nullptr;
     int sms = 148;

@@ -67,6 +67,9 @@ constexpr int kPrefillKeyTile = 128;
 void main_kernel_event_before(cudaStream_t stream);
 void main_kernel_event_after(cudaStream_t stream);
 
+cudaError_t launch_kvcache_cu(const int32_t *cache_seqlens, int batch, int seqlen_q, int max_cache_seqlen,
+                              int32_t *cu_q, int32_t *cu_k, uint32_t *err, cudaStream_t stream);
+
 cudaError_t launch_prefill(const CUtensorMap &qmap, const CUtensorMap &kmap, const CUtensorMap &vmap,
                            const PrefillParams &p, int head_dim, cudaStream_t stream);
 

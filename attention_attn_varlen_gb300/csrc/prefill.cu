@@ -94,7 +94,11 @@ __device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint3
 // V -> V' = fp16(V / 16), laid out [total_k, Hkv, D] by logical key
 // (cu_seqlens_k[b] + j), read contiguously or through the block table.
 // One CTA per (32 keys, sequence).  |v| >= 2^20 (or non-finite) does not fit
-// and is clamped and reported.
+// and is clamped and reported.  The 128 rows after the last sequence's keys
+// are zeroed: the last key tile reads them (with zero weights), and with a
+// paged cache they lie inside the buffer (total_k is then an upper bound), so
+// stale contents there could be NaN.  Rows of a key whose block id is out of
+// range are zeroed too.
 // ---------------------------------------------------------------------------
 constexpr int kCvtThreads = 256;
 constexpr int kCvtKeys = 32;
@@ -104,6 +108,13 @@ __global__ void __launch_bounds__(kCvtThreads) attn_v_to_f16_kernel(const Prefil
     const int k0 = __ldg(p.cu_k + b), k1 = __ldg(p.cu_k + b + 1);
     const int Lk = k1 - k0;
     const int key0 = blockIdx.x * kCvtKeys;
+    const int row_chunks = p.Hkv * p.head_dim / 8;   // 16-byte chunks per key row
+    if (b == p.batch - 1 && blockIdx.x == 0) {
+        const int64_t t0 = __ldg(p.cu_k + p.batch);
+        const int64_t t1 = min(t0 + (int64_t)kPrefillKeyTile, p.total_k);
+        for (int64_t i = (t0 < 0 ? 0 : t0) * row_chunks + threadIdx.x; i < t1 * row_chunks; i += kCvtThreads)
+            reinterpret_cast<uint4 *>(p.v16)[i] = make_uint4(0u, 0u, 0u, 0u);
+    }
     if (blockIdx.x == gridDim.x - 1 && threadIdx.x == 0 && key0 + kCvtKeys < Lk)
         record_error(p.err, ERR_INDEX | SRC_PREFILL);   // longer than the stated max_seqlen_k
     if (Lk <= 0 || key0 >= Lk) return;
@@ -111,7 +122,6 @@ __global__ void __launch_bounds__(kCvtThreads) attn_v_to_f16_kernel(const Prefil
         if (threadIdx.x == 0 && blockIdx.x == 0) record_error(p.err, ERR_INDEX | SRC_PREFILL);
         return;
     }
-    const int row_chunks = p.Hkv * p.head_dim / 8;   // 16-byte chunks per key row
     const int nkeys = min(kCvtKeys, Lk - key0);
     const int32_t *bt = p.block_table ? p.block_table + (int64_t)b * p.bt_stride : nullptr;
     uint32_t big = 0;
@@ -123,6 +133,8 @@ __global__ void __launch_bounds__(kCvtThreads) attn_v_to_f16_kernel(const Prefil
             const int blk = __ldg(bt + key / p.block_size);
             if (blk < 0 || (int64_t)blk >= p.num_blocks) {
                 record_error(p.err, ERR_INDEX | SRC_PREFILL);
+                *reinterpret_cast<uint4 *>(p.v16 + ((int64_t)k0 + key) * (row_chunks * 8) + ch * 8) =
+                    make_uint4(0u, 0u, 0u, 0u);
                 continue;
             }
             src_row = (int64_t)blk * p.block_size + key % p.block_size;
@@ -546,6 +558,68 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         tc_fence_after();
         tmem_dealloc(tmem, 512);
     }
+}
+
+// ---------------------------------------------------------------------------
+// cu_seqlens for the kv-cache entry: cu_q[b] = b * seqlen_q, cu_k = exclusive
+// prefix sum of cache_seqlens (each clamped to [0, max_cache_seqlen]; a value
+// outside is reported).  One CTA.
+// ---------------------------------------------------------------------------
+constexpr int kCuThreads = 1024;
+
+__global__ void __launch_bounds__(kCuThreads)
+    attn_kvcache_cu_kernel(const int32_t *cache_seqlens, int batch, int seqlen_q, int max_cache_seqlen,
+                           int32_t *cu_q, int32_t *cu_k, uint32_t *err) {
+    __shared__ int wsum[kCuThreads / 32];
+    const int per = (batch + kCuThreads - 1) / kCuThreads;
+    const int b0 = threadIdx.x * per, b1 = min(b0 + per, batch);
+    int sum = 0;
+    for (int b = b0; b < b1; ++b) {
+        int v = cache_seqlens[b];
+        if (v < 0 || v > max_cache_seqlen) {
+            record_error(err, ERR_INDEX | SRC_PREFILL);
+            v = min(max(v, 0), max_cache_seqlen);
+        }
+        sum += v;
+    }
+    // exclusive scan of the per-thread sums
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    int incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+    }
+    if (lane == 31) wsum[wid] = incl;
+    __syncthreads();
+    if (wid == 0) {
+        const int w = wsum[lane];
+        int wi = w;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, wi, o);
+            if (lane >= o) wi += y;
+        }
+        wsum[lane] = wi - w;
+    }
+    __syncthreads();
+    int run = wsum[wid] + incl - sum;
+    for (int b = b0; b < b1; ++b) {
+        cu_k[b] = run;
+        cu_q[b] = b * seqlen_q;
+        run += min(max(cache_seqlens[b], 0), max_cache_seqlen);
+    }
+    if (threadIdx.x == kCuThreads - 1) {
+        cu_k[batch] = wsum[wid] + incl;
+        cu_q[batch] = batch * seqlen_q;
+    }
+}
+
+cudaError_t launch_kvcache_cu(const int32_t *cache_seqlens, int batch, int seqlen_q, int max_cache_seqlen,
+                              int32_t *cu_q, int32_t *cu_k, uint32_t *err, cudaStream_t stream) {
+    attn_kvcache_cu_kernel<<<1, kCuThreads, 0, stream>>>(cache_seqlens, batch, seqlen_q, max_cache_seqlen, cu_q,
+                                                         cu_k, err);
+    return cudaGetLastError();
 }
 
 template <int D>

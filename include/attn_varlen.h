@@ -208,6 +208,42 @@ ATTN_API attn_status store_kvcache(const void *k, const void *v, void *k_cache, 
                           int64_t num_slots, void *stream);
 
 /* ------------------------------------------------------------------------
+ * attn_kvcache_fwd -- several new query tokens per sequence against a paged
+ * KV cache ([A] "Decode": flash_attn_with_kvcache(q, k_cache, v_cache,
+ * cache_seqlens, block_table, softmax_scale, causal) with q of shape
+ * [B, seqlen_q, H, D] and seqlen_q >= 1: chunked append, speculative
+ * verification).  It computes cu_seqlens_q = b * seqlen_q and cu_seqlens_k =
+ * prefix sums of cache_seqlens on the device, then runs the paged varlen
+ * prefill (attn_varlen_fwd).  For seqlen_q = 1, attn_decode_paged is the fast
+ * path (split-KV); this entry is correct there too.
+ *
+ *   q, out       [batch * seqlen_q, num_heads_q, head_dim] bf16, packed
+ *                (the article's [B, seqlen_q, H, D])
+ *   lse          nullable; [num_heads_q, batch * seqlen_q] float32
+ *   cache_seqlens int32 [batch]: keys 0 .. cache_seqlens[b]-1 of sequence b,
+ *                including its seqlen_q new tokens (stored beforehand); values
+ *                outside [0, max_cache_seqlen] are clamped and reported as
+ *                ATTN_ERR_DEVICE_INDEX
+ *   causal       bottom-right: new token i sees keys j <= cache_seqlens[b] -
+ *                seqlen_q + i; 0 = every cached key
+ *   block_table, block_size, num_blocks: as for attn_varlen_fwd (paged mode)
+ *   workspace    at least attn_kvcache_workspace_size(...) bytes, 256-byte
+ *                aligned.  It holds the fp16 copy of V for batch *
+ *                max_cache_seqlen keys, so it grows with the cache length.
+ * Returns the statuses of attn_varlen_fwd.
+ * ------------------------------------------------------------------------ */
+ATTN_API attn_status attn_kvcache_fwd(const void *q, const void *k_cache, const void *v_cache, void *out,
+                                      float *lse, const int32_t *cache_seqlens, const int32_t *block_table,
+                                      int block_table_stride, int batch, int seqlen_q, int num_heads_q,
+                                      int num_heads_kv, int head_dim, int block_size, int64_t num_blocks,
+                                      int max_cache_seqlen, float softmax_scale, int causal, void *workspace,
+                                      size_t workspace_bytes, void *stream);
+
+/* Workspace bytes attn_kvcache_fwd needs (0 for invalid sizes). */
+ATTN_API size_t attn_kvcache_workspace_size(int batch, int seqlen_q, int num_heads_q, int num_heads_kv,
+                                            int head_dim, int max_cache_seqlen);
+
+/* ------------------------------------------------------------------------
  * Diagnostics
  * ------------------------------------------------------------------------ */
 

@@ -306,3 +306,24 @@ def test_kernel_event_hook_times_the_attention_kernel_only():
     assert a.elapsed_time(ka) >= 0.0 and kb.elapsed_time(b) >= 0.0
     with pytest.raises(ValueError):
         av.set_kernel_events(ka, None)
+
+
+def test_paged_prefill_ignores_stale_workspace():
+    """With a block table the fp16 V' buffer is sized by an upper bound of the
+    key count; a workspace full of NaN bit patterns must not reach the output."""
+    cfg = workloads.small_paged(35, ctx=[90, 700, 1], new=[64, 64, 64], Hq=16, Hkv=2, D=64, block_size=32)
+    q = cfg.q()
+    kc, vc, k_new, v_new = _paged_device(cfg)
+    B = cfg.batch
+    total_k = B * int(cfg.lens_k.max()) + 300
+    ws_bytes = av.lib().attn_varlen_workspace_size(B, cfg.Hq, cfg.Hkv, cfg.D, int(cfg.new.max()), total_k)
+    ws = torch.full((ws_bytes,), 0xFF, dtype=torch.uint8, device="cuda")
+    cu_q = torch.from_numpy(workloads.cu_from_lens(cfg.new)).cuda()
+    cu_k = torch.from_numpy(workloads.cu_from_lens(cfg.lens_k)).cuda()
+    av.get_last_device_error()
+    out = av.attn_varlen_fwd(q.cuda(), kc, vc, cu_q, cu_k, int(cfg.new.max()), int(cfg.lens_k.max()), cfg.scale,
+                             block_table=torch.from_numpy(cfg.block_table).cuda(), total_k=total_k, workspace=ws)
+    torch.cuda.synchronize()
+    assert av.get_last_device_error()[0] == 0
+    ref, _, _ = _paged_oracle(cfg, q, k_new, v_new, list(range(B)))
+    assert_close(out, ref.reshape(out.shape), "paged, stale workspace")
