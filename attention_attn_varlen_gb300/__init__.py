@@ -25,7 +25,7 @@ import torch
 from ._build import LIB as _LIB_PATH
 from ._build import build
 
-__all__ = ["attn_varlen_fwd", "attn_decode_paged", "attn_with_kvcache", "store_kvcache", "get_last_device_error", "lib",
+__all__ = ["attn_varlen_fwd", "attn_decode_paged", "attn_with_kvcache", "attn_padded_fwd", "store_kvcache", "get_last_device_error", "lib",
            "build", "AttnError", "exported_symbols", "set_kernel_events", "decode_num_splits", "decode_workspace_size"]
 
 ATTN_OK = 0
@@ -81,6 +81,11 @@ def lib():
     L.attn_kvcache_fwd.restype = _i32
     L.attn_kvcache_workspace_size.argtypes = [_i32, _i32, _i32, _i32, _i32, _i32]
     L.attn_kvcache_workspace_size.restype = _sz
+    L.attn_padded_fwd.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _f32, _i32,
+                                  _vp, _sz, _vp]
+    L.attn_padded_fwd.restype = _i32
+    L.attn_padded_workspace_size.argtypes = [_i32, _i32, _i32, _i32, _i32, _i32]
+    L.attn_padded_workspace_size.restype = _sz
     L.attn_set_kernel_events.argtypes = [_vp, _vp]
     L.attn_set_kernel_events.restype = None
     _lib = L
@@ -282,6 +287,46 @@ def attn_with_kvcache(q, k_cache, v_cache, cache_seqlens, block_table, softmax_s
                             int(max_cache_seqlen), scale, 1 if causal else 0, _ptr(workspace), ws_have,
                             _stream(stream))
     _check(st, "attn_kvcache_fwd")
+    return (out, lse) if return_lse else out
+
+
+def attn_padded_fwd(q, k, v, seqlens_q=None, seqlens_k=None, softmax_scale: float | None = None,
+                    causal: bool = True, out=None, lse=None, return_lse: bool = False, workspace=None,
+                    stream=None):
+    """Padded batch: q [B, Sq, Hq, D], k/v [B, Sk, Hkv, D] (contiguous); only the
+    first seqlens_q[b] / seqlens_k[b] rows of sequence b are real (int32 [B],
+    None = all).  Returns out [B, Sq, Hq, D] (padding rows are not written) and
+    lse [Hq, B*Sq] if asked."""
+    if q.dim() != 4 or k.dim() != 4 or v.shape != k.shape:
+        raise ValueError("q must be [B, Sq, Hq, D] and k, v [B, Sk, Hkv, D]")
+    _bf16_cuda(("q", q), ("k", k), ("v", v), ("out", out))
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    B, Sq, Hq, D = q.shape
+    _, Sk, Hkv, _ = k.shape
+    if k.shape[0] != B or k.shape[3] != D:
+        raise ValueError("k does not match q")
+    for name, t in (("seqlens_q", seqlens_q), ("seqlens_k", seqlens_k)):
+        if t is not None:
+            _int_cuda(name, t, torch.int32)
+            if t.numel() != B:
+                raise ValueError(f"{name} must have one entry per sequence")
+    if out is None:
+        out = torch.empty_like(q)
+    elif out.shape != q.shape or not out.is_contiguous():
+        raise ValueError("out must be a contiguous tensor shaped like q")
+    if return_lse and lse is None:
+        lse = torch.empty((Hq, B * Sq), dtype=torch.float32, device=q.device)
+    scale = 1.0 / math.sqrt(D) if softmax_scale is None else float(softmax_scale)
+    L = lib()
+    ws_bytes = L.attn_padded_workspace_size(B, Sq, Sk, Hq, Hkv, D)
+    if workspace is None:
+        workspace = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=q.device)
+    ws_have = workspace.numel() * workspace.element_size()
+    st = L.attn_padded_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(seqlens_q), _ptr(seqlens_k), B, Sq,
+                           Sk, Hq, Hkv, D, scale, 1 if causal else 0, _ptr(workspace), ws_have, _stream(stream))
+    _check(st, "attn_padded_fwd")
     return (out, lse) if return_lse else out
 
 

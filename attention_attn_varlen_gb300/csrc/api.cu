@@ -204,6 +204,9 @@ attn_status attn_get_last_device_error(void *stream, uint32_t *detail) {
 // (sequence, query pair, KV head)).
 static const size_t kWsHeader = 256;
 
+// derived cu_seqlens arrays at the head of a workspace (kv-cache and padded entries)
+static size_t kvcache_cu_bytes(int batch) { return ((size_t)2 * (batch + 1) * sizeof(int32_t) + 255) & ~(size_t)255; }
+
 static int64_t varlen_max_pairs(int num_heads_q, int num_heads_kv, int max_seqlen_q) {
     if (num_heads_kv <= 0 || num_heads_q <= 0 || num_heads_q % num_heads_kv || max_seqlen_q < 0) return -1;
     const int G = num_heads_q / num_heads_kv;
@@ -225,13 +228,17 @@ size_t attn_varlen_workspace_size(int batch, int num_heads_q, int num_heads_kv, 
            (size_t)batch * (size_t)mp * (size_t)num_heads_kv * sizeof(int2);
 }
 
-attn_status attn_varlen_fwd(const void *q, const void *k, const void *v, void *out, float *lse,
-                            const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k, int batch, int64_t total_q,
-                            int64_t total_k, int max_seqlen_q, int max_seqlen_k, int num_heads_q, int num_heads_kv,
-                            int head_dim, float softmax_scale, int causal, const int32_t *block_table,
-                            int block_table_stride, int block_size, int64_t num_blocks, int64_t q_row_stride,
-                            int64_t k_row_stride, int64_t v_row_stride, int64_t out_row_stride, void *workspace,
-                            size_t workspace_bytes, void *stream) {
+}  // extern "C"
+
+// attn_varlen_fwd with optional per-sequence used lengths (a padded batch)
+static attn_status varlen_impl(const void *q, const void *k, const void *v, void *out, float *lse,
+                               const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k, const int32_t *seqused_q,
+                               const int32_t *seqused_k, int batch, int64_t total_q, int64_t total_k,
+                               int max_seqlen_q, int max_seqlen_k, int num_heads_q, int num_heads_kv, int head_dim,
+                               float softmax_scale, int causal, const int32_t *block_table, int block_table_stride,
+                               int block_size, int64_t num_blocks, int64_t q_row_stride, int64_t k_row_stride,
+                               int64_t v_row_stride, int64_t out_row_stride, void *workspace, size_t workspace_bytes,
+                               void *stream) {
 
     if (!q || !k || !v || !out || !cu_seqlens_q || !cu_seqlens_k) return ATTN_ERR_INVALID_ARG;
     if (batch <= 0 || num_heads_q <= 0 || num_heads_kv <= 0 || num_heads_q % num_heads_kv != 0)
@@ -293,6 +300,8 @@ attn_status attn_varlen_fwd(const void *q, const void *k, const void *v, void *o
     p.lse = lse;
     p.cu_q = cu_seqlens_q;
     p.cu_k = cu_seqlens_k;
+    p.seqused_q = seqused_q;
+    p.seqused_k = seqused_k;
     p.block_table = block_table;
     p.total_q = total_q;
     p.total_k = total_k;
@@ -324,10 +333,65 @@ attn_status attn_varlen_fwd(const void *q, const void *k, const void *v, void *o
     return ATTN_OK;
 }
 
+extern "C" {
+
+attn_status attn_varlen_fwd(const void *q, const void *k, const void *v, void *out, float *lse,
+                            const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k, int batch, int64_t total_q,
+                            int64_t total_k, int max_seqlen_q, int max_seqlen_k, int num_heads_q, int num_heads_kv,
+                            int head_dim, float softmax_scale, int causal, const int32_t *block_table,
+                            int block_table_stride, int block_size, int64_t num_blocks, int64_t q_row_stride,
+                            int64_t k_row_stride, int64_t v_row_stride, int64_t out_row_stride, void *workspace,
+                            size_t workspace_bytes, void *stream) {
+    return varlen_impl(q, k, v, out, lse, cu_seqlens_q, cu_seqlens_k, nullptr, nullptr, batch, total_q, total_k,
+                       max_seqlen_q, max_seqlen_k, num_heads_q, num_heads_kv, head_dim, softmax_scale, causal,
+                       block_table, block_table_stride, block_size, num_blocks, q_row_stride, k_row_stride,
+                       v_row_stride, out_row_stride, workspace, workspace_bytes, stream);
+}
+
+// ---------------------------------------------------------------------------
+// padded batch: [cu_seqlens_q | cu_seqlens_k] (256-byte aligned), then the
+// varlen workspace for total_k = batch * seqlen_k.
+size_t attn_padded_workspace_size(int batch, int seqlen_q, int seqlen_k, int num_heads_q, int num_heads_kv,
+                                  int head_dim) {
+    if (batch <= 0 || seqlen_q <= 0 || seqlen_k < 0) return 0;
+    const size_t v = attn_varlen_workspace_size(batch, num_heads_q, num_heads_kv, head_dim, seqlen_q,
+                                                (int64_t)batch * seqlen_k);
+    return v ? kvcache_cu_bytes(batch) + v : 0;
+}
+
+attn_status attn_padded_fwd(const void *q, const void *k, const void *v, void *out, float *lse,
+                            const int32_t *seqlens_q, const int32_t *seqlens_k, int batch, int seqlen_q,
+                            int seqlen_k, int num_heads_q, int num_heads_kv, int head_dim, float softmax_scale,
+                            int causal, void *workspace, size_t workspace_bytes, void *stream) {
+    if (!q || !k || !v || !out) return ATTN_ERR_INVALID_ARG;
+    if (batch <= 0 || seqlen_q <= 0 || seqlen_k < 0) return ATTN_ERR_INVALID_ARG;
+    if ((int64_t)batch * seqlen_q >= (int64_t)INT32_MAX || (int64_t)batch * seqlen_k >= (int64_t)INT32_MAX)
+        return ATTN_ERR_UNSUPPORTED;
+    const size_t need = attn_padded_workspace_size(batch, seqlen_q, seqlen_k, num_heads_q, num_heads_kv, head_dim);
+    if (need == 0) return ATTN_ERR_INVALID_ARG;
+    if (!workspace || workspace_bytes < need) return ATTN_ERR_WORKSPACE_TOO_SMALL;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return ATTN_ERR_INVALID_ARG;
+    DevInfo *d = nullptr;
+    attn_status st = dev_info(&d);
+    if (st != ATTN_OK) return st;
+    if ((st = check_arch(d)) != ATTN_OK) return st;
+    int32_t *cu_q = reinterpret_cast<int32_t *>(workspace);
+    int32_t *cu_k = cu_q + (batch + 1);
+    const size_t cu_b = kvcache_cu_bytes(batch);
+    if (launch_padded_cu(batch, seqlen_q, seqlen_k, cu_q, cu_k, reinterpret_cast<cudaStream_t>(stream)) !=
+        cudaSuccess) {
+        cudaGetLastError();
+        return ATTN_ERR_LAUNCH_FAILED;
+    }
+    return varlen_impl(q, k, v, out, lse, cu_q, cu_k, seqlens_q, seqlens_k, batch, (int64_t)batch * seqlen_q,
+                       (int64_t)batch * seqlen_k, seqlen_q, seqlen_k, num_heads_q, num_heads_kv, head_dim,
+                       softmax_scale, causal, nullptr, 0, 0, 0, 0, 0, 0, 0, reinterpret_cast<uint8_t *>(workspace) + cu_b,
+                       workspace_bytes - cu_b, stream);
+}
+
 // ---------------------------------------------------------------------------
 // kv-cache entry: [cu_seqlens_q | cu_seqlens_k] (256-byte aligned), then the
 // varlen workspace for total_k = batch * max_cache_seqlen.
-static size_t kvcache_cu_bytes(int batch) { return ((size_t)2 * (batch + 1) * sizeof(int32_t) + 255) & ~(size_t)255; }
 
 size_t attn_kvcache_workspace_size(int batch, int seqlen_q, int num_heads_q, int num_heads_kv, int head_dim,
                                    int max_cache_seqlen) {

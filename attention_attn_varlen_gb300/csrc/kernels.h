@@ -33,6 +33,8 @@ struct PrefillParams {
     __nv_bfloat16 *out;          // [total_q, Hq, D], row stride out_row_stride
     float *lse;                  // [Hq, total_q] or null
     const int32_t *cu_q, *cu_k;
+    const int32_t *seqused_q;    // null, or [batch]: sequence b uses the first seqused_q[b] rows of its range
+    const int32_t *seqused_k;    // null, or [batch]: the same for its keys
     const int32_t *block_table;  // null: contiguous K/V
     int64_t total_q, total_k, out_row_stride, v_row_stride;
     int64_t num_blocks;
@@ -66,6 +68,9 @@ constexpr int kPrefillKeyTile = 128;
 // before and right after the main kernel of a call
 void main_kernel_event_before(cudaStream_t stream);
 void main_kernel_event_after(cudaStream_t stream);
+
+cudaError_t launch_padded_cu(int batch, int seqlen_q, int seqlen_k, int32_t *cu_q, int32_t *cu_k,
+                             cudaStream_t stream);
 
 cudaError_t launch_kvcache_cu(const int32_t *cache_seqlens, int batch, int seqlen_q, int max_cache_seqlen,
                               int32_t *cu_q, int32_t *cu_k, uint32_t *err, cudaStream_t stream);

@@ -91,37 +91,67 @@ __device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint3
 }
 
 // ---------------------------------------------------------------------------
+// Rows of sequence b: queries [qs, qs + Lq), keys [ks, ks + Lk) of the packed
+// tensors.  The range is cu_seqlens[b] .. cu_seqlens[b+1]; with seqused_q/k only
+// its first seqused[b] rows are the sequence (a padded batch).  False, and the
+// error word set when `report`, if the offsets are invalid; a used length
+// outside [0, range] is clamped (and reported).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ bool seq_rows(const PrefillParams &p, int b, bool report, int &qs, int &Lq, int &ks,
+                                         int &Lk) {
+    qs = __ldg(p.cu_q + b);
+    ks = __ldg(p.cu_k + b);
+    const int qe = __ldg(p.cu_q + b + 1), ke = __ldg(p.cu_k + b + 1);
+    if (qs < 0 || qe < qs || ks < 0 || ke < ks || (int64_t)qe > p.total_q || (int64_t)ke > p.total_k) {
+        if (report) record_error(p.err, ERR_INDEX | SRC_PREFILL);
+        return false;
+    }
+    Lq = qe - qs;
+    Lk = ke - ks;
+    if (p.seqused_q) {
+        const int u = __ldg(p.seqused_q + b);
+        if ((u < 0 || u > Lq) && report) record_error(p.err, ERR_INDEX | SRC_PREFILL);
+        Lq = min(max(u, 0), Lq);
+    }
+    if (p.seqused_k) {
+        const int u = __ldg(p.seqused_k + b);
+        if ((u < 0 || u > Lk) && report) record_error(p.err, ERR_INDEX | SRC_PREFILL);
+        Lk = min(max(u, 0), Lk);
+    }
+    return true;
+}
+
+// ---------------------------------------------------------------------------
 // V -> V' = fp16(V / 16), laid out [total_k, Hkv, D] by logical key
 // (cu_seqlens_k[b] + j), read contiguously or through the block table.
 // One CTA per (32 keys, sequence).  |v| >= 2^20 (or non-finite) does not fit
-// and is clamped and reported.  The 128 rows after the last sequence's keys
-// are zeroed: the last key tile reads them (with zero weights), and with a
-// paged cache they lie inside the buffer (total_k is then an upper bound), so
-// stale contents there could be NaN.  Rows of a key whose block id is out of
-// range are zeroed too.
+// and is clamped and reported.  Up to 128 rows after each sequence's keys are
+// zeroed (within its range; the last range runs to total_k): its last key tile
+// reads them with zero weights, and they may hold padding or, with a paged
+// cache (total_k an upper bound), stale workspace contents that could be NaN.
+// Rows of a key whose block id is out of range are zeroed too.
 // ---------------------------------------------------------------------------
 constexpr int kCvtThreads = 256;
 constexpr int kCvtKeys = 32;
 
 __global__ void __launch_bounds__(kCvtThreads) attn_v_to_f16_kernel(const PrefillParams p) {
     const int b = blockIdx.y;
-    const int k0 = __ldg(p.cu_k + b), k1 = __ldg(p.cu_k + b + 1);
-    const int Lk = k1 - k0;
+    int qs, Lq, k0, Lk;
+    if (!seq_rows(p, b, false, qs, Lq, k0, Lk)) return;   // reported by the scheduler
     const int key0 = blockIdx.x * kCvtKeys;
     const int row_chunks = p.Hkv * p.head_dim / 8;   // 16-byte chunks per key row
-    if (b == p.batch - 1 && blockIdx.x == 0) {
-        const int64_t t0 = __ldg(p.cu_k + p.batch);
-        const int64_t t1 = min(t0 + (int64_t)kPrefillKeyTile, p.total_k);
-        for (int64_t i = (t0 < 0 ? 0 : t0) * row_chunks + threadIdx.x; i < t1 * row_chunks; i += kCvtThreads)
+    if (blockIdx.x == 0) {
+        // rows after the sequence's keys up to one key tile, inside its range
+        // (the last sequence's range runs to total_k)
+        const int64_t t0 = (int64_t)k0 + Lk;
+        const int64_t lim = b == p.batch - 1 ? p.total_k : (int64_t)__ldg(p.cu_k + b + 1);
+        const int64_t t1 = min(t0 + (int64_t)kPrefillKeyTile, lim);
+        for (int64_t i = t0 * row_chunks + threadIdx.x; i < t1 * row_chunks; i += kCvtThreads)
             reinterpret_cast<uint4 *>(p.v16)[i] = make_uint4(0u, 0u, 0u, 0u);
     }
     if (blockIdx.x == gridDim.x - 1 && threadIdx.x == 0 && key0 + kCvtKeys < Lk)
         record_error(p.err, ERR_INDEX | SRC_PREFILL);   // longer than the stated max_seqlen_k
     if (Lk <= 0 || key0 >= Lk) return;
-    if (k0 < 0 || (int64_t)k1 > p.total_k) {
-        if (threadIdx.x == 0 && blockIdx.x == 0) record_error(p.err, ERR_INDEX | SRC_PREFILL);
-        return;
-    }
     const int nkeys = min(kCvtKeys, Lk - key0);
     const int32_t *bt = p.block_table ? p.block_table + (int64_t)b * p.bt_stride : nullptr;
     uint32_t big = 0;
@@ -169,13 +199,9 @@ constexpr int kSchedBuckets = 4096;
 
 __device__ __forceinline__ int pf_pairs(const PrefillParams &p, int b, bool report) {
     const int tps = BM / p.G;
-    const int qs = __ldg(p.cu_q + b), qe = __ldg(p.cu_q + b + 1);
-    const int ks0 = __ldg(p.cu_k + b), ke = __ldg(p.cu_k + b + 1);
-    if (qs < 0 || qe < qs || ke < ks0 || (int64_t)qe > p.total_q) {
-        if (report) record_error(p.err, ERR_INDEX | SRC_PREFILL);
-        return 0;
-    }
-    int pairs = (qe - qs + 2 * tps - 1) / (2 * tps);
+    int qs, Lq, ks, Lk;
+    if (!seq_rows(p, b, report, qs, Lq, ks, Lk)) return 0;
+    int pairs = (Lq + 2 * tps - 1) / (2 * tps);
     if (pairs > p.max_pairs) {   // longer than the stated max_seqlen_q
         if (report) record_error(p.err, ERR_INDEX | SRC_PREFILL);
         pairs = p.max_pairs;
@@ -264,10 +290,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     const int b = unit.x, pair = unit.y & 0xFFFF, hkv = unit.y >> 16;
     const int G = p.G, tps = BM / G;
 
-    const int qs = __ldg(p.cu_q + b), qe = __ldg(p.cu_q + b + 1);
-    const int ks0 = __ldg(p.cu_k + b), ke = __ldg(p.cu_k + b + 1);
-    const int Lq = qe - qs, Lk = ke - ks0;
-    if (qs < 0 || Lq < 0 || Lk < 0 || (int64_t)qe > p.total_q) return;   // reported by the scheduler
+    int qs, Lq, ks0, Lk;
+    if (!seq_rows(p, b, false, qs, Lq, ks0, Lk)) return;   // reported by the scheduler
     const int t0A = pair * 2 * tps;
     if (t0A >= Lq) return;
     const int t0B = t0A + tps;
@@ -613,6 +637,20 @@ __global__ void __launch_bounds__(kCuThreads)
         cu_k[batch] = wsum[wid] + incl;
         cu_q[batch] = batch * seqlen_q;
     }
+}
+
+// cu_seqlens of a padded batch: sequence b owns rows [b * seqlen, (b + 1) * seqlen)
+__global__ void attn_padded_cu_kernel(int batch, int seqlen_q, int seqlen_k, int32_t *cu_q, int32_t *cu_k) {
+    for (int b = blockIdx.x * blockDim.x + threadIdx.x; b <= batch; b += gridDim.x * blockDim.x) {
+        cu_q[b] = b * seqlen_q;
+        cu_k[b] = b * seqlen_k;
+    }
+}
+
+cudaError_t launch_padded_cu(int batch, int seqlen_q, int seqlen_k, int32_t *cu_q, int32_t *cu_k,
+                             cudaStream_t stream) {
+    attn_padded_cu_kernel<<<(batch + 256) / 256, 256, 0, stream>>>(batch, seqlen_q, seqlen_k, cu_q, cu_k);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_kvcache_cu(const int32_t *cache_seqlens, int batch, int seqlen_q, int max_cache_seqlen,

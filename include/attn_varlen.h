@@ -208,6 +208,36 @@ ATTN_API attn_status store_kvcache(const void *k, const void *v, void *k_cache, 
                           int64_t num_slots, void *stream);
 
 /* ------------------------------------------------------------------------
+ * attn_padded_fwd -- prefill of a padded batch: every sequence occupies a
+ * fixed number of rows and only its first seqlens[b] rows are real (the layout
+ * the article contrasts with varlen packing, section "Prefill": padding plus a
+ * mask instead of cu_seqlens).  Same attention as attn_varlen_fwd; the padding
+ * rows are never read as keys or values that count, whatever they hold.
+ *
+ *   q, out       [batch, seqlen_q, num_heads_q, head_dim] bf16, packed
+ *   k, v         [batch, seqlen_k, num_heads_kv, head_dim] bf16, packed
+ *   lse          nullable; [num_heads_q, batch * seqlen_q] float32
+ *   seqlens_q    nullable int32 [batch]: real query rows of sequence b
+ *                (NULL: all seqlen_q); seqlens_k likewise for the keys.  Values
+ *                outside [0, seqlen] are clamped and reported as
+ *                ATTN_ERR_DEVICE_INDEX.
+ *   causal       bottom-right on the real lengths (query i sees keys
+ *                j <= seqlens_k[b] - seqlens_q[b] + i)
+ *   workspace    at least attn_padded_workspace_size(...) bytes, 256-byte aligned
+ * Output rows and lse entries of padding rows are left as they were.
+ * Returns the statuses of attn_varlen_fwd.
+ * ------------------------------------------------------------------------ */
+ATTN_API attn_status attn_padded_fwd(const void *q, const void *k, const void *v, void *out, float *lse,
+                                     const int32_t *seqlens_q, const int32_t *seqlens_k, int batch, int seqlen_q,
+                                     int seqlen_k, int num_heads_q, int num_heads_kv, int head_dim,
+                                     float softmax_scale, int causal, void *workspace, size_t workspace_bytes,
+                                     void *stream);
+
+/* Workspace bytes attn_padded_fwd needs (0 for invalid sizes). */
+ATTN_API size_t attn_padded_workspace_size(int batch, int seqlen_q, int seqlen_k, int num_heads_q,
+                                           int num_heads_kv, int head_dim);
+
+/* ------------------------------------------------------------------------
  * attn_kvcache_fwd -- several new query tokens per sequence against a paged
  * KV cache ([A] "Decode": flash_attn_with_kvcache(q, k_cache, v_cache,
  * cache_seqlens, block_table, softmax_scale, causal) with q of shape
