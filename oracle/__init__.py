@@ -62,6 +62,7 @@ def _load():
         lib.oracle_softmax_naive_f64.argtypes = [_f64p, ctypes.c_int, _f64p]
         lib.oracle_softmax_safe.argtypes = [_f64p, ctypes.c_int, _f64p]
         lib.oracle_softmax_online.argtypes = [_f64p, ctypes.c_int, _f64p, _f64p, _f64p]
+        lib.oracle_softmax_rows.argtypes = [_f64p, ctypes.c_int64, ctypes.c_int, _f64p, ctypes.c_int]
         lib.oracle_attn_tiled_row.argtypes = [_f64p, _f64p, _f64p, _u8p, ctypes.c_int, ctypes.c_int,
                                               ctypes.c_double, ctypes.c_int, _f64p, _f64p, _f64p]
         lib.oracle_attn_varlen.argtypes = [
@@ -146,6 +147,19 @@ def softmax_online(x):
     dt = np.empty_like(xa)
     lib.oracle_softmax_online(_ptr(xa, _f64p), xa.size, _ptr(y, _f64p), _ptr(mt, _f64p), _ptr(dt, _f64p))
     return y, mt, dt
+
+
+def softmax_rows(x, nthreads: int = 0) -> np.ndarray:
+    """Safe softmax of every row of a 2-D array (float64 result).  Accepts
+    float32 / float64 arrays and torch tensors (bf16 included, upcast exactly)."""
+    if hasattr(x, "detach"):
+        x = x.detach().cpu().float().numpy()
+    xa = np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+    if xa.ndim != 2:
+        raise ValueError("softmax_rows takes a 2-D array")
+    y = np.empty_like(xa)
+    _load().oracle_softmax_rows(_ptr(xa, _f64p), xa.shape[0], xa.shape[1], _ptr(y, _f64p), int(nthreads))
+    return y
 
 
 def attn_tiled_row(q, K, V, scale: float, block: int, visible=None):

@@ -20,6 +20,8 @@
  *   oracle_softmax_safe           -- 3-pass safe softmax (same section)
  *   oracle_softmax_online         -- 2-pass online softmax with the d' recurrence
  *                                    (section 减少遍历次数的"在线 Softmax")
+ *   oracle_softmax_rows           -- the safe softmax of every row of a matrix
+ *                                    (section "安全 Softmax"), OpenMP over rows
  *   oracle_attn_tiled_row         -- 1-pass m, d', o' recurrence over key blocks
  *                                    (sections "FlashAttention 的最终实现" and
  *                                    "计算流程（1-Pass 算法与分块）")
@@ -94,6 +96,15 @@ void oracle_softmax_safe(const double *x, int n, double *y)
     double d = 0.0;
     for (int i = 0; i < n; ++i) d += exp(x[i] - m);               /* pass 2 */
     for (int i = 0; i < n; ++i) y[i] = exp(x[i] - m) / d;         /* pass 3 */
+}
+
+/* Row-wise softmax of a [rows, cols] matrix (row stride cols): every row
+ * goes through oracle_softmax_safe, the plain definition. */
+void oracle_softmax_rows(const double *x, int64_t rows, int cols, double *y, int nthreads)
+{
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#pragma omp parallel for schedule(dynamic, 16)
+    for (int64_t r = 0; r < rows; ++r) oracle_softmax_safe(x + r * (int64_t)cols, cols, y + r * (int64_t)cols);
 }
 
 /* Online softmax, two passes.  Pass 1 runs the running maximum

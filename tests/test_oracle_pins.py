@@ -396,3 +396,18 @@ def test_empty_and_no_visible_rows():
     out, lse = oracle.attn_varlen(q, k, k, [0, 2, 3], [0, 0, 1], 1, 1, 4, 1.0, True)
     assert np.all(out[:2] == 0) and np.all(np.isneginf(lse[:2]))
     np.testing.assert_array_equal(out[2], 1.0)
+
+
+def test_softmax_rows_pins():
+    """oracle.softmax_rows: every row equals scipy's softmax, sums to 1, and the
+    overflow row [700, 710, 705] keeps its closed form."""
+    from scipy.special import softmax as sp_softmax
+    rng = np.random.default_rng(5)
+    x = rng.normal(size=(37, 301)) * 30.0
+    x[3] = -1e3
+    y = oracle.softmax_rows(x)
+    np.testing.assert_allclose(y, sp_softmax(x, axis=1), rtol=1e-12, atol=1e-300)
+    np.testing.assert_allclose(y.sum(axis=1), 1.0, rtol=1e-12)
+    z = oracle.softmax_rows(np.array([[700.0, 710.0, 705.0]]))[0]
+    e = np.exp(np.array([-10.0, 0.0, -5.0]))
+    np.testing.assert_allclose(z, e / e.sum(), rtol=1e-14)
