@@ -25,7 +25,7 @@ import torch
 from ._build import LIB as _LIB_PATH
 from ._build import build
 
-__all__ = ["attn_varlen_fwd", "attn_decode_paged", "attn_with_kvcache", "attn_padded_fwd", "store_kvcache", "get_last_device_error", "lib",
+__all__ = ["attn_varlen_fwd", "attn_decode_paged", "attn_with_kvcache", "attn_padded_fwd", "softmax_rows", "store_kvcache", "get_last_device_error", "lib",
            "build", "AttnError", "exported_symbols", "set_kernel_events", "decode_num_splits", "decode_workspace_size"]
 
 ATTN_OK = 0
@@ -86,6 +86,8 @@ def lib():
     L.attn_padded_fwd.restype = _i32
     L.attn_padded_workspace_size.argtypes = [_i32, _i32, _i32, _i32, _i32, _i32]
     L.attn_padded_workspace_size.restype = _sz
+    L.attn_softmax_rows.argtypes = [_vp, _vp, _i64, _i32, _i64, _i64, _i32, _vp]
+    L.attn_softmax_rows.restype = _i32
     L.attn_set_kernel_events.argtypes = [_vp, _vp]
     L.attn_set_kernel_events.restype = None
     _lib = L
@@ -328,6 +330,30 @@ def attn_padded_fwd(q, k, v, seqlens_q=None, seqlens_k=None, softmax_scale: floa
                            Sk, Hq, Hkv, D, scale, 1 if causal else 0, _ptr(workspace), ws_have, _stream(stream))
     _check(st, "attn_padded_fwd")
     return (out, lse) if return_lse else out
+
+
+def softmax_rows(x, out=None, stream=None):
+    """Softmax along the last dimension of a float32 or bfloat16 CUDA tensor
+    (any leading shape; rows may be strided, the last dimension contiguous).
+    out: same shape and dtype (may be x)."""
+    if not x.is_cuda or x.dtype not in (torch.float32, torch.bfloat16):
+        raise ValueError("x must be a float32 or bfloat16 CUDA tensor")
+    if x.dim() == 0 or x.stride(-1) != 1:
+        raise ValueError("the last dimension of x must be contiguous")
+    cols = x.shape[-1]
+    x2 = x.reshape(-1, cols) if x.dim() != 2 else x
+    if out is None:
+        out = torch.empty_like(x, memory_format=torch.contiguous_format)
+    if out.shape != x.shape or out.dtype != x.dtype or out.stride(-1) != 1:
+        raise ValueError("out must match x in shape and dtype")
+    o2 = out.reshape(-1, cols) if out.dim() != 2 else out
+    if o2.data_ptr() != out.data_ptr() or x2.data_ptr() != x.data_ptr():
+        raise ValueError("x and out must be viewable as [rows, cols]")
+    dtype = 1 if x.dtype == torch.bfloat16 else 0
+    st = lib().attn_softmax_rows(_ptr(x2), _ptr(o2), x2.shape[0], cols, x2.stride(0) if x2.shape[0] > 1 else cols,
+                                 o2.stride(0) if o2.shape[0] > 1 else cols, dtype, _stream(stream))
+    _check(st, "attn_softmax_rows")
+    return out
 
 
 def store_kvcache(k, v, k_cache, v_cache, slot_mapping, stream=None):

@@ -434,6 +434,28 @@ attn_status attn_kvcache_fwd(const void *q, const void *k_cache, const void *v_c
 }
 
 // ---------------------------------------------------------------------------
+attn_status attn_softmax_rows(const void *x, void *y, int64_t rows, int cols, int64_t x_row_stride,
+                              int64_t y_row_stride, int dtype, void *stream) {
+    if (!x || !y || rows < 0 || cols < 0 || (dtype != ATTN_DTYPE_F32 && dtype != ATTN_DTYPE_BF16))
+        return ATTN_ERR_INVALID_ARG;
+    // any stride that covers a row (the kernels use 16-byte accesses only where rows allow it)
+    if (x_row_stride == 0) x_row_stride = cols;
+    if (y_row_stride == 0) y_row_stride = cols;
+    if (x_row_stride < cols || y_row_stride < cols) return ATTN_ERR_INVALID_ARG;
+    DevInfo *d = nullptr;
+    attn_status st = dev_info(&d);
+    if (st != ATTN_OK) return st;
+    if ((st = check_arch(d)) != ATTN_OK) return st;
+    if (rows == 0 || cols == 0) return ATTN_OK;
+    if (launch_softmax_rows(x, y, rows, cols, x_row_stride, y_row_stride, dtype == ATTN_DTYPE_BF16 ? 1 : 0,
+                            d->num_sms, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) {
+        cudaGetLastError();
+        return ATTN_ERR_LAUNCH_FAILED;
+    }
+    return ATTN_OK;
+}
+
+// ---------------------------------------------------------------------------
 int attn_decode_num_splits(int batch, int num_heads_kv, int max_cache_seqlen, int num_splits) {
     DevInfo *d = nullptr;
     int sms = 148;

@@ -359,6 +359,38 @@ def bench_prefix(av, device, steps, warmup, flush, peaks):
     return res
 
 
+def bench_softmax(av, device, steps, warmup, flush, peaks):
+    """Row softmax (online two-pass kernel): algorithmic bytes = one read and one
+    write of the matrix."""
+    import torch
+    res = {}
+    for name, rows, cols, dt in (("f32_32768x8192", 32768, 8192, torch.float32),
+                                 ("bf16_262144x1024", 262144, 1024, torch.bfloat16)):
+        g = torch.Generator(device=device).manual_seed(1234 + rows)
+        x = (torch.randn(rows, cols, device=device, generator=g) * 30.0).to(dt)
+        y = torch.empty_like(x)
+
+        def step():
+            av.softmax_rows(x, out=y)
+        for _ in range(warmup):
+            step()
+        torch.cuda.synchronize()
+        ms = time_steps(step, steps, flush)
+        t = float(np.mean(ms)) / 1e3
+        nbytes = 2 * x.numel() * x.element_size()
+        gbs = nbytes / t / 1e9
+        res[name] = {"value": gbs, "unit": "GB/s", "ms_per_step": t * 1e3, "algorithmic_bytes": nbytes,
+                     "roofline": {"bound": "hbm", "kernel": "softmax_rows_%s_kernel" % ("cta" if cols > 2048 else "warp"),
+                                  "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                                  "frac": gbs / peaks["hbm_gbs"], "traffic": None},
+                     "launches_per_step": 1}
+        del x, y
+    torch.cuda.empty_cache()
+    res["workload"] = ("row softmax, N(0, 30^2) logits: fp32 32768 x 8192 (two passes per row, the second from "
+                       "L2) and bf16 262144 x 1024 (one read, row in registers)")
+    return res
+
+
 def bench_long(av, device, steps, warmup, flush, peaks):
     import torch
     cfg = workloads.make("c5_long")
@@ -505,6 +537,7 @@ def main():
         extras["decode"] = bench_decode(av, device, args.steps, args.warmup, flush, peaks)
         extras["prefix_prefill"] = bench_prefix(av, device, args.steps, args.warmup, flush, peaks)
         extras["long_prefill"] = bench_long(av, device, max(3, args.steps // 3), args.warmup, flush, peaks)
+        extras["row_softmax"] = bench_softmax(av, device, args.steps, args.warmup, flush, peaks)
     clocks = sampler.stop()
 
     status, word = av.get_last_device_error()

@@ -274,6 +274,27 @@ ATTN_API size_t attn_kvcache_workspace_size(int batch, int seqlen_q, int num_hea
                                             int head_dim, int max_cache_seqlen);
 
 /* ------------------------------------------------------------------------
+ * attn_softmax_rows -- y = softmax(x) along every row of a matrix, with the
+ * online two-pass algorithm of the article's section 减少遍历次数的“在线
+ * Softmax”: pass 1 runs the maximum m and the proxy denominator
+ * d' = d' * e^(m_old - m_new) + e^(x - m_new) in one sweep, pass 2 writes
+ * e^(x - m) / d'.  Arithmetic in fp32; no overflow for any finite input.
+ *
+ *   x, y          [rows, cols], row strides x_row_stride / y_row_stride in
+ *                 elements (0 = cols); y may be x (in place)
+ *   dtype         ATTN_DTYPE_F32 (x and y float32) or ATTN_DTYPE_BF16 (x and
+ *                 y bfloat16, y rounded to nearest even)
+ * A row whose maximum is not finite (all -inf, or a +inf or NaN in it) gives
+ * NaN, as the definition does.  HBM-bound: one read and one write of the
+ * matrix for rows up to 2048 (fp32) / 4096 (bf16) elements; longer rows are
+ * read twice, the second time mostly from L2.
+ * ------------------------------------------------------------------------ */
+enum { ATTN_DTYPE_F32 = 0, ATTN_DTYPE_BF16 = 1 };
+
+ATTN_API attn_status attn_softmax_rows(const void *x, void *y, int64_t rows, int cols, int64_t x_row_stride,
+                                       int64_t y_row_stride, int dtype, void *stream);
+
+/* ------------------------------------------------------------------------
  * Diagnostics
  * ------------------------------------------------------------------------ */
 

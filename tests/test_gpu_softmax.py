@@ -1,0 +1,71 @@
+"""Row softmax (online two-pass kernel) on the GPU against the float64 oracle."""
+import numpy as np
+import pytest
+import torch
+
+import attention_attn_varlen_gb300 as av
+import oracle
+
+pytestmark = pytest.mark.gpu
+
+SHAPES = [(1, 1), (3, 7), (33, 31), (64, 128), (17, 1000), (8, 2048), (5, 2049), (9, 4096), (4, 4097),
+          (2, 100003), (700, 512)]
+
+
+def _inputs(seed, rows, cols, scale=30.0):
+    rng = np.random.default_rng(seed)
+    x = (rng.standard_normal((rows, cols)) * scale).astype(np.float32)
+    if rows > 1 and cols >= 3:
+        x[1, :3] = [700.0, 710.0, 705.0]   # large logits: no overflow with the running max
+    return x
+
+
+def _check(y, ref, bf16):
+    y = y.float().cpu().double().numpy()
+    assert np.all(np.isfinite(y))
+    rel = 2.0 ** -8 + 1e-4 if bf16 else 1e-4
+    err = np.abs(y - ref)
+    bad = err > rel * np.abs(ref) + 1e-7
+    assert not bad.any(), f"max err {err.max():.3e} at {np.argwhere(bad)[0]}"
+    np.testing.assert_allclose(y.sum(axis=1), 1.0, rtol=(2e-2 if bf16 else 1e-4))
+
+
+@pytest.mark.parametrize("rows,cols", SHAPES)
+@pytest.mark.parametrize("bf16", [False, True])
+def test_softmax_rows_matches_oracle(rows, cols, bf16):
+    x = torch.from_numpy(_inputs(rows * 7 + cols, rows, cols))
+    if bf16:
+        x = x.to(torch.bfloat16)
+    ref = oracle.softmax_rows(x)
+    y = av.softmax_rows(x.cuda())
+    torch.cuda.synchronize()
+    _check(y, ref, bf16)
+
+
+def test_softmax_rows_strided_inplace_and_unaligned():
+    x = torch.from_numpy(_inputs(91, 40, 3001))
+    wide = torch.zeros(40, 3100, dtype=torch.float32)
+    wide[:, :3001] = x
+    wide = wide.cuda()
+    view = wide[:, :3001]                      # row stride 3100
+    ref = oracle.softmax_rows(x)
+    y = av.softmax_rows(view)
+    _check(y, ref, False)
+    av.softmax_rows(view, out=view)            # in place
+    _check(view, ref, False)
+    assert torch.equal(wide[:, 3001:], torch.zeros(40, 99, device="cuda"))
+    # a view that starts 4 bytes past a 16-byte boundary (element accesses)
+    buf = torch.zeros(40 * 301 + 1, dtype=torch.float32, device="cuda")
+    xu = buf[1:].view(40, 301)
+    x2 = torch.from_numpy(_inputs(92, 40, 301))
+    xu.copy_(x2.cuda())
+    _check(av.softmax_rows(xu), oracle.softmax_rows(x2), False)
+
+
+def test_softmax_rows_online_recurrence_on_the_article_example():
+    """[10, 0, 8, 12, 5]: the kernel's result equals the online recurrence's."""
+    x = torch.tensor([[10.0, 0.0, 8.0, 12.0, 5.0]])
+    y = av.softmax_rows(x.cuda()).cpu().double().numpy()[0]
+    ref, m_trace, _ = oracle.softmax_online(x.numpy()[0])
+    np.testing.assert_allclose(y, ref, rtol=1e-5)
+    assert m_trace[-1] == 12.0
