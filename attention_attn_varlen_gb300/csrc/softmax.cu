@@ -7,8 +7,8 @@
 // elements.  Partial (m, d') states of threads merge exactly:
 //   m = max(m1, m2),  d' = d1 e^(m1 - m) + d2 e^(m2 - m).
 //
-// HBM-bound.  Rows of up to 2048 elements: one warp per row, the row held in
-// registers (one read, one write).  Longer rows: one CTA per row; pass 2
+// HBM-bound.  Rows of up to 1024 fp32 / 2048 bf16 elements: one warp per row,
+// the row held in registers (one read, one write).  Longer rows: one CTA per row; pass 2
 // re-reads the row, which the CTAs in flight keep in L2.
 #include "common.cuh"
 #include "kernels.h"
@@ -257,14 +257,14 @@ template <typename T, bool VEC>
 cudaError_t launch_t(const T *x, T *y, int64_t rows, int cols, int64_t xs, int64_t ys, int sms,
                      cudaStream_t stream) {
     constexpr int N = VEC ? Vec<T>::N : 1;
-    // a warp per row while the row fits in 16 accesses per lane (2048 fp32 or
-    // 4096 bf16 elements with 16-byte accesses, 512 elements otherwise)
+    // a warp per row while the row fits in 8 accesses per lane (1024 fp32 or
+    // 2048 bf16 elements with 16-byte accesses, 256 elements otherwise); longer
+    // rows hold too many registers for enough warps per SM
     const int per_lane = (cols + 32 * N - 1) / (32 * N);
     if (per_lane <= 1) return launch_warp<T, 1, VEC>(x, y, rows, cols, xs, ys, sms, stream);
     if (per_lane <= 2) return launch_warp<T, 2, VEC>(x, y, rows, cols, xs, ys, sms, stream);
     if (per_lane <= 4) return launch_warp<T, 4, VEC>(x, y, rows, cols, xs, ys, sms, stream);
     if (per_lane <= 8) return launch_warp<T, 8, VEC>(x, y, rows, cols, xs, ys, sms, stream);
-    if (per_lane <= 16) return launch_warp<T, 16, VEC>(x, y, rows, cols, xs, ys, sms, stream);
     const int grid = (int)(rows < (int64_t)sms * 4 ? rows : (int64_t)sms * 4);
     softmax_rows_cta_kernel<T, VEC><<<grid, kRowThreads, 0, stream>>>(x, y, rows, cols, xs, ys);
     return cudaGetLastError();

@@ -286,7 +286,7 @@ ATTN_API size_t attn_kvcache_workspace_size(int batch, int seqlen_q, int num_hea
  *                 y bfloat16, y rounded to nearest even)
  * A row whose maximum is not finite (all -inf, or a +inf or NaN in it) gives
  * NaN, as the definition does.  HBM-bound: one read and one write of the
- * matrix for rows up to 2048 (fp32) / 4096 (bf16) elements; longer rows are
+ * matrix for rows up to 1024 (fp32) / 2048 (bf16) elements; longer rows are
  * read twice, the second time mostly from L2.
  * ------------------------------------------------------------------------ */
 enum { ATTN_DTYPE_F32 = 0, ATTN_DTYPE_BF16 = 1 };
