@@ -320,7 +320,9 @@ static attn_status varlen_impl(const void *q, const void *k, const void *v, void
     p.G = G;
     p.causal = causal ? 1 : 0;
     p.max_pairs = (int)max_pairs;
-    p.num_ctas = (int)((int64_t)batch * max_pairs * num_heads_kv);
+    // persistent CTAs: one per SM (fewer when there are fewer possible units)
+    const int64_t max_units = (int64_t)batch * max_pairs * num_heads_kv;
+    p.num_ctas = (int)(max_units < d->num_sms ? max_units : d->num_sms);
     p.unit_count = reinterpret_cast<int *>(ws);
     p.units = reinterpret_cast<int2 *>(ws + kWsHeader + v16_bytes(num_heads_kv, head_dim, total_k));
     p.scale_log2 = softmax_scale * 1.4426950408889634f;

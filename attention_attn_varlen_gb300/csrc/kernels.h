@@ -41,7 +41,7 @@ struct PrefillParams {
     int bt_stride, block_size, rows_per_box;
     int batch, Hq, Hkv, G, causal, head_dim, max_seqlen_k;
     int max_pairs;               // slot pairs per sequence at max_seqlen_q
-    int num_ctas;                // grid size: the largest possible number of units
+    int num_ctas;                // grid size: persistent CTAs (one per SM, at most the possible units)
     int2 *units;                 // workspace: (sequence, pair | kv_head << 16), scheduled order
     int *unit_count;             // workspace: [0] number of units
     float scale_log2;            // softmax_scale * log2(e), > 0

@@ -13,8 +13,9 @@
 //   * causal masking is bottom-right aligned: query i of a sequence with Lq
 //     queries and Lk keys sees keys j <= Lk - Lq + i.
 //
-// Work unit (one CTA, taken from the scheduler's list): a sequence b, a KV
-// head, and two query "slots" A and B
+// Work unit (taken from the scheduler's list; persistent CTAs, one per SM,
+// take the next entry from a global counter when they start a unit): a
+// sequence b, a KV head, and two query "slots" A and B
 // of 128 rows each.  A slot packs 128/G consecutive tokens x the G query heads
 // that share the KV head (row r = token_offset * G + g), so one K/V stream
 // feeds 256 query rows.  Slot B holds the 128/G tokens after slot A.
@@ -42,6 +43,17 @@
 // S_X(j) also covers PV_X(j-1): a softmax thread that sees S_X(j) may rescale
 // O_X safely.
 //
+// Persistence: barriers and TMEM are set up once per CTA and the ring, S and P
+// barrier phases run on across units.  The producer warp takes unit indices
+// (atomicAdd) and hands them to the other roles through a two-entry ring in
+// shared memory.  The producer loads the next unit's Q as
+// soon as the current unit's last QK^T has read Q (q_empty), and K/V tiles of
+// the next unit as ring slots free up, so the tensor core starts the next unit
+// while the softmax warps store the current one's output.  The first PV_X of a
+// unit waits until the epilogue of slot X has read O_X (o_empty).  MMA and
+// softmax commit / wait o_full and o_empty once per unit, which keeps their
+// phases in step.
+//
 // The rescale is lazy: the reference max of a row moves only when the tile
 // max exceeds it by more than 8 (log2 units), so P stays <= 256 and O is
 // rarely touched; the final O / d' uses the same reference, so the result is
@@ -63,7 +75,7 @@ struct PfSmem {
     static constexpr int kTileBytes = kPanels * kPanelBytes; // one Q slot, K tile or V tile
     static constexpr int kRingOff = 2 * kTileBytes;
     static constexpr int kBarOff = kRingOff + kPfStages * kTileBytes;
-    static constexpr int kNumBars = 16;
+    static constexpr int kNumBars = 2 * kPfStages + 16;
     static constexpr int kBytes = kBarOff + kNumBars * 8 + 16 + 1024 /*align slack*/;
 };
 
@@ -253,7 +265,10 @@ __global__ void __launch_bounds__(kSchedThreads) attn_prefill_schedule_kernel(co
         units_in[kSchedBuckets - 1 - (threadIdx.x * PER + i)] = run;
         run += local[i];
     }
-    if (threadIdx.x == kSchedThreads - 1) p.unit_count[0] = run;
+    if (threadIdx.x == kSchedThreads - 1) {
+        p.unit_count[0] = run;
+        p.unit_count[1] = 0;   // the attention kernel's next-unit counter
+    }
     __syncthreads();
     for (int b = threadIdx.x; b < p.batch; b += kSchedThreads) {
         const int pairs = pf_pairs(p, b, false);
@@ -262,6 +277,40 @@ __global__ void __launch_bounds__(kSchedThreads) attn_prefill_schedule_kernel(co
         for (int h = 0; h < p.Hkv; ++h)
             for (int i = 0; i < pairs; ++i) p.units[off++] = make_int2(b, (pairs - 1 - i) | (h << 16));
     }
+}
+
+// Work of one unit: rows [t0A, t0A + tps) and [t0B, t0B + tps) of sequence b
+// (tps = 128 / G tokens), nA / nB key tiles.  An invalid unit (bad offsets,
+// reported by the scheduler) has no rows and no tiles.
+struct PfUnit {
+    int b, hkv, qs, Lq, ks0, Lk, off, t0A, t0B, nA, nB, n;
+};
+
+__device__ __forceinline__ PfUnit pf_unit(const PrefillParams &p, int u) {
+    PfUnit w;
+    const int2 e = p.units[u];
+    w.b = e.x;
+    w.hkv = e.y >> 16;
+    const int pair = e.y & 0xFFFF, tps = BM / p.G;
+    if (!seq_rows(p, w.b, false, w.qs, w.Lq, w.ks0, w.Lk) || pair * 2 * tps >= w.Lq) {
+        w.qs = w.ks0 = w.Lk = w.off = w.nA = w.nB = w.n = 0;
+        w.Lq = 0;
+        w.t0A = w.t0B = 0;
+        return w;
+    }
+    w.off = w.Lk - w.Lq;
+    w.t0A = pair * 2 * tps;
+    w.t0B = w.t0A + tps;
+    auto tiles_for = [&](int t0) -> int {
+        if (t0 >= w.Lq) return 0;
+        const int t1 = min(t0 + tps, w.Lq);
+        const int kend = p.causal ? min(max(t1 + w.off, 0), w.Lk) : w.Lk;
+        return (kend + BN - 1) / BN;
+    };
+    w.nA = tiles_for(w.t0A);
+    w.nB = tiles_for(w.t0B);
+    w.n = max(w.nA, w.nB);
+    return w;
 }
 
 template <int D>
@@ -275,39 +324,28 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     uint8_t *sRing = sm + S::kRingOff;
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + S::kBarOff);
     uint64_t *q_full = bars;
-    uint64_t *full = bars + 1;
-    uint64_t *empty = bars + 1 + kPfStages;
-    uint64_t *s_full = bars + 1 + 2 * kPfStages;   // [2]
+    uint64_t *q_empty = bars + 1;                  // this unit's QK^T have read Q
+    uint64_t *full = bars + 2;
+    uint64_t *empty = full + kPfStages;
+    uint64_t *s_full = empty + kPfStages;          // [2]
     uint64_t *p_ready = s_full + 2;                // [2]
-    uint64_t *o_full = p_ready + 2;                // [2]
-    uint64_t *drain_bar = o_full + 2;
+    uint64_t *o_full = p_ready + 2;                // [2]: O_X of this unit complete
+    uint64_t *o_empty = o_full + 2;                // [2]: the epilogue has read O_X
+    uint64_t *drain_bar = o_empty + 2;
+    uint64_t *idx_full = drain_bar + 1;            // [2]: unit_idx[s] written
+    uint64_t *idx_empty = idx_full + 2;            // [2]: every role has read unit_idx[s]
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + S::kNumBars);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    volatile int *unit_idx = reinterpret_cast<volatile int *>(tmem_slot + 2);   // [2]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    if ((int)blockIdx.x >= p.unit_count[0]) return;
-    const int2 unit = p.units[blockIdx.x];
-    const int b = unit.x, pair = unit.y & 0xFFFF, hkv = unit.y >> 16;
-    const int G = p.G, tps = BM / G;
-
-    int qs, Lq, ks0, Lk;
-    if (!seq_rows(p, b, false, qs, Lq, ks0, Lk)) return;   // reported by the scheduler
-    const int t0A = pair * 2 * tps;
-    if (t0A >= Lq) return;
-    const int t0B = t0A + tps;
-    const int off = Lk - Lq;
-    auto tiles_for = [&](int t0) -> int {
-        if (t0 >= Lq) return 0;
-        const int t1 = min(t0 + tps, Lq);
-        const int kend = p.causal ? min(max(t1 + off, 0), Lk) : Lk;
-        return (kend + BN - 1) / BN;
-    };
-    const int nA = tiles_for(t0A), nB = tiles_for(t0B);
-    const int n = max(nA, nB);
-    const bool activeB = t0B < Lq;
+    const int G = p.G;
+    const int num_units = p.unit_count[0];
+    int *next_unit = p.unit_count + 1;   // zeroed by the scheduler
 
     if (threadIdx.x == 0) {
         mbar_init(q_full, 1);
+        mbar_init(q_empty, 1);
         for (int i = 0; i < kPfStages; ++i) {
             mbar_init(&full[i], 1);
             mbar_init(&empty[i], 1);
@@ -316,8 +354,13 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             mbar_init(&s_full[x], 1);
             mbar_init(&p_ready[x], 128);
             mbar_init(&o_full[x], 1);
+            mbar_init(&o_empty[x], 128);
         }
         mbar_init(drain_bar, 1);
+        for (int x = 0; x < 2; ++x) {
+            mbar_init(&idx_full[x], 1);
+            mbar_init(&idx_empty[x], 1 + 256);   // the MMA thread and every softmax thread
+        }
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -336,119 +379,179 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             tma_prefetch_desc(&qmap);
             tma_prefetch_desc(&kmap);
             tma_prefetch_desc(&vmap);
-            if (n > 0) {
-                mbar_arrive_expect_tx(q_full, (uint32_t)S::kTileBytes * (activeB ? 2u : 1u));
-#pragma unroll
-                for (int pn = 0; pn < S::kPanels; ++pn)
-                    tma_load_3d(sQ + pn * S::kPanelBytes, &qmap, q_full, pn * 64, hkv * G, qs + t0A);
-                if (activeB) {
-#pragma unroll
-                    for (int pn = 0; pn < S::kPanels; ++pn)
-                        tma_load_3d(sQ + S::kTileBytes + pn * S::kPanelBytes, &qmap, q_full, pn * 64, hkv * G,
-                                    qs + t0B);
-                }
-            }
         }
         const bool paged = p.block_table != nullptr;
-        const int32_t *bt = paged ? p.block_table + (int64_t)b * p.bt_stride : nullptr;
         const int oob_row = paged ? (int)(p.num_blocks * p.block_size) : 0;
-        int it = 0;
+        int it = 0, k = 0;
         bool ok = true;
-        for (int j = 0; j < n && ok; ++j) {
-            for (int w = 0; w < 2; ++w) {   // 0: K tile, 1: V tile
-                const int st = it % kPfStages;
-                const uint32_t ph = (uint32_t)(it / kPfStages) & 1u;
-                int got = 1;
-                if (lane == 0) got = mbar_wait(&empty[st], ph ^ 1u, abort_flag, p.err, SRC_PREFILL);
-                got = __shfl_sync(0xffffffffu, got, 0);
-                if (!got) { ok = false; break; }
-                uint8_t *dst = sRing + st * S::kTileBytes;
-                const CUtensorMap *map = w ? &vmap : &kmap;
-                const int key0 = j * BN;
-                uint64_t *bar = &full[st];
-                if (lane == 0) {
-                    mbar_arrive_expect_tx(bar, (uint32_t)S::kTileBytes);
-                    // V' is contiguous by logical key (rows past the sequence hold the
-                    // next sequence's keys or lie past the end: finite, zero-filled)
-                    if (!paged || w == 1) {
+        for (;; ++k) {
+            // next unit index (-1: none left) into the ring entry k & 1
+            int u = -1;
+            if (lane == 0) {
+                const int q = k >> 1;
+                if (q == 0 || mbar_wait(&idx_empty[k & 1], (uint32_t)(q - 1) & 1u, abort_flag, p.err, SRC_PREFILL)) {
+                    u = atomicAdd(next_unit, 1);
+                    if (u >= num_units) u = -1;
+                    unit_idx[k & 1] = u;
+                    mbar_arrive(&idx_full[k & 1]);
+                }
+            }
+            u = __shfl_sync(0xffffffffu, u, 0);
+            if (u < 0 || !ok) break;
+            const PfUnit w = pf_unit(p, u);
+            const int32_t *bt = paged ? p.block_table + (int64_t)w.b * p.bt_stride : nullptr;
+            // Q of this unit once the previous unit's QK^T are done with the Q buffers
+            int got = 1;
+            if (lane == 0 && k > 0)
+                got = mbar_wait(q_empty, (uint32_t)(k - 1) & 1u, abort_flag, p.err, SRC_PREFILL);
+            got = __shfl_sync(0xffffffffu, got, 0);
+            if (!got) break;
+            if (lane == 0) {
+                if (w.n > 0) {
+                    const bool activeB = w.t0B < w.Lq;
+                    mbar_arrive_expect_tx(q_full, (uint32_t)S::kTileBytes * (activeB ? 2u : 1u));
+#pragma unroll
+                    for (int pn = 0; pn < S::kPanels; ++pn)
+                        tma_load_3d(sQ + pn * S::kPanelBytes, &qmap, q_full, pn * 64, w.hkv * G, w.qs + w.t0A);
+                    if (activeB) {
 #pragma unroll
                         for (int pn = 0; pn < S::kPanels; ++pn)
-                            tma_load_3d(dst + pn * S::kPanelBytes, map, bar, pn * 64, hkv, ks0 + key0);
-                    } else {
-                        const int rpb = p.rows_per_box;
-                        for (int i = 0; i < BN / rpb; ++i) {
-                            const int key = key0 + i * rpb;
-                            int row = oob_row;   // past the end of the cache: zero-filled
-                            if (key < Lk) {
-                                const int blk = __ldg(bt + key / p.block_size);
-                                if (blk < 0 || (int64_t)blk >= p.num_blocks)
-                                    record_error(p.err, ERR_INDEX | SRC_PREFILL);
-                                else
-                                    row = blk * p.block_size + key % p.block_size;
-                            }
+                            tma_load_3d(sQ + S::kTileBytes + pn * S::kPanelBytes, &qmap, q_full, pn * 64,
+                                        w.hkv * G, w.qs + w.t0B);
+                    }
+                } else {
+                    mbar_arrive(q_full);
+                }
+            }
+            for (int j = 0; j < w.n && ok; ++j) {
+                for (int wv = 0; wv < 2; ++wv) {   // 0: K tile, 1: V tile
+                    const int st = it % kPfStages;
+                    const uint32_t ph = (uint32_t)(it / kPfStages) & 1u;
+                    got = 1;
+                    if (lane == 0) got = mbar_wait(&empty[st], ph ^ 1u, abort_flag, p.err, SRC_PREFILL);
+                    got = __shfl_sync(0xffffffffu, got, 0);
+                    if (!got) { ok = false; break; }
+                    uint8_t *dst = sRing + st * S::kTileBytes;
+                    const CUtensorMap *map = wv ? &vmap : &kmap;
+                    const int key0 = j * BN;
+                    uint64_t *bar = &full[st];
+                    if (lane == 0) {
+                        mbar_arrive_expect_tx(bar, (uint32_t)S::kTileBytes);
+                        // V' is contiguous by logical key (rows past the sequence hold the
+                        // next sequence's keys or zeroed rows)
+                        if (!paged || wv == 1) {
 #pragma unroll
                             for (int pn = 0; pn < S::kPanels; ++pn)
-                                tma_load_3d(dst + pn * S::kPanelBytes + i * rpb * 128, map, bar, pn * 64, hkv, row);
+                                tma_load_3d(dst + pn * S::kPanelBytes, map, bar, pn * 64, w.hkv, w.ks0 + key0);
+                        } else {
+                            const int rpb = p.rows_per_box;
+                            for (int i = 0; i < BN / rpb; ++i) {
+                                const int key = key0 + i * rpb;
+                                int row = oob_row;   // past the end of the cache: zero-filled
+                                if (key < w.Lk) {
+                                    const int blk = __ldg(bt + key / p.block_size);
+                                    if (blk < 0 || (int64_t)blk >= p.num_blocks)
+                                        record_error(p.err, ERR_INDEX | SRC_PREFILL);
+                                    else
+                                        row = blk * p.block_size + key % p.block_size;
+                                }
+#pragma unroll
+                                for (int pn = 0; pn < S::kPanels; ++pn)
+                                    tma_load_3d(dst + pn * S::kPanelBytes + i * rpb * 128, map, bar, pn * 64,
+                                                w.hkv, row);
+                            }
                         }
                     }
+                    ++it;
                 }
-                ++it;
             }
         }
         if (lane == 0) {
             // every copy issued here lands before the CTA may exit
             for (int t = it - kPfStages < 0 ? 0 : it - kPfStages; t < it; ++t)
                 mbar_wait(&full[t % kPfStages], (uint32_t)(t / kPfStages) & 1u, nullptr, p.err, SRC_PREFILL);
-            if (n > 0) mbar_wait(q_full, 0, nullptr, p.err, SRC_PREFILL);
+            if (k > 0) mbar_wait(q_full, (uint32_t)(k - 1) & 1u, nullptr, p.err, SRC_PREFILL);
         }
     } else if (warp == 9) {
         // ================================================================ MMA issuer
-        if (lane == 0 && n > 0) {
-            bool ok = mbar_wait(q_full, 0, abort_flag, p.err, SRC_PREFILL);
-            tc_fence_after();
+        if (lane == 0) {
             const uint32_t tS0 = tmem, tS1 = tmem + 128;
             const uint32_t tO0 = tmem + 256, tO1 = tmem + 256 + D;
             const uint32_t qA = smem_u32(sQ), qB = smem_u32(sQ + S::kTileBytes);
             const uint32_t ring = smem_u32(sRing);
-            for (int j = 0; j <= n && ok; ++j) {
-                const int itK = 2 * j, stK = itK % kPfStages;
-                const int itV = 2 * j + 1, stV = itV % kPfStages;
-                if (j < n) {
-                    ok = mbar_wait(&full[stK], (uint32_t)(itK / kPfStages) & 1u, abort_flag, p.err, SRC_PREFILL);
-                    if (!ok) break;
-                    tc_fence_after();
-                    if (j < nA) {
-                        issue_qk<D>(tS0, qA, ring + stK * S::kTileBytes);
-                        tc_commit(&s_full[0]);
-                    }
-                }
-                if (j >= 1 && j - 1 < nB) {
-                    const int jj = j - 1;
-                    const int itP = 2 * jj + 1, stP = itP % kPfStages;
-                    ok = mbar_wait(&full[stP], (uint32_t)(itP / kPfStages) & 1u, abort_flag, p.err, SRC_PREFILL) &&
-                         mbar_wait(&p_ready[1], (uint32_t)jj & 1u, abort_flag, p.err, SRC_PREFILL);
-                    if (!ok) break;
-                    tc_fence_after();
-                    issue_pv<D>(tO1, tS1, ring + stP * S::kTileBytes, jj > 0);
-                    if (jj == nB - 1) tc_commit(&o_full[1]);
-                    tc_commit(&empty[stP]);
-                }
-                if (j < n) {
-                    if (j < nB) {
-                        issue_qk<D>(tS1, qB, ring + stK * S::kTileBytes);
-                        tc_commit(&s_full[1]);
-                    }
-                    tc_commit(&empty[stK]);
-                    if (j < nA) {
-                        ok = mbar_wait(&full[stV], (uint32_t)(itV / kPfStages) & 1u, abort_flag, p.err, SRC_PREFILL) &&
-                             mbar_wait(&p_ready[0], (uint32_t)j & 1u, abort_flag, p.err, SRC_PREFILL);
+            int itb = 0, cA = 0, cB = 0, k = 0;   // ring items, P' tiles of A / B before this unit
+            bool ok = true;
+            for (;; ++k) {
+                ok = mbar_wait(&idx_full[k & 1], (uint32_t)(k >> 1) & 1u, abort_flag, p.err, SRC_PREFILL);
+                if (!ok) break;
+                const int u = unit_idx[k & 1];
+                mbar_arrive(&idx_empty[k & 1]);
+                if (u < 0) break;
+                const PfUnit w = pf_unit(p, u);
+                const int n = w.n, nA = w.nA, nB = w.nB;
+                ok = mbar_wait(q_full, (uint32_t)k & 1u, abort_flag, p.err, SRC_PREFILL);
+                if (!ok) break;
+                tc_fence_after();
+                for (int j = 0; j <= n && ok; ++j) {
+                    const int itK = itb + 2 * j, stK = itK % kPfStages;
+                    const int itV = itb + 2 * j + 1, stV = itV % kPfStages;
+                    if (j < n) {
+                        ok = mbar_wait(&full[stK], (uint32_t)(itK / kPfStages) & 1u, abort_flag, p.err, SRC_PREFILL);
                         if (!ok) break;
                         tc_fence_after();
-                        issue_pv<D>(tO0, tS0, ring + stV * S::kTileBytes, j > 0);
-                        if (j == nA - 1) tc_commit(&o_full[0]);
-                        if (j >= nB) tc_commit(&empty[stV]);
+                        if (j < nA) {
+                            issue_qk<D>(tS0, qA, ring + stK * S::kTileBytes);
+                            tc_commit(&s_full[0]);
+                        }
+                    }
+                    if (j >= 1 && j - 1 < nB) {
+                        const int jj = j - 1;
+                        const int itP = itb + 2 * jj + 1, stP = itP % kPfStages;
+                        // O_B of the previous unit read by its epilogue
+                        if (jj == 0 && k > 0)
+                            ok = mbar_wait(&o_empty[1], (uint32_t)(k - 1) & 1u, abort_flag, p.err, SRC_PREFILL);
+                        ok = ok &&
+                             mbar_wait(&full[stP], (uint32_t)(itP / kPfStages) & 1u, abort_flag, p.err, SRC_PREFILL) &&
+                             mbar_wait(&p_ready[1], (uint32_t)(cB + jj) & 1u, abort_flag, p.err, SRC_PREFILL);
+                        if (!ok) break;
+                        tc_fence_after();
+                        issue_pv<D>(tO1, tS1, ring + stP * S::kTileBytes, jj > 0);
+                        if (jj == nB - 1) tc_commit(&o_full[1]);
+                        tc_commit(&empty[stP]);
+                    }
+                    if (j < n) {
+                        if (j < nB) {
+                            issue_qk<D>(tS1, qB, ring + stK * S::kTileBytes);
+                            tc_commit(&s_full[1]);
+                        }
+                        tc_commit(&empty[stK]);
+                        if (j == n - 1) tc_commit(q_empty);   // every QK^T of the unit is issued
+                        if (j < nA) {
+                            if (j == 0 && k > 0)
+                                ok = mbar_wait(&o_empty[0], (uint32_t)(k - 1) & 1u, abort_flag, p.err, SRC_PREFILL);
+                            ok = ok &&
+                                 mbar_wait(&full[stV], (uint32_t)(itV / kPfStages) & 1u, abort_flag, p.err,
+                                           SRC_PREFILL) &&
+                                 mbar_wait(&p_ready[0], (uint32_t)(cA + j) & 1u, abort_flag, p.err, SRC_PREFILL);
+                            if (!ok) break;
+                            tc_fence_after();
+                            issue_pv<D>(tO0, tS0, ring + stV * S::kTileBytes, j > 0);
+                            if (j == nA - 1) tc_commit(&o_full[0]);
+                            if (j >= nB) tc_commit(&empty[stV]);
+                        }
                     }
                 }
+                if (!ok) break;
+                // a slot without key tiles still completes its o_full / o_empty phase
+                for (int x = 0; x < 2 && ok; ++x) {
+                    if ((x ? nB : nA) > 0) continue;
+                    if (k > 0) ok = mbar_wait(&o_empty[x], (uint32_t)(k - 1) & 1u, abort_flag, p.err, SRC_PREFILL);
+                    if (ok) tc_commit(&o_full[x]);
+                }
+                if (n == 0) tc_commit(q_empty);
+                itb += 2 * n;
+                cA += nA;
+                cB += nB;
             }
             // no MMA may still run when TMEM is released
             tc_commit(drain_bar);
@@ -460,119 +563,138 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         const int X = warp >> 2;
         const int r = (warp & 3) * 32 + lane;
         const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
-        const int t0 = X ? t0B : t0A;
-        const int nX = X ? nB : nA;
-        const int tok = t0 + r / G;
-        const int head = hkv * G + r % G;
-        const bool row_valid = tok < Lq;
-        // last key this row may see (negative: none)
-        const int lim = p.causal ? min(tok + off, Lk - 1) : Lk - 1;
         const uint32_t tS = tmem + (uint32_t)(X * 128) + lane_off;
         const uint32_t tO = tmem + 256u + (uint32_t)(X * D) + lane_off;
         const float sl2 = p.scale_log2;
-        float m_ref = -INFINITY;   // reference max (log2 units) used for P
-        float l = 0.f;             // proxy denominator d'
+        int cX = 0, k = 0;   // S tiles of this slot before this unit
         bool ok = true;
-        for (int j = 0; j < nX; ++j) {
-            ok = __all_sync(0xffffffffu, mbar_wait(&s_full[X], (uint32_t)j & 1u, abort_flag, p.err, SRC_PREFILL));
+        for (;; ++k) {
+            ok = __all_sync(0xffffffffu,
+                            mbar_wait(&idx_full[k & 1], (uint32_t)(k >> 1) & 1u, abort_flag, p.err, SRC_PREFILL));
+            if (!ok) break;
+            const int u = unit_idx[k & 1];
+            mbar_arrive(&idx_empty[k & 1]);
+            if (u < 0) break;
+            const PfUnit w = pf_unit(p, u);
+            const int t0 = X ? w.t0B : w.t0A;
+            const int nX = X ? w.nB : w.nA;
+            const int tok = t0 + r / G;
+            const int head = w.hkv * G + r % G;
+            const bool row_valid = tok < w.Lq;
+            // last key this row may see (negative: none)
+            const int lim = p.causal ? min(tok + w.off, w.Lk - 1) : w.Lk - 1;
+            float m_ref = -INFINITY;   // reference max (log2 units) used for P
+            float l = 0.f;             // proxy denominator d'
+            for (int j = 0; j < nX; ++j) {
+                ok = __all_sync(0xffffffffu,
+                                mbar_wait(&s_full[X], (uint32_t)(cX + j) & 1u, abort_flag, p.err, SRC_PREFILL));
+                if (!ok) break;
+                tc_fence_after();
+                float s[BN];
+                tmem_ld32(tS + 0, *reinterpret_cast<uint32_t(*)[32]>(&s[0]));
+                tmem_ld32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&s[32]));
+                tmem_ld32(tS + 64, *reinterpret_cast<uint32_t(*)[32]>(&s[64]));
+                tmem_ld32(tS + 96, *reinterpret_cast<uint32_t(*)[32]>(&s[96]));
+                tc_wait_ld();
+                const int key0 = j * BN;
+                if (key0 + BN - 1 > lim) {
+#pragma unroll
+                    for (int c = 0; c < BN; ++c)
+                        if (key0 + c > lim) s[c] = -INFINITY;
+                }
+                // row max: eight independent chains (chain q takes columns q, q + 8, ...)
+                float mx8[8];
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    mx8[q] = max3f(s[q], s[q + 8], s[q + 16]);
+#pragma unroll
+                    for (int kk = 3; kk < 15; kk += 2) mx8[q] = max3f(mx8[q], s[q + 8 * kk], s[q + 8 * kk + 8]);
+                    mx8[q] = fmaxf(mx8[q], s[q + 120]);
+                }
+                const float mx =
+                    max3f(max3f(mx8[0], mx8[1], mx8[2]), max3f(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]));
+                const float m_new = fmaxf(m_ref, mx * sl2);
+                const bool need = m_new > m_ref + 8.0f;
+                float alpha = 1.f;
+                if (need) {
+                    alpha = (m_ref == -INFINITY) ? 0.f : ex2(m_ref - m_new);
+                    m_ref = m_new;
+                }
+                l *= alpha;
+                // P' = 2^(s*scale*log2e - m_ref + 4) = 16 P, fp16 over the first 64 columns of S;
+                // the row sum in four paired accumulators
+                const float nref = ((m_ref == -INFINITY) ? 0.f : -m_ref) + 4.0f;
+                float la[4] = {0.f, 0.f, 0.f, 0.f}, lb[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int c4 = 0; c4 < BN / 32; ++c4) {
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        float x0, x1;
+                        fma2(x0, x1, s[c4 * 32 + 2 * i], s[c4 * 32 + 2 * i + 1], sl2, sl2, nref, nref);
+                        x0 = ex2(x0);
+                        x1 = ex2(x1);
+                        add2(la[i & 3], lb[i & 3], x0, x1);
+                        pk[i] = pack_f16x2(x0, x1);
+                    }
+                    tmem_st16(tS + (uint32_t)(c4 * 16), pk);
+                }
+                l += ((la[0] + lb[0]) + (la[1] + lb[1])) + ((la[2] + lb[2]) + (la[3] + lb[3]));
+                // O *= alpha where the reference moved (O of tile 0 is written, not accumulated);
+                // the commit of S_X(j) covered PV_X(j-1)
+                if (j > 0 && __any_sync(0xffffffffu, need)) {
+#pragma unroll
+                    for (int c = 0; c < D / 32; ++c) {
+                        uint32_t o[32];
+                        tmem_ld32(tO + (uint32_t)(c * 32), o);
+                        tc_wait_ld();
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                        tmem_st32(tO + (uint32_t)(c * 32), o);
+                    }
+                }
+                tc_wait_st();
+                tc_fence_before();
+                mbar_arrive(&p_ready[X]);
+            }
+            if (!ok) break;
+            cX += nX;
+            // ------------------------------------------------------------ epilogue
+            ok = __all_sync(0xffffffffu, mbar_wait(&o_full[X], (uint32_t)k & 1u, abort_flag, p.err, SRC_PREFILL));
             if (!ok) break;
             tc_fence_after();
-            float s[BN];
-            tmem_ld32(tS + 0, *reinterpret_cast<uint32_t(*)[32]>(&s[0]));
-            tmem_ld32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&s[32]));
-            tmem_ld32(tS + 64, *reinterpret_cast<uint32_t(*)[32]>(&s[64]));
-            tmem_ld32(tS + 96, *reinterpret_cast<uint32_t(*)[32]>(&s[96]));
-            tc_wait_ld();
-            const int key0 = j * BN;
-            if (key0 + BN - 1 > lim) {
-#pragma unroll
-                for (int c = 0; c < BN; ++c)
-                    if (key0 + c > lim) s[c] = -INFINITY;
-            }
-            // row max: eight independent chains (chain q takes columns q, q + 8, ...)
-            float mx8[8];
-#pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                mx8[q] = max3f(s[q], s[q + 8], s[q + 16]);
-#pragma unroll
-                for (int k = 3; k < 15; k += 2) mx8[q] = max3f(mx8[q], s[q + 8 * k], s[q + 8 * k + 8]);
-                mx8[q] = fmaxf(mx8[q], s[q + 120]);
-            }
-            const float mx = max3f(max3f(mx8[0], mx8[1], mx8[2]), max3f(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]));
-            const float m_new = fmaxf(m_ref, mx * sl2);
-            const bool need = m_new > m_ref + 8.0f;
-            float alpha = 1.f;
-            if (need) {
-                alpha = (m_ref == -INFINITY) ? 0.f : ex2(m_ref - m_new);
-                m_ref = m_new;
-            }
-            l *= alpha;
-            // P' = 2^(s*scale*log2e - m_ref + 4) = 16 P
-            const float nref = ((m_ref == -INFINITY) ? 0.f : -m_ref) + 4.0f;
-            // P' (fp16) over the first 64 columns of S; the row sum in four paired accumulators
-            float la[4] = {0.f, 0.f, 0.f, 0.f}, lb[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-            for (int c4 = 0; c4 < BN / 32; ++c4) {
-                uint32_t pk[16];
-#pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    float x0, x1;
-                    fma2(x0, x1, s[c4 * 32 + 2 * i], s[c4 * 32 + 2 * i + 1], sl2, sl2, nref, nref);
-                    x0 = ex2(x0);
-                    x1 = ex2(x1);
-                    add2(la[i & 3], lb[i & 3], x0, x1);
-                    pk[i] = pack_f16x2(x0, x1);
-                }
-                tmem_st16(tS + (uint32_t)(c4 * 16), pk);
-            }
-            l += ((la[0] + lb[0]) + (la[1] + lb[1])) + ((la[2] + lb[2]) + (la[3] + lb[3]));
-            // O *= alpha where the reference moved (O of tile 0 is written, not accumulated)
-            if (j > 0 && __any_sync(0xffffffffu, need)) {
+            if (__any_sync(0xffffffffu, row_valid)) {
+                const float inv = l > 0.f ? 16.f / l : 0.f;   // l accumulated P' = 16 P
+                __nv_bfloat16 *orow =
+                    p.out + (int64_t)(w.qs + (row_valid ? tok : 0)) * p.out_row_stride + (int64_t)head * D;
 #pragma unroll
                 for (int c = 0; c < D / 32; ++c) {
                     uint32_t o[32];
-                    tmem_ld32(tO + (uint32_t)(c * 32), o);
-                    tc_wait_ld();
+                    if (nX > 0) {
+                        tmem_ld32(tO + (uint32_t)(c * 32), o);
+                        tc_wait_ld();
+                    } else {
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-                    tmem_st32(tO + (uint32_t)(c * 32), o);
+                        for (int i = 0; i < 32; ++i) o[i] = 0u;
+                    }
+                    if (row_valid) {
+                        uint32_t pk[16];
+#pragma unroll
+                        for (int i = 0; i < 16; ++i)
+                            pk[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv, __uint_as_float(o[2 * i + 1]) * inv);
+                        uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+                            dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+                    }
                 }
+                if (row_valid && p.lse)
+                    p.lse[(int64_t)head * p.total_q + w.qs + tok] =
+                        l > 0.f ? (m_ref + __log2f(l) - 4.0f) * 0.69314718055994531f : -INFINITY;
             }
-            tc_wait_st();
+            // O_X may be overwritten by the next unit
             tc_fence_before();
-            mbar_arrive(&p_ready[X]);
-        }
-        // ---------------------------------------------------------------- epilogue
-        if (ok && nX > 0) {
-            ok = __all_sync(0xffffffffu, mbar_wait(&o_full[X], 0, abort_flag, p.err, SRC_PREFILL));
-            tc_fence_after();
-        }
-        if (ok) {
-            const float inv = l > 0.f ? 16.f / l : 0.f;   // l accumulated P' = 16 P
-            __nv_bfloat16 *orow = p.out + (int64_t)(qs + (row_valid ? tok : 0)) * p.out_row_stride + (int64_t)head * D;
-#pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
-                uint32_t o[32];
-                if (nX > 0) {
-                    tmem_ld32(tO + (uint32_t)(c * 32), o);
-                    tc_wait_ld();
-                } else {
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) o[i] = 0u;
-                }
-                if (row_valid) {
-                    uint32_t pk[16];
-#pragma unroll
-                    for (int i = 0; i < 16; ++i)
-                        pk[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv, __uint_as_float(o[2 * i + 1]) * inv);
-                    uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
-                }
-            }
-            if (row_valid && p.lse)
-                p.lse[(int64_t)head * p.total_q + qs + tok] =
-                    l > 0.f ? (m_ref + __log2f(l) - 4.0f) * 0.69314718055994531f : -INFINITY;
+            mbar_arrive(&o_empty[X]);
         }
     }
 
