@@ -59,3 +59,39 @@ def test_decode_split_rule_is_host_side(L):
     assert L.attn_decode_num_splits(1, 8, 16384, 0) >= 8
     assert L.attn_decode_num_splits(4, 8, 100, 5) == 2          # capped by 64-token tiles
     assert L.attn_decode_workspace_size(256, 32, 8, 128, 16384, 1) == 0
+
+
+def test_new_entries_validate_on_the_host(L):
+    """kv-cache, padded and softmax entries reject bad arguments before any device work."""
+    null = None
+    fake = ctypes.c_void_p(0x1000)
+    L.attn_kvcache_fwd.restype = ctypes.c_int
+    L.attn_padded_fwd.restype = ctypes.c_int
+    L.attn_softmax_rows.restype = ctypes.c_int
+    # kv-cache: null pointers, non-positive seqlen_q, batch
+    assert L.attn_kvcache_fwd(null, fake, fake, fake, null, fake, fake, 4, 2, 3, 32, 8, 128, 16, 64, 64,
+                              ctypes.c_float(0.1), 1, fake, ctypes.c_size_t(1 << 30), null) == 1
+    assert L.attn_kvcache_fwd(fake, fake, fake, fake, null, fake, fake, 4, 2, 0, 32, 8, 128, 16, 64, 64,
+                              ctypes.c_float(0.1), 1, fake, ctypes.c_size_t(1 << 30), null) == 1
+    # padded: null q, zero batch
+    assert L.attn_padded_fwd(null, fake, fake, fake, null, null, null, 2, 16, 16, 8, 8, 64, ctypes.c_float(0.1), 1,
+                             fake, ctypes.c_size_t(1 << 30), null) == 1
+    assert L.attn_padded_fwd(fake, fake, fake, fake, null, null, null, 0, 16, 16, 8, 8, 64, ctypes.c_float(0.1), 1,
+                             fake, ctypes.c_size_t(1 << 30), null) == 1
+    # softmax: null pointers, negative rows, unknown dtype, stride shorter than a row
+    i64 = ctypes.c_int64
+    assert L.attn_softmax_rows(null, fake, i64(4), 8, i64(0), i64(0), 0, null) == 1
+    assert L.attn_softmax_rows(fake, fake, i64(-1), 8, i64(0), i64(0), 0, null) == 1
+    assert L.attn_softmax_rows(fake, fake, i64(4), 8, i64(0), i64(0), 7, null) == 1
+    assert L.attn_softmax_rows(fake, fake, i64(4), 8, i64(4), i64(0), 0, null) == 1
+
+
+def test_new_workspace_sizes_are_host_side(L):
+    L.attn_kvcache_workspace_size.restype = ctypes.c_size_t
+    L.attn_padded_workspace_size.restype = ctypes.c_size_t
+    assert L.attn_kvcache_workspace_size(0, 1, 32, 8, 128, 100) == 0
+    assert L.attn_padded_workspace_size(2, 0, 16, 8, 8, 64) == 0
+    a = L.attn_kvcache_workspace_size(4, 3, 32, 8, 128, 1000)
+    b = L.attn_kvcache_workspace_size(4, 3, 32, 8, 128, 2000)
+    assert 0 < a < b            # the fp16 V' copy grows with the cache length
+    assert L.attn_padded_workspace_size(2, 16, 64, 8, 8, 64) > 0
