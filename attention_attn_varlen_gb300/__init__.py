@@ -25,7 +25,7 @@ import torch
 from ._build import LIB as _LIB_PATH
 from ._build import build
 
-__all__ = ["attn_varlen_fwd", "attn_decode_paged", "attn_with_kvcache", "attn_padded_fwd", "softmax_rows", "store_kvcache", "get_last_device_error", "lib",
+__all__ = ["attn_varlen_fwd", "attn_varlen_fwd_host", "attn_decode_paged", "attn_with_kvcache", "attn_padded_fwd", "softmax_rows", "store_kvcache", "get_last_device_error", "lib",
            "build", "AttnError", "exported_symbols", "set_kernel_events", "decode_num_splits", "decode_workspace_size"]
 
 ATTN_OK = 0
@@ -207,6 +207,69 @@ def decode_num_splits(batch: int, num_heads_kv: int, max_cache_seqlen: int, num_
 def decode_workspace_size(batch, num_heads_q, num_heads_kv, head_dim, max_cache_seqlen, num_splits=0) -> int:
     return lib().attn_decode_workspace_size(batch, num_heads_q, num_heads_kv, head_dim, max_cache_seqlen,
                                             num_splits)
+
+
+def attn_varlen_fwd_host(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, max_seqlen_k: int,
+                         softmax_scale: float | None = None, causal: bool = True, out=None, chunks: int = 8,
+                         device=None):
+    """attn_varlen_fwd for host-resident inputs: q, k, v (pinned CPU bf16, packed),
+    cu_seqlens (CPU int32).  Sequences are split into `chunks` groups of about equal
+    token count; the copy of group i+1 to the device overlaps the attention of group
+    i and the copy back of group i-1 (three CUDA streams).  Returns the output in a
+    pinned CPU tensor (`out` if given) once it has arrived.  Each group runs the
+    same kernels as attn_varlen_fwd on the whole batch, so the result is the same."""
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if t.is_cuda or t.dtype != torch.bfloat16 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous bf16 CPU tensor (pinned for overlap)")
+    device = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    cq = cu_seqlens_q.cpu().numpy().astype("int64")
+    ck = cu_seqlens_k.cpu().numpy().astype("int64")
+    B = len(cq) - 1
+    if out is None:
+        out = torch.empty(q.shape, dtype=q.dtype).pin_memory()
+    dq, dk, dv = (torch.empty(t.shape, dtype=t.dtype, device=device) for t in (q, k, v))
+    dout = torch.empty(q.shape, dtype=q.dtype, device=device)
+    dcq = cu_seqlens_q.to(device=device, dtype=torch.int32)
+    dck = cu_seqlens_k.to(device=device, dtype=torch.int32)
+    # group boundaries: whole sequences, about equal query tokens
+    target = [int(round(cq[-1] * (i + 1) / chunks)) for i in range(chunks)]
+    bounds, b0 = [], 0
+    for tgt in target:
+        b1 = b0
+        while b1 < B and (cq[b1 + 1] <= tgt or b1 == b0):
+            b1 += 1
+        if b1 > b0:
+            bounds.append((b0, b1))
+        b0 = b1
+        if b0 >= B:
+            break
+    if b0 < B:
+        bounds.append((b0, B))
+    main = torch.cuda.current_stream(device)
+    s_in, s_out = torch.cuda.Stream(device), torch.cuda.Stream(device)
+    s_in.wait_stream(main)
+    s_out.wait_stream(main)
+    for b0, b1 in bounds:
+        q0, q1, k0, k1 = int(cq[b0]), int(cq[b1]), int(ck[b0]), int(ck[b1])
+        with torch.cuda.stream(s_in):
+            dq[q0:q1].copy_(q[q0:q1], non_blocking=True)
+            dk[k0:k1].copy_(k[k0:k1], non_blocking=True)
+            dv[k0:k1].copy_(v[k0:k1], non_blocking=True)
+            arrived = torch.cuda.Event()
+            arrived.record(s_in)
+        main.wait_event(arrived)
+        mq = int((cq[b0 + 1:b1 + 1] - cq[b0:b1]).max())
+        mk = int((ck[b0 + 1:b1 + 1] - ck[b0:b1]).max())
+        attn_varlen_fwd(dq, dk, dv, dcq[b0:b1 + 1], dck[b0:b1 + 1], min(mq, max_seqlen_q), min(mk, max_seqlen_k),
+                        softmax_scale, causal=causal, out=dout)
+        computed = torch.cuda.Event()
+        computed.record(main)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(computed)
+            out[q0:q1].copy_(dout[q0:q1], non_blocking=True)
+    main.wait_stream(s_out)
+    main.synchronize()   # the device buffers die with this call
+    return out
 
 
 def attn_decode_paged(q, k_cache, v_cache, cache_seqlens, block_table, softmax_scale: float | None = None,

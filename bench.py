@@ -242,23 +242,16 @@ def bench_varlen(av, cfg, inp, steps, warmup, flush):
 
 
 def bench_varlen_e2e(av, cfg, inp, steps, warmup, flush):
-    """Host buffers in, host buffer out, through the public call."""
+    """Host buffers in, host buffer out, through the public host-input call
+    (attn_varlen_fwd_host: the copies of one group of sequences overlap the
+    attention of another)."""
     import torch
     hq, hk, hv = (inp[n].cpu().pin_memory() for n in ("q", "k", "v"))
     hcq, hck = inp["cu_q"].cpu().pin_memory(), inp["cu_k"].cpu().pin_memory()
     hout = torch.empty(hq.shape, dtype=hq.dtype).pin_memory()
-    dq, dk, dv = torch.empty_like(inp["q"]), torch.empty_like(inp["k"]), torch.empty_like(inp["v"])
-    dcq, dck = torch.empty_like(inp["cu_q"]), torch.empty_like(inp["cu_k"])
-    dout = torch.empty_like(inp["q"])
 
     def step():
-        dq.copy_(hq, non_blocking=True)
-        dk.copy_(hk, non_blocking=True)
-        dv.copy_(hv, non_blocking=True)
-        dcq.copy_(hcq, non_blocking=True)
-        dck.copy_(hck, non_blocking=True)
-        av.attn_varlen_fwd(dq, dk, dv, dcq, dck, inp["mq"], inp["mk"], cfg.scale, out=dout)
-        hout.copy_(dout, non_blocking=True)
+        av.attn_varlen_fwd_host(hq, hk, hv, hcq, hck, inp["mq"], inp["mk"], cfg.scale, out=hout)
     for _ in range(warmup):
         step()
     torch.cuda.synchronize()

@@ -327,3 +327,18 @@ def test_paged_prefill_ignores_stale_workspace():
     assert av.get_last_device_error()[0] == 0
     ref, _, _ = _paged_oracle(cfg, q, k_new, v_new, list(range(B)))
     assert_close(out, ref.reshape(out.shape), "paged, stale workspace")
+
+
+@pytest.mark.parametrize("chunks", [1, 3, 8])
+def test_host_pipelined_prefill_equals_device_call(chunks):
+    """attn_varlen_fwd_host (copies overlapped with the attention of other sequence
+    groups) returns the device call's bits."""
+    cfg = workloads.small_varlen(36, [700, 5, 1300, 64, 129, 900], [700, 5, 1300, 64, 129, 900], 32, 8, 128)
+    q, k, v = cfg.q(), cfg.k(), cfg.v()
+    ref = av.attn_varlen_fwd(q.cuda(), k.cuda(), v.cuda(), torch.from_numpy(cfg.cu_q).cuda(),
+                             torch.from_numpy(cfg.cu_k).cuda(), 1300, 1300, cfg.scale)
+    got = av.attn_varlen_fwd_host(q.pin_memory(), k.pin_memory(), v.pin_memory(), torch.from_numpy(cfg.cu_q),
+                                  torch.from_numpy(cfg.cu_k), 1300, 1300, cfg.scale, chunks=chunks)
+    torch.cuda.synchronize()
+    assert not got.is_cuda
+    assert torch.equal(got.view(torch.int16), ref.cpu().view(torch.int16))
