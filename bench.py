@@ -295,6 +295,28 @@ def bench_decode(av, device, steps, warmup, flush, peaks):
                         "kernel_ms": tk * 1e3,
                         "traffic": ncu_traffic("decode", float(cfg.ctx.sum()) * cfg.Hkv)},
            "launches_per_step": 2 if splits > 1 else 1}
+    # the same cache, 4 new query tokens per sequence (multi-token decode through
+    # attn_with_kvcache; the last 4 cached tokens are the new ones)
+    Sq = 4
+    g = torch.Generator(device=device).manual_seed(4321)
+    q4 = torch.randn(cfg.batch, Sq, cfg.Hq, cfg.D, device=device, generator=g).to(torch.bfloat16)
+    ws4 = torch.empty(av.lib().attn_kvcache_workspace_size(cfg.batch, Sq, cfg.Hq, cfg.Hkv, cfg.D, mx),
+                      dtype=torch.uint8, device=device)
+    out4 = torch.empty_like(q4)
+
+    def step4():
+        av.attn_with_kvcache(q4, kc, vc, cs, bt, cfg.scale, max_cache_seqlen=mx, out=out4, workspace=ws4)
+    for _ in range(warmup):
+        step4()
+    torch.cuda.synchronize()
+    ms4 = time_steps(step4, steps, flush)
+    t4 = float(np.mean(ms4)) / 1e3
+    fl4 = workloads.prefill_flops(np.full(cfg.batch, Sq), cfg.ctx, cfg.Hq, cfg.D)
+    res["kvcache_4_tokens"] = {
+        "workload": "c4_decode cache, 4 new query tokens per sequence (attn_with_kvcache: fp16 V' pre-pass + "
+                    "paged prefill kernel)",
+        "value": nbytes / t4 / 1e9, "unit": "GB/s", "tflops": fl4 / t4 / 1e12, "ms_per_step": t4 * 1e3,
+        "frac_hbm": nbytes / t4 / 1e9 / peaks["hbm_gbs"], "launches_per_step": 4}
     del kc, vc
     torch.cuda.empty_cache()
     return res
@@ -350,6 +372,42 @@ def bench_prefix(av, device, steps, warmup, flush, peaks):
     del kc, vc
     torch.cuda.empty_cache()
     return res
+
+
+def bench_padded(av, device, steps, warmup, flush, peaks):
+    """c2_varlen_gqa as a padded batch [16, 4096, H, D] with per-sequence lengths."""
+    import torch
+    cfg = workloads.make("c2_varlen_gqa")
+    S = 4096
+    B = cfg.batch
+    q, k, v = cfg.q(), cfg.k(), cfg.v()
+    qp = torch.zeros(B, S, cfg.Hq, cfg.D, dtype=torch.bfloat16)
+    kp = torch.zeros(B, S, cfg.Hkv, cfg.D, dtype=torch.bfloat16)
+    vp = torch.zeros_like(kp)
+    for b in range(B):
+        qp[b, :cfg.lens_q[b]] = q[cfg.cu_q[b]:cfg.cu_q[b + 1]]
+        kp[b, :cfg.lens_k[b]] = k[cfg.cu_k[b]:cfg.cu_k[b + 1]]
+        vp[b, :cfg.lens_k[b]] = v[cfg.cu_k[b]:cfg.cu_k[b + 1]]
+    qp, kp, vp = qp.to(device), kp.to(device), vp.to(device)
+    sq = torch.from_numpy(cfg.lens_q.astype(np.int32)).to(device)
+    sk = torch.from_numpy(cfg.lens_k.astype(np.int32)).to(device)
+    out = torch.empty_like(qp)
+    ws = torch.empty(av.lib().attn_padded_workspace_size(B, S, S, cfg.Hq, cfg.Hkv, cfg.D), dtype=torch.uint8,
+                     device=device)
+
+    def step():
+        av.attn_padded_fwd(qp, kp, vp, sq, sk, cfg.scale, out=out, workspace=ws)
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    ms = time_steps(step, steps, flush)
+    t = float(np.mean(ms)) / 1e3
+    flops = workloads.prefill_flops(cfg.lens_q, cfg.lens_k, cfg.Hq, cfg.D)
+    del qp, kp, vp, out, ws
+    torch.cuda.empty_cache()
+    return {"workload": "c2_varlen_gqa as a padded batch [16, 4096, 32|8, 128] with per-sequence lengths",
+            "value": flops / t / 1e12, "unit": "TFLOP/s", "ms_per_step": t * 1e3,
+            "frac": flops / t / 1e12 / peaks["bf16_tflops"], "launches_per_step": 4}
 
 
 def bench_softmax(av, device, steps, warmup, flush, peaks):
@@ -531,6 +589,7 @@ def main():
         extras["prefix_prefill"] = bench_prefix(av, device, args.steps, args.warmup, flush, peaks)
         extras["long_prefill"] = bench_long(av, device, max(3, args.steps // 3), args.warmup, flush, peaks)
         extras["row_softmax"] = bench_softmax(av, device, args.steps, args.warmup, flush, peaks)
+        extras["padded_prefill"] = bench_padded(av, device, args.steps, args.warmup, flush, peaks)
     clocks = sampler.stop()
 
     status, word = av.get_last_device_error()
