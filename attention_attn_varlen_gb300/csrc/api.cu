@@ -131,6 +131,110 @@ int split_tokens_for(int max_len, int splits) {
     return ((per + kDecodeTile - 1) / kDecodeTile) * kDecodeTile;
 }
 
+// Split plan of the decode kernel: the split count for these sizes and the
+// tokens per split (a multiple of the 64-token tile), with splits * tokens
+// covering max_len.
+void decode_plan(int num_sms, int batch, int num_heads_kv, int max_len, int requested, int *splits, int *split_tok) {
+    int s = choose_splits(num_sms, batch, num_heads_kv, max_len, requested);
+    const int tok = split_tokens_for(max_len > 0 ? max_len : 1, s);
+    s = max_len > 0 ? (max_len + tok - 1) / tok : 1;
+    *splits = s < 1 ? 1 : s;
+    *split_tok = tok;
+}
+
+// Bytes of split partials: an fp32 output row and a log-sum-exp per query row,
+// head and split.
+size_t decode_partial_bytes(int batch, int seqlen_q, int num_heads_q, int head_dim, int splits) {
+    return splits > 1 ? (size_t)batch * seqlen_q * num_heads_q * splits * (head_dim + 1) * sizeof(float) : 0;
+}
+
+// The kv-cache entry runs on the decode kernel when the Sq x G query rows of a
+// KV head fit its two n8 column tiles; otherwise on the paged varlen prefill.
+bool kvcache_on_decode(int batch, int seqlen_q, int num_heads_q, int num_heads_kv, int head_dim) {
+    if (num_heads_q <= 0 || num_heads_kv <= 0 || num_heads_q % num_heads_kv) return false;
+    if (head_dim != 64 && head_dim != 128) return false;
+    if (batch > 65535 || num_heads_kv > 65535) return false;
+    return (int64_t)seqlen_q * (num_heads_q / num_heads_kv) <= 16;
+}
+
+struct DecodeCall {
+    const void *q, *k_cache, *v_cache;
+    void *out;
+    float *lse;
+    const int32_t *cache_seqlens, *block_table;
+    int bt_stride, batch, seqlen_q, Hq, Hkv, head_dim, block_size;
+    int64_t num_blocks;
+    int max_len, causal, num_splits;
+    float scale;
+    int64_t q_row_stride, out_row_stride, lse_row_stride, lse_head_stride;
+};
+
+// Host checks shared by the decode-kernel entries (strides already resolved).
+attn_status decode_check(const DecodeCall &c) {
+    if (!c.q || !c.k_cache || !c.v_cache || !c.out || !c.cache_seqlens || !c.block_table) return ATTN_ERR_INVALID_ARG;
+    if (c.batch <= 0 || c.seqlen_q <= 0 || c.Hq <= 0 || c.Hkv <= 0 || c.Hq % c.Hkv != 0) return ATTN_ERR_INVALID_ARG;
+    if (c.max_len < 0 || c.num_splits < 0 || c.bt_stride <= 0) return ATTN_ERR_INVALID_ARG;
+    if (!(c.scale > 0.f) || !isfinite(c.scale)) return ATTN_ERR_INVALID_ARG;
+    if (!pow2(c.block_size) || c.block_size < 16 || c.num_blocks <= 0) return ATTN_ERR_INVALID_ARG;
+    if (c.head_dim != 64 && c.head_dim != 128) return ATTN_ERR_UNSUPPORTED;
+    if ((int64_t)c.seqlen_q * (c.Hq / c.Hkv) > 16) return ATTN_ERR_UNSUPPORTED;
+    if (c.batch > 65535 || c.Hkv > 65535) return ATTN_ERR_UNSUPPORTED;
+    if (c.num_blocks * (int64_t)c.block_size >= (int64_t)INT32_MAX) return ATTN_ERR_UNSUPPORTED;
+    if ((int64_t)c.batch * c.seqlen_q * c.Hq >= (int64_t)INT32_MAX) return ATTN_ERR_UNSUPPORTED;
+    if (!aligned16(c.q) || !aligned16(c.k_cache) || !aligned16(c.v_cache) || !aligned16(c.out))
+        return ATTN_ERR_INVALID_ARG;
+    return ATTN_OK;
+}
+
+// Launch the split and combine kernels.  partials: at least
+// decode_partial_bytes(...) bytes for the given plan, 16-byte aligned (unused
+// with one split).
+attn_status decode_launch(const DecodeCall &c, const DevInfo *d, int splits, int split_tok, float *partials,
+                          void *stream) {
+    DecodeParams p;
+    memset(&p, 0, sizeof p);
+    if (splits > 1) {
+        p.o_part = partials;
+        p.lse_part = partials + (size_t)c.batch * c.seqlen_q * c.Hq * splits * c.head_dim;
+    }
+    const int rpb = c.block_size < kDecodeTile ? c.block_size : kDecodeTile;
+    const int64_t rows = c.num_blocks * (int64_t)c.block_size;
+    const int64_t row_stride = (int64_t)c.Hkv * c.head_dim;
+    CUtensorMap kmap, vmap;
+    if (!make_map(&kmap, c.k_cache, rows, c.Hkv, c.head_dim, row_stride, 1, rpb) ||
+        !make_map(&vmap, c.v_cache, rows, c.Hkv, c.head_dim, row_stride, 1, rpb))
+        return ATTN_ERR_LAUNCH_FAILED;
+    p.q = reinterpret_cast<const __nv_bfloat16 *>(c.q);
+    p.out = reinterpret_cast<__nv_bfloat16 *>(c.out);
+    p.lse = c.lse;
+    p.cache_seqlens = c.cache_seqlens;
+    p.block_table = c.block_table;
+    p.q_row_stride = c.q_row_stride;
+    p.out_row_stride = c.out_row_stride;
+    p.lse_row_stride = c.lse_row_stride;
+    p.lse_head_stride = c.lse_head_stride;
+    p.bt_stride = c.bt_stride;
+    p.block_size = c.block_size;
+    p.rows_per_box = rpb;
+    p.num_splits = splits;
+    p.split_tokens = split_tok;
+    p.num_blocks = c.num_blocks;
+    p.Hq = c.Hq;
+    p.Hkv = c.Hkv;
+    p.G = c.Hq / c.Hkv;
+    p.Sq = c.seqlen_q;
+    p.causal = c.causal ? 1 : 0;
+    p.max_seqlen = c.max_len;
+    p.scale_log2 = c.scale * 1.4426950408889634f;
+    p.err = d->err;
+    cudaError_t e = launch_decode(kmap, vmap, p, c.batch, c.head_dim, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return ATTN_ERR_LAUNCH_FAILED;
+    }
+    return ATTN_OK;
+}
+
 }  // namespace
 
 // measurement hook (see attn_set_kernel_events)
@@ -398,6 +502,15 @@ attn_status attn_padded_fwd(const void *q, const void *k, const void *v, void *o
 size_t attn_kvcache_workspace_size(int batch, int seqlen_q, int num_heads_q, int num_heads_kv, int head_dim,
                                    int max_cache_seqlen) {
     if (batch <= 0 || seqlen_q <= 0 || max_cache_seqlen < 0) return 0;
+    if (kvcache_on_decode(batch, seqlen_q, num_heads_q, num_heads_kv, head_dim)) {
+        // split partials of the decode kernel (never 0: 0 means invalid sizes)
+        DevInfo *d = nullptr;
+        int sms = 148;
+        if (dev_info(&d) == ATTN_OK) sms = d->num_sms;
+        int splits = 1, tok = 0;
+        decode_plan(sms, batch, num_heads_kv, max_cache_seqlen, 0, &splits, &tok);
+        return decode_partial_bytes(batch, seqlen_q, num_heads_q, head_dim, splits) + 256;
+    }
     const size_t v = attn_varlen_workspace_size(batch, num_heads_q, num_heads_kv, head_dim, seqlen_q,
                                                 (int64_t)batch * max_cache_seqlen);
     return v ? kvcache_cu_bytes(batch) + v : 0;
@@ -421,6 +534,18 @@ attn_status attn_kvcache_fwd(const void *q, const void *k_cache, const void *v_c
     attn_status st = dev_info(&d);
     if (st != ATTN_OK) return st;
     if ((st = check_arch(d)) != ATTN_OK) return st;
+    if (kvcache_on_decode(batch, seqlen_q, num_heads_q, num_heads_kv, head_dim)) {
+        // Sq x G query rows per KV head fit the decode kernel: stream the cache
+        // once, no fp16 copy of V.  lse is [Hq, batch * seqlen_q].
+        DecodeCall c = {q, k_cache, v_cache, out, lse, cache_seqlens, block_table, block_table_stride, batch,
+                        seqlen_q, num_heads_q, num_heads_kv, head_dim, block_size, num_blocks, max_cache_seqlen,
+                        causal, 0, softmax_scale, (int64_t)num_heads_q * head_dim, (int64_t)num_heads_q * head_dim,
+                        1, (int64_t)batch * seqlen_q};
+        if ((st = decode_check(c)) != ATTN_OK) return st;
+        int splits = 1, split_tok = 0;
+        decode_plan(d->num_sms, batch, num_heads_kv, max_cache_seqlen, 0, &splits, &split_tok);
+        return decode_launch(c, d, splits, split_tok, reinterpret_cast<float *>(workspace), stream);
+    }
     int32_t *cu_q = reinterpret_cast<int32_t *>(workspace);
     int32_t *cu_k = cu_q + (batch + 1);
     const size_t cu_b = kvcache_cu_bytes(batch);
@@ -468,12 +593,13 @@ int attn_decode_num_splits(int batch, int num_heads_kv, int max_cache_seqlen, in
 size_t attn_decode_workspace_size(int batch, int num_heads_q, int num_heads_kv, int head_dim, int max_cache_seqlen,
                                   int num_splits) {
     if (batch <= 0 || num_heads_q <= 0 || num_heads_kv <= 0 || head_dim <= 0) return 0;
-    const int s = attn_decode_num_splits(batch, num_heads_kv, max_cache_seqlen, num_splits);
-    if (s <= 1) return 0;
-    const int splits = (max_cache_seqlen + split_tokens_for(max_cache_seqlen, s) - 1) /
-                       split_tokens_for(max_cache_seqlen, s);
+    DevInfo *d = nullptr;
+    int sms = 148;
+    if (dev_info(&d) == ATTN_OK) sms = d->num_sms;
+    int splits = 1, tok = 0;
+    decode_plan(sms, batch, num_heads_kv, max_cache_seqlen, num_splits, &splits, &tok);
     if (splits <= 1) return 0;
-    return (size_t)batch * num_heads_q * splits * (head_dim + 1) * sizeof(float) + 256;
+    return decode_partial_bytes(batch, 1, num_heads_q, head_dim, splits) + 256;
 }
 
 attn_status attn_decode_paged(const void *q, const void *k_cache, const void *v_cache, void *out, float *lse,
@@ -482,72 +608,25 @@ attn_status attn_decode_paged(const void *q, const void *k_cache, const void *v_
                               int64_t num_blocks, int max_cache_seqlen, float softmax_scale, int num_splits,
                               int64_t q_row_stride, int64_t out_row_stride, void *workspace, size_t workspace_bytes,
                               void *stream) {
-    if (!q || !k_cache || !v_cache || !out || !cache_seqlens || !block_table) return ATTN_ERR_INVALID_ARG;
-    if (batch <= 0 || num_heads_q <= 0 || num_heads_kv <= 0 || num_heads_q % num_heads_kv != 0)
-        return ATTN_ERR_INVALID_ARG;
-    if (max_cache_seqlen < 0 || num_splits < 0 || block_table_stride <= 0) return ATTN_ERR_INVALID_ARG;
-    if (!(softmax_scale > 0.f) || !isfinite(softmax_scale)) return ATTN_ERR_INVALID_ARG;
-    if (!pow2(block_size) || block_size < 16 || num_blocks <= 0) return ATTN_ERR_INVALID_ARG;
-    if (head_dim != 64 && head_dim != 128) return ATTN_ERR_UNSUPPORTED;
-    const int G = num_heads_q / num_heads_kv;
-    if (G > 8) return ATTN_ERR_UNSUPPORTED;
-    if (batch > 65535 || num_heads_kv > 65535) return ATTN_ERR_UNSUPPORTED;
-    if (num_blocks * (int64_t)block_size >= (int64_t)INT32_MAX) return ATTN_ERR_UNSUPPORTED;
-    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out)) return ATTN_ERR_INVALID_ARG;
-    if (!fix_stride(&q_row_stride, (int64_t)num_heads_q * head_dim) ||
-        !fix_stride(&out_row_stride, (int64_t)num_heads_q * head_dim))
-        return ATTN_ERR_INVALID_ARG;
-
-    DevInfo *d = nullptr;
-    attn_status st = dev_info(&d);
+    DecodeCall c = {q, k_cache, v_cache, out, lse, cache_seqlens, block_table, block_table_stride, batch, 1,
+                    num_heads_q, num_heads_kv, head_dim, block_size, num_blocks, max_cache_seqlen, 1, num_splits,
+                    softmax_scale, q_row_stride, out_row_stride, num_heads_q, 1};
+    attn_status st = decode_check(c);
     if (st != ATTN_OK) return st;
+    if (!fix_stride(&c.q_row_stride, (int64_t)num_heads_q * head_dim) ||
+        !fix_stride(&c.out_row_stride, (int64_t)num_heads_q * head_dim))
+        return ATTN_ERR_INVALID_ARG;
+    DevInfo *d = nullptr;
+    if ((st = dev_info(&d)) != ATTN_OK) return st;
     if ((st = check_arch(d)) != ATTN_OK) return st;
-
-    int splits = choose_splits(d->num_sms, batch, num_heads_kv, max_cache_seqlen, num_splits);
-    const int split_tok = split_tokens_for(max_cache_seqlen > 0 ? max_cache_seqlen : 1, splits);
-    splits = max_cache_seqlen > 0 ? (max_cache_seqlen + split_tok - 1) / split_tok : 1;
-    if (splits < 1) splits = 1;
-
-    DecodeParams p;
-    memset(&p, 0, sizeof p);
+    int splits = 1, split_tok = 0;
+    decode_plan(d->num_sms, batch, num_heads_kv, max_cache_seqlen, num_splits, &splits, &split_tok);
     if (splits > 1) {
-        const size_t need = (size_t)batch * num_heads_q * splits * (head_dim + 1) * sizeof(float);
-        if (!workspace || workspace_bytes < need) return ATTN_ERR_WORKSPACE_TOO_SMALL;
+        if (!workspace || workspace_bytes < decode_partial_bytes(batch, 1, num_heads_q, head_dim, splits))
+            return ATTN_ERR_WORKSPACE_TOO_SMALL;
         if ((reinterpret_cast<uintptr_t>(workspace) & 15u) != 0) return ATTN_ERR_INVALID_ARG;
-        p.o_part = reinterpret_cast<float *>(workspace);
-        p.lse_part = p.o_part + (size_t)batch * num_heads_q * splits * head_dim;
     }
-    const int rpb = block_size < kDecodeTile ? block_size : kDecodeTile;
-    const int64_t rows = num_blocks * (int64_t)block_size;
-    const int64_t row_stride = (int64_t)num_heads_kv * head_dim;
-    CUtensorMap kmap, vmap;
-    if (!make_map(&kmap, k_cache, rows, num_heads_kv, head_dim, row_stride, 1, rpb) ||
-        !make_map(&vmap, v_cache, rows, num_heads_kv, head_dim, row_stride, 1, rpb))
-        return ATTN_ERR_LAUNCH_FAILED;
-    p.q = reinterpret_cast<const __nv_bfloat16 *>(q);
-    p.out = reinterpret_cast<__nv_bfloat16 *>(out);
-    p.lse = lse;
-    p.cache_seqlens = cache_seqlens;
-    p.block_table = block_table;
-    p.q_row_stride = q_row_stride;
-    p.out_row_stride = out_row_stride;
-    p.bt_stride = block_table_stride;
-    p.block_size = block_size;
-    p.rows_per_box = rpb;
-    p.num_splits = splits;
-    p.split_tokens = split_tok;
-    p.num_blocks = num_blocks;
-    p.Hq = num_heads_q;
-    p.Hkv = num_heads_kv;
-    p.G = G;
-    p.scale_log2 = softmax_scale * 1.4426950408889634f;
-    p.err = d->err;
-    cudaError_t e = launch_decode(kmap, vmap, p, batch, head_dim, reinterpret_cast<cudaStream_t>(stream));
-    if (e != cudaSuccess) {
-        cudaGetLastError();
-        return ATTN_ERR_LAUNCH_FAILED;
-    }
-    return ATTN_OK;
+    return decode_launch(c, d, splits, split_tok, reinterpret_cast<float *>(workspace), stream);
 }
 
 // ---------------------------------------------------------------------------
@@ -557,25 +636,16 @@ attn_status attn_decode_paged_noalloc(const void *q, const void *k_cache, const 
                                       int head_dim, int block_size, int64_t num_blocks, int max_cache_seqlen,
                                       float softmax_scale, int num_splits, int64_t q_row_stride,
                                       int64_t out_row_stride, void *stream) {
-    if (!q || !k_cache || !v_cache || !out || !cache_seqlens || !block_table) return ATTN_ERR_INVALID_ARG;
-    if (batch <= 0 || num_heads_q <= 0 || num_heads_kv <= 0 || num_heads_q % num_heads_kv != 0)
-        return ATTN_ERR_INVALID_ARG;
-    if (max_cache_seqlen < 0 || num_splits < 0 || block_table_stride <= 0) return ATTN_ERR_INVALID_ARG;
-    if (!(softmax_scale > 0.f) || !isfinite(softmax_scale)) return ATTN_ERR_INVALID_ARG;
-    if (!pow2(block_size) || block_size < 16 || num_blocks <= 0) return ATTN_ERR_INVALID_ARG;
-    if (head_dim != 64 && head_dim != 128) return ATTN_ERR_UNSUPPORTED;
-    const int G = num_heads_q / num_heads_kv;
-    if (G > 8) return ATTN_ERR_UNSUPPORTED;
-    if (batch > 65535 || num_heads_kv > 65535) return ATTN_ERR_UNSUPPORTED;
-    if (num_blocks * (int64_t)block_size >= (int64_t)INT32_MAX) return ATTN_ERR_UNSUPPORTED;
-    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out)) return ATTN_ERR_INVALID_ARG;
-    if (!fix_stride(&q_row_stride, (int64_t)num_heads_q * head_dim) ||
-        !fix_stride(&out_row_stride, (int64_t)num_heads_q * head_dim))
-        return ATTN_ERR_INVALID_ARG;
-
-    DevInfo *d = nullptr;
-    attn_status st = dev_info(&d);
+    DecodeCall c = {q, k_cache, v_cache, out, lse, cache_seqlens, block_table, block_table_stride, batch, 1,
+                    num_heads_q, num_heads_kv, head_dim, block_size, num_blocks, max_cache_seqlen, 1, num_splits,
+                    softmax_scale, q_row_stride, out_row_stride, num_heads_q, 1};
+    attn_status st = decode_check(c);
     if (st != ATTN_OK) return st;
+    if (!fix_stride(&c.q_row_stride, (int64_t)num_heads_q * head_dim) ||
+        !fix_stride(&c.out_row_stride, (int64_t)num_heads_q * head_dim))
+        return ATTN_ERR_INVALID_ARG;
+    DevInfo *d = nullptr;
+    if ((st = dev_info(&d)) != ATTN_OK) return st;
     if ((st = check_arch(d)) != ATTN_OK) return st;
     float *scratch = nullptr;
     size_t scratch_bytes = 0;
@@ -583,59 +653,18 @@ attn_status attn_decode_paged_noalloc(const void *q, const void *k_cache, const 
         cudaGetLastError();
         return ATTN_ERR_LAUNCH_FAILED;
     }
-
-    // split partials: [batch, Hq, splits, head_dim] outputs + [batch, Hq, splits] lse
-    const size_t per_split = (size_t)batch * num_heads_q * (head_dim + 1) * sizeof(float);
-    int splits = choose_splits(d->num_sms, batch, num_heads_kv, max_cache_seqlen, num_splits);
-    int split_tok = split_tokens_for(max_cache_seqlen > 0 ? max_cache_seqlen : 1, splits);
-    splits = max_cache_seqlen > 0 ? (max_cache_seqlen + split_tok - 1) / split_tok : 1;
-    if (splits < 1) splits = 1;
-    if (splits > 1 && (size_t)splits * per_split > scratch_bytes) {
+    int splits = 1, split_tok = 0;
+    decode_plan(d->num_sms, batch, num_heads_kv, max_cache_seqlen, num_splits, &splits, &split_tok);
+    if (decode_partial_bytes(batch, 1, num_heads_q, head_dim, splits) > scratch_bytes) {
         if (num_splits > 0) return ATTN_ERR_WORKSPACE_TOO_SMALL;   // the asked split count does not fit
         // library's choice: the largest split count whose partials fit (1 needs none)
+        const size_t per_split = (size_t)batch * num_heads_q * (head_dim + 1) * sizeof(float);
         int fit = (int)(scratch_bytes / per_split);
         if (fit < 2) fit = 1;
         split_tok = split_tokens_for(max_cache_seqlen, fit);
         splits = (max_cache_seqlen + split_tok - 1) / split_tok;
     }
-
-    DecodeParams p;
-    memset(&p, 0, sizeof p);
-    if (splits > 1) {
-        p.o_part = scratch;
-        p.lse_part = scratch + (size_t)batch * num_heads_q * splits * head_dim;
-    }
-    const int rpb = block_size < kDecodeTile ? block_size : kDecodeTile;
-    const int64_t rows = num_blocks * (int64_t)block_size;
-    const int64_t row_stride = (int64_t)num_heads_kv * head_dim;
-    CUtensorMap kmap, vmap;
-    if (!make_map(&kmap, k_cache, rows, num_heads_kv, head_dim, row_stride, 1, rpb) ||
-        !make_map(&vmap, v_cache, rows, num_heads_kv, head_dim, row_stride, 1, rpb))
-        return ATTN_ERR_LAUNCH_FAILED;
-    p.q = reinterpret_cast<const __nv_bfloat16 *>(q);
-    p.out = reinterpret_cast<__nv_bfloat16 *>(out);
-    p.lse = lse;
-    p.cache_seqlens = cache_seqlens;
-    p.block_table = block_table;
-    p.q_row_stride = q_row_stride;
-    p.out_row_stride = out_row_stride;
-    p.bt_stride = block_table_stride;
-    p.block_size = block_size;
-    p.rows_per_box = rpb;
-    p.num_splits = splits;
-    p.split_tokens = split_tok;
-    p.num_blocks = num_blocks;
-    p.Hq = num_heads_q;
-    p.Hkv = num_heads_kv;
-    p.G = G;
-    p.scale_log2 = softmax_scale * 1.4426950408889634f;
-    p.err = d->err;
-    cudaError_t e = launch_decode(kmap, vmap, p, batch, head_dim, reinterpret_cast<cudaStream_t>(stream));
-    if (e != cudaSuccess) {
-        cudaGetLastError();
-        return ATTN_ERR_LAUNCH_FAILED;
-    }
-    return ATTN_OK;
+    return decode_launch(c, d, splits, split_tok, scratch, stream);
 }
 
 // ---------------------------------------------------------------------------

@@ -1,11 +1,13 @@
-// decode.cu -- single-token decode through the paged KV cache
+// decode.cu -- decode through the paged KV cache: one query token per sequence
 // ("从零实现 vLLM (1.3)：如何加速 Attention 计算", section "Decode":
 // flash_attn_with_kvcache(q.unsqueeze(1), k_cache, v_cache, cache_seqlens,
-// block_table, softmax_scale, causal=True)), as a split-KV pass plus an exact
-// log-sum-exp combine.
+// block_table, softmax_scale, causal=True)), or a few (seqlen_q = Sq > 1, the
+// same call with q of shape [B, Sq, H, D] and the bottom-right causal mask:
+// new token t of a sequence with L cached keys sees keys j <= L - Sq + t), as a
+// split-KV pass plus an exact log-sum-exp combine.
 //
 // The work is HBM-bound: every cached K/V byte of a (sequence, KV head) is read
-// once and serves all G = Hq/Hkv query heads of the group.
+// once and serves all Sq x G query rows of the group (G = Hq/Hkv heads).
 //
 // attn_decode_split_kernel: one CTA per (split, KV head, sequence).
 //   warp 4 (lane 0)   TMA producer: 64-token K and V tiles of the split,
@@ -17,14 +19,17 @@
 //                     "FlashAttention 的最终实现": running max, proxy
 //                     denominator, proxy output rescaled by 2^(m_old - m_new)).
 //                     S^T = K Q^T and O^T += V^T P^T run on mma.sync m16n8k16
-//                     with the tokens (then head_dim) in M and the G query
-//                     heads (padded to 8) in N; P^T is moved into the
-//                     B-operand layout with movmatrix.  The four warps' states
-//                     are merged exactly at the end.
-// attn_decode_combine_kernel: one warp per (sequence, query head) merges the
+//                     with the tokens (then head_dim) in M and the Sq x G
+//                     query columns (token-major, padded to one or two n8
+//                     tiles) in N; each column masks the keys past its own
+//                     causal limit.  P^T is moved into the B-operand layout
+//                     with movmatrix.  The four warps' states are merged
+//                     exactly at the end.
+// attn_decode_combine_kernel: one warp per (query row, query head) merges the
 //   split partials: lse = log2 sum_s 2^lse_s, O = sum_s 2^(lse_s - lse) O_s.
 //   This merge is exact because the update is associative ("计算流程（1-Pass
-//   算法与分块）": tiles may be folded in any grouping).
+//   算法与分块）": tiles may be folded in any grouping).  A split that holds no
+//   key a row may see leaves lse_s = -inf and weight 0.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -44,12 +49,13 @@ struct DecSmem {
 };
 
 
-template <int D>
+template <int D, int NT>
 __global__ void __launch_bounds__(kDecThreads) attn_decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
                                                                        const __grid_constant__ CUtensorMap vmap,
                                                                        const DecodeParams p) {
     using S = DecSmem<D>;
     constexpr int KS = D / 16;       // k-steps of the QK^T product
+    constexpr int NC = 8 * NT;       // query columns, padded to whole n8 tiles
     extern __shared__ uint8_t dsmem_raw[];
     uint8_t *ring = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(dsmem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *full = reinterpret_cast<uint64_t *>(ring + S::kRingBytes);
@@ -58,22 +64,23 @@ __global__ void __launch_bounds__(kDecThreads) attn_decode_split_kernel(const __
 
     const int split = blockIdx.x, hkv = blockIdx.y, b = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int L = __ldg(p.cache_seqlens + b);
-    const int s0 = split * p.split_tokens;
-    if (L < 0) {
-        if (threadIdx.x == 0) record_error(p.err, ERR_INDEX | SRC_DECODE);
-        return;
+    const int NQ = p.Sq * p.G;       // live columns: query token t = n / G, head hkv * G + n % G
+    int L = __ldg(p.cache_seqlens + b);
+    if (L < 0 || L > p.max_seqlen) {
+        // outside [0, max_seqlen]: reported once, then clamped
+        if (split == 0 && threadIdx.x == 0) record_error(p.err, ERR_INDEX | SRC_DECODE);
+        L = L < 0 ? 0 : p.max_seqlen;
     }
-    if (split == 0 && threadIdx.x == 0 && (int64_t)L > (int64_t)p.num_splits * p.split_tokens)
-        record_error(p.err, ERR_INDEX | SRC_DECODE);   // longer than the stated max_cache_seqlen
+    const int s0 = split * p.split_tokens;
     if (s0 >= L) {
         // no tokens for this split.  With one split the output is written here.
-        if (p.num_splits == 1 && split == 0 && threadIdx.x < 32 * 4) {
-            for (int i = threadIdx.x; i < p.G * D; i += 128) {
+        if (p.num_splits == 1 && split == 0) {
+            for (int i = threadIdx.x; i < NQ * D; i += kDecThreads) {
                 const int n = i / D, d = i % D;
-                const int h = hkv * p.G + n;
-                p.out[(int64_t)b * p.out_row_stride + (int64_t)h * D + d] = __float2bfloat16(0.f);
-                if (p.lse && d == 0) p.lse[(int64_t)b * p.Hq + h] = -INFINITY;
+                const int h = hkv * p.G + n % p.G;
+                const int64_t row = (int64_t)b * p.Sq + n / p.G;
+                p.out[row * p.out_row_stride + (int64_t)h * D + d] = __float2bfloat16(0.f);
+                if (p.lse && d == 0) p.lse[row * p.lse_row_stride + (int64_t)h * p.lse_head_stride] = -INFINITY;
             }
         }
         return;
@@ -141,22 +148,40 @@ __global__ void __launch_bounds__(kDecThreads) attn_decode_split_kernel(const __
 
     // ---------------------------------------------------------------- consumers
     const int g = lane >> 2, c = lane & 3;
-    // Q^T as B fragments: b0 = Q[n=g][16ks + 2c .. +1], b1 = Q[g][16ks + 2c + 8 .. +9]
-    uint32_t qf[KS][2];
-    {
-        const bool valid = g < p.G;
-        const uint32_t *qrow = reinterpret_cast<const uint32_t *>(p.q + (int64_t)b * p.q_row_stride +
-                                                                  (int64_t)(hkv * p.G + (valid ? g : 0)) * D);
+    // Q^T as B fragments of n-tile nt: b0 = Q[n=8nt+g][16ks + 2c .. +1], b1 = Q[8nt+g][16ks + 2c + 8 .. +9]
+    uint32_t qf[NT][KS][2];
+    // keys at or past kend[nt][j] are masked for this lane's column 8nt + 2c + j:
+    // the end of the split and, causally, the bottom-right limit L - Sq + t + 1
+    int kend[NT][2];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+        const int n = nt * 8 + g;
+        const bool valid = n < NQ;
+        const int64_t qrow_idx = (int64_t)b * p.Sq + (valid ? n / p.G : 0);
+        const uint32_t *qrow = reinterpret_cast<const uint32_t *>(p.q + qrow_idx * p.q_row_stride +
+                                                                  (int64_t)(hkv * p.G + (valid ? n % p.G : 0)) * D);
 #pragma unroll
         for (int ks = 0; ks < KS; ++ks) {
-            qf[ks][0] = valid ? __ldg(qrow + ks * 8 + c) : 0u;
-            qf[ks][1] = valid ? __ldg(qrow + ks * 8 + 4 + c) : 0u;
+            qf[nt][ks][0] = valid ? __ldg(qrow + ks * 8 + c) : 0u;
+            qf[nt][ks][1] = valid ? __ldg(qrow + ks * 8 + 4 + c) : 0u;
+        }
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const int col = nt * 8 + 2 * c + j;
+            int e = s1;
+            if (p.causal && col < NQ) e = min(e, L - p.Sq + col / p.G + 1);
+            kend[nt][j] = e;
         }
     }
-    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-    float o[KS][4];
+    float m[NT][2], l[NT][2];
+    float o[NT][KS][4];
 #pragma unroll
-    for (int i = 0; i < KS; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+    for (int nt = 0; nt < NT; ++nt) {
+        m[nt][0] = m[nt][1] = -INFINITY;
+        l[nt][0] = l[nt][1] = 0.f;
+#pragma unroll
+        for (int i = 0; i < KS; ++i) o[nt][i][0] = o[nt][i][1] = o[nt][i][2] = o[nt][i][3] = 0.f;
+    }
 
     const float sl2 = p.scale_log2;
     bool ok = true;
@@ -184,54 +209,64 @@ __global__ void __launch_bounds__(kDecThreads) attn_decode_split_kernel(const __
                 }
                 __syncwarp();
             }
-            // S^T[16 tokens x 8 heads] = K[16 x D] * Q^T[D x 8]
-            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+            // S^T[16 tokens x 8 columns] = K[16 x D] * Q^T[D x 8], per n-tile
+            float acc[NT][4];
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
             const int arow = r0 + (lane & 7) + ((lane >> 3) & 1) * 8;
 #pragma unroll
             for (int ks = 0; ks < KS; ++ks) {
                 uint32_t a0, a1, a2, a3;
                 const uint32_t addr = kb + (ks / 4) * S::kPanelBytes + sw128_off(arow, (ks % 4) * 2 + (lane >> 4));
                 ldsm_x4(addr, a0, a1, a2, a3);
-                mma_bf16_16816(acc, a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
-            }
-            // scale into the log2 domain, mask tokens past the sequence
-            float s_0 = acc[0] * sl2, s_1 = acc[1] * sl2, s_2 = acc[2] * sl2, s_3 = acc[3] * sl2;
-            if (r0 + g >= nvalid) s_0 = s_1 = -INFINITY;
-            if (r0 + g + 8 >= nvalid) s_2 = s_3 = -INFINITY;
-            float mx0 = fmaxf(s_0, s_2), mx1 = fmaxf(s_1, s_3);
 #pragma unroll
-            for (int sh = 4; sh < 32; sh <<= 1) {
-                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, sh));
-                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, sh));
+                for (int nt = 0; nt < NT; ++nt) mma_bf16_16816(acc[nt], a0, a1, a2, a3, qf[nt][ks][0], qf[nt][ks][1]);
             }
-            const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-            const float a_0 = (m0 == -INFINITY) ? 0.f : ex2(m0 - mn0);
-            const float a_1 = (m1 == -INFINITY) ? 0.f : ex2(m1 - mn1);
-            const float ref0 = (mn0 == -INFINITY) ? 0.f : mn0;
-            const float ref1 = (mn1 == -INFINITY) ? 0.f : mn1;
-            const float p0 = ex2(s_0 - ref0), p2 = ex2(s_2 - ref0);
-            const float p1 = ex2(s_1 - ref1), p3 = ex2(s_3 - ref1);
-            l0 = l0 * a_0 + (p0 + p2);
-            l1 = l1 * a_1 + (p1 + p3);
-            m0 = mn0;
-            m1 = mn1;
+            const int key0 = tok0 + r0 + g, key1 = key0 + 8;
+            uint32_t bp[NT][2], bl[NT][2];
 #pragma unroll
-            for (int i = 0; i < KS; ++i) {
-                o[i][0] *= a_0;
-                o[i][1] *= a_1;
-                o[i][2] *= a_0;
-                o[i][3] *= a_1;
+            for (int nt = 0; nt < NT; ++nt) {
+                // scale into the log2 domain, mask keys past each column's end
+                float s_0 = acc[nt][0] * sl2, s_1 = acc[nt][1] * sl2, s_2 = acc[nt][2] * sl2, s_3 = acc[nt][3] * sl2;
+                if (key0 >= kend[nt][0]) s_0 = -INFINITY;
+                if (key0 >= kend[nt][1]) s_1 = -INFINITY;
+                if (key1 >= kend[nt][0]) s_2 = -INFINITY;
+                if (key1 >= kend[nt][1]) s_3 = -INFINITY;
+                float mx0 = fmaxf(s_0, s_2), mx1 = fmaxf(s_1, s_3);
+#pragma unroll
+                for (int sh = 4; sh < 32; sh <<= 1) {
+                    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, sh));
+                    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, sh));
+                }
+                const float mn0 = fmaxf(m[nt][0], mx0), mn1 = fmaxf(m[nt][1], mx1);
+                const float a_0 = (m[nt][0] == -INFINITY) ? 0.f : ex2(m[nt][0] - mn0);
+                const float a_1 = (m[nt][1] == -INFINITY) ? 0.f : ex2(m[nt][1] - mn1);
+                const float ref0 = (mn0 == -INFINITY) ? 0.f : mn0;
+                const float ref1 = (mn1 == -INFINITY) ? 0.f : mn1;
+                const float p0 = ex2(s_0 - ref0), p2 = ex2(s_2 - ref0);
+                const float p1 = ex2(s_1 - ref1), p3 = ex2(s_3 - ref1);
+                l[nt][0] = l[nt][0] * a_0 + (p0 + p2);
+                l[nt][1] = l[nt][1] * a_1 + (p1 + p3);
+                m[nt][0] = mn0;
+                m[nt][1] = mn1;
+#pragma unroll
+                for (int i = 0; i < KS; ++i) {
+                    o[nt][i][0] *= a_0;
+                    o[nt][i][1] *= a_1;
+                    o[nt][i][2] *= a_0;
+                    o[nt][i][3] *= a_1;
+                }
+                // P^T into the B layout: rows = tokens, cols = query columns -> transpose.
+                // P is carried as bf16 hi + lo terms (about 16 significant bits).
+                const uint32_t h01 = pack_bf16x2(p0, p1), h23 = pack_bf16x2(p2, p3);
+                bp[nt][0] = movmatrix_t(h01);
+                bp[nt][1] = movmatrix_t(h23);
+                bl[nt][0] = movmatrix_t(
+                    pack_bf16x2(p0 - __uint_as_float(h01 << 16), p1 - __uint_as_float(h01 & 0xFFFF0000u)));
+                bl[nt][1] = movmatrix_t(
+                    pack_bf16x2(p2 - __uint_as_float(h23 << 16), p3 - __uint_as_float(h23 & 0xFFFF0000u)));
             }
-            // P^T into the B layout: rows = tokens, cols = heads -> transpose.
-            // P is carried as bf16 hi + lo terms (about 16 significant bits).
-            const uint32_t h01 = pack_bf16x2(p0, p1), h23 = pack_bf16x2(p2, p3);
-            const uint32_t bp0 = movmatrix_t(h01);
-            const uint32_t bp1 = movmatrix_t(h23);
-            const uint32_t bl0 = movmatrix_t(
-                pack_bf16x2(p0 - __uint_as_float(h01 << 16), p1 - __uint_as_float(h01 & 0xFFFF0000u)));
-            const uint32_t bl1 = movmatrix_t(
-                pack_bf16x2(p2 - __uint_as_float(h23 << 16), p3 - __uint_as_float(h23 & 0xFFFF0000u)));
-            // O^T[D x 8] += V^T[D x 16 tokens] * P^T[16 x 8]
+            // O^T[D x 8] += V^T[D x 16 tokens] * P^T[16 x 8], per n-tile
             const int mi = lane >> 3;
             const int vrow = r0 + (lane & 7) + (mi >> 1) * 8;
 #pragma unroll
@@ -239,8 +274,11 @@ __global__ void __launch_bounds__(kDecThreads) attn_decode_split_kernel(const __
                 const int ch = 2 * mt + (mi & 1);
                 uint32_t a0, a1, a2, a3;
                 ldsm_x4_t(vb + (ch / 8) * S::kPanelBytes + sw128_off(vrow, ch % 8), a0, a1, a2, a3);
-                mma_bf16_16816(o[mt], a0, a1, a2, a3, bp0, bp1);
-                mma_bf16_16816(o[mt], a0, a1, a2, a3, bl0, bl1);
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    mma_bf16_16816(o[nt][mt], a0, a1, a2, a3, bp[nt][0], bp[nt][1]);
+                    mma_bf16_16816(o[nt][mt], a0, a1, a2, a3, bl[nt][0], bl[nt][1]);
+                }
             }
             if (tail) fence_proxy_async_smem();
         }
@@ -251,71 +289,82 @@ __global__ void __launch_bounds__(kDecThreads) attn_decode_split_kernel(const __
     // ---------------------------------------------------------------- merge the four warps
     // full per-warp denominators
 #pragma unroll
-    for (int sh = 4; sh < 32; sh <<= 1) {
-        l0 += __shfl_xor_sync(0xffffffffu, l0, sh);
-        l1 += __shfl_xor_sync(0xffffffffu, l1, sh);
+    for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+        for (int sh = 4; sh < 32; sh <<= 1) {
+            l[nt][0] += __shfl_xor_sync(0xffffffffu, l[nt][0], sh);
+            l[nt][1] += __shfl_xor_sync(0xffffffffu, l[nt][1], sh);
+        }
     }
     // all consumer warps are past the ring: reuse stage memory for the merge
     asm volatile("bar.sync 1, 128;" ::: "memory");
     if (*abort_flag) ok = false;
-    float *mo = reinterpret_cast<float *>(ring);          // [4][D][8]
-    float *mm = mo + 4 * D * 8;                           // [4][8]
-    float *ml = mm + 4 * 8;                               // [4][8]
+    float *mo = reinterpret_cast<float *>(ring);          // [4][D][NC]
+    float *mm = mo + 4 * D * NC;                          // [4][NC]
+    float *ml = mm + 4 * NC;                              // [4][NC]
     if (ok) {
 #pragma unroll
-        for (int mt = 0; mt < KS; ++mt) {
-            const int d = mt * 16 + g;
-            mo[(warp * D + d) * 8 + 2 * c] = o[mt][0];
-            mo[(warp * D + d) * 8 + 2 * c + 1] = o[mt][1];
-            mo[(warp * D + d + 8) * 8 + 2 * c] = o[mt][2];
-            mo[(warp * D + d + 8) * 8 + 2 * c + 1] = o[mt][3];
-        }
-        if (g == 0) {
-            mm[warp * 8 + 2 * c] = m0;
-            mm[warp * 8 + 2 * c + 1] = m1;
-            ml[warp * 8 + 2 * c] = l0;
-            ml[warp * 8 + 2 * c + 1] = l1;
+        for (int nt = 0; nt < NT; ++nt) {
+            const int cc = nt * 8 + 2 * c;
+#pragma unroll
+            for (int mt = 0; mt < KS; ++mt) {
+                const int d = mt * 16 + g;
+                mo[(warp * D + d) * NC + cc] = o[nt][mt][0];
+                mo[(warp * D + d) * NC + cc + 1] = o[nt][mt][1];
+                mo[(warp * D + d + 8) * NC + cc] = o[nt][mt][2];
+                mo[(warp * D + d + 8) * NC + cc + 1] = o[nt][mt][3];
+            }
+            if (g == 0) {
+                mm[warp * NC + cc] = m[nt][0];
+                mm[warp * NC + cc + 1] = m[nt][1];
+                ml[warp * NC + cc] = l[nt][0];
+                ml[warp * NC + cc + 1] = l[nt][1];
+            }
         }
     }
     asm volatile("bar.sync 1, 128;" ::: "memory");
     if (!ok) return;
-    for (int i = threadIdx.x; i < p.G * D; i += 128) {
+    for (int i = threadIdx.x; i < NQ * D; i += 128) {
         const int n = i / D, d = i % D;
         float M = -INFINITY;
 #pragma unroll
-        for (int w = 0; w < 4; ++w) M = fmaxf(M, mm[w * 8 + n]);
+        for (int w = 0; w < 4; ++w) M = fmaxf(M, mm[w * NC + n]);
         float Ls = 0.f, O = 0.f;
         if (M != -INFINITY) {
 #pragma unroll
             for (int w = 0; w < 4; ++w) {
-                const float mw = mm[w * 8 + n];
+                const float mw = mm[w * NC + n];
                 const float f = (mw == -INFINITY) ? 0.f : ex2(mw - M);
-                Ls += ml[w * 8 + n] * f;
-                O += mo[(w * D + d) * 8 + n] * f;
+                Ls += ml[w * NC + n] * f;
+                O += mo[(w * D + d) * NC + n] * f;
             }
         }
-        const int h = hkv * p.G + n;
+        const int h = hkv * p.G + n % p.G;
+        const int64_t row = (int64_t)b * p.Sq + n / p.G;
         const float on = Ls > 0.f ? O / Ls : 0.f;
         const float l2 = Ls > 0.f ? M + __log2f(Ls) : -INFINITY;
         if (p.num_splits == 1) {
-            p.out[(int64_t)b * p.out_row_stride + (int64_t)h * D + d] = __float2bfloat16(on);
-            if (p.lse && d == 0) p.lse[(int64_t)b * p.Hq + h] = l2 * 0.69314718055994531f;
+            p.out[row * p.out_row_stride + (int64_t)h * D + d] = __float2bfloat16(on);
+            if (p.lse && d == 0)
+                p.lse[row * p.lse_row_stride + (int64_t)h * p.lse_head_stride] = l2 * 0.69314718055994531f;
         } else {
-            const int64_t row = ((int64_t)b * p.Hq + h) * p.num_splits + split;
-            p.o_part[row * D + d] = on;
-            if (d == 0) p.lse_part[row] = l2;
+            const int64_t prow = (row * p.Hq + h) * p.num_splits + split;
+            p.o_part[prow * D + d] = on;
+            if (d == 0) p.lse_part[prow] = l2;
         }
     }
 }
 
-// One warp per (sequence, query head): exact merge of the split partials.
+// One warp per (query row, query head): exact merge of the split partials.
 template <int D>
 __global__ void __launch_bounds__(128) attn_decode_combine_kernel(const DecodeParams p, int total_rows) {
     const int w = blockIdx.x * 4 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (w >= total_rows) return;
-    const int b = w / p.Hq, h = w % p.Hq;
-    const int L = __ldg(p.cache_seqlens + b);
+    const int per_seq = p.Sq * p.Hq;
+    const int b = w / per_seq, t = (w % per_seq) / p.Hq, h = w % p.Hq;
+    int L = __ldg(p.cache_seqlens + b);
+    L = L < 0 ? 0 : (L > p.max_seqlen ? p.max_seqlen : L);   // the split kernel's clamp
     int ns = L <= 0 ? 0 : (L + p.split_tokens - 1) / p.split_tokens;
     if (ns > p.num_splits) ns = p.num_splits;
     const int64_t row0 = (int64_t)w * p.num_splits;
@@ -335,6 +384,7 @@ __global__ void __launch_bounds__(128) attn_decode_combine_kernel(const DecodePa
     for (int i = 0; i < PER; ++i) acc[i] = 0.f;
     for (int s = 0; s < ns; ++s) {
         const float ws = __shfl_sync(0xffffffffu, s < 32 ? wa : wb, s & 31);
+        if (ws == 0.f) continue;   // warp-uniform; a split that saw no key of this row holds 0 partials
         const float *src = p.o_part + (row0 + s) * D + lane * PER;
         if (PER == 4) {
             const float4 v4 = *reinterpret_cast<const float4 *>(src);
@@ -348,14 +398,16 @@ __global__ void __launch_bounds__(128) attn_decode_combine_kernel(const DecodePa
         }
     }
     const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
-    __nv_bfloat16 *dst = p.out + (int64_t)b * p.out_row_stride + (int64_t)h * D + lane * PER;
+    const int64_t row = (int64_t)b * p.Sq + t;
+    __nv_bfloat16 *dst = p.out + row * p.out_row_stride + (int64_t)h * D + lane * PER;
 #pragma unroll
     for (int i = 0; i < PER; ++i) dst[i] = __float2bfloat16(acc[i] * inv);
     if (p.lse && lane == 0)
-        p.lse[(int64_t)b * p.Hq + h] = Ls > 0.f ? (M + __log2f(Ls)) * 0.69314718055994531f : -INFINITY;
+        p.lse[row * p.lse_row_stride + (int64_t)h * p.lse_head_stride] =
+            Ls > 0.f ? (M + __log2f(Ls)) * 0.69314718055994531f : -INFINITY;
 }
 
-template <int D>
+template <int D, int NT>
 static cudaError_t launch_decode_t(const CUtensorMap &kmap, const CUtensorMap &vmap, const DecodeParams &p,
                                    int batch, cudaStream_t stream) {
     using S = DecSmem<D>;
@@ -363,26 +415,30 @@ static cudaError_t launch_decode_t(const CUtensorMap &kmap, const CUtensorMap &v
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 64 && !attr_done[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(attn_decode_split_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             S::kBytes);
+        cudaError_t e = cudaFuncSetAttribute(attn_decode_split_kernel<D, NT>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, S::kBytes);
         if (e != cudaSuccess) return e;
         attr_done[dev] = true;
     }
     dim3 grid(p.num_splits, p.Hkv, batch);
     main_kernel_event_before(stream);
-    attn_decode_split_kernel<D><<<grid, kDecThreads, S::kBytes, stream>>>(kmap, vmap, p);
+    attn_decode_split_kernel<D, NT><<<grid, kDecThreads, S::kBytes, stream>>>(kmap, vmap, p);
     main_kernel_event_after(stream);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess || p.num_splits == 1) return e;
-    const int rows = batch * p.Hq;
+    const int rows = batch * p.Sq * p.Hq;
     attn_decode_combine_kernel<D><<<(rows + 3) / 4, 128, 0, stream>>>(p, rows);
     return cudaGetLastError();
 }
 
 cudaError_t launch_decode(const CUtensorMap &kmap, const CUtensorMap &vmap, const DecodeParams &p, int batch,
                           int head_dim, cudaStream_t stream) {
-    if (head_dim == 128) return launch_decode_t<128>(kmap, vmap, p, batch, stream);
-    return launch_decode_t<64>(kmap, vmap, p, batch, stream);
+    const bool two = p.Sq * p.G > 8;
+    if (head_dim == 128)
+        return two ? launch_decode_t<128, 2>(kmap, vmap, p, batch, stream)
+                   : launch_decode_t<128, 1>(kmap, vmap, p, batch, stream);
+    return two ? launch_decode_t<64, 2>(kmap, vmap, p, batch, stream)
+               : launch_decode_t<64, 1>(kmap, vmap, p, batch, stream);
 }
 
 }  // namespace attn

@@ -12,17 +12,21 @@
 namespace attn {
 
 struct DecodeParams {
-    const __nv_bfloat16 *q;      // [B, Hq, D], row stride q_row_stride
-    __nv_bfloat16 *out;          // [B, Hq, D], row stride out_row_stride
-    float *lse;                  // [B, Hq] or null
-    float *o_part;               // [B, Hq, S, D]  split partial outputs (normalised)
-    float *lse_part;             // [B, Hq, S]     split partial log2-sum-exp
+    const __nv_bfloat16 *q;      // [B * Sq, Hq, D], row stride q_row_stride
+    __nv_bfloat16 *out;          // [B * Sq, Hq, D], row stride out_row_stride
+    float *lse;                  // null, or element (row, h) at row * lse_row_stride + h * lse_head_stride
+    float *o_part;               // [B * Sq, Hq, S, D]  split partial outputs (normalised)
+    float *lse_part;             // [B * Sq, Hq, S]     split partial log2-sum-exp
     const int32_t *cache_seqlens;
     const int32_t *block_table;
     int64_t q_row_stride, out_row_stride;
+    int64_t lse_row_stride, lse_head_stride;
     int bt_stride, block_size, rows_per_box, num_splits, split_tokens;
     int64_t num_blocks;
     int Hq, Hkv, G;
+    int Sq;                      // query tokens per sequence; Sq * G <= 16
+    int causal;                  // bottom-right: token t sees keys j <= L - Sq + t
+    int max_seqlen;              // cache_seqlens outside [0, max_seqlen] are clamped and reported
     float scale_log2;            // softmax_scale * log2(e)
     uint32_t *err;
 };

@@ -312,11 +312,13 @@ def bench_decode(av, device, steps, warmup, flush, peaks):
     ms4 = time_steps(step4, steps, flush)
     t4 = float(np.mean(ms4)) / 1e3
     fl4 = workloads.prefill_flops(np.full(cfg.batch, Sq), cfg.ctx, cfg.Hq, cfg.D)
+    # 4 tokens x 4 heads = 16 query rows per KV head: the split-KV decode kernel
+    splits4 = av.lib().attn_decode_num_splits(cfg.batch, cfg.Hkv, mx, 0)
     res["kvcache_4_tokens"] = {
-        "workload": "c4_decode cache, 4 new query tokens per sequence (attn_with_kvcache: fp16 V' pre-pass + "
-                    "paged prefill kernel)",
+        "workload": "c4_decode cache, 4 new query tokens per sequence (attn_with_kvcache: split-KV decode kernel "
+                    "with 16 query rows per KV head, bottom-right causal)",
         "value": nbytes / t4 / 1e9, "unit": "GB/s", "tflops": fl4 / t4 / 1e12, "ms_per_step": t4 * 1e3,
-        "frac_hbm": nbytes / t4 / 1e9 / peaks["hbm_gbs"], "launches_per_step": 4}
+        "frac_hbm": nbytes / t4 / 1e9 / peaks["hbm_gbs"], "launches_per_step": 2 if splits4 > 1 else 1}
     del kc, vc
     torch.cuda.empty_cache()
     return res

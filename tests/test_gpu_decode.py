@@ -50,6 +50,8 @@ CASES = [
     (6, [5, 129, 4096, 700, 33], 16, 2, 64, 64, 0),
     (7, [1000, 513], 4, 4, 128, 128, 3),
     (8, [4097, 31, 2500], 24, 8, 128, 16, 0),
+    (9, [300, 2000, 1], 32, 2, 128, 16, 0),     # 16 query heads per KV head: two n8 column tiles
+    (10, [700, 65], 48, 3, 64, 32, 5),
 ]
 
 

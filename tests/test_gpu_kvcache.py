@@ -13,11 +13,19 @@ pytestmark = pytest.mark.gpu
 
 CASES = [
     # seed, ctx, Sq, Hq, Hkv, D, block_size
+    # Sq x G <= 16 query rows per KV head: the split-KV decode kernel
     (61, [37, 5, 300], 1, 32, 8, 128, 16),
     (62, [1000, 257, 0], 2, 32, 8, 128, 256),
     (63, [511, 2048], 7, 8, 8, 128, 64),
+    (68, [254, 3, 1900, 126], 4, 32, 8, 128, 16),    # two n8 column tiles; causal ends straddle split edges
+    (69, [30, 1000, 0], 16, 16, 16, 64, 32),         # G = 1, sixteen new tokens
+    (70, [500, 77], 2, 64, 8, 128, 64),              # G = 8
+    (71, [1200, 5, 64], 1, 32, 2, 128, 16),          # G = 16, one token
+    (72, [64, 0, 191], 3, 16, 4, 64, 16),            # twelve live columns of sixteen
+    # larger Sq x G: the paged varlen prefill
     (64, [90, 700, 1], 64, 16, 2, 64, 32),
     (65, [3000, 129], 130, 32, 8, 128, 128),
+    (73, [400, 20], 5, 32, 8, 128, 64),
 ]
 
 
@@ -58,9 +66,70 @@ def test_kvcache_equals_paged_varlen_bitexact():
     assert torch.equal(lse_k, lse_v)
 
 
-def test_kvcache_seqlen_above_stated_max_is_reported():
-    """A cache_seqlens entry above max_cache_seqlen is clamped and reported, not read past."""
-    cfg = workloads.small_paged(67, ctx=[300, 40], new=[4, 4], Hq=8, Hkv=8, D=128, block_size=64)
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("Sq,Hq,Hkv,D", [(4, 16, 4, 128), (2, 8, 8, 64), (9, 16, 8, 128)])
+def test_kvcache_causal_flag(causal, Sq, Hq, Hkv, D):
+    """causal=False lets every new token see all cached keys (decode kernel and prefill route)."""
+    cfg = workloads.small_paged(74 + Sq, ctx=[300, 64, 5], new=[Sq] * 3, Hq=Hq, Hkv=Hkv, D=D, block_size=32)
+    q = cfg.q()
+    kc, vc, k_new, v_new = _paged_device(cfg)
+    cs, bt = _as_kvcache_args(cfg, kc, vc)
+    av.get_last_device_error()
+    out, lse = av.attn_with_kvcache(q.cuda().view(cfg.batch, Sq, Hq, D), kc, vc, cs, bt, cfg.scale,
+                                    causal=causal, return_lse=True)
+    torch.cuda.synchronize()
+    assert av.get_last_device_error()[0] == 0
+    ref, ref_lse, _ = _paged_oracle(cfg, q, k_new, v_new, list(range(cfg.batch)), causal=causal)
+    assert_close(out.view(-1, Hq, D), ref.reshape(-1, Hq, D), f"kvcache causal={causal} Sq={Sq}")
+    assert_lse_close(lse.t().contiguous(), ref_lse.reshape(-1, Hq), "kvcache lse")
+
+
+@pytest.mark.parametrize("Sq,Hq,Hkv", [(4, 16, 4), (6, 8, 8), (4, 64, 8)])
+def test_kvcache_fewer_keys_than_new_tokens(Sq, Hq, Hkv):
+    """cache_seqlens[b] < seqlen_q: the first new tokens see no key at all (output
+    0, lse -inf) and the rest see a causal prefix of the keys."""
+    cfg = workloads.small_paged(80 + Sq, ctx=[0, 150], new=[Sq, Sq], Hq=Hq, Hkv=Hkv, D=128, block_size=16)
+    q = cfg.q()
+    kc, vc, k_new, v_new = _paged_device(cfg)
+    lens = [2, 150 + Sq]
+    cs = torch.tensor(lens, dtype=torch.int32, device="cuda")
+    bt = torch.from_numpy(cfg.block_table).cuda()
+    av.get_last_device_error()
+    out, lse = av.attn_with_kvcache(q.cuda().view(cfg.batch, Sq, Hq, 128), kc, vc, cs, bt, cfg.scale,
+                                    return_lse=True)
+    torch.cuda.synchronize()
+    assert av.get_last_device_error()[0] == 0
+    ref, ref_lse, _ = _paged_oracle(cfg, q, k_new, v_new, [0, 1], lens_k=lens)
+    o = out.view(-1, Hq, 128)
+    n_empty = Sq - lens[0]            # token t sees keys j <= L - Sq + t: none for t < Sq - L
+    assert torch.equal(o[:n_empty].float().cpu(), torch.zeros(n_empty, Hq, 128))
+    assert torch.isneginf(lse.t()[:n_empty]).all()
+    assert_close(o, ref.reshape(-1, Hq, 128), f"kvcache short Sq={Sq}")
+    assert_lse_close(lse.t().contiguous(), ref_lse.reshape(-1, Hq), "kvcache short lse")
+
+
+def test_kvcache_one_token_equals_decode_bitexact():
+    """With seqlen_q = 1 the kv-cache entry runs the decode kernel on the same
+    split plan as attn_decode_paged: outputs agree bit for bit, lse transposed."""
+    cfg = workloads.small_paged(76, ctx=[700, 90, 1500, 3], new=[1] * 4, Hq=32, Hkv=8, D=128, block_size=64)
+    q = cfg.q()
+    kc, vc, _, _ = _paged_device(cfg)
+    cs, bt = _as_kvcache_args(cfg, kc, vc)
+    mx = int(cfg.lens_k.max())
+    out_k, lse_k = av.attn_with_kvcache(q.cuda().view(cfg.batch, 1, cfg.Hq, cfg.D), kc, vc, cs, bt, cfg.scale,
+                                        max_cache_seqlen=mx, return_lse=True)
+    out_d, lse_d = av.attn_decode_paged(q.cuda(), kc, vc, cs, bt, cfg.scale, max_cache_seqlen=mx,
+                                        return_lse=True)
+    torch.cuda.synchronize()
+    assert torch.equal(out_k.view(-1, cfg.Hq, cfg.D).view(torch.int16), out_d.view(torch.int16))
+    assert torch.equal(lse_k, lse_d.t())
+
+
+@pytest.mark.parametrize("Hq,Hkv", [(8, 8), (64, 8)])
+def test_kvcache_seqlen_above_stated_max_is_reported(Hq, Hkv):
+    """A cache_seqlens entry above max_cache_seqlen is clamped and reported, not
+    read past (Sq x G = 4: decode kernel; 32: prefill route)."""
+    cfg = workloads.small_paged(67, ctx=[300, 40], new=[4, 4], Hq=Hq, Hkv=Hkv, D=128, block_size=64)
     q = cfg.q()
     kc, vc, _, _ = _paged_device(cfg)
     cs, bt = _as_kvcache_args(cfg, kc, vc)

@@ -107,8 +107,9 @@ def _paged_device(cfg):
     return kc, vc, k_new, v_new
 
 
-def _paged_oracle(cfg, q, k_new, v_new, seqs, rows_local=None):
-    """Oracle on a compact pool of `seqs` after its own store of the new tokens."""
+def _paged_oracle(cfg, q, k_new, v_new, seqs, rows_local=None, causal=True, lens_k=None):
+    """Oracle on a compact pool of `seqs` after its own store of the new tokens
+    (lens_k: attended keys per sequence of `seqs`, default all cached ones)."""
     kp, vp, bt = workloads.compact_paged(cfg, seqs)
     # slots of the new tokens of `seqs` in the compact pool
     bs = cfg.block_size
@@ -123,9 +124,9 @@ def _paged_oracle(cfg, q, k_new, v_new, seqs, rows_local=None):
     kb, vb = oracle.store_kvcache(k_new[tok_idx], v_new[tok_idx], kp, vp, slots)
     qs = q[torch.from_numpy(tok_idx)]
     cu_q = workloads.cu_from_lens(cfg.new[seqs])
-    cu_k = workloads.cu_from_lens(cfg.lens_k[seqs])
+    cu_k = workloads.cu_from_lens(cfg.lens_k[seqs] if lens_k is None else np.asarray(lens_k, dtype=np.int64))
     ref, ref_lse = oracle.attn_varlen(qs, kb.reshape(kp.shape), vb.reshape(vp.shape), cu_q, cu_k, cfg.Hq, cfg.Hkv,
-                                      cfg.D, cfg.scale, True, block_table=bt, block_size=bs,
+                                      cfg.D, cfg.scale, causal, block_table=bt, block_size=bs,
                                       num_blocks=kp.shape[0], rows=rows_local)
     return ref, ref_lse, tok_idx
 
