@@ -9,6 +9,7 @@ with the device error status.  No timing, no comparison.
   --op prefill  attn_varlen_fwd (contiguous workloads c1, c2, c5; paged c3)
   --op store    store_kvcache of the new tokens (c3)
   --op decode   attn_decode_paged (c4)
+  --op kvcache  attn_with_kvcache with --sq new query tokens per sequence (c4 cache)
   --seqs N      keep only the first N sequences (smaller captures)
 """
 from __future__ import annotations
@@ -42,7 +43,8 @@ def _trim(cfg, n):
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--workload", required=True, choices=workloads.CONFIG_NAMES)
-    ap.add_argument("--op", required=True, choices=["prefill", "store", "decode"])
+    ap.add_argument("--op", required=True, choices=["prefill", "store", "decode", "kvcache"])
+    ap.add_argument("--sq", type=int, default=4, help="new query tokens per sequence (--op kvcache)")
     ap.add_argument("--iters", type=int, default=3)
     ap.add_argument("--seqs", type=int, default=None)
     a = ap.parse_args(argv)
@@ -69,6 +71,14 @@ def main(argv=None):
             out = torch.empty_like(q)
             for _ in range(a.iters):
                 av.attn_decode_paged(q, kc, vc, cs, bt, cfg.scale, max_cache_seqlen=int(cfg.ctx.max()), out=out)
+        elif a.op == "kvcache":
+            # the last --sq cached tokens of each sequence are its new ones
+            cs = torch.from_numpy(cfg.ctx.astype(np.int32)).to(dev)
+            g = torch.Generator(device=dev).manual_seed(4321)
+            qn = torch.randn(cfg.batch, a.sq, cfg.Hq, cfg.D, device=dev, generator=g).to(torch.bfloat16)
+            out = torch.empty_like(qn)
+            for _ in range(a.iters):
+                av.attn_with_kvcache(qn, kc, vc, cs, bt, cfg.scale, max_cache_seqlen=int(cfg.ctx.max()), out=out)
         else:
             k_new, v_new = cfg.k_new().to(dev), cfg.v_new().to(dev)
             slots = torch.from_numpy(cfg.slot_mapping()).to(dev)

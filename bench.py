@@ -157,6 +157,7 @@ def src_digest(files) -> str:
 KERNEL_SOURCES = {
     "prefill": ["attention_attn_varlen_gb300/csrc/prefill.cu", "attention_attn_varlen_gb300/csrc/common.cuh"],
     "decode": ["attention_attn_varlen_gb300/csrc/decode.cu", "attention_attn_varlen_gb300/csrc/common.cuh"],
+    "decode_sq4": ["attention_attn_varlen_gb300/csrc/decode.cu", "attention_attn_varlen_gb300/csrc/common.cuh"],
     "store": ["attention_attn_varlen_gb300/csrc/store_kvcache.cu"],
 }
 
@@ -309,16 +310,23 @@ def bench_decode(av, device, steps, warmup, flush, peaks):
     for _ in range(warmup):
         step4()
     torch.cuda.synchronize()
-    ms4 = time_steps(step4, steps, flush)
+    ms4, kms4 = time_steps(step4, steps, flush, kernel=True)
     t4 = float(np.mean(ms4)) / 1e3
+    tk4 = float(np.mean(kms4)) / 1e3
     fl4 = workloads.prefill_flops(np.full(cfg.batch, Sq), cfg.ctx, cfg.Hq, cfg.D)
+    nbytes4 = nbytes + 2 * cfg.batch * (Sq - 1) * cfg.Hq * cfg.D * 2    # the extra query and output rows
     # 4 tokens x 4 heads = 16 query rows per KV head: the split-KV decode kernel
     splits4 = av.lib().attn_decode_num_splits(cfg.batch, cfg.Hkv, mx, 0)
     res["kvcache_4_tokens"] = {
         "workload": "c4_decode cache, 4 new query tokens per sequence (attn_with_kvcache: split-KV decode kernel "
                     "with 16 query rows per KV head, bottom-right causal)",
-        "value": nbytes / t4 / 1e9, "unit": "GB/s", "tflops": fl4 / t4 / 1e12, "ms_per_step": t4 * 1e3,
-        "frac_hbm": nbytes / t4 / 1e9 / peaks["hbm_gbs"], "launches_per_step": 2 if splits4 > 1 else 1}
+        "value": nbytes4 / t4 / 1e9, "unit": "GB/s", "tflops": fl4 / t4 / 1e12, "ms_per_step": t4 * 1e3,
+        "algorithmic_bytes": nbytes4,
+        "roofline": {"bound": "hbm", "kernel": "attn_decode_split_kernel", "achieved": nbytes4 / tk4 / 1e9,
+                     "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": nbytes4 / tk4 / 1e9 / peaks["hbm_gbs"],
+                     "kernel_ms": tk4 * 1e3,
+                     "traffic": ncu_traffic("decode_sq4", float(cfg.ctx.sum()) * cfg.Hkv)},
+        "launches_per_step": 2 if splits4 > 1 else 1}
     del kc, vc
     torch.cuda.empty_cache()
     return res
