@@ -130,8 +130,12 @@ ATTN_API size_t attn_varlen_workspace_size(int batch, int num_heads_q, int num_h
  *   k_cache, v_cache  [num_blocks, block_size, num_heads_kv, head_dim]
  *   out          [batch, num_heads_q, head_dim] bf16; row stride out_row_stride
  *   lse          nullable; [batch, num_heads_q] float32
+ *   num_heads_q  a multiple of num_heads_kv, at most 16 query heads per KV
+ *                head (ATTN_ERR_UNSUPPORTED above)
  *   cache_seqlens int32 [batch]: keys 0 .. cache_seqlens[b]-1 are attended
- *                (they include the current token, stored beforehand)
+ *                (they include the current token, stored beforehand); values
+ *                outside [0, max_cache_seqlen] are clamped and reported as
+ *                ATTN_ERR_DEVICE_INDEX
  *   block_table  int32 [batch, block_table_stride]
  *   max_cache_seqlen host-side upper bound of cache_seqlens
  *   num_splits   0 = chosen by the library; otherwise the number of KV splits
@@ -242,10 +246,14 @@ ATTN_API size_t attn_padded_workspace_size(int batch, int seqlen_q, int seqlen_k
  * KV cache ([A] "Decode": flash_attn_with_kvcache(q, k_cache, v_cache,
  * cache_seqlens, block_table, softmax_scale, causal) with q of shape
  * [B, seqlen_q, H, D] and seqlen_q >= 1: chunked append, speculative
- * verification).  It computes cu_seqlens_q = b * seqlen_q and cu_seqlens_k =
- * prefix sums of cache_seqlens on the device, then runs the paged varlen
- * prefill (attn_varlen_fwd).  For seqlen_q = 1, attn_decode_paged is the fast
- * path (split-KV); this entry is correct there too.
+ * verification).  Two routes, chosen from the sizes alone:
+ *  - seqlen_q * (num_heads_q / num_heads_kv) <= 16 and head_dim 64 or 128:
+ *    the split-KV decode kernel of attn_decode_paged with one query column
+ *    per (new token, head); the cache is read once.  With seqlen_q = 1 the
+ *    result equals attn_decode_paged's bit for bit.
+ *  - otherwise: cu_seqlens_q = b * seqlen_q and cu_seqlens_k = prefix sums of
+ *    cache_seqlens are computed on the device, then the paged varlen prefill
+ *    (attn_varlen_fwd) runs.
  *
  *   q, out       [batch * seqlen_q, num_heads_q, head_dim] bf16, packed
  *                (the article's [B, seqlen_q, H, D])
@@ -258,8 +266,10 @@ ATTN_API size_t attn_padded_workspace_size(int batch, int seqlen_q, int seqlen_k
  *                seqlen_q + i; 0 = every cached key
  *   block_table, block_size, num_blocks: as for attn_varlen_fwd (paged mode)
  *   workspace    at least attn_kvcache_workspace_size(...) bytes, 256-byte
- *                aligned.  It holds the fp16 copy of V for batch *
- *                max_cache_seqlen keys, so it grows with the cache length.
+ *                aligned.  On the decode route it holds the split partials
+ *                (at most 64 splits of fp32 rows); on the prefill route the
+ *                fp16 copy of V for batch * max_cache_seqlen keys, so there it
+ *                grows with the cache length.
  * Returns the statuses of attn_varlen_fwd.
  * ------------------------------------------------------------------------ */
 ATTN_API attn_status attn_kvcache_fwd(const void *q, const void *k_cache, const void *v_cache, void *out,
