@@ -20,39 +20,43 @@
 // that share the KV head (row r = token_offset * G + g), so one K/V stream
 // feeds 256 query rows.  Slot B holds the 128/G tokens after slot A.
 //
-// Roles (320 threads):
+// Roles (352 threads):
 //   warps 0-3  softmax for slot A, one thread per row (TMEM lanes 0-127)
 //   warps 4-7  softmax for slot B
 //   warp 8     TMA producer: Q_A, Q_B once, then K_j, V_j tiles through a
-//              4-stage ring (128 keys x head_dim, 128-byte swizzle)
-//   warp 9     TMEM allocator and single-thread MMA issuer
+//              3-stage ring (4 for head_dim 64) of 128 keys x head_dim,
+//              128-byte swizzle, in the order K_0, K_1, V_0, K_2, V_1, ...
+//   warp 9     TMEM allocator and the thread that issues every QK^T
+//   warp 10    the thread that issues every PV
 // TMEM (512 columns): S_A [0,128), S_B [128,256) fp32; O_A, O_B after them.
 //
-// PV runs in fp16: the softmax threads write P' = 16 P as fp16 over the first
-// 64 columns of S, and V comes from an fp16 copy V' = V / 16 made by
-// attn_v_to_f16_kernel before the attention kernel (laid out contiguously by
-// sequence, also for a paged cache).  The product P' V' equals P V, and the
-// weights keep 11 significant bits: with bf16 weights (8 bits) the weight
-// rounding adds about as much error as the bf16 output rounding and the result
-// exceeds a 2e-3 relative RMS error.  One MMA takes A and B of the same type,
-// hence the fp16 copy of V.
+// PV runs in fp16: the softmax threads write P' = 16 P as fp16 into shared
+// memory (one 128 x 128 tile per slot, K-major, 128-byte swizzle), and V comes
+// from an fp16 copy V' = V / 16 made by attn_v_to_f16_kernel before the
+// attention kernel (laid out contiguously by sequence, also for a paged
+// cache).  The product P' V' equals P V, and the weights keep 11 significant
+// bits: with bf16 weights (8 bits) the weight rounding adds about as much error
+// as the bf16 output rounding and the result exceeds a 2e-3 relative RMS error.
+// One MMA takes A and B of the same type, hence the fp16 copy of V.
 //
-// MMA order per key tile j:  S_A(j), PV_B(j-1), S_B(j), PV_A(j)
-// so the tensor core works on one slot while the other slot's softmax runs.
-// Because tcgen05 operations of one thread complete in order, the commit of
-// S_X(j) also covers PV_X(j-1): a softmax thread that sees S_X(j) may rescale
-// O_X safely.
+// Because P' does not live in S's columns, S_X(t+1) can be computed as soon as
+// the softmax threads of slot X have read S_X(t) into registers (s_free), while
+// they still work on it: the QK^T of the next key tile overlaps the softmax of
+// the current one, and the two slots need no fixed phase.  PV_X(t) starts when
+// P'_X(t) is in shared memory (p_ready); the softmax of tile t+1 computes its
+// exponentials first and waits for PV_X(t) to finish (pv_done) only before it
+// overwrites P'_X or rescales O_X.  The two issuing threads feed the tensor
+// core independently; each orders its own work (tcgen05 operations of one
+// thread complete in order) and reports through tcgen05.commit.
 //
-// Persistence: barriers and TMEM are set up once per CTA and the ring, S and P
-// barrier phases run on across units.  The producer warp takes unit indices
+// Persistence: barriers and TMEM are set up once per CTA and the barrier
+// phases run on across units.  The producer warp takes unit indices
 // (atomicAdd) and hands them to the other roles through a two-entry ring in
-// shared memory.  The producer loads the next unit's Q as
-// soon as the current unit's last QK^T has read Q (q_empty), and K/V tiles of
-// the next unit as ring slots free up, so the tensor core starts the next unit
-// while the softmax warps store the current one's output.  The first PV_X of a
-// unit waits until the epilogue of slot X has read O_X (o_empty).  MMA and
-// softmax commit / wait o_full and o_empty once per unit, which keeps their
-// phases in step.
+// shared memory.  The producer loads the next unit's Q as soon as the current
+// unit's last QK^T has read Q (q_empty), and K/V tiles of the next unit as ring
+// slots free up, so the tensor core starts the next unit while the softmax
+// warps store the current one's output.  The first PV of a unit waits until
+// both slots' epilogues have read O (o_empty).
 //
 // The rescale is lazy: the reference max of a row moves only when the tile
 // max exceeds it by more than 8 (log2 units), so P stays <= 256 and O is
@@ -63,20 +67,24 @@
 
 namespace attn {
 
-constexpr int kPfThreads = 320;
-constexpr int kPfStages = 4;
+constexpr int kPfThreads = 352;
 constexpr int BM = kPrefillSlotRows;   // 128 rows per slot
 constexpr int BN = kPrefillKeyTile;    // 128 keys per tile
+constexpr int kPBytes = BM * BN * 2;   // one slot's P' tile (fp16)
+constexpr int kPPanelBytes = BM * 128; // 64 keys of P' per 128-byte-swizzled panel
 
 template <int D>
 struct PfSmem {
+    static constexpr int kStages = D == 128 ? 3 : 4;          // K / V' ring stages
     static constexpr int kPanels = D / 64;
     static constexpr int kPanelBytes = 128 * 128;            // 128 rows x 128 B
     static constexpr int kTileBytes = kPanels * kPanelBytes; // one Q slot, K tile or V tile
     static constexpr int kRingOff = 2 * kTileBytes;
-    static constexpr int kBarOff = kRingOff + kPfStages * kTileBytes;
-    static constexpr int kNumBars = 2 * kPfStages + 16;
+    static constexpr int kPOff = kRingOff + kStages * kTileBytes;
+    static constexpr int kBarOff = kPOff + 2 * kPBytes;
+    static constexpr int kNumBars = 2 * kStages + 24;
     static constexpr int kBytes = kBarOff + kNumBars * 8 + 16 + 1024 /*align slack*/;
+    static_assert(kBytes <= 227 * 1024, "shared memory");
 };
 
 template <int D>
@@ -90,15 +98,17 @@ __device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t q_base, uint3
     }
 }
 
-// O (+)= P' V': fp16 operands, P' from TMEM, V' (MN-major) from shared memory
+// O (+)= P' V': fp16 operands from shared memory, P' K-major (keys along the
+// 128-byte rows), V' MN-major
 template <int D>
-__device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint32_t v_base, bool accumulate) {
+__device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_base, uint32_t v_base, bool accumulate) {
     using S = PfSmem<D>;
     constexpr uint32_t idesc = idesc_f16_f32(BM, D, 1);
 #pragma unroll
     for (int kk = 0; kk < BN / 16; ++kk) {
+        const uint64_t pd = sw128_desc(p_base + (kk / 4) * kPPanelBytes + (kk % 4) * 32, 16, 1024);
         const uint64_t vd = sw128_desc(v_base + kk * 16 * 128, S::kPanelBytes, 1024);
-        tc_mma_ts(d_tmem, p_tmem + kk * 8, vd, idesc, (accumulate || kk > 0) ? 1u : 0u);
+        tc_mma_ss(d_tmem, pd, vd, idesc, (accumulate || kk > 0) ? 1u : 0u);
     }
 }
 
@@ -318,21 +328,25 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     attn_prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                         const __grid_constant__ CUtensorMap vmap, const PrefillParams p) {
     using S = PfSmem<D>;
+    constexpr int ST = S::kStages;
     extern __shared__ uint8_t psmem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(psmem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *sQ = sm;
     uint8_t *sRing = sm + S::kRingOff;
+    uint8_t *sP = sm + S::kPOff;                   // P'_A, P'_B
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + S::kBarOff);
     uint64_t *q_full = bars;
     uint64_t *q_empty = bars + 1;                  // this unit's QK^T have read Q
     uint64_t *full = bars + 2;
-    uint64_t *empty = full + kPfStages;
-    uint64_t *s_full = empty + kPfStages;          // [2]
-    uint64_t *p_ready = s_full + 2;                // [2]
-    uint64_t *o_full = p_ready + 2;                // [2]: O_X of this unit complete
+    uint64_t *empty = full + ST;
+    uint64_t *s_full = empty + ST;                 // [2]: S_X(t) in TMEM
+    uint64_t *s_free = s_full + 2;                 // [2]: the softmax has read S_X(t)
+    uint64_t *p_ready = s_free + 2;                // [2]: P'_X(t) in shared memory (and O_X rescaled)
+    uint64_t *pv_done = p_ready + 2;               // [2]: PV_X(t) complete
+    uint64_t *o_full = pv_done + 2;                // [2]: O_X of this unit complete
     uint64_t *o_empty = o_full + 2;                // [2]: the epilogue has read O_X
-    uint64_t *drain_bar = o_empty + 2;
-    uint64_t *idx_full = drain_bar + 1;            // [2]: unit_idx[s] written
+    uint64_t *drain = o_empty + 2;                 // [2]: per issuing thread
+    uint64_t *idx_full = drain + 2;                // [2]: unit_idx[s] written
     uint64_t *idx_empty = idx_full + 2;            // [2]: every role has read unit_idx[s]
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + S::kNumBars);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
@@ -346,20 +360,20 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     if (threadIdx.x == 0) {
         mbar_init(q_full, 1);
         mbar_init(q_empty, 1);
-        for (int i = 0; i < kPfStages; ++i) {
+        for (int i = 0; i < ST; ++i) {
             mbar_init(&full[i], 1);
             mbar_init(&empty[i], 1);
         }
         for (int x = 0; x < 2; ++x) {
             mbar_init(&s_full[x], 1);
+            mbar_init(&s_free[x], 128);
             mbar_init(&p_ready[x], 128);
+            mbar_init(&pv_done[x], 1);
             mbar_init(&o_full[x], 1);
             mbar_init(&o_empty[x], 128);
-        }
-        mbar_init(drain_bar, 1);
-        for (int x = 0; x < 2; ++x) {
+            mbar_init(&drain[x], 1);
             mbar_init(&idx_full[x], 1);
-            mbar_init(&idx_empty[x], 1 + 256);   // the MMA thread and every softmax thread
+            mbar_init(&idx_empty[x], 2 + 256);   // both MMA threads and every softmax thread
         }
         *abort_flag = 0;
         fence_mbar_init();
@@ -423,17 +437,30 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                     mbar_arrive(q_full);
                 }
             }
+            // ring order K_0, K_1, V_0, K_2, V_1, ..., K_{n-1}, V_{n-2}, V_{n-1}: each K tile
+            // one step ahead of the V tile it pairs with, so the next QK^T's tile can
+            // land while the PV of the current one still holds its stage
             for (int j = 0; j < w.n && ok; ++j) {
-                for (int wv = 0; wv < 2; ++wv) {   // 0: K tile, 1: V tile
-                    const int st = it % kPfStages;
-                    const uint32_t ph = (uint32_t)(it / kPfStages) & 1u;
+                for (int step = 0; step < 3; ++step) {
+                    int wv, tj;   // 0: K tile, 1: V tile; key tile index
+                    if (step == 0) {
+                        if (j > 0) continue;
+                        wv = 0, tj = 0;
+                    } else if (step == 1) {
+                        if (j + 1 >= w.n) continue;
+                        wv = 0, tj = j + 1;
+                    } else {
+                        wv = 1, tj = j;
+                    }
+                    const int st = it % ST;
+                    const uint32_t ph = (uint32_t)(it / ST) & 1u;
                     got = 1;
                     if (lane == 0) got = mbar_wait(&empty[st], ph ^ 1u, abort_flag, p.err, SRC_PREFILL);
                     got = __shfl_sync(0xffffffffu, got, 0);
                     if (!got) { ok = false; break; }
                     uint8_t *dst = sRing + st * S::kTileBytes;
                     const CUtensorMap *map = wv ? &vmap : &kmap;
-                    const int key0 = j * BN;
+                    const int key0 = tj * BN;
                     uint64_t *bar = &full[st];
                     if (lane == 0) {
                         mbar_arrive_expect_tx(bar, (uint32_t)S::kTileBytes);
@@ -468,18 +495,19 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         }
         if (lane == 0) {
             // every copy issued here lands before the CTA may exit
-            for (int t = it - kPfStages < 0 ? 0 : it - kPfStages; t < it; ++t)
-                mbar_wait(&full[t % kPfStages], (uint32_t)(t / kPfStages) & 1u, nullptr, p.err, SRC_PREFILL);
+            for (int t = it - ST < 0 ? 0 : it - ST; t < it; ++t)
+                mbar_wait(&full[t % ST], (uint32_t)(t / ST) & 1u, nullptr, p.err, SRC_PREFILL);
             if (k > 0) mbar_wait(q_full, (uint32_t)(k - 1) & 1u, nullptr, p.err, SRC_PREFILL);
         }
     } else if (warp == 9) {
-        // ================================================================ MMA issuer
+        // ================================================================ QK^T issuer
+        // S_X(t) may be issued as soon as the softmax of slot X has read S_X(t-1)
+        // into registers: P' lives in shared memory, so S_X does not wait for PV.
         if (lane == 0) {
-            const uint32_t tS0 = tmem, tS1 = tmem + 128;
-            const uint32_t tO0 = tmem + 256, tO1 = tmem + 256 + D;
-            const uint32_t qA = smem_u32(sQ), qB = smem_u32(sQ + S::kTileBytes);
+            const uint32_t tS[2] = {tmem, tmem + 128};
+            const uint32_t qX[2] = {smem_u32(sQ), smem_u32(sQ + S::kTileBytes)};
             const uint32_t ring = smem_u32(sRing);
-            int itb = 0, cA = 0, cB = 0, k = 0;   // ring items, P' tiles of A / B before this unit
+            int itb = 0, tc[2] = {0, 0}, k = 0;   // ring items before this unit; S tiles issued per slot
             bool ok = true;
             for (;; ++k) {
                 ok = mbar_wait(&idx_full[k & 1], (uint32_t)(k >> 1) & 1u, abort_flag, p.err, SRC_PREFILL);
@@ -488,74 +516,86 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                 mbar_arrive(&idx_empty[k & 1]);
                 if (u < 0) break;
                 const PfUnit w = pf_unit(p, u);
-                const int n = w.n, nA = w.nA, nB = w.nB;
+                const int nX[2] = {w.nA, w.nB};
                 ok = mbar_wait(q_full, (uint32_t)k & 1u, abort_flag, p.err, SRC_PREFILL);
                 if (!ok) break;
                 tc_fence_after();
-                for (int j = 0; j <= n && ok; ++j) {
-                    const int itK = itb + 2 * j, stK = itK % kPfStages;
-                    const int itV = itb + 2 * j + 1, stV = itV % kPfStages;
-                    if (j < n) {
-                        ok = mbar_wait(&full[stK], (uint32_t)(itK / kPfStages) & 1u, abort_flag, p.err, SRC_PREFILL);
+                for (int j = 0; j < w.n && ok; ++j) {
+                    const int itK = itb + (j == 0 ? 0 : 2 * j - 1), stK = itK % ST;   // the producer's ring order
+                    ok = mbar_wait(&full[stK], (uint32_t)(itK / ST) & 1u, abort_flag, p.err, SRC_PREFILL);
+                    if (!ok) break;
+#pragma unroll
+                    for (int x = 0; x < 2; ++x) {
+                        if (j >= nX[x]) continue;
+                        if (tc[x] > 0)
+                            ok = ok && mbar_wait(&s_free[x], (uint32_t)(tc[x] - 1) & 1u, abort_flag, p.err,
+                                                 SRC_PREFILL);
                         if (!ok) break;
                         tc_fence_after();
-                        if (j < nA) {
-                            issue_qk<D>(tS0, qA, ring + stK * S::kTileBytes);
-                            tc_commit(&s_full[0]);
-                        }
+                        issue_qk<D>(tS[x], qX[x], ring + stK * S::kTileBytes);
+                        tc_commit(&s_full[x]);
+                        ++tc[x];
                     }
-                    if (j >= 1 && j - 1 < nB) {
-                        const int jj = j - 1;
-                        const int itP = itb + 2 * jj + 1, stP = itP % kPfStages;
-                        // O_B of the previous unit read by its epilogue
-                        if (jj == 0 && k > 0)
-                            ok = mbar_wait(&o_empty[1], (uint32_t)(k - 1) & 1u, abort_flag, p.err, SRC_PREFILL);
-                        ok = ok &&
-                             mbar_wait(&full[stP], (uint32_t)(itP / kPfStages) & 1u, abort_flag, p.err, SRC_PREFILL) &&
-                             mbar_wait(&p_ready[1], (uint32_t)(cB + jj) & 1u, abort_flag, p.err, SRC_PREFILL);
-                        if (!ok) break;
-                        tc_fence_after();
-                        issue_pv<D>(tO1, tS1, ring + stP * S::kTileBytes, jj > 0);
-                        if (jj == nB - 1) tc_commit(&o_full[1]);
-                        tc_commit(&empty[stP]);
-                    }
-                    if (j < n) {
-                        if (j < nB) {
-                            issue_qk<D>(tS1, qB, ring + stK * S::kTileBytes);
-                            tc_commit(&s_full[1]);
-                        }
-                        tc_commit(&empty[stK]);
-                        if (j == n - 1) tc_commit(q_empty);   // every QK^T of the unit is issued
-                        if (j < nA) {
-                            if (j == 0 && k > 0)
-                                ok = mbar_wait(&o_empty[0], (uint32_t)(k - 1) & 1u, abort_flag, p.err, SRC_PREFILL);
-                            ok = ok &&
-                                 mbar_wait(&full[stV], (uint32_t)(itV / kPfStages) & 1u, abort_flag, p.err,
-                                           SRC_PREFILL) &&
-                                 mbar_wait(&p_ready[0], (uint32_t)(cA + j) & 1u, abort_flag, p.err, SRC_PREFILL);
-                            if (!ok) break;
-                            tc_fence_after();
-                            issue_pv<D>(tO0, tS0, ring + stV * S::kTileBytes, j > 0);
-                            if (j == nA - 1) tc_commit(&o_full[0]);
-                            if (j >= nB) tc_commit(&empty[stV]);
-                        }
-                    }
+                    if (!ok) break;
+                    tc_commit(&empty[stK]);
                 }
                 if (!ok) break;
-                // a slot without key tiles still completes its o_full / o_empty phase
-                for (int x = 0; x < 2 && ok; ++x) {
-                    if ((x ? nB : nA) > 0) continue;
-                    if (k > 0) ok = mbar_wait(&o_empty[x], (uint32_t)(k - 1) & 1u, abort_flag, p.err, SRC_PREFILL);
-                    if (ok) tc_commit(&o_full[x]);
-                }
-                if (n == 0) tc_commit(q_empty);
-                itb += 2 * n;
-                cA += nA;
-                cB += nB;
+                tc_commit(q_empty);   // completes when every QK^T of the unit has read Q
+                itb += 2 * w.n;
             }
             // no MMA may still run when TMEM is released
-            tc_commit(drain_bar);
-            mbar_wait(drain_bar, 0, nullptr, p.err, SRC_PREFILL);
+            tc_commit(&drain[0]);
+            mbar_wait(&drain[0], 0, nullptr, p.err, SRC_PREFILL);
+        }
+        __syncwarp();
+    } else if (warp == 10) {
+        // ================================================================ PV issuer
+        if (lane == 0) {
+            const uint32_t tO[2] = {tmem + 256, tmem + 256 + D};
+            const uint32_t pX[2] = {smem_u32(sP), smem_u32(sP + kPBytes)};
+            const uint32_t ring = smem_u32(sRing);
+            int itb = 0, tc[2] = {0, 0}, k = 0;   // ring items before this unit; PV tiles issued per slot
+            bool ok = true;
+            for (;; ++k) {
+                ok = mbar_wait(&idx_full[k & 1], (uint32_t)(k >> 1) & 1u, abort_flag, p.err, SRC_PREFILL);
+                if (!ok) break;
+                const int u = unit_idx[k & 1];
+                mbar_arrive(&idx_empty[k & 1]);
+                if (u < 0) break;
+                const PfUnit w = pf_unit(p, u);
+                const int nX[2] = {w.nA, w.nB};
+                // O_X of the previous unit read by its epilogue; a slot without key
+                // tiles still completes its o_full phase
+#pragma unroll
+                for (int x = 0; x < 2; ++x) {
+                    if (k > 0)
+                        ok = ok && mbar_wait(&o_empty[x], (uint32_t)(k - 1) & 1u, abort_flag, p.err, SRC_PREFILL);
+                    if (ok && nX[x] == 0) tc_commit(&o_full[x]);
+                }
+                if (!ok) break;
+                for (int j = 0; j < w.n && ok; ++j) {
+                    const int itV = itb + (j < w.n - 1 ? 2 * j + 2 : 2 * w.n - 1), stV = itV % ST;
+                    ok = mbar_wait(&full[stV], (uint32_t)(itV / ST) & 1u, abort_flag, p.err, SRC_PREFILL);
+                    if (!ok) break;
+#pragma unroll
+                    for (int x = 0; x < 2; ++x) {
+                        if (j >= nX[x]) continue;
+                        ok = ok && mbar_wait(&p_ready[x], (uint32_t)tc[x] & 1u, abort_flag, p.err, SRC_PREFILL);
+                        if (!ok) break;
+                        tc_fence_after();
+                        issue_pv<D>(tO[x], pX[x], ring + stV * S::kTileBytes, j > 0);
+                        tc_commit(&pv_done[x]);
+                        if (j == nX[x] - 1) tc_commit(&o_full[x]);
+                        ++tc[x];
+                    }
+                    if (!ok) break;
+                    tc_commit(&empty[stV]);
+                }
+                if (!ok) break;
+                itb += 2 * w.n;
+            }
+            tc_commit(&drain[1]);
+            mbar_wait(&drain[1], 0, nullptr, p.err, SRC_PREFILL);
         }
         __syncwarp();
     } else {
@@ -565,6 +605,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
         const uint32_t tS = tmem + (uint32_t)(X * 128) + lane_off;
         const uint32_t tO = tmem + 256u + (uint32_t)(X * D) + lane_off;
+        uint8_t *prow = sP + X * kPBytes + r * 128;   // this row of P'_X in both 64-key panels
         const float sl2 = p.scale_log2;
         int cX = 0, k = 0;   // S tiles of this slot before this unit
         bool ok = true;
@@ -586,8 +627,9 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             float m_ref = -INFINITY;   // reference max (log2 units) used for P
             float l = 0.f;             // proxy denominator d'
             for (int j = 0; j < nX; ++j) {
+                const int t = cX + j;   // S tiles of this slot so far
                 ok = __all_sync(0xffffffffu,
-                                mbar_wait(&s_full[X], (uint32_t)(cX + j) & 1u, abort_flag, p.err, SRC_PREFILL));
+                                mbar_wait(&s_full[X], (uint32_t)t & 1u, abort_flag, p.err, SRC_PREFILL));
                 if (!ok) break;
                 tc_fence_after();
                 float s[BN];
@@ -596,6 +638,9 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                 tmem_ld32(tS + 64, *reinterpret_cast<uint32_t(*)[32]>(&s[64]));
                 tmem_ld32(tS + 96, *reinterpret_cast<uint32_t(*)[32]>(&s[96]));
                 tc_wait_ld();
+                // S_X is in registers: the tensor core may overwrite it with S_X(t+1)
+                tc_fence_before();
+                mbar_arrive(&s_free[X]);
                 const int key0 = j * BN;
                 if (key0 + BN - 1 > lim) {
 #pragma unroll
@@ -621,27 +666,29 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                     m_ref = m_new;
                 }
                 l *= alpha;
-                // P' = 2^(s*scale*log2e - m_ref + 4) = 16 P, fp16 over the first 64 columns of S;
-                // the row sum in four paired accumulators
+                // P' = 2^(s*scale*log2e - m_ref + 4) = 16 P as fp16, and the row sum in
+                // four paired accumulators
                 const float nref = ((m_ref == -INFINITY) ? 0.f : -m_ref) + 4.0f;
                 float la[4] = {0.f, 0.f, 0.f, 0.f}, lb[4] = {0.f, 0.f, 0.f, 0.f};
+                uint32_t pk[BN / 2];
 #pragma unroll
-                for (int c4 = 0; c4 < BN / 32; ++c4) {
-                    uint32_t pk[16];
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        float x0, x1;
-                        fma2(x0, x1, s[c4 * 32 + 2 * i], s[c4 * 32 + 2 * i + 1], sl2, sl2, nref, nref);
-                        x0 = ex2(x0);
-                        x1 = ex2(x1);
-                        add2(la[i & 3], lb[i & 3], x0, x1);
-                        pk[i] = pack_f16x2(x0, x1);
-                    }
-                    tmem_st16(tS + (uint32_t)(c4 * 16), pk);
+                for (int i = 0; i < BN / 2; ++i) {
+                    float x0, x1;
+                    fma2(x0, x1, s[2 * i], s[2 * i + 1], sl2, sl2, nref, nref);
+                    x0 = ex2(x0);
+                    x1 = ex2(x1);
+                    add2(la[i & 3], lb[i & 3], x0, x1);
+                    pk[i] = pack_f16x2(x0, x1);
                 }
                 l += ((la[0] + lb[0]) + (la[1] + lb[1])) + ((la[2] + lb[2]) + (la[3] + lb[3]));
-                // O *= alpha where the reference moved (O of tile 0 is written, not accumulated);
-                // the commit of S_X(j) covered PV_X(j-1)
+                // PV_X(t-1) has read P'_X and written O_X
+                if (t > 0) {
+                    ok = __all_sync(0xffffffffu, mbar_wait(&pv_done[X], (uint32_t)(t - 1) & 1u, abort_flag, p.err,
+                                                           SRC_PREFILL));
+                    if (!ok) break;
+                    tc_fence_after();
+                }
+                // O *= alpha where the reference moved (O of tile 0 is written, not accumulated)
                 if (j > 0 && __any_sync(0xffffffffu, need)) {
 #pragma unroll
                     for (int c = 0; c < D / 32; ++c) {
@@ -652,8 +699,19 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                         for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
                         tmem_st32(tO + (uint32_t)(c * 32), o);
                     }
+                    tc_wait_st();
                 }
-                tc_wait_st();
+                // P' row into the two 128-byte-swizzled 64-key panels (K-major A operand)
+#pragma unroll
+                for (int pn = 0; pn < 2; ++pn) {
+#pragma unroll
+                    for (int ch = 0; ch < 8; ++ch) {
+                        const int i = pn * 32 + ch * 4;
+                        *reinterpret_cast<uint4 *>(prow + pn * kPPanelBytes + ((ch ^ (r & 7)) << 4)) =
+                            make_uint4(pk[i], pk[i + 1], pk[i + 2], pk[i + 3]);
+                    }
+                }
+                fence_proxy_async_smem();
                 tc_fence_before();
                 mbar_arrive(&p_ready[X]);
             }
