@@ -55,8 +55,10 @@
 // shared memory.  The producer loads the next unit's Q as soon as the current
 // unit's last QK^T has read Q (q_empty), and K/V tiles of the next unit as ring
 // slots free up, so the tensor core starts the next unit while the softmax
-// warps store the current one's output.  The first PV of a unit waits until
-// both slots' epilogues have read O (o_empty).
+// warps finish the current one.  A unit's output rows are written by the
+// softmax threads during the first tile of their next unit, once the last PV
+// of the unit is done and before P'_X(0) of the next one is published, so the
+// wait for that PV overlaps the next tile's exponentials.
 //
 // The rescale is lazy: the reference max of a row moves only when the tile
 // max exceeds it by more than 8 (log2 units), so P stays <= 256 and O is
@@ -323,6 +325,40 @@ __device__ __forceinline__ PfUnit pf_unit(const PrefillParams &p, int u) {
     return w;
 }
 
+// Output rows of one slot (warp-collective; every argument but the row data is
+// warp-uniform where it steers a tcgen05 op): O_X / d' -> bf16, and the lse,
+// read from TMEM when the slot had key tiles, zeros otherwise.
+template <int D>
+__device__ __forceinline__ void pf_store_rows(const PrefillParams &p, uint32_t tO, bool has_tiles, bool row_valid,
+                                              int64_t qrow, int head, float l, float m_ref) {
+    if (!__any_sync(0xffffffffu, row_valid)) return;
+    const float inv = l > 0.f ? 16.f / l : 0.f;   // l accumulated P' = 16 P
+    __nv_bfloat16 *orow = p.out + (row_valid ? qrow : 0) * p.out_row_stride + (int64_t)head * D;
+#pragma unroll
+    for (int c = 0; c < D / 32; ++c) {
+        uint32_t o[32];
+        if (has_tiles) {
+            tmem_ld32(tO + (uint32_t)(c * 32), o);
+            tc_wait_ld();
+        } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = 0u;
+        }
+        if (row_valid) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+                pk[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv, __uint_as_float(o[2 * i + 1]) * inv);
+            uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+        }
+    }
+    if (row_valid && p.lse)
+        p.lse[(int64_t)head * p.total_q + qrow] = l > 0.f ? (m_ref + __log2f(l) - 4.0f) * 0.69314718055994531f
+                                                          : -INFINITY;
+}
+
 template <int D>
 __global__ void __launch_bounds__(kPfThreads, 1)
     attn_prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
@@ -343,9 +379,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     uint64_t *s_free = s_full + 2;                 // [2]: the softmax has read S_X(t)
     uint64_t *p_ready = s_free + 2;                // [2]: P'_X(t) in shared memory (and O_X rescaled)
     uint64_t *pv_done = p_ready + 2;               // [2]: PV_X(t) complete
-    uint64_t *o_full = pv_done + 2;                // [2]: O_X of this unit complete
-    uint64_t *o_empty = o_full + 2;                // [2]: the epilogue has read O_X
-    uint64_t *drain = o_empty + 2;                 // [2]: per issuing thread
+    uint64_t *drain = pv_done + 2;                 // [2]: per issuing thread
     uint64_t *idx_full = drain + 2;                // [2]: unit_idx[s] written
     uint64_t *idx_empty = idx_full + 2;            // [2]: every role has read unit_idx[s]
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + S::kNumBars);
@@ -369,8 +403,6 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             mbar_init(&s_free[x], 128);
             mbar_init(&p_ready[x], 128);
             mbar_init(&pv_done[x], 1);
-            mbar_init(&o_full[x], 1);
-            mbar_init(&o_empty[x], 128);
             mbar_init(&drain[x], 1);
             mbar_init(&idx_full[x], 1);
             mbar_init(&idx_empty[x], 2 + 256);   // both MMA threads and every softmax thread
@@ -564,15 +596,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                 if (u < 0) break;
                 const PfUnit w = pf_unit(p, u);
                 const int nX[2] = {w.nA, w.nB};
-                // O_X of the previous unit read by its epilogue; a slot without key
-                // tiles still completes its o_full phase
-#pragma unroll
-                for (int x = 0; x < 2; ++x) {
-                    if (k > 0)
-                        ok = ok && mbar_wait(&o_empty[x], (uint32_t)(k - 1) & 1u, abort_flag, p.err, SRC_PREFILL);
-                    if (ok && nX[x] == 0) tc_commit(&o_full[x]);
-                }
-                if (!ok) break;
+                // PV_X(0) of a unit writes O_X afresh: its p_ready comes after the
+                // softmax threads have read O_X of the previous unit
                 for (int j = 0; j < w.n && ok; ++j) {
                     const int itV = itb + (j < w.n - 1 ? 2 * j + 2 : 2 * w.n - 1), stV = itV % ST;
                     ok = mbar_wait(&full[stV], (uint32_t)(itV / ST) & 1u, abort_flag, p.err, SRC_PREFILL);
@@ -585,7 +610,6 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                         tc_fence_after();
                         issue_pv<D>(tO[x], pX[x], ring + stV * S::kTileBytes, j > 0);
                         tc_commit(&pv_done[x]);
-                        if (j == nX[x] - 1) tc_commit(&o_full[x]);
                         ++tc[x];
                     }
                     if (!ok) break;
@@ -609,6 +633,13 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         const float sl2 = p.scale_log2;
         int cX = 0, k = 0;   // S tiles of this slot before this unit
         bool ok = true;
+        // The rows of the previous unit are stored once its last PV is done: in
+        // the first tile of the next unit, after the exponentials and before
+        // P'_X(0) is published (so PV_X(0) cannot overwrite O_X before it is read).
+        bool pend = false, pend_tiles = false, pend_valid = false;
+        int64_t pend_qrow = 0;
+        int pend_head = 0;
+        float pend_l = 0.f, pend_m = 0.f;
         for (;; ++k) {
             ok = __all_sync(0xffffffffu,
                             mbar_wait(&idx_full[k & 1], (uint32_t)(k >> 1) & 1u, abort_flag, p.err, SRC_PREFILL));
@@ -688,6 +719,10 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                     if (!ok) break;
                     tc_fence_after();
                 }
+                if (pend) {   // j == 0: O_X holds the previous unit's result
+                    pf_store_rows<D>(p, tO, pend_tiles, pend_valid, pend_qrow, pend_head, pend_l, pend_m);
+                    pend = false;
+                }
                 // O *= alpha where the reference moved (O of tile 0 is written, not accumulated)
                 if (j > 0 && __any_sync(0xffffffffu, need)) {
 #pragma unroll
@@ -716,46 +751,35 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                 mbar_arrive(&p_ready[X]);
             }
             if (!ok) break;
-            cX += nX;
-            // ------------------------------------------------------------ epilogue
-            ok = __all_sync(0xffffffffu, mbar_wait(&o_full[X], (uint32_t)k & 1u, abort_flag, p.err, SRC_PREFILL));
-            if (!ok) break;
-            tc_fence_after();
-            if (__any_sync(0xffffffffu, row_valid)) {
-                const float inv = l > 0.f ? 16.f / l : 0.f;   // l accumulated P' = 16 P
-                __nv_bfloat16 *orow =
-                    p.out + (int64_t)(w.qs + (row_valid ? tok : 0)) * p.out_row_stride + (int64_t)head * D;
-#pragma unroll
-                for (int c = 0; c < D / 32; ++c) {
-                    uint32_t o[32];
-                    if (nX > 0) {
-                        tmem_ld32(tO + (uint32_t)(c * 32), o);
-                        tc_wait_ld();
-                    } else {
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) o[i] = 0u;
-                    }
-                    if (row_valid) {
-                        uint32_t pk[16];
-#pragma unroll
-                        for (int i = 0; i < 16; ++i)
-                            pk[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv, __uint_as_float(o[2 * i + 1]) * inv);
-                        uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
-#pragma unroll
-                        for (int i = 0; i < 4; ++i)
-                            dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
-                    }
+            if (pend) {   // no key tiles for slot X in this unit: store the previous unit's rows now
+                if (cX > 0) {
+                    ok = __all_sync(0xffffffffu, mbar_wait(&pv_done[X], (uint32_t)(cX - 1) & 1u, abort_flag, p.err,
+                                                           SRC_PREFILL));
+                    if (!ok) break;
+                    tc_fence_after();
                 }
-                if (row_valid && p.lse)
-                    p.lse[(int64_t)head * p.total_q + w.qs + tok] =
-                        l > 0.f ? (m_ref + __log2f(l) - 4.0f) * 0.69314718055994531f : -INFINITY;
+                pf_store_rows<D>(p, tO, pend_tiles, pend_valid, pend_qrow, pend_head, pend_l, pend_m);
             }
-            // O_X may be overwritten by the next unit
-            tc_fence_before();
-            mbar_arrive(&o_empty[X]);
+            cX += nX;
+            pend = true;
+            pend_tiles = nX > 0;
+            pend_valid = row_valid;
+            pend_qrow = (int64_t)w.qs + tok;
+            pend_head = head;
+            pend_l = l;
+            pend_m = m_ref;
+        }
+        // the last unit's rows
+        if (ok && pend) {
+            if (cX > 0)
+                ok = __all_sync(0xffffffffu, mbar_wait(&pv_done[X], (uint32_t)(cX - 1) & 1u, abort_flag, p.err,
+                                                       SRC_PREFILL));
+            if (ok) {
+                tc_fence_after();
+                pf_store_rows<D>(p, tO, pend_tiles, pend_valid, pend_qrow, pend_head, pend_l, pend_m);
+            }
         }
     }
-
     tc_fence_before();
     __syncthreads();
     if (warp == 9) {
