@@ -32,7 +32,7 @@
 //
 // PV runs in fp16: the softmax threads write P' = 16 P as fp16 into shared
 // memory (one 128 x 128 tile per slot, K-major, 128-byte swizzle), and V comes
-// from an fp16 copy V' = V / 16 made by attn_v_to_f16_kernel before the
+// from an fp16 copy V' = V / 16 made by attn_prefill_prep_kernel before the
 // attention kernel (laid out contiguously by sequence, also for a paged
 // cache).  The product P' V' equals P V, and the weights keep 11 significant
 // bits: with bf16 weights (8 bits) the weight rounding adds about as much error
@@ -158,7 +158,7 @@ __device__ __forceinline__ bool seq_rows(const PrefillParams &p, int b, bool rep
 constexpr int kCvtThreads = 256;
 constexpr int kCvtKeys = 32;
 
-__global__ void __launch_bounds__(kCvtThreads) attn_v_to_f16_kernel(const PrefillParams p) {
+__device__ __forceinline__ void v_to_f16_keys(const PrefillParams &p) {
     const int b = blockIdx.y;
     int qs, Lq, k0, Lk;
     if (!seq_rows(p, b, false, qs, Lq, k0, Lk)) return;   // reported by the scheduler
@@ -209,17 +209,18 @@ __global__ void __launch_bounds__(kCvtThreads) attn_v_to_f16_kernel(const Prefil
 }
 
 // ---------------------------------------------------------------------------
-// Scheduler: one CTA writes the unit list; CTA i of the attention kernel
-// takes entry i (CTAs past the end exit at once, and they come last).
-// Sequences come longest first (counting sort on their pair count), so the
-// last units launched are short; inside a sequence units are grouped by KV
-// head and run from the last query pair (most key tiles) to the first, so
+// Scheduler (one CTA of the pre-pass launch): writes the unit list that the
+// persistent attention CTAs take entries from, in order, through a global
+// counter.  Sequences come longest first (counting sort on their pair count),
+// so the last units taken are short; inside a sequence units are grouped by
+// KV head and run from the last query pair (most key tiles) to the first, so
 // units running together share one K/V stream in L2.
 // Entry = (sequence, pair | kv_head << 16).  Also flags invalid offsets and
 // sequences longer than max_seqlen_q.
 // ---------------------------------------------------------------------------
-constexpr int kSchedThreads = 1024;
+constexpr int kSchedThreads = kCvtThreads;   // the scheduler is one CTA of the pre-pass kernel
 constexpr int kSchedBuckets = 4096;
+constexpr int kSchedWarps = kSchedThreads / 32;
 
 __device__ __forceinline__ int pf_pairs(const PrefillParams &p, int b, bool report) {
     const int tps = BM / p.G;
@@ -233,9 +234,9 @@ __device__ __forceinline__ int pf_pairs(const PrefillParams &p, int b, bool repo
     return pairs;
 }
 
-__global__ void __launch_bounds__(kSchedThreads) attn_prefill_schedule_kernel(const PrefillParams p) {
+__device__ __forceinline__ void schedule_units(const PrefillParams &p) {
     __shared__ int units_in[kSchedBuckets];   // units per pair-count bucket, then running offsets
-    __shared__ int wsum[kSchedThreads / 32];
+    __shared__ int wsum[kSchedWarps];
     for (int i = threadIdx.x; i < kSchedBuckets; i += kSchedThreads) units_in[i] = 0;
     __syncthreads();
     for (int b = threadIdx.x; b < p.batch; b += kSchedThreads) {
@@ -261,14 +262,14 @@ __global__ void __launch_bounds__(kSchedThreads) attn_prefill_schedule_kernel(co
     if (lane == 31) wsum[wid] = incl;
     __syncthreads();
     if (wid == 0) {
-        const int w = wsum[lane];
+        const int w = lane < kSchedWarps ? wsum[lane] : 0;
         int wi = w;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
             const int y = __shfl_up_sync(0xffffffffu, wi, o);
             if (lane >= o) wi += y;
         }
-        wsum[lane] = wi - w;   // exclusive
+        if (lane < kSchedWarps) wsum[lane] = wi - w;   // exclusive
     }
     __syncthreads();
     int run = wsum[wid] + incl - sum;
@@ -289,6 +290,19 @@ __global__ void __launch_bounds__(kSchedThreads) attn_prefill_schedule_kernel(co
         for (int h = 0; h < p.Hkv; ++h)
             for (int i = 0; i < pairs; ++i) p.units[off++] = make_int2(b, (pairs - 1 - i) | (h << 16));
     }
+}
+
+// ---------------------------------------------------------------------------
+// Pre-pass before the attention kernel, one launch: CTA (0, batch) writes the
+// unit list (schedule_units); CTAs (x, b) with b < batch convert V of
+// sequence b to V' (v_to_f16_keys).
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kCvtThreads) attn_prefill_prep_kernel(const PrefillParams p) {
+    if (blockIdx.y == (unsigned)p.batch) {
+        if (blockIdx.x == 0) schedule_units(p);
+        return;
+    }
+    v_to_f16_keys(p);
 }
 
 // Work of one unit: rows [t0A, t0A + tps) and [t0B, t0B + tps) of sequence b
@@ -877,9 +891,9 @@ static cudaError_t launch_prefill_t(const CUtensorMap &qmap, const CUtensorMap &
         if (e != cudaSuccess) return e;
         attr_done[dev] = true;
     }
-    attn_prefill_schedule_kernel<<<1, kSchedThreads, 0, stream>>>(p);
-    dim3 cgrid((p.max_seqlen_k + kCvtKeys - 1) / kCvtKeys, p.batch);
-    attn_v_to_f16_kernel<<<cgrid, kCvtThreads, 0, stream>>>(p);
+    // unit list and V' in one launch: one extra row of CTAs (y = batch) holds the scheduler
+    dim3 cgrid((p.max_seqlen_k + kCvtKeys - 1) / kCvtKeys, p.batch + 1);
+    attn_prefill_prep_kernel<<<cgrid, kCvtThreads, 0, stream>>>(p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     main_kernel_event_before(stream);

@@ -378,7 +378,7 @@ def bench_prefix(av, device, steps, warmup, flush, peaks):
                         "frac": flops / tk / 1e12 / peaks["bf16_tflops"], "kernel_ms": tk * 1e3, "traffic": None},
            "store_kvcache": {"value": sbytes / ts / 1e9, "unit": "GB/s", "frac": sbytes / ts / 1e9 / peaks["hbm_gbs"],
                              "tokens": int(cfg.new.sum())},
-           "launches_per_step": 4}
+           "launches_per_step": 3}
     del kc, vc
     torch.cuda.empty_cache()
     return res
@@ -417,7 +417,7 @@ def bench_padded(av, device, steps, warmup, flush, peaks):
     torch.cuda.empty_cache()
     return {"workload": "c2_varlen_gqa as a padded batch [16, 4096, 32|8, 128] with per-sequence lengths",
             "value": flops / t / 1e12, "unit": "TFLOP/s", "ms_per_step": t * 1e3,
-            "frac": flops / t / 1e12 / peaks["bf16_tflops"], "launches_per_step": 4}
+            "frac": flops / t / 1e12 / peaks["bf16_tflops"], "launches_per_step": 3}
 
 
 def bench_softmax(av, device, steps, warmup, flush, peaks):
@@ -620,8 +620,8 @@ def main():
                      else "fallback 1.9 PFLOP/s"},
         "e2e": {"value": aggregate(flops, e2e_max / 1e3, world) / 1e12, "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_max},
-        # per step: the unit scheduler, the V fp16 pre-pass and the attention kernel
-        "gpu_launches": 3 * args.steps,
+        # per step: the pre-pass (unit list + fp16 V') and the attention kernel
+        "gpu_launches": 2 * args.steps,
         "clocks": clocks,
         "wall_s_timed": wall,
         "device_status": status,
