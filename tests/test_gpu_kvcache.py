@@ -5,6 +5,7 @@ import pytest
 import torch
 
 import attention_attn_varlen_gb300 as av
+import oracle
 import workloads
 from _util import assert_close, assert_lse_close
 from test_gpu_prefill import _paged_device, _paged_oracle, _run_paged
@@ -139,3 +140,39 @@ def test_kvcache_seqlen_above_stated_max_is_reported(Hq, Hkv):
     torch.cuda.synchronize()
     st, word = av.get_last_device_error()
     assert st == 6, (st, hex(word))   # ATTN_ERR_DEVICE_INDEX
+
+
+def test_kvcache_c4_four_tokens_full_size_sampled():
+    """The 4-token kv-cache step at full size (the 256-sequence decode cache; the
+    last 4 cached tokens of every sequence are its new ones), in the launch
+    configuration the benchmark times; the oracle checks 12 sequences (every
+    new token and head)."""
+    from test_gpu_decode import poison_tail
+    cfg = workloads.make("c4_decode")
+    Sq = 4
+    kc = torch.empty((cfg.num_blocks, cfg.block_size, cfg.Hkv, cfg.D), dtype=torch.bfloat16, device="cuda")
+    vc = torch.empty_like(kc)
+    workloads.fill_paged_cache(cfg, kc, vc)
+    poison_tail(cfg, kc, vc)
+    rng = np.random.default_rng(4321)
+    q4 = torch.from_numpy(rng.standard_normal((cfg.batch, Sq, cfg.Hq, cfg.D), dtype=np.float32)).to(torch.bfloat16)
+    cs = torch.from_numpy(cfg.ctx.astype(np.int32)).cuda()
+    bt = torch.from_numpy(cfg.block_table).cuda()
+    av.get_last_device_error()
+    out, lse = av.attn_with_kvcache(q4.cuda(), kc, vc, cs, bt, cfg.scale, max_cache_seqlen=int(cfg.ctx.max()),
+                                    return_lse=True)
+    torch.cuda.synchronize()
+    assert av.get_last_device_error()[0] == 0
+    seqs = sorted(np.random.default_rng(45).choice(cfg.batch, 10, replace=False).tolist())
+    seqs = sorted(set(seqs) | {int(np.argmax(cfg.ctx)), int(np.argmin(cfg.ctx))})
+    kp, vp, btc = workloads.compact_paged(cfg, seqs)
+    cu_q = workloads.cu_from_lens(np.full(len(seqs), Sq, dtype=np.int64))
+    cu_k = workloads.cu_from_lens(cfg.ctx[seqs])
+    ref, ref_lse = oracle.attn_varlen(q4[seqs].reshape(-1, cfg.Hq, cfg.D), kp, vp, cu_q, cu_k, cfg.Hq, cfg.Hkv,
+                                      cfg.D, cfg.scale, True, block_table=btc, block_size=cfg.block_size,
+                                      num_blocks=kp.shape[0])
+    assert_close(out[seqs].reshape(-1, cfg.Hq, cfg.D), ref.reshape(-1, cfg.Hq, cfg.D), "c4 cache, 4 new tokens")
+    got_lse = lse.view(cfg.Hq, cfg.batch, Sq)[:, seqs].reshape(cfg.Hq, -1).t().contiguous()
+    assert_lse_close(got_lse, ref_lse.reshape(-1, cfg.Hq), "c4 cache, 4 new tokens, lse")
+    del kc, vc
+    torch.cuda.empty_cache()
