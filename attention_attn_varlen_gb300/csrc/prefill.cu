@@ -25,7 +25,7 @@
 //   warps 4-7  softmax for slot B
 //   warp 8     TMA producer: Q_A, Q_B once, then K_j, V_j tiles through a
 //              3-stage ring (4 for head_dim 64) of 128 keys x head_dim,
-//              128-byte swizzle, in the order K_0, K_1, V_0, K_2, V_1, ...
+//              128-byte swizzle, in the order K_0, K_1, K_2, V_0, K_3, V_1, ...
 //   warp 9     TMEM allocator and the thread that issues every QK^T
 //   warp 10    the thread that issues every PV
 // TMEM (512 columns): S_A [0,128), S_B [128,256) fp32; O_A, O_B after them.
@@ -84,7 +84,7 @@ struct PfSmem {
     static constexpr int kRingOff = 2 * kTileBytes;
     static constexpr int kPOff = kRingOff + kStages * kTileBytes;
     static constexpr int kBarOff = kPOff + 2 * kPBytes;
-    static constexpr int kNumBars = 2 * kStages + 24;
+    static constexpr int kNumBars = 3 * kStages + 24;
     static constexpr int kBytes = kBarOff + kNumBars * 8 + 16 + 1024 /*align slack*/;
     static_assert(kBytes <= 227 * 1024, "shared memory");
 };
@@ -387,8 +387,13 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + S::kBarOff);
     uint64_t *q_full = bars;
     uint64_t *q_empty = bars + 1;                  // this unit's QK^T have read Q
-    uint64_t *full = bars + 2;
-    uint64_t *empty = full + ST;
+    // A ring stage holds K and V' tiles in turn, and the two kinds have different
+    // consumers (the QK^T and the PV thread).  Each kind completes its own
+    // barrier of the stage, so a consumer only ever waits for the next phase
+    // of a barrier whose previous phase it has itself observed.
+    uint64_t *full_k = bars + 2;                   // [ST]: a K tile landed in the stage
+    uint64_t *full_v = full_k + ST;                // [ST]: a V' tile landed in the stage
+    uint64_t *empty = full_v + ST;                 // [ST]: the stage's tile has been read
     uint64_t *s_full = empty + ST;                 // [2]: S_X(t) in TMEM
     uint64_t *s_free = s_full + 2;                 // [2]: the softmax has read S_X(t)
     uint64_t *p_ready = s_free + 2;                // [2]: P'_X(t) in shared memory (and O_X rescaled)
@@ -409,7 +414,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         mbar_init(q_full, 1);
         mbar_init(q_empty, 1);
         for (int i = 0; i < ST; ++i) {
-            mbar_init(&full[i], 1);
+            mbar_init(&full_k[i], 1);
+            mbar_init(&full_v[i], 1);
             mbar_init(&empty[i], 1);
         }
         for (int x = 0; x < 2; ++x) {
@@ -443,6 +449,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         const bool paged = p.block_table != nullptr;
         const int oob_row = paged ? (int)(p.num_blocks * p.block_size) : 0;
         int it = 0, k = 0;
+        uint32_t kpar = 0, vpar = 0, kused = 0, vused = 0;   // per stage: parity of the loads of each kind, any load
         bool ok = true;
         for (;; ++k) {
             // next unit index (-1: none left) into the ring entry k & 1
@@ -483,9 +490,10 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                     mbar_arrive(q_full);
                 }
             }
-            // ring order K_0, K_1, V_0, K_2, V_1, ..., K_{n-1}, V_{n-2}, V_{n-1}: each K tile
-            // one step ahead of the V tile it pairs with, so the next QK^T's tile can
-            // land while the PV of the current one still holds its stage
+            // ring order K_0, K_1, K_2, V_0, K_3, V_1, ..., K_{n-1}, V_{n-3}, V_{n-2}, V_{n-1}:
+            // K tiles run two steps ahead of the V tiles, so a QK^T's tile is loaded well
+            // before the softmax asks for it (the V' tile is needed only at the end of that
+            // softmax)
             for (int j = 0; j < w.n && ok; ++j) {
                 for (int step = 0; step < 3; ++step) {
                     int wv, tj;   // 0: K tile, 1: V tile; key tile index
@@ -507,7 +515,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                     uint8_t *dst = sRing + st * S::kTileBytes;
                     const CUtensorMap *map = wv ? &vmap : &kmap;
                     const int key0 = tj * BN;
-                    uint64_t *bar = &full[st];
+                    uint64_t *bar = wv ? &full_v[st] : &full_k[st];
                     if (lane == 0) {
                         mbar_arrive_expect_tx(bar, (uint32_t)S::kTileBytes);
                         // V' is contiguous by logical key (rows past the sequence hold the
@@ -535,14 +543,24 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                             }
                         }
                     }
+                    if (wv) {
+                        vpar ^= 1u << st;
+                        vused |= 1u << st;
+                    } else {
+                        kpar ^= 1u << st;
+                        kused |= 1u << st;
+                    }
                     ++it;
                 }
             }
         }
         if (lane == 0) {
-            // every copy issued here lands before the CTA may exit
-            for (int t = it - ST < 0 ? 0 : it - ST; t < it; ++t)
-                mbar_wait(&full[t % ST], (uint32_t)(t / ST) & 1u, nullptr, p.err, SRC_PREFILL);
+            // every copy issued here lands before the CTA may exit (the last load of
+            // each kind in each stage completes the phase of parity count - 1)
+            for (int st = 0; st < ST; ++st) {
+                if ((kused >> st) & 1u) mbar_wait(&full_k[st], ((kpar >> st) & 1u) ^ 1u, nullptr, p.err, SRC_PREFILL);
+                if ((vused >> st) & 1u) mbar_wait(&full_v[st], ((vpar >> st) & 1u) ^ 1u, nullptr, p.err, SRC_PREFILL);
+            }
             if (k > 0) mbar_wait(q_full, (uint32_t)(k - 1) & 1u, nullptr, p.err, SRC_PREFILL);
         }
     } else if (warp == 9) {
@@ -554,6 +572,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             const uint32_t qX[2] = {smem_u32(sQ), smem_u32(sQ + S::kTileBytes)};
             const uint32_t ring = smem_u32(sRing);
             int itb = 0, tc[2] = {0, 0}, k = 0;   // ring items before this unit; S tiles issued per slot
+            uint32_t kpar = 0;                    // per stage: parity of the K tiles read from it
             bool ok = true;
             for (;; ++k) {
                 ok = mbar_wait(&idx_full[k & 1], (uint32_t)(k >> 1) & 1u, abort_flag, p.err, SRC_PREFILL);
@@ -568,7 +587,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                 tc_fence_after();
                 for (int j = 0; j < w.n && ok; ++j) {
                     const int itK = itb + (j == 0 ? 0 : 2 * j - 1), stK = itK % ST;   // the producer's ring order
-                    ok = mbar_wait(&full[stK], (uint32_t)(itK / ST) & 1u, abort_flag, p.err, SRC_PREFILL);
+                    ok = mbar_wait(&full_k[stK], (kpar >> stK) & 1u, abort_flag, p.err, SRC_PREFILL);
+                    kpar ^= 1u << stK;
                     if (!ok) break;
 #pragma unroll
                     for (int x = 0; x < 2; ++x) {
@@ -601,6 +621,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             const uint32_t pX[2] = {smem_u32(sP), smem_u32(sP + kPBytes)};
             const uint32_t ring = smem_u32(sRing);
             int itb = 0, tc[2] = {0, 0}, k = 0;   // ring items before this unit; PV tiles issued per slot
+            uint32_t vpar = 0;                    // per stage: parity of the V' tiles read from it
             bool ok = true;
             for (;; ++k) {
                 ok = mbar_wait(&idx_full[k & 1], (uint32_t)(k >> 1) & 1u, abort_flag, p.err, SRC_PREFILL);
@@ -614,7 +635,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                 // softmax threads have read O_X of the previous unit
                 for (int j = 0; j < w.n && ok; ++j) {
                     const int itV = itb + (j < w.n - 1 ? 2 * j + 2 : 2 * w.n - 1), stV = itV % ST;
-                    ok = mbar_wait(&full[stV], (uint32_t)(itV / ST) & 1u, abort_flag, p.err, SRC_PREFILL);
+                    ok = mbar_wait(&full_v[stV], (vpar >> stV) & 1u, abort_flag, p.err, SRC_PREFILL);
+                    vpar ^= 1u << stV;
                     if (!ok) break;
 #pragma unroll
                     for (int x = 0; x < 2; ++x) {
