@@ -30,6 +30,10 @@ struct Vec<float> {
         const float4 v = *reinterpret_cast<const float4 *>(p);
         f[0] = v.x; f[1] = v.y; f[2] = v.z; f[3] = v.w;
     }
+    __device__ static void from_bits(const uint4 &v, float (&f)[4]) {
+        f[0] = __uint_as_float(v.x); f[1] = __uint_as_float(v.y);
+        f[2] = __uint_as_float(v.z); f[3] = __uint_as_float(v.w);
+    }
     __device__ static void store(float *p, const float (&f)[4]) {
         *reinterpret_cast<float4 *>(p) = make_float4(f[0], f[1], f[2], f[3]);
     }
@@ -41,7 +45,9 @@ template <>
 struct Vec<__nv_bfloat16> {
     static constexpr int N = 8;
     __device__ static void load(const __nv_bfloat16 *p, float (&f)[8]) {
-        const uint4 v = *reinterpret_cast<const uint4 *>(p);
+        from_bits(*reinterpret_cast<const uint4 *>(p), f);
+    }
+    __device__ static void from_bits(const uint4 &v, float (&f)[8]) {
         const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
@@ -105,7 +111,8 @@ struct Online {
 
 // ---------------------------------------------------------------------------
 // one warp per row, NV vectors per lane held in registers (VEC: 16-byte
-// accesses; otherwise one element at a time, lane-strided)
+// accesses, and the warp's next row is loaded while it works on the current
+// one; otherwise one element at a time, lane-strided)
 // ---------------------------------------------------------------------------
 template <typename T, int NV, bool VEC>
 __global__ void __launch_bounds__(256) softmax_rows_warp_kernel(const T *x, T *y, int64_t rows, int cols,
@@ -113,9 +120,26 @@ __global__ void __launch_bounds__(256) softmax_rows_warp_kernel(const T *x, T *y
     constexpr int N = VEC ? Vec<T>::N : 1;
     const int lane = threadIdx.x & 31;
     const int64_t nw = (int64_t)gridDim.x * (blockDim.x >> 5);
-    for (int64_t r = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < rows; r += nw) {
+    int64_t r = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    uint4 next[NV];   // VEC: the whole 16-byte vectors of row r (then of the row after it)
+    auto fetch = [&](int64_t row) {
+        if constexpr (VEC) {
+            const T *xr = x + row * xs;
+#pragma unroll
+            for (int i = 0; i < NV; ++i) {
+                const int c0 = (i * 32 + lane) * N;
+                if (c0 + N <= cols) next[i] = *reinterpret_cast<const uint4 *>(xr + c0);
+            }
+        }
+    };
+    if (r < rows) fetch(r);
+    for (; r < rows; r += nw) {
         const T *xr = x + r * xs;
         T *yr = y + r * ys;
+        uint4 cur[NV];
+#pragma unroll
+        for (int i = 0; i < NV; ++i) cur[i] = next[i];
+        if (r + nw < rows) fetch(r + nw);
         float v[NV][N];
         Online st;
 #pragma unroll
@@ -126,7 +150,7 @@ __global__ void __launch_bounds__(256) softmax_rows_warp_kernel(const T *x, T *y
             bool whole = false;
             if constexpr (VEC) {
                 if (valid == N) {
-                    Vec<T>::load(xr + c0, v[i]);
+                    Vec<T>::from_bits(cur[i], v[i]);
 #pragma unroll
                     for (int e = 0; e < N; ++e) v[i][e] *= kLog2e;
                     whole = true;
