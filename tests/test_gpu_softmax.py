@@ -9,7 +9,8 @@ import oracle
 pytestmark = pytest.mark.gpu
 
 SHAPES = [(1, 1), (3, 7), (33, 31), (64, 128), (17, 1000), (8, 2048), (5, 2049), (9, 4096), (4, 4097),
-          (2, 100003), (700, 512)]
+          (2, 100003), (700, 512),
+          (6, 16384), (3, 12296), (2, 32768)]   # long rows: a CTA per row, two passes
 
 
 def _inputs(seed, rows, cols, scale=30.0):
