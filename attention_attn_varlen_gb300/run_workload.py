@@ -10,6 +10,8 @@ with the device error status.  No timing, no comparison.
   --op store    store_kvcache of the new tokens (c3)
   --op decode   attn_decode_paged (c4)
   --op kvcache  attn_with_kvcache with --sq new query tokens per sequence (c4 cache)
+  --op softmax  attn_softmax_rows on a seeded [--rows, --cols] matrix (--dtype f32 | bf16;
+                --workload is ignored)
   --seqs N      keep only the first N sequences (smaller captures)
 """
 from __future__ import annotations
@@ -42,14 +44,28 @@ def _trim(cfg, n):
 
 def main(argv=None):
     ap = argparse.ArgumentParser()
-    ap.add_argument("--workload", required=True, choices=workloads.CONFIG_NAMES)
-    ap.add_argument("--op", required=True, choices=["prefill", "store", "decode", "kvcache"])
+    ap.add_argument("--workload", default="c2_varlen_gqa", choices=workloads.CONFIG_NAMES)
+    ap.add_argument("--op", required=True, choices=["prefill", "store", "decode", "kvcache", "softmax"])
+    ap.add_argument("--rows", type=int, default=262144)
+    ap.add_argument("--cols", type=int, default=1024)
+    ap.add_argument("--dtype", choices=["f32", "bf16"], default="bf16")
     ap.add_argument("--sq", type=int, default=4, help="new query tokens per sequence (--op kvcache)")
     ap.add_argument("--iters", type=int, default=3)
     ap.add_argument("--seqs", type=int, default=None)
     a = ap.parse_args(argv)
     av.lib()
     dev = torch.device("cuda", 0)
+    if a.op == "softmax":
+        g = torch.Generator(device=dev).manual_seed(1)
+        x = torch.randn(a.rows, a.cols, device=dev, generator=g) * 30.0
+        x = x.to(torch.bfloat16 if a.dtype == "bf16" else torch.float32)
+        y = torch.empty_like(x)
+        for _ in range(a.iters):
+            av.softmax_rows(x, out=y)
+        torch.cuda.synchronize()
+        st, word = av.get_last_device_error()
+        print(f"softmax {a.rows}x{a.cols} {a.dtype} x{a.iters}: device status {st} word {word:#x}")
+        return 0 if st == 0 else 1
     cfg = _trim(workloads.make(a.workload), a.seqs)
     if isinstance(cfg, workloads.Varlen):
         if a.op != "prefill":
