@@ -191,13 +191,13 @@ __global__ void __launch_bounds__(256) softmax_rows_warp_kernel(const T *x, T *y
 // ---------------------------------------------------------------------------
 // one CTA per row, two passes over the row
 // ---------------------------------------------------------------------------
-constexpr int kRowThreads = 512;
-
-template <typename T, bool VEC>
-__global__ void __launch_bounds__(kRowThreads) softmax_rows_cta_kernel(const T *x, T *y, int64_t rows, int cols,
+// NT threads per CTA: 256 for rows of up to 32 KB (more rows in flight per SM),
+// 512 beyond
+template <typename T, bool VEC, int NT>
+__global__ void __launch_bounds__(NT) softmax_rows_cta_kernel(const T *x, T *y, int64_t rows, int cols,
                                                                        int64_t xs, int64_t ys) {
     constexpr int N = VEC ? Vec<T>::N : 1;
-    __shared__ float sm_m[kRowThreads / 32], sm_d[kRowThreads / 32];
+    __shared__ float sm_m[NT / 32], sm_d[NT / 32];
     __shared__ float fin[2];
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
     const int nvec = (cols + N - 1) / N;
@@ -205,7 +205,7 @@ __global__ void __launch_bounds__(kRowThreads) softmax_rows_cta_kernel(const T *
         const T *xr = x + r * xs;
         T *yr = y + r * ys;
         Online st;
-        for (int i = threadIdx.x; i < nvec; i += kRowThreads) {
+        for (int i = threadIdx.x; i < nvec; i += NT) {
             const int c0 = i * N;
             const int valid = min(N, cols - c0);
             float f[N];
@@ -232,7 +232,7 @@ __global__ void __launch_bounds__(kRowThreads) softmax_rows_cta_kernel(const T *
         __syncthreads();
         if (wid == 0) {
             Online t;
-            if (lane < kRowThreads / 32) {
+            if (lane < NT / 32) {
                 t.m = sm_m[lane];
                 t.d = sm_d[lane];
             }
@@ -244,7 +244,7 @@ __global__ void __launch_bounds__(kRowThreads) softmax_rows_cta_kernel(const T *
         }
         __syncthreads();
         const float m = fin[0], inv = fin[1];
-        for (int i = threadIdx.x; i < nvec; i += kRowThreads) {
+        for (int i = threadIdx.x; i < nvec; i += NT) {
             const int c0 = i * N;
             const int valid = min(N, cols - c0);
             float f[N];
@@ -289,8 +289,13 @@ cudaError_t launch_t(const T *x, T *y, int64_t rows, int cols, int64_t xs, int64
     if (per_lane <= 2) return launch_warp<T, 2, VEC>(x, y, rows, cols, xs, ys, sms, stream);
     if (per_lane <= 4) return launch_warp<T, 4, VEC>(x, y, rows, cols, xs, ys, sms, stream);
     if (per_lane <= 8) return launch_warp<T, 8, VEC>(x, y, rows, cols, xs, ys, sms, stream);
-    const int grid = (int)(rows < (int64_t)sms * 4 ? rows : (int64_t)sms * 4);
-    softmax_rows_cta_kernel<T, VEC><<<grid, kRowThreads, 0, stream>>>(x, y, rows, cols, xs, ys);
+    if ((int64_t)cols * (int64_t)sizeof(T) <= 32768) {
+        const int grid = (int)(rows < (int64_t)sms * 8 ? rows : (int64_t)sms * 8);
+        softmax_rows_cta_kernel<T, VEC, 256><<<grid, 256, 0, stream>>>(x, y, rows, cols, xs, ys);
+    } else {
+        const int grid = (int)(rows < (int64_t)sms * 4 ? rows : (int64_t)sms * 4);
+        softmax_rows_cta_kernel<T, VEC, 512><<<grid, 512, 0, stream>>>(x, y, rows, cols, xs, ys);
+    }
     return cudaGetLastError();
 }
 
