@@ -214,8 +214,8 @@ def attn_varlen_fwd_host(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int,
                          device=None):
     """attn_varlen_fwd for host-resident inputs: q, k, v (pinned CPU bf16, packed),
     cu_seqlens (CPU int32).  Sequences are split into `chunks` groups of about equal
-    token count; the copy of group i+1 to the device overlaps the attention of group
-    i and the copy back of group i-1 (three CUDA streams).  Returns the output in a
+    token count (the last two smaller); the copy of group i+1 to the device overlaps
+    the attention of group i and the copy back of group i-1 (three CUDA streams).  Returns the output in a
     pinned CPU tensor (`out` if given) once it has arrived.  Each group runs the
     same kernels as attn_varlen_fwd on the whole batch, so the result is the same."""
     for name, t in (("q", q), ("k", k), ("v", v)):
@@ -231,8 +231,12 @@ def attn_varlen_fwd_host(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int,
     dout = torch.empty(q.shape, dtype=q.dtype, device=device)
     dcq = cu_seqlens_q.to(device=device, dtype=torch.int32)
     dck = cu_seqlens_k.to(device=device, dtype=torch.int32)
-    # group boundaries: whole sequences, about equal query tokens
-    target = [int(round(cq[-1] * (i + 1) / chunks)) for i in range(chunks)]
+    # group boundaries: whole sequences, about equal query tokens except the last two
+    # groups, which are smaller (0.6 and 0.3 of the others) so that less compute and
+    # copy-back trail the last copy-in
+    weights = [1.0] * chunks if chunks < 3 else [1.0] * (chunks - 2) + [0.6, 0.3]
+    acc = [sum(weights[:i + 1]) for i in range(chunks)]
+    target = [int(round(cq[-1] * a / acc[-1])) for a in acc]
     bounds, b0 = [], 0
     for tgt in target:
         b1 = b0
