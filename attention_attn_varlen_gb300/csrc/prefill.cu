@@ -25,7 +25,7 @@
 //   warps 4-7  softmax for slot B
 //   warp 8     TMA producer: Q_A, Q_B once, then K_j, V_j tiles through a
 //              3-stage ring (4 for head_dim 64) of 128 keys x head_dim,
-//              128-byte swizzle, in the order K_0, K_1, K_2, V_0, K_3, V_1, ...
+//              128-byte swizzle, in the order K_0, K_1, V_0, K_2, V_1, ...
 //   warp 9     TMEM allocator and the thread that issues every QK^T
 //   warp 10    the thread that issues every PV
 // TMEM (512 columns): S_A [0,128), S_B [128,256) fp32; O_A, O_B after them.
@@ -490,10 +490,9 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                     mbar_arrive(q_full);
                 }
             }
-            // ring order K_0, K_1, K_2, V_0, K_3, V_1, ..., K_{n-1}, V_{n-3}, V_{n-2}, V_{n-1}:
-            // K tiles run two steps ahead of the V tiles, so a QK^T's tile is loaded well
-            // before the softmax asks for it (the V' tile is needed only at the end of that
-            // softmax)
+            // ring order K_0, K_1, V_0, K_2, V_1, ..., K_{n-1}, V_{n-2}, V_{n-1}: each K tile
+            // one step ahead of the V' tile it pairs with, so the next QK^T's tile can land
+            // while the PV of the current one still holds its stage
             for (int j = 0; j < w.n && ok; ++j) {
                 for (int step = 0; step < 3; ++step) {
                     int wv, tj;   // 0: K tile, 1: V tile; key tile index
