@@ -104,6 +104,7 @@ bool fix_stride(int64_t *stride, int64_t packed) {
 }
 
 constexpr int kMaxSplits = 64;
+constexpr int kDecodeMaxColumns = 64;   // Sq x G query columns per KV head on the decode kernel
 constexpr int kDecodeTile = 64;
 
 int choose_splits(int num_sms, int batch, int num_heads_kv, int max_len, int requested) {
@@ -149,12 +150,12 @@ size_t decode_partial_bytes(int batch, int seqlen_q, int num_heads_q, int head_d
 }
 
 // The kv-cache entry runs on the decode kernel when the Sq x G query rows of a
-// KV head fit its two n8 column tiles; otherwise on the paged varlen prefill.
+// KV head fit four column groups of 16; otherwise on the paged varlen prefill.
 bool kvcache_on_decode(int batch, int seqlen_q, int num_heads_q, int num_heads_kv, int head_dim) {
     if (num_heads_q <= 0 || num_heads_kv <= 0 || num_heads_q % num_heads_kv) return false;
     if (head_dim != 64 && head_dim != 128) return false;
     if (batch > 65535 || num_heads_kv > 65535) return false;
-    return (int64_t)seqlen_q * (num_heads_q / num_heads_kv) <= 16;
+    return (int64_t)seqlen_q * (num_heads_q / num_heads_kv) <= kDecodeMaxColumns;
 }
 
 struct DecodeCall {
@@ -177,7 +178,7 @@ attn_status decode_check(const DecodeCall &c) {
     if (!(c.scale > 0.f) || !isfinite(c.scale)) return ATTN_ERR_INVALID_ARG;
     if (!pow2(c.block_size) || c.block_size < 16 || c.num_blocks <= 0) return ATTN_ERR_INVALID_ARG;
     if (c.head_dim != 64 && c.head_dim != 128) return ATTN_ERR_UNSUPPORTED;
-    if ((int64_t)c.seqlen_q * (c.Hq / c.Hkv) > 16) return ATTN_ERR_UNSUPPORTED;
+    if ((int64_t)c.seqlen_q * (c.Hq / c.Hkv) > kDecodeMaxColumns) return ATTN_ERR_UNSUPPORTED;
     if (c.batch > 65535 || c.Hkv > 65535) return ATTN_ERR_UNSUPPORTED;
     if (c.num_blocks * (int64_t)c.block_size >= (int64_t)INT32_MAX) return ATTN_ERR_UNSUPPORTED;
     if ((int64_t)c.batch * c.seqlen_q * c.Hq >= (int64_t)INT32_MAX) return ATTN_ERR_UNSUPPORTED;
@@ -223,6 +224,10 @@ attn_status decode_launch(const DecodeCall &c, const DevInfo *d, int splits, int
     p.Hkv = c.Hkv;
     p.G = c.Hq / c.Hkv;
     p.Sq = c.seqlen_q;
+    {
+        const int cols = c.seqlen_q * p.G;   // 16 columns per CTA (8 when one n8 tile covers them)
+        p.ncg = cols <= 8 ? 1 : (cols + 15) / 16;
+    }
     p.causal = c.causal ? 1 : 0;
     p.max_seqlen = c.max_len;
     p.scale_log2 = c.scale * 1.4426950408889634f;

@@ -9,7 +9,7 @@
 // The work is HBM-bound: every cached K/V byte of a (sequence, KV head) is read
 // once and serves all Sq x G query rows of the group (G = Hq/Hkv heads).
 //
-// attn_decode_split_kernel: one CTA per (split, KV head, sequence).
+// attn_decode_split_kernel: one CTA per (split, column group, KV head, sequence).
 //   warp 4 (lane 0)   TMA producer: 64-token K and V tiles of the split,
 //                     addressed through the block table, into a 3-stage ring
 //                     of 128-byte-swizzled shared-memory panels.
@@ -20,9 +20,11 @@
 //                     denominator, proxy output rescaled by 2^(m_old - m_new)).
 //                     S^T = K Q^T and O^T += V^T P^T run on mma.sync m16n8k16
 //                     with the tokens (then head_dim) in M and the Sq x G
-//                     query columns (token-major, padded to one or two n8
-//                     tiles) in N; each column masks the keys past its own
-//                     causal limit.  P^T is moved into the B-operand layout
+//                     query columns (token-major) in N: up to 16 per CTA
+//                     (one or two n8 tiles); more columns are split into
+//                     groups of 16 over adjacent CTAs that read the same K/V
+//                     tiles (the repeats come from L2).  Each column masks the
+//                     keys past its own causal limit.  P^T is moved into the B-operand layout
 //                     with movmatrix.  The four warps' states are merged
 //                     exactly at the end.
 // attn_decode_combine_kernel: one warp per (query row, query head) merges the
@@ -62,13 +64,18 @@ __global__ void __launch_bounds__(kDecThreads) attn_decode_split_kernel(const __
     uint64_t *empty = full + kDecStages;
     volatile int *abort_flag = reinterpret_cast<volatile int *>(empty + kDecStages);
 
-    const int split = blockIdx.x, hkv = blockIdx.y, b = blockIdx.z;
+    // blockIdx.x = split * ncg + column group: the CTAs of one split's column groups
+    // are adjacent, so the second and later read the split's K/V tiles from L2
+    const int split = blockIdx.x / p.ncg, cgrp = blockIdx.x % p.ncg, hkv = blockIdx.y, b = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int NQ = p.Sq * p.G;       // live columns: query token t = n / G, head hkv * G + n % G
+    // this CTA's columns: global column c0 + n (n < NQ) is query token (c0 + n) / G,
+    // head hkv * G + (c0 + n) % G
+    const int c0 = cgrp * NC;
+    const int NQ = min(NC, p.Sq * p.G - c0);
     int L = __ldg(p.cache_seqlens + b);
     if (L < 0 || L > p.max_seqlen) {
         // outside [0, max_seqlen]: reported once, then clamped
-        if (split == 0 && threadIdx.x == 0) record_error(p.err, ERR_INDEX | SRC_DECODE);
+        if (split == 0 && cgrp == 0 && threadIdx.x == 0) record_error(p.err, ERR_INDEX | SRC_DECODE);
         L = L < 0 ? 0 : p.max_seqlen;
     }
     const int s0 = split * p.split_tokens;
@@ -76,7 +83,7 @@ __global__ void __launch_bounds__(kDecThreads) attn_decode_split_kernel(const __
         // no tokens for this split.  With one split the output is written here.
         if (p.num_splits == 1 && split == 0) {
             for (int i = threadIdx.x; i < NQ * D; i += kDecThreads) {
-                const int n = i / D, d = i % D;
+                const int n = c0 + i / D, d = i % D;
                 const int h = hkv * p.G + n % p.G;
                 const int64_t row = (int64_t)b * p.Sq + n / p.G;
                 p.out[row * p.out_row_stride + (int64_t)h * D + d] = __float2bfloat16(0.f);
@@ -157,9 +164,10 @@ __global__ void __launch_bounds__(kDecThreads) attn_decode_split_kernel(const __
     for (int nt = 0; nt < NT; ++nt) {
         const int n = nt * 8 + g;
         const bool valid = n < NQ;
-        const int64_t qrow_idx = (int64_t)b * p.Sq + (valid ? n / p.G : 0);
+        const int gn = c0 + n;
+        const int64_t qrow_idx = (int64_t)b * p.Sq + (valid ? gn / p.G : 0);
         const uint32_t *qrow = reinterpret_cast<const uint32_t *>(p.q + qrow_idx * p.q_row_stride +
-                                                                  (int64_t)(hkv * p.G + (valid ? n % p.G : 0)) * D);
+                                                                  (int64_t)(hkv * p.G + (valid ? gn % p.G : 0)) * D);
 #pragma unroll
         for (int ks = 0; ks < KS; ++ks) {
             qf[nt][ks][0] = valid ? __ldg(qrow + ks * 8 + c) : 0u;
@@ -169,7 +177,7 @@ __global__ void __launch_bounds__(kDecThreads) attn_decode_split_kernel(const __
         for (int j = 0; j < 2; ++j) {
             const int col = nt * 8 + 2 * c + j;
             int e = s1;
-            if (p.causal && col < NQ) e = min(e, L - p.Sq + col / p.G + 1);
+            if (p.causal && col < NQ) e = min(e, L - p.Sq + (c0 + col) / p.G + 1);
             kend[nt][j] = e;
         }
     }
@@ -339,8 +347,8 @@ __global__ void __launch_bounds__(kDecThreads) attn_decode_split_kernel(const __
                 O += mo[(w * D + d) * NC + n] * f;
             }
         }
-        const int h = hkv * p.G + n % p.G;
-        const int64_t row = (int64_t)b * p.Sq + n / p.G;
+        const int h = hkv * p.G + (c0 + n) % p.G;
+        const int64_t row = (int64_t)b * p.Sq + (c0 + n) / p.G;
         const float on = Ls > 0.f ? O / Ls : 0.f;
         const float l2 = Ls > 0.f ? M + __log2f(Ls) : -INFINITY;
         if (p.num_splits == 1) {
@@ -420,7 +428,7 @@ static cudaError_t launch_decode_t(const CUtensorMap &kmap, const CUtensorMap &v
         if (e != cudaSuccess) return e;
         attr_done[dev] = true;
     }
-    dim3 grid(p.num_splits, p.Hkv, batch);
+    dim3 grid(p.num_splits * p.ncg, p.Hkv, batch);
     main_kernel_event_before(stream);
     attn_decode_split_kernel<D, NT><<<grid, kDecThreads, S::kBytes, stream>>>(kmap, vmap, p);
     main_kernel_event_after(stream);

@@ -24,7 +24,8 @@ struct DecodeParams {
     int bt_stride, block_size, rows_per_box, num_splits, split_tokens;
     int64_t num_blocks;
     int Hq, Hkv, G;
-    int Sq;                      // query tokens per sequence; Sq * G <= 16
+    int Sq;                      // query tokens per sequence; Sq * G <= 64
+    int ncg;                     // column groups: CTAs per (split, KV head, sequence), 16 columns each
     int causal;                  // bottom-right: token t sees keys j <= L - Sq + t
     int max_seqlen;              // cache_seqlens outside [0, max_seqlen] are clamped and reported
     float scale_log2;            // softmax_scale * log2(e)

@@ -158,6 +158,7 @@ KERNEL_SOURCES = {
     "prefill": ["attention_attn_varlen_gb300/csrc/prefill.cu", "attention_attn_varlen_gb300/csrc/common.cuh"],
     "decode": ["attention_attn_varlen_gb300/csrc/decode.cu", "attention_attn_varlen_gb300/csrc/common.cuh"],
     "decode_sq4": ["attention_attn_varlen_gb300/csrc/decode.cu", "attention_attn_varlen_gb300/csrc/common.cuh"],
+    "decode_sq8": ["attention_attn_varlen_gb300/csrc/decode.cu", "attention_attn_varlen_gb300/csrc/common.cuh"],
     "store": ["attention_attn_varlen_gb300/csrc/store_kvcache.cu"],
 }
 
@@ -326,6 +327,32 @@ def bench_decode(av, device, steps, warmup, flush, peaks):
                      "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": nbytes4 / tk4 / 1e9 / peaks["hbm_gbs"],
                      "kernel_ms": tk4 * 1e3,
                      "traffic": ncu_traffic("decode_sq4", float(cfg.ctx.sum()) * cfg.Hkv)},
+        "launches_per_step": 2 if splits4 > 1 else 1}
+    # 8 new tokens: 32 query columns per KV head, two column groups of CTAs that
+    # share each K/V tile (the second read comes from L2)
+    Sq8 = 8
+    q8 = torch.randn(cfg.batch, Sq8, cfg.Hq, cfg.D, device=device, generator=g).to(torch.bfloat16)
+    ws8 = torch.empty(av.lib().attn_kvcache_workspace_size(cfg.batch, Sq8, cfg.Hq, cfg.Hkv, cfg.D, mx),
+                      dtype=torch.uint8, device=device)
+    out8 = torch.empty_like(q8)
+
+    def step8():
+        av.attn_with_kvcache(q8, kc, vc, cs, bt, cfg.scale, max_cache_seqlen=mx, out=out8, workspace=ws8)
+    for _ in range(warmup):
+        step8()
+    torch.cuda.synchronize()
+    ms8, kms8 = time_steps(step8, steps, flush, kernel=True)
+    t8 = float(np.mean(ms8)) / 1e3
+    tk8 = float(np.mean(kms8)) / 1e3
+    nbytes8 = nbytes + 2 * cfg.batch * (Sq8 - 1) * cfg.Hq * cfg.D * 2
+    res["kvcache_8_tokens"] = {
+        "workload": "c4_decode cache, 8 new query tokens per sequence (attn_with_kvcache: split-KV decode kernel, "
+                    "32 query rows per KV head in two column groups)",
+        "value": nbytes8 / t8 / 1e9, "unit": "GB/s", "ms_per_step": t8 * 1e3, "algorithmic_bytes": nbytes8,
+        "roofline": {"bound": "hbm", "kernel": "attn_decode_split_kernel", "achieved": nbytes8 / tk8 / 1e9,
+                     "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": nbytes8 / tk8 / 1e9 / peaks["hbm_gbs"],
+                     "kernel_ms": tk8 * 1e3,
+                     "traffic": ncu_traffic("decode_sq8", float(cfg.ctx.sum()) * cfg.Hkv)},
         "launches_per_step": 2 if splits4 > 1 else 1}
     del kc, vc
     torch.cuda.empty_cache()

@@ -130,8 +130,9 @@ ATTN_API size_t attn_varlen_workspace_size(int batch, int num_heads_q, int num_h
  *   k_cache, v_cache  [num_blocks, block_size, num_heads_kv, head_dim]
  *   out          [batch, num_heads_q, head_dim] bf16; row stride out_row_stride
  *   lse          nullable; [batch, num_heads_q] float32
- *   num_heads_q  a multiple of num_heads_kv, at most 16 query heads per KV
- *                head (ATTN_ERR_UNSUPPORTED above)
+ *   num_heads_q  a multiple of num_heads_kv, at most 64 query heads per KV
+ *                head (ATTN_ERR_UNSUPPORTED above); past 16 the heads of a
+ *                KV head are spread over several CTAs in groups of 16
  *   cache_seqlens int32 [batch]: keys 0 .. cache_seqlens[b]-1 are attended
  *                (they include the current token, stored beforehand); values
  *                outside [0, max_cache_seqlen] are clamped and reported as
@@ -247,10 +248,11 @@ ATTN_API size_t attn_padded_workspace_size(int batch, int seqlen_q, int seqlen_k
  * cache_seqlens, block_table, softmax_scale, causal) with q of shape
  * [B, seqlen_q, H, D] and seqlen_q >= 1: chunked append, speculative
  * verification).  Two routes, chosen from the sizes alone:
- *  - seqlen_q * (num_heads_q / num_heads_kv) <= 16 and head_dim 64 or 128:
+ *  - seqlen_q * (num_heads_q / num_heads_kv) <= 64 and head_dim 64 or 128:
  *    the split-KV decode kernel of attn_decode_paged with one query column
- *    per (new token, head); the cache is read once.  With seqlen_q = 1 the
- *    result equals attn_decode_paged's bit for bit.
+ *    per (new token, head), up to 16 columns per CTA; the cache is read from
+ *    HBM once (CTAs holding other columns of the same KV head re-read it from
+ *    L2).  With seqlen_q = 1 the result equals attn_decode_paged's bit for bit.
  *  - otherwise: cu_seqlens_q = b * seqlen_q and cu_seqlens_k = prefix sums of
  *    cache_seqlens are computed on the device, then the paged varlen prefill
  *    (attn_varlen_fwd) runs.

@@ -46,11 +46,11 @@ def test_host_validation_without_device(L):
     assert L.attn_varlen_fwd(*args(Hq=12, Hkv=4)) == 2       # group of 3 does not divide the 128-row slot
     assert L.attn_varlen_fwd(*args(qs=4 * 64 + 3)) == 1        # row stride not 16-byte aligned
     assert L.attn_varlen_fwd(*args(B=0)) == 1
-    # decode: block size must be a power of two >= 16; group <= 16
+    # decode: block size must be a power of two >= 16; group <= 64
     dec = lambda **kw: [fake, fake, fake, fake, null, fake, fake, 4, 2, kw.get("Hq", 8), kw.get("Hkv", 8), 128,
                         kw.get("bs", 16), 10, 64, 0.1, 0, 0, 0, null, 0, null]
     assert L.attn_decode_paged(*dec(bs=24)) == 1
-    assert L.attn_decode_paged(*dec(Hq=64, Hkv=2)) == 2
+    assert L.attn_decode_paged(*dec(Hq=128, Hkv=1)) == 2
 
 
 def test_decode_split_rule_is_host_side(L):
@@ -91,9 +91,9 @@ def test_new_workspace_sizes_are_host_side(L):
     L.attn_padded_workspace_size.restype = ctypes.c_size_t
     assert L.attn_kvcache_workspace_size(0, 1, 32, 8, 128, 100) == 0
     assert L.attn_padded_workspace_size(2, 0, 16, 8, 8, 64) == 0
-    a = L.attn_kvcache_workspace_size(4, 5, 32, 8, 128, 1000)
-    b = L.attn_kvcache_workspace_size(4, 5, 32, 8, 128, 2000)
-    assert 0 < a < b            # prefill route (5 x 4 query rows per KV head): the fp16 V' copy grows with the cache
+    a = L.attn_kvcache_workspace_size(4, 17, 32, 8, 128, 1000)
+    b = L.attn_kvcache_workspace_size(4, 17, 32, 8, 128, 2000)
+    assert 0 < a < b            # prefill route (17 x 4 query rows per KV head): the fp16 V' copy grows with the cache
     # decode route (3 x 4 rows): only split partials, at most 64 splits of fp32 rows, whatever the cache length
     for n in (0, 1000, 1 << 20):
         c = L.attn_kvcache_workspace_size(4, 3, 32, 8, 128, n)

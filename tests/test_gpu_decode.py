@@ -52,6 +52,8 @@ CASES = [
     (8, [4097, 31, 2500], 24, 8, 128, 16, 0),
     (9, [300, 2000, 1], 32, 2, 128, 16, 0),     # 16 query heads per KV head: two n8 column tiles
     (10, [700, 65], 48, 3, 64, 32, 5),
+    (11, [900, 40, 3000], 64, 2, 128, 64, 0),   # 32 query heads per KV head: two column groups
+    (12, [257, 1200], 64, 1, 64, 16, 4),        # 64 heads on one KV head: four column groups
 ]
 
 

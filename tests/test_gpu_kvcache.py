@@ -23,10 +23,13 @@ CASES = [
     (70, [500, 77], 2, 64, 8, 128, 64),              # G = 8
     (71, [1200, 5, 64], 1, 32, 2, 128, 16),          # G = 16, one token
     (72, [64, 0, 191], 3, 16, 4, 64, 16),            # twelve live columns of sixteen
+    (77, [300, 1500, 7], 8, 32, 8, 128, 64),         # 32 columns: two column groups
+    (78, [129, 640], 5, 64, 8, 128, 16),             # 40 columns: three groups, the last one half full
+    (79, [2000, 33], 64, 8, 8, 64, 32),              # G = 1, 64 new tokens: four groups
     # larger Sq x G: the paged varlen prefill
     (64, [90, 700, 1], 64, 16, 2, 64, 32),
     (65, [3000, 129], 130, 32, 8, 128, 128),
-    (73, [400, 20], 5, 32, 8, 128, 64),
+    (73, [400, 20], 17, 32, 8, 128, 64),
 ]
 
 
@@ -53,13 +56,14 @@ def test_kvcache_matches_oracle(seed, ctx, Sq, Hq, Hkv, D, bs):
 
 
 def test_kvcache_equals_paged_varlen_bitexact():
-    """The kv-cache entry only derives cu_seqlens on the device; the attention is
-    the paged varlen path, bit for bit."""
-    cfg = workloads.small_paged(66, ctx=[700, 90, 1500], new=[5, 5, 5], Hq=32, Hkv=8, D=128, block_size=64)
+    """Past 64 query columns per KV head (17 tokens x 4 heads) the kv-cache entry
+    only derives cu_seqlens on the device; the attention is the paged varlen path,
+    bit for bit."""
+    cfg = workloads.small_paged(66, ctx=[700, 90, 1500], new=[17, 17, 17], Hq=32, Hkv=8, D=128, block_size=64)
     q = cfg.q()
     kc, vc, _, _ = _paged_device(cfg)
     cs, bt = _as_kvcache_args(cfg, kc, vc)
-    out_k, lse_k = av.attn_with_kvcache(q.cuda().view(cfg.batch, 5, cfg.Hq, cfg.D), kc, vc, cs, bt, cfg.scale,
+    out_k, lse_k = av.attn_with_kvcache(q.cuda().view(cfg.batch, 17, cfg.Hq, cfg.D), kc, vc, cs, bt, cfg.scale,
                                         max_cache_seqlen=int(cfg.lens_k.max()), return_lse=True)
     out_v, lse_v = _run_paged(cfg, q, kc, vc)
     torch.cuda.synchronize()
@@ -68,7 +72,7 @@ def test_kvcache_equals_paged_varlen_bitexact():
 
 
 @pytest.mark.parametrize("causal", [False, True])
-@pytest.mark.parametrize("Sq,Hq,Hkv,D", [(4, 16, 4, 128), (2, 8, 8, 64), (9, 16, 8, 128)])
+@pytest.mark.parametrize("Sq,Hq,Hkv,D", [(4, 16, 4, 128), (2, 8, 8, 64), (9, 16, 8, 128), (17, 32, 8, 128)])
 def test_kvcache_causal_flag(causal, Sq, Hq, Hkv, D):
     """causal=False lets every new token see all cached keys (decode kernel and prefill route)."""
     cfg = workloads.small_paged(74 + Sq, ctx=[300, 64, 5], new=[Sq] * 3, Hq=Hq, Hkv=Hkv, D=D, block_size=32)
@@ -85,7 +89,7 @@ def test_kvcache_causal_flag(causal, Sq, Hq, Hkv, D):
     assert_lse_close(lse.t().contiguous(), ref_lse.reshape(-1, Hq), "kvcache lse")
 
 
-@pytest.mark.parametrize("Sq,Hq,Hkv", [(4, 16, 4), (6, 8, 8), (4, 64, 8)])
+@pytest.mark.parametrize("Sq,Hq,Hkv", [(4, 16, 4), (6, 8, 8), (4, 64, 8), (17, 32, 8)])
 def test_kvcache_fewer_keys_than_new_tokens(Sq, Hq, Hkv):
     """cache_seqlens[b] < seqlen_q: the first new tokens see no key at all (output
     0, lse -inf) and the rest see a causal prefix of the keys."""
@@ -126,16 +130,16 @@ def test_kvcache_one_token_equals_decode_bitexact():
     assert torch.equal(lse_k, lse_d.t())
 
 
-@pytest.mark.parametrize("Hq,Hkv", [(8, 8), (64, 8)])
-def test_kvcache_seqlen_above_stated_max_is_reported(Hq, Hkv):
+@pytest.mark.parametrize("Sq,Hq,Hkv", [(4, 8, 8), (4, 64, 8), (17, 32, 8)])
+def test_kvcache_seqlen_above_stated_max_is_reported(Sq, Hq, Hkv):
     """A cache_seqlens entry above max_cache_seqlen is clamped and reported, not
-    read past (Sq x G = 4: decode kernel; 32: prefill route)."""
-    cfg = workloads.small_paged(67, ctx=[300, 40], new=[4, 4], Hq=Hq, Hkv=Hkv, D=128, block_size=64)
+    read past (Sq x G = 4 and 32: decode kernel; 68: prefill route)."""
+    cfg = workloads.small_paged(67, ctx=[300, 40], new=[Sq, Sq], Hq=Hq, Hkv=Hkv, D=128, block_size=64)
     q = cfg.q()
     kc, vc, _, _ = _paged_device(cfg)
     cs, bt = _as_kvcache_args(cfg, kc, vc)
     av.get_last_device_error()
-    av.attn_with_kvcache(q.cuda().view(cfg.batch, 4, cfg.Hq, cfg.D), kc, vc, cs, bt, cfg.scale,
+    av.attn_with_kvcache(q.cuda().view(cfg.batch, Sq, cfg.Hq, cfg.D), kc, vc, cs, bt, cfg.scale,
                          max_cache_seqlen=100)
     torch.cuda.synchronize()
     st, word = av.get_last_device_error()
