@@ -1,4 +1,7 @@
 """Shared helpers for the parity tests (comparison metrics, device placement)."""
+import json
+import os
+
 import numpy as np
 import torch
 
@@ -27,10 +30,20 @@ def errors(got, ref):
     return max_abs, rel
 
 
+def _log_parity(what, max_abs, rel):
+    """With ATTN_PARITY_LOG=<file> set, append each comparison's metrics to that
+    file (one JSON object per line) so a run of the parity tests can be tabulated."""
+    path = os.environ.get("ATTN_PARITY_LOG")
+    if path:
+        with open(path, "a") as f:
+            f.write(json.dumps({"what": what, "max_abs_minus_rounding": max_abs, "rel_rms": rel}) + "\n")
+
+
 def assert_close(got, ref, what=""):
     g = got.float().cpu().double().numpy() if isinstance(got, torch.Tensor) else np.asarray(got, np.float64)
     assert np.all(np.isfinite(g)), f"{what}: non-finite output"
     max_abs, rel = errors(got, ref)
+    _log_parity(what, max_abs, rel)
     assert max_abs <= MAX_ABS and rel <= REL_RMS, f"{what}: max|err|={max_abs:.3e} relRMS={rel:.3e}"
     return max_abs, rel
 
