@@ -8,7 +8,10 @@ paged cache (store_kvcache at slot_mapping), then
     block tables (prefix cache), K/V are read from the caches instead of the
     step's own k/v;
   * decode: one query token per sequence against the cache (context_lens =
-    cache_seqlens, which include the token just stored).
+    cache_seqlens, which include the token just stored).  A decode step that
+    carries the same number of new tokens for every sequence (speculative
+    verification; the page shows one) goes through the kv-cache entry with
+    bottom-right causality among the new tokens.
 
 Everything runs in the library's kernels; this module only routes tensors.
 """
@@ -18,7 +21,7 @@ from dataclasses import dataclass
 
 import torch
 
-from . import attn_decode_paged, attn_varlen_fwd, store_kvcache
+from . import attn_decode_paged, attn_varlen_fwd, attn_with_kvcache, store_kvcache
 
 
 @dataclass
@@ -30,7 +33,7 @@ class AttentionContext:
     cu_seqlens_k: torch.Tensor | None = None     # int32 [B+1] (prefill)
     max_seqlen_q: int = 0
     max_seqlen_k: int = 0
-    context_lens: torch.Tensor | None = None     # int32 [B] (decode): cached keys incl. the new token
+    context_lens: torch.Tensor | None = None     # int32 [B] (decode): cached keys incl. the new tokens
     block_tables: torch.Tensor | None = None     # int32 [B, max_blocks] (prefix prefill, decode)
 
 
@@ -76,8 +79,17 @@ class Attention:
                 raise ValueError("decode needs the KV cache")
             if ctx.context_lens is None or ctx.block_tables is None:
                 raise ValueError("decode needs context_lens and block_tables")
-            o = attn_decode_paged(q, self.k_cache, self.v_cache, ctx.context_lens, ctx.block_tables, self.scale,
-                                  max_cache_seqlen=ctx.max_seqlen_k or None)
+            batch, n = ctx.context_lens.numel(), q.shape[0]
+            if n == batch:
+                o = attn_decode_paged(q, self.k_cache, self.v_cache, ctx.context_lens, ctx.block_tables, self.scale,
+                                      max_cache_seqlen=ctx.max_seqlen_k or None)
+            else:
+                if batch == 0 or n % batch:
+                    raise ValueError("a decode step carries the same number of new tokens for every sequence")
+                sq = n // batch
+                o = attn_with_kvcache(q.reshape(batch, sq, self.num_heads, self.head_dim), self.k_cache,
+                                      self.v_cache, ctx.context_lens, ctx.block_tables, self.scale, causal=True,
+                                      max_cache_seqlen=ctx.max_seqlen_k or None)
         return o.view(shape)
 
     __call__ = forward

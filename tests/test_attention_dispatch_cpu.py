@@ -23,7 +23,12 @@ def calls(monkeypatch):
 
     monkeypatch.setattr(at, "store_kvcache", fake_store)
     monkeypatch.setattr(at, "attn_varlen_fwd", fake_varlen)
+    def fake_kvcache(q, kc, vc, lens, bt, scale, causal=True, max_cache_seqlen=None):
+        log.append(("kvcache", tuple(q.shape), lens, bt, causal, max_cache_seqlen))
+        return torch.zeros_like(q)
+
     monkeypatch.setattr(at, "attn_decode_paged", fake_decode)
+    monkeypatch.setattr(at, "attn_with_kvcache", fake_kvcache)
     return log
 
 
@@ -96,3 +101,21 @@ def test_decode_without_cache_is_refused(calls):
                                            block_tables=torch.zeros(1, 1, dtype=torch.int32)))
     with pytest.raises(ValueError):
         at.Attention(num_heads=6, head_dim=16, scale=1.0, num_kv_heads=4)
+
+
+def test_multi_token_decode_goes_through_the_kvcache_entry(calls):
+    layer = _layer()
+    q, k, v = _qkv(6)                               # 2 sequences x 3 new tokens
+    lens = torch.tensor([9, 17], dtype=torch.int32)
+    bt = torch.zeros(2, 4, dtype=torch.int32)
+    ctx = at.AttentionContext(is_prefill=False, slot_mapping=torch.arange(6), context_lens=lens, block_tables=bt,
+                              max_seqlen_k=17)
+    o = layer(q, k, v, ctx)
+    assert o.shape == q.shape
+    assert [c[0] for c in calls] == ["store", "kvcache"]
+    assert calls[1][1] == (2, 3, 8, 16) and calls[1][2] is lens and calls[1][3] is bt
+    assert calls[1][4] is True and calls[1][5] == 17
+    with pytest.raises(ValueError):                 # 5 tokens over 2 sequences
+        q5, k5, v5 = _qkv(5)
+        layer(q5, k5, v5, ctx)
+

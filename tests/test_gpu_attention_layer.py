@@ -1,5 +1,5 @@
 """The Attention layer through an engine-like sequence of steps (prefill, two
-decode steps, a prefix-cache prefill) on one paged cache, each step against the
+decode steps, a three-token decode step, a prefix-cache prefill) on one paged cache, each step against the
 float64 oracle over the whole history."""
 import numpy as np
 import pytest
@@ -73,4 +73,5 @@ def test_engine_steps_match_oracle():
     step(prompts, "prefill")
     step([1, 1, 1], "decode")
     step([1, 1, 1], "decode")
+    step([3, 3, 3], "decode")        # three new tokens per sequence (the kv-cache entry)
     step([20, 3, 40], "prefix")
