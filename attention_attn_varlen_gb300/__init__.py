@@ -280,8 +280,9 @@ def attn_decode_paged(q, k_cache, v_cache, cache_seqlens, block_table, softmax_s
                       max_cache_seqlen: int | None = None, num_splits: int = 0, out=None, lse=None,
                       return_lse: bool = False, workspace=None, stream=None):
     """Decode: q [B, Hq, D] (or [B, 1, Hq, D]); caches [num_blocks, block_size,
-    Hkv, D]; cache_seqlens int32 [B]; block_table int32 [B, max_blocks].
-    max_cache_seqlen defaults to the block table's capacity (no device sync)."""
+    Hkv, D]; cache_seqlens int32 [B]; block_table int32 [B, max_blocks]; at most
+    64 query heads per KV head.  max_cache_seqlen defaults to the block table's
+    capacity (no device sync)."""
     if q.dim() == 4:
         if q.shape[1] != 1:
             raise ValueError("attn_decode_paged takes one query token per sequence")
@@ -322,7 +323,8 @@ def attn_with_kvcache(q, k_cache, v_cache, cache_seqlens, block_table, softmax_s
     """Several new tokens per sequence against the paged cache: q [B, Sq, Hq, D]
     (Sq >= 1, all sequences the same Sq); caches [num_blocks, block_size, Hkv, D];
     cache_seqlens int32 [B] counts the cached keys including the Sq new ones.
-    Returns out [B, Sq, Hq, D] (and lse [Hq, B*Sq])."""
+    Returns out [B, Sq, Hq, D] (and lse [Hq, B*Sq]).  Up to 64 query rows per KV
+    head (Sq x Hq/Hkv) run on the split-KV decode kernel, more on the prefill kernel."""
     if q.dim() != 4:
         raise ValueError("q must be [B, seqlen_q, Hq, D]")
     _bf16_cuda(("q", q), ("k_cache", k_cache), ("v_cache", v_cache), ("out", out))
