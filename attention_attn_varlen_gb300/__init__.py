@@ -25,7 +25,7 @@ import torch
 from ._build import LIB as _LIB_PATH
 from ._build import build
 
-__all__ = ["attn_varlen_fwd", "attn_varlen_fwd_host", "attn_decode_paged", "attn_with_kvcache", "attn_padded_fwd", "softmax_rows", "store_kvcache", "get_last_device_error", "lib",
+__all__ = ["attn_varlen_fwd", "attn_varlen_fwd_host", "host_staging", "attn_decode_paged", "attn_with_kvcache", "attn_padded_fwd", "softmax_rows", "store_kvcache", "get_last_device_error", "lib",
            "build", "AttnError", "exported_symbols", "set_kernel_events", "decode_num_splits", "decode_workspace_size"]
 
 ATTN_OK = 0
@@ -90,6 +90,9 @@ def lib():
     L.attn_softmax_rows.restype = _i32
     L.attn_set_kernel_events.argtypes = [_vp, _vp]
     L.attn_set_kernel_events.restype = None
+    L.attn_varlen_fwd_host.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _f32, _i32,
+                                       _vp, _vp, _vp, _vp, _vp, _vp, _sz, _i32, _vp, _vp, _vp, _vp, _vp]
+    L.attn_varlen_fwd_host.restype = _i32
     _lib = L
     return L
 
@@ -209,70 +212,72 @@ def decode_workspace_size(batch, num_heads_q, num_heads_kv, head_dim, max_cache_
                                             num_splits)
 
 
+def host_staging(batch: int, total_q: int, total_k: int, num_heads_q: int, num_heads_kv: int, head_dim: int,
+                 max_seqlen_q: int, device=None) -> dict:
+    """Device buffers, copy streams and events that attn_varlen_fwd_host uses;
+    make them once and pass them to every call of the same (or smaller) sizes."""
+    device = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    ws = lib().attn_varlen_workspace_size(batch, num_heads_q, num_heads_kv, head_dim, int(max_seqlen_q), int(total_k))
+    if ws == 0:
+        raise ValueError("unsupported sizes for attn_varlen_fwd_host")
+    bf = torch.bfloat16
+    st = dict(q=torch.empty((total_q, num_heads_q, head_dim), dtype=bf, device=device),
+              k=torch.empty((total_k, num_heads_kv, head_dim), dtype=bf, device=device),
+              v=torch.empty((total_k, num_heads_kv, head_dim), dtype=bf, device=device),
+              out=torch.empty((total_q, num_heads_q, head_dim), dtype=bf, device=device),
+              cu=torch.empty(2 * (batch + 1), dtype=torch.int32, device=device),
+              ws=torch.empty(ws, dtype=torch.uint8, device=device),
+              s_in=torch.cuda.Stream(device), s_out=torch.cuda.Stream(device),
+              ev=(torch.cuda.Event(), torch.cuda.Event()))
+    for e in st["ev"]:
+        e.record(torch.cuda.current_stream(device))   # torch creates the CUDA event on its first record
+    return st
+
+
 def attn_varlen_fwd_host(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, max_seqlen_k: int,
                          softmax_scale: float | None = None, causal: bool = True, out=None, chunks: int = 8,
-                         device=None):
-    """attn_varlen_fwd for host-resident inputs: q, k, v (pinned CPU bf16, packed),
-    cu_seqlens (CPU int32).  Sequences are split into `chunks` groups of about equal
-    token count (the last two smaller); the copy of group i+1 to the device overlaps
-    the attention of group i and the copy back of group i-1 (three CUDA streams).  Returns the output in a
-    pinned CPU tensor (`out` if given) once it has arrived.  Each group runs the
-    same kernels as attn_varlen_fwd on the whole batch, so the result is the same."""
+                         device=None, staging=None, synchronize: bool = True):
+    """attn_varlen_fwd for host-resident inputs (C entry attn_varlen_fwd_host):
+    q, k, v contiguous bf16 CPU tensors (pinned for the copies to overlap),
+    cu_seqlens int32 CPU tensors.  The library copies groups of sequences in,
+    runs the attention of each group and copies its output back, overlapped on
+    three streams.  Returns the output in a pinned CPU tensor (`out` if given);
+    with synchronize=True (default) after it has arrived.  `staging` (from
+    host_staging) supplies reusable device buffers, streams and events."""
     for name, t in (("q", q), ("k", k), ("v", v)):
-        if t.is_cuda or t.dtype != torch.bfloat16 or not t.is_contiguous():
-            raise ValueError(f"{name} must be a contiguous bf16 CPU tensor (pinned for overlap)")
+        if t.is_cuda or t.dtype != torch.bfloat16 or not t.is_contiguous() or t.dim() != 3:
+            raise ValueError(f"{name} must be a contiguous [rows, heads, dim] bf16 CPU tensor")
+    cq = torch.as_tensor(cu_seqlens_q)
+    ck = torch.as_tensor(cu_seqlens_k)
+    for name, t in (("cu_seqlens_q", cq), ("cu_seqlens_k", ck)):
+        if t.is_cuda or t.dtype != torch.int32 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous int32 CPU tensor")
+    total_q, Hq, D = q.shape
+    total_k, Hkv, _ = k.shape
+    B = cq.numel() - 1
+    if ck.numel() != B + 1 or v.shape != k.shape:
+        raise ValueError("cu_seqlens_q / cu_seqlens_k / k / v do not match")
     device = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
-    cq = cu_seqlens_q.cpu().numpy().astype("int64")
-    ck = cu_seqlens_k.cpu().numpy().astype("int64")
-    B = len(cq) - 1
+    if staging is None:
+        staging = host_staging(B, total_q, total_k, Hq, Hkv, D, max_seqlen_q, device)
     if out is None:
         out = torch.empty(q.shape, dtype=q.dtype).pin_memory()
-    dq, dk, dv = (torch.empty(t.shape, dtype=t.dtype, device=device) for t in (q, k, v))
-    dout = torch.empty(q.shape, dtype=q.dtype, device=device)
-    dcq = cu_seqlens_q.to(device=device, dtype=torch.int32)
-    dck = cu_seqlens_k.to(device=device, dtype=torch.int32)
-    # group boundaries: whole sequences, about equal query tokens except the last two
-    # groups, which are smaller (0.6 and 0.3 of the others) so that less compute and
-    # copy-back trail the last copy-in
-    weights = [1.0] * chunks if chunks < 3 else [1.0] * (chunks - 2) + [0.6, 0.3]
-    acc = [sum(weights[:i + 1]) for i in range(chunks)]
-    target = [int(round(cq[-1] * a / acc[-1])) for a in acc]
-    bounds, b0 = [], 0
-    for tgt in target:
-        b1 = b0
-        while b1 < B and (cq[b1 + 1] <= tgt or b1 == b0):
-            b1 += 1
-        if b1 > b0:
-            bounds.append((b0, b1))
-        b0 = b1
-        if b0 >= B:
-            break
-    if b0 < B:
-        bounds.append((b0, B))
+    elif out.is_cuda or out.shape != q.shape or out.dtype != q.dtype or not out.is_contiguous():
+        raise ValueError("out must be a contiguous bf16 CPU tensor shaped like q")
+    scale = 1.0 / math.sqrt(D) if softmax_scale is None else float(softmax_scale)
     main = torch.cuda.current_stream(device)
-    s_in, s_out = torch.cuda.Stream(device), torch.cuda.Stream(device)
-    s_in.wait_stream(main)
-    s_out.wait_stream(main)
-    for b0, b1 in bounds:
-        q0, q1, k0, k1 = int(cq[b0]), int(cq[b1]), int(ck[b0]), int(ck[b1])
-        with torch.cuda.stream(s_in):
-            dq[q0:q1].copy_(q[q0:q1], non_blocking=True)
-            dk[k0:k1].copy_(k[k0:k1], non_blocking=True)
-            dv[k0:k1].copy_(v[k0:k1], non_blocking=True)
-            arrived = torch.cuda.Event()
-            arrived.record(s_in)
-        main.wait_event(arrived)
-        mq = int((cq[b0 + 1:b1 + 1] - cq[b0:b1]).max())
-        mk = int((ck[b0 + 1:b1 + 1] - ck[b0:b1]).max())
-        attn_varlen_fwd(dq, dk, dv, dcq[b0:b1 + 1], dck[b0:b1 + 1], min(mq, max_seqlen_q), min(mk, max_seqlen_k),
-                        softmax_scale, causal=causal, out=dout)
-        computed = torch.cuda.Event()
-        computed.record(main)
-        with torch.cuda.stream(s_out):
-            s_out.wait_event(computed)
-            out[q0:q1].copy_(dout[q0:q1], non_blocking=True)
-    main.wait_stream(s_out)
-    main.synchronize()   # the device buffers die with this call
+    ws = staging["ws"]
+    ev_a, ev_b = staging["ev"]
+    st = lib().attn_varlen_fwd_host(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(cq), _ptr(ck), B, int(max_seqlen_q), int(max_seqlen_k), Hq, Hkv,
+        D, scale, 1 if causal else 0, _ptr(staging["q"]), _ptr(staging["k"]), _ptr(staging["v"]),
+        _ptr(staging["out"]), _ptr(staging["cu"]), _ptr(ws), ws.numel(), int(chunks),
+        ctypes.c_void_p(main.cuda_stream), ctypes.c_void_p(staging["s_in"].cuda_stream),
+        ctypes.c_void_p(staging["s_out"].cuda_stream), ctypes.c_void_p(ev_a.cuda_event),
+        ctypes.c_void_p(ev_b.cuda_event))
+    _check(st, "attn_varlen_fwd_host")
+    if synchronize:
+        main.synchronize()
     return out
 
 

@@ -8,6 +8,8 @@
 // flash_attn_with_kvcache(q.unsqueeze(1), k_cache, v_cache, cache_seqlens,
 // block_table, softmax_scale, causal).
 #include <math.h>
+
+#include <mutex>
 #include <stdint.h>
 #include <string.h>
 
@@ -25,13 +27,16 @@ constexpr int kMaxDevices = 64;
 __device__ uint32_t g_attn_error_word;
 
 struct DevInfo {
-    bool ready = false;
+    attn_status st = ATTN_ERR_NO_DEVICE;
     int num_sms = 0;
     int cc_major = 0, cc_minor = 0;
     uint32_t *err = nullptr;
 };
 DevInfo g_dev[kMaxDevices];
+std::once_flag g_dev_once[kMaxDevices];
 
+// Attributes of the current device, queried once per device (also when several
+// host threads make their first call together).
 attn_status dev_info(DevInfo **out) {
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
@@ -39,16 +44,18 @@ attn_status dev_info(DevInfo **out) {
         return ATTN_ERR_NO_DEVICE;
     }
     DevInfo &d = g_dev[dev];
-    if (!d.ready) {
+    std::call_once(g_dev_once[dev], [&] {
         if (cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
             cudaDeviceGetAttribute(&d.cc_major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
             cudaDeviceGetAttribute(&d.cc_minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
             cudaGetSymbolAddress(reinterpret_cast<void **>(&d.err), g_attn_error_word) != cudaSuccess) {
             cudaGetLastError();
-            return ATTN_ERR_NO_DEVICE;
+            d.st = ATTN_ERR_NO_DEVICE;
+        } else {
+            d.st = ATTN_OK;
         }
-        d.ready = true;
-    }
+    });
+    if (d.st != ATTN_OK) return d.st;
     *out = &d;
     return ATTN_OK;
 }
@@ -62,18 +69,19 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t
                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
+// the driver's cuTensorMapEncodeTiled, looked up once (a function-local static
+// is initialised once even under concurrent first calls)
 EncodeTiledFn encode_fn() {
-    static EncodeTiledFn fn = nullptr;
-    if (!fn) {
+    static const EncodeTiledFn fn = [] {
         void *p = nullptr;
         cudaDriverEntryPointQueryResult q;
         if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
                 cudaSuccess &&
             q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(p);
-        else
-            cudaGetLastError();
-    }
+            return reinterpret_cast<EncodeTiledFn>(p);
+        cudaGetLastError();
+        return (EncodeTiledFn) nullptr;
+    }();
     return fn;
 }
 
@@ -457,6 +465,121 @@ attn_status attn_varlen_fwd(const void *q, const void *k, const void *v, void *o
                        max_seqlen_q, max_seqlen_k, num_heads_q, num_heads_kv, head_dim, softmax_scale, causal,
                        block_table, block_table_stride, block_size, num_blocks, q_row_stride, k_row_stride,
                        v_row_stride, out_row_stride, workspace, workspace_bytes, stream);
+}
+
+// ---------------------------------------------------------------------------
+// Host-resident inputs: whole sequences in groups of about equal query-token
+// counts (the last two groups 0.6 and 0.3 of the others, so that less work
+// trails the last copy in); group i's copy in (copy_in_stream) overlaps the
+// attention of group i-1 (stream) and the copy out of group i-2
+// (copy_out_stream).  Each group is one attn_varlen_fwd call on the device
+// buffers with cu_seqlens pointing into the full arrays, so rows are addressed
+// in place and the result equals one call over the whole batch.
+static int host_groups(const int32_t *cu_q, int batch, int num_groups, int *bounds) {
+    const int64_t total = cu_q[batch];
+    double w_all = 0.0;
+    for (int g = 0; g < num_groups; ++g)
+        w_all += (num_groups >= 3 && g == num_groups - 2) ? 0.6 : (num_groups >= 3 && g == num_groups - 1) ? 0.3 : 1.0;
+    int n = 0, b0 = 0;
+    double acc = 0.0;
+    bounds[0] = 0;
+    for (int g = 0; g < num_groups && b0 < batch; ++g) {
+        acc += (num_groups >= 3 && g == num_groups - 2) ? 0.6 : (num_groups >= 3 && g == num_groups - 1) ? 0.3 : 1.0;
+        const int64_t target = (int64_t)llround((double)total * acc / w_all);
+        int b1 = b0;
+        while (b1 < batch && (cu_q[b1 + 1] <= target || b1 == b0)) ++b1;
+        if (b1 > b0) bounds[++n] = b1;
+        b0 = b1;
+    }
+    if (b0 < batch) bounds[++n] = batch;
+    return n;
+}
+
+extern "C" attn_status attn_varlen_fwd_host(const void *q_host, const void *k_host, const void *v_host,
+                                            void *out_host, const int32_t *cu_seqlens_q_host,
+                                            const int32_t *cu_seqlens_k_host, int batch, int max_seqlen_q,
+                                            int max_seqlen_k, int num_heads_q, int num_heads_kv, int head_dim,
+                                            float softmax_scale, int causal, void *q_dev, void *k_dev, void *v_dev,
+                                            void *out_dev, int32_t *cu_dev, void *workspace, size_t workspace_bytes,
+                                            int num_groups, void *stream, void *copy_in_stream,
+                                            void *copy_out_stream, void *event_a, void *event_b) {
+    if (!q_host || !k_host || !v_host || !out_host || !cu_seqlens_q_host || !cu_seqlens_k_host) return ATTN_ERR_INVALID_ARG;
+    if (!q_dev || !k_dev || !v_dev || !out_dev || !cu_dev || !event_a || !event_b) return ATTN_ERR_INVALID_ARG;
+    if (batch <= 0 || num_groups <= 0 || num_groups > 64 || max_seqlen_q < 0 || max_seqlen_k < 0)
+        return ATTN_ERR_INVALID_ARG;
+    if (num_heads_q <= 0 || num_heads_kv <= 0 || head_dim <= 0) return ATTN_ERR_INVALID_ARG;
+    // the host offsets are readable here: check them once
+    if (cu_seqlens_q_host[0] != 0 || cu_seqlens_k_host[0] != 0) return ATTN_ERR_INVALID_ARG;
+    for (int b = 0; b < batch; ++b) {
+        const int64_t lq = (int64_t)cu_seqlens_q_host[b + 1] - cu_seqlens_q_host[b];
+        const int64_t lk = (int64_t)cu_seqlens_k_host[b + 1] - cu_seqlens_k_host[b];
+        if (lq < 0 || lk < 0 || lq > max_seqlen_q || lk > max_seqlen_k) return ATTN_ERR_INVALID_ARG;
+    }
+    const int64_t total_q = cu_seqlens_q_host[batch], total_k = cu_seqlens_k_host[batch];
+    const size_t need = attn_varlen_workspace_size(batch, num_heads_q, num_heads_kv, head_dim, max_seqlen_q, total_k);
+    if (need == 0) return head_dim != 64 && head_dim != 128 ? ATTN_ERR_UNSUPPORTED : ATTN_ERR_INVALID_ARG;
+    if (!workspace || workspace_bytes < need) return ATTN_ERR_WORKSPACE_TOO_SMALL;
+    DevInfo *d = nullptr;
+    attn_status st = dev_info(&d);
+    if (st != ATTN_OK) return st;
+    if ((st = check_arch(d)) != ATTN_OK) return st;
+
+    cudaStream_t s_main = reinterpret_cast<cudaStream_t>(stream);
+    cudaStream_t s_in = reinterpret_cast<cudaStream_t>(copy_in_stream);
+    cudaStream_t s_out = reinterpret_cast<cudaStream_t>(copy_out_stream);
+    cudaEvent_t ev_a = reinterpret_cast<cudaEvent_t>(event_a), ev_b = reinterpret_cast<cudaEvent_t>(event_b);
+    const size_t qrow = (size_t)num_heads_q * head_dim * 2, kvrow = (size_t)num_heads_kv * head_dim * 2;
+    int bounds[65];
+    const int ng = host_groups(cu_seqlens_q_host, batch, num_groups, bounds);
+    bool fail = false;
+    auto ck = [&](cudaError_t e) {
+        if (e != cudaSuccess) fail = true;
+    };
+    // the copy streams start after the work already queued on `stream`
+    ck(cudaEventRecord(ev_b, s_main));
+    ck(cudaStreamWaitEvent(s_in, ev_b, 0));
+    ck(cudaStreamWaitEvent(s_out, ev_b, 0));
+    ck(cudaMemcpyAsync(cu_dev, cu_seqlens_q_host, (size_t)(batch + 1) * 4, cudaMemcpyHostToDevice, s_in));
+    ck(cudaMemcpyAsync(cu_dev + batch + 1, cu_seqlens_k_host, (size_t)(batch + 1) * 4, cudaMemcpyHostToDevice, s_in));
+    uint8_t *qd = reinterpret_cast<uint8_t *>(q_dev), *kd = reinterpret_cast<uint8_t *>(k_dev);
+    uint8_t *vd = reinterpret_cast<uint8_t *>(v_dev), *od = reinterpret_cast<uint8_t *>(out_dev);
+    const uint8_t *qh = reinterpret_cast<const uint8_t *>(q_host), *kh = reinterpret_cast<const uint8_t *>(k_host);
+    const uint8_t *vh = reinterpret_cast<const uint8_t *>(v_host);
+    uint8_t *oh = reinterpret_cast<uint8_t *>(out_host);
+    for (int g = 0; g < ng && !fail && st == ATTN_OK; ++g) {
+        const int b0 = bounds[g], b1 = bounds[g + 1];
+        const int64_t q0 = cu_seqlens_q_host[b0], q1 = cu_seqlens_q_host[b1];
+        const int64_t k0 = cu_seqlens_k_host[b0], k1 = cu_seqlens_k_host[b1];
+        int mq = 0, mk = 0;
+        for (int b = b0; b < b1; ++b) {
+            const int lq = cu_seqlens_q_host[b + 1] - cu_seqlens_q_host[b];
+            const int lk = cu_seqlens_k_host[b + 1] - cu_seqlens_k_host[b];
+            mq = lq > mq ? lq : mq;
+            mk = lk > mk ? lk : mk;
+        }
+        if (q1 > q0) ck(cudaMemcpyAsync(qd + q0 * qrow, qh + q0 * qrow, (q1 - q0) * qrow, cudaMemcpyHostToDevice, s_in));
+        if (k1 > k0) {
+            ck(cudaMemcpyAsync(kd + k0 * kvrow, kh + k0 * kvrow, (k1 - k0) * kvrow, cudaMemcpyHostToDevice, s_in));
+            ck(cudaMemcpyAsync(vd + k0 * kvrow, vh + k0 * kvrow, (k1 - k0) * kvrow, cudaMemcpyHostToDevice, s_in));
+        }
+        ck(cudaEventRecord(ev_a, s_in));
+        ck(cudaStreamWaitEvent(s_main, ev_a, 0));
+        if (fail) break;
+        st = varlen_impl(q_dev, k_dev, v_dev, out_dev, nullptr, cu_dev + b0, cu_dev + batch + 1 + b0, nullptr, nullptr,
+                         b1 - b0, total_q, total_k, mq, mk, num_heads_q, num_heads_kv, head_dim, softmax_scale,
+                         causal, nullptr, 0, 0, 0, 0, 0, 0, 0, workspace, workspace_bytes, stream);
+        ck(cudaEventRecord(ev_b, s_main));
+        ck(cudaStreamWaitEvent(s_out, ev_b, 0));
+        if (q1 > q0) ck(cudaMemcpyAsync(oh + q0 * qrow, od + q0 * qrow, (q1 - q0) * qrow, cudaMemcpyDeviceToHost, s_out));
+    }
+    // `stream` ends after the last copy out
+    ck(cudaEventRecord(ev_a, s_out));
+    ck(cudaStreamWaitEvent(s_main, ev_a, 0));
+    if (fail) {
+        cudaGetLastError();
+        return ATTN_ERR_LAUNCH_FAILED;
+    }
+    return st;
 }
 
 // ---------------------------------------------------------------------------

@@ -32,6 +32,8 @@
 //   This merge is exact because the update is associative ("计算流程（1-Pass
 //   算法与分块）": tiles may be folded in any grouping).  A split that holds no
 //   key a row may see leaves lse_s = -inf and weight 0.
+#include <mutex>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -331,7 +333,25 @@ __global__ void __launch_bounds__(kDecThreads) attn_decode_split_kernel(const __
         }
     }
     asm volatile("bar.sync 1, 128;" ::: "memory");
-    if (!ok) return;
+    if (!ok) {
+        // a bounded wait gave up (the error word says so): leave NaN, not the
+        // previous contents of the output or of the split partials, so that a
+        // result of this call can never look plausible
+        for (int i = threadIdx.x; i < NQ * D; i += 128) {
+            const int n = i / D, d = i % D;
+            const int h = hkv * p.G + (c0 + n) % p.G;
+            const int64_t row = (int64_t)b * p.Sq + (c0 + n) / p.G;
+            if (p.num_splits == 1) {
+                p.out[row * p.out_row_stride + (int64_t)h * D + d] = __float2bfloat16(NAN);
+                if (p.lse && d == 0) p.lse[row * p.lse_row_stride + (int64_t)h * p.lse_head_stride] = NAN;
+            } else {
+                const int64_t prow = (row * p.Hq + h) * p.num_splits + split;
+                p.o_part[prow * D + d] = NAN;
+                if (d == 0) p.lse_part[prow] = NAN;
+            }
+        }
+        return;
+    }
     for (int i = threadIdx.x; i < NQ * D; i += 128) {
         const int n = i / D, d = i % D;
         float M = -INFINITY;
@@ -419,15 +439,17 @@ template <int D, int NT>
 static cudaError_t launch_decode_t(const CUtensorMap &kmap, const CUtensorMap &vmap, const DecodeParams &p,
                                    int batch, cudaStream_t stream) {
     using S = DecSmem<D>;
-    static bool attr_done[64] = {false};
+    static std::once_flag attr_once[kMaxDev];
+    static cudaError_t attr_err[kMaxDev];
     int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev < 64 && !attr_done[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(attn_decode_split_kernel<D, NT>,
+    cudaError_t e0 = cudaGetDevice(&dev);
+    if (e0 != cudaSuccess) return e0;
+    if (dev < 0 || dev >= kMaxDev) return cudaErrorInvalidDevice;
+    std::call_once(attr_once[dev], [&] {
+        attr_err[dev] = cudaFuncSetAttribute(attn_decode_split_kernel<D, NT>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, S::kBytes);
-        if (e != cudaSuccess) return e;
-        attr_done[dev] = true;
-    }
+    });
+    if (attr_err[dev] != cudaSuccess) return attr_err[dev];
     dim3 grid(p.num_splits * p.ncg, p.Hkv, batch);
     main_kernel_event_before(stream);
     attn_decode_split_kernel<D, NT><<<grid, kDecThreads, S::kBytes, stream>>>(kmap, vmap, p);
@@ -465,36 +487,34 @@ namespace attn {
 // bytes until the process exits.  All calls share it: two calls that overlap
 // on the GPU (different streams, no ordering between them) race on it.
 // Nothing in it needs clearing between calls: every partial the combine
-// kernel reads is written earlier by the same call.
+// kernel reads is written earlier by the same call (a split CTA whose bounded
+// wait gave up writes NaN partials, so stale contents never reach the output).
 // ---------------------------------------------------------------------------
 namespace {
 constexpr size_t kNoAllocScratchBytes = 32ull << 20;   // 32 MiB
 static __device__ __align__(256) float g_decode_noalloc_scratch[kNoAllocScratchBytes / sizeof(float)];
 
-struct ScratchAddr {
-    bool ready = false;
-    float *ptr = nullptr;
-};
-ScratchAddr g_scratch_addr[64];
+std::once_flag g_scratch_once[kMaxDev];
+float *g_scratch_ptr[kMaxDev];
+cudaError_t g_scratch_err[kMaxDev];
 }  // namespace
 
 // Device address of the static scratch on the current device.  The first call
-// on a device looks it up (cudaGetSymbolAddress, with that device current);
-// later calls reuse the cached address.
+// on a device looks it up (cudaGetSymbolAddress, with that device current),
+// once even if several host threads get there together; later calls reuse the
+// cached address.
 cudaError_t decode_noalloc_scratch(float **ptr, size_t *bytes) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    ScratchAddr &s = g_scratch_addr[dev];
-    if (!s.ready) {
+    if (dev < 0 || dev >= kMaxDev) return cudaErrorInvalidDevice;
+    std::call_once(g_scratch_once[dev], [&] {
         void *p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_decode_noalloc_scratch);
-        if (e != cudaSuccess) return e;
-        s.ptr = reinterpret_cast<float *>(p);
-        s.ready = true;
-    }
-    *ptr = s.ptr;
+        g_scratch_err[dev] = cudaGetSymbolAddress(&p, g_decode_noalloc_scratch);
+        g_scratch_ptr[dev] = reinterpret_cast<float *>(p);
+    });
+    if (g_scratch_err[dev] != cudaSuccess) return g_scratch_err[dev];
+    *ptr = g_scratch_ptr[dev];
     *bytes = kNoAllocScratchBytes;
     return cudaSuccess;
 }

@@ -11,6 +11,9 @@
 
 namespace attn {
 
+// devices the per-device lazy set-ups (function attributes, symbol addresses) cover
+constexpr int kMaxDev = 64;
+
 struct DecodeParams {
     const __nv_bfloat16 *q;      // [B * Sq, Hq, D], row stride q_row_stride
     __nv_bfloat16 *out;          // [B * Sq, Hq, D], row stride out_row_stride

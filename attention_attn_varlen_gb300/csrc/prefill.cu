@@ -64,6 +64,8 @@
 // max exceeds it by more than 8 (log2 units), so P stays <= 256 and O is
 // rarely touched; the final O / d' uses the same reference, so the result is
 // unchanged.
+#include <mutex>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -903,15 +905,17 @@ template <int D>
 static cudaError_t launch_prefill_t(const CUtensorMap &qmap, const CUtensorMap &kmap, const CUtensorMap &vmap,
                                     const PrefillParams &p, cudaStream_t stream) {
     using S = PfSmem<D>;
-    static bool attr_done[64] = {false};
+    static std::once_flag attr_once[kMaxDev];
+    static cudaError_t attr_err[kMaxDev];
     int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev < 64 && !attr_done[dev]) {
-        cudaError_t e =
+    cudaError_t e0 = cudaGetDevice(&dev);
+    if (e0 != cudaSuccess) return e0;
+    if (dev < 0 || dev >= kMaxDev) return cudaErrorInvalidDevice;
+    std::call_once(attr_once[dev], [&] {
+        attr_err[dev] =
             cudaFuncSetAttribute(attn_prefill_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kBytes);
-        if (e != cudaSuccess) return e;
-        attr_done[dev] = true;
-    }
+    });
+    if (attr_err[dev] != cudaSuccess) return attr_err[dev];
     // unit list and V' in one launch: one extra row of CTAs (y = batch) holds the scheduler
     dim3 cgrid((p.max_seqlen_k + kCvtKeys - 1) / kCvtKeys, p.batch + 1);
     attn_prefill_prep_kernel<<<cgrid, kCvtThreads, 0, stream>>>(p);

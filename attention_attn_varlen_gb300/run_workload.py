@@ -13,6 +13,9 @@ with the device error status.  No timing, no comparison.
   --op softmax  attn_softmax_rows on a seeded [--rows, --cols] matrix (--dtype f32 | bf16;
                 --workload is ignored)
   --seqs N      keep only the first N sequences (smaller captures)
+  --compact-pool  paged workloads: a pool of just the blocks the block table
+                uses, ids randomly permuted (same block size, lengths and
+                shared-prefix blocks; for profiler captures of a few GB at most)
 """
 from __future__ import annotations
 
@@ -42,6 +45,20 @@ def _trim(cfg, n):
     return cfg
 
 
+def _compact_pool(cfg, seed=7):
+    """Renumber the referenced blocks into a pool of exactly that many blocks
+    (random order); contents are keyed by logical (sequence, block), so the
+    workload is unchanged apart from the physical ids."""
+    bt = cfg.block_table
+    ids = np.unique(bt[bt >= 0])
+    perm = np.random.default_rng(seed).permutation(len(ids)).astype(np.int32)
+    remap = np.full(int(ids.max()) + 1, -1, dtype=np.int32)
+    remap[ids] = perm
+    cfg.block_table = np.where(bt >= 0, remap[np.maximum(bt, 0)], -1).astype(np.int32)
+    cfg.num_blocks = len(ids)
+    return cfg
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--workload", default="c2_varlen_gqa", choices=workloads.CONFIG_NAMES)
@@ -52,6 +69,7 @@ def main(argv=None):
     ap.add_argument("--sq", type=int, default=4, help="new query tokens per sequence (--op kvcache)")
     ap.add_argument("--iters", type=int, default=3)
     ap.add_argument("--seqs", type=int, default=None)
+    ap.add_argument("--compact-pool", action="store_true")
     a = ap.parse_args(argv)
     av.lib()
     dev = torch.device("cuda", 0)
@@ -67,6 +85,8 @@ def main(argv=None):
         print(f"softmax {a.rows}x{a.cols} {a.dtype} x{a.iters}: device status {st} word {word:#x}")
         return 0 if st == 0 else 1
     cfg = _trim(workloads.make(a.workload), a.seqs)
+    if a.compact_pool and isinstance(cfg, workloads.Paged):
+        cfg = _compact_pool(cfg)
     if isinstance(cfg, workloads.Varlen):
         if a.op != "prefill":
             raise SystemExit("contiguous workloads only have --op prefill")

@@ -6,17 +6,28 @@ Main line: varlen causal prefill, 16 sequences with L ~ U{256..4096} (Lq = Lk),
 GQA 32/8, head_dim 128, bf16 (the prefill half of the metric), in TFLOP/s of
 algorithmic work (4 * D * Hq * visible pairs).  One step = one attn_varlen_fwd
 call over the batch.  L2 is flushed (a 512 MB write) between timed steps,
-outside the timed events.  The same line carries the decode half of the metric
-(256-sequence paged decode, KV GB/s) and the other workloads as extra objects,
-each with its roofline, plus:
-  roofline      dominant kernel: algorithmic FLOPs per launch / event time,
-                against MEASURED_PEAKS.json
-  cpu_baseline  the float64 oracle on a bounded sample of the same workload,
+outside the timed events.  The same line carries every other workload as an
+extra object with its roofline and the oracle timed on a sample of it:
+  tiny_prefill    the article's 3-sequence example (launch-bound)
+  decode          256-sequence paged decode (KV GB/s, the decode half of the
+                  metric) and 4 / 8 new tokens per sequence on the same cache
+  prefix_prefill  store_kvcache + paged prefix-cache prefill
+  long_prefill    2 x 32k tokens with logits ~700 on half the heads
+  row_softmax, padded_prefill
+Each roofline is the dominant kernel's algorithmic work per launch over its
+own device time (events the library records around that launch), against the
+measured peaks of MEASURED_PEAKS.json: the bf16 burst figure for every
+prefill (each kernel is timed by itself at full clocks), the copy bandwidth
+for the HBM-bound kernels.
+  cpu_baseline  the float64 oracle on a bounded sample of the main workload,
                 timed on this host's cores (rank 0, N = 1 only)
-  e2e           the same metric through the public call with host buffers:
-                pinned host -> device copies of q, k, v, cu_seqlens, the kernel,
-                and the device -> host copy of the output, all inside the events
+  e2e           the same metric through the C entry attn_varlen_fwd_host with
+                host buffers: pinned host -> device copies of q, k, v and
+                cu_seqlens, the kernels, and the device -> host copy of the
+                output, all inside the events
   clocks        nvidia-smi samples taken while the measurements ran
+  summary       (last key) one compact entry per workload: step value, kernel
+                value, roofline fraction, oracle value
 
 Under torchrun (N > 1) every rank runs its own independent batch (replicas,
 weak scaling: the units never need another rank's data); the timing is
@@ -156,6 +167,7 @@ def src_digest(files) -> str:
 
 KERNEL_SOURCES = {
     "prefill": ["attention_attn_varlen_gb300/csrc/prefill.cu", "attention_attn_varlen_gb300/csrc/common.cuh"],
+    "prefill_paged": ["attention_attn_varlen_gb300/csrc/prefill.cu", "attention_attn_varlen_gb300/csrc/common.cuh"],
     "decode": ["attention_attn_varlen_gb300/csrc/decode.cu", "attention_attn_varlen_gb300/csrc/common.cuh"],
     "decode_sq4": ["attention_attn_varlen_gb300/csrc/decode.cu", "attention_attn_varlen_gb300/csrc/common.cuh"],
     "decode_sq8": ["attention_attn_varlen_gb300/csrc/decode.cu", "attention_attn_varlen_gb300/csrc/common.cuh"],
@@ -244,32 +256,53 @@ def bench_varlen(av, cfg, inp, steps, warmup, flush):
 
 
 def bench_varlen_e2e(av, cfg, inp, steps, warmup, flush):
-    """Host buffers in, host buffer out, through the public host-input call
-    (attn_varlen_fwd_host: the copies of one group of sequences overlap the
-    attention of another)."""
+    """Host buffers in, host buffer out, through the C entry attn_varlen_fwd_host
+    (the library copies one group of sequences in while it runs the attention of
+    the previous group and copies an earlier group's output back)."""
     import torch
     hq, hk, hv = (inp[n].cpu().pin_memory() for n in ("q", "k", "v"))
     hcq, hck = inp["cu_q"].cpu().pin_memory(), inp["cu_k"].cpu().pin_memory()
     hout = torch.empty(hq.shape, dtype=hq.dtype).pin_memory()
+    staging = av.host_staging(cfg.batch, hq.shape[0], hk.shape[0], cfg.Hq, cfg.Hkv, cfg.D, inp["mq"])
 
     def step():
-        av.attn_varlen_fwd_host(hq, hk, hv, hcq, hck, inp["mq"], inp["mk"], cfg.scale, out=hout)
+        av.attn_varlen_fwd_host(hq, hk, hv, hcq, hck, inp["mq"], inp["mk"], cfg.scale, out=hout, staging=staging)
     for _ in range(warmup):
         step()
     torch.cuda.synchronize()
     ms = time_steps(step, steps, flush)
     h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hcq, hck))
     d2h = hout.numel() * hout.element_size()
+    del staging
     return ms, h2d, d2h
 
 
-def bench_decode(av, device, steps, warmup, flush, peaks):
+def oracle_timed(fn, min_seconds: float = 0.0):
+    """Run fn() (an oracle call) until at least min_seconds have passed; returns
+    (seconds per call, calls)."""
+    t0 = time.perf_counter()
+    n = 0
+    while True:
+        fn()
+        n += 1
+        t = time.perf_counter() - t0
+        if t >= min_seconds:
+            return t / n, n
+
+
+def oracle_line(value, unit, sample, seconds):
+    return {"value": value, "unit": unit, "cores": os.cpu_count(), "kind": "oracle", "sample": sample,
+            "seconds": seconds}
+
+
+def bench_decode(av, device, steps, warmup, flush, peaks, with_oracle=True):
     import torch
     cfg = workloads.make("c4_decode")
     kc = torch.empty((cfg.num_blocks, cfg.block_size, cfg.Hkv, cfg.D), dtype=torch.bfloat16, device=device)
     vc = torch.empty_like(kc)
     workloads.fill_paged_cache(cfg, kc, vc)
-    q = cfg.q().to(device)
+    qh = cfg.q()
+    q = qh.to(device)
     cs = torch.from_numpy(cfg.ctx.astype(np.int32)).to(device)
     bt = torch.from_numpy(cfg.block_table).to(device)
     out = torch.empty_like(q)
@@ -297,76 +330,62 @@ def bench_decode(av, device, steps, warmup, flush, peaks):
                         "kernel_ms": tk * 1e3,
                         "traffic": ncu_traffic("decode", float(cfg.ctx.sum()) * cfg.Hkv)},
            "launches_per_step": 2 if splits > 1 else 1}
-    # the same cache, 4 new query tokens per sequence (multi-token decode through
-    # attn_with_kvcache; the last 4 cached tokens are the new ones)
-    Sq = 4
+    # the same cache, Sq new query tokens per sequence (multi-token decode through
+    # attn_with_kvcache; the last Sq cached tokens are the new ones)
     g = torch.Generator(device=device).manual_seed(4321)
-    q4 = torch.randn(cfg.batch, Sq, cfg.Hq, cfg.D, device=device, generator=g).to(torch.bfloat16)
-    ws4 = torch.empty(av.lib().attn_kvcache_workspace_size(cfg.batch, Sq, cfg.Hq, cfg.Hkv, cfg.D, mx),
-                      dtype=torch.uint8, device=device)
-    out4 = torch.empty_like(q4)
+    for Sq in (4, 8):
+        qn = torch.randn(cfg.batch, Sq, cfg.Hq, cfg.D, device=device, generator=g).to(torch.bfloat16)
+        wsn = torch.empty(av.lib().attn_kvcache_workspace_size(cfg.batch, Sq, cfg.Hq, cfg.Hkv, cfg.D, mx),
+                          dtype=torch.uint8, device=device)
+        outn = torch.empty_like(qn)
 
-    def step4():
-        av.attn_with_kvcache(q4, kc, vc, cs, bt, cfg.scale, max_cache_seqlen=mx, out=out4, workspace=ws4)
-    for _ in range(warmup):
-        step4()
-    torch.cuda.synchronize()
-    ms4, kms4 = time_steps(step4, steps, flush, kernel=True)
-    t4 = float(np.mean(ms4)) / 1e3
-    tk4 = float(np.mean(kms4)) / 1e3
-    fl4 = workloads.prefill_flops(np.full(cfg.batch, Sq), cfg.ctx, cfg.Hq, cfg.D)
-    nbytes4 = nbytes + 2 * cfg.batch * (Sq - 1) * cfg.Hq * cfg.D * 2    # the extra query and output rows
-    # 4 tokens x 4 heads = 16 query rows per KV head: the split-KV decode kernel
-    splits4 = av.lib().attn_decode_num_splits(cfg.batch, cfg.Hkv, mx, 0)
-    res["kvcache_4_tokens"] = {
-        "workload": "c4_decode cache, 4 new query tokens per sequence (attn_with_kvcache: split-KV decode kernel "
-                    "with 16 query rows per KV head, bottom-right causal)",
-        "value": nbytes4 / t4 / 1e9, "unit": "GB/s", "tflops": fl4 / t4 / 1e12, "ms_per_step": t4 * 1e3,
-        "algorithmic_bytes": nbytes4,
-        "roofline": {"bound": "hbm", "kernel": "attn_decode_split_kernel", "achieved": nbytes4 / tk4 / 1e9,
-                     "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": nbytes4 / tk4 / 1e9 / peaks["hbm_gbs"],
-                     "kernel_ms": tk4 * 1e3,
-                     "traffic": ncu_traffic("decode_sq4", float(cfg.ctx.sum()) * cfg.Hkv)},
-        "launches_per_step": 2 if splits4 > 1 else 1}
-    # 8 new tokens: 32 query columns per KV head, two column groups of CTAs that
-    # share each K/V tile (the second read comes from L2)
-    Sq8 = 8
-    q8 = torch.randn(cfg.batch, Sq8, cfg.Hq, cfg.D, device=device, generator=g).to(torch.bfloat16)
-    ws8 = torch.empty(av.lib().attn_kvcache_workspace_size(cfg.batch, Sq8, cfg.Hq, cfg.Hkv, cfg.D, mx),
-                      dtype=torch.uint8, device=device)
-    out8 = torch.empty_like(q8)
-
-    def step8():
-        av.attn_with_kvcache(q8, kc, vc, cs, bt, cfg.scale, max_cache_seqlen=mx, out=out8, workspace=ws8)
-    for _ in range(warmup):
-        step8()
-    torch.cuda.synchronize()
-    ms8, kms8 = time_steps(step8, steps, flush, kernel=True)
-    t8 = float(np.mean(ms8)) / 1e3
-    tk8 = float(np.mean(kms8)) / 1e3
-    nbytes8 = nbytes + 2 * cfg.batch * (Sq8 - 1) * cfg.Hq * cfg.D * 2
-    res["kvcache_8_tokens"] = {
-        "workload": "c4_decode cache, 8 new query tokens per sequence (attn_with_kvcache: split-KV decode kernel, "
-                    "32 query rows per KV head in two column groups)",
-        "value": nbytes8 / t8 / 1e9, "unit": "GB/s", "ms_per_step": t8 * 1e3, "algorithmic_bytes": nbytes8,
-        "roofline": {"bound": "hbm", "kernel": "attn_decode_split_kernel", "achieved": nbytes8 / tk8 / 1e9,
-                     "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": nbytes8 / tk8 / 1e9 / peaks["hbm_gbs"],
-                     "kernel_ms": tk8 * 1e3,
-                     "traffic": ncu_traffic("decode_sq8", float(cfg.ctx.sum()) * cfg.Hkv)},
-        "launches_per_step": 2 if splits4 > 1 else 1}
+        def stepn():
+            av.attn_with_kvcache(qn, kc, vc, cs, bt, cfg.scale, max_cache_seqlen=mx, out=outn, workspace=wsn)
+        for _ in range(warmup):
+            stepn()
+        torch.cuda.synchronize()
+        msn, kmsn = time_steps(stepn, steps, flush, kernel=True)
+        tn = float(np.mean(msn)) / 1e3
+        tkn = float(np.mean(kmsn)) / 1e3
+        fln = workloads.prefill_flops(np.full(cfg.batch, Sq), cfg.ctx, cfg.Hq, cfg.D)
+        nbn = nbytes + 2 * cfg.batch * (Sq - 1) * cfg.Hq * cfg.D * 2    # the extra query and output rows
+        res[f"kvcache_{Sq}_tokens"] = {
+            "workload": f"c4_decode cache, {Sq} new query tokens per sequence (attn_with_kvcache: split-KV decode "
+                        f"kernel, {Sq * cfg.Hq // cfg.Hkv} query rows per KV head, bottom-right causal)",
+            "value": nbn / tn / 1e9, "unit": "GB/s", "tflops": fln / tn / 1e12, "ms_per_step": tn * 1e3,
+            "algorithmic_bytes": nbn,
+            "roofline": {"bound": "hbm", "kernel": "attn_decode_split_kernel", "achieved": nbn / tkn / 1e9,
+                         "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": nbn / tkn / 1e9 / peaks["hbm_gbs"],
+                         "kernel_ms": tkn * 1e3,
+                         "traffic": ncu_traffic(f"decode_sq{Sq}", float(cfg.ctx.sum()) * cfg.Hkv)},
+            "launches_per_step": 2 if splits > 1 else 1}
+        del qn, wsn, outn
     del kc, vc
     torch.cuda.empty_cache()
+    if with_oracle:
+        # the oracle on 48 of the 256 sequences, every query row
+        seqs = sorted(np.random.default_rng(cfg.seed + 11).choice(cfg.batch, 48, replace=False).tolist())
+        kp, vp, btc = workloads.compact_paged(cfg, seqs)
+        qs = qh[torch.tensor(seqs)]
+        import oracle
+        oracle.build()
+        sec, n = oracle_timed(lambda: oracle.decode_paged(qs, kp, vp, cfg.ctx[seqs], btc, cfg.Hq, cfg.Hkv, cfg.D,
+                                                          cfg.block_size, kp.shape[0], cfg.scale))
+        ob = workloads.decode_bytes(cfg.ctx[seqs], cfg.Hq, cfg.Hkv, cfg.D, cfg.block_size)
+        res["oracle"] = oracle_line(ob / sec / 1e9, "GB/s", f"48 of 256 sequences, all their query rows "
+                                    f"({int(cfg.ctx[seqs].sum())} cached tokens); float64, OpenMP", sec)
     return res
 
 
-def bench_prefix(av, device, steps, warmup, flush, peaks):
+def bench_prefix(av, device, steps, warmup, flush, peaks, with_oracle=True):
     import torch
     cfg = workloads.make("c3_prefix_paged")
     kc = torch.empty((cfg.num_blocks, cfg.block_size, cfg.Hkv, cfg.D), dtype=torch.bfloat16, device=device)
     vc = torch.empty_like(kc)
     workloads.fill_paged_cache(cfg, kc, vc)
-    q = cfg.q().to(device)
-    k_new, v_new = cfg.k_new().to(device), cfg.v_new().to(device)
+    qh, k_new_h, v_new_h = cfg.q(), cfg.k_new(), cfg.v_new()
+    q = qh.to(device)
+    k_new, v_new = k_new_h.to(device), v_new_h.to(device)
     slots = torch.from_numpy(cfg.slot_mapping()).to(device)
     cu_q = torch.from_numpy(workloads.cu_from_lens(cfg.new)).to(device)
     cu_k = torch.from_numpy(workloads.cu_from_lens(cfg.lens_k)).to(device)
@@ -402,12 +421,42 @@ def bench_prefix(av, device, steps, warmup, flush, peaks):
            "attn_ms": ta * 1e3, "store_ms": ts * 1e3,
            "roofline": {"bound": "tensor", "kernel": "attn_prefill_kernel", "achieved": flops / tk / 1e12,
                         "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                        "frac": flops / tk / 1e12 / peaks["bf16_tflops"], "kernel_ms": tk * 1e3, "traffic": None},
+                        "frac": flops / tk / 1e12 / peaks["bf16_tflops"], "kernel_ms": tk * 1e3,
+                        "traffic": ncu_traffic("prefill_paged", float(cfg.new.sum()))},
            "store_kvcache": {"value": sbytes / ts / 1e9, "unit": "GB/s", "frac": sbytes / ts / 1e9 / peaks["hbm_gbs"],
-                             "tokens": int(cfg.new.sum())},
+                             "tokens": int(cfg.new.sum()), "ms": ts * 1e3,
+                             "traffic": ncu_traffic("store", float(cfg.new.sum()))},
            "launches_per_step": 3}
     del kc, vc
     torch.cuda.empty_cache()
+    if with_oracle:
+        # the oracle on 6 sequences (3 of them sharing the prefix), 1/16 of their query rows,
+        # after its own store of their new tokens into a compact pool
+        import oracle
+        oracle.build()
+        seqs = [0, 3, 7, 12, 20, 31]
+        kp, vp, btc = workloads.compact_paged(cfg, seqs)
+        bs = cfg.block_size
+        cu_new = workloads.cu_from_lens(cfg.new)
+        sl, tok = [], []
+        for r, b in enumerate(seqs):
+            j = np.arange(int(cfg.ctx[b]), int(cfg.ctx[b] + cfg.new[b]))
+            sl.append(btc[r, j // bs].astype(np.int64) * bs + j % bs)
+            tok.append(np.arange(cu_new[b], cu_new[b + 1]))
+        sl, tok = np.concatenate(sl), np.concatenate(tok)
+        kb, vb = oracle.store_kvcache(k_new_h[tok], v_new_h[tok], kp, vp, sl)
+        kb, vb = kb.reshape(kp.shape), vb.reshape(vp.shape)
+        qs = qh[torch.from_numpy(tok)]
+        lq, lk = cfg.new[seqs], cfg.lens_k[seqs]
+        cq, ckk = workloads.cu_from_lens(lq), workloads.cu_from_lens(lk)
+        rows = workloads.sample_rows(cfg.seed + 12, len(tok) * cfg.Hq, 1 / 16)
+        sec, n = oracle_timed(lambda: oracle.attn_varlen(qs, kb, vb, cq, ckk, cfg.Hq, cfg.Hkv, cfg.D, cfg.scale, True,
+                                                         block_table=btc, block_size=bs, num_blocks=kp.shape[0],
+                                                         rows=rows))
+        fl = rows_flops_lens(lq, lk, cfg.Hq, cfg.D, rows)
+        res["oracle"] = oracle_line(fl / sec / 1e12, "TFLOP/s", f"{len(rows)} query rows (1/16) of 6 of the 32 "
+                                    f"sequences, paged through a compact pool; {fl / 1e9:.1f} GFLOP; float64, OpenMP",
+                                    sec)
     return res
 
 
@@ -479,22 +528,51 @@ def bench_softmax(av, device, steps, warmup, flush, peaks):
     return res
 
 
-def bench_long(av, device, steps, warmup, flush, peaks):
+def bench_contig(av, name, device, steps, warmup, flush, peaks, with_oracle=True):
+    """A contiguous varlen workload (c1_tiny, c5_long) through attn_varlen_fwd,
+    with the oracle on the whole workload (c1) or 4 (sequence, head) pairs (c5)."""
     import torch
-    cfg = workloads.make("c5_long")
-    inp = varlen_inputs(cfg, device)
+    cfg = workloads.make(name)
+    qh, kh, vh = cfg.q(), cfg.k(), cfg.v()
+    inp = dict(q=qh.to(device), k=kh.to(device), v=vh.to(device), cu_q=torch.from_numpy(cfg.cu_q).to(device),
+               cu_k=torch.from_numpy(cfg.cu_k).to(device), mq=int(cfg.lens_q.max()), mk=int(cfg.lens_k.max()))
     ms, _, kms = bench_varlen(av, cfg, inp, steps, warmup, flush)
     flops = workloads.prefill_flops(cfg.lens_q, cfg.lens_k, cfg.Hq, cfg.D)
     t = float(np.mean(ms)) / 1e3
     tk = float(np.mean(kms)) / 1e3
-    res = {"workload": "c5_long: 2 x 32768 tokens, MHA 32 heads, D128, heads 0-15 with Q x160 (logits ~700)",
-           "value": flops / t / 1e12, "unit": "TFLOP/s", "ms_per_step": t * 1e3,
+    desc = {"c1_tiny": "c1_tiny: the article's example, cu_seqlens_q [0,5,7,8], cu_seqlens_k [0,9,16,19], 4 heads, "
+                       "D64 (launch-bound: 52 kFLOP)",
+            "c5_long": "c5_long: 2 x 32768 tokens, MHA 32 heads, D128, heads 0-15 with Q x160 (logits ~700)"}[name]
+    res = {"workload": desc, "value": flops / t / 1e12, "unit": "TFLOP/s", "ms_per_step": t * 1e3,
+           "algorithmic_flops": flops,
            "roofline": {"bound": "tensor", "kernel": "attn_prefill_kernel", "achieved": flops / tk / 1e12,
-                        "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
-                        "frac": flops / tk / 1e12 / peaks["bf16_tflops_sustained"], "kernel_ms": tk * 1e3,
-                        "traffic": None}}
+                        "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                        "frac": flops / tk / 1e12 / peaks["bf16_tflops"], "kernel_ms": tk * 1e3,
+                        "traffic": None, "peak_source": "measured bf16 burst"},
+           "launches_per_step": 2}
     del inp
     torch.cuda.empty_cache()
+    if with_oracle:
+        import oracle
+        oracle.build()
+        if name == "c1_tiny":
+            sec, n = oracle_timed(lambda: oracle.attn_varlen(qh, kh, vh, cfg.cu_q, cfg.cu_k, cfg.Hq, cfg.Hkv, cfg.D,
+                                                             cfg.scale, True), 0.5)
+            res["oracle"] = oracle_line(flops / sec / 1e12, "TFLOP/s", f"the whole workload (32 query rows), mean "
+                                        f"of {n} calls; float64, OpenMP", sec)
+        else:
+            rng = np.random.default_rng(cfg.seed + 13)
+            rows = []
+            for b, h in [(0, 3), (1, 12), (0, 20), (1, 31)]:
+                i = np.sort(rng.choice(int(cfg.lens_q[b]), 256, replace=False))
+                rows.append((int(cfg.cu_q[b]) + i) * cfg.Hq + h)
+            rows = np.concatenate(rows).astype(np.int64)
+            sec, n = oracle_timed(lambda: oracle.attn_varlen(qh, kh, vh, cfg.cu_q, cfg.cu_k, cfg.Hq, cfg.Hkv, cfg.D,
+                                                             cfg.scale, True, rows=rows))
+            fl = rows_flops_lens(cfg.lens_q, cfg.lens_k, cfg.Hq, cfg.D, rows)
+            res["oracle"] = oracle_line(fl / sec / 1e12, "TFLOP/s", f"{len(rows)} query rows: 256 of each of 4 "
+                                        f"(sequence, head) pairs, two with logits ~700; {fl / 1e9:.1f} GFLOP; "
+                                        f"float64, OpenMP", sec)
     return res
 
 
@@ -509,18 +587,24 @@ def oracle_sample_run(cfg, q, k, v, rows):
     return time.perf_counter() - t0
 
 
+def rows_flops_lens(lens_q, lens_k, Hq, D, rows):
+    """Algorithmic flops of sampled query rows (row id = token * Hq + head of a
+    varlen packing with these lengths): 4 * D * visible keys each."""
+    lens_q = np.asarray(lens_q, dtype=np.int64)
+    lens_k = np.asarray(lens_k, dtype=np.int64)
+    cu = workloads.cu_from_lens(lens_q)
+    t = np.asarray(rows, dtype=np.int64) // Hq
+    b = np.searchsorted(cu, t, side="right") - 1
+    i = t - cu[b]
+    vis = np.clip(lens_k[b] - lens_q[b] + i + 1, 0, lens_k[b])
+    return float(4 * D * vis.sum())
+
+
 def rows_flops(cfg, rows):
-    """Algorithmic flops of the sampled query rows (4 * D * visible keys each)."""
-    t = rows // cfg.Hq
-    b = np.searchsorted(cfg.cu_q, t, side="right") - 1
-    i = t - cfg.cu_q[b]
-    Lq = cfg.lens_q[b]
-    Lk = cfg.lens_k[b]
-    vis = np.clip(Lk - Lq + i + 1, 0, Lk)
-    return float(4 * cfg.D * vis.sum())
+    return rows_flops_lens(cfg.lens_q, cfg.lens_k, cfg.Hq, cfg.D, rows)
 
 
-def cpu_baseline(cfg, q, k, v, target_s: float = 12.0):
+def cpu_baseline(cfg, q, k, v, target_s: float = 8.0):
     import oracle
     oracle.build()
     n_rows = q.shape[0] * cfg.Hq
@@ -571,6 +655,57 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def _r(x, nd=4):
+    """Round for the compact summary (significant digits)."""
+    if x is None or not isinstance(x, (int, float)) or x == 0 or not math.isfinite(x):
+        return x
+    return float(f"{x:.{nd}g}")
+
+
+def summary(line, peaks, peak_src):
+    """Compact per-workload table: step value, dominant-kernel value, roofline
+    fraction (against the measured peaks) and the oracle's value, one entry per
+    workload, so that the end of the line carries every number."""
+    out = {}
+
+    def put(key, d, oracle=None, extra=None):
+        if not d:
+            return
+        rf = d.get("roofline", {})
+        e = {"value": _r(d.get("value")), "unit": d.get("unit"), "kernel": _r(rf.get("achieved")),
+             "frac": _r(rf.get("frac", d.get("frac")), 3), "ms": _r(d.get("ms_per_step"))}
+        if oracle:
+            e["oracle"] = _r(oracle.get("value"))
+        if extra:
+            e.update(extra)
+        out[key] = {k: v for k, v in e.items() if v is not None}
+
+    main = {"value": line["value"], "unit": "TFLOP/s", "roofline": line["roofline"], "ms_per_step": line["ms_per_step"]}
+    put("c2", main, line.get("cpu_baseline"), {"step_frac": _r(line["value"] / peaks["bf16_tflops"], 3),
+                                               "e2e": _r(line["e2e"]["value"])})
+    put("c1", line.get("tiny_prefill"), (line.get("tiny_prefill") or {}).get("oracle"))
+    c3 = line.get("prefix_prefill")
+    if c3:
+        put("c3", c3, c3.get("oracle"), {"step_frac": _r(c3["value"] / peaks["bf16_tflops"], 3)})
+        st = c3["store_kvcache"]
+        out["c3_store"] = {"value": _r(st["value"]), "unit": "GB/s", "frac": _r(st["frac"], 3), "ms": _r(st["ms"])}
+    c4 = line.get("decode")
+    if c4:
+        put("c4", c4, c4.get("oracle"))
+        put("c4_sq4", c4.get("kvcache_4_tokens"))
+        put("c4_sq8", c4.get("kvcache_8_tokens"))
+    c5 = line.get("long_prefill")
+    if c5:
+        put("c5", c5, c5.get("oracle"), {"step_frac": _r(c5["value"] / peaks["bf16_tflops"], 3)})
+    sm = line.get("row_softmax")
+    if sm:
+        put("softmax_f32", sm.get("f32_32768x8192"))
+        put("softmax_bf16", sm.get("bf16_262144x1024"))
+    put("padded", line.get("padded_prefill"))
+    out["peaks"] = {"bf16_burst_tflops": peaks["bf16_tflops"], "hbm_gbs": peaks["hbm_gbs"], "source": peak_src}
+    return out
+
+
 # --------------------------------------------------------------------------
 def main():
     ap = argparse.ArgumentParser()
@@ -579,6 +714,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--only-main", action="store_true", help="skip the extra workloads")
+    ap.add_argument("--no-oracle", action="store_true", help="skip the oracle timings")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
 
@@ -596,6 +732,7 @@ def main():
     av.build()
     av.lib()
     peaks, peak_src = load_peaks()
+    with_oracle = rank == 0 and world == 1 and not args.no_oracle
 
     flush_buf = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=device)
 
@@ -619,12 +756,17 @@ def main():
     achieved = flops / (kernel_ms / 1e3) / 1e12
     e2e_ms, h2d, d2h = bench_varlen_e2e(av, cfg, inp, args.steps, args.warmup, flush)
     e2e_max = dist_max(float(np.mean(e2e_ms)), device)
+    del inp
+    torch.cuda.empty_cache()
 
     extras = {}
     if not args.only_main:
-        extras["decode"] = bench_decode(av, device, args.steps, args.warmup, flush, peaks)
-        extras["prefix_prefill"] = bench_prefix(av, device, args.steps, args.warmup, flush, peaks)
-        extras["long_prefill"] = bench_long(av, device, max(3, args.steps // 3), args.warmup, flush, peaks)
+        extras["tiny_prefill"] = bench_contig(av, "c1_tiny", device, args.steps, args.warmup, flush, peaks,
+                                              with_oracle)
+        extras["decode"] = bench_decode(av, device, args.steps, args.warmup, flush, peaks, with_oracle)
+        extras["prefix_prefill"] = bench_prefix(av, device, args.steps, args.warmup, flush, peaks, with_oracle)
+        extras["long_prefill"] = bench_contig(av, "c5_long", device, max(3, args.steps // 3), args.warmup, flush,
+                                              peaks, with_oracle)
         extras["row_softmax"] = bench_softmax(av, device, args.steps, args.warmup, flush, peaks)
         extras["padded_prefill"] = bench_padded(av, device, args.steps, args.warmup, flush, peaks)
     clocks = sampler.stop()
@@ -646,7 +788,8 @@ def main():
                      "peak_source": f"{peak_src} bf16 burst (MEASURED_PEAKS.json)" if peak_src == "measured"
                      else "fallback 1.9 PFLOP/s"},
         "e2e": {"value": aggregate(flops, e2e_max / 1e3, world) / 1e12, "unit": "TFLOP/s",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_max},
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_max,
+                "path": "C entry attn_varlen_fwd_host: pinned host q/k/v in, host out, 8 overlapped groups"},
         # per step: the pre-pass (unit list + fp16 V') and the attention kernel
         "gpu_launches": 2 * args.steps,
         "clocks": clocks,
@@ -654,8 +797,9 @@ def main():
         "device_status": status,
     }
     line.update(extras)
-    if rank == 0 and world == 1:
+    if with_oracle:
         line["cpu_baseline"] = cpu_baseline(cfg, cfg.q(), cfg.k(), cfg.v())
+    line["summary"] = summary(line, peaks, peak_src)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -29,7 +29,12 @@
  *    recorded in the device error word (attn_get_last_device_error).
  *  - head_dim must be 64 or 128; num_heads_q must be a multiple of
  *    num_heads_kv (GQA: query head h reads KV head h / (num_heads_q /
- *    num_heads_kv)).
+ *    num_heads_kv)).  The prefill kernels (attn_varlen_fwd, attn_padded_fwd,
+ *    the prefill route of attn_kvcache_fwd) also need the group size
+ *    G = num_heads_q / num_heads_kv to divide 128 (G in 1, 2, 4, 8, ..., 128):
+ *    a 128-row query slot packs 128 / G tokens x G heads.  Other groups
+ *    (3, 5, 6, 7, ...) return ATTN_ERR_UNSUPPORTED there; the decode kernels
+ *    take any G up to 64.
  *  - No function aborts, throws or prints.
  */
 #ifndef ATTN_VARLEN_H
@@ -98,6 +103,8 @@ typedef enum attn_status {
  * Value range: the P V product runs in fp16 on 16 P and V / 16, so V entries
  * must satisfy |v| < 2^20; larger (or non-finite) entries are clamped and
  * reported as ATTN_ERR_DEVICE_RANGE by attn_get_last_device_error.
+ * Limits: head_dim 64 or 128, and G = num_heads_q / num_heads_kv must divide
+ * 128 (1, 2, 4, ..., 128); anything else returns ATTN_ERR_UNSUPPORTED.
  * Returns ATTN_OK, ATTN_ERR_INVALID_ARG, ATTN_ERR_UNSUPPORTED,
  * ATTN_ERR_WORKSPACE_TOO_SMALL, ATTN_ERR_LAUNCH_FAILED or ATTN_ERR_NO_DEVICE.
  * ------------------------------------------------------------------------ */
@@ -117,6 +124,54 @@ ATTN_API attn_status attn_varlen_fwd(const void *q, const void *k, const void *v
  * passed to attn_varlen_fwd). */
 ATTN_API size_t attn_varlen_workspace_size(int batch, int num_heads_q, int num_heads_kv, int head_dim,
                                            int max_seqlen_q, int64_t total_k);
+
+/* ------------------------------------------------------------------------
+ * attn_varlen_fwd_host -- attn_varlen_fwd (contiguous K/V) for a caller whose
+ * q, k, v and output live in HOST memory: the article's Prefill call with the
+ * transfers to and from the device made part of it.
+ *
+ * The batch is cut into `num_groups` groups of whole sequences with about the
+ * same number of query tokens (the last two groups 0.6 and 0.3 of the others,
+ * so that less work trails the last copy in).  Group i's host -> device copies
+ * (on copy_in_stream) overlap the attention of group i-1 (on `stream`) and the
+ * device -> host copy of group i-2's output (on copy_out_stream): one
+ * cudaMemcpyAsync per group, tensor and direction, ordered by the two events.
+ * Each group is one attn_varlen_fwd call whose cu_seqlens point into the full
+ * arrays, so rows are addressed in place and the output is bit-identical to
+ * one attn_varlen_fwd call over the whole batch.
+ *
+ *   q_host, k_host, v_host  packed [total, heads, head_dim] bf16 in host
+ *                memory; page-locked (pinned) for the copies to overlap
+ *   out_host     packed [total_q, num_heads_q, head_dim] bf16 host buffer, written
+ *   cu_seqlens_q_host, cu_seqlens_k_host  int32 [batch + 1] in HOST memory,
+ *                starting at 0, non-decreasing, lengths <= max_seqlen_q / _k
+ *                (checked here: ATTN_ERR_INVALID_ARG otherwise); total_q =
+ *                cu_seqlens_q_host[batch], total_k = cu_seqlens_k_host[batch]
+ *   q_dev, k_dev, v_dev, out_dev  device staging buffers of the same packed
+ *                shapes (caller-owned); cu_dev int32 [2 * (batch + 1)] device
+ *   workspace    attn_varlen_workspace_size(batch, num_heads_q, num_heads_kv,
+ *                head_dim, max_seqlen_q, total_k) bytes, 256-byte aligned
+ *   num_groups   1..64
+ *   stream, copy_in_stream, copy_out_stream  three distinct cudaStream_t; the
+ *                copies start after the work already queued on `stream`, and
+ *                `stream` waits for the last copy out, so synchronising `stream`
+ *                (or an event recorded on it after this call) means out_host is
+ *                complete
+ *   event_a, event_b  two caller-created cudaEvent_t the call records and waits
+ *                on (reused for every group; timing may be disabled)
+ * Everything is asynchronous: host buffers must stay valid, and unmodified,
+ * until `stream` has passed this call.  The library allocates nothing.
+ * Returns the statuses of attn_varlen_fwd (ATTN_ERR_LAUNCH_FAILED if a copy
+ * or event call fails).
+ * ------------------------------------------------------------------------ */
+ATTN_API attn_status attn_varlen_fwd_host(const void *q_host, const void *k_host, const void *v_host,
+                                          void *out_host, const int32_t *cu_seqlens_q_host,
+                                          const int32_t *cu_seqlens_k_host, int batch, int max_seqlen_q,
+                                          int max_seqlen_k, int num_heads_q, int num_heads_kv, int head_dim,
+                                          float softmax_scale, int causal, void *q_dev, void *k_dev, void *v_dev,
+                                          void *out_dev, int32_t *cu_dev, void *workspace, size_t workspace_bytes,
+                                          int num_groups, void *stream, void *copy_in_stream,
+                                          void *copy_out_stream, void *event_a, void *event_b);
 
 /* ------------------------------------------------------------------------
  * attn_decode_paged -- one new query token per sequence against its paged

@@ -17,9 +17,10 @@ REL_RMS = 2e-3
 LSE_ABS = 2e-3
 
 
-def errors(got, ref):
+def errors(got, ref, raw: bool = False):
     """(max over elements of |err| - 2^-8 |ref|, relative RMS) of got
-    (bf16/float tensor or array) vs ref (float64)."""
+    (bf16/float tensor or array) vs ref (float64); with raw=True also the plain
+    max |err| and the largest |ref| (third and fourth entries)."""
     g = got.float().cpu().double().numpy() if isinstance(got, torch.Tensor) else np.asarray(got, np.float64)
     r = np.asarray(ref, dtype=np.float64)
     g = g.reshape(r.shape)
@@ -27,23 +28,28 @@ def errors(got, ref):
     max_abs = float(np.max(np.abs(d) - OUT_ROUND * np.abs(r))) if d.size else 0.0
     den = float(np.sqrt(np.sum(r * r)))
     rel = float(np.sqrt(np.sum(d * d)) / den) if den > 0 else float(np.sqrt(np.sum(d * d)))
-    return max_abs, rel
+    if not raw:
+        return max_abs, rel
+    return max_abs, rel, float(np.max(np.abs(d))) if d.size else 0.0, float(np.max(np.abs(r))) if r.size else 0.0
 
 
-def _log_parity(what, max_abs, rel):
+def _log_parity(what, max_abs, rel, raw_max=None, ref_max=None):
     """With ATTN_PARITY_LOG=<file> set, append each comparison's metrics to that
-    file (one JSON object per line) so a run of the parity tests can be tabulated."""
+    file (one JSON object per line) so a run of the parity tests can be tabulated:
+    the plain max |err|, the max of |err| - 2^-8 |ref| (the bf16 output's own
+    rounding taken out), the largest |ref| and the relative RMS."""
     path = os.environ.get("ATTN_PARITY_LOG")
     if path:
         with open(path, "a") as f:
-            f.write(json.dumps({"what": what, "max_abs_minus_rounding": max_abs, "rel_rms": rel}) + "\n")
+            f.write(json.dumps({"what": what, "max_abs_err": raw_max, "max_abs_minus_rounding": max_abs,
+                                "max_abs_ref": ref_max, "rel_rms": rel}) + "\n")
 
 
 def assert_close(got, ref, what=""):
     g = got.float().cpu().double().numpy() if isinstance(got, torch.Tensor) else np.asarray(got, np.float64)
     assert np.all(np.isfinite(g)), f"{what}: non-finite output"
-    max_abs, rel = errors(got, ref)
-    _log_parity(what, max_abs, rel)
+    max_abs, rel, raw_max, ref_max = errors(got, ref, raw=True)
+    _log_parity(what, max_abs, rel, raw_max, ref_max)
     assert max_abs <= MAX_ABS and rel <= REL_RMS, f"{what}: max|err|={max_abs:.3e} relRMS={rel:.3e}"
     return max_abs, rel
 

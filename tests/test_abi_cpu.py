@@ -99,3 +99,33 @@ def test_new_workspace_sizes_are_host_side(L):
         c = L.attn_kvcache_workspace_size(4, 3, 32, 8, 128, n)
         assert 0 < c <= 4 * 3 * 32 * 64 * 129 * 4 + 256
     assert L.attn_padded_workspace_size(2, 16, 64, 8, 8, 64) > 0
+
+
+def test_host_entry_checks_offsets_on_the_host(L):
+    """attn_varlen_fwd_host reads cu_seqlens in host memory and refuses offsets
+    that do not start at 0, decrease, or exceed the stated maxima, before it
+    queries a device or queues a copy."""
+    null = None
+    fake = ctypes.c_void_p(0x1000)
+
+    def cu(*v):
+        a = (ctypes.c_int32 * len(v))(*v)
+        return a, ctypes.cast(a, ctypes.c_void_p)
+
+    keep = []
+
+    def call(cq, ck, mq=100, mk=100, groups=4, ev=fake):
+        (aq, pq), (ak, pk) = cu(*cq), cu(*ck)
+        keep.extend([aq, ak])
+        return L.attn_varlen_fwd_host(fake, fake, fake, fake, pq, pk, len(cq) - 1, mq, mk, 8, 2, 64,
+                                      ctypes.c_float(0.125), 1, fake, fake, fake, fake, fake, fake,
+                                      ctypes.c_size_t(1 << 20), groups, null, null, null, ev, ev)
+
+    assert call([0, 120, 150], [0, 100, 150]) == 1      # a query length above max_seqlen_q
+    assert call([1, 100, 150], [0, 100, 150]) == 1      # does not start at 0
+    assert call([0, 100, 90], [0, 100, 150]) == 1       # decreasing
+    assert call([0, 100, 150], [0, 100, 250]) == 1      # a key length above max_seqlen_k
+    assert call([0, 100, 150], [0, 100, 150], groups=0) == 1
+    assert call([0, 100, 150], [0, 100, 150], ev=null) == 1
+    # valid offsets reach the device query, which fails without a GPU
+    assert call([0, 100, 150], [0, 100, 150]) == 7

@@ -332,14 +332,34 @@ def test_paged_prefill_ignores_stale_workspace():
 
 @pytest.mark.parametrize("chunks", [1, 3, 8])
 def test_host_pipelined_prefill_equals_device_call(chunks):
-    """attn_varlen_fwd_host (copies overlapped with the attention of other sequence
-    groups) returns the device call's bits."""
+    """attn_varlen_fwd_host (C entry: host buffers in and out, copies of one
+    sequence group overlapped with the attention of another) returns the device
+    call's bits, and matches the oracle on sampled rows."""
     cfg = workloads.small_varlen(36, [700, 5, 1300, 64, 129, 900], [700, 5, 1300, 64, 129, 900], 32, 8, 128)
     q, k, v = cfg.q(), cfg.k(), cfg.v()
     ref = av.attn_varlen_fwd(q.cuda(), k.cuda(), v.cuda(), torch.from_numpy(cfg.cu_q).cuda(),
                              torch.from_numpy(cfg.cu_k).cuda(), 1300, 1300, cfg.scale)
+    av.get_last_device_error()
     got = av.attn_varlen_fwd_host(q.pin_memory(), k.pin_memory(), v.pin_memory(), torch.from_numpy(cfg.cu_q),
                                   torch.from_numpy(cfg.cu_k), 1300, 1300, cfg.scale, chunks=chunks)
     torch.cuda.synchronize()
+    assert av.get_last_device_error()[0] == 0
     assert not got.is_cuda
     assert torch.equal(got.view(torch.int16), ref.cpu().view(torch.int16))
+    rows = workloads.sample_rows(cfg.seed + chunks, q.shape[0] * cfg.Hq, 1 / 16)
+    oref, _ = oracle.attn_varlen(q, k, v, cfg.cu_q, cfg.cu_k, cfg.Hq, cfg.Hkv, cfg.D, cfg.scale, True, rows=rows)
+    assert_close(got.reshape(-1, cfg.D)[torch.from_numpy(rows)], oref, f"host pipeline, {chunks} groups")
+
+
+def test_host_pipelined_prefill_rejects_bad_offsets():
+    """The host entry reads cu_seqlens on the host and refuses offsets that are
+    not monotone or exceed the stated maxima, before any copy."""
+    cfg = workloads.small_varlen(37, [100, 50], [100, 50], 8, 2, 64)
+    q, k, v = cfg.q().pin_memory(), cfg.k().pin_memory(), cfg.v().pin_memory()
+    bad = torch.tensor([0, 120, 150], dtype=torch.int32)   # lengths 120, 30 on 150 rows
+    with pytest.raises(av.AttnError) as e:
+        av.attn_varlen_fwd_host(q, k, v, bad, torch.from_numpy(cfg.cu_k), 100, 100, cfg.scale)
+    assert e.value.status == 1
+    dec = torch.tensor([0, 100, 90], dtype=torch.int32)
+    with pytest.raises((av.AttnError, ValueError)):
+        av.attn_varlen_fwd_host(q, k, v, dec, torch.from_numpy(cfg.cu_k), 100, 100, cfg.scale)
