@@ -54,7 +54,7 @@ def lib():
                            "run attention_attn_varlen_gb300.build() on a machine with nvcc")
     L = ctypes.CDLL(_LIB_PATH)
     L.attn_varlen_fwd.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i64, _i64, _i32, _i32, _i32, _i32, _i32,
-                                  _f32, _i32, _vp, _i32, _i32, _i64, _i64, _i64, _i64, _i64, _vp, _sz, _vp]
+                                  _f32, _i32, _vp, _i32, _i32, _i64, _vp, _i64, _i64, _i64, _i64, _vp, _sz, _vp]
     L.attn_varlen_fwd.restype = _i32
     L.attn_varlen_workspace_size.argtypes = [_i32, _i32, _i32, _i32, _i32, _i64]
     L.attn_varlen_workspace_size.restype = _sz
@@ -68,7 +68,7 @@ def lib():
     L.attn_decode_workspace_size.restype = _sz
     L.attn_decode_num_splits.argtypes = [_i32, _i32, _i32, _i32]
     L.attn_decode_num_splits.restype = _i32
-    L.store_kvcache.argtypes = [_vp, _vp, _vp, _vp, _vp, _i64, _i32, _i32, _i64, _i64, _i64, _vp]
+    L.store_kvcache.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i32, _i32, _i64, _i64, _i64, _vp]
     L.store_kvcache.restype = _i32
     L.attn_status_string.argtypes = [_i32]
     L.attn_status_string.restype = _c.c_char_p
@@ -77,7 +77,7 @@ def lib():
     L.attn_abi_version.argtypes = []
     L.attn_abi_version.restype = _i32
     L.attn_kvcache_fwd.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _i32,
-                                   _i64, _i32, _f32, _i32, _vp, _sz, _vp]
+                                   _i64, _i32, _f32, _i32, _vp, _vp, _sz, _vp]
     L.attn_kvcache_fwd.restype = _i32
     L.attn_kvcache_workspace_size.argtypes = [_i32, _i32, _i32, _i32, _i32, _i32]
     L.attn_kvcache_workspace_size.restype = _sz
@@ -154,13 +154,20 @@ def _int_cuda(name, t, dtype):
 def attn_varlen_fwd(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, max_seqlen_k: int,
                     softmax_scale: float | None = None, causal: bool = True, block_table=None,
                     out=None, lse=None, return_lse: bool = False, total_k: int | None = None,
-                    workspace=None, stream=None):
+                    workspace=None, stream=None, v16_cache=None):
     """Varlen prefill.  q [total_q, Hq, D]; k/v [total_k, Hkv, D] or, with
     block_table [B, max_blocks] int32, caches [num_blocks, block_size, Hkv, D].
     total_k (paged only): an upper bound of cu_seqlens_k[-1]; defaults to
-    B * max_seqlen_k (no device sync).
+    B * max_seqlen_k (no device sync).  v16_cache (paged only): the fp16 V / 16
+    cache kept by store_kvcache(..., v16_cache=...); the call then converts nothing.
     Returns out [total_q, Hq, D] (and lse [Hq, total_q] float32 if asked)."""
     _bf16_cuda(("q", q), ("k", k), ("v", v), ("out", out))
+    if v16_cache is not None:
+        if block_table is None:
+            raise ValueError("v16_cache goes with a paged cache (block_table)")
+        if not v16_cache.is_cuda or v16_cache.dtype != torch.float16 or v16_cache.shape != k.shape \
+                or not v16_cache.is_contiguous():
+            raise ValueError("v16_cache must be a contiguous float16 CUDA tensor shaped like the caches")
     _int_cuda("cu_seqlens_q", cu_seqlens_q, torch.int32)
     _int_cuda("cu_seqlens_k", cu_seqlens_k, torch.int32)
     total_q, Hq, D = q.shape
@@ -191,14 +198,16 @@ def attn_varlen_fwd(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, max_
         lse = torch.empty((Hq, total_q), dtype=torch.float32, device=q.device)
     scale = 1.0 / math.sqrt(D) if softmax_scale is None else float(softmax_scale)
     L = lib()
-    ws_bytes = L.attn_varlen_workspace_size(B, Hq, Hkv, D, int(max_seqlen_q), int(total_k))
+    ws_bytes = L.attn_varlen_workspace_size(B, Hq, Hkv, D, int(max_seqlen_q), 0 if v16_cache is not None
+                                            else int(total_k))
     if workspace is None or workspace.numel() * workspace.element_size() < ws_bytes:
         workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device)
     ws = workspace
     st = L.attn_varlen_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(cu_seqlens_q), _ptr(cu_seqlens_k),
                            B, total_q, total_k, int(max_seqlen_q), int(max_seqlen_k), Hq, Hkv, D, scale,
-                           1 if causal else 0, _ptr(block_table), bt_stride, block_size, num_blocks, q_stride,
-                           k_stride, v_stride, out_stride, _ptr(ws), ws.numel() * ws.element_size(), _stream(stream))
+                           1 if causal else 0, _ptr(block_table), bt_stride, block_size, num_blocks, _ptr(v16_cache),
+                           q_stride, k_stride, v_stride, out_stride, _ptr(ws), ws.numel() * ws.element_size(),
+                           _stream(stream))
     _check(st, "attn_varlen_fwd")
     return (out, lse) if return_lse else out
 
@@ -324,12 +333,16 @@ def attn_decode_paged(q, k_cache, v_cache, cache_seqlens, block_table, softmax_s
 
 def attn_with_kvcache(q, k_cache, v_cache, cache_seqlens, block_table, softmax_scale: float | None = None,
                       causal: bool = True, max_cache_seqlen: int | None = None, out=None, lse=None,
-                      return_lse: bool = False, workspace=None, stream=None):
+                      return_lse: bool = False, workspace=None, stream=None, v16_cache=None):
     """Several new tokens per sequence against the paged cache: q [B, Sq, Hq, D]
     (Sq >= 1, all sequences the same Sq); caches [num_blocks, block_size, Hkv, D];
     cache_seqlens int32 [B] counts the cached keys including the Sq new ones.
     Returns out [B, Sq, Hq, D] (and lse [Hq, B*Sq]).  Up to 64 query rows per KV
-    head (Sq x Hq/Hkv) run on the split-KV decode kernel, more on the prefill kernel."""
+    head (Sq x Hq/Hkv) run on the split-KV decode kernel, more on the prefill kernel
+    (which reads v16_cache, the fp16 V / 16 cache, when given)."""
+    if v16_cache is not None and (not v16_cache.is_cuda or v16_cache.dtype != torch.float16
+                                  or v16_cache.shape != k_cache.shape or not v16_cache.is_contiguous()):
+        raise ValueError("v16_cache must be a contiguous float16 CUDA tensor shaped like the caches")
     if q.dim() != 4:
         raise ValueError("q must be [B, seqlen_q, Hq, D]")
     _bf16_cuda(("q", q), ("k_cache", k_cache), ("v_cache", v_cache), ("out", out))
@@ -360,8 +373,8 @@ def attn_with_kvcache(q, k_cache, v_cache, cache_seqlens, block_table, softmax_s
     ws_have = workspace.numel() * workspace.element_size()
     st = L.attn_kvcache_fwd(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(out), _ptr(lse), _ptr(cache_seqlens),
                             _ptr(block_table), block_table.shape[1], B, Sq, Hq, Hkv, D, block_size, num_blocks,
-                            int(max_cache_seqlen), scale, 1 if causal else 0, _ptr(workspace), ws_have,
-                            _stream(stream))
+                            int(max_cache_seqlen), scale, 1 if causal else 0, _ptr(v16_cache), _ptr(workspace),
+                            ws_have, _stream(stream))
     _check(st, "attn_kvcache_fwd")
     return (out, lse) if return_lse else out
 
@@ -430,10 +443,14 @@ def softmax_rows(x, out=None, stream=None):
     return out
 
 
-def store_kvcache(k, v, k_cache, v_cache, slot_mapping, stream=None):
+def store_kvcache(k, v, k_cache, v_cache, slot_mapping, stream=None, v16_cache=None):
     """Scatter k/v [N, Hkv, D] into caches [num_blocks, block_size, Hkv, D] (or
-    any [num_slots, Hkv, D] view) at the flat slots slot_mapping (int64 [N])."""
+    any [num_slots, Hkv, D] view) at the flat slots slot_mapping (int64 [N]).
+    v16_cache (float16, shaped like the caches): also receives V / 16."""
     _bf16_cuda(("k", k), ("v", v), ("k_cache", k_cache), ("v_cache", v_cache))
+    if v16_cache is not None and (not v16_cache.is_cuda or v16_cache.dtype != torch.float16
+                                  or v16_cache.shape != v_cache.shape or not v16_cache.is_contiguous()):
+        raise ValueError("v16_cache must be a contiguous float16 CUDA tensor shaped like the caches")
     _int_cuda("slot_mapping", slot_mapping, torch.int64)
     N, Hkv, D = k.shape
     if not k_cache.is_contiguous() or not v_cache.is_contiguous() or k_cache.shape != v_cache.shape:
@@ -445,8 +462,8 @@ def store_kvcache(k, v, k_cache, v_cache, slot_mapping, stream=None):
     vs = _rows(v, "v", Hkv, D)
     if slot_mapping.numel() != N:
         raise ValueError("slot_mapping must have one entry per token")
-    st = lib().store_kvcache(_ptr(k), _ptr(v), _ptr(k_cache), _ptr(v_cache), _ptr(slot_mapping), N, Hkv, D, ks, vs,
-                             num_slots, _stream(stream))
+    st = lib().store_kvcache(_ptr(k), _ptr(v), _ptr(k_cache), _ptr(v_cache), _ptr(v16_cache), _ptr(slot_mapping), N,
+                             Hkv, D, ks, vs, num_slots, _stream(stream))
     _check(st, "store_kvcache")
 
 

@@ -42,7 +42,9 @@ class Attention:
 
     k_cache / v_cache ([num_blocks, block_size, num_kv_heads, head_dim] bf16)
     are bound by the owner (for instance after sizing the pool); until then the
-    layer runs without a cache (prefill only)."""
+    layer runs without a cache (prefill only).  An optional v16_cache (float16,
+    same shape) keeps V / 16 next to the bf16 V: the store fills it and the
+    prefix prefill reads it instead of converting the cached V every step."""
 
     def __init__(self, num_heads: int, head_dim: int, scale: float, num_kv_heads: int):
         if num_heads % num_kv_heads:
@@ -53,6 +55,7 @@ class Attention:
         self.num_kv_heads = num_kv_heads
         self.k_cache: torch.Tensor | None = None
         self.v_cache: torch.Tensor | None = None
+        self.v16_cache: torch.Tensor | None = None
 
     def forward(self, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, ctx: AttentionContext) -> torch.Tensor:
         """q [N, Hq*D] or [N, Hq, D]; k, v [N, Hkv*D] or [N, Hkv, D].  Returns o
@@ -63,14 +66,14 @@ class Attention:
         v = v.view(-1, self.num_kv_heads, self.head_dim)
         cached = self.k_cache is not None and self.v_cache is not None and self.k_cache.numel() > 0
         if cached and ctx.slot_mapping is not None and ctx.slot_mapping.numel():
-            store_kvcache(k, v, self.k_cache, self.v_cache, ctx.slot_mapping)
+            store_kvcache(k, v, self.k_cache, self.v_cache, ctx.slot_mapping, v16_cache=self.v16_cache)
         if ctx.is_prefill:
             if ctx.block_tables is not None:
                 if not cached:
                     raise ValueError("prefix prefill needs the KV cache")
                 o = attn_varlen_fwd(q, self.k_cache, self.v_cache, ctx.cu_seqlens_q, ctx.cu_seqlens_k,
                                     ctx.max_seqlen_q, ctx.max_seqlen_k, self.scale, causal=True,
-                                    block_table=ctx.block_tables)
+                                    block_table=ctx.block_tables, v16_cache=self.v16_cache)
             else:
                 o = attn_varlen_fwd(q, k, v, ctx.cu_seqlens_q, ctx.cu_seqlens_k, ctx.max_seqlen_q,
                                     ctx.max_seqlen_k, self.scale, causal=True)
@@ -89,7 +92,7 @@ class Attention:
                 sq = n // batch
                 o = attn_with_kvcache(q.reshape(batch, sq, self.num_heads, self.head_dim), self.k_cache,
                                       self.v_cache, ctx.context_lens, ctx.block_tables, self.scale, causal=True,
-                                      max_cache_seqlen=ctx.max_seqlen_k or None)
+                                      max_cache_seqlen=ctx.max_seqlen_k or None, v16_cache=self.v16_cache)
         return o.view(shape)
 
     __call__ = forward

@@ -353,9 +353,9 @@ static attn_status varlen_impl(const void *q, const void *k, const void *v, void
                                const int32_t *seqused_k, int batch, int64_t total_q, int64_t total_k,
                                int max_seqlen_q, int max_seqlen_k, int num_heads_q, int num_heads_kv, int head_dim,
                                float softmax_scale, int causal, const int32_t *block_table, int block_table_stride,
-                               int block_size, int64_t num_blocks, int64_t q_row_stride, int64_t k_row_stride,
-                               int64_t v_row_stride, int64_t out_row_stride, void *workspace, size_t workspace_bytes,
-                               void *stream) {
+                               int block_size, int64_t num_blocks, const void *v16_cache, int64_t q_row_stride,
+                               int64_t k_row_stride, int64_t v_row_stride, int64_t out_row_stride, void *workspace,
+                               size_t workspace_bytes, void *stream) {
 
     if (!q || !k || !v || !out || !cu_seqlens_q || !cu_seqlens_k) return ATTN_ERR_INVALID_ARG;
     if (batch <= 0 || num_heads_q <= 0 || num_heads_kv <= 0 || num_heads_q % num_heads_kv != 0)
@@ -375,6 +375,7 @@ static attn_status varlen_impl(const void *q, const void *k, const void *v, void
     if (total_k >= (int64_t)INT32_MAX) return ATTN_ERR_UNSUPPORTED;
     if (total_q >= (int64_t)INT32_MAX) return ATTN_ERR_UNSUPPORTED;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return ATTN_ERR_INVALID_ARG;
+    if (v16_cache && (!paged || !aligned16(v16_cache))) return ATTN_ERR_INVALID_ARG;   // a cache goes with a block table
     if (!fix_stride(&q_row_stride, (int64_t)num_heads_q * head_dim) ||
         !fix_stride(&out_row_stride, (int64_t)num_heads_q * head_dim) ||
         !fix_stride(&k_row_stride, (int64_t)num_heads_kv * head_dim) ||
@@ -394,7 +395,9 @@ static attn_status varlen_impl(const void *q, const void *k, const void *v, void
     if (max_pairs <= 0 || max_pairs > 0xFFFF || num_heads_kv > 0x7FFF ||
         (int64_t)batch * max_pairs * num_heads_kv > (int64_t)INT32_MAX / 4)
         return ATTN_ERR_UNSUPPORTED;
-    const size_t ws_need = attn_varlen_workspace_size(batch, num_heads_q, num_heads_kv, head_dim, max_seqlen_q, total_k);
+    // with a paged V' cache the workspace holds no V' copy (sized for total_k = 0)
+    const int64_t ws_keys = v16_cache ? 0 : total_k;
+    const size_t ws_need = attn_varlen_workspace_size(batch, num_heads_q, num_heads_kv, head_dim, max_seqlen_q, ws_keys);
     if (!workspace || workspace_bytes < ws_need) return ATTN_ERR_WORKSPACE_TOO_SMALL;
     if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return ATTN_ERR_INVALID_ARG;
     uint8_t *ws = reinterpret_cast<uint8_t *>(workspace);
@@ -403,16 +406,19 @@ static attn_status varlen_impl(const void *q, const void *k, const void *v, void
     const int kv_box = paged ? (block_size < kPrefillKeyTile ? block_size : kPrefillKeyTile) : kPrefillKeyTile;
     CUtensorMap qmap, kmap, vmap;
     if (!make_map(&qmap, q, total_q, num_heads_q, head_dim, q_row_stride, G, tps) ||
-        !make_map(&kmap, k, kv_rows, num_heads_kv, head_dim, k_row_stride, 1, kv_box) ||
-        !make_map(&vmap, v16, total_k, num_heads_kv, head_dim, (int64_t)num_heads_kv * head_dim, 1,
-                  kPrefillKeyTile, CU_TENSOR_MAP_DATA_TYPE_FLOAT16))
+        !make_map(&kmap, k, kv_rows, num_heads_kv, head_dim, k_row_stride, 1, kv_box))
+        return ATTN_ERR_LAUNCH_FAILED;
+    if (v16_cache ? !make_map(&vmap, v16_cache, kv_rows, num_heads_kv, head_dim, (int64_t)num_heads_kv * head_dim, 1,
+                              kv_box, CU_TENSOR_MAP_DATA_TYPE_FLOAT16)
+                  : !make_map(&vmap, v16, total_k, num_heads_kv, head_dim, (int64_t)num_heads_kv * head_dim, 1,
+                              kPrefillKeyTile, CU_TENSOR_MAP_DATA_TYPE_FLOAT16))
         return ATTN_ERR_LAUNCH_FAILED;
 
     PrefillParams p;
     memset(&p, 0, sizeof p);
     p.v = reinterpret_cast<const __nv_bfloat16 *>(v);
-    p.v = reinterpret_cast<const __nv_bfloat16 *>(v);
-    p.v16 = reinterpret_cast<__half *>(v16);
+    p.v16 = v16_cache ? nullptr : reinterpret_cast<__half *>(v16);
+    p.v16_paged = v16_cache ? 1 : 0;
     p.out = reinterpret_cast<__nv_bfloat16 *>(out);
     p.lse = lse;
     p.cu_q = cu_seqlens_q;
@@ -441,7 +447,7 @@ static attn_status varlen_impl(const void *q, const void *k, const void *v, void
     const int64_t max_units = (int64_t)batch * max_pairs * num_heads_kv;
     p.num_ctas = (int)(max_units < d->num_sms ? max_units : d->num_sms);
     p.unit_count = reinterpret_cast<int *>(ws);
-    p.units = reinterpret_cast<int2 *>(ws + kWsHeader + v16_bytes(num_heads_kv, head_dim, total_k));
+    p.units = reinterpret_cast<int2 *>(ws + kWsHeader + v16_bytes(num_heads_kv, head_dim, ws_keys));
     p.scale_log2 = softmax_scale * 1.4426950408889634f;
     p.err = d->err;
     cudaError_t e = launch_prefill(qmap, kmap, vmap, p, head_dim, reinterpret_cast<cudaStream_t>(stream));
@@ -458,12 +464,12 @@ attn_status attn_varlen_fwd(const void *q, const void *k, const void *v, void *o
                             const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k, int batch, int64_t total_q,
                             int64_t total_k, int max_seqlen_q, int max_seqlen_k, int num_heads_q, int num_heads_kv,
                             int head_dim, float softmax_scale, int causal, const int32_t *block_table,
-                            int block_table_stride, int block_size, int64_t num_blocks, int64_t q_row_stride,
-                            int64_t k_row_stride, int64_t v_row_stride, int64_t out_row_stride, void *workspace,
-                            size_t workspace_bytes, void *stream) {
+                            int block_table_stride, int block_size, int64_t num_blocks, const void *v16_cache,
+                            int64_t q_row_stride, int64_t k_row_stride, int64_t v_row_stride, int64_t out_row_stride,
+                            void *workspace, size_t workspace_bytes, void *stream) {
     return varlen_impl(q, k, v, out, lse, cu_seqlens_q, cu_seqlens_k, nullptr, nullptr, batch, total_q, total_k,
                        max_seqlen_q, max_seqlen_k, num_heads_q, num_heads_kv, head_dim, softmax_scale, causal,
-                       block_table, block_table_stride, block_size, num_blocks, q_row_stride, k_row_stride,
+                       block_table, block_table_stride, block_size, num_blocks, v16_cache, q_row_stride, k_row_stride,
                        v_row_stride, out_row_stride, workspace, workspace_bytes, stream);
 }
 
@@ -567,7 +573,7 @@ extern "C" attn_status attn_varlen_fwd_host(const void *q_host, const void *k_ho
         if (fail) break;
         st = varlen_impl(q_dev, k_dev, v_dev, out_dev, nullptr, cu_dev + b0, cu_dev + batch + 1 + b0, nullptr, nullptr,
                          b1 - b0, total_q, total_k, mq, mk, num_heads_q, num_heads_kv, head_dim, softmax_scale,
-                         causal, nullptr, 0, 0, 0, 0, 0, 0, 0, workspace, workspace_bytes, stream);
+                         causal, nullptr, 0, 0, 0, nullptr, 0, 0, 0, 0, workspace, workspace_bytes, stream);
         ck(cudaEventRecord(ev_b, s_main));
         ck(cudaStreamWaitEvent(s_out, ev_b, 0));
         if (q1 > q0) ck(cudaMemcpyAsync(oh + q0 * qrow, od + q0 * qrow, (q1 - q0) * qrow, cudaMemcpyDeviceToHost, s_out));
@@ -619,16 +625,16 @@ attn_status attn_padded_fwd(const void *q, const void *k, const void *v, void *o
     }
     return varlen_impl(q, k, v, out, lse, cu_q, cu_k, seqlens_q, seqlens_k, batch, (int64_t)batch * seqlen_q,
                        (int64_t)batch * seqlen_k, seqlen_q, seqlen_k, num_heads_q, num_heads_kv, head_dim,
-                       softmax_scale, causal, nullptr, 0, 0, 0, 0, 0, 0, 0, reinterpret_cast<uint8_t *>(workspace) + cu_b,
-                       workspace_bytes - cu_b, stream);
+                       softmax_scale, causal, nullptr, 0, 0, 0, nullptr, 0, 0, 0, 0,
+                       reinterpret_cast<uint8_t *>(workspace) + cu_b, workspace_bytes - cu_b, stream);
 }
 
 // ---------------------------------------------------------------------------
 // kv-cache entry: [cu_seqlens_q | cu_seqlens_k] (256-byte aligned), then the
 // varlen workspace for total_k = batch * max_cache_seqlen.
 
-size_t attn_kvcache_workspace_size(int batch, int seqlen_q, int num_heads_q, int num_heads_kv, int head_dim,
-                                   int max_cache_seqlen) {
+static size_t kvcache_ws(int batch, int seqlen_q, int num_heads_q, int num_heads_kv, int head_dim,
+                         int max_cache_seqlen, bool v16_cache) {
     if (batch <= 0 || seqlen_q <= 0 || max_cache_seqlen < 0) return 0;
     if (kvcache_on_decode(batch, seqlen_q, num_heads_q, num_heads_kv, head_dim)) {
         // split partials of the decode kernel (never 0: 0 means invalid sizes)
@@ -640,21 +646,28 @@ size_t attn_kvcache_workspace_size(int batch, int seqlen_q, int num_heads_q, int
         return decode_partial_bytes(batch, seqlen_q, num_heads_q, head_dim, splits) + 256;
     }
     const size_t v = attn_varlen_workspace_size(batch, num_heads_q, num_heads_kv, head_dim, seqlen_q,
-                                                (int64_t)batch * max_cache_seqlen);
+                                                v16_cache ? 0 : (int64_t)batch * max_cache_seqlen);
     return v ? kvcache_cu_bytes(batch) + v : 0;
+}
+
+size_t attn_kvcache_workspace_size(int batch, int seqlen_q, int num_heads_q, int num_heads_kv, int head_dim,
+                                   int max_cache_seqlen) {
+    return kvcache_ws(batch, seqlen_q, num_heads_q, num_heads_kv, head_dim, max_cache_seqlen, false);
 }
 
 attn_status attn_kvcache_fwd(const void *q, const void *k_cache, const void *v_cache, void *out, float *lse,
                              const int32_t *cache_seqlens, const int32_t *block_table, int block_table_stride,
                              int batch, int seqlen_q, int num_heads_q, int num_heads_kv, int head_dim,
                              int block_size, int64_t num_blocks, int max_cache_seqlen, float softmax_scale,
-                             int causal, void *workspace, size_t workspace_bytes, void *stream) {
+                             int causal, const void *v16_cache, void *workspace, size_t workspace_bytes,
+                             void *stream) {
     if (!q || !k_cache || !v_cache || !out || !cache_seqlens || !block_table) return ATTN_ERR_INVALID_ARG;
     if (batch <= 0 || seqlen_q <= 0 || max_cache_seqlen < 0) return ATTN_ERR_INVALID_ARG;
     if ((int64_t)batch * max_cache_seqlen >= (int64_t)INT32_MAX || (int64_t)batch * seqlen_q >= (int64_t)INT32_MAX)
         return ATTN_ERR_UNSUPPORTED;
-    const size_t need = attn_kvcache_workspace_size(batch, seqlen_q, num_heads_q, num_heads_kv, head_dim,
-                                                    max_cache_seqlen);
+    // the decode route reads the bf16 V cache; the prefill route reads v16_cache when given
+    const size_t need = kvcache_ws(batch, seqlen_q, num_heads_q, num_heads_kv, head_dim, max_cache_seqlen,
+                                   v16_cache != nullptr);
     if (need == 0) return ATTN_ERR_INVALID_ARG;
     if (!workspace || workspace_bytes < need) return ATTN_ERR_WORKSPACE_TOO_SMALL;
     if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return ATTN_ERR_INVALID_ARG;
@@ -685,7 +698,8 @@ attn_status attn_kvcache_fwd(const void *q, const void *k_cache, const void *v_c
     return attn_varlen_fwd(q, k_cache, v_cache, out, lse, cu_q, cu_k, batch, (int64_t)batch * seqlen_q,
                            (int64_t)batch * max_cache_seqlen, seqlen_q, max_cache_seqlen, num_heads_q, num_heads_kv,
                            head_dim, softmax_scale, causal, block_table, block_table_stride, block_size, num_blocks,
-                           0, 0, 0, 0, reinterpret_cast<uint8_t *>(workspace) + cu_b, workspace_bytes - cu_b, stream);
+                           v16_cache, 0, 0, 0, 0, reinterpret_cast<uint8_t *>(workspace) + cu_b,
+                           workspace_bytes - cu_b, stream);
 }
 
 // ---------------------------------------------------------------------------
@@ -796,9 +810,9 @@ attn_status attn_decode_paged_noalloc(const void *q, const void *k_cache, const 
 }
 
 // ---------------------------------------------------------------------------
-attn_status store_kvcache(const void *k, const void *v, void *k_cache, void *v_cache, const int64_t *slot_mapping,
-                          int64_t num_tokens, int num_heads_kv, int head_dim, int64_t k_row_stride,
-                          int64_t v_row_stride, int64_t num_slots, void *stream) {
+attn_status store_kvcache(const void *k, const void *v, void *k_cache, void *v_cache, void *v16_cache,
+                          const int64_t *slot_mapping, int64_t num_tokens, int num_heads_kv, int head_dim,
+                          int64_t k_row_stride, int64_t v_row_stride, int64_t num_slots, void *stream) {
     if (num_tokens < 0 || num_heads_kv <= 0 || head_dim <= 0 || num_slots < 0) return ATTN_ERR_INVALID_ARG;
     if (num_tokens == 0) return ATTN_OK;
     if (!k || !v || !k_cache || !v_cache || !slot_mapping) return ATTN_ERR_INVALID_ARG;
@@ -811,7 +825,8 @@ attn_status store_kvcache(const void *k, const void *v, void *k_cache, void *v_c
     attn_status st = dev_info(&d);
     if (st != ATTN_OK) return st;
     if ((st = check_arch(d)) != ATTN_OK) return st;
-    cudaError_t e = launch_store_kvcache(k, v, k_cache, v_cache, slot_mapping, num_tokens, (int)row, k_row_stride,
+    cudaError_t e = launch_store_kvcache(k, v, k_cache, v_cache, v16_cache, slot_mapping, num_tokens, (int)row,
+                                         k_row_stride,
                                          v_row_stride, num_slots, d->num_sms, d->err,
                                          reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) {

@@ -49,6 +49,8 @@ struct PrefillParams {
     int bt_stride, block_size, rows_per_box;
     int batch, Hq, Hkv, G, causal, head_dim, max_seqlen_k;
     int max_pairs;               // slot pairs per sequence at max_seqlen_q
+    int v16_paged;               // 1: V' tiles come from a paged fp16 V / 16 cache through the block
+                                 //    table (written by store_kvcache); no conversion pass
     int num_ctas;                // grid size: persistent CTAs (one per SM, at most the possible units)
     int2 *units;                 // workspace: (sequence, pair | kv_head << 16), scheduled order
     int *unit_count;             // workspace: [0] number of units
@@ -56,7 +58,7 @@ struct PrefillParams {
     uint32_t *err;
 };
 
-cudaError_t launch_store_kvcache(const void *k, const void *v, void *k_cache, void *v_cache,
+cudaError_t launch_store_kvcache(const void *k, const void *v, void *k_cache, void *v_cache, void *v16_cache,
                                  const int64_t *slot_mapping, int64_t num_tokens, int row_elems,
                                  int64_t k_stride, int64_t v_stride, int64_t num_slots, int num_sms,
                                  uint32_t *err, cudaStream_t stream);

@@ -297,10 +297,12 @@ __device__ __forceinline__ void schedule_units(const PrefillParams &p) {
 // ---------------------------------------------------------------------------
 // Pre-pass before the attention kernel, one launch: CTA (0, batch) writes the
 // unit list (schedule_units); CTAs (x, b) with b < batch convert V of
-// sequence b to V' (v_to_f16_keys).
+// sequence b to V' (v_to_f16_keys).  With a paged V' cache (v16_paged) the
+// launch is the scheduler's CTA alone.
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(kCvtThreads) attn_prefill_prep_kernel(const PrefillParams p) {
-    if (blockIdx.y == (unsigned)p.batch) {
+    if (p.v16_paged || blockIdx.y == (unsigned)p.batch) {
+        // with a paged V' cache there is nothing to convert: one CTA, the scheduler
         if (blockIdx.x == 0) schedule_units(p);
         return;
     }
@@ -519,9 +521,10 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                     uint64_t *bar = wv ? &full_v[st] : &full_k[st];
                     if (lane == 0) {
                         mbar_arrive_expect_tx(bar, (uint32_t)S::kTileBytes);
-                        // V' is contiguous by logical key (rows past the sequence hold the
-                        // next sequence's keys or zeroed rows)
-                        if (!paged || wv == 1) {
+                        // V' converted by the pre-pass is contiguous by logical key (rows past
+                        // the sequence hold the next sequence's keys or zeroed rows); a paged
+                        // V' cache is read through the block table like K
+                        if (!paged || (wv == 1 && !p.v16_paged)) {
 #pragma unroll
                             for (int pn = 0; pn < S::kPanels; ++pn)
                                 tma_load_3d(dst + pn * S::kPanelBytes, map, bar, pn * 64, w.hkv, w.ks0 + key0);
@@ -617,28 +620,47 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         __syncwarp();
     } else if (warp == 10) {
         // ================================================================ PV issuer
-        if (lane == 0) {
-            const uint32_t tO[2] = {tmem + 256, tmem + 256 + D};
-            const uint32_t pX[2] = {smem_u32(sP), smem_u32(sP + kPBytes)};
-            const uint32_t ring = smem_u32(sRing);
-            int itb = 0, tc[2] = {0, 0}, k = 0;   // ring items before this unit; PV tiles issued per slot
-            uint32_t vpar = 0;                    // per stage: parity of the V' tiles read from it
-            bool ok = true;
-            for (;; ++k) {
-                ok = mbar_wait(&idx_full[k & 1], (uint32_t)(k >> 1) & 1u, abort_flag, p.err, SRC_PREFILL);
+        // Lane 0 issues every PV.  With a paged V' cache the rows of a tile past the
+        // sequence's last key come from cache slots that may hold anything (even NaN,
+        // and 0 * NaN is NaN inside the MMA): the whole warp zeroes them in shared
+        // memory before the PV that reads the tile.
+        const uint32_t tO[2] = {tmem + 256, tmem + 256 + D};
+        const uint32_t pX[2] = {smem_u32(sP), smem_u32(sP + kPBytes)};
+        const uint32_t ring = smem_u32(sRing);
+        int itb = 0, tc[2] = {0, 0}, k = 0;   // ring items before this unit; PV tiles issued per slot
+        uint32_t vpar = 0;                    // per stage: parity of the V' tiles read from it
+        bool ok = true;
+        for (;; ++k) {
+            int u = -1;
+            ok = __all_sync(0xffffffffu,
+                            mbar_wait(&idx_full[k & 1], (uint32_t)(k >> 1) & 1u, abort_flag, p.err, SRC_PREFILL));
+            if (!ok) break;
+            u = unit_idx[k & 1];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&idx_empty[k & 1]);
+            if (u < 0) break;
+            const PfUnit w = pf_unit(p, u);
+            const int nX[2] = {w.nA, w.nB};
+            // PV_X(0) of a unit writes O_X afresh: its p_ready comes after the
+            // softmax threads have read O_X of the previous unit
+            for (int j = 0; j < w.n && ok; ++j) {
+                const int itV = itb + (j < w.n - 1 ? 2 * j + 2 : 2 * w.n - 1), stV = itV % ST;
+                ok = __all_sync(0xffffffffu,
+                                mbar_wait(&full_v[stV], (vpar >> stV) & 1u, abort_flag, p.err, SRC_PREFILL));
+                vpar ^= 1u << stV;
                 if (!ok) break;
-                const int u = unit_idx[k & 1];
-                mbar_arrive(&idx_empty[k & 1]);
-                if (u < 0) break;
-                const PfUnit w = pf_unit(p, u);
-                const int nX[2] = {w.nA, w.nB};
-                // PV_X(0) of a unit writes O_X afresh: its p_ready comes after the
-                // softmax threads have read O_X of the previous unit
-                for (int j = 0; j < w.n && ok; ++j) {
-                    const int itV = itb + (j < w.n - 1 ? 2 * j + 2 : 2 * w.n - 1), stV = itV % ST;
-                    ok = mbar_wait(&full_v[stV], (vpar >> stV) & 1u, abort_flag, p.err, SRC_PREFILL);
-                    vpar ^= 1u << stV;
-                    if (!ok) break;
+                if (p.v16_paged && (j + 1) * BN > w.Lk) {
+                    const int r0 = max(w.Lk - j * BN, 0);
+                    uint8_t *tile = sRing + stV * S::kTileBytes;
+                    for (int i = lane; i < (BN - r0) * S::kPanels * 8; i += 32) {
+                        const int rr = r0 + i / (S::kPanels * 8), c = i % (S::kPanels * 8);
+                        *reinterpret_cast<uint4 *>(tile + (c >> 3) * S::kPanelBytes + rr * 128 + ((c & 7) << 4)) =
+                            make_uint4(0u, 0u, 0u, 0u);
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                }
+                if (lane == 0) {
 #pragma unroll
                     for (int x = 0; x < 2; ++x) {
                         if (j >= nX[x]) continue;
@@ -649,12 +671,14 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                         tc_commit(&pv_done[x]);
                         ++tc[x];
                     }
-                    if (!ok) break;
-                    tc_commit(&empty[stV]);
+                    if (ok) tc_commit(&empty[stV]);
                 }
-                if (!ok) break;
-                itb += 2 * w.n;
+                ok = __shfl_sync(0xffffffffu, ok, 0);
             }
+            if (!ok) break;
+            itb += 2 * w.n;
+        }
+        if (lane == 0) {
             tc_commit(&drain[1]);
             mbar_wait(&drain[1], 0, nullptr, p.err, SRC_PREFILL);
         }
@@ -916,8 +940,9 @@ static cudaError_t launch_prefill_t(const CUtensorMap &qmap, const CUtensorMap &
             cudaFuncSetAttribute(attn_prefill_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kBytes);
     });
     if (attr_err[dev] != cudaSuccess) return attr_err[dev];
-    // unit list and V' in one launch: one extra row of CTAs (y = batch) holds the scheduler
-    dim3 cgrid((p.max_seqlen_k + kCvtKeys - 1) / kCvtKeys, p.batch + 1);
+    // unit list and V' in one launch: one extra row of CTAs (y = batch) holds the
+    // scheduler; with a paged V' cache the scheduler alone
+    const dim3 cgrid = p.v16_paged ? dim3(1, 1) : dim3((p.max_seqlen_k + kCvtKeys - 1) / kCvtKeys, p.batch + 1);
     attn_prefill_prep_kernel<<<cgrid, kCvtThreads, 0, stream>>>(p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;

@@ -53,7 +53,7 @@
 extern "C" {
 #endif
 
-#define ATTN_ABI_VERSION 1
+#define ATTN_ABI_VERSION 2
 
 typedef enum attn_status {
     ATTN_OK = 0,
@@ -97,9 +97,18 @@ typedef enum attn_status {
  *   causal       nonzero: bottom-right aligned mask, query i of a sequence
  *                with Lq queries and Lk keys sees keys j <= Lk - Lq + i
  *   block_size   paged only: a power of two >= 16; num_blocks > 0
+ *   v16_cache    nullable, paged only: an fp16 cache [num_blocks, block_size,
+ *                num_heads_kv, head_dim] holding V / 16 for every cached key,
+ *                kept by store_kvcache (its v16_cache argument).  The P V
+ *                product then reads V / 16 from it through the block table and
+ *                the call converts nothing; without it each call writes an fp16
+ *                copy of the V rows it reads into the workspace.  (A paged V
+ *                tile past a sequence's last key is zeroed in shared memory, so
+ *                cache slots past the end may hold anything.)
  *   workspace    device scratch of at least attn_varlen_workspace_size(...)
- *                bytes, 256-byte aligned: it receives an fp16 copy of V (V / 16)
- *                laid out by logical key, which the P V product reads
+ *                bytes, 256-byte aligned: without v16_cache it receives an fp16
+ *                copy of V (V / 16) laid out by logical key, which the P V
+ *                product reads; with v16_cache size it with total_k = 0
  * Value range: the P V product runs in fp16 on 16 P and V / 16, so V entries
  * must satisfy |v| < 2^20; larger (or non-finite) entries are clamped and
  * reported as ATTN_ERR_DEVICE_RANGE by attn_get_last_device_error.
@@ -115,7 +124,7 @@ ATTN_API attn_status attn_varlen_fwd(const void *q, const void *k, const void *v
                             int num_heads_q, int num_heads_kv, int head_dim,
                             float softmax_scale, int causal,
                             const int32_t *block_table, int block_table_stride,
-                            int block_size, int64_t num_blocks,
+                            int block_size, int64_t num_blocks, const void *v16_cache,
                             int64_t q_row_stride, int64_t k_row_stride, int64_t v_row_stride,
                             int64_t out_row_stride,
                             void *workspace, size_t workspace_bytes, void *stream);
@@ -256,6 +265,11 @@ ATTN_API attn_status attn_decode_paged_noalloc(const void *q, const void *k_cach
  *                 k_row_stride / v_row_stride (elements, 0 = packed)
  *   k_cache, v_cache  viewed as [num_slots, num_heads_kv, head_dim]
  *                 (num_slots = num_blocks * block_size)
+ *   v16_cache     nullable: an fp16 cache shaped like v_cache that also
+ *                 receives V / 16 (round to nearest) at the same slots, for
+ *                 attn_varlen_fwd's and attn_kvcache_fwd's v16_cache argument;
+ *                 values with |v| >= 2^20 (or non-finite) saturate and are
+ *                 reported as ATTN_ERR_DEVICE_RANGE
  *   slot_mapping  int64 [num_tokens]: flat slot block_id * block_size +
  *                 offset; a negative slot skips the token; a slot >=
  *                 num_slots is skipped and flagged in the error word.
@@ -263,8 +277,8 @@ ATTN_API attn_status attn_decode_paged_noalloc(const void *q, const void *k_cach
  * head_dim may be any even value here (the copy is type-agnostic).
  * ------------------------------------------------------------------------ */
 ATTN_API attn_status store_kvcache(const void *k, const void *v, void *k_cache, void *v_cache,
-                          const int64_t *slot_mapping, int64_t num_tokens, int num_heads_kv,
-                          int head_dim, int64_t k_row_stride, int64_t v_row_stride,
+                          void *v16_cache, const int64_t *slot_mapping, int64_t num_tokens,
+                          int num_heads_kv, int head_dim, int64_t k_row_stride, int64_t v_row_stride,
                           int64_t num_slots, void *stream);
 
 /* ------------------------------------------------------------------------
@@ -322,19 +336,23 @@ ATTN_API size_t attn_padded_workspace_size(int batch, int seqlen_q, int seqlen_k
  *   causal       bottom-right: new token i sees keys j <= cache_seqlens[b] -
  *                seqlen_q + i; 0 = every cached key
  *   block_table, block_size, num_blocks: as for attn_varlen_fwd (paged mode)
+ *   v16_cache    nullable: the fp16 V / 16 cache kept by store_kvcache; the
+ *                prefill route then reads it instead of converting V (the
+ *                decode route reads the bf16 v_cache either way)
  *   workspace    at least attn_kvcache_workspace_size(...) bytes, 256-byte
  *                aligned.  On the decode route it holds the split partials
- *                (at most 64 splits of fp32 rows); on the prefill route the
- *                fp16 copy of V for batch * max_cache_seqlen keys, so there it
- *                grows with the cache length.
+ *                (at most 64 splits of fp32 rows); on the prefill route without
+ *                v16_cache the fp16 copy of V for batch * max_cache_seqlen keys,
+ *                so there it grows with the cache length.
  * Returns the statuses of attn_varlen_fwd.
  * ------------------------------------------------------------------------ */
 ATTN_API attn_status attn_kvcache_fwd(const void *q, const void *k_cache, const void *v_cache, void *out,
                                       float *lse, const int32_t *cache_seqlens, const int32_t *block_table,
                                       int block_table_stride, int batch, int seqlen_q, int num_heads_q,
                                       int num_heads_kv, int head_dim, int block_size, int64_t num_blocks,
-                                      int max_cache_seqlen, float softmax_scale, int causal, void *workspace,
-                                      size_t workspace_bytes, void *stream);
+                                      int max_cache_seqlen, float softmax_scale, int causal,
+                                      const void *v16_cache, void *workspace, size_t workspace_bytes,
+                                      void *stream);
 
 /* Workspace bytes attn_kvcache_fwd needs (0 for invalid sizes). */
 ATTN_API size_t attn_kvcache_workspace_size(int batch, int seqlen_q, int num_heads_q, int num_heads_kv,

@@ -22,7 +22,7 @@ def test_every_declared_symbol_is_exported(L):
 
 
 def test_abi_version_and_status_strings(L):
-    assert L.attn_abi_version() == 1
+    assert L.attn_abi_version() == 2
     for s in range(9):
         assert L.attn_status_string(s)
     assert L.attn_status_string(99) == b"unknown status"
@@ -31,14 +31,14 @@ def test_abi_version_and_status_strings(L):
 def test_host_validation_without_device(L):
     null = None
     # store_kvcache: null pointers / negative sizes
-    assert L.store_kvcache(null, null, null, null, null, 5, 8, 128, 0, 0, 10, null) == 1
-    assert L.store_kvcache(null, null, null, null, null, -1, 8, 128, 0, 0, 10, null) == 1
-    assert L.store_kvcache(null, null, null, null, null, 0, 8, 128, 0, 0, 10, null) == 0   # nothing to do
+    assert L.store_kvcache(null, null, null, null, null, null, 5, 8, 128, 0, 0, 10, null) == 1
+    assert L.store_kvcache(null, null, null, null, null, null, -1, 8, 128, 0, 0, 10, null) == 1
+    assert L.store_kvcache(null, null, null, null, null, null, 0, 8, 128, 0, 0, 10, null) == 0   # nothing to do
     fake = ctypes.c_void_p(0x1000)
     # varlen: Hq not a multiple of Hkv, bad scale, unsupported head_dim, misaligned stride
     args = lambda **kw: [fake, fake, fake, fake, null, fake, fake, kw.get("B", 2), 8, 8, 4, 4, kw.get("Hq", 4),
-                         kw.get("Hkv", 4), kw.get("D", 64), kw.get("scale", 0.125), 1, null, 0, 0, 0,
-                         kw.get("qs", 0), 0, 0, 0, null, 0, null]
+                         kw.get("Hkv", 4), kw.get("D", 64), kw.get("scale", 0.125), 1, kw.get("bt", null), 0, 0, 0,
+                         kw.get("v16", null), kw.get("qs", 0), 0, 0, 0, null, 0, null]
     assert L.attn_varlen_fwd(*args(Hq=6, Hkv=4)) == 1
     assert L.attn_varlen_fwd(*args(scale=0.0)) == 1
     assert L.attn_varlen_fwd(*args(scale=float("nan"))) == 1
@@ -46,6 +46,7 @@ def test_host_validation_without_device(L):
     assert L.attn_varlen_fwd(*args(Hq=12, Hkv=4)) == 2       # group of 3 does not divide the 128-row slot
     assert L.attn_varlen_fwd(*args(qs=4 * 64 + 3)) == 1        # row stride not 16-byte aligned
     assert L.attn_varlen_fwd(*args(B=0)) == 1
+    assert L.attn_varlen_fwd(*args(v16=fake)) == 1            # a V / 16 cache needs a block table
     # decode: block size must be a power of two >= 16; group <= 64
     dec = lambda **kw: [fake, fake, fake, fake, null, fake, fake, 4, 2, kw.get("Hq", 8), kw.get("Hkv", 8), 128,
                         kw.get("bs", 16), 10, 64, 0.1, 0, 0, 0, null, 0, null]
@@ -70,9 +71,9 @@ def test_new_entries_validate_on_the_host(L):
     L.attn_softmax_rows.restype = ctypes.c_int
     # kv-cache: null pointers, non-positive seqlen_q, batch
     assert L.attn_kvcache_fwd(null, fake, fake, fake, null, fake, fake, 4, 2, 3, 32, 8, 128, 16, 64, 64,
-                              ctypes.c_float(0.1), 1, fake, ctypes.c_size_t(1 << 30), null) == 1
+                              ctypes.c_float(0.1), 1, null, fake, ctypes.c_size_t(1 << 30), null) == 1
     assert L.attn_kvcache_fwd(fake, fake, fake, fake, null, fake, fake, 4, 2, 0, 32, 8, 128, 16, 64, 64,
-                              ctypes.c_float(0.1), 1, fake, ctypes.c_size_t(1 << 30), null) == 1
+                              ctypes.c_float(0.1), 1, null, fake, ctypes.c_size_t(1 << 30), null) == 1
     # padded: null q, zero batch
     assert L.attn_padded_fwd(null, fake, fake, fake, null, null, null, 2, 16, 16, 8, 8, 64, ctypes.c_float(0.1), 1,
                              fake, ctypes.c_size_t(1 << 30), null) == 1

@@ -10,11 +10,11 @@ import attention_attn_varlen_gb300.attention as at
 def calls(monkeypatch):
     log = []
 
-    def fake_store(k, v, kc, vc, slots):
-        log.append(("store", k, kc, slots))
+    def fake_store(k, v, kc, vc, slots, v16_cache=None):
+        log.append(("store", k, kc, slots, v16_cache))
 
-    def fake_varlen(q, k, v, cu_q, cu_k, mq, mk, scale, causal=True, block_table=None):
-        log.append(("varlen", k, block_table, causal, scale))
+    def fake_varlen(q, k, v, cu_q, cu_k, mq, mk, scale, causal=True, block_table=None, v16_cache=None):
+        log.append(("varlen", k, block_table, causal, scale, v16_cache))
         return torch.zeros_like(q)
 
     def fake_decode(q, kc, vc, lens, bt, scale, max_cache_seqlen=None):
@@ -23,7 +23,7 @@ def calls(monkeypatch):
 
     monkeypatch.setattr(at, "store_kvcache", fake_store)
     monkeypatch.setattr(at, "attn_varlen_fwd", fake_varlen)
-    def fake_kvcache(q, kc, vc, lens, bt, scale, causal=True, max_cache_seqlen=None):
+    def fake_kvcache(q, kc, vc, lens, bt, scale, causal=True, max_cache_seqlen=None, v16_cache=None):
         log.append(("kvcache", tuple(q.shape), lens, bt, causal, max_cache_seqlen))
         return torch.zeros_like(q)
 
@@ -119,3 +119,16 @@ def test_multi_token_decode_goes_through_the_kvcache_entry(calls):
         q5, k5, v5 = _qkv(5)
         layer(q5, k5, v5, ctx)
 
+
+
+def test_v16_cache_is_filled_by_the_store_and_read_by_the_prefix_prefill(calls):
+    layer = _layer()
+    layer.v16_cache = torch.zeros(4, 16, 2, 16, dtype=torch.float16)
+    q, k, v = _qkv(5)
+    bt = torch.zeros(1, 4, dtype=torch.int32)
+    ctx = at.AttentionContext(True, slot_mapping=torch.arange(5), cu_seqlens_q=torch.tensor([0, 5]),
+                              cu_seqlens_k=torch.tensor([0, 9]), max_seqlen_q=5, max_seqlen_k=9, block_tables=bt)
+    layer(q, k, v, ctx)
+    assert [c[0] for c in calls] == ["store", "varlen"]
+    assert calls[0][4] is layer.v16_cache
+    assert calls[1][5] is layer.v16_cache and calls[1][1] is layer.k_cache

@@ -22,7 +22,10 @@ def _cu(lens):
     return torch.tensor(np.concatenate([[0], np.cumsum(lens)]), dtype=torch.int32)
 
 
-def test_engine_steps_match_oracle():
+@pytest.mark.parametrize("v16", [False, True])
+def test_engine_steps_match_oracle(v16):
+    """v16: the layer also keeps the fp16 V / 16 cache (filled by the store, read
+    by the prefix prefill and the kv-cache entry's prefill route)."""
     gen = torch.Generator().manual_seed(77)
     rng = np.random.default_rng(77)
     prompts = np.array([37, 300, 5])
@@ -33,6 +36,8 @@ def test_engine_steps_match_oracle():
     layer = Attention(Hq, D, D ** -0.5, Hkv)
     layer.k_cache = torch.full((num_blocks, BS, Hkv, D), float("nan"), dtype=torch.bfloat16, device="cuda")
     layer.v_cache = torch.full_like(layer.k_cache, float("nan"))
+    if v16:
+        layer.v16_cache = torch.full(layer.k_cache.shape, float("nan"), dtype=torch.float16, device="cuda")
     hist_k = [torch.empty(0, Hkv, D, dtype=torch.bfloat16) for _ in range(B)]
     hist_v = [torch.empty(0, Hkv, D, dtype=torch.bfloat16) for _ in range(B)]
     lens = np.zeros(B, dtype=np.int64)
@@ -75,3 +80,4 @@ def test_engine_steps_match_oracle():
     step([1, 1, 1], "decode")
     step([3, 3, 3], "decode")        # three new tokens per sequence (the kv-cache entry)
     step([20, 3, 40], "prefix")
+    step([17, 17, 17], "decode")     # 17 x 4 query rows per KV head: the kv-cache entry's prefill route

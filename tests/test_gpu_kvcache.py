@@ -8,7 +8,7 @@ import attention_attn_varlen_gb300 as av
 import oracle
 import workloads
 from _util import assert_close, assert_lse_close
-from test_gpu_prefill import _paged_device, _paged_oracle, _run_paged
+from test_gpu_prefill import _paged_device, _paged_oracle, _run_paged, v16_of
 
 pytestmark = pytest.mark.gpu
 
@@ -69,6 +69,14 @@ def test_kvcache_equals_paged_varlen_bitexact():
     torch.cuda.synchronize()
     assert torch.equal(out_k.view(-1, cfg.Hq, cfg.D).view(torch.int16), out_v.view(torch.int16))
     assert torch.equal(lse_k, lse_v)
+    # the prefill route with the fp16 V / 16 cache: same bits
+    out_h, lse_h = av.attn_with_kvcache(q.cuda().view(cfg.batch, 17, cfg.Hq, cfg.D), kc, vc, cs, bt, cfg.scale,
+                                        max_cache_seqlen=int(cfg.lens_k.max()), return_lse=True,
+                                        v16_cache=v16_of(vc))
+    torch.cuda.synchronize()
+    assert av.get_last_device_error()[0] == 0
+    assert torch.equal(out_h.view(torch.int16), out_k.view(torch.int16))
+    assert torch.equal(lse_h, lse_k)
 
 
 @pytest.mark.parametrize("causal", [False, True])

@@ -131,11 +131,24 @@ def _paged_oracle(cfg, q, k_new, v_new, seqs, rows_local=None, causal=True, lens
     return ref, ref_lse, tok_idx
 
 
-def _run_paged(cfg, q, kc, vc):
+def _run_paged(cfg, q, kc, vc, v16=None):
     cu_q = torch.from_numpy(workloads.cu_from_lens(cfg.new)).cuda()
     cu_k = torch.from_numpy(workloads.cu_from_lens(cfg.lens_k)).cuda()
     return av.attn_varlen_fwd(q.cuda(), kc, vc, cu_q, cu_k, int(cfg.new.max()), int(cfg.lens_k.max()), cfg.scale,
-                              causal=True, block_table=torch.from_numpy(cfg.block_table).cuda(), return_lse=True)
+                              causal=True, block_table=torch.from_numpy(cfg.block_table).cuda(), return_lse=True,
+                              v16_cache=v16)
+
+
+def v16_of(vc, blocks=None):
+    """An fp16 V / 16 cache for the bf16 cache vc, as store_kvcache keeps it (torch's
+    round-to-nearest conversion; NaN stays NaN).  blocks: only these block ids, the
+    rest NaN."""
+    out = torch.full(vc.shape, float("nan"), dtype=torch.float16, device=vc.device)
+    idx = torch.arange(vc.shape[0], device=vc.device) if blocks is None else blocks
+    for i in range(0, idx.numel(), 256):
+        j = idx[i:i + 256]
+        out[j] = (vc[j].float() / 16.0).half()
+    return out
 
 
 PAGED_CASES = [
@@ -145,6 +158,25 @@ PAGED_CASES = [
     (33, [511, 2048], [129, 3], 8, 8, 128, 64),
     (34, [90, 700], [40, 333], 16, 2, 64, 32),
 ]
+
+
+@pytest.mark.parametrize("seed,ctx,new,Hq,Hkv,D,bs", PAGED_CASES)
+def test_paged_prefill_v16_cache_is_bitexact(seed, ctx, new, Hq, Hkv, D, bs):
+    """Reading V / 16 from an fp16 cache kept beside the bf16 one gives the bits
+    of the call that converts V itself; the V' cache rows past every sequence
+    hold NaN (they must be zeroed before the P V product)."""
+    cfg = workloads.small_paged(seed, ctx=ctx, new=new, Hq=Hq, Hkv=Hkv, D=D, block_size=bs)
+    q = cfg.q()
+    kc, vc, _, _ = _paged_device(cfg)
+    v16 = v16_of(vc)
+    av.get_last_device_error()
+    out_a, lse_a = _run_paged(cfg, q, kc, vc)
+    out_b, lse_b = _run_paged(cfg, q, kc, vc, v16)
+    torch.cuda.synchronize()
+    assert av.get_last_device_error()[0] == 0
+    assert torch.isfinite(out_b.float()).all()
+    assert torch.equal(out_a.view(torch.int16), out_b.view(torch.int16))
+    assert torch.equal(lse_a, lse_b)
 
 
 @pytest.mark.parametrize("seed,ctx,new,Hq,Hkv,D,bs", PAGED_CASES)
@@ -255,7 +287,15 @@ def test_c3_prefix_paged_full_size_sampled():
     ref, ref_lse, tok_idx = _paged_oracle(cfg, q, k_new, v_new, seqs, rows_local)
     rows = tok_idx[rows_local // Hq] * Hq + rows_local % Hq
     check_rows(out, lse, ref, ref_lse, rows, Hq, "c3")
-    del kc, vc
+    # the same step with the fp16 V / 16 cache (referenced blocks only; the rest NaN)
+    used = torch.from_numpy(np.unique(cfg.block_table[cfg.block_table >= 0]).astype(np.int64)).cuda()
+    v16 = v16_of(vc, used)
+    out16, lse16 = _run_paged(cfg, q, kc, vc, v16)
+    torch.cuda.synchronize()
+    assert av.get_last_device_error()[0] == 0
+    assert torch.equal(out.view(torch.int16), out16.view(torch.int16))
+    assert torch.equal(lse, lse16)
+    del kc, vc, v16
     torch.cuda.empty_cache()
 
 

@@ -59,3 +59,54 @@ def test_store_kvcache_bad_slot_is_flagged_not_written():
     assert kc[0].float().eq(1).all() and kc[3].float().eq(1).all()
     assert kc[1].float().eq(0).all() and kc[2].float().eq(0).all()
     assert av.get_last_device_error()[0] == 0          # the word was cleared
+
+
+@pytest.mark.parametrize("Hkv,D,strided", [(8, 128, False), (8, 128, True), (2, 96, False), (2, 3, False)])
+def test_store_kvcache_fp16_v_over_16(Hkv, D, strided):
+    """With v16_cache the store also writes V / 16 as fp16 at the same slots
+    (round to nearest, torch's conversion as the reference); other slots keep
+    their sentinel bits, and K/V are written exactly as without it."""
+    rng = np.random.default_rng(200 + D)
+    N, num_slots = 257, 700
+    slots = rng.permutation(num_slots)[:N].astype(np.int64)
+    slots[::13] = -1
+    if strided:
+        big = workloads.normal_bf16((8, 1), N, 3 * Hkv * D).view(N, 3 * Hkv, D)
+        k_h, v_h = big[:, Hkv:2 * Hkv], big[:, 2 * Hkv:]
+    else:
+        k_h = workloads.normal_bf16((8, 2), N, Hkv * D).view(N, Hkv, D)
+        v_h = (workloads.normal_bf16((8, 3), N, Hkv * D).float() * 300.0).to(torch.bfloat16).view(N, Hkv, D)
+    sentinel = torch.from_numpy(rng.integers(0, 1 << 16, size=(num_slots, Hkv, D), dtype=np.uint16).view(np.int16))
+    kc_h = sentinel.view(torch.bfloat16).clone()
+    vc_h = sentinel.view(torch.bfloat16).clone()
+    v16_h = sentinel.view(torch.float16).clone()
+    exp_k, exp_v = oracle.store_kvcache(k_h.contiguous(), v_h.contiguous(), kc_h, vc_h, slots)
+    exp_16 = v16_h.clone()
+    keep = slots >= 0
+    exp_16[torch.from_numpy(slots[keep])] = (v_h.contiguous()[torch.from_numpy(keep)].float() / 16.0).half()
+    if strided:
+        big_d = big.cuda()
+        k_d, v_d = big_d[:, Hkv:2 * Hkv], big_d[:, 2 * Hkv:]
+    else:
+        k_d, v_d = k_h.cuda(), v_h.cuda()
+    kc_d, vc_d, v16_d = kc_h.cuda(), vc_h.cuda(), v16_h.cuda()
+    av.get_last_device_error()
+    av.store_kvcache(k_d, v_d, kc_d, vc_d, torch.from_numpy(slots).cuda(), v16_cache=v16_d)
+    torch.cuda.synchronize()
+    assert av.get_last_device_error()[0] == 0
+    assert np.array_equal(_bits(kc_d), exp_k.reshape(num_slots, Hkv, D))
+    assert np.array_equal(_bits(vc_d), exp_v.reshape(num_slots, Hkv, D))
+    assert torch.equal(v16_d.cpu().view(torch.int16), exp_16.view(torch.int16))
+
+
+def test_store_kvcache_v_beyond_fp16_range_is_reported():
+    N, Hkv, D, num_slots = 4, 2, 64, 16
+    v = torch.ones((N, Hkv, D), dtype=torch.bfloat16, device="cuda")
+    v[2, 1, 5] = 3.0e6
+    kc = torch.zeros((num_slots, Hkv, D), dtype=torch.bfloat16, device="cuda")
+    vc, v16 = torch.zeros_like(kc), torch.zeros((num_slots, Hkv, D), dtype=torch.float16, device="cuda")
+    av.get_last_device_error()
+    av.store_kvcache(v, v, kc, vc, torch.tensor([0, 1, 2, 3], dtype=torch.int64, device="cuda"), v16_cache=v16)
+    st, word = av.get_last_device_error()
+    assert st == 8 and word & 4
+    assert torch.isfinite(v16.float()).all() and v16[2, 1, 5].item() == 65504.0
