@@ -404,9 +404,12 @@ static attn_status varlen_impl(const void *q, const void *k, const void *v, void
     void *v16 = ws + kWsHeader;
     const int64_t kv_rows = paged ? num_blocks * (int64_t)block_size : total_k;
     const int kv_box = paged ? (block_size < kPrefillKeyTile ? block_size : kPrefillKeyTile) : kPrefillKeyTile;
-    CUtensorMap qmap, kmap, vmap;
+    CUtensorMap qmap, kmap, vmap, omap;
+    // output boxes: one warp's 32 rows of a slot (min(G, 32) heads x 32 / min(G, 32) tokens)
+    const int obh = G < 32 ? G : 32;
     if (!make_map(&qmap, q, total_q, num_heads_q, head_dim, q_row_stride, G, tps) ||
-        !make_map(&kmap, k, kv_rows, num_heads_kv, head_dim, k_row_stride, 1, kv_box))
+        !make_map(&kmap, k, kv_rows, num_heads_kv, head_dim, k_row_stride, 1, kv_box) ||
+        !make_map(&omap, out, total_q, num_heads_q, head_dim, out_row_stride, obh, 32 / obh))
         return ATTN_ERR_LAUNCH_FAILED;
     if (v16_cache ? !make_map(&vmap, v16_cache, kv_rows, num_heads_kv, head_dim, (int64_t)num_heads_kv * head_dim, 1,
                               kv_box, CU_TENSOR_MAP_DATA_TYPE_FLOAT16)
@@ -450,7 +453,7 @@ static attn_status varlen_impl(const void *q, const void *k, const void *v, void
     p.units = reinterpret_cast<int2 *>(ws + kWsHeader + v16_bytes(num_heads_kv, head_dim, ws_keys));
     p.scale_log2 = softmax_scale * 1.4426950408889634f;
     p.err = d->err;
-    cudaError_t e = launch_prefill(qmap, kmap, vmap, p, head_dim, reinterpret_cast<cudaStream_t>(stream));
+    cudaError_t e = launch_prefill(qmap, kmap, vmap, omap, p, head_dim, reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) {
         cudaGetLastError();
         return ATTN_ERR_LAUNCH_FAILED;

@@ -89,6 +89,6 @@ cudaError_t launch_kvcache_cu(const int32_t *cache_seqlens, int batch, int seqle
                               int32_t *cu_q, int32_t *cu_k, uint32_t *err, cudaStream_t stream);
 
 cudaError_t launch_prefill(const CUtensorMap &qmap, const CUtensorMap &kmap, const CUtensorMap &vmap,
-                           const PrefillParams &p, int head_dim, cudaStream_t stream);
+                           const CUtensorMap &omap, const PrefillParams &p, int head_dim, cudaStream_t stream);
 
 }  // namespace attn

@@ -343,15 +343,27 @@ __device__ __forceinline__ PfUnit pf_unit(const PrefillParams &p, int u) {
     return w;
 }
 
-// Output rows of one slot (warp-collective; every argument but the row data is
-// warp-uniform where it steers a tcgen05 op): O_X / d' -> bf16, and the lse,
-// read from TMEM when the slot had key tiles, zeros otherwise.
+// Output rows of one slot, 32 rows per warp (warp-collective; every argument
+// but l and m_ref is warp-uniform): O_X / d' -> bf16, read from TMEM when the
+// slot had key tiles (zeros otherwise), and the lse.  The rows are staged in
+// this warp's own rows of the slot's P' tile (free: the slot's last PV has
+// completed) in the 128-byte-swizzled layout of an output box (64 dims x
+// min(G, 32) heads x 32 / min(G, 32) tokens per panel), and one thread writes
+// them with a TMA store per panel.  A warp holding rows past the sequence's
+// end (its last slot) writes its valid rows itself instead: a box would
+// overwrite the next sequence's rows.  Out of line: it runs once per unit, and
+// its registers then do not constrain the softmax's per-tile code.
 template <int D>
-__device__ __forceinline__ void pf_store_rows(const PrefillParams &p, uint32_t tO, bool has_tiles, bool row_valid,
-                                              int64_t qrow, int head, float l, float m_ref) {
-    if (!__any_sync(0xffffffffu, row_valid)) return;
+__device__ __noinline__ void pf_store_rows(const PrefillParams &p, const CUtensorMap *omap, uint32_t tO,
+                                              uint8_t *pslot, bool has_tiles, int64_t qbase, int ntok, int hkv,
+                                              float l, float m_ref) {
+    const int G = p.G, lane = threadIdx.x & 31, wrow0 = ((threadIdx.x >> 5) & 3) * 32;
+    if (wrow0 / G >= ntok) return;   // no valid row in this warp
+    const int r = wrow0 + lane;
+    const bool row_valid = r / G < ntok, whole = (wrow0 + 31) / G < ntok;
     const float inv = l > 0.f ? 16.f / l : 0.f;   // l accumulated P' = 16 P
-    __nv_bfloat16 *orow = p.out + (row_valid ? qrow : 0) * p.out_row_stride + (int64_t)head * D;
+    uint8_t *srow = pslot + r * 128;
+    __nv_bfloat16 *orow = p.out + (qbase + r / G) * p.out_row_stride + (int64_t)(hkv * G + r % G) * D;
 #pragma unroll
     for (int c = 0; c < D / 32; ++c) {
         uint32_t o[32];
@@ -362,25 +374,43 @@ __device__ __forceinline__ void pf_store_rows(const PrefillParams &p, uint32_t t
 #pragma unroll
             for (int i = 0; i < 32; ++i) o[i] = 0u;
         }
-        if (row_valid) {
-            uint32_t pk[16];
+        uint32_t pk[16];
 #pragma unroll
-            for (int i = 0; i < 16; ++i)
-                pk[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv, __uint_as_float(o[2 * i + 1]) * inv);
-            uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
+        for (int i = 0; i < 16; ++i)
+            pk[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv, __uint_as_float(o[2 * i + 1]) * inv);
 #pragma unroll
-            for (int i = 0; i < 4; ++i) dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+        for (int i = 0; i < 4; ++i) {
+            const uint4 v4 = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+            const int ch = c * 4 + i;   // 16-byte chunk of the row
+            if (whole)
+                *reinterpret_cast<uint4 *>(srow + (ch >> 3) * kPPanelBytes + (((ch & 7) ^ (r & 7)) << 4)) = v4;
+            else if (row_valid)
+                reinterpret_cast<uint4 *>(orow)[ch] = v4;
         }
     }
     if (row_valid && p.lse)
-        p.lse[(int64_t)head * p.total_q + qrow] = l > 0.f ? (m_ref + __log2f(l) - 4.0f) * 0.69314718055994531f
-                                                          : -INFINITY;
+        p.lse[(int64_t)(hkv * G + r % G) * p.total_q + qbase + r / G] =
+            l > 0.f ? (m_ref + __log2f(l) - 4.0f) * 0.69314718055994531f : -INFINITY;
+    if (whole) {
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+#pragma unroll
+            for (int pn = 0; pn < D / 64; ++pn)
+                tma_store_3d(omap, pslot + pn * kPPanelBytes + wrow0 * 128, pn * 64, hkv * G + wrow0 % G,
+                             (int)(qbase + wrow0 / G));
+            bulk_commit();
+            bulk_wait_read();   // the staging rows are P' rows again right after
+        }
+        __syncwarp();
+    }
 }
 
 template <int D>
 __global__ void __launch_bounds__(kPfThreads, 1)
     attn_prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
-                        const __grid_constant__ CUtensorMap vmap, const PrefillParams p) {
+                        const __grid_constant__ CUtensorMap vmap, const __grid_constant__ CUtensorMap omap,
+                        const PrefillParams p) {
     using S = PfSmem<D>;
     constexpr int ST = S::kStages;
     extern __shared__ uint8_t psmem_raw[];
@@ -620,47 +650,42 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         __syncwarp();
     } else if (warp == 10) {
         // ================================================================ PV issuer
-        // Lane 0 issues every PV.  With a paged V' cache the rows of a tile past the
-        // sequence's last key come from cache slots that may hold anything (even NaN,
-        // and 0 * NaN is NaN inside the MMA): the whole warp zeroes them in shared
-        // memory before the PV that reads the tile.
-        const uint32_t tO[2] = {tmem + 256, tmem + 256 + D};
-        const uint32_t pX[2] = {smem_u32(sP), smem_u32(sP + kPBytes)};
-        const uint32_t ring = smem_u32(sRing);
-        int itb = 0, tc[2] = {0, 0}, k = 0;   // ring items before this unit; PV tiles issued per slot
-        uint32_t vpar = 0;                    // per stage: parity of the V' tiles read from it
-        bool ok = true;
-        for (;; ++k) {
-            int u = -1;
-            ok = __all_sync(0xffffffffu,
-                            mbar_wait(&idx_full[k & 1], (uint32_t)(k >> 1) & 1u, abort_flag, p.err, SRC_PREFILL));
-            if (!ok) break;
-            u = unit_idx[k & 1];
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&idx_empty[k & 1]);
-            if (u < 0) break;
-            const PfUnit w = pf_unit(p, u);
-            const int nX[2] = {w.nA, w.nB};
-            // PV_X(0) of a unit writes O_X afresh: its p_ready comes after the
-            // softmax threads have read O_X of the previous unit
-            for (int j = 0; j < w.n && ok; ++j) {
-                const int itV = itb + (j < w.n - 1 ? 2 * j + 2 : 2 * w.n - 1), stV = itV % ST;
-                ok = __all_sync(0xffffffffu,
-                                mbar_wait(&full_v[stV], (vpar >> stV) & 1u, abort_flag, p.err, SRC_PREFILL));
-                vpar ^= 1u << stV;
+        if (lane == 0) {
+            const uint32_t tO[2] = {tmem + 256, tmem + 256 + D};
+            const uint32_t pX[2] = {smem_u32(sP), smem_u32(sP + kPBytes)};
+            const uint32_t ring = smem_u32(sRing);
+            int itb = 0, tc[2] = {0, 0}, k = 0;   // ring items before this unit; PV tiles issued per slot
+            uint32_t vpar = 0;                    // per stage: parity of the V' tiles read from it
+            bool ok = true;
+            for (;; ++k) {
+                ok = mbar_wait(&idx_full[k & 1], (uint32_t)(k >> 1) & 1u, abort_flag, p.err, SRC_PREFILL);
                 if (!ok) break;
-                if (p.v16_paged && (j + 1) * BN > w.Lk) {
-                    const int r0 = max(w.Lk - j * BN, 0);
-                    uint8_t *tile = sRing + stV * S::kTileBytes;
-                    for (int i = lane; i < (BN - r0) * S::kPanels * 8; i += 32) {
-                        const int rr = r0 + i / (S::kPanels * 8), c = i % (S::kPanels * 8);
-                        *reinterpret_cast<uint4 *>(tile + (c >> 3) * S::kPanelBytes + rr * 128 + ((c & 7) << 4)) =
-                            make_uint4(0u, 0u, 0u, 0u);
+                const int u = unit_idx[k & 1];
+                mbar_arrive(&idx_empty[k & 1]);
+                if (u < 0) break;
+                const PfUnit w = pf_unit(p, u);
+                const int nX[2] = {w.nA, w.nB};
+                // PV_X(0) of a unit writes O_X afresh: its p_ready comes after the
+                // softmax threads have read O_X of the previous unit
+                for (int j = 0; j < w.n && ok; ++j) {
+                    const int itV = itb + (j < w.n - 1 ? 2 * j + 2 : 2 * w.n - 1), stV = itV % ST;
+                    ok = mbar_wait(&full_v[stV], (vpar >> stV) & 1u, abort_flag, p.err, SRC_PREFILL);
+                    vpar ^= 1u << stV;
+                    if (!ok) break;
+                    if (p.v16_paged && (j + 1) * BN > w.Lk) {
+                        // with a paged V' cache the tile's rows past the sequence's last key
+                        // come from cache slots that may hold anything (NaN included, and
+                        // 0 * NaN is NaN inside the MMA): zero them first
+                        const int r0 = max(w.Lk - j * BN, 0);
+                        uint8_t *tile = sRing + stV * S::kTileBytes;
+                        for (int pn = 0; pn < S::kPanels; ++pn)
+                            for (int rr = r0; rr < BN; ++rr) {
+                                uint4 *row = reinterpret_cast<uint4 *>(tile + pn * S::kPanelBytes + rr * 128);
+#pragma unroll
+                                for (int c = 0; c < 8; ++c) row[c] = make_uint4(0u, 0u, 0u, 0u);
+                            }
+                        fence_proxy_async_smem();
                     }
-                    fence_proxy_async_smem();
-                    __syncwarp();
-                }
-                if (lane == 0) {
 #pragma unroll
                     for (int x = 0; x < 2; ++x) {
                         if (j >= nX[x]) continue;
@@ -671,14 +696,12 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                         tc_commit(&pv_done[x]);
                         ++tc[x];
                     }
-                    if (ok) tc_commit(&empty[stV]);
+                    if (!ok) break;
+                    tc_commit(&empty[stV]);
                 }
-                ok = __shfl_sync(0xffffffffu, ok, 0);
+                if (!ok) break;
+                itb += 2 * w.n;
             }
-            if (!ok) break;
-            itb += 2 * w.n;
-        }
-        if (lane == 0) {
             tc_commit(&drain[1]);
             mbar_wait(&drain[1], 0, nullptr, p.err, SRC_PREFILL);
         }
@@ -697,10 +720,11 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         // The rows of the previous unit are stored once its last PV is done: in
         // the first tile of the next unit, after the exponentials and before
         // P'_X(0) is published (so PV_X(0) cannot overwrite O_X before it is read).
-        bool pend = false, pend_tiles = false, pend_valid = false;
-        int64_t pend_qrow = 0;
-        int pend_head = 0;
+        bool pend = false, pend_tiles = false;
+        int64_t pend_qbase = 0;   // packed row of the slot's first token
+        int pend_ntok = 0, pend_hkv = 0;
         float pend_l = 0.f, pend_m = 0.f;
+        uint8_t *pslot = sP + X * kPBytes;
         for (;; ++k) {
             ok = __all_sync(0xffffffffu,
                             mbar_wait(&idx_full[k & 1], (uint32_t)(k >> 1) & 1u, abort_flag, p.err, SRC_PREFILL));
@@ -712,8 +736,6 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             const int t0 = X ? w.t0B : w.t0A;
             const int nX = X ? w.nB : w.nA;
             const int tok = t0 + r / G;
-            const int head = w.hkv * G + r % G;
-            const bool row_valid = tok < w.Lq;
             // last key this row may see (negative: none)
             const int lim = p.causal ? min(tok + w.off, w.Lk - 1) : w.Lk - 1;
             float m_ref = -INFINITY;   // reference max (log2 units) used for P
@@ -781,7 +803,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                     tc_fence_after();
                 }
                 if (pend) {   // j == 0: O_X holds the previous unit's result
-                    pf_store_rows<D>(p, tO, pend_tiles, pend_valid, pend_qrow, pend_head, pend_l, pend_m);
+                    pf_store_rows<D>(p, &omap, tO, pslot, pend_tiles, pend_qbase, pend_ntok, pend_hkv, pend_l, pend_m);
                     pend = false;
                 }
                 // O *= alpha where the reference moved (O of tile 0 is written, not accumulated)
@@ -819,14 +841,14 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                     if (!ok) break;
                     tc_fence_after();
                 }
-                pf_store_rows<D>(p, tO, pend_tiles, pend_valid, pend_qrow, pend_head, pend_l, pend_m);
+                pf_store_rows<D>(p, &omap, tO, pslot, pend_tiles, pend_qbase, pend_ntok, pend_hkv, pend_l, pend_m);
             }
             cX += nX;
             pend = true;
             pend_tiles = nX > 0;
-            pend_valid = row_valid;
-            pend_qrow = (int64_t)w.qs + tok;
-            pend_head = head;
+            pend_qbase = (int64_t)w.qs + t0;
+            pend_ntok = min(max(w.Lq - t0, 0), BM / G);
+            pend_hkv = w.hkv;
             pend_l = l;
             pend_m = m_ref;
         }
@@ -837,9 +859,10 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                                                        SRC_PREFILL));
             if (ok) {
                 tc_fence_after();
-                pf_store_rows<D>(p, tO, pend_tiles, pend_valid, pend_qrow, pend_head, pend_l, pend_m);
+                pf_store_rows<D>(p, &omap, tO, pslot, pend_tiles, pend_qbase, pend_ntok, pend_hkv, pend_l, pend_m);
             }
         }
+        if (lane == 0) bulk_wait_all();   // this warp's output stores are complete before it exits
     }
     tc_fence_before();
     __syncthreads();
@@ -927,7 +950,7 @@ cudaError_t launch_kvcache_cu(const int32_t *cache_seqlens, int batch, int seqle
 
 template <int D>
 static cudaError_t launch_prefill_t(const CUtensorMap &qmap, const CUtensorMap &kmap, const CUtensorMap &vmap,
-                                    const PrefillParams &p, cudaStream_t stream) {
+                                    const CUtensorMap &omap, const PrefillParams &p, cudaStream_t stream) {
     using S = PfSmem<D>;
     static std::once_flag attr_once[kMaxDev];
     static cudaError_t attr_err[kMaxDev];
@@ -947,15 +970,15 @@ static cudaError_t launch_prefill_t(const CUtensorMap &qmap, const CUtensorMap &
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     main_kernel_event_before(stream);
-    attn_prefill_kernel<D><<<p.num_ctas, kPfThreads, S::kBytes, stream>>>(qmap, kmap, vmap, p);
+    attn_prefill_kernel<D><<<p.num_ctas, kPfThreads, S::kBytes, stream>>>(qmap, kmap, vmap, omap, p);
     main_kernel_event_after(stream);
     return cudaGetLastError();
 }
 
 cudaError_t launch_prefill(const CUtensorMap &qmap, const CUtensorMap &kmap, const CUtensorMap &vmap,
-                           const PrefillParams &p, int head_dim, cudaStream_t stream) {
-    if (head_dim == 128) return launch_prefill_t<128>(qmap, kmap, vmap, p, stream);
-    return launch_prefill_t<64>(qmap, kmap, vmap, p, stream);
+                           const CUtensorMap &omap, const PrefillParams &p, int head_dim, cudaStream_t stream) {
+    if (head_dim == 128) return launch_prefill_t<128>(qmap, kmap, vmap, omap, p, stream);
+    return launch_prefill_t<64>(qmap, kmap, vmap, omap, p, stream);
 }
 
 }  // namespace attn

@@ -13,6 +13,8 @@ with the device error status.  No timing, no comparison.
   --op softmax  attn_softmax_rows on a seeded [--rows, --cols] matrix (--dtype f32 | bf16;
                 --workload is ignored)
   --seqs N      keep only the first N sequences (smaller captures)
+  --v16         paged prefill / store: keep the fp16 V / 16 cache beside the bf16
+                one (filled for the blocks in use, then by the store)
   --compact-pool  paged workloads: a pool of just the blocks the block table
                 uses, ids randomly permuted (same block size, lengths and
                 shared-prefix blocks; for profiler captures of a few GB at most)
@@ -70,6 +72,7 @@ def main(argv=None):
     ap.add_argument("--iters", type=int, default=3)
     ap.add_argument("--seqs", type=int, default=None)
     ap.add_argument("--compact-pool", action="store_true")
+    ap.add_argument("--v16", action="store_true")
     a = ap.parse_args(argv)
     av.lib()
     dev = torch.device("cuda", 0)
@@ -121,11 +124,18 @@ def main(argv=None):
             cu_q = torch.from_numpy(workloads.cu_from_lens(cfg.new)).to(dev)
             cu_k = torch.from_numpy(workloads.cu_from_lens(cfg.lens_k)).to(dev)
             out = torch.empty_like(q)
+            v16 = None
+            if a.v16:
+                v16 = torch.empty(kc.shape, dtype=torch.float16, device=dev)
+                used = torch.from_numpy(np.unique(cfg.block_table[cfg.block_table >= 0]).astype(np.int64)).to(dev)
+                for i in range(0, used.numel(), 256):
+                    j = used[i:i + 256]
+                    v16[j] = (vc[j].float() / 16.0).half()
             for _ in range(a.iters):
-                av.store_kvcache(k_new, v_new, kc, vc, slots)
+                av.store_kvcache(k_new, v_new, kc, vc, slots, v16_cache=v16)
                 if a.op == "prefill":
                     av.attn_varlen_fwd(q, kc, vc, cu_q, cu_k, int(cfg.new.max()), int(cfg.lens_k.max()), cfg.scale,
-                                       block_table=bt, out=out)
+                                       block_table=bt, out=out, v16_cache=v16)
     st, word = av.get_last_device_error()
     print(f"{a.workload} {a.op} x{a.iters}: device status {st} word {word:#x}")
     return 0 if st == 0 else 1
