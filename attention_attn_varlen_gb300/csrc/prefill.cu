@@ -159,6 +159,7 @@ __device__ __forceinline__ bool seq_rows(const PrefillParams &p, int b, bool rep
 // ---------------------------------------------------------------------------
 constexpr int kCvtThreads = 256;
 constexpr int kCvtKeys = 32;
+constexpr int kCvtUnroll = 8;   // 16-byte chunks each thread keeps in flight
 
 __device__ __forceinline__ void v_to_f16_keys(const PrefillParams &p) {
     const int b = blockIdx.y;
@@ -181,30 +182,45 @@ __device__ __forceinline__ void v_to_f16_keys(const PrefillParams &p) {
     const int nkeys = min(kCvtKeys, Lk - key0);
     const int32_t *bt = p.block_table ? p.block_table + (int64_t)b * p.bt_stride : nullptr;
     uint32_t big = 0;
-    for (int idx = threadIdx.x; idx < nkeys * row_chunks; idx += kCvtThreads) {
-        const int kk = idx / row_chunks, ch = idx % row_chunks;
-        const int key = key0 + kk;
-        int64_t src_row;
-        if (bt) {
-            const int blk = __ldg(bt + key / p.block_size);
-            if (blk < 0 || (int64_t)blk >= p.num_blocks) {
-                record_error(p.err, ERR_INDEX | SRC_PREFILL);
-                *reinterpret_cast<uint4 *>(p.v16 + ((int64_t)k0 + key) * (row_chunks * 8) + ch * 8) =
-                    make_uint4(0u, 0u, 0u, 0u);
-                continue;
+    // kCvtUnroll chunks per thread in flight: all loads of a batch before its stores
+    const int total = nkeys * row_chunks;
+    for (int base = threadIdx.x; base < total; base += kCvtThreads * kCvtUnroll) {
+        uint4 v[kCvtUnroll];
+        int64_t dst[kCvtUnroll];   // chunk of V' (-1: none)
+#pragma unroll
+        for (int u = 0; u < kCvtUnroll; ++u) {
+            const int idx = base + u * kCvtThreads;
+            dst[u] = -1;
+            if (idx >= total) continue;
+            const int kk = idx / row_chunks, ch = idx % row_chunks;
+            const int key = key0 + kk;
+            dst[u] = ((int64_t)k0 + key) * row_chunks + ch;
+            int64_t src_row;
+            if (bt) {
+                const int blk = __ldg(bt + key / p.block_size);
+                if (blk < 0 || (int64_t)blk >= p.num_blocks) {
+                    record_error(p.err, ERR_INDEX | SRC_PREFILL);
+                    v[u] = make_uint4(0u, 0u, 0u, 0u);   // zeroed row
+                    continue;
+                }
+                src_row = (int64_t)blk * p.block_size + key % p.block_size;
+            } else {
+                src_row = (int64_t)k0 + key;
             }
-            src_row = (int64_t)blk * p.block_size + key % p.block_size;
-        } else {
-            src_row = (int64_t)k0 + key;
+            v[u] = ldg_stream16(p.v + src_row * p.v_row_stride + ch * 8);
         }
-        uint4 v = ldg_stream16(p.v + src_row * p.v_row_stride + ch * 8);
-        big = __vmaxu2(big, __vmaxu2(v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu));
-        big = __vmaxu2(big, __vmaxu2(v.z & 0x7FFF7FFFu, v.w & 0x7FFF7FFFu));
-        v.x = bf16x2_to_f16x2_div16(v.x);
-        v.y = bf16x2_to_f16x2_div16(v.y);
-        v.z = bf16x2_to_f16x2_div16(v.z);
-        v.w = bf16x2_to_f16x2_div16(v.w);
-        *reinterpret_cast<uint4 *>(p.v16 + ((int64_t)k0 + key) * (row_chunks * 8) + ch * 8) = v;
+#pragma unroll
+        for (int u = 0; u < kCvtUnroll; ++u) {
+            if (dst[u] < 0) continue;
+            uint4 w = v[u];
+            big = __vmaxu2(big, __vmaxu2(w.x & 0x7FFF7FFFu, w.y & 0x7FFF7FFFu));
+            big = __vmaxu2(big, __vmaxu2(w.z & 0x7FFF7FFFu, w.w & 0x7FFF7FFFu));
+            w.x = bf16x2_to_f16x2_div16(w.x);
+            w.y = bf16x2_to_f16x2_div16(w.y);
+            w.z = bf16x2_to_f16x2_div16(w.z);
+            w.w = bf16x2_to_f16x2_div16(w.w);
+            reinterpret_cast<uint4 *>(p.v16)[dst[u]] = w;
+        }
     }
     if (__any_sync(0xffffffffu, (big & 0xFFFFu) >= 0x4980u || (big >> 16) >= 0x4980u) && (threadIdx.x & 31) == 0)
         record_error(p.err, ERR_RANGE | SRC_PREFILL);

@@ -136,15 +136,19 @@ cudaError_t launch_store_kvcache(const void *k, const void *v, void *k_cache, vo
         const int64_t need = (chunks + (int64_t)kStoreThreads * kStoreUnroll - 1) / ((int64_t)kStoreThreads * kStoreUnroll);
         int64_t grid = (int64_t)num_sms * per_sm[dev];
         if (grid > need) grid = need;
+        main_kernel_event_before(stream);
         store_kvcache_kernel<<<(unsigned)grid, kStoreThreads, 0, stream>>>(
             (const uint4 *)k, (const uint4 *)v, (uint4 *)k_cache, (uint4 *)v_cache, (uint4 *)v16_cache, slot_mapping,
             num_tokens, row_elems / 8, k_stride / 8, v_stride / 8, num_slots, err);
+        main_kernel_event_after(stream);
     } else {
         int64_t grid = num_sms * 8;
         if (grid > num_tokens) grid = num_tokens;
+        main_kernel_event_before(stream);
         store_kvcache_kernel_b16<<<(unsigned)grid, kStoreThreads, 0, stream>>>(
             (const uint16_t *)k, (const uint16_t *)v, (uint16_t *)k_cache, (uint16_t *)v_cache, (__half *)v16_cache,
             slot_mapping, num_tokens, row_elems, k_stride, v_stride, num_slots, err);
+        main_kernel_event_after(stream);
     }
     return cudaGetLastError();
 }

@@ -171,7 +171,7 @@ KERNEL_SOURCES = {
     "decode": ["attention_attn_varlen_gb300/csrc/decode.cu", "attention_attn_varlen_gb300/csrc/common.cuh"],
     "decode_sq4": ["attention_attn_varlen_gb300/csrc/decode.cu", "attention_attn_varlen_gb300/csrc/common.cuh"],
     "decode_sq8": ["attention_attn_varlen_gb300/csrc/decode.cu", "attention_attn_varlen_gb300/csrc/common.cuh"],
-    "store": ["attention_attn_varlen_gb300/csrc/store_kvcache.cu"],
+    "store": ["attention_attn_varlen_gb300/csrc/store_kvcache.cu", "attention_attn_varlen_gb300/csrc/common.cuh"],
 }
 
 
@@ -420,14 +420,30 @@ def bench_prefix(av, device, steps, warmup, flush, peaks, with_oracle=True):
     ms = time_steps(step, steps, flush)
     ms_conv = time_steps(step_convert, steps, flush)
     ms_attn, kms_attn = time_steps(attn, steps, flush, kernel=True)
-    ms_store = time_steps(store, steps, flush)
+    ms_store, kms_store = time_steps(store, steps, flush, kernel=True)
     flops = workloads.prefill_flops(cfg.new, cfg.lens_k, cfg.Hq, cfg.D)
-    sbytes = workloads.store_bytes(int(cfg.new.sum()), cfg.Hkv, cfg.D)
+    sbytes = workloads.store_bytes(int(cfg.new.sum()), cfg.Hkv, cfg.D, v16=True)
     t = float(np.mean(ms)) / 1e3
     ta = float(np.mean(ms_attn)) / 1e3
     tk = float(np.mean(kms_attn)) / 1e3
     ts = float(np.mean(ms_store)) / 1e3
+    tks = float(np.mean(kms_store)) / 1e3
     tc = float(np.mean(ms_conv)) / 1e3
+    # the same scatter at 8x the tokens (random distinct slots of the pool), to
+    # separate the kernel's fixed cost from its bandwidth
+    n8 = 8 * int(cfg.new.sum())
+    kb8, vb8 = k_new.repeat(8, 1, 1), v_new.repeat(8, 1, 1)
+    sl8 = torch.from_numpy(np.random.default_rng(cfg.seed + 14).choice(cfg.num_blocks * cfg.block_size, n8,
+                                                                       replace=False).astype(np.int64)).to(device)
+
+    def store8():
+        av.store_kvcache(kb8, vb8, kc, vc, sl8, v16_cache=v16)
+    for _ in range(warmup):
+        store8()
+    ms_s8, kms_s8 = time_steps(store8, steps, flush, kernel=True)
+    sb8 = workloads.store_bytes(n8, cfg.Hkv, cfg.D, v16=True)
+    t8, tk8 = float(np.mean(ms_s8)) / 1e3, float(np.mean(kms_s8)) / 1e3
+    del kb8, vb8, sl8
     res = {"workload": "c3_prefix_paged: 32 seqs, context U{512..8192} + 1..512 new tokens, GQA 32/8, D128, "
                        "block_size 256, 65536-block pool, 8 seqs share prefix blocks; step = store_kvcache + "
                        "paged prefill, with the fp16 V/16 cache the store keeps",
@@ -438,9 +454,21 @@ def bench_prefix(av, device, steps, warmup, flush, peaks, with_oracle=True):
                         "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                         "frac": flops / tk / 1e12 / peaks["bf16_tflops"], "kernel_ms": tk * 1e3,
                         "traffic": ncu_traffic("prefill_paged", float(cfg.new.sum()))},
-           "store_kvcache": {"value": sbytes / ts / 1e9, "unit": "GB/s", "frac": sbytes / ts / 1e9 / peaks["hbm_gbs"],
-                             "tokens": int(cfg.new.sum()), "ms": ts * 1e3,
-                             "traffic": ncu_traffic("store", float(cfg.new.sum()))},
+           "store_kvcache": {"workload": "the step's 8503 new tokens: K, V and the fp16 V/16 row of each",
+                             "value": sbytes / ts / 1e9, "unit": "GB/s", "ms_per_step": ts * 1e3,
+                             "algorithmic_bytes": sbytes,
+                             "roofline": {"bound": "hbm", "kernel": "store_kvcache_kernel",
+                                          "achieved": sbytes / tks / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                                          "frac": sbytes / tks / 1e9 / peaks["hbm_gbs"], "kernel_ms": tks * 1e3,
+                                          "traffic": ncu_traffic("store", float(cfg.new.sum()))},
+                             "tokens": int(cfg.new.sum())},
+           "store_kvcache_8x": {"workload": f"{n8} tokens (the step's new tokens 8 times over) into random distinct "
+                                            "slots of the pool, K, V and V/16 rows",
+                                "value": sb8 / t8 / 1e9, "unit": "GB/s", "ms_per_step": t8 * 1e3,
+                                "algorithmic_bytes": sb8,
+                                "roofline": {"bound": "hbm", "kernel": "store_kvcache_kernel",
+                                             "achieved": sb8 / tk8 / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                                             "frac": sb8 / tk8 / 1e9 / peaks["hbm_gbs"], "kernel_ms": tk8 * 1e3}},
            "launches_per_step": 3}
     del kc, vc, v16
     torch.cuda.empty_cache()
@@ -703,8 +731,8 @@ def summary(line, peaks, peak_src):
     if c3:
         put("c3", c3, c3.get("oracle"), {"step_frac": _r(c3["value"] / peaks["bf16_tflops"], 3),
                                          "no_v16": _r(c3["without_v16_cache"]["value"])})
-        st = c3["store_kvcache"]
-        out["c3_store"] = {"value": _r(st["value"]), "unit": "GB/s", "frac": _r(st["frac"], 3), "ms": _r(st["ms"])}
+        put("c3_store", c3["store_kvcache"])
+        put("store_8x", c3.get("store_kvcache_8x"))
     c4 = line.get("decode")
     if c4:
         put("c4", c4, c4.get("oracle"))

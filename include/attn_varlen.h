@@ -400,10 +400,11 @@ ATTN_API int attn_abi_version(void);
  * benchmark can time the dominant kernel of a call by itself).  `before` and
  * `after` are the caller's cudaEvent_t handles (cast to void *); the library
  * neither creates nor destroys them.  While both are non-NULL, every later
- * attn_varlen_fwd, attn_decode_paged and attn_decode_paged_noalloc call made
- * from the same host thread records `before` on its stream just before
- * launching its main kernel (the attention kernel of the prefill; the
- * split-KV kernel of the decode) and `after` just after it, so
+ * attn_varlen_fwd, attn_decode_paged, attn_decode_paged_noalloc and
+ * store_kvcache call made from the same host thread records `before` on its
+ * stream just before launching its main kernel (the attention kernel of the
+ * prefill; the split-KV kernel of the decode; the scatter kernel of the store)
+ * and `after` just after it, so
  * cudaEventElapsedTime(before, after) is that kernel's device time.  The
  * scheduling and V-conversion kernels of the prefill and the combine kernel
  * of the decode fall outside.  Pass NULL, NULL to switch it off (the

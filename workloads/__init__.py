@@ -329,9 +329,10 @@ def decode_bytes(cache_seqlens, Hq: int, Hkv: int, D: int, block_size: int) -> i
     return kv + qo + bt + B * 4
 
 
-def store_bytes(num_tokens: int, Hkv: int, D: int) -> int:
-    """store_kvcache: read k and v rows, write them, read the int64 slots."""
-    return 2 * num_tokens * Hkv * D * 2 * 2 + 8 * num_tokens
+def store_bytes(num_tokens: int, Hkv: int, D: int, v16: bool = False) -> int:
+    """store_kvcache: read k and v rows, write them, read the int64 slots; with
+    the fp16 V / 16 cache, write a third row per token."""
+    return 2 * num_tokens * Hkv * D * 2 * 2 + 8 * num_tokens + (num_tokens * Hkv * D * 2 if v16 else 0)
 
 
 def sample_rows(seed: int, n_rows: int, fraction: float = 1 / 64, cap: int | None = None) -> np.ndarray:
