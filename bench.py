@@ -370,10 +370,11 @@ def bench_decode(av, device, steps, warmup, flush, peaks, with_oracle=True):
         import oracle
         oracle.build()
         sec, n = oracle_timed(lambda: oracle.decode_paged(qs, kp, vp, cfg.ctx[seqs], btc, cfg.Hq, cfg.Hkv, cfg.D,
-                                                          cfg.block_size, kp.shape[0], cfg.scale))
+                                                          cfg.block_size, kp.shape[0], cfg.scale), 1.0)
         ob = workloads.decode_bytes(cfg.ctx[seqs], cfg.Hq, cfg.Hkv, cfg.D, cfg.block_size)
         res["oracle"] = oracle_line(ob / sec / 1e9, "GB/s", f"48 of 256 sequences, all their query rows "
-                                    f"({int(cfg.ctx[seqs].sum())} cached tokens); float64, OpenMP", sec)
+                                    f"({int(cfg.ctx[seqs].sum())} cached tokens), mean of {n} calls; float64, "
+                                    f"OpenMP", sec)
     return res
 
 
@@ -495,11 +496,11 @@ def bench_prefix(av, device, steps, warmup, flush, peaks, with_oracle=True):
         rows = workloads.sample_rows(cfg.seed + 12, len(tok) * cfg.Hq, 1 / 16)
         sec, n = oracle_timed(lambda: oracle.attn_varlen(qs, kb, vb, cq, ckk, cfg.Hq, cfg.Hkv, cfg.D, cfg.scale, True,
                                                          block_table=btc, block_size=bs, num_blocks=kp.shape[0],
-                                                         rows=rows))
+                                                         rows=rows), 1.0)
         fl = rows_flops_lens(lq, lk, cfg.Hq, cfg.D, rows)
         res["oracle"] = oracle_line(fl / sec / 1e12, "TFLOP/s", f"{len(rows)} query rows (1/16) of 6 of the 32 "
-                                    f"sequences, paged through a compact pool; {fl / 1e9:.1f} GFLOP; float64, OpenMP",
-                                    sec)
+                                    f"sequences, paged through a compact pool; {fl / 1e9:.1f} GFLOP, mean of {n} "
+                                    f"calls; float64, OpenMP", sec)
     return res
 
 
@@ -611,11 +612,11 @@ def bench_contig(av, name, device, steps, warmup, flush, peaks, with_oracle=True
                 rows.append((int(cfg.cu_q[b]) + i) * cfg.Hq + h)
             rows = np.concatenate(rows).astype(np.int64)
             sec, n = oracle_timed(lambda: oracle.attn_varlen(qh, kh, vh, cfg.cu_q, cfg.cu_k, cfg.Hq, cfg.Hkv, cfg.D,
-                                                             cfg.scale, True, rows=rows))
+                                                             cfg.scale, True, rows=rows), 1.0)
             fl = rows_flops_lens(cfg.lens_q, cfg.lens_k, cfg.Hq, cfg.D, rows)
             res["oracle"] = oracle_line(fl / sec / 1e12, "TFLOP/s", f"{len(rows)} query rows: 256 of each of 4 "
-                                        f"(sequence, head) pairs, two with logits ~700; {fl / 1e9:.1f} GFLOP; "
-                                        f"float64, OpenMP", sec)
+                                        f"(sequence, head) pairs, two with logits ~700; {fl / 1e9:.1f} GFLOP, mean "
+                                        f"of {n} calls; float64, OpenMP", sec)
     return res
 
 
