@@ -176,6 +176,7 @@ struct DecodeCall {
     int max_len, causal, num_splits;
     float scale;
     int64_t q_row_stride, out_row_stride, lse_row_stride, lse_head_stride;
+    const void *v16_cache;   // null, or the fp16 V / 16 cache read instead of v_cache
 };
 
 // Host checks shared by the decode-kernel entries (strides already resolved).
@@ -192,6 +193,7 @@ attn_status decode_check(const DecodeCall &c) {
     if ((int64_t)c.batch * c.seqlen_q * c.Hq >= (int64_t)INT32_MAX) return ATTN_ERR_UNSUPPORTED;
     if (!aligned16(c.q) || !aligned16(c.k_cache) || !aligned16(c.v_cache) || !aligned16(c.out))
         return ATTN_ERR_INVALID_ARG;
+    if (c.v16_cache && !aligned16(c.v16_cache)) return ATTN_ERR_INVALID_ARG;
     return ATTN_OK;
 }
 
@@ -211,8 +213,10 @@ attn_status decode_launch(const DecodeCall &c, const DevInfo *d, int splits, int
     const int64_t row_stride = (int64_t)c.Hkv * c.head_dim;
     CUtensorMap kmap, vmap;
     if (!make_map(&kmap, c.k_cache, rows, c.Hkv, c.head_dim, row_stride, 1, rpb) ||
-        !make_map(&vmap, c.v_cache, rows, c.Hkv, c.head_dim, row_stride, 1, rpb))
+        !make_map(&vmap, c.v16_cache ? c.v16_cache : c.v_cache, rows, c.Hkv, c.head_dim, row_stride, 1, rpb,
+                  c.v16_cache ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16))
         return ATTN_ERR_LAUNCH_FAILED;
+    p.v16 = c.v16_cache ? 1 : 0;
     p.q = reinterpret_cast<const __nv_bfloat16 *>(c.q);
     p.out = reinterpret_cast<__nv_bfloat16 *>(c.out);
     p.lse = c.lse;
@@ -684,7 +688,7 @@ attn_status attn_kvcache_fwd(const void *q, const void *k_cache, const void *v_c
         DecodeCall c = {q, k_cache, v_cache, out, lse, cache_seqlens, block_table, block_table_stride, batch,
                         seqlen_q, num_heads_q, num_heads_kv, head_dim, block_size, num_blocks, max_cache_seqlen,
                         causal, 0, softmax_scale, (int64_t)num_heads_q * head_dim, (int64_t)num_heads_q * head_dim,
-                        1, (int64_t)batch * seqlen_q};
+                        1, (int64_t)batch * seqlen_q, v16_cache};
         if ((st = decode_check(c)) != ATTN_OK) return st;
         int splits = 1, split_tok = 0;
         decode_plan(d->num_sms, batch, num_heads_kv, max_cache_seqlen, 0, &splits, &split_tok);

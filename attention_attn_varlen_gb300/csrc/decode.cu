@@ -53,7 +53,9 @@ struct DecSmem {
 };
 
 
-template <int D, int NT>
+// VH: V tiles come from the fp16 V / 16 cache; PV then multiplies them by one fp16
+// term P' = 16 P (11 significant bits) instead of P's bf16 hi + lo terms.
+template <int D, int NT, bool VH>
 __global__ void __launch_bounds__(kDecThreads) attn_decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
                                                                        const __grid_constant__ CUtensorMap vmap,
                                                                        const DecodeParams p) {
@@ -267,14 +269,20 @@ __global__ void __launch_bounds__(kDecThreads) attn_decode_split_kernel(const __
                     o[nt][i][3] *= a_1;
                 }
                 // P^T into the B layout: rows = tokens, cols = query columns -> transpose.
-                // P is carried as bf16 hi + lo terms (about 16 significant bits).
-                const uint32_t h01 = pack_bf16x2(p0, p1), h23 = pack_bf16x2(p2, p3);
-                bp[nt][0] = movmatrix_t(h01);
-                bp[nt][1] = movmatrix_t(h23);
-                bl[nt][0] = movmatrix_t(
-                    pack_bf16x2(p0 - __uint_as_float(h01 << 16), p1 - __uint_as_float(h01 & 0xFFFF0000u)));
-                bl[nt][1] = movmatrix_t(
-                    pack_bf16x2(p2 - __uint_as_float(h23 << 16), p3 - __uint_as_float(h23 & 0xFFFF0000u)));
+                if constexpr (VH) {
+                    // P' = 16 P as fp16 against V' = V / 16: the product is P V
+                    bp[nt][0] = movmatrix_t(pack_f16x2(16.f * p0, 16.f * p1));
+                    bp[nt][1] = movmatrix_t(pack_f16x2(16.f * p2, 16.f * p3));
+                } else {
+                    // P is carried as bf16 hi + lo terms (about 16 significant bits)
+                    const uint32_t h01 = pack_bf16x2(p0, p1), h23 = pack_bf16x2(p2, p3);
+                    bp[nt][0] = movmatrix_t(h01);
+                    bp[nt][1] = movmatrix_t(h23);
+                    bl[nt][0] = movmatrix_t(
+                        pack_bf16x2(p0 - __uint_as_float(h01 << 16), p1 - __uint_as_float(h01 & 0xFFFF0000u)));
+                    bl[nt][1] = movmatrix_t(
+                        pack_bf16x2(p2 - __uint_as_float(h23 << 16), p3 - __uint_as_float(h23 & 0xFFFF0000u)));
+                }
             }
             // O^T[D x 8] += V^T[D x 16 tokens] * P^T[16 x 8], per n-tile
             const int mi = lane >> 3;
@@ -286,8 +294,12 @@ __global__ void __launch_bounds__(kDecThreads) attn_decode_split_kernel(const __
                 ldsm_x4_t(vb + (ch / 8) * S::kPanelBytes + sw128_off(vrow, ch % 8), a0, a1, a2, a3);
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) {
-                    mma_bf16_16816(o[nt][mt], a0, a1, a2, a3, bp[nt][0], bp[nt][1]);
-                    mma_bf16_16816(o[nt][mt], a0, a1, a2, a3, bl[nt][0], bl[nt][1]);
+                    if constexpr (VH) {
+                        mma_f16_16816(o[nt][mt], a0, a1, a2, a3, bp[nt][0], bp[nt][1]);
+                    } else {
+                        mma_bf16_16816(o[nt][mt], a0, a1, a2, a3, bp[nt][0], bp[nt][1]);
+                        mma_bf16_16816(o[nt][mt], a0, a1, a2, a3, bl[nt][0], bl[nt][1]);
+                    }
                 }
             }
             if (tail) fence_proxy_async_smem();
@@ -435,7 +447,7 @@ __global__ void __launch_bounds__(128) attn_decode_combine_kernel(const DecodePa
             Ls > 0.f ? (M + __log2f(Ls)) * 0.69314718055994531f : -INFINITY;
 }
 
-template <int D, int NT>
+template <int D, int NT, bool VH>
 static cudaError_t launch_decode_t(const CUtensorMap &kmap, const CUtensorMap &vmap, const DecodeParams &p,
                                    int batch, cudaStream_t stream) {
     using S = DecSmem<D>;
@@ -446,13 +458,13 @@ static cudaError_t launch_decode_t(const CUtensorMap &kmap, const CUtensorMap &v
     if (e0 != cudaSuccess) return e0;
     if (dev < 0 || dev >= kMaxDev) return cudaErrorInvalidDevice;
     std::call_once(attr_once[dev], [&] {
-        attr_err[dev] = cudaFuncSetAttribute(attn_decode_split_kernel<D, NT>,
+        attr_err[dev] = cudaFuncSetAttribute(attn_decode_split_kernel<D, NT, VH>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, S::kBytes);
     });
     if (attr_err[dev] != cudaSuccess) return attr_err[dev];
     dim3 grid(p.num_splits * p.ncg, p.Hkv, batch);
     main_kernel_event_before(stream);
-    attn_decode_split_kernel<D, NT><<<grid, kDecThreads, S::kBytes, stream>>>(kmap, vmap, p);
+    attn_decode_split_kernel<D, NT, VH><<<grid, kDecThreads, S::kBytes, stream>>>(kmap, vmap, p);
     main_kernel_event_after(stream);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess || p.num_splits == 1) return e;
@@ -464,11 +476,18 @@ static cudaError_t launch_decode_t(const CUtensorMap &kmap, const CUtensorMap &v
 cudaError_t launch_decode(const CUtensorMap &kmap, const CUtensorMap &vmap, const DecodeParams &p, int batch,
                           int head_dim, cudaStream_t stream) {
     const bool two = p.Sq * p.G > 8;
+    if (p.v16) {
+        if (head_dim == 128)
+            return two ? launch_decode_t<128, 2, true>(kmap, vmap, p, batch, stream)
+                       : launch_decode_t<128, 1, true>(kmap, vmap, p, batch, stream);
+        return two ? launch_decode_t<64, 2, true>(kmap, vmap, p, batch, stream)
+                   : launch_decode_t<64, 1, true>(kmap, vmap, p, batch, stream);
+    }
     if (head_dim == 128)
-        return two ? launch_decode_t<128, 2>(kmap, vmap, p, batch, stream)
-                   : launch_decode_t<128, 1>(kmap, vmap, p, batch, stream);
-    return two ? launch_decode_t<64, 2>(kmap, vmap, p, batch, stream)
-               : launch_decode_t<64, 1>(kmap, vmap, p, batch, stream);
+        return two ? launch_decode_t<128, 2, false>(kmap, vmap, p, batch, stream)
+                   : launch_decode_t<128, 1, false>(kmap, vmap, p, batch, stream);
+    return two ? launch_decode_t<64, 2, false>(kmap, vmap, p, batch, stream)
+               : launch_decode_t<64, 1, false>(kmap, vmap, p, batch, stream);
 }
 
 }  // namespace attn

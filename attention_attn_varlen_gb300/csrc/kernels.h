@@ -31,6 +31,7 @@ struct DecodeParams {
     int ncg;                     // column groups: CTAs per (split, KV head, sequence), 16 columns each
     int causal;                  // bottom-right: token t sees keys j <= L - Sq + t
     int max_seqlen;              // cache_seqlens outside [0, max_seqlen] are clamped and reported
+    int v16;                     // 1: V tiles are the fp16 V / 16 cache (PV on one fp16 term P' = 16 P)
     float scale_log2;            // softmax_scale * log2(e)
     uint32_t *err;
 };

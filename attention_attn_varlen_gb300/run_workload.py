@@ -13,8 +13,8 @@ with the device error status.  No timing, no comparison.
   --op softmax  attn_softmax_rows on a seeded [--rows, --cols] matrix (--dtype f32 | bf16;
                 --workload is ignored)
   --seqs N      keep only the first N sequences (smaller captures)
-  --v16         paged prefill / store: keep the fp16 V / 16 cache beside the bf16
-                one (filled for the blocks in use, then by the store)
+  --v16         paged prefill / store / kvcache: keep the fp16 V / 16 cache beside
+                the bf16 one (filled for the blocks in use, then by the store)
   --compact-pool  paged workloads: a pool of just the blocks the block table
                 uses, ids randomly permuted (same block size, lengths and
                 shared-prefix blocks; for profiler captures of a few GB at most)
@@ -116,8 +116,14 @@ def main(argv=None):
             g = torch.Generator(device=dev).manual_seed(4321)
             qn = torch.randn(cfg.batch, a.sq, cfg.Hq, cfg.D, device=dev, generator=g).to(torch.bfloat16)
             out = torch.empty_like(qn)
+            v16 = None
+            if a.v16:
+                v16 = torch.empty(kc.shape, dtype=torch.float16, device=dev)
+                for i in range(0, cfg.num_blocks, 256):
+                    v16[i:i + 256] = (vc[i:i + 256].float() / 16.0).half()
             for _ in range(a.iters):
-                av.attn_with_kvcache(qn, kc, vc, cs, bt, cfg.scale, max_cache_seqlen=int(cfg.ctx.max()), out=out)
+                av.attn_with_kvcache(qn, kc, vc, cs, bt, cfg.scale, max_cache_seqlen=int(cfg.ctx.max()), out=out,
+                                     v16_cache=v16)
         else:
             k_new, v_new = cfg.k_new().to(dev), cfg.v_new().to(dev)
             slots = torch.from_numpy(cfg.slot_mapping()).to(dev)

@@ -333,6 +333,11 @@ def bench_decode(av, device, steps, warmup, flush, peaks, with_oracle=True):
     # the same cache, Sq new query tokens per sequence (multi-token decode through
     # attn_with_kvcache; the last Sq cached tokens are the new ones)
     g = torch.Generator(device=device).manual_seed(4321)
+    # the fp16 V / 16 cache the store would keep beside the bf16 one (here converted once,
+    # outside the timing); the multi-token lines are also measured reading it
+    v16 = torch.empty(kc.shape, dtype=torch.float16, device=device)
+    for i in range(0, cfg.num_blocks, 256):
+        v16[i:i + 256] = (vc[i:i + 256].float() / 16.0).half()
     for Sq in (4, 8):
         qn = torch.randn(cfg.batch, Sq, cfg.Hq, cfg.D, device=device, generator=g).to(torch.bfloat16)
         wsn = torch.empty(av.lib().attn_kvcache_workspace_size(cfg.batch, Sq, cfg.Hq, cfg.Hkv, cfg.D, mx),
@@ -359,8 +364,24 @@ def bench_decode(av, device, steps, warmup, flush, peaks, with_oracle=True):
                          "kernel_ms": tkn * 1e3,
                          "traffic": ncu_traffic(f"decode_sq{Sq}", float(cfg.ctx.sum()) * cfg.Hkv)},
             "launches_per_step": 2 if splits > 1 else 1}
+
+        def stepv():
+            av.attn_with_kvcache(qn, kc, vc, cs, bt, cfg.scale, max_cache_seqlen=mx, out=outn, workspace=wsn,
+                                 v16_cache=v16)
+        for _ in range(warmup):
+            stepv()
+        torch.cuda.synchronize()
+        msv, kmsv = time_steps(stepv, steps, flush, kernel=True)
+        tv, tkv = float(np.mean(msv)) / 1e3, float(np.mean(kmsv)) / 1e3
+        res[f"kvcache_{Sq}_tokens_v16"] = {
+            "workload": f"the same {Sq}-token step reading the fp16 V/16 cache (PV on one fp16 term 16 P)",
+            "value": nbn / tv / 1e9, "unit": "GB/s", "ms_per_step": tv * 1e3, "algorithmic_bytes": nbn,
+            "roofline": {"bound": "hbm", "kernel": "attn_decode_split_kernel", "achieved": nbn / tkv / 1e9,
+                         "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": nbn / tkv / 1e9 / peaks["hbm_gbs"],
+                         "kernel_ms": tkv * 1e3, "traffic": None},
+            "launches_per_step": 2 if splits > 1 else 1}
         del qn, wsn, outn
-    del kc, vc
+    del kc, vc, v16
     torch.cuda.empty_cache()
     if with_oracle:
         # the oracle on 48 of the 256 sequences, every query row
@@ -739,6 +760,8 @@ def summary(line, peaks, peak_src):
         put("c4", c4, c4.get("oracle"))
         put("c4_sq4", c4.get("kvcache_4_tokens"))
         put("c4_sq8", c4.get("kvcache_8_tokens"))
+        put("c4_sq4_v16", c4.get("kvcache_4_tokens_v16"))
+        put("c4_sq8_v16", c4.get("kvcache_8_tokens_v16"))
     c5 = line.get("long_prefill")
     if c5:
         put("c5", c5, c5.get("oracle"), {"step_frac": _r(c5["value"] / peaks["bf16_tflops"], 3)})

@@ -336,9 +336,11 @@ ATTN_API size_t attn_padded_workspace_size(int batch, int seqlen_q, int seqlen_k
  *   causal       bottom-right: new token i sees keys j <= cache_seqlens[b] -
  *                seqlen_q + i; 0 = every cached key
  *   block_table, block_size, num_blocks: as for attn_varlen_fwd (paged mode)
- *   v16_cache    nullable: the fp16 V / 16 cache kept by store_kvcache; the
- *                prefill route then reads it instead of converting V (the
- *                decode route reads the bf16 v_cache either way)
+ *   v16_cache    nullable: the fp16 V / 16 cache kept by store_kvcache.  Both
+ *                routes then read V / 16 from it instead of V: the prefill route
+ *                converts nothing, and the decode route multiplies it by one fp16
+ *                term 16 P (11 significant bits) instead of P's two bf16 terms,
+ *                half the P V work
  *   workspace    at least attn_kvcache_workspace_size(...) bytes, 256-byte
  *                aligned.  On the decode route it holds the split partials
  *                (at most 64 splits of fp32 rows); on the prefill route without

@@ -33,6 +33,25 @@ CASES = [
 ]
 
 
+@pytest.mark.parametrize("seed,ctx,Sq,Hq,Hkv,D,bs", CASES)
+def test_kvcache_with_v16_cache_matches_oracle(seed, ctx, Sq, Hq, Hkv, D, bs):
+    """The same calls reading the fp16 V / 16 cache (NaN past every sequence's end):
+    the decode route multiplies it by fp16 16 P, the prefill route skips its
+    conversion; both against the oracle."""
+    cfg = workloads.small_paged(seed, ctx=ctx, new=[Sq] * len(ctx), Hq=Hq, Hkv=Hkv, D=D, block_size=bs)
+    q = cfg.q()
+    av.get_last_device_error()
+    kc, vc, k_new, v_new = _paged_device(cfg)
+    cs, bt = _as_kvcache_args(cfg, kc, vc)
+    out, lse = av.attn_with_kvcache(q.cuda().view(cfg.batch, Sq, Hq, D), kc, vc, cs, bt, cfg.scale,
+                                    return_lse=True, v16_cache=v16_of(vc))
+    torch.cuda.synchronize()
+    assert av.get_last_device_error()[0] == 0
+    ref, ref_lse, _ = _paged_oracle(cfg, q, k_new, v_new, list(range(cfg.batch)))
+    assert_close(out.view(-1, Hq, D), ref.reshape(-1, Hq, D), f"kvcache v16 Sq={Sq}")
+    assert_lse_close(lse.t().contiguous(), ref_lse.reshape(-1, Hq), "kvcache v16 lse")
+
+
 def _as_kvcache_args(cfg, kc, vc):
     cs = torch.from_numpy(cfg.lens_k.astype(np.int32)).cuda()
     bt = torch.from_numpy(cfg.block_table).cuda()
@@ -187,4 +206,41 @@ def test_kvcache_c4_four_tokens_full_size_sampled():
     got_lse = lse.view(cfg.Hq, cfg.batch, Sq)[:, seqs].reshape(cfg.Hq, -1).t().contiguous()
     assert_lse_close(got_lse, ref_lse.reshape(-1, cfg.Hq), "c4 cache, 4 new tokens, lse")
     del kc, vc
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.slow
+def test_kvcache_c4_eight_tokens_v16_full_size_sampled():
+    """The 8-token kv-cache step at full size with the fp16 V / 16 cache (32 query
+    columns per KV head, two column groups), as the benchmark times it; the
+    oracle checks 12 sequences."""
+    from test_gpu_decode import poison_tail
+    cfg = workloads.make("c4_decode")
+    Sq = 8
+    kc = torch.empty((cfg.num_blocks, cfg.block_size, cfg.Hkv, cfg.D), dtype=torch.bfloat16, device="cuda")
+    vc = torch.empty_like(kc)
+    workloads.fill_paged_cache(cfg, kc, vc)
+    poison_tail(cfg, kc, vc)
+    v16 = v16_of(vc)
+    rng = np.random.default_rng(8642)
+    q8 = torch.from_numpy(rng.standard_normal((cfg.batch, Sq, cfg.Hq, cfg.D), dtype=np.float32)).to(torch.bfloat16)
+    cs = torch.from_numpy(cfg.ctx.astype(np.int32)).cuda()
+    bt = torch.from_numpy(cfg.block_table).cuda()
+    av.get_last_device_error()
+    out, lse = av.attn_with_kvcache(q8.cuda(), kc, vc, cs, bt, cfg.scale, max_cache_seqlen=int(cfg.ctx.max()),
+                                    return_lse=True, v16_cache=v16)
+    torch.cuda.synchronize()
+    assert av.get_last_device_error()[0] == 0
+    seqs = sorted(np.random.default_rng(46).choice(cfg.batch, 10, replace=False).tolist())
+    seqs = sorted(set(seqs) | {int(np.argmax(cfg.ctx)), int(np.argmin(cfg.ctx))})
+    kp, vp, btc = workloads.compact_paged(cfg, seqs)
+    cu_q = workloads.cu_from_lens(np.full(len(seqs), Sq, dtype=np.int64))
+    cu_k = workloads.cu_from_lens(cfg.ctx[seqs])
+    ref, ref_lse = oracle.attn_varlen(q8[seqs].reshape(-1, cfg.Hq, cfg.D), kp, vp, cu_q, cu_k, cfg.Hq, cfg.Hkv,
+                                      cfg.D, cfg.scale, True, block_table=btc, block_size=cfg.block_size,
+                                      num_blocks=kp.shape[0])
+    assert_close(out[seqs].reshape(-1, cfg.Hq, cfg.D), ref.reshape(-1, cfg.Hq, cfg.D), "c4 cache, 8 new tokens, v16")
+    got_lse = lse.view(cfg.Hq, cfg.batch, Sq)[:, seqs].reshape(cfg.Hq, -1).t().contiguous()
+    assert_lse_close(got_lse, ref_lse.reshape(-1, cfg.Hq), "c4 cache, 8 new tokens, v16, lse")
+    del kc, vc, v16
     torch.cuda.empty_cache()
