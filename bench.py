@@ -171,6 +171,7 @@ KERNEL_SOURCES = {
     "decode": ["attention_attn_varlen_gb300/csrc/decode.cu", "attention_attn_varlen_gb300/csrc/common.cuh"],
     "decode_sq4": ["attention_attn_varlen_gb300/csrc/decode.cu", "attention_attn_varlen_gb300/csrc/common.cuh"],
     "decode_sq8": ["attention_attn_varlen_gb300/csrc/decode.cu", "attention_attn_varlen_gb300/csrc/common.cuh"],
+    "decode_sq8_v16": ["attention_attn_varlen_gb300/csrc/decode.cu", "attention_attn_varlen_gb300/csrc/common.cuh"],
     "store": ["attention_attn_varlen_gb300/csrc/store_kvcache.cu", "attention_attn_varlen_gb300/csrc/common.cuh"],
 }
 
@@ -378,7 +379,8 @@ def bench_decode(av, device, steps, warmup, flush, peaks, with_oracle=True):
             "value": nbn / tv / 1e9, "unit": "GB/s", "ms_per_step": tv * 1e3, "algorithmic_bytes": nbn,
             "roofline": {"bound": "hbm", "kernel": "attn_decode_split_kernel", "achieved": nbn / tkv / 1e9,
                          "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": nbn / tkv / 1e9 / peaks["hbm_gbs"],
-                         "kernel_ms": tkv * 1e3, "traffic": None},
+                         "kernel_ms": tkv * 1e3,
+                         "traffic": ncu_traffic("decode_sq8_v16", float(cfg.ctx.sum()) * cfg.Hkv) if Sq == 8 else None},
             "launches_per_step": 2 if splits > 1 else 1}
         del qn, wsn, outn
     del kc, vc, v16
