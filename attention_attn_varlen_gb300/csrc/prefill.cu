@@ -162,7 +162,7 @@ constexpr int kCvtKeys = 32;
 constexpr int kCvtUnroll = 8;   // 16-byte chunks each thread keeps in flight
 
 __device__ __forceinline__ void v_to_f16_keys(const PrefillParams &p) {
-    const int b = blockIdx.y;
+    const int b = blockIdx.y - 1;   // row 0 of the grid is the scheduler's
     int qs, Lq, k0, Lk;
     if (!seq_rows(p, b, false, qs, Lq, k0, Lk)) return;   // reported by the scheduler
     const int key0 = blockIdx.x * kCvtKeys;
@@ -239,6 +239,7 @@ __device__ __forceinline__ void v_to_f16_keys(const PrefillParams &p) {
 constexpr int kSchedThreads = kCvtThreads;   // the scheduler is one CTA of the pre-pass kernel
 constexpr int kSchedBuckets = 4096;
 constexpr int kSchedWarps = kSchedThreads / 32;
+constexpr int kSchedWarpBatch = 1024;   // up to this many sequences, a warp writes each one's units
 
 __device__ __forceinline__ int pf_pairs(const PrefillParams &p, int b, bool report) {
     const int tps = BM / p.G;
@@ -301,24 +302,40 @@ __device__ __forceinline__ void schedule_units(const PrefillParams &p) {
         p.unit_count[1] = 0;   // the attention kernel's next-unit counter
     }
     __syncthreads();
-    for (int b = threadIdx.x; b < p.batch; b += kSchedThreads) {
-        const int pairs = pf_pairs(p, b, false);
-        if (!pairs) continue;
-        int off = atomicAdd(&units_in[min(pairs, kSchedBuckets - 1)], pairs * p.Hkv);
-        for (int h = 0; h < p.Hkv; ++h)
-            for (int i = 0; i < pairs; ++i) p.units[off++] = make_int2(b, (pairs - 1 - i) | (h << 16));
+    if (p.batch <= kSchedWarpBatch) {
+        // few sequences (each with many units): a warp writes each sequence's entries
+        for (int b = wid; b < p.batch; b += kSchedWarps) {
+            const int pairs = pf_pairs(p, b, false);
+            if (!pairs) continue;
+            int off = 0;
+            if (lane == 0) off = atomicAdd(&units_in[min(pairs, kSchedBuckets - 1)], pairs * p.Hkv);
+            off = __shfl_sync(0xffffffffu, off, 0);
+            for (int e = lane; e < pairs * p.Hkv; e += 32) {
+                const int h = e / pairs, i = e % pairs;
+                p.units[off + e] = make_int2(b, (pairs - 1 - i) | (h << 16));
+            }
+        }
+    } else {
+        for (int b = threadIdx.x; b < p.batch; b += kSchedThreads) {
+            const int pairs = pf_pairs(p, b, false);
+            if (!pairs) continue;
+            int off = atomicAdd(&units_in[min(pairs, kSchedBuckets - 1)], pairs * p.Hkv);
+            for (int h = 0; h < p.Hkv; ++h)
+                for (int i = 0; i < pairs; ++i) p.units[off++] = make_int2(b, (pairs - 1 - i) | (h << 16));
+        }
     }
 }
 
 // ---------------------------------------------------------------------------
-// Pre-pass before the attention kernel, one launch: CTA (0, batch) writes the
-// unit list (schedule_units); CTAs (x, b) with b < batch convert V of
-// sequence b to V' (v_to_f16_keys).  With a paged V' cache (v16_paged) the
-// launch is the scheduler's CTA alone.
+// Pre-pass before the attention kernel, one launch: CTA (0, 0) writes the unit
+// list (schedule_units); CTAs (x, b + 1) convert V of sequence b to V'
+// (v_to_f16_keys).  With a paged V' cache (v16_paged) the launch is the
+// scheduler's CTA alone.
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(kCvtThreads) attn_prefill_prep_kernel(const PrefillParams p) {
-    if (p.v16_paged || blockIdx.y == (unsigned)p.batch) {
-        // with a paged V' cache there is nothing to convert: one CTA, the scheduler
+    if (p.v16_paged || blockIdx.y == 0) {
+        // the scheduler (grid row 0, dispatched first); with a paged V' cache there is
+        // nothing to convert and the launch is this one CTA
         if (blockIdx.x == 0) schedule_units(p);
         return;
     }
@@ -979,8 +996,8 @@ static cudaError_t launch_prefill_t(const CUtensorMap &qmap, const CUtensorMap &
             cudaFuncSetAttribute(attn_prefill_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kBytes);
     });
     if (attr_err[dev] != cudaSuccess) return attr_err[dev];
-    // unit list and V' in one launch: one extra row of CTAs (y = batch) holds the
-    // scheduler; with a paged V' cache the scheduler alone
+    // unit list and V' in one launch: grid row 0 holds the scheduler (dispatched
+    // before the conversion CTAs); with a paged V' cache the scheduler alone
     const dim3 cgrid = p.v16_paged ? dim3(1, 1) : dim3((p.max_seqlen_k + kCvtKeys - 1) / kCvtKeys, p.batch + 1);
     attn_prefill_prep_kernel<<<cgrid, kCvtThreads, 0, stream>>>(p);
     cudaError_t e = cudaGetLastError();
