@@ -724,7 +724,7 @@ attn_status attn_softmax_rows(const void *x, void *y, int64_t rows, int cols, in
     if ((st = check_arch(d)) != ATTN_OK) return st;
     if (rows == 0 || cols == 0) return ATTN_OK;
     if (launch_softmax_rows(x, y, rows, cols, x_row_stride, y_row_stride, dtype == ATTN_DTYPE_BF16 ? 1 : 0,
-                            d->num_sms, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) {
+                            d->num_sms, d->err, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) {
         cudaGetLastError();
         return ATTN_ERR_LAUNCH_FAILED;
     }

@@ -81,7 +81,7 @@ void main_kernel_event_before(cudaStream_t stream);
 void main_kernel_event_after(cudaStream_t stream);
 
 cudaError_t launch_softmax_rows(const void *x, void *y, int64_t rows, int cols, int64_t x_row_stride,
-                                int64_t y_row_stride, int bf16, int sms, cudaStream_t stream);
+                                int64_t y_row_stride, int bf16, int sms, uint32_t *err, cudaStream_t stream);
 
 cudaError_t launch_padded_cu(int batch, int seqlen_q, int seqlen_k, int32_t *cu_q, int32_t *cu_k,
                              cudaStream_t stream);

@@ -7,9 +7,18 @@
 // elements.  Partial (m, d') states of threads merge exactly:
 //   m = max(m1, m2),  d' = d1 e^(m1 - m) + d2 e^(m2 - m).
 //
-// HBM-bound.  Rows of up to 1024 fp32 / 2048 bf16 elements: one warp per row,
-// the row held in registers (one read, one write).  Longer rows: one CTA per row; pass 2
-// re-reads the row, which the CTAs in flight keep in L2.
+// HBM-bound; every path below reads the matrix once and writes it once except
+// the last.  Rows of up to 1024 fp32 / 2048 bf16 elements: one warp per row,
+// the row held in registers.  Up to 16 KB: one CTA per row, rows streamed into a
+// shared-memory ring by bulk copies.  Up to 64 KB: one CTA per row, the row held
+// in registers across the CTA's threads; up to 512 KB: a thread-block cluster
+// per row, each CTA holding a slice and the CTAs' (m, d') pairs exchanged
+// through distributed shared memory.  Longer rows (or rows that are not 16-byte
+// aligned): one CTA per row, pass 2 re-reads the row, which the CTAs in flight
+// keep in L2.
+#include <mutex>
+#include <unordered_map>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -39,6 +48,14 @@ struct Vec<float> {
     }
     __device__ static float one(const float *p) { return *p; }
     __device__ static void put(float *p, float f) { *p = f; }
+    // the first `valid` (< 4) elements at p as raw bits; the rest are left 0
+    __device__ static uint4 bits_partial(const float *p, int valid) {
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (valid > 0) v.x = __float_as_uint(p[0]);
+        if (valid > 1) v.y = __float_as_uint(p[1]);
+        if (valid > 2) v.z = __float_as_uint(p[2]);
+        return v;
+    }
 };
 
 template <>
@@ -65,6 +82,15 @@ struct Vec<__nv_bfloat16> {
     }
     __device__ static float one(const __nv_bfloat16 *p) { return __bfloat162float(*p); }
     __device__ static void put(__nv_bfloat16 *p, float f) { *p = __float2bfloat16_rn(f); }
+    // the first `valid` (< 8) elements at p as raw bits; the rest are left 0
+    __device__ static uint4 bits_partial(const __nv_bfloat16 *p, int valid) {
+        const unsigned short *h = reinterpret_cast<const unsigned short *>(p);
+        uint32_t w[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+        for (int e = 0; e < 7; ++e)
+            if (e < valid) w[e >> 1] |= (uint32_t)h[e] << ((e & 1) * 16);
+        return make_uint4(w[0], w[1], w[2], w[3]);
+    }
 };
 
 // running state of the online recurrence (m in log2 units, d')
@@ -189,6 +215,239 @@ __global__ void __launch_bounds__(256) softmax_rows_warp_kernel(const T *x, T *y
 }
 
 // ---------------------------------------------------------------------------
+// one CTA per row, rows streamed through shared memory: thread 0 keeps the
+// next `stages` rows of the CTA in flight with bulk copies (one per row, its
+// whole 16-byte vectors; the few elements past the last one are read
+// directly), so the bytes in flight are bounded by shared memory, not by
+// registers.  Pass 1 (online m, d') and pass 2 both read the row from shared
+// memory; a stage is refilled once every thread has passed the row's last
+// barrier.  Every mbarrier wait is bounded: on a timeout the kernel records it
+// in the error word, lets its copies in flight land (again bounded) and stops.
+// ---------------------------------------------------------------------------
+constexpr int kSmemMaxStages = 8;
+constexpr int kSmemThreads = 128;
+
+template <typename T, int NT>
+__global__ void __launch_bounds__(NT) softmax_rows_smem_kernel(const T *x, T *y, int64_t rows, int cols,
+                                                               int64_t xs, int64_t ys, int stages, uint32_t slot,
+                                                               uint32_t *err) {
+    constexpr int N = Vec<T>::N;
+    constexpr int NWARP = NT / 32;
+    extern __shared__ __align__(128) uint8_t stage_mem[];
+    __shared__ uint64_t full[kSmemMaxStages];
+    __shared__ float sm_m[2][NWARP], sm_d[2][NWARP];
+    __shared__ int abort_flag;
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    const int nwhole = cols / N;                        // 16-byte vectors in the bulk copy
+    const int nvec = (cols + N - 1) / N;
+    const uint32_t bulk = (uint32_t)nwhole * 16u;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < stages; ++s) mbar_init(&full[s], 1);
+        abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    auto issue = [&](int s, int64_t row) {
+        mbar_arrive_expect_tx(&full[s], bulk);
+        bulk_load(stage_mem + (size_t)s * slot, x + row * xs, bulk, &full[s]);
+    };
+    if (threadIdx.x == 0)
+        for (int s = 0; s < stages; ++s) {
+            const int64_t row = blockIdx.x + (int64_t)s * gridDim.x;
+            if (row < rows) issue(s, row);
+        }
+    int64_t it = 0;
+    bool ok = true;
+    for (int64_t r = blockIdx.x; r < rows; r += gridDim.x, ++it) {
+        const int s = (int)(it % stages);
+        const int par = (int)(it & 1);
+        ok = mbar_wait(&full[s], (uint32_t)((it / stages) & 1), &abort_flag, err, SRC_SOFTMAX);
+        const uint4 *sv = reinterpret_cast<const uint4 *>(stage_mem + (size_t)s * slot);
+        const T *xr = x + r * xs;
+        T *yr = y + r * ys;
+        Online st;
+        if (ok) {
+            for (int i = threadIdx.x; i < nvec; i += NT) {
+                float f[N];
+                int valid = N;
+                if (i < nwhole) {
+                    Vec<T>::from_bits(sv[i], f);
+                } else {
+                    valid = cols - i * N;
+#pragma unroll
+                    for (int e = 0; e < N; ++e) f[e] = e < valid ? Vec<T>::one(xr + i * N + e) : -INFINITY;
+                }
+#pragma unroll
+                for (int e = 0; e < N; ++e) f[e] *= kLog2e;
+                st.add<N>(f, valid);
+            }
+        }
+        st.warp_merge();
+        if (lane == 0) {
+            sm_m[par][wid] = st.m;
+            sm_d[par][wid] = st.d;
+        }
+        // every thread agrees: all waits succeeded, or all stop here
+        if (!__syncthreads_and(ok)) {
+            ok = false;
+            break;
+        }
+        Online t;
+        if (lane < NWARP) {
+            t.m = sm_m[par][lane];
+            t.d = sm_d[par][lane];
+        }
+        t.warp_merge();
+        const float m = t.m, inv = 1.f / t.d;
+        for (int i = threadIdx.x; i < nvec; i += NT) {
+            float f[N];
+            if (i < nwhole) {
+                Vec<T>::from_bits(sv[i], f);
+#pragma unroll
+                for (int e = 0; e < N; ++e) f[e] = ex2(f[e] * kLog2e - m) * inv;
+                Vec<T>::store(yr + i * N, f);
+            } else {
+                const int valid = cols - i * N;
+#pragma unroll
+                for (int e = 0; e < N; ++e)
+                    if (e < valid) Vec<T>::put(yr + i * N + e, ex2(Vec<T>::one(xr + i * N + e) * kLog2e - m) * inv);
+            }
+        }
+        __syncthreads();   // stage s has been read by every thread
+        if (threadIdx.x == 0) {
+            const int64_t nxt = r + (int64_t)stages * gridDim.x;
+            if (nxt < rows) issue(s, nxt);
+        }
+    }
+    if (!ok && threadIdx.x == 0) {
+        // the copies issued for iterations it .. it + stages - 1 may still be in flight
+        for (int j = 0; j < stages; ++j) {
+            const int64_t jt = it + j;
+            if (blockIdx.x + jt * gridDim.x < rows)
+                mbar_wait(&full[jt % stages], (uint32_t)((jt / stages) & 1), nullptr, err, SRC_SOFTMAX);
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// one CTA (or one cluster of CTAs) per row, the row held in registers.  CTA c of
+// a cluster of C owns the row's slice of NT*KV 16-byte vectors starting at
+// vector c*NT*KV; thread t holds vectors t, t + NT, ..., t + (KV-1) NT of the
+// slice (coalesced loads), so pass 2 runs from registers and the row is read
+// from HBM once.  Each CTA loads its next row while the current one is reduced
+// and written.  A thread's elements are all in registers, so it takes their
+// maximum first and sums e^(x - m) against it once; the (m, d') pairs of threads,
+// warps, CTAs and cluster ranks then merge with the online rule.  Every thread
+// writes only the vectors it read, so y may alias x.
+// ---------------------------------------------------------------------------
+constexpr int kMaxCluster = 8;
+
+template <typename T, int KV, int NT>
+__global__ void __launch_bounds__(NT) softmax_rows_cta_reg_kernel(const T *x, T *y, int64_t rows, int cols,
+                                                                  int64_t xs, int64_t ys) {
+    constexpr int N = Vec<T>::N;
+    constexpr int NWARP = NT / 32;
+    // (m, d') of each warp, and of each CTA of the cluster; two copies, by row
+    // parity, so a row needs one barrier of each kind: a copy is rewritten only
+    // after the next row's barrier, which every reader reaches after reading it
+    __shared__ float sm_m[2][NWARP], sm_d[2][NWARP];
+    __shared__ float cl_m[2][kMaxCluster], cl_d[2][kMaxCluster];
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    const uint32_t crank = cluster_ctarank(), csize = cluster_nctarank();
+    const int base = (int)crank * NT * KV * N;
+    uint4 next[KV];
+    auto fetch = [&](int64_t row) {
+        const T *xr = x + row * xs;
+#pragma unroll
+        for (int k = 0; k < KV; ++k) {
+            const int c0 = base + (k * NT + (int)threadIdx.x) * N;
+            if (c0 + N <= cols)
+                next[k] = *reinterpret_cast<const uint4 *>(xr + c0);
+            else if (c0 < cols)
+                next[k] = Vec<T>::bits_partial(xr + c0, cols - c0);
+            else
+                next[k] = make_uint4(0u, 0u, 0u, 0u);
+        }
+    };
+    // every CTA of a cluster walks the same rows, so all reach each cluster barrier
+    const int64_t rstep = gridDim.x / csize;
+    int64_t r = blockIdx.x / csize;
+    if (r < rows) fetch(r);
+    for (int par = 0; r < rows; r += rstep, par ^= 1) {
+        uint4 cur[KV];
+#pragma unroll
+        for (int k = 0; k < KV; ++k) cur[k] = next[k];
+        if (r + rstep < rows) fetch(r + rstep);
+        float mx = -INFINITY;
+#pragma unroll
+        for (int k = 0; k < KV; ++k) {
+            const int valid = cols - (base + (k * NT + (int)threadIdx.x) * N);
+            float f[N];
+            Vec<T>::from_bits(cur[k], f);
+#pragma unroll
+            for (int e = 0; e < N; ++e)
+                if (e < valid) mx = fmaxf(mx, f[e]);
+        }
+        Online st;
+        if (mx != -INFINITY) {
+            st.m = mx * kLog2e;
+#pragma unroll
+            for (int k = 0; k < KV; ++k) {
+                const int valid = cols - (base + (k * NT + (int)threadIdx.x) * N);
+                float f[N];
+                Vec<T>::from_bits(cur[k], f);
+#pragma unroll
+                for (int e = 0; e < N; ++e)
+                    if (e < valid) st.d += ex2(fmaf(f[e], kLog2e, -st.m));
+            }
+        }
+        st.warp_merge();
+        if (lane == 0) {
+            sm_m[par][wid] = st.m;
+            sm_d[par][wid] = st.d;
+        }
+        __syncthreads();
+        Online t;
+        if (lane < NWARP) {
+            t.m = sm_m[par][lane];
+            t.d = sm_d[par][lane];
+        }
+        t.warp_merge();
+        if (csize > 1) {
+            if (threadIdx.x < csize) {
+                st_cluster_f32(&cl_m[par][crank], threadIdx.x, t.m);
+                st_cluster_f32(&cl_d[par][crank], threadIdx.x, t.d);
+            }
+            cluster_sync();
+            t = Online();
+            if (lane < (int)csize) {
+                t.m = cl_m[par][lane];
+                t.d = cl_d[par][lane];
+            }
+            t.warp_merge();
+        }
+        const float m = t.m, inv = 1.f / t.d;
+        T *yr = y + r * ys;
+#pragma unroll
+        for (int k = 0; k < KV; ++k) {
+            const int c0 = base + (k * NT + (int)threadIdx.x) * N;
+            if (c0 >= cols) continue;
+            float f[N];
+            Vec<T>::from_bits(cur[k], f);
+#pragma unroll
+            for (int e = 0; e < N; ++e) f[e] = ex2(fmaf(f[e], kLog2e, -m)) * inv;
+            if (c0 + N <= cols) {
+                Vec<T>::store(yr + c0, f);
+            } else {
+#pragma unroll
+                for (int e = 0; e < N; ++e)
+                    if (c0 + e < cols) Vec<T>::put(yr + c0 + e, f[e]);
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
 // one CTA per row, two passes over the row
 // ---------------------------------------------------------------------------
 // NT threads per CTA: 256 for rows of up to 32 KB (more rows in flight per SM),
@@ -277,8 +536,102 @@ cudaError_t launch_warp(const T *x, T *y, int64_t rows, int cols, int64_t xs, in
     return cudaGetLastError();
 }
 
+// A register-row kernel over rows split into `csize` slices (csize CTAs per
+// cluster; 1: no cluster).  The grid is as many rows (clusters) as fit on the
+// GPU at once, asked of the runtime once per instance and cluster size; returns
+// cudaErrorNotSupported when no cluster of that size fits.
+template <typename T, int KV, int NT>
+cudaError_t launch_cta_reg(const T *x, T *y, int64_t rows, int cols, int64_t xs, int64_t ys, int sms, int csize,
+                           cudaStream_t stream) {
+    static std::once_flag once[kMaxCluster + 1];
+    static int resident[kMaxCluster + 1];   // CTAs per SM (csize 1) or clusters per GPU
+    auto kern = softmax_rows_cta_reg_kernel<T, KV, NT>;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)csize;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.blockDim = dim3(NT);
+    cfg.stream = stream;
+    if (csize > 1) {
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    std::call_once(once[csize], [&] {
+        int n = 0;
+        cudaError_t e;
+        if (csize == 1) {
+            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, NT, 0);
+        } else {
+            cfg.gridDim = dim3(csize);
+            e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
+        }
+        if (e != cudaSuccess) {
+            (void)cudaGetLastError();
+            n = csize == 1 ? 1 : 0;
+        }
+        resident[csize] = n;
+    });
+    int64_t cap = csize == 1 ? (int64_t)sms * resident[csize] : (int64_t)resident[csize];
+    if (cap <= 0) return cudaErrorNotSupported;
+    const int64_t units = rows < cap ? rows : cap;
+    cfg.gridDim = dim3((unsigned)(units * csize));
+    return cudaLaunchKernelEx(&cfg, kern, x, y, rows, cols, xs, ys);
+}
+
+// Rows of `row_bytes` bytes through the shared-memory ring: stages and CTAs per
+// SM chosen so that about 200 KB of each SM's shared memory holds rows.
+// cudaErrorNotSupported when no CTA of that size fits on an SM.
+template <typename T>
+cudaError_t launch_smem(const T *x, T *y, int64_t rows, int cols, int64_t xs, int64_t ys, int sms, uint32_t *err,
+                        cudaStream_t stream) {
+    constexpr int NT = kSmemThreads;
+    constexpr int kMaxDyn = 200 * 1024;
+    static std::once_flag once;
+    static bool attr_ok = false;
+    auto kern = softmax_rows_smem_kernel<T, NT>;
+    std::call_once(once, [&] {
+        attr_ok = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDyn) == cudaSuccess;
+        if (!attr_ok) (void)cudaGetLastError();
+    });
+    if (!attr_ok) return cudaErrorNotSupported;
+    const uint32_t bulk = (uint32_t)(cols / Vec<T>::N) * 16u;
+    const uint32_t slot = (bulk + 127u) & ~127u;
+    // as many CTAs per SM as the threads allow (each row's reductions take a
+    // fixed latency that other CTAs' rows hide), each with the stages that share
+    // the SM's ~200 KB among them (at least two: one row read while the next lands)
+    constexpr int kCtasPerSm = 2048 / NT;
+    int stages = (int)(kMaxDyn / ((size_t)kCtasPerSm * slot));
+    stages = stages < 2 ? 2 : (stages > kSmemMaxStages ? kSmemMaxStages : stages);
+    const size_t dyn = (size_t)stages * slot;
+    if (slot == 0 || dyn > (size_t)kMaxDyn) return cudaErrorNotSupported;
+    // CTAs per SM for this shared-memory size, asked once per size
+    static std::mutex mu;
+    static std::unordered_map<size_t, int> per_sm_of;
+    int per_sm = 0;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        auto f = per_sm_of.find(dyn);
+        if (f != per_sm_of.end()) {
+            per_sm = f->second;
+        } else {
+            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, NT, dyn) != cudaSuccess) {
+                (void)cudaGetLastError();
+                per_sm = 0;
+            }
+            per_sm_of[dyn] = per_sm;
+        }
+    }
+    if (per_sm <= 0) return cudaErrorNotSupported;
+    const int64_t cap = (int64_t)sms * per_sm;
+    const int grid = (int)(rows < cap ? rows : cap);
+    kern<<<grid, NT, dyn, stream>>>(x, y, rows, cols, xs, ys, stages, slot, err);
+    return cudaGetLastError();
+}
+
 template <typename T, bool VEC>
-cudaError_t launch_t(const T *x, T *y, int64_t rows, int cols, int64_t xs, int64_t ys, int sms,
+cudaError_t launch_t(const T *x, T *y, int64_t rows, int cols, int64_t xs, int64_t ys, int sms, uint32_t *err,
                      cudaStream_t stream) {
     constexpr int N = VEC ? Vec<T>::N : 1;
     // a warp per row while the row fits in 8 accesses per lane (1024 fp32 or
@@ -289,7 +642,31 @@ cudaError_t launch_t(const T *x, T *y, int64_t rows, int cols, int64_t xs, int64
     if (per_lane <= 2) return launch_warp<T, 2, VEC>(x, y, rows, cols, xs, ys, sms, stream);
     if (per_lane <= 4) return launch_warp<T, 4, VEC>(x, y, rows, cols, xs, ys, sms, stream);
     if (per_lane <= 8) return launch_warp<T, 8, VEC>(x, y, rows, cols, xs, ys, sms, stream);
-    if ((int64_t)cols * (int64_t)sizeof(T) <= 32768) {
+    const int64_t row_bytes = (int64_t)cols * (int64_t)sizeof(T);
+    if constexpr (VEC) {
+        // up to 16 KB: a CTA of 128 threads per row, 16 CTAs per SM, rows
+        // streamed through shared memory (short rows need many rows in flight at
+        // once).  Beyond, the row in registers: one CTA of 256 threads (32 KB
+        // slice) up to 32 KB, of 512 threads (64 KB) up to 64 KB, a cluster of up
+        // to 8 of the 256-thread CTAs up to 256 KB, of the 512-thread ones up to
+        // 512 KB
+        constexpr int64_t kSlice256 = 256 * 8 * 16, kSlice512 = 512 * 8 * 16;
+        cudaError_t e = cudaErrorNotSupported;
+        if (row_bytes <= 16384)
+            e = launch_smem<T>(x, y, rows, cols, xs, ys, sms, err, stream);
+        else if (row_bytes <= kSlice256)
+            e = launch_cta_reg<T, 8, 256>(x, y, rows, cols, xs, ys, sms, 1, stream);
+        else if (row_bytes <= kSlice512)
+            e = launch_cta_reg<T, 8, 512>(x, y, rows, cols, xs, ys, sms, 1, stream);
+        else if (row_bytes <= kMaxCluster * kSlice256)
+            e = launch_cta_reg<T, 8, 256>(x, y, rows, cols, xs, ys, sms,
+                                          (int)((row_bytes + kSlice256 - 1) / kSlice256), stream);
+        else if (row_bytes <= kMaxCluster * kSlice512)
+            e = launch_cta_reg<T, 8, 512>(x, y, rows, cols, xs, ys, sms,
+                                          (int)((row_bytes + kSlice512 - 1) / kSlice512), stream);
+        if (e != cudaErrorNotSupported) return e;
+    }
+    if (row_bytes <= 32768) {
         const int grid = (int)(rows < (int64_t)sms * 8 ? rows : (int64_t)sms * 8);
         softmax_rows_cta_kernel<T, VEC, 256><<<grid, 256, 0, stream>>>(x, y, rows, cols, xs, ys);
     } else {
@@ -302,20 +679,20 @@ cudaError_t launch_t(const T *x, T *y, int64_t rows, int cols, int64_t xs, int64
 }  // namespace
 
 cudaError_t launch_softmax_rows(const void *x, void *y, int64_t rows, int cols, int64_t x_row_stride,
-                                int64_t y_row_stride, int bf16, int sms, cudaStream_t stream) {
+                                int64_t y_row_stride, int bf16, int sms, uint32_t *err, cudaStream_t stream) {
     const size_t es = bf16 ? 2 : 4;
     const bool vec = ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(y)) & 15u) == 0 &&
                      ((size_t)x_row_stride * es) % 16 == 0 && ((size_t)y_row_stride * es) % 16 == 0;
     if (bf16) {
         const auto *xb = reinterpret_cast<const __nv_bfloat16 *>(x);
         auto *yb = reinterpret_cast<__nv_bfloat16 *>(y);
-        return vec ? launch_t<__nv_bfloat16, true>(xb, yb, rows, cols, x_row_stride, y_row_stride, sms, stream)
-                   : launch_t<__nv_bfloat16, false>(xb, yb, rows, cols, x_row_stride, y_row_stride, sms, stream);
+        return vec ? launch_t<__nv_bfloat16, true>(xb, yb, rows, cols, x_row_stride, y_row_stride, sms, err, stream)
+                   : launch_t<__nv_bfloat16, false>(xb, yb, rows, cols, x_row_stride, y_row_stride, sms, err, stream);
     }
     const auto *xf = reinterpret_cast<const float *>(x);
     auto *yf = reinterpret_cast<float *>(y);
-    return vec ? launch_t<float, true>(xf, yf, rows, cols, x_row_stride, y_row_stride, sms, stream)
-               : launch_t<float, false>(xf, yf, rows, cols, x_row_stride, y_row_stride, sms, stream);
+    return vec ? launch_t<float, true>(xf, yf, rows, cols, x_row_stride, y_row_stride, sms, err, stream)
+               : launch_t<float, false>(xf, yf, rows, cols, x_row_stride, y_row_stride, sms, err, stream);
 }
 
 }  // namespace attn

@@ -569,7 +569,8 @@ def bench_softmax(av, device, steps, warmup, flush, peaks):
     import torch
     res = {}
     for name, rows, cols, dt in (("f32_32768x8192", 32768, 8192, torch.float32),
-                                 ("bf16_262144x1024", 262144, 1024, torch.bfloat16)):
+                                 ("bf16_262144x1024", 262144, 1024, torch.bfloat16),
+                                 ("f32_4096x65536", 4096, 65536, torch.float32)):
         g = torch.Generator(device=device).manual_seed(1234 + rows)
         x = (torch.randn(rows, cols, device=device, generator=g) * 30.0).to(dt)
         y = torch.empty_like(x)
@@ -584,14 +585,15 @@ def bench_softmax(av, device, steps, warmup, flush, peaks):
         nbytes = 2 * x.numel() * x.element_size()
         gbs = nbytes / t / 1e9
         res[name] = {"value": gbs, "unit": "GB/s", "ms_per_step": t * 1e3, "algorithmic_bytes": nbytes,
-                     "roofline": {"bound": "hbm", "kernel": "softmax_rows_%s_kernel" % ("cta" if cols > 2048 else "warp"),
+                     "roofline": {"bound": "hbm", "kernel": "softmax_rows_%s_kernel" % ("cta_reg" if cols > 2048 else "warp"),
                                   "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                                   "frac": gbs / peaks["hbm_gbs"], "traffic": None},
                      "launches_per_step": 1}
         del x, y
     torch.cuda.empty_cache()
-    res["workload"] = ("row softmax, N(0, 30^2) logits: fp32 32768 x 8192 (two passes per row, the second from "
-                       "L2) and bf16 262144 x 1024 (one read, row in registers)")
+    res["workload"] = ("row softmax, N(0, 30^2) logits, each row read once and held in registers: fp32 32768 x 8192 "
+                       "(a CTA per row), bf16 262144 x 1024 (a warp per row), fp32 4096 x 65536 (a cluster of 8 CTAs "
+                       "per row)")
     return res
 
 
@@ -771,6 +773,7 @@ def summary(line, peaks, peak_src):
     if sm:
         put("softmax_f32", sm.get("f32_32768x8192"))
         put("softmax_bf16", sm.get("bf16_262144x1024"))
+        put("softmax_f32_long", sm.get("f32_4096x65536"))
     put("padded", line.get("padded_prefill"))
     out["peaks"] = {"bf16_burst_tflops": peaks["bf16_tflops"], "hbm_gbs": peaks["hbm_gbs"], "source": peak_src}
     return out

@@ -10,7 +10,12 @@ pytestmark = pytest.mark.gpu
 
 SHAPES = [(1, 1), (3, 7), (33, 31), (64, 128), (17, 1000), (8, 2048), (5, 2049), (9, 4096), (4, 4097),
           (2, 100003), (700, 512),
-          (6, 16384), (3, 12296), (2, 32768)]   # long rows: a CTA per row, two passes
+          (6, 16384), (3, 12296), (2, 32768),   # long rows: a CTA per row (in registers up to 64 KB)
+          (1000, 3000), (400, 9000),            # more rows than CTAs: each CTA loads its next row early
+          (20000, 1500),                        # rows streamed through shared memory, the ring wraps often
+          (3, 40000), (3, 65536), (200, 20000),  # a cluster of CTAs per row: 5, 8, 3 slices of 32 KB
+          (2, 131072), (40, 200000),            # fp32 8 / bf16 7 slices of 64 KB
+          (2, 200000)]                          # fp32 beyond 8 slices of 64 KB: two passes
 
 
 def _inputs(seed, rows, cols, scale=30.0):
@@ -55,6 +60,18 @@ def test_softmax_rows_strided_inplace_and_unaligned():
     av.softmax_rows(view, out=view)            # in place
     _check(view, ref, False)
     assert torch.equal(wide[:, 3001:], torch.zeros(40, 99, device="cuda"))
+    # bf16 rows with a partial last 16-byte vector (5003 = 625 * 8 + 3), stride 5008
+    xb = torch.from_numpy(_inputs(93, 30, 5003)).to(torch.bfloat16)
+    wb = torch.zeros(30, 5008, dtype=torch.bfloat16)
+    wb[:, :5003] = xb
+    wb = wb.cuda()
+    _check(av.softmax_rows(wb[:, :5003]), oracle.softmax_rows(xb), True)
+    # fp32 rows of 3 cluster slices with a partial last vector, stride 40004
+    xc = torch.from_numpy(_inputs(94, 5, 40001))
+    wc = torch.zeros(5, 40004, dtype=torch.float32)
+    wc[:, :40001] = xc
+    wc = wc.cuda()
+    _check(av.softmax_rows(wc[:, :40001]), oracle.softmax_rows(xc), False)
     # a view that starts 4 bytes past a 16-byte boundary (element accesses)
     buf = torch.zeros(40 * 301 + 1, dtype=torch.float32, device="cuda")
     xu = buf[1:].view(40, 301)
