@@ -113,6 +113,9 @@ bool fix_stride(int64_t *stride, int64_t packed) {
 
 constexpr int kMaxSplits = 64;
 constexpr int kDecodeMaxColumns = 64;   // Sq x G query columns per KV head on the decode kernel
+// ... with the fp16 V / 16 cache: past one column group of 16 the paged prefill
+// (tcgen05, no conversion pass with that cache) streams the cache faster
+constexpr int kDecodeMaxColumnsV16 = 16;
 constexpr int kDecodeTile = 64;
 
 int choose_splits(int num_sms, int batch, int num_heads_kv, int max_len, int requested) {
@@ -158,12 +161,13 @@ size_t decode_partial_bytes(int batch, int seqlen_q, int num_heads_q, int head_d
 }
 
 // The kv-cache entry runs on the decode kernel when the Sq x G query rows of a
-// KV head fit four column groups of 16; otherwise on the paged varlen prefill.
-bool kvcache_on_decode(int batch, int seqlen_q, int num_heads_q, int num_heads_kv, int head_dim) {
+// KV head fit four column groups of 16 (one group when the fp16 V / 16 cache is
+// given); otherwise on the paged varlen prefill.
+bool kvcache_on_decode(int batch, int seqlen_q, int num_heads_q, int num_heads_kv, int head_dim, bool v16) {
     if (num_heads_q <= 0 || num_heads_kv <= 0 || num_heads_q % num_heads_kv) return false;
     if (head_dim != 64 && head_dim != 128) return false;
     if (batch > 65535 || num_heads_kv > 65535) return false;
-    return (int64_t)seqlen_q * (num_heads_q / num_heads_kv) <= kDecodeMaxColumns;
+    return (int64_t)seqlen_q * (num_heads_q / num_heads_kv) <= (v16 ? kDecodeMaxColumnsV16 : kDecodeMaxColumns);
 }
 
 struct DecodeCall {
@@ -643,7 +647,7 @@ attn_status attn_padded_fwd(const void *q, const void *k, const void *v, void *o
 static size_t kvcache_ws(int batch, int seqlen_q, int num_heads_q, int num_heads_kv, int head_dim,
                          int max_cache_seqlen, bool v16_cache) {
     if (batch <= 0 || seqlen_q <= 0 || max_cache_seqlen < 0) return 0;
-    if (kvcache_on_decode(batch, seqlen_q, num_heads_q, num_heads_kv, head_dim)) {
+    if (kvcache_on_decode(batch, seqlen_q, num_heads_q, num_heads_kv, head_dim, v16_cache)) {
         // split partials of the decode kernel (never 0: 0 means invalid sizes)
         DevInfo *d = nullptr;
         int sms = 148;
@@ -659,7 +663,10 @@ static size_t kvcache_ws(int batch, int seqlen_q, int num_heads_q, int num_heads
 
 size_t attn_kvcache_workspace_size(int batch, int seqlen_q, int num_heads_q, int num_heads_kv, int head_dim,
                                    int max_cache_seqlen) {
-    return kvcache_ws(batch, seqlen_q, num_heads_q, num_heads_kv, head_dim, max_cache_seqlen, false);
+    // enough for either route: with or without the fp16 V / 16 cache
+    const size_t a = kvcache_ws(batch, seqlen_q, num_heads_q, num_heads_kv, head_dim, max_cache_seqlen, false);
+    const size_t b = kvcache_ws(batch, seqlen_q, num_heads_q, num_heads_kv, head_dim, max_cache_seqlen, true);
+    return a == 0 || b == 0 ? 0 : (a > b ? a : b);
 }
 
 attn_status attn_kvcache_fwd(const void *q, const void *k_cache, const void *v_cache, void *out, float *lse,
@@ -682,7 +689,7 @@ attn_status attn_kvcache_fwd(const void *q, const void *k_cache, const void *v_c
     attn_status st = dev_info(&d);
     if (st != ATTN_OK) return st;
     if ((st = check_arch(d)) != ATTN_OK) return st;
-    if (kvcache_on_decode(batch, seqlen_q, num_heads_q, num_heads_kv, head_dim)) {
+    if (kvcache_on_decode(batch, seqlen_q, num_heads_q, num_heads_kv, head_dim, v16_cache != nullptr)) {
         // Sq x G query rows per KV head fit the decode kernel: stream the cache
         // once, no fp16 copy of V.  lse is [Hq, batch * seqlen_q].
         DecodeCall c = {q, k_cache, v_cache, out, lse, cache_seqlens, block_table, block_table_stride, batch,

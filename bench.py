@@ -171,8 +171,12 @@ KERNEL_SOURCES = {
     "decode": ["attention_attn_varlen_gb300/csrc/decode.cu", "attention_attn_varlen_gb300/csrc/common.cuh"],
     "decode_sq4": ["attention_attn_varlen_gb300/csrc/decode.cu", "attention_attn_varlen_gb300/csrc/common.cuh"],
     "decode_sq8": ["attention_attn_varlen_gb300/csrc/decode.cu", "attention_attn_varlen_gb300/csrc/common.cuh"],
-    "decode_sq8_v16": ["attention_attn_varlen_gb300/csrc/decode.cu", "attention_attn_varlen_gb300/csrc/common.cuh"],
+    "kvcache_sq4_v16": ["attention_attn_varlen_gb300/csrc/decode.cu", "attention_attn_varlen_gb300/csrc/common.cuh"],
+    "kvcache_sq8_v16": ["attention_attn_varlen_gb300/csrc/prefill.cu", "attention_attn_varlen_gb300/csrc/common.cuh"],
     "store": ["attention_attn_varlen_gb300/csrc/store_kvcache.cu", "attention_attn_varlen_gb300/csrc/common.cuh"],
+    "softmax_warp": ["attention_attn_varlen_gb300/csrc/softmax.cu", "attention_attn_varlen_gb300/csrc/common.cuh"],
+    "softmax_cta_reg": ["attention_attn_varlen_gb300/csrc/softmax.cu", "attention_attn_varlen_gb300/csrc/common.cuh"],
+    "softmax_cluster": ["attention_attn_varlen_gb300/csrc/softmax.cu", "attention_attn_varlen_gb300/csrc/common.cuh"],
 }
 
 
@@ -374,14 +378,20 @@ def bench_decode(av, device, steps, warmup, flush, peaks, with_oracle=True):
         torch.cuda.synchronize()
         msv, kmsv = time_steps(stepv, steps, flush, kernel=True)
         tv, tkv = float(np.mean(msv)) / 1e3, float(np.mean(kmsv)) / 1e3
+        # with the V/16 cache, more than 16 query rows per KV head run on the paged prefill
+        on_prefill = Sq * cfg.Hq // cfg.Hkv > 16
         res[f"kvcache_{Sq}_tokens_v16"] = {
-            "workload": f"the same {Sq}-token step reading the fp16 V/16 cache (PV on one fp16 term 16 P)",
+            "workload": (f"the same {Sq}-token step reading the fp16 V/16 cache: " +
+                         ("the paged varlen prefill (tcgen05), no conversion pass" if on_prefill else
+                          "split-KV decode kernel, PV on one fp16 term 16 P")),
             "value": nbn / tv / 1e9, "unit": "GB/s", "ms_per_step": tv * 1e3, "algorithmic_bytes": nbn,
-            "roofline": {"bound": "hbm", "kernel": "attn_decode_split_kernel", "achieved": nbn / tkv / 1e9,
+            "roofline": {"bound": "hbm", "kernel": "attn_prefill_kernel" if on_prefill else "attn_decode_split_kernel",
+                         "achieved": nbn / tkv / 1e9,
                          "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": nbn / tkv / 1e9 / peaks["hbm_gbs"],
                          "kernel_ms": tkv * 1e3,
-                         "traffic": ncu_traffic("decode_sq8_v16", float(cfg.ctx.sum()) * cfg.Hkv) if Sq == 8 else None},
-            "launches_per_step": 2 if splits > 1 else 1}
+                         "traffic": ncu_traffic(f"kvcache_sq{Sq}_v16", float(cfg.ctx.sum()) * cfg.Hkv)},
+            # prefill route: cu_seqlens kernel, scheduling pre-pass, attention
+            "launches_per_step": 3 if on_prefill else (2 if splits > 1 else 1)}
         del qn, wsn, outn
     del kc, vc, v16
     torch.cuda.empty_cache()
@@ -568,9 +578,9 @@ def bench_softmax(av, device, steps, warmup, flush, peaks):
     write of the matrix."""
     import torch
     res = {}
-    for name, rows, cols, dt in (("f32_32768x8192", 32768, 8192, torch.float32),
-                                 ("bf16_262144x1024", 262144, 1024, torch.bfloat16),
-                                 ("f32_4096x65536", 4096, 65536, torch.float32)):
+    for name, rows, cols, dt, kern in (("f32_32768x8192", 32768, 8192, torch.float32, "softmax_cta_reg"),
+                                       ("bf16_262144x1024", 262144, 1024, torch.bfloat16, "softmax_warp"),
+                                       ("f32_4096x65536", 4096, 65536, torch.float32, "softmax_cluster")):
         g = torch.Generator(device=device).manual_seed(1234 + rows)
         x = (torch.randn(rows, cols, device=device, generator=g) * 30.0).to(dt)
         y = torch.empty_like(x)
@@ -585,9 +595,11 @@ def bench_softmax(av, device, steps, warmup, flush, peaks):
         nbytes = 2 * x.numel() * x.element_size()
         gbs = nbytes / t / 1e9
         res[name] = {"value": gbs, "unit": "GB/s", "ms_per_step": t * 1e3, "algorithmic_bytes": nbytes,
-                     "roofline": {"bound": "hbm", "kernel": "softmax_rows_%s_kernel" % ("cta_reg" if cols > 2048 else "warp"),
+                     "roofline": {"bound": "hbm", "kernel": {"softmax_cta_reg": "softmax_rows_cta_reg_kernel",
+                                                             "softmax_warp": "softmax_rows_warp_kernel",
+                                                             "softmax_cluster": "softmax_rows_cta_reg_kernel (cluster of 8)"}[kern],
                                   "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                                  "frac": gbs / peaks["hbm_gbs"], "traffic": None},
+                                  "frac": gbs / peaks["hbm_gbs"], "traffic": ncu_traffic(kern, x.numel())},
                      "launches_per_step": 1}
         del x, y
     torch.cuda.empty_cache()

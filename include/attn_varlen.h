@@ -316,12 +316,14 @@ ATTN_API size_t attn_padded_workspace_size(int batch, int seqlen_q, int seqlen_k
  * KV cache ([A] "Decode": flash_attn_with_kvcache(q, k_cache, v_cache,
  * cache_seqlens, block_table, softmax_scale, causal) with q of shape
  * [B, seqlen_q, H, D] and seqlen_q >= 1: chunked append, speculative
- * verification).  Two routes, chosen from the sizes alone:
- *  - seqlen_q * (num_heads_q / num_heads_kv) <= 64 and head_dim 64 or 128:
- *    the split-KV decode kernel of attn_decode_paged with one query column
- *    per (new token, head), up to 16 columns per CTA; the cache is read from
- *    HBM once (CTAs holding other columns of the same KV head re-read it from
- *    L2).  With seqlen_q = 1 the result equals attn_decode_paged's bit for bit.
+ * verification).  Two routes, chosen from the sizes and from whether
+ * v16_cache is given:
+ *  - seqlen_q * (num_heads_q / num_heads_kv) <= 64 (<= 16 with v16_cache) and
+ *    head_dim 64 or 128: the split-KV decode kernel of attn_decode_paged with
+ *    one query column per (new token, head), up to 16 columns per CTA; the
+ *    cache is read from HBM once (CTAs holding other columns of the same KV
+ *    head re-read it from L2).  With seqlen_q = 1 the result equals
+ *    attn_decode_paged's bit for bit.
  *  - otherwise: cu_seqlens_q = b * seqlen_q and cu_seqlens_k = prefix sums of
  *    cache_seqlens are computed on the device, then the paged varlen prefill
  *    (attn_varlen_fwd) runs.
@@ -341,7 +343,8 @@ ATTN_API size_t attn_padded_workspace_size(int batch, int seqlen_q, int seqlen_k
  *                converts nothing, and the decode route multiplies it by one fp16
  *                term 16 P (11 significant bits) instead of P's two bf16 terms,
  *                half the P V work
- *   workspace    at least attn_kvcache_workspace_size(...) bytes, 256-byte
+ *   workspace    at least attn_kvcache_workspace_size(...) bytes (enough for
+ *                either route, with or without v16_cache), 256-byte
  *                aligned.  On the decode route it holds the split partials
  *                (at most 64 splits of fp32 rows); on the prefill route without
  *                v16_cache the fp16 copy of V for batch * max_cache_seqlen keys,
@@ -356,7 +359,8 @@ ATTN_API attn_status attn_kvcache_fwd(const void *q, const void *k_cache, const 
                                       const void *v16_cache, void *workspace, size_t workspace_bytes,
                                       void *stream);
 
-/* Workspace bytes attn_kvcache_fwd needs (0 for invalid sizes). */
+/* Workspace bytes attn_kvcache_fwd needs on either route, with or without
+ * v16_cache (0 for invalid sizes). */
 ATTN_API size_t attn_kvcache_workspace_size(int batch, int seqlen_q, int num_heads_q, int num_heads_kv,
                                             int head_dim, int max_cache_seqlen);
 

@@ -98,6 +98,28 @@ def test_kvcache_equals_paged_varlen_bitexact():
     assert torch.equal(lse_h, lse_k)
 
 
+def test_kvcache_v16_past_one_column_group_runs_the_paged_prefill_bitexact():
+    """With the fp16 V / 16 cache, more than 16 query columns per KV head (8 tokens x
+    4 heads) go to the paged varlen prefill: the kv-cache entry equals
+    attn_varlen_fwd on the same caches bit for bit, and the oracle."""
+    cfg = workloads.small_paged(67, ctx=[900, 64, 2100, 8], new=[8, 8, 8, 8], Hq=32, Hkv=8, D=128, block_size=64)
+    q = cfg.q()
+    av.get_last_device_error()
+    kc, vc, k_new, v_new = _paged_device(cfg)
+    cs, bt = _as_kvcache_args(cfg, kc, vc)
+    v16 = v16_of(vc)
+    out_k, lse_k = av.attn_with_kvcache(q.cuda().view(cfg.batch, 8, cfg.Hq, cfg.D), kc, vc, cs, bt, cfg.scale,
+                                        max_cache_seqlen=int(cfg.lens_k.max()), return_lse=True, v16_cache=v16)
+    out_v, lse_v = _run_paged(cfg, q, kc, vc, v16=v16)
+    torch.cuda.synchronize()
+    assert av.get_last_device_error()[0] == 0
+    assert torch.equal(out_k.view(-1, cfg.Hq, cfg.D).view(torch.int16), out_v.view(torch.int16))
+    assert torch.equal(lse_k, lse_v)
+    ref, ref_lse, _ = _paged_oracle(cfg, q, k_new, v_new, list(range(cfg.batch)))
+    assert_close(out_k.view(-1, cfg.Hq, cfg.D), ref.reshape(-1, cfg.Hq, cfg.D), "kvcache v16 8 tokens (prefill route)")
+    assert_lse_close(lse_k.t().contiguous(), ref_lse.reshape(-1, cfg.Hq), "kvcache v16 8 tokens lse (prefill route)")
+
+
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("Sq,Hq,Hkv,D", [(4, 16, 4, 128), (2, 8, 8, 64), (9, 16, 8, 128), (17, 32, 8, 128)])
 def test_kvcache_causal_flag(causal, Sq, Hq, Hkv, D):
