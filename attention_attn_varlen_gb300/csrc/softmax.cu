@@ -28,6 +28,41 @@ namespace {
 
 constexpr float kLog2e = 1.4426950408889634f;
 
+// error-word source bit of this file's kernels (beside SRC_STORE ... SRC_PREFILL)
+constexpr uint32_t SRC_SOFTMAX = 1u << 12;
+
+// thread-block cluster: this CTA's rank and the cluster's size (1 without a cluster)
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ uint32_t cluster_nctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+    return r;
+}
+// store v into the shared-memory word of CTA `rank` of the cluster that sits at
+// the address `local` has in this CTA
+__device__ __forceinline__ void st_cluster_f32(const void *local, uint32_t rank, float v) {
+    uint32_t a = smem_u32(local), ra;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(a), "r"(rank));
+    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(ra), "f"(v) : "memory");
+}
+// every thread of every CTA of the cluster: stores before it are visible after it
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// untiled bulk copy global -> shared (16-byte aligned addresses, bytes a
+// multiple of 16), completion on an mbarrier
+__device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_u32(dst)),
+                 "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
+                 : "memory");
+}
+
 // 16-byte vector of T as floats
 template <typename T>
 struct Vec;
@@ -219,16 +254,18 @@ __global__ void __launch_bounds__(256) softmax_rows_warp_kernel(const T *x, T *y
 // next `stages` rows of the CTA in flight with bulk copies (one per row, its
 // whole 16-byte vectors; the few elements past the last one are read
 // directly), so the bytes in flight are bounded by shared memory, not by
-// registers.  Pass 1 (online m, d') and pass 2 both read the row from shared
-// memory; a stage is refilled once every thread has passed the row's last
-// barrier.  Every mbarrier wait is bounded: on a timeout the kernel records it
+// registers.  Each thread copies its (at most KV) vectors of the landed row into
+// registers, takes their maximum, sums e^(x - m) against it, and after the
+// CTA's merge writes the normalised vectors from the same registers; a stage
+// is refilled once every thread has passed the row's last barrier.  Every mbarrier wait is bounded: on a timeout the kernel records it
 // in the error word, lets its copies in flight land (again bounded) and stops.
 // ---------------------------------------------------------------------------
 constexpr int kSmemMaxStages = 8;
 constexpr int kSmemThreads = 128;
+constexpr int kSmemVecs = 8;   // 16-byte vectors per thread: rows of up to 128 x 8 x 16 B = 16 KB
 
-template <typename T, int NT>
-__global__ void __launch_bounds__(NT) softmax_rows_smem_kernel(const T *x, T *y, int64_t rows, int cols,
+template <typename T, int NT, int KV>
+__global__ void __launch_bounds__(NT, 2048 / NT / 2) softmax_rows_smem_kernel(const T *x, T *y, int64_t rows, int cols,
                                                                int64_t xs, int64_t ys, int stages, uint32_t slot,
                                                                uint32_t *err) {
     constexpr int N = Vec<T>::N;
@@ -265,21 +302,55 @@ __global__ void __launch_bounds__(NT) softmax_rows_smem_kernel(const T *x, T *y,
         const uint4 *sv = reinterpret_cast<const uint4 *>(stage_mem + (size_t)s * slot);
         const T *xr = x + r * xs;
         T *yr = y + r * ys;
-        Online st;
-        if (ok) {
-            for (int i = threadIdx.x; i < nvec; i += NT) {
-                float f[N];
-                int valid = N;
-                if (i < nwhole) {
-                    Vec<T>::from_bits(sv[i], f);
-                } else {
-                    valid = cols - i * N;
+        // the thread's vectors tid, tid + NT, ... (at most KV) into registers, as
+        // floats when they fit in 32 registers (unpacked once), else as raw bits;
+        // the partial vector past the bulk copy comes from global memory
+        constexpr bool kAsFloat = KV * N <= 32;
+        uint4 v[kAsFloat ? 1 : KV];
+        float fv[kAsFloat ? KV : 1][N];
+        auto elems = [&](int k, float (&f)[N]) {
+            if constexpr (kAsFloat) {
 #pragma unroll
-                    for (int e = 0; e < N; ++e) f[e] = e < valid ? Vec<T>::one(xr + i * N + e) : -INFINITY;
+                for (int e = 0; e < N; ++e) f[e] = fv[k][e];
+            } else {
+                Vec<T>::from_bits(v[k], f);
+            }
+        };
+        float mx = -INFINITY;
+        if (ok) {
+#pragma unroll
+            for (int k = 0; k < KV; ++k) {
+                const int i = (int)threadIdx.x + k * NT;
+                uint4 bits = make_uint4(0u, 0u, 0u, 0u);
+                if (i < nwhole)
+                    bits = sv[i];
+                else if (i < nvec)
+                    bits = Vec<T>::bits_partial(xr + i * N, cols - i * N);
+                const int valid = cols - i * N;
+                float f[N];
+                Vec<T>::from_bits(bits, f);
+                if constexpr (kAsFloat) {
+#pragma unroll
+                    for (int e = 0; e < N; ++e) fv[k][e] = f[e];
+                } else {
+                    v[k] = bits;
                 }
 #pragma unroll
-                for (int e = 0; e < N; ++e) f[e] *= kLog2e;
-                st.add<N>(f, valid);
+                for (int e = 0; e < N; ++e)
+                    if (e < valid) mx = fmaxf(mx, f[e]);
+            }
+        }
+        Online st;
+        if (mx != -INFINITY) {
+            st.m = mx * kLog2e;
+#pragma unroll
+            for (int k = 0; k < KV; ++k) {
+                const int valid = cols - ((int)threadIdx.x + k * NT) * N;
+                float f[N];
+                elems(k, f);
+#pragma unroll
+                for (int e = 0; e < N; ++e)
+                    if (e < valid) st.d += ex2(fmaf(f[e], kLog2e, -st.m));
             }
         }
         st.warp_merge();
@@ -299,18 +370,20 @@ __global__ void __launch_bounds__(NT) softmax_rows_smem_kernel(const T *x, T *y,
         }
         t.warp_merge();
         const float m = t.m, inv = 1.f / t.d;
-        for (int i = threadIdx.x; i < nvec; i += NT) {
-            float f[N];
-            if (i < nwhole) {
-                Vec<T>::from_bits(sv[i], f);
 #pragma unroll
-                for (int e = 0; e < N; ++e) f[e] = ex2(f[e] * kLog2e - m) * inv;
+        for (int k = 0; k < KV; ++k) {
+            const int i = (int)threadIdx.x + k * NT;
+            if (i >= nvec) continue;
+            float f[N];
+            elems(k, f);
+#pragma unroll
+            for (int e = 0; e < N; ++e) f[e] = ex2(fmaf(f[e], kLog2e, -m)) * inv;
+            if (i < nwhole) {
                 Vec<T>::store(yr + i * N, f);
             } else {
-                const int valid = cols - i * N;
 #pragma unroll
                 for (int e = 0; e < N; ++e)
-                    if (e < valid) Vec<T>::put(yr + i * N + e, ex2(Vec<T>::one(xr + i * N + e) * kLog2e - m) * inv);
+                    if (i * N + e < cols) Vec<T>::put(yr + i * N + e, f[e]);
             }
         }
         __syncthreads();   // stage s has been read by every thread
@@ -583,19 +656,20 @@ cudaError_t launch_cta_reg(const T *x, T *y, int64_t rows, int cols, int64_t xs,
 // Rows of `row_bytes` bytes through the shared-memory ring: stages and CTAs per
 // SM chosen so that about 200 KB of each SM's shared memory holds rows.
 // cudaErrorNotSupported when no CTA of that size fits on an SM.
-template <typename T>
-cudaError_t launch_smem(const T *x, T *y, int64_t rows, int cols, int64_t xs, int64_t ys, int sms, uint32_t *err,
-                        cudaStream_t stream) {
+template <typename T, int KV>
+cudaError_t launch_smem_kv(const T *x, T *y, int64_t rows, int cols, int64_t xs, int64_t ys, int sms, uint32_t *err,
+                           cudaStream_t stream) {
     constexpr int NT = kSmemThreads;
     constexpr int kMaxDyn = 200 * 1024;
     static std::once_flag once;
     static bool attr_ok = false;
-    auto kern = softmax_rows_smem_kernel<T, NT>;
+    auto kern = softmax_rows_smem_kernel<T, NT, KV>;
     std::call_once(once, [&] {
         attr_ok = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDyn) == cudaSuccess;
         if (!attr_ok) (void)cudaGetLastError();
     });
     if (!attr_ok) return cudaErrorNotSupported;
+    if ((cols + Vec<T>::N - 1) / Vec<T>::N > NT * KV) return cudaErrorNotSupported;
     const uint32_t bulk = (uint32_t)(cols / Vec<T>::N) * 16u;
     const uint32_t slot = (bulk + 127u) & ~127u;
     // as many CTAs per SM as the threads allow (each row's reductions take a
@@ -628,6 +702,16 @@ cudaError_t launch_smem(const T *x, T *y, int64_t rows, int cols, int64_t xs, in
     const int grid = (int)(rows < cap ? rows : cap);
     kern<<<grid, NT, dyn, stream>>>(x, y, rows, cols, xs, ys, stages, slot, err);
     return cudaGetLastError();
+}
+
+// the ring kernel with as few vectors per thread as the row needs (4 or 8): the
+// unused ones would still cost their instructions
+template <typename T>
+cudaError_t launch_smem(const T *x, T *y, int64_t rows, int cols, int64_t xs, int64_t ys, int sms, uint32_t *err,
+                        cudaStream_t stream) {
+    const int nvec = (cols + Vec<T>::N - 1) / Vec<T>::N;
+    if (nvec <= kSmemThreads * 4) return launch_smem_kv<T, 4>(x, y, rows, cols, xs, ys, sms, err, stream);
+    return launch_smem_kv<T, kSmemVecs>(x, y, rows, cols, xs, ys, sms, err, stream);
 }
 
 template <typename T, bool VEC>
