@@ -162,12 +162,16 @@ size_t decode_partial_bytes(int batch, int seqlen_q, int num_heads_q, int head_d
 
 // The kv-cache entry runs on the decode kernel when the Sq x G query rows of a
 // KV head fit four column groups of 16 (one group when the fp16 V / 16 cache is
-// given); otherwise on the paged varlen prefill.
+// given and the prefill can take the group size); otherwise on the paged
+// varlen prefill.
 bool kvcache_on_decode(int batch, int seqlen_q, int num_heads_q, int num_heads_kv, int head_dim, bool v16) {
     if (num_heads_q <= 0 || num_heads_kv <= 0 || num_heads_q % num_heads_kv) return false;
     if (head_dim != 64 && head_dim != 128) return false;
     if (batch > 65535 || num_heads_kv > 65535) return false;
-    return (int64_t)seqlen_q * (num_heads_q / num_heads_kv) <= (v16 ? kDecodeMaxColumnsV16 : kDecodeMaxColumns);
+    const int G = num_heads_q / num_heads_kv;
+    // the prefill packs 128 / G tokens x G heads per query slot: other groups stay here
+    const bool prefill_ok = kPrefillSlotRows % G == 0;
+    return (int64_t)seqlen_q * G <= (v16 && prefill_ok ? kDecodeMaxColumnsV16 : kDecodeMaxColumns);
 }
 
 struct DecodeCall {
