@@ -22,7 +22,6 @@ enum : uint32_t {
     SRC_DECODE = 1u << 9,
     SRC_COMBINE = 1u << 10,
     SRC_PREFILL = 1u << 11,
-    SRC_SOFTMAX = 1u << 12,
 };
 
 __device__ __forceinline__ void record_error(uint32_t *err, uint32_t code) {
@@ -123,14 +122,6 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap *map, const void 
     asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
                      reinterpret_cast<uint64_t>(map)),
                  "r"(smem_u32(src)), "r"(c0), "r"(c1), "r"(c2)
-                 : "memory");
-}
-// untiled bulk copy global -> shared (16-byte aligned addresses, bytes a
-// multiple of 16), completion on an mbarrier
-__device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                     smem_u32(dst)),
-                 "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
                  : "memory");
 }
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
@@ -299,29 +290,6 @@ __device__ __forceinline__ void add2(float &d0, float &d1, float a0, float a1) {
         "add.rn.f32x2 rd, rd, ra;\nmov.b64 {%0, %1}, rd;\n}"
         : "+f"(d0), "+f"(d1)
         : "f"(a0), "f"(a1));
-}
-
-// thread-block cluster: this CTA's rank and the cluster's size (1 without a cluster)
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-__device__ __forceinline__ uint32_t cluster_nctarank() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
-    return r;
-}
-// store v into the shared-memory word of CTA `rank` of the cluster that sits at
-// the address `local` has in this CTA
-__device__ __forceinline__ void st_cluster_f32(const void *local, uint32_t rank, float v) {
-    uint32_t a = smem_u32(local), ra;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(a), "r"(rank));
-    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(ra), "f"(v) : "memory");
-}
-// every thread of every CTA of the cluster: stores before it are visible after it
-__device__ __forceinline__ void cluster_sync() {
-    asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
 __device__ __forceinline__ float ex2(float x) {
