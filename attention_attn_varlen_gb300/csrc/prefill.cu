@@ -159,6 +159,7 @@ __device__ __forceinline__ bool seq_rows(const PrefillParams &p, int b, bool rep
 // ---------------------------------------------------------------------------
 constexpr int kCvtThreads = 256;
 constexpr int kCvtKeys = 32;
+constexpr int kEarlyMaxKeys = 4096;   // longest key range for which the next unit is taken a unit ahead
 constexpr int kCvtUnroll = 8;   // 16-byte chunks each thread keeps in flight
 
 __device__ __forceinline__ void v_to_f16_keys(const PrefillParams &p) {
@@ -439,7 +440,13 @@ __device__ __noinline__ void pf_store_rows(const PrefillParams &p, const CUtenso
     }
 }
 
-template <int D>
+// EARLY: the producer takes and publishes the next unit's index at the start of
+// each unit, so every role has it a whole unit ahead (the unit boundary costs
+// less).  Otherwise it takes it when it starts the unit's loads, which keeps
+// the units of one sequence and KV head side by side in time, sharing their
+// K / V tiles through L2: the launcher chooses EARLY for short keys only, where
+// that sharing is worth little and the boundary costs weigh most.
+template <int D, bool EARLY>
 __global__ void __launch_bounds__(kPfThreads, 1)
     attn_prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                         const __grid_constant__ CUtensorMap vmap, const __grid_constant__ CUtensorMap omap,
@@ -518,20 +525,44 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         int it = 0, k = 0;
         uint32_t kpar = 0, vpar = 0, kused = 0, vused = 0;   // per stage: parity of the loads of each kind, any load
         bool ok = true;
+        // lane 0 (EARLY): publish the counter value v as unit kk's index (-1: none
+        // left) in the ring entry kk & 1 once every role has read the entry's
+        // previous index; -1 without publishing when that wait gives up
+        auto publish = [&](int kk, int v) {
+            const int q = kk >> 1;
+            if (q > 0 && !mbar_wait(&idx_empty[kk & 1], (uint32_t)(q - 1) & 1u, abort_flag, p.err, SRC_PREFILL))
+                return -1;
+            if (v >= num_units) v = -1;
+            unit_idx[kk & 1] = v;
+            mbar_arrive(&idx_full[kk & 1]);
+            return v;
+        };
+        int u_next = -1;   // EARLY: unit k's index, published during unit k - 1
+        if constexpr (EARLY) {
+            if (lane == 0) u_next = publish(0, atomicAdd(next_unit, 1));
+        }
         for (;; ++k) {
-            // next unit index (-1: none left) into the ring entry k & 1
             int u = -1;
-            if (lane == 0) {
-                const int q = k >> 1;
-                if (q == 0 || mbar_wait(&idx_empty[k & 1], (uint32_t)(q - 1) & 1u, abort_flag, p.err, SRC_PREFILL)) {
-                    u = atomicAdd(next_unit, 1);
-                    if (u >= num_units) u = -1;
-                    unit_idx[k & 1] = u;
-                    mbar_arrive(&idx_full[k & 1]);
+            if constexpr (EARLY) {
+                u = __shfl_sync(0xffffffffu, u_next, 0);
+            } else {
+                // next unit index (-1: none left) into the ring entry k & 1
+                if (lane == 0) {
+                    const int q = k >> 1;
+                    if (q == 0 ||
+                        mbar_wait(&idx_empty[k & 1], (uint32_t)(q - 1) & 1u, abort_flag, p.err, SRC_PREFILL)) {
+                        u = atomicAdd(next_unit, 1);
+                        if (u >= num_units) u = -1;
+                        unit_idx[k & 1] = u;
+                        mbar_arrive(&idx_full[k & 1]);
+                    }
                 }
+                u = __shfl_sync(0xffffffffu, u, 0);
             }
-            u = __shfl_sync(0xffffffffu, u, 0);
             if (u < 0 || !ok) break;
+            // EARLY: the next unit, taken now (its atomic lands while this unit's Q is set up)
+            int taken = -1;
+            if constexpr (EARLY) taken = lane == 0 ? atomicAdd(next_unit, 1) : -1;
             const PfUnit w = pf_unit(p, u);
             const int32_t *bt = paged ? p.block_table + (int64_t)w.b * p.bt_stride : nullptr;
             // Q of this unit once the previous unit's QK^T are done with the Q buffers
@@ -556,6 +587,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                 } else {
                     mbar_arrive(q_full);
                 }
+                if constexpr (EARLY) u_next = publish(k + 1, taken);
             }
             // ring order K_0, K_1, V_0, K_2, V_1, ..., K_{n-1}, V_{n-2}, V_{n-1}: each K tile
             // one step ahead of the V' tile it pairs with, so the next QK^T's tile can land
@@ -981,7 +1013,7 @@ cudaError_t launch_kvcache_cu(const int32_t *cache_seqlens, int batch, int seqle
     return cudaGetLastError();
 }
 
-template <int D>
+template <int D, bool EARLY>
 static cudaError_t launch_prefill_t(const CUtensorMap &qmap, const CUtensorMap &kmap, const CUtensorMap &vmap,
                                     const CUtensorMap &omap, const PrefillParams &p, cudaStream_t stream) {
     using S = PfSmem<D>;
@@ -993,7 +1025,7 @@ static cudaError_t launch_prefill_t(const CUtensorMap &qmap, const CUtensorMap &
     if (dev < 0 || dev >= kMaxDev) return cudaErrorInvalidDevice;
     std::call_once(attr_once[dev], [&] {
         attr_err[dev] =
-            cudaFuncSetAttribute(attn_prefill_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kBytes);
+            cudaFuncSetAttribute(attn_prefill_kernel<D, EARLY>, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kBytes);
     });
     if (attr_err[dev] != cudaSuccess) return attr_err[dev];
     // unit list and V' in one launch: grid row 0 holds the scheduler (dispatched
@@ -1003,15 +1035,19 @@ static cudaError_t launch_prefill_t(const CUtensorMap &qmap, const CUtensorMap &
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     main_kernel_event_before(stream);
-    attn_prefill_kernel<D><<<p.num_ctas, kPfThreads, S::kBytes, stream>>>(qmap, kmap, vmap, omap, p);
+    attn_prefill_kernel<D, EARLY><<<p.num_ctas, kPfThreads, S::kBytes, stream>>>(qmap, kmap, vmap, omap, p);
     main_kernel_event_after(stream);
     return cudaGetLastError();
 }
 
 cudaError_t launch_prefill(const CUtensorMap &qmap, const CUtensorMap &kmap, const CUtensorMap &vmap,
                            const CUtensorMap &omap, const PrefillParams &p, int head_dim, cudaStream_t stream) {
-    if (head_dim == 128) return launch_prefill_t<128>(qmap, kmap, vmap, omap, p, stream);
-    return launch_prefill_t<64>(qmap, kmap, vmap, omap, p, stream);
+    // the next unit taken a unit ahead when keys are short (each unit's K / V is
+    // small, so its siblings gain little from sharing it through L2)
+    if (head_dim == 128)
+        return p.max_seqlen_k <= kEarlyMaxKeys ? launch_prefill_t<128, true>(qmap, kmap, vmap, omap, p, stream)
+                                               : launch_prefill_t<128, false>(qmap, kmap, vmap, omap, p, stream);
+    return launch_prefill_t<64, false>(qmap, kmap, vmap, omap, p, stream);
 }
 
 }  // namespace attn

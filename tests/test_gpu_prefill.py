@@ -69,6 +69,23 @@ def test_varlen_matches_oracle(seed, lq, lk, Hq, Hkv, D, causal):
         assert_lse_close(lse.t().contiguous(), ref_lse.reshape(-1, Hq), "varlen lse")
 
 
+def test_unit_order_does_not_change_the_result():
+    """Short key ranges take the next unit a whole unit ahead, long ones later: the
+    same inputs with max_seqlen_k at the true maximum (1900) and raised past that
+    threshold (5000) run the two forms; each unit's result does not depend on
+    which CTA computes it or when, so the outputs agree bit for bit."""
+    cfg = workloads.small_varlen(95, [300, 1900, 40, 700, 1], [300, 1900, 40, 700, 1], 32, 8, 128, True)
+    q, k, v = cfg.q().cuda(), cfg.k().cuda(), cfg.v().cuda()
+    cu_q, cu_k = torch.from_numpy(cfg.cu_q).cuda(), torch.from_numpy(cfg.cu_k).cuda()
+    av.get_last_device_error()
+    o1, l1 = av.attn_varlen_fwd(q, k, v, cu_q, cu_k, 1900, 1900, cfg.scale, causal=True, return_lse=True)
+    o2, l2 = av.attn_varlen_fwd(q, k, v, cu_q, cu_k, 1900, 5000, cfg.scale, causal=True, return_lse=True)
+    torch.cuda.synchronize()
+    assert av.get_last_device_error()[0] == 0
+    assert torch.equal(o1.view(torch.int16), o2.view(torch.int16))
+    assert torch.equal(l1, l2)
+
+
 def test_varlen_strided_qkv_views():
     """q, k, v as views of one packed [tokens, Hq + 2 Hkv, D] projection."""
     lens = np.array([300, 129])
