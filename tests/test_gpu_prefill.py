@@ -69,6 +69,32 @@ def test_varlen_matches_oracle(seed, lq, lk, Hq, Hkv, D, causal):
         assert_lse_close(lse.t().contiguous(), ref_lse.reshape(-1, Hq), "varlen lse")
 
 
+SHORT_Q_CASES = [
+    # a few queries per sequence (each <= 128 / G, one query slot) against longer
+    # keys: one key tile, odd and even tile counts, rows that see no key (Lq > Lk,
+    # causal), an empty sequence
+    (96, [1, 5, 32, 0, 17, 32, 9], [1, 130, 4000, 0, 17, 257, 3], 32, 8, 128),
+    (97, [64, 3, 64, 1], [64, 640, 1000, 2048], 16, 8, 64),
+    (98, [8, 8, 8], [2049, 100, 7000], 32, 8, 128),
+]
+
+
+@pytest.mark.parametrize("causal", [True, False])
+@pytest.mark.parametrize("seed,lq,lk,Hq,Hkv,D", SHORT_Q_CASES)
+def test_short_queries_against_long_keys_match_oracle(seed, lq, lk, Hq, Hkv, D, causal):
+    """Decode-like varlen calls: every unit has a single active query slot."""
+    cfg = workloads.small_varlen(seed, lq, lk, Hq, Hkv, D, causal)
+    assert max(lq) * (Hq // Hkv) <= 128
+    q, k, v = cfg.q(), cfg.k(), cfg.v()
+    av.get_last_device_error()
+    out, lse = run_contig(cfg, q, k, v, causal)
+    torch.cuda.synchronize()
+    assert av.get_last_device_error()[0] == 0
+    ref, ref_lse = oracle.attn_varlen(q, k, v, cfg.cu_q, cfg.cu_k, Hq, Hkv, D, cfg.scale, causal)
+    assert_close(out, ref.reshape(out.shape), f"short-q varlen {lq}/{lk}")
+    assert_lse_close(lse.t().contiguous(), ref_lse.reshape(-1, Hq), "short-q varlen lse")
+
+
 def test_unit_order_does_not_change_the_result():
     """Short key ranges take the next unit a whole unit ahead, long ones later: the
     same inputs with max_seqlen_k at the true maximum (1900) and raised past that
