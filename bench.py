@@ -457,6 +457,16 @@ def bench_prefix(av, device, steps, warmup, flush, peaks, with_oracle=True):
     ms_store, kms_store = time_steps(store, steps, flush, kernel=True)
     flops = workloads.prefill_flops(cfg.new, cfg.lens_k, cfg.Hq, cfg.D)
     sbytes = workloads.store_bytes(int(cfg.new.sum()), cfg.Hkv, cfg.D, v16=True)
+    # the attention call's algorithmic bytes: q and out once, every distinct cache row
+    # the block tables reach read once as K (bf16) and V / 16 (fp16)
+    rows_used = {}
+    for b in range(cfg.batch):
+        lk = int(cfg.lens_k[b])
+        for i in range((lk + cfg.block_size - 1) // cfg.block_size):
+            blk = int(cfg.block_table[b, i])
+            rows_used[blk] = max(rows_used.get(blk, 0), min(cfg.block_size, lk - i * cfg.block_size))
+    distinct_rows = sum(rows_used.values())
+    abytes = (2 * int(cfg.new.sum()) * cfg.Hq * cfg.D * 2) + distinct_rows * cfg.Hkv * cfg.D * 2 * 2
     t = float(np.mean(ms)) / 1e3
     ta = float(np.mean(ms_attn)) / 1e3
     tk = float(np.mean(kms_attn)) / 1e3
@@ -488,6 +498,12 @@ def bench_prefix(av, device, steps, warmup, flush, peaks, with_oracle=True):
                         "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                         "frac": flops / tk / 1e12 / peaks["bf16_tflops"], "kernel_ms": tk * 1e3,
                         "traffic": ncu_traffic("prefill_paged", float(cfg.new.sum()))},
+           # C3 has both bounds: the HBM side of the same kernel time, and t_min / t with
+           # t_min = max(FLOPs / bf16 peak, bytes / copy bandwidth)
+           "hbm": {"algorithmic_bytes": abytes, "distinct_cache_rows": distinct_rows,
+                   "achieved": abytes / tk / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                   "frac": abytes / tk / 1e9 / peaks["hbm_gbs"]},
+           "roofline_tmin_frac": max(flops / (peaks["bf16_tflops"] * 1e12), abytes / (peaks["hbm_gbs"] * 1e9)) / tk,
            "store_kvcache": {"workload": "the step's 8503 new tokens: K, V and the fp16 V/16 row of each",
                              "value": sbytes / ts / 1e9, "unit": "GB/s", "ms_per_step": ts * 1e3,
                              "algorithmic_bytes": sbytes,
@@ -768,7 +784,9 @@ def summary(line, peaks, peak_src):
     c3 = line.get("prefix_prefill")
     if c3:
         put("c3", c3, c3.get("oracle"), {"step_frac": _r(c3["value"] / peaks["bf16_tflops"], 3),
-                                         "no_v16": _r(c3["without_v16_cache"]["value"])})
+                                         "no_v16": _r(c3["without_v16_cache"]["value"]),
+                                         "hbm_frac": _r(c3["hbm"]["frac"], 3),
+                                         "tmin_frac": _r(c3["roofline_tmin_frac"], 3)})
         put("c3_store", c3["store_kvcache"])
         put("store_8x", c3.get("store_kvcache_8x"))
     c4 = line.get("decode")
