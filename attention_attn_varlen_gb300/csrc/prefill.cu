@@ -334,6 +334,9 @@ __device__ __forceinline__ void schedule_units(const PrefillParams &p) {
 // scheduler's CTA alone.
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(kCvtThreads) attn_prefill_prep_kernel(const PrefillParams p) {
+    // the attention kernel may be scheduled now (it waits for this grid before
+    // reading anything it writes)
+    asm volatile("griddepcontrol.launch_dependents;");
     if (p.v16_paged || blockIdx.y == 0) {
         // the scheduler (grid row 0, dispatched first); with a paged V' cache there is
         // nothing to convert and the launch is this one CTA
@@ -481,7 +484,6 @@ __global__ void __launch_bounds__(kPfThreads, 1)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G = p.G;
-    const int num_units = p.unit_count[0];
     int *next_unit = p.unit_count + 1;   // zeroed by the scheduler
 
     if (threadIdx.x == 0) {
@@ -512,6 +514,10 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    // launched as a programmatic dependent of the pre-pass: everything above ran
+    // while it finished; its unit list (and V') are read only after this
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const int num_units = p.unit_count[0];
 
     if (warp == 8) {
         // ================================================================ TMA producer
@@ -1035,9 +1041,25 @@ static cudaError_t launch_prefill_t(const CUtensorMap &qmap, const CUtensorMap &
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     main_kernel_event_before(stream);
-    attn_prefill_kernel<D, EARLY><<<p.num_ctas, kPfThreads, S::kBytes, stream>>>(qmap, kmap, vmap, omap, p);
+    // a programmatic dependent launch: the kernel's prologue overlaps the pre-pass's end
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = dim3(p.num_ctas);
+    cfg.blockDim = dim3(kPfThreads);
+    cfg.dynamicSmemBytes = S::kBytes;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, attn_prefill_kernel<D, EARLY>, qmap, kmap, vmap, omap, p);
+    if (e == cudaErrorNotSupported || e == cudaErrorInvalidValue) {
+        (void)cudaGetLastError();
+        attn_prefill_kernel<D, EARLY><<<p.num_ctas, kPfThreads, S::kBytes, stream>>>(qmap, kmap, vmap, omap, p);
+        e = cudaGetLastError();
+    }
     main_kernel_event_after(stream);
-    return cudaGetLastError();
+    return e;
 }
 
 cudaError_t launch_prefill(const CUtensorMap &qmap, const CUtensorMap &kmap, const CUtensorMap &vmap,
