@@ -2,9 +2,11 @@
 // algorithm of "从零实现 vLLM (1.3)：如何加速 Attention 计算", section
 // 减少遍历次数的“在线 Softmax”: pass 1 keeps the running maximum m and the proxy
 // denominator d' = d' * e^(m_old - m_new) + e^(x - m_new); pass 2 writes
-// y = e^(x - m) / d'.  The update runs on 16-byte vectors (the vector's max
-// first, then its terms), which is the same recurrence over blocks of 4 or 8
-// elements.  Partial (m, d') states of threads merge exactly:
+// y = e^(x - m) / d'.  The update runs on blocks of elements, the same
+// recurrence in exact arithmetic: per 16-byte vector (its max first, then its
+// terms) in the warp and two-pass kernels, and over all of a thread's elements
+// at once (their max first, then one sum) where the row sits in registers.
+// Partial (m, d') states of threads merge exactly:
 //   m = max(m1, m2),  d' = d1 e^(m1 - m) + d2 e^(m2 - m).
 //
 // HBM-bound; every path below reads the matrix once and writes it once except
@@ -521,7 +523,8 @@ __global__ void __launch_bounds__(NT) softmax_rows_cta_reg_kernel(const T *x, T 
 }
 
 // ---------------------------------------------------------------------------
-// one CTA per row, two passes over the row
+// one CTA per row, two passes over the row (rows past 512 KB, or not 16-byte
+// aligned)
 // ---------------------------------------------------------------------------
 // NT threads per CTA: 256 for rows of up to 32 KB (more rows in flight per SM),
 // 512 beyond

@@ -368,7 +368,8 @@ ATTN_API size_t attn_kvcache_workspace_size(int batch, int seqlen_q, int num_hea
  * attn_softmax_rows -- y = softmax(x) along every row of a matrix, with the
  * online two-pass algorithm of the article's section 减少遍历次数的“在线
  * Softmax”: pass 1 runs the maximum m and the proxy denominator
- * d' = d' * e^(m_old - m_new) + e^(x - m_new) in one sweep, pass 2 writes
+ * d' = d' * e^(m_old - m_new) + e^(x - m_new) (partial (m, d') pairs of
+ * threads, warps and CTAs merge by the same rule), pass 2 writes
  * e^(x - m) / d'.  Arithmetic in fp32; no overflow for any finite input.
  *
  *   x, y          [rows, cols], row strides x_row_stride / y_row_stride in
@@ -377,8 +378,12 @@ ATTN_API size_t attn_kvcache_workspace_size(int batch, int seqlen_q, int num_hea
  *                 y bfloat16, y rounded to nearest even)
  * A row whose maximum is not finite (all -inf, or a +inf or NaN in it) gives
  * NaN, as the definition does.  HBM-bound: one read and one write of the
- * matrix for rows up to 1024 (fp32) / 2048 (bf16) elements; longer rows are
- * read twice, the second time mostly from L2.
+ * matrix for 16-byte-aligned rows of up to 512 KB (a warp, a CTA or a
+ * thread-block cluster per row, the row held on chip between the passes);
+ * longer or unaligned rows are read twice, the second time mostly from L2.
+ * A bounded wait that gives up (rows up to 16 KB, streamed through shared
+ * memory) is reported by attn_get_last_device_error as
+ * ATTN_ERR_DEVICE_TIMEOUT.
  * ------------------------------------------------------------------------ */
 enum { ATTN_DTYPE_F32 = 0, ATTN_DTYPE_BF16 = 1 };
 
