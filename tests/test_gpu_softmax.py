@@ -87,3 +87,21 @@ def test_softmax_rows_online_recurrence_on_the_article_example():
     ref, m_trace, _ = oracle.softmax_online(x.numpy()[0])
     np.testing.assert_allclose(y, ref, rtol=1e-5)
     assert m_trace[-1] == 12.0
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("rows,cols,dt", [(32768, 8192, "f32"), (262144, 1024, "bf16"), (4096, 65536, "f32")])
+def test_softmax_bench_shapes_sampled_rows(rows, cols, dt):
+    """The bench's three shapes at full size (the kernels it times: a CTA per row, a
+    warp per row, a cluster per row), 64 sampled rows against the oracle."""
+    g = torch.Generator(device="cuda").manual_seed(1234 + rows)
+    x = torch.randn(rows, cols, device="cuda", generator=g) * 30.0
+    if dt == "bf16":
+        x = x.to(torch.bfloat16)
+    y = av.softmax_rows(x)
+    torch.cuda.synchronize()
+    pick = torch.from_numpy(np.sort(np.random.default_rng(rows).choice(rows, 64, replace=False))).cuda()
+    xs = x[pick].cpu()
+    _check(y[pick], oracle.softmax_rows(xs), dt == "bf16")
+    del x, y
+    torch.cuda.empty_cache()
