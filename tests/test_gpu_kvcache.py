@@ -233,10 +233,12 @@ def test_kvcache_c4_four_tokens_full_size_sampled():
 
 
 @pytest.mark.slow
-def test_kvcache_c4_eight_tokens_v16_full_size_sampled():
-    """The 8-token kv-cache step at full size with the fp16 V / 16 cache (32 query
-    columns per KV head, two column groups), as the benchmark times it; the
-    oracle checks 12 sequences."""
+@pytest.mark.parametrize("use16", [False, True])
+def test_kvcache_c4_eight_tokens_full_size_sampled(use16):
+    """The 8-token kv-cache step at full size (32 query columns per KV head), as
+    the benchmark times it: without the fp16 V / 16 cache on the decode kernel in
+    two column-group CTAs, with it on the paged prefill; the oracle checks 12
+    sequences."""
     from test_gpu_decode import poison_tail
     cfg = workloads.make("c4_decode")
     Sq = 8
@@ -244,7 +246,7 @@ def test_kvcache_c4_eight_tokens_v16_full_size_sampled():
     vc = torch.empty_like(kc)
     workloads.fill_paged_cache(cfg, kc, vc)
     poison_tail(cfg, kc, vc)
-    v16 = v16_of(vc)
+    v16 = v16_of(vc) if use16 else None
     rng = np.random.default_rng(8642)
     q8 = torch.from_numpy(rng.standard_normal((cfg.batch, Sq, cfg.Hq, cfg.D), dtype=np.float32)).to(torch.bfloat16)
     cs = torch.from_numpy(cfg.ctx.astype(np.int32)).cuda()
@@ -262,8 +264,9 @@ def test_kvcache_c4_eight_tokens_v16_full_size_sampled():
     ref, ref_lse = oracle.attn_varlen(q8[seqs].reshape(-1, cfg.Hq, cfg.D), kp, vp, cu_q, cu_k, cfg.Hq, cfg.Hkv,
                                       cfg.D, cfg.scale, True, block_table=btc, block_size=cfg.block_size,
                                       num_blocks=kp.shape[0])
-    assert_close(out[seqs].reshape(-1, cfg.Hq, cfg.D), ref.reshape(-1, cfg.Hq, cfg.D), "c4 cache, 8 new tokens, v16")
+    what = "c4 cache, 8 new tokens" + (", v16" if use16 else "")
+    assert_close(out[seqs].reshape(-1, cfg.Hq, cfg.D), ref.reshape(-1, cfg.Hq, cfg.D), what)
     got_lse = lse.view(cfg.Hq, cfg.batch, Sq)[:, seqs].reshape(cfg.Hq, -1).t().contiguous()
-    assert_lse_close(got_lse, ref_lse.reshape(-1, cfg.Hq), "c4 cache, 8 new tokens, v16, lse")
+    assert_lse_close(got_lse, ref_lse.reshape(-1, cfg.Hq), what + ", lse")
     del kc, vc, v16
     torch.cuda.empty_cache()

@@ -80,3 +80,27 @@ def test_padded_length_beyond_padding_is_reported():
     torch.cuda.synchronize()
     st, word = av.get_last_device_error()
     assert st == 6, (st, hex(word))   # ATTN_ERR_DEVICE_INDEX
+
+
+@pytest.mark.slow
+def test_padded_c2_full_size_equals_varlen():
+    """The benchmark's padded batch: c2_varlen_gqa as [16, 4096, H, D] with the
+    per-sequence lengths and NaN in the padding; the real rows equal the varlen
+    call on the packed tensors bit for bit (that call is checked against the
+    oracle at this size by the prefill tests)."""
+    cfg = workloads.make("c2_varlen_gqa")
+    S = 4096
+    q, k, v = cfg.q(), cfg.k(), cfg.v()
+    qp, kp, vp = _pad(q, cfg.cu_q, S).cuda(), _pad(k, cfg.cu_k, S).cuda(), _pad(v, cfg.cu_k, S).cuda()
+    sq = torch.from_numpy(cfg.lens_q.astype(np.int32)).cuda()
+    sk = torch.from_numpy(cfg.lens_k.astype(np.int32)).cuda()
+    av.get_last_device_error()
+    out_p = av.attn_padded_fwd(qp, kp, vp, sq, sk, cfg.scale)
+    out_v = av.attn_varlen_fwd(q.cuda(), k.cuda(), v.cuda(), torch.from_numpy(cfg.cu_q).cuda(),
+                               torch.from_numpy(cfg.cu_k).cuda(), int(cfg.lens_q.max()), int(cfg.lens_k.max()),
+                               cfg.scale)
+    torch.cuda.synchronize()
+    assert av.get_last_device_error()[0] == 0
+    assert torch.equal(_real_rows(out_p, cfg.cu_q).view(torch.int16), out_v.view(torch.int16))
+    del qp, kp, vp, out_p, out_v
+    torch.cuda.empty_cache()

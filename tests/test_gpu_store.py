@@ -110,3 +110,38 @@ def test_store_kvcache_v_beyond_fp16_range_is_reported():
     st, word = av.get_last_device_error()
     assert st == 8 and word & 4
     assert torch.isfinite(v16.float()).all() and v16[2, 1, 5].item() == 65504.0
+
+
+@pytest.mark.slow
+def test_store_kvcache_bench_8x_tokens():
+    """The benchmark's 8x store: 8 x the c3 step's new tokens (68,024) into random
+    distinct slots, with the V/16 cache, the launch configuration the benchmark
+    times (its grid follows the token count); a smaller pool than the benchmark's
+    65,536 blocks keeps the test's memory down.  Every written slot is compared
+    with the oracle's copy bit for bit, on a sample of slots."""
+    cfg = workloads.make("c3_prefix_paged")
+    n = 8 * int(cfg.new.sum())
+    Hkv, D, num_slots = cfg.Hkv, cfg.D, 1 << 20
+    slots = np.random.default_rng(cfg.seed + 14).choice(num_slots, n, replace=False).astype(np.int64)
+    k_h = workloads.normal_bf16((9, 1), n, Hkv * D).view(n, Hkv, D)
+    v_h = workloads.normal_bf16((9, 2), n, Hkv * D).view(n, Hkv, D)
+    kc = torch.zeros((num_slots, Hkv, D), dtype=torch.bfloat16, device="cuda")
+    vc = torch.zeros_like(kc)
+    v16 = torch.zeros((num_slots, Hkv, D), dtype=torch.float16, device="cuda")
+    av.get_last_device_error()
+    av.store_kvcache(k_h.cuda(), v_h.cuda(), kc, vc, torch.from_numpy(slots).cuda(), v16_cache=v16)
+    torch.cuda.synchronize()
+    assert av.get_last_device_error()[0] == 0
+    pick = np.sort(np.random.default_rng(3).choice(n, 4096, replace=False))
+    sl = torch.from_numpy(slots[pick])
+    # the oracle's copy loop on the sampled tokens into a compact pool of their slots
+    ref_k, ref_v = oracle.store_kvcache(k_h[pick].contiguous(), v_h[pick].contiguous(),
+                                        torch.zeros((len(pick), Hkv, D), dtype=torch.bfloat16),
+                                        torch.zeros((len(pick), Hkv, D), dtype=torch.bfloat16),
+                                        np.arange(len(pick), dtype=np.int64))
+    assert np.array_equal(_bits(kc[sl.cuda()]), ref_k.reshape(len(pick), Hkv, D))
+    assert np.array_equal(_bits(vc[sl.cuda()]), ref_v.reshape(len(pick), Hkv, D))
+    assert torch.equal(v16[sl.cuda()].cpu().view(torch.int16),
+                       (v_h[pick].float() / 16.0).half().view(torch.int16))
+    del kc, vc, v16
+    torch.cuda.empty_cache()
