@@ -41,30 +41,36 @@ namespace attn {
 
 constexpr int kDecThreads = 160;   // 4 consumer warps + 1 producer warp
 constexpr int kDecTile = 64;       // tokens per ring stage
-constexpr int kDecStages = 3;
 
-template <int D>
+// QS: the CTA's query columns live in shared memory (read by ldmatrix per tile)
+// instead of in every consumer's registers, which lets three CTAs share an SM;
+// each then keeps two ring stages instead of three
+template <int D, bool QS = false>
 struct DecSmem {
+    static constexpr int kStages = QS ? 2 : 3;
     static constexpr int kPanels = D / 64;
     static constexpr int kPanelBytes = kDecTile * 128;             // 64 rows x 128 B
     static constexpr int kStageBytes = 2 * kPanels * kPanelBytes;  // K then V
-    static constexpr int kRingBytes = kDecStages * kStageBytes;
-    static constexpr int kBytes = kRingBytes + 1024 /*align slack*/ + 64 /*barriers*/;
+    static constexpr int kRingBytes = kStages * kStageBytes;
+    static constexpr int kQBytes = QS ? 16 * D * 2 : 0;            // 16 query columns x D bf16, swizzled
+    static constexpr int kBytes = kRingBytes + kQBytes + 1024 /*align slack*/ + 64 /*barriers*/;
 };
 
 
 // VH: V tiles come from the fp16 V / 16 cache; PV then multiplies them by one fp16
 // term P' = 16 P (11 significant bits) instead of P's bf16 hi + lo terms.
-template <int D, int NT, bool VH>
-__global__ void __launch_bounds__(kDecThreads) attn_decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
-                                                                       const __grid_constant__ CUtensorMap vmap,
-                                                                       const DecodeParams p) {
-    using S = DecSmem<D>;
+template <int D, int NT, bool VH, bool QS>
+__global__ void __launch_bounds__(kDecThreads, QS ? 3 : 0) attn_decode_split_kernel(
+    const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap, const DecodeParams p) {
+    using S = DecSmem<D, QS>;
+    constexpr int kDecStages = S::kStages;
+    static_assert(!QS || NT == 2, "query columns in shared memory: two n8 tiles");
     constexpr int KS = D / 16;       // k-steps of the QK^T product
     constexpr int NC = 8 * NT;       // query columns, padded to whole n8 tiles
     extern __shared__ uint8_t dsmem_raw[];
     uint8_t *ring = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(dsmem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t *full = reinterpret_cast<uint64_t *>(ring + S::kRingBytes);
+    uint8_t *sQ = ring + S::kRingBytes;   // QS: [16 columns][D], 16-byte chunks XOR-swizzled by column
+    uint64_t *full = reinterpret_cast<uint64_t *>(ring + S::kRingBytes + S::kQBytes);
     uint64_t *empty = full + kDecStages;
     volatile int *abort_flag = reinterpret_cast<volatile int *>(empty + kDecStages);
 
@@ -160,7 +166,24 @@ __global__ void __launch_bounds__(kDecThreads) attn_decode_split_kernel(const __
     // ---------------------------------------------------------------- consumers
     const int g = lane >> 2, c = lane & 3;
     // Q^T as B fragments of n-tile nt: b0 = Q[n=8nt+g][16ks + 2c .. +1], b1 = Q[8nt+g][16ks + 2c + 8 .. +9]
-    uint32_t qf[NT][KS][2];
+    uint32_t qf[QS ? 1 : NT][QS ? 1 : KS][2];
+    if constexpr (QS) {
+        // the CTA's 16 query columns into shared memory: row n (column c0 + n, zeros
+        // past NQ) holds its D values, 16-byte chunk ch at chunk ch ^ (n & 7)
+        for (int i = threadIdx.x; i < 16 * (D / 8); i += 128) {
+            const int n = i / (D / 8), ch = i % (D / 8);
+            uint4 v = make_uint4(0u, 0u, 0u, 0u);
+            if (n < NQ) {
+                const int gn = c0 + n;
+                const uint32_t *src = reinterpret_cast<const uint32_t *>(
+                    p.q + ((int64_t)b * p.Sq + gn / p.G) * p.q_row_stride + (int64_t)(hkv * p.G + gn % p.G) * D) +
+                                      ch * 4;
+                v = make_uint4(__ldg(src), __ldg(src + 1), __ldg(src + 2), __ldg(src + 3));
+            }
+            *reinterpret_cast<uint4 *>(sQ + n * (D * 2) + ((ch ^ (n & 7)) << 4)) = v;
+        }
+        asm volatile("bar.sync 1, 128;" ::: "memory");
+    }
     // keys at or past kend[nt][j] are masked for this lane's column 8nt + 2c + j:
     // the end of the split and, causally, the bottom-right limit L - Sq + t + 1
     int kend[NT][2];
@@ -169,13 +192,15 @@ __global__ void __launch_bounds__(kDecThreads) attn_decode_split_kernel(const __
         const int n = nt * 8 + g;
         const bool valid = n < NQ;
         const int gn = c0 + n;
-        const int64_t qrow_idx = (int64_t)b * p.Sq + (valid ? gn / p.G : 0);
-        const uint32_t *qrow = reinterpret_cast<const uint32_t *>(p.q + qrow_idx * p.q_row_stride +
-                                                                  (int64_t)(hkv * p.G + (valid ? gn % p.G : 0)) * D);
+        if constexpr (!QS) {
+            const int64_t qrow_idx = (int64_t)b * p.Sq + (valid ? gn / p.G : 0);
+            const uint32_t *qrow = reinterpret_cast<const uint32_t *>(
+                p.q + qrow_idx * p.q_row_stride + (int64_t)(hkv * p.G + (valid ? gn % p.G : 0)) * D);
 #pragma unroll
-        for (int ks = 0; ks < KS; ++ks) {
-            qf[nt][ks][0] = valid ? __ldg(qrow + ks * 8 + c) : 0u;
-            qf[nt][ks][1] = valid ? __ldg(qrow + ks * 8 + 4 + c) : 0u;
+            for (int ks = 0; ks < KS; ++ks) {
+                qf[nt][ks][0] = valid ? __ldg(qrow + ks * 8 + c) : 0u;
+                qf[nt][ks][1] = valid ? __ldg(qrow + ks * 8 + 4 + c) : 0u;
+            }
         }
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
@@ -231,8 +256,19 @@ __global__ void __launch_bounds__(kDecThreads) attn_decode_split_kernel(const __
                 uint32_t a0, a1, a2, a3;
                 const uint32_t addr = kb + (ks / 4) * S::kPanelBytes + sw128_off(arow, (ks % 4) * 2 + (lane >> 4));
                 ldsm_x4(addr, a0, a1, a2, a3);
+                if constexpr (QS) {
+                    // Q^T B fragments of both n8 tiles: matrix m = lane / 8 is column block
+                    // m / 2, k half m % 2 of this k-step
+                    const int qn = ((lane >> 4) << 3) + (lane & 7), qch = 2 * ks + ((lane >> 3) & 1);
+                    uint32_t b00, b01, b10, b11;
+                    ldsm_x4(smem_u32(sQ) + qn * (D * 2) + ((qch ^ (qn & 7)) << 4), b00, b01, b10, b11);
+                    mma_bf16_16816(acc[0], a0, a1, a2, a3, b00, b01);
+                    mma_bf16_16816(acc[1], a0, a1, a2, a3, b10, b11);
+                } else {
 #pragma unroll
-                for (int nt = 0; nt < NT; ++nt) mma_bf16_16816(acc[nt], a0, a1, a2, a3, qf[nt][ks][0], qf[nt][ks][1]);
+                    for (int nt = 0; nt < NT; ++nt)
+                        mma_bf16_16816(acc[nt], a0, a1, a2, a3, qf[nt][ks][0], qf[nt][ks][1]);
+                }
             }
             const int key0 = tok0 + r0 + g, key1 = key0 + 8;
             uint32_t bp[NT][2], bl[NT][2];
@@ -447,10 +483,10 @@ __global__ void __launch_bounds__(128) attn_decode_combine_kernel(const DecodePa
             Ls > 0.f ? (M + __log2f(Ls)) * 0.69314718055994531f : -INFINITY;
 }
 
-template <int D, int NT, bool VH>
+template <int D, int NT, bool VH, bool QS = false>
 static cudaError_t launch_decode_t(const CUtensorMap &kmap, const CUtensorMap &vmap, const DecodeParams &p,
                                    int batch, cudaStream_t stream) {
-    using S = DecSmem<D>;
+    using S = DecSmem<D, QS>;
     static std::once_flag attr_once[kMaxDev];
     static cudaError_t attr_err[kMaxDev];
     int dev = 0;
@@ -458,13 +494,13 @@ static cudaError_t launch_decode_t(const CUtensorMap &kmap, const CUtensorMap &v
     if (e0 != cudaSuccess) return e0;
     if (dev < 0 || dev >= kMaxDev) return cudaErrorInvalidDevice;
     std::call_once(attr_once[dev], [&] {
-        attr_err[dev] = cudaFuncSetAttribute(attn_decode_split_kernel<D, NT, VH>,
+        attr_err[dev] = cudaFuncSetAttribute(attn_decode_split_kernel<D, NT, VH, QS>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, S::kBytes);
     });
     if (attr_err[dev] != cudaSuccess) return attr_err[dev];
     dim3 grid(p.num_splits * p.ncg, p.Hkv, batch);
     main_kernel_event_before(stream);
-    attn_decode_split_kernel<D, NT, VH><<<grid, kDecThreads, S::kBytes, stream>>>(kmap, vmap, p);
+    attn_decode_split_kernel<D, NT, VH, QS><<<grid, kDecThreads, S::kBytes, stream>>>(kmap, vmap, p);
     main_kernel_event_after(stream);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess || p.num_splits == 1) return e;
@@ -476,6 +512,9 @@ static cudaError_t launch_decode_t(const CUtensorMap &kmap, const CUtensorMap &v
 cudaError_t launch_decode(const CUtensorMap &kmap, const CUtensorMap &vmap, const DecodeParams &p, int batch,
                           int head_dim, cudaStream_t stream) {
     const bool two = p.Sq * p.G > 8;
+    // several column groups (more than 16 query columns per KV head): their CTAs
+    // read the same tiles, and three per SM keep more consumer warps in flight
+    const bool qs = p.ncg > 1;
     if (p.v16) {
         if (head_dim == 128)
             return two ? launch_decode_t<128, 2, true>(kmap, vmap, p, batch, stream)
@@ -484,7 +523,8 @@ cudaError_t launch_decode(const CUtensorMap &kmap, const CUtensorMap &vmap, cons
                    : launch_decode_t<64, 1, true>(kmap, vmap, p, batch, stream);
     }
     if (head_dim == 128)
-        return two ? launch_decode_t<128, 2, false>(kmap, vmap, p, batch, stream)
+        return two ? (qs ? launch_decode_t<128, 2, false, true>(kmap, vmap, p, batch, stream)
+                         : launch_decode_t<128, 2, false>(kmap, vmap, p, batch, stream))
                    : launch_decode_t<128, 1, false>(kmap, vmap, p, batch, stream);
     return two ? launch_decode_t<64, 2, false>(kmap, vmap, p, batch, stream)
                : launch_decode_t<64, 1, false>(kmap, vmap, p, batch, stream);
