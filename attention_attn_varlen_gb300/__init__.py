@@ -76,6 +76,8 @@ def lib():
     L.attn_get_last_device_error.restype = _i32
     L.attn_abi_version.argtypes = []
     L.attn_abi_version.restype = _i32
+    L.attn_selftest_bounded_wait.argtypes = [_vp, _c.POINTER(_c.c_ulonglong)]
+    L.attn_selftest_bounded_wait.restype = _i32
     L.attn_kvcache_fwd.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _i32,
                                    _i64, _i32, _f32, _i32, _vp, _vp, _sz, _vp]
     L.attn_kvcache_fwd.restype = _i32
@@ -484,6 +486,16 @@ def set_kernel_events(before=None, after=None) -> None:
     if not before.cuda_event or not after.cuda_event:
         raise ValueError("events have no CUDA event handle")
     lib().attn_set_kernel_events(ctypes.c_void_p(before.cuda_event), ctypes.c_void_p(after.cuda_event))
+
+
+def selftest_bounded_wait(stream=None) -> dict:
+    """Run the library's failure-detection self-test (a bounded wait that runs
+    out on purpose; see attn_selftest_bounded_wait).  Returns the two waiters'
+    success flags and waited nanoseconds; the device error word then holds the
+    timeout."""
+    res = (ctypes.c_ulonglong * 4)()
+    _check(lib().attn_selftest_bounded_wait(_stream(stream), res), "attn_selftest_bounded_wait")
+    return {"first_ok": bool(res[0]), "first_ns": int(res[1]), "second_ok": bool(res[2]), "second_ns": int(res[3])}
 
 
 def get_last_device_error(stream=None) -> tuple[int, int]:

@@ -262,6 +262,47 @@ attn_status decode_launch(const DecodeCall &c, const DevInfo *d, int splits, int
 
 }  // namespace
 
+// ---------------------------------------------------------------------------
+// Failure-detection self-test (attn_selftest_bounded_wait).  One CTA, two
+// warps.  Lane 0 of warp 0 waits on an mbarrier that nothing completes: its
+// bounded wait gives up after the wait limit, records a timeout in the error
+// word and raises the CTA's abort flag.  Lane 0 of warp 1 first idles for
+// half that limit, then waits on another such mbarrier with the same abort
+// flag: it must give up as soon as it sees the flag, before its own limit.
+// Each records whether its wait succeeded and how long it waited.
+// ---------------------------------------------------------------------------
+namespace attn {
+namespace {
+constexpr uint32_t SRC_SELFTEST = 1u << 13;
+static __device__ unsigned long long g_selftest_out[4];
+
+__global__ void __launch_bounds__(64) attn_selftest_wait_kernel(uint32_t *err) {
+    __shared__ uint64_t bars[2];
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        mbar_init(&bars[0], 1);
+        mbar_init(&bars[1], 1);
+        abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    const int w = threadIdx.x >> 5;
+    if ((threadIdx.x & 31) == 0) {
+        if (w == 1) {   // idle for half the limit (bounded by the clock)
+            const uint64_t t = globaltimer_ns();
+            while (globaltimer_ns() - t < kWaitLimitNs / 2) {
+            }
+        }
+        const uint64_t t0 = globaltimer_ns();
+        // phase 0 of a fresh barrier never completes: nothing arrives on it
+        const bool ok = mbar_wait(&bars[w], 0u, &abort_flag, err, SRC_SELFTEST);
+        g_selftest_out[2 * w] = ok ? 1ull : 0ull;
+        g_selftest_out[2 * w + 1] = globaltimer_ns() - t0;
+    }
+}
+}  // namespace
+}  // namespace attn
+
 // measurement hook (see attn_set_kernel_events)
 static thread_local cudaEvent_t g_ev_before = nullptr, g_ev_after = nullptr;
 
@@ -283,6 +324,22 @@ void attn_set_kernel_events(void *before, void *after) {
 }
 
 int attn_abi_version(void) { return ATTN_ABI_VERSION; }
+
+attn_status attn_selftest_bounded_wait(void *stream, unsigned long long *result) {
+    if (!result) return ATTN_ERR_INVALID_ARG;
+    DevInfo *d = nullptr;
+    attn_status st = dev_info(&d);
+    if (st != ATTN_OK) return st;
+    if ((st = check_arch(d)) != ATTN_OK) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    attn_selftest_wait_kernel<<<1, 64, 0, s>>>(d->err);
+    if (cudaGetLastError() != cudaSuccess || cudaStreamSynchronize(s) != cudaSuccess ||
+        cudaMemcpyFromSymbol(result, g_selftest_out, sizeof(g_selftest_out)) != cudaSuccess) {
+        cudaGetLastError();
+        return ATTN_ERR_LAUNCH_FAILED;
+    }
+    return ATTN_OK;
+}
 
 const char *attn_status_string(attn_status s) {
     switch (s) {

@@ -404,6 +404,20 @@ ATTN_API const char *attn_status_string(attn_status status);
  * ATTN_ERR_LAUNCH_FAILED if the stream itself reports a CUDA error.  *detail (nullable) receives the raw error word. */
 ATTN_API attn_status attn_get_last_device_error(void *stream, uint32_t *detail);
 
+/* Failure-detection self-test: one small kernel in which a bounded mbarrier
+ * wait runs out on purpose (nothing ever completes the barrier; no fault, no
+ * trap).  The first waiter gives up after the library's wait limit (about one
+ * second), records ATTN_ERR_DEVICE_TIMEOUT in the device error word and raises
+ * the kernel's abort flag; a second waiter, which started half a limit later,
+ * must give up on seeing that flag before its own limit runs out.  Synchronises
+ * `stream`.  result (host, 4 entries): the first waiter's success flag (0 when
+ * it gave up, as it must) and nanoseconds waited, then the same for the
+ * second.  The context stays usable; attn_get_last_device_error then reports
+ * ATTN_ERR_DEVICE_TIMEOUT and clears the word.  Returns ATTN_OK,
+ * ATTN_ERR_INVALID_ARG (result NULL), ATTN_ERR_NO_DEVICE, ATTN_ERR_UNSUPPORTED
+ * or ATTN_ERR_LAUNCH_FAILED. */
+ATTN_API attn_status attn_selftest_bounded_wait(void *stream, unsigned long long *result);
+
 /* ATTN_ABI_VERSION of the loaded library. */
 ATTN_API int attn_abi_version(void);
 

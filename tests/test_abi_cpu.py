@@ -34,6 +34,8 @@ def test_host_validation_without_device(L):
     assert L.store_kvcache(null, null, null, null, null, null, 5, 8, 128, 0, 0, 10, null) == 1
     assert L.store_kvcache(null, null, null, null, null, null, -1, 8, 128, 0, 0, 10, null) == 1
     assert L.store_kvcache(null, null, null, null, null, null, 0, 8, 128, 0, 0, 10, null) == 0   # nothing to do
+    # the failure-detection self-test needs somewhere to put its result
+    assert L.attn_selftest_bounded_wait(null, null) == 1
     fake = ctypes.c_void_p(0x1000)
     # varlen: Hq not a multiple of Hkv, bad scale, unsupported head_dim, misaligned stride
     args = lambda **kw: [fake, fake, fake, fake, null, fake, fake, kw.get("B", 2), 8, 8, 4, 4, kw.get("Hq", 4),
