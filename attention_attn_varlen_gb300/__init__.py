@@ -7,11 +7,17 @@ memory and streams) and calls the C entry points of ``include/attn_varlen.h``
 with their raw pointers on the current stream.  There is no fallback: if the
 library is missing or the device is not sm_103 the calls raise.
 
-Entry points (same names as the C ABI):
-    attn_varlen_fwd     varlen prefill, contiguous or paged K/V
-    attn_decode_paged   single-token decode through the paged cache
-    store_kvcache       slot_mapping scatter into the caches
-and the article-shaped wrappers in :mod:`attention_attn_varlen_gb300.attention`.
+Entry points (the C ABI's names):
+    attn_varlen_fwd         varlen prefill, contiguous or paged K/V (optionally the fp16 V/16 cache)
+    attn_varlen_fwd_host    the same prefill for pinned host tensors (copies overlapped by the library)
+    attn_decode_paged       single-token decode through the paged cache
+    attn_with_kvcache       several new tokens per sequence against the paged cache (attn_kvcache_fwd)
+    attn_padded_fwd         a padded [B, S, H, D] batch with per-sequence lengths
+    store_kvcache           slot_mapping scatter into the caches (optionally also V/16 in fp16)
+    softmax_rows            row softmax (attn_softmax_rows)
+    get_last_device_error   the device error word (index, range and timeout checks)
+    selftest_bounded_wait   the failure-detection self-test
+and the layer-shaped dispatcher in :mod:`attention_attn_varlen_gb300.attention`.
 """
 from __future__ import annotations
 
@@ -25,8 +31,10 @@ import torch
 from ._build import LIB as _LIB_PATH
 from ._build import build
 
-__all__ = ["attn_varlen_fwd", "attn_varlen_fwd_host", "host_staging", "attn_decode_paged", "attn_with_kvcache", "attn_padded_fwd", "softmax_rows", "store_kvcache", "get_last_device_error", "lib",
-           "build", "AttnError", "exported_symbols", "set_kernel_events", "decode_num_splits", "decode_workspace_size"]
+__all__ = ["attn_varlen_fwd", "attn_varlen_fwd_host", "host_staging", "attn_decode_paged", "attn_with_kvcache",
+           "attn_padded_fwd", "softmax_rows", "store_kvcache", "get_last_device_error", "selftest_bounded_wait",
+           "lib", "build", "AttnError", "exported_symbols", "set_kernel_events", "decode_num_splits",
+           "decode_workspace_size"]
 
 ATTN_OK = 0
 _STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "workspace too small", 4: "launch failed",
