@@ -18,6 +18,10 @@
 //                     its tokens ("减少遍历次数的“在线 Softmax”" and
 //                     "FlashAttention 的最终实现": running max, proxy
 //                     denominator, proxy output rescaled by 2^(m_old - m_new)).
+//                     The reference m of a column moves only when a tile's
+//                     max exceeds it by more than 8 (log2 units), so the
+//                     rescale is rare and P stays <= 256; d', o' and the
+//                     merges all use that reference, so the result is the same.
 //                     S^T = K Q^T and O^T += V^T P^T run on mma.sync m16n8k16
 //                     with the tokens (then head_dim) in M and the Sq x G
 //                     query columns (token-major) in N: up to 16 per CTA
@@ -286,24 +290,30 @@ __global__ void __launch_bounds__(kDecThreads, QS ? 3 : 0) attn_decode_split_ker
                     mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, sh));
                     mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, sh));
                 }
-                const float mn0 = fmaxf(m[nt][0], mx0), mn1 = fmaxf(m[nt][1], mx1);
-                const float a_0 = (m[nt][0] == -INFINITY) ? 0.f : ex2(m[nt][0] - mn0);
-                const float a_1 = (m[nt][1] == -INFINITY) ? 0.f : ex2(m[nt][1] - mn1);
-                const float ref0 = (mn0 == -INFINITY) ? 0.f : mn0;
-                const float ref1 = (mn1 == -INFINITY) ? 0.f : mn1;
+                // the reference of a column moves only when the tile's max exceeds it by
+                // more than 8 (log2 units): P <= 256, and O is rarely rescaled
+                const bool nd0 = mx0 > m[nt][0] + 8.f, nd1 = mx1 > m[nt][1] + 8.f;
+                if (__any_sync(0xffffffffu, nd0 || nd1)) {
+                    const float a_0 = !nd0 ? 1.f : (m[nt][0] == -INFINITY) ? 0.f : ex2(m[nt][0] - mx0);
+                    const float a_1 = !nd1 ? 1.f : (m[nt][1] == -INFINITY) ? 0.f : ex2(m[nt][1] - mx1);
+                    if (nd0) m[nt][0] = mx0;
+                    if (nd1) m[nt][1] = mx1;
+                    l[nt][0] *= a_0;
+                    l[nt][1] *= a_1;
+#pragma unroll
+                    for (int i = 0; i < KS; ++i) {
+                        o[nt][i][0] *= a_0;
+                        o[nt][i][1] *= a_1;
+                        o[nt][i][2] *= a_0;
+                        o[nt][i][3] *= a_1;
+                    }
+                }
+                const float ref0 = (m[nt][0] == -INFINITY) ? 0.f : m[nt][0];
+                const float ref1 = (m[nt][1] == -INFINITY) ? 0.f : m[nt][1];
                 const float p0 = ex2(s_0 - ref0), p2 = ex2(s_2 - ref0);
                 const float p1 = ex2(s_1 - ref1), p3 = ex2(s_3 - ref1);
-                l[nt][0] = l[nt][0] * a_0 + (p0 + p2);
-                l[nt][1] = l[nt][1] * a_1 + (p1 + p3);
-                m[nt][0] = mn0;
-                m[nt][1] = mn1;
-#pragma unroll
-                for (int i = 0; i < KS; ++i) {
-                    o[nt][i][0] *= a_0;
-                    o[nt][i][1] *= a_1;
-                    o[nt][i][2] *= a_0;
-                    o[nt][i][3] *= a_1;
-                }
+                l[nt][0] += p0 + p2;
+                l[nt][1] += p1 + p3;
                 // P^T into the B layout: rows = tokens, cols = query columns -> transpose.
                 if constexpr (VH) {
                     // P' = 16 P as fp16 against V' = V / 16: the product is P V
