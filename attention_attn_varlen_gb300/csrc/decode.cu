@@ -284,16 +284,18 @@ __global__ void __launch_bounds__(kDecThreads, QS ? 3 : 0) attn_decode_split_ker
                 if (key0 >= kend[nt][1]) s_1 = -INFINITY;
                 if (key1 >= kend[nt][0]) s_2 = -INFINITY;
                 if (key1 >= kend[nt][1]) s_3 = -INFINITY;
-                float mx0 = fmaxf(s_0, s_2), mx1 = fmaxf(s_1, s_3);
-#pragma unroll
-                for (int sh = 4; sh < 32; sh <<= 1) {
-                    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, sh));
-                    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, sh));
-                }
                 // the reference of a column moves only when the tile's max exceeds it by
-                // more than 8 (log2 units): P <= 256, and O is rarely rescaled
-                const bool nd0 = mx0 > m[nt][0] + 8.f, nd1 = mx1 > m[nt][1] + 8.f;
-                if (__any_sync(0xffffffffu, nd0 || nd1)) {
+                // more than 8 (log2 units): P <= 256, and O is rarely rescaled.  Whether
+                // any value of the warp does is one vote; the column maxima (over the
+                // eight lanes sharing a column) are reduced only then.
+                float mx0 = fmaxf(s_0, s_2), mx1 = fmaxf(s_1, s_3);
+                if (__any_sync(0xffffffffu, mx0 > m[nt][0] + 8.f || mx1 > m[nt][1] + 8.f)) {
+#pragma unroll
+                    for (int sh = 4; sh < 32; sh <<= 1) {
+                        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, sh));
+                        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, sh));
+                    }
+                    const bool nd0 = mx0 > m[nt][0] + 8.f, nd1 = mx1 > m[nt][1] + 8.f;
                     const float a_0 = !nd0 ? 1.f : (m[nt][0] == -INFINITY) ? 0.f : ex2(m[nt][0] - mx0);
                     const float a_1 = !nd1 ? 1.f : (m[nt][1] == -INFINITY) ? 0.f : ex2(m[nt][1] - mx1);
                     if (nd0) m[nt][0] = mx0;
