@@ -45,6 +45,15 @@ namespace attn {
 
 constexpr int kDecThreads = 160;   // 4 consumer warps + 1 producer warp
 constexpr int kDecTile = 64;       // tokens per ring stage
+constexpr int kDecPrefetch = 3;   // tiles ahead of the loads that the L2 prefetch runs (two-stage ring)
+
+// bulk prefetch of one tensor-map box into L2 (no shared memory, no completion)
+__device__ __forceinline__ void tma_prefetch_l2_3d(const CUtensorMap *map, int c0, int c1, int c2) {
+    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(c0), "r"(c1), "r"(c2)
+                 : "memory");
+}
 
 // QS: the CTA's query columns live in shared memory (read by ldmatrix per tile)
 // instead of in every consumer's registers, which lets three CTAs share an SM;
@@ -156,6 +165,26 @@ __global__ void __launch_bounds__(kDecThreads, QS ? 3 : 0) attn_decode_split_ker
                     for (int pn = 0; pn < S::kPanels; ++pn) {
                         tma_load_3d(kbase + pn * S::kPanelBytes + i * box_bytes, &kmap, &full[st], pn * 64, hkv, row);
                         tma_load_3d(vbase + pn * S::kPanelBytes + i * box_bytes, &vmap, &full[st], pn * 64, hkv, row);
+                    }
+                }
+                if constexpr (QS) {
+                    // two ring stages hold less than the load latency covers here: the first
+                    // column group's producer pulls the K / V boxes kDecPrefetch tiles ahead
+                    // into L2, so those tiles' loads (its own and the other groups') hit L2
+                    if (cgrp == 0) {
+                        const int tp0 = s0 + (t + kDecPrefetch) * kDecTile;
+                        for (int i = 0; i < boxes; ++i) {
+                            const int tok = tp0 + i * rpb;
+                            if (tok >= s1) break;
+                            const int blk = __ldg(bt + tok / p.block_size);
+                            if (blk < 0 || (int64_t)blk >= p.num_blocks) continue;   // reported by its load
+                            const int row = blk * p.block_size + tok % p.block_size;
+#pragma unroll
+                            for (int pn = 0; pn < S::kPanels; ++pn) {
+                                tma_prefetch_l2_3d(&kmap, pn * 64, hkv, row);
+                                tma_prefetch_l2_3d(&vmap, pn * 64, hkv, row);
+                            }
+                        }
                     }
                 }
             }
