@@ -230,10 +230,12 @@ __device__ __forceinline__ void v_to_f16_keys(const PrefillParams &p) {
 // ---------------------------------------------------------------------------
 // Scheduler (one CTA of the pre-pass launch): writes the unit list that the
 // persistent attention CTAs take entries from, in order, through a global
-// counter.  Sequences come longest first (counting sort on their pair count),
-// so the last units taken are short; inside a sequence units are grouped by
-// KV head and run from the last query pair (most key tiles) to the first, so
-// units running together share one K/V stream in L2.
+// counter.  Sequences come longest first (counting sort on the key tiles of
+// their longest unit, the one of the last query pair: with a cached context
+// that is not proportional to the number of query pairs), so the last units
+// taken are short; inside a sequence units are grouped by KV head and run from
+// the last query pair (most key tiles) to the first, so units running together
+// share one K/V stream in L2.
 // Entry = (sequence, pair | kv_head << 16).  Also flags invalid offsets and
 // sequences longer than max_seqlen_q.
 // ---------------------------------------------------------------------------
@@ -242,10 +244,13 @@ constexpr int kSchedBuckets = 4096;
 constexpr int kSchedWarps = kSchedThreads / 32;
 constexpr int kSchedWarpBatch = 1024;   // up to this many sequences, a warp writes each one's units
 
-__device__ __forceinline__ int pf_pairs(const PrefillParams &p, int b, bool report) {
+__device__ __forceinline__ int pf_pairs(const PrefillParams &p, int b, bool report, int &bucket) {
     const int tps = BM / p.G;
     int qs, Lq, ks, Lk;
+    bucket = 0;
     if (!seq_rows(p, b, report, qs, Lq, ks, Lk)) return 0;
+    // sort key: the key tiles of the sequence's longest unit (its last query pair)
+    bucket = min((Lk + BN - 1) / BN, kSchedBuckets - 1);
     int pairs = (Lq + 2 * tps - 1) / (2 * tps);
     if (pairs > p.max_pairs) {   // longer than the stated max_seqlen_q
         if (report) record_error(p.err, ERR_INDEX | SRC_PREFILL);
@@ -260,8 +265,9 @@ __device__ __forceinline__ void schedule_units(const PrefillParams &p) {
     for (int i = threadIdx.x; i < kSchedBuckets; i += kSchedThreads) units_in[i] = 0;
     __syncthreads();
     for (int b = threadIdx.x; b < p.batch; b += kSchedThreads) {
-        const int pairs = pf_pairs(p, b, true);
-        if (pairs) atomicAdd(&units_in[min(pairs, kSchedBuckets - 1)], pairs * p.Hkv);
+        int bucket;
+        const int pairs = pf_pairs(p, b, true, bucket);
+        if (pairs) atomicAdd(&units_in[bucket], pairs * p.Hkv);
     }
     __syncthreads();
     // descending exclusive scan: offset of a bucket = units of all larger buckets
@@ -306,10 +312,11 @@ __device__ __forceinline__ void schedule_units(const PrefillParams &p) {
     if (p.batch <= kSchedWarpBatch) {
         // few sequences (each with many units): a warp writes each sequence's entries
         for (int b = wid; b < p.batch; b += kSchedWarps) {
-            const int pairs = pf_pairs(p, b, false);
+            int bucket;
+            const int pairs = pf_pairs(p, b, false, bucket);
             if (!pairs) continue;
             int off = 0;
-            if (lane == 0) off = atomicAdd(&units_in[min(pairs, kSchedBuckets - 1)], pairs * p.Hkv);
+            if (lane == 0) off = atomicAdd(&units_in[bucket], pairs * p.Hkv);
             off = __shfl_sync(0xffffffffu, off, 0);
             for (int e = lane; e < pairs * p.Hkv; e += 32) {
                 const int h = e / pairs, i = e % pairs;
@@ -318,9 +325,10 @@ __device__ __forceinline__ void schedule_units(const PrefillParams &p) {
         }
     } else {
         for (int b = threadIdx.x; b < p.batch; b += kSchedThreads) {
-            const int pairs = pf_pairs(p, b, false);
+            int bucket;
+            const int pairs = pf_pairs(p, b, false, bucket);
             if (!pairs) continue;
-            int off = atomicAdd(&units_in[min(pairs, kSchedBuckets - 1)], pairs * p.Hkv);
+            int off = atomicAdd(&units_in[bucket], pairs * p.Hkv);
             for (int h = 0; h < p.Hkv; ++h)
                 for (int i = 0; i < pairs; ++i) p.units[off++] = make_int2(b, (pairs - 1 - i) | (h << 16));
         }
