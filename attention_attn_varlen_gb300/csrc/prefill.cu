@@ -1073,10 +1073,12 @@ static cudaError_t launch_prefill_t(const CUtensorMap &qmap, const CUtensorMap &
 cudaError_t launch_prefill(const CUtensorMap &qmap, const CUtensorMap &kmap, const CUtensorMap &vmap,
                            const CUtensorMap &omap, const PrefillParams &p, int head_dim, cudaStream_t stream) {
     // the next unit taken a unit ahead when keys are short (each unit's K / V is
-    // small, so its siblings gain little from sharing it through L2)
+    // small, so its siblings gain little from sharing it through L2) or when every
+    // sequence is one query pair (a unit has no siblings)
     if (head_dim == 128)
-        return p.max_seqlen_k <= kEarlyMaxKeys ? launch_prefill_t<128, true>(qmap, kmap, vmap, omap, p, stream)
-                                               : launch_prefill_t<128, false>(qmap, kmap, vmap, omap, p, stream);
+        return (p.max_seqlen_k <= kEarlyMaxKeys || p.max_pairs == 1)
+                   ? launch_prefill_t<128, true>(qmap, kmap, vmap, omap, p, stream)
+                   : launch_prefill_t<128, false>(qmap, kmap, vmap, omap, p, stream);
     return launch_prefill_t<64, false>(qmap, kmap, vmap, omap, p, stream);
 }
 
