@@ -118,16 +118,25 @@ constexpr int kDecodeMaxColumns = 64;   // Sq x G query columns per KV head on t
 constexpr int kDecodeMaxColumnsV16 = 16;
 constexpr int kDecodeTile = 64;
 
-int choose_splits(int num_sms, int batch, int num_heads_kv, int max_len, int requested) {
+// Tokens a split streams at most when the library chooses the split count: long
+// enough that a CTA's fixed costs (query columns, barriers, the merge of its warps,
+// its partials and their combine) stay small, short enough to balance very
+// different lengths.  When a KV head's query columns span several column-group
+// CTAs those fixed costs are paid once per group: longer splits.
+constexpr int kSplitTokens = 4096;
+constexpr int kSplitTokensGroups = 8192;
+
+int choose_splits(int num_sms, int batch, int num_heads_kv, int max_len, int requested,
+                  int split_cap = kSplitTokens) {
     if (max_len <= 0) return 1;
     const int max_tiles = (max_len + kDecodeTile - 1) / kDecodeTile;
     int s;
     if (requested > 0) {
         s = requested;
     } else {
-        // each split streams at most ~2048 tokens (load balance across very
-        // different lengths), and there are at least ~2 CTAs per SM in total
-        const int s_balance = (max_len + 2047) / 2048;
+        // each split streams at most split_cap tokens, and there are at least ~2
+        // CTAs per SM in total
+        const int s_balance = (max_len + split_cap - 1) / split_cap;
         const int64_t units = (int64_t)batch * num_heads_kv;
         const int s_par = (int)((2LL * 2 * num_sms + units - 1) / units);
         s = s_balance > s_par ? s_balance : s_par;
@@ -146,8 +155,9 @@ int split_tokens_for(int max_len, int splits) {
 // Split plan of the decode kernel: the split count for these sizes and the
 // tokens per split (a multiple of the 64-token tile), with splits * tokens
 // covering max_len.
-void decode_plan(int num_sms, int batch, int num_heads_kv, int max_len, int requested, int *splits, int *split_tok) {
-    int s = choose_splits(num_sms, batch, num_heads_kv, max_len, requested);
+void decode_plan(int num_sms, int batch, int num_heads_kv, int max_len, int requested, int *splits, int *split_tok,
+                 int split_cap = kSplitTokens) {
+    int s = choose_splits(num_sms, batch, num_heads_kv, max_len, requested, split_cap);
     const int tok = split_tokens_for(max_len > 0 ? max_len : 1, s);
     s = max_len > 0 ? (max_len + tok - 1) / tok : 1;
     *splits = s < 1 ? 1 : s;
@@ -705,6 +715,12 @@ attn_status attn_padded_fwd(const void *q, const void *k, const void *v, void *o
 // kv-cache entry: [cu_seqlens_q | cu_seqlens_k] (256-byte aligned), then the
 // varlen workspace for total_k = batch * max_cache_seqlen.
 
+// split cap of the kv-cache entry's decode route: longer splits when the Sq x G
+// query columns of a KV head need several column-group CTAs (more than 16)
+static int kvcache_split_cap(int seqlen_q, int num_heads_q, int num_heads_kv) {
+    return (int64_t)seqlen_q * (num_heads_q / num_heads_kv) > 16 ? kSplitTokensGroups : kSplitTokens;
+}
+
 static size_t kvcache_ws(int batch, int seqlen_q, int num_heads_q, int num_heads_kv, int head_dim,
                          int max_cache_seqlen, bool v16_cache) {
     if (batch <= 0 || seqlen_q <= 0 || max_cache_seqlen < 0) return 0;
@@ -714,7 +730,8 @@ static size_t kvcache_ws(int batch, int seqlen_q, int num_heads_q, int num_heads
         int sms = 148;
         if (dev_info(&d) == ATTN_OK) sms = d->num_sms;
         int splits = 1, tok = 0;
-        decode_plan(sms, batch, num_heads_kv, max_cache_seqlen, 0, &splits, &tok);
+        decode_plan(sms, batch, num_heads_kv, max_cache_seqlen, 0, &splits, &tok,
+                    kvcache_split_cap(seqlen_q, num_heads_q, num_heads_kv));
         return decode_partial_bytes(batch, seqlen_q, num_heads_q, head_dim, splits) + 256;
     }
     const size_t v = attn_varlen_workspace_size(batch, num_heads_q, num_heads_kv, head_dim, seqlen_q,
@@ -759,7 +776,8 @@ attn_status attn_kvcache_fwd(const void *q, const void *k_cache, const void *v_c
                         1, (int64_t)batch * seqlen_q, v16_cache};
         if ((st = decode_check(c)) != ATTN_OK) return st;
         int splits = 1, split_tok = 0;
-        decode_plan(d->num_sms, batch, num_heads_kv, max_cache_seqlen, 0, &splits, &split_tok);
+        decode_plan(d->num_sms, batch, num_heads_kv, max_cache_seqlen, 0, &splits, &split_tok,
+                    kvcache_split_cap(seqlen_q, num_heads_q, num_heads_kv));
         return decode_launch(c, d, splits, split_tok, reinterpret_cast<float *>(workspace), stream);
     }
     int32_t *cu_q = reinterpret_cast<int32_t *>(workspace);

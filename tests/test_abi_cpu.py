@@ -58,7 +58,7 @@ def test_host_validation_without_device(L):
 
 def test_decode_split_rule_is_host_side(L):
     # no device: the rule falls back to a default SM count but stays well defined
-    assert L.attn_decode_num_splits(256, 8, 16384, 0) == 8
+    assert L.attn_decode_num_splits(256, 8, 16384, 0) == 4      # at most 4096 tokens per split
     assert L.attn_decode_num_splits(1, 8, 16384, 0) >= 8
     assert L.attn_decode_num_splits(4, 8, 100, 5) == 2          # capped by 64-token tiles
     assert L.attn_decode_workspace_size(256, 32, 8, 128, 16384, 1) == 0

@@ -71,14 +71,14 @@ def test_noalloc_decode_matches_oracle_and_workspace_decode_twice():
 
 
 def test_noalloc_lowers_the_automatic_split_count_to_fit():
-    """96 sequences, 32 query heads, a stated max length of 65,536 keys: the
-    automatic plan (32 splits) needs 50.7 MB of partials, more than the 32 MiB
+    """192 sequences, 32 query heads, a stated max length of 65,536 keys: the
+    automatic plan (16 splits) needs 50.7 MB of partials, more than the 32 MiB
     scratch, so the entry point runs the largest count that fits."""
     L = av.lib()
     rng = np.random.default_rng(93)
-    ctx = rng.integers(1, 2000, size=96, endpoint=True)
+    ctx = rng.integers(1, 2000, size=192, endpoint=True)
     ctx[5], ctx[40] = 65536, 20000
-    cfg = workloads.small_paged(93, ctx=ctx.tolist(), new=[0] * 96, Hq=32, Hkv=8, D=128, block_size=256, decode=True)
+    cfg = workloads.small_paged(93, ctx=ctx.tolist(), new=[0] * 192, Hq=32, Hkv=8, D=128, block_size=256, decode=True)
     max_len = 65536
     auto = L.attn_decode_num_splits(cfg.batch, cfg.Hkv, max_len, 0)
     assert _partial_bytes(cfg.batch, cfg.Hq, cfg.D, auto) > SCRATCH_BYTES
