@@ -525,6 +525,7 @@ static attn_status varlen_impl(const void *q, const void *k, const void *v, void
     p.G = G;
     p.causal = causal ? 1 : 0;
     p.max_pairs = (int)max_pairs;
+    p.one_slot = max_seqlen_q <= tps ? 1 : 0;
     // persistent CTAs: one per SM (fewer when there are fewer possible units)
     const int64_t max_units = (int64_t)batch * max_pairs * num_heads_kv;
     p.num_ctas = (int)(max_units < d->num_sms ? max_units : d->num_sms);

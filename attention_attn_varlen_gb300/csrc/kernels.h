@@ -53,6 +53,7 @@ struct PrefillParams {
     int v16_paged;               // 1: V' tiles come from a paged fp16 V / 16 cache through the block
                                  //    table (written by store_kvcache); no conversion pass
     int num_ctas;                // grid size: persistent CTAs (one per SM, at most the possible units)
+    int one_slot;                // 1: max_seqlen_q <= 128 / G, every sequence fits one query slot
     int2 *units;                 // workspace: (sequence, pair | kv_head << 16), scheduled order
     int *unit_count;             // workspace: [0] number of units
     float scale_log2;            // softmax_scale * log2(e), > 0

@@ -388,6 +388,18 @@ __device__ __forceinline__ PfUnit pf_unit(const PrefillParams &p, int u) {
     return w;
 }
 
+// HALF: slot B is never used (a sequence longer than one slot, already reported
+// against max_seqlen_q, keeps only slot A's rows)
+template <bool HALF>
+__device__ __forceinline__ PfUnit pf_unit_k(const PrefillParams &p, int u) {
+    PfUnit w = pf_unit(p, u);
+    if (HALF) {
+        w.nB = 0;
+        w.n = w.nA;
+    }
+    return w;
+}
+
 // Output rows of one slot, 32 rows per warp (warp-collective; every argument
 // but l and m_ref is warp-uniform): O_X / d' -> bf16, read from TMEM when the
 // slot had key tiles (zeros otherwise), and the lse.  The rows are staged in
@@ -451,13 +463,69 @@ __device__ __noinline__ void pf_store_rows(const PrefillParams &p, const CUtenso
     }
 }
 
+// pf_store_rows for one half of the head dimension (HALF kernel): the warp's 32
+// rows, dims [64 h, 64 h + 64) from O's columns of that half, staged in panel h
+// of the slot's P' rows and written by one TMA store; half 0 writes the lse.
+template <int D>
+__device__ __noinline__ void pf_store_rows_half(const PrefillParams &p, const CUtensorMap *omap, uint32_t tO,
+                                                uint8_t *pslot, bool has_tiles, int64_t qbase, int ntok, int hkv,
+                                                float l, float m_ref, int h) {
+    const int G = p.G, lane = threadIdx.x & 31, wrow0 = ((threadIdx.x >> 5) & 3) * 32;
+    if (wrow0 / G >= ntok) return;   // no valid row in this warp
+    const int r = wrow0 + lane;
+    const bool row_valid = r / G < ntok, whole = (wrow0 + 31) / G < ntok;
+    const float inv = l > 0.f ? 16.f / l : 0.f;   // l accumulated P' = 16 P
+    uint8_t *srow = pslot + r * 128;
+    __nv_bfloat16 *orow = p.out + (qbase + r / G) * p.out_row_stride + (int64_t)(hkv * G + r % G) * D;
+#pragma unroll
+    for (int c = 2 * h; c < 2 * h + 2; ++c) {
+        uint32_t o[32];
+        if (has_tiles) {
+            tmem_ld32(tO + (uint32_t)(c * 32), o);
+            tc_wait_ld();
+        } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = 0u;
+        }
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+            pk[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv, __uint_as_float(o[2 * i + 1]) * inv);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint4 v4 = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+            const int ch = c * 4 + i;   // 16-byte chunk of the row
+            if (whole)
+                *reinterpret_cast<uint4 *>(srow + (ch >> 3) * kPPanelBytes + (((ch & 7) ^ (r & 7)) << 4)) = v4;
+            else if (row_valid)
+                reinterpret_cast<uint4 *>(orow)[ch] = v4;
+        }
+    }
+    if (h == 0 && row_valid && p.lse)
+        p.lse[(int64_t)(hkv * G + r % G) * p.total_q + qbase + r / G] =
+            l > 0.f ? (m_ref + __log2f(l) - 4.0f) * 0.69314718055994531f : -INFINITY;
+    if (whole) {
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+            tma_store_3d(omap, pslot + h * kPPanelBytes + wrow0 * 128, h * 64, hkv * G + wrow0 % G,
+                         (int)(qbase + wrow0 / G));
+            bulk_commit();
+            bulk_wait_read();   // the staging rows are P' rows again right after
+        }
+        __syncwarp();
+    }
+}
+
 // EARLY: the producer takes and publishes the next unit's index at the start of
 // each unit, so every role has it a whole unit ahead (the unit boundary costs
 // less).  Otherwise it takes it when it starts the unit's loads, which keeps
 // the units of one sequence and KV head side by side in time, sharing their
 // K / V tiles through L2: the launcher chooses EARLY for short keys only, where
 // that sharing is worth little and the boundary costs weigh most.
-template <int D, bool EARLY>
+// HALF: every sequence fits one query slot (at most 128 / G tokens), so slot B
+// never has rows; its softmax warps take half of each of slot A's key tiles.
+template <int D, bool EARLY, bool HALF>
 __global__ void __launch_bounds__(kPfThreads, 1)
     attn_prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                         const __grid_constant__ CUtensorMap vmap, const __grid_constant__ CUtensorMap omap,
@@ -486,6 +554,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     uint64_t *drain = pv_done + 2;                 // [2]: per issuing thread
     uint64_t *idx_full = drain + 2;                // [2]: unit_idx[s] written
     uint64_t *idx_empty = idx_full + 2;            // [2]: every role has read unit_idx[s]
+    uint64_t *pair_bar = idx_empty + 2;            // [4] (HALF): the two warps of a lane group exchanged a value
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + S::kNumBars);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     volatile int *unit_idx = reinterpret_cast<volatile int *>(tmem_slot + 2);   // [2]
@@ -504,13 +573,15 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         }
         for (int x = 0; x < 2; ++x) {
             mbar_init(&s_full[x], 1);
-            mbar_init(&s_free[x], 128);
-            mbar_init(&p_ready[x], 128);
+            mbar_init(&s_free[x], HALF && x == 0 ? 256 : 128);   // HALF: both halves read slot A's S
+            mbar_init(&p_ready[x], HALF && x == 0 ? 256 : 128);
             mbar_init(&pv_done[x], 1);
             mbar_init(&drain[x], 1);
             mbar_init(&idx_full[x], 1);
             mbar_init(&idx_empty[x], 2 + 256);   // both MMA threads and every softmax thread
         }
+        if (HALF)
+            for (int g = 0; g < 4; ++g) mbar_init(&pair_bar[g], 64);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -577,7 +648,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             // EARLY: the next unit, taken now (its atomic lands while this unit's Q is set up)
             int taken = -1;
             if constexpr (EARLY) taken = lane == 0 ? atomicAdd(next_unit, 1) : -1;
-            const PfUnit w = pf_unit(p, u);
+            const PfUnit w = pf_unit_k<HALF>(p, u);
             const int32_t *bt = paged ? p.block_table + (int64_t)w.b * p.bt_stride : nullptr;
             // Q of this unit once the previous unit's QK^T are done with the Q buffers
             int got = 1;
@@ -693,7 +764,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                 const int u = unit_idx[k & 1];
                 mbar_arrive(&idx_empty[k & 1]);
                 if (u < 0) break;
-                const PfUnit w = pf_unit(p, u);
+                const PfUnit w = pf_unit_k<HALF>(p, u);
                 const int nX[2] = {w.nA, w.nB};
                 ok = mbar_wait(q_full, (uint32_t)k & 1u, abort_flag, p.err, SRC_PREFILL);
                 if (!ok) break;
@@ -742,7 +813,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                 const int u = unit_idx[k & 1];
                 mbar_arrive(&idx_empty[k & 1]);
                 if (u < 0) break;
-                const PfUnit w = pf_unit(p, u);
+                const PfUnit w = pf_unit_k<HALF>(p, u);
                 const int nX[2] = {w.nA, w.nB};
                 // PV_X(0) of a unit writes O_X afresh: its p_ready comes after the
                 // softmax threads have read O_X of the previous unit
@@ -785,6 +856,168 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             mbar_wait(&drain[1], 0, nullptr, p.err, SRC_PREFILL);
         }
         __syncwarp();
+    } else if constexpr (HALF) {
+        // ================================================================ softmax, one slot per unit
+        // Warps w and w + 4 share a TMEM lane group: both take the same 32 rows of
+        // slot A, w keys [0, 64) and w + 4 keys [64, 128) of every tile, each its
+        // half of O's columns and its 64-key panel of P'.  A tile's row max and a
+        // unit's row sum are exchanged between the two through shared memory (slot
+        // B's P' buffer is free), synchronised by a bounded mbarrier per lane group.
+        const int h = warp >> 2, g4 = warp & 3;
+        const int r = g4 * 32 + lane;
+        const uint32_t lane_off = (uint32_t)(g4 * 32) << 16;
+        const uint32_t tS = tmem + (uint32_t)(h * 64) + lane_off;
+        const uint32_t tO = tmem + 256u + lane_off;   // the slot's O; this half's columns [64 h, 64 h + 64)
+        uint8_t *prow = sP + r * 128 + h * kPPanelBytes;   // this row of P'_A, this half's panel
+        float *xch = reinterpret_cast<float *>(sP + kPBytes);   // [parity][half][row]
+        const float sl2 = p.scale_log2;
+        int cX = 0, k = 0, xp = 0;   // S tiles of slot A before this unit; exchanges so far
+        bool ok = true;
+        // the partner warp's value for this row (every exchange is made by both
+        // warps of the lane group, in the same order)
+        auto exchange = [&](float v) -> float {
+            float *slot = xch + (xp & 1) * 256;
+            slot[h * 128 + r] = v;
+            mbar_arrive(&pair_bar[g4]);
+            ok = __all_sync(0xffffffffu, mbar_wait(&pair_bar[g4], (uint32_t)xp & 1u, abort_flag, p.err,
+                                                   SRC_PREFILL)) && ok;
+            ++xp;
+            return slot[(h ^ 1) * 128 + r];
+        };
+        bool pend = false, pend_tiles = false;
+        int64_t pend_qbase = 0;
+        int pend_ntok = 0, pend_hkv = 0;
+        float pend_l = 0.f, pend_m = 0.f;
+        for (;; ++k) {
+            ok = __all_sync(0xffffffffu,
+                            mbar_wait(&idx_full[k & 1], (uint32_t)(k >> 1) & 1u, abort_flag, p.err, SRC_PREFILL));
+            if (!ok) break;
+            const int u = unit_idx[k & 1];
+            mbar_arrive(&idx_empty[k & 1]);
+            if (u < 0) break;
+            const PfUnit w = pf_unit_k<HALF>(p, u);
+            const int t0 = w.t0A;
+            const int nX = w.nA;
+            const int tok = t0 + r / G;
+            const int lim = p.causal ? min(tok + w.off, w.Lk - 1) : w.Lk - 1;
+            float m_ref = -INFINITY;
+            float l = 0.f;   // this half's share of d'
+            for (int j = 0; j < nX; ++j) {
+                const int t = cX + j;
+                ok = __all_sync(0xffffffffu,
+                                mbar_wait(&s_full[0], (uint32_t)t & 1u, abort_flag, p.err, SRC_PREFILL));
+                if (!ok) break;
+                tc_fence_after();
+                float s[64];
+                tmem_ld32(tS + 0, *reinterpret_cast<uint32_t(*)[32]>(&s[0]));
+                tmem_ld32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&s[32]));
+                tc_wait_ld();
+                tc_fence_before();
+                mbar_arrive(&s_free[0]);
+                const int key0 = j * BN + h * 64;
+                if (key0 + 63 > lim) {
+#pragma unroll
+                    for (int c = 0; c < 64; ++c)
+                        if (key0 + c > lim) s[c] = -INFINITY;
+                }
+                float mx8[8];
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    mx8[q] = max3f(s[q], s[q + 8], s[q + 16]);
+                    mx8[q] = max3f(mx8[q], s[q + 24], s[q + 32]);
+                    mx8[q] = max3f(mx8[q], s[q + 40], s[q + 48]);
+                    mx8[q] = fmaxf(mx8[q], s[q + 56]);
+                }
+                const float mxh =
+                    max3f(max3f(mx8[0], mx8[1], mx8[2]), max3f(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]));
+                const float mx = fmaxf(mxh, exchange(mxh));
+                if (!ok) break;
+                // the same inputs in both halves: the same reference, alpha and need
+                const float m_new = fmaxf(m_ref, mx * sl2);
+                const bool need = m_new > m_ref + 8.0f;
+                float alpha = 1.f;
+                if (need) {
+                    alpha = (m_ref == -INFINITY) ? 0.f : ex2(m_ref - m_new);
+                    m_ref = m_new;
+                }
+                l *= alpha;
+                const float nref = ((m_ref == -INFINITY) ? 0.f : -m_ref) + 4.0f;
+                float la[4] = {0.f, 0.f, 0.f, 0.f}, lb[4] = {0.f, 0.f, 0.f, 0.f};
+                uint32_t pk[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    float x0, x1;
+                    fma2(x0, x1, s[2 * i], s[2 * i + 1], sl2, sl2, nref, nref);
+                    x0 = ex2(x0);
+                    x1 = ex2(x1);
+                    add2(la[i & 3], lb[i & 3], x0, x1);
+                    pk[i] = pack_f16x2(x0, x1);
+                }
+                l += ((la[0] + lb[0]) + (la[1] + lb[1])) + ((la[2] + lb[2]) + (la[3] + lb[3]));
+                if (t > 0) {
+                    ok = __all_sync(0xffffffffu, mbar_wait(&pv_done[0], (uint32_t)(t - 1) & 1u, abort_flag, p.err,
+                                                           SRC_PREFILL));
+                    if (!ok) break;
+                    tc_fence_after();
+                }
+                if (pend) {
+                    pf_store_rows_half<D>(p, &omap, tO, sP, pend_tiles, pend_qbase, pend_ntok, pend_hkv, pend_l,
+                                          pend_m, h);
+                    pend = false;
+                }
+                if (j > 0 && __any_sync(0xffffffffu, need)) {
+#pragma unroll
+                    for (int c = 2 * h; c < 2 * h + 2; ++c) {
+                        uint32_t o[32];
+                        tmem_ld32(tO + (uint32_t)(c * 32), o);
+                        tc_wait_ld();
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                        tmem_st32(tO + (uint32_t)(c * 32), o);
+                    }
+                    tc_wait_st();
+                }
+#pragma unroll
+                for (int ch = 0; ch < 8; ++ch)
+                    *reinterpret_cast<uint4 *>(prow + ((ch ^ (r & 7)) << 4)) =
+                        make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
+                fence_proxy_async_smem();
+                tc_fence_before();
+                mbar_arrive(&p_ready[0]);
+            }
+            if (!ok) break;
+            const float ltot = l + exchange(l);   // the unit's d' over both halves
+            if (!ok) break;
+            if (pend) {   // no key tiles in this unit: store the previous unit's rows now
+                if (cX > 0) {
+                    ok = __all_sync(0xffffffffu, mbar_wait(&pv_done[0], (uint32_t)(cX - 1) & 1u, abort_flag, p.err,
+                                                           SRC_PREFILL));
+                    if (!ok) break;
+                    tc_fence_after();
+                }
+                pf_store_rows_half<D>(p, &omap, tO, sP, pend_tiles, pend_qbase, pend_ntok, pend_hkv, pend_l, pend_m,
+                                      h);
+            }
+            cX += nX;
+            pend = true;
+            pend_tiles = nX > 0;
+            pend_qbase = (int64_t)w.qs + t0;
+            pend_ntok = min(max(w.Lq - t0, 0), BM / G);
+            pend_hkv = w.hkv;
+            pend_l = ltot;
+            pend_m = m_ref;
+        }
+        if (ok && pend) {
+            if (cX > 0)
+                ok = __all_sync(0xffffffffu, mbar_wait(&pv_done[0], (uint32_t)(cX - 1) & 1u, abort_flag, p.err,
+                                                       SRC_PREFILL));
+            if (ok) {
+                tc_fence_after();
+                pf_store_rows_half<D>(p, &omap, tO, sP, pend_tiles, pend_qbase, pend_ntok, pend_hkv, pend_l, pend_m,
+                                      h);
+            }
+        }
+        if (lane == 0) bulk_wait_all();
     } else {
         // ================================================================ softmax (one row per thread)
         const int X = warp >> 2;
@@ -811,7 +1044,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             const int u = unit_idx[k & 1];
             mbar_arrive(&idx_empty[k & 1]);
             if (u < 0) break;
-            const PfUnit w = pf_unit(p, u);
+            const PfUnit w = pf_unit_k<HALF>(p, u);
             const int t0 = X ? w.t0B : w.t0A;
             const int nX = X ? w.nB : w.nA;
             const int tok = t0 + r / G;
@@ -1027,7 +1260,7 @@ cudaError_t launch_kvcache_cu(const int32_t *cache_seqlens, int batch, int seqle
     return cudaGetLastError();
 }
 
-template <int D, bool EARLY>
+template <int D, bool EARLY, bool HALF = false>
 static cudaError_t launch_prefill_t(const CUtensorMap &qmap, const CUtensorMap &kmap, const CUtensorMap &vmap,
                                     const CUtensorMap &omap, const PrefillParams &p, cudaStream_t stream) {
     using S = PfSmem<D>;
@@ -1039,7 +1272,8 @@ static cudaError_t launch_prefill_t(const CUtensorMap &qmap, const CUtensorMap &
     if (dev < 0 || dev >= kMaxDev) return cudaErrorInvalidDevice;
     std::call_once(attr_once[dev], [&] {
         attr_err[dev] =
-            cudaFuncSetAttribute(attn_prefill_kernel<D, EARLY>, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kBytes);
+            cudaFuncSetAttribute(attn_prefill_kernel<D, EARLY, HALF>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 S::kBytes);
     });
     if (attr_err[dev] != cudaSuccess) return attr_err[dev];
     // unit list and V' in one launch: grid row 0 holds the scheduler (dispatched
@@ -1060,10 +1294,11 @@ static cudaError_t launch_prefill_t(const CUtensorMap &qmap, const CUtensorMap &
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, attn_prefill_kernel<D, EARLY>, qmap, kmap, vmap, omap, p);
+    e = cudaLaunchKernelEx(&cfg, attn_prefill_kernel<D, EARLY, HALF>, qmap, kmap, vmap, omap, p);
     if (e == cudaErrorNotSupported || e == cudaErrorInvalidValue) {
         (void)cudaGetLastError();
-        attn_prefill_kernel<D, EARLY><<<p.num_ctas, kPfThreads, S::kBytes, stream>>>(qmap, kmap, vmap, omap, p);
+        attn_prefill_kernel<D, EARLY, HALF><<<p.num_ctas, kPfThreads, S::kBytes, stream>>>(qmap, kmap, vmap, omap,
+                                                                                           p);
         e = cudaGetLastError();
     }
     main_kernel_event_after(stream);
@@ -1075,6 +1310,9 @@ cudaError_t launch_prefill(const CUtensorMap &qmap, const CUtensorMap &kmap, con
     // the next unit taken a unit ahead when keys are short (each unit's K / V is
     // small, so its siblings gain little from sharing it through L2) or when every
     // sequence is one query pair (a unit has no siblings)
+    // every sequence fits one query slot: slot B's softmax warps share slot A's tiles
+    if (head_dim == 128 && p.one_slot)
+        return launch_prefill_t<128, true, true>(qmap, kmap, vmap, omap, p, stream);
     if (head_dim == 128)
         return (p.max_seqlen_k <= kEarlyMaxKeys || p.max_pairs == 1)
                    ? launch_prefill_t<128, true>(qmap, kmap, vmap, omap, p, stream)
