@@ -77,15 +77,18 @@ constexpr int BN = kPrefillKeyTile;    // 128 keys per tile
 constexpr int kPBytes = BM * BN * 2;   // one slot's P' tile (fp16)
 constexpr int kPPanelBytes = BM * 128; // 64 keys of P' per 128-byte-swizzled panel
 
-template <int D>
+// HALF (one query slot per unit): no Q_B and no P'_B, a fourth ring stage and
+// the two softmax halves' exchange area instead
+template <int D, bool HALF = false>
 struct PfSmem {
-    static constexpr int kStages = D == 128 ? 3 : 4;          // K / V' ring stages
+    static constexpr int kStages = HALF ? 4 : (D == 128 ? 3 : 4);   // K / V' ring stages
     static constexpr int kPanels = D / 64;
     static constexpr int kPanelBytes = 128 * 128;            // 128 rows x 128 B
     static constexpr int kTileBytes = kPanels * kPanelBytes; // one Q slot, K tile or V tile
-    static constexpr int kRingOff = 2 * kTileBytes;
+    static constexpr int kRingOff = (HALF ? 1 : 2) * kTileBytes;
     static constexpr int kPOff = kRingOff + kStages * kTileBytes;
-    static constexpr int kBarOff = kPOff + 2 * kPBytes;
+    static constexpr int kXchOff = kPOff + (HALF ? 1 : 2) * kPBytes;   // [parity][half][row] floats
+    static constexpr int kBarOff = kXchOff + (HALF ? 2 * 2 * BM * 4 : 0);
     static constexpr int kNumBars = 3 * kStages + 24;
     static constexpr int kBytes = kBarOff + kNumBars * 8 + 16 + 1024 /*align slack*/;
     static_assert(kBytes <= 227 * 1024, "shared memory");
@@ -530,7 +533,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     attn_prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                         const __grid_constant__ CUtensorMap vmap, const __grid_constant__ CUtensorMap omap,
                         const PrefillParams p) {
-    using S = PfSmem<D>;
+    using S = PfSmem<D, HALF>;
     constexpr int ST = S::kStages;
     extern __shared__ uint8_t psmem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(psmem_raw) + 1023) & ~uintptr_t(1023));
@@ -658,7 +661,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             if (!got) break;
             if (lane == 0) {
                 if (w.n > 0) {
-                    const bool activeB = w.t0B < w.Lq;
+                    const bool activeB = !HALF && w.t0B < w.Lq;   // HALF: no Q_B buffer
                     mbar_arrive_expect_tx(q_full, (uint32_t)S::kTileBytes * (activeB ? 2u : 1u));
 #pragma unroll
                     for (int pn = 0; pn < S::kPanels; ++pn)
@@ -861,15 +864,15 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         // Warps w and w + 4 share a TMEM lane group: both take the same 32 rows of
         // slot A, w keys [0, 64) and w + 4 keys [64, 128) of every tile, each its
         // half of O's columns and its 64-key panel of P'.  A tile's row max and a
-        // unit's row sum are exchanged between the two through shared memory (slot
-        // B's P' buffer is free), synchronised by a bounded mbarrier per lane group.
+        // unit's row sum are exchanged between the two through a shared-memory area
+        // of their own, synchronised by a bounded mbarrier per lane group.
         const int h = warp >> 2, g4 = warp & 3;
         const int r = g4 * 32 + lane;
         const uint32_t lane_off = (uint32_t)(g4 * 32) << 16;
         const uint32_t tS = tmem + (uint32_t)(h * 64) + lane_off;
         const uint32_t tO = tmem + 256u + lane_off;   // the slot's O; this half's columns [64 h, 64 h + 64)
         uint8_t *prow = sP + r * 128 + h * kPPanelBytes;   // this row of P'_A, this half's panel
-        float *xch = reinterpret_cast<float *>(sP + kPBytes);   // [parity][half][row]
+        float *xch = reinterpret_cast<float *>(sm + S::kXchOff);   // [parity][half][row]
         const float sl2 = p.scale_log2;
         int cX = 0, k = 0, xp = 0;   // S tiles of slot A before this unit; exchanges so far
         bool ok = true;
@@ -1263,7 +1266,7 @@ cudaError_t launch_kvcache_cu(const int32_t *cache_seqlens, int batch, int seqle
 template <int D, bool EARLY, bool HALF = false>
 static cudaError_t launch_prefill_t(const CUtensorMap &qmap, const CUtensorMap &kmap, const CUtensorMap &vmap,
                                     const CUtensorMap &omap, const PrefillParams &p, cudaStream_t stream) {
-    using S = PfSmem<D>;
+    using S = PfSmem<D, HALF>;
     static std::once_flag attr_once[kMaxDev];
     static cudaError_t attr_err[kMaxDev];
     int dev = 0;
