@@ -29,6 +29,11 @@
 //   warp 9     TMEM allocator and the thread that issues every QK^T
 //   warp 10    the thread that issues every PV
 // TMEM (512 columns): S_A [0,128), S_B [128,256) fp32; O_A, O_B after them.
+// When every sequence fits one slot (at most 128 / G tokens: a few new tokens
+// per sequence against a cached context) slot B never has rows; the HALF
+// instance then gives warps 4-7 the keys [64, 128) of slot A's tiles, so each
+// softmax thread works on half a tile, and uses the freed Q_B / P'_B memory for
+// a fourth ring stage.
 //
 // PV runs in fp16: the softmax threads write P' = 16 P as fp16 into shared
 // memory (one 128 x 128 tile per slot, K-major, 128-byte swizzle), and V comes
