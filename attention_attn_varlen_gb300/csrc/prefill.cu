@@ -414,7 +414,10 @@ __device__ __forceinline__ PfUnit pf_unit_k(const PrefillParams &p, int u) {
 // this warp's own rows of the slot's P' tile (free: the slot's last PV has
 // completed) in the 128-byte-swizzled layout of an output box (64 dims x
 // min(G, 32) heads x 32 / min(G, 32) tokens per panel), and one thread writes
-// them with a TMA store per panel.  A warp holding rows past the sequence's
+// them with a TMA store per panel.  Panel by panel: a panel's two TMEM loads
+// before one wait, its conversion, its staging and its store, so the first
+// panel's store reads shared memory while the second is converted (all four
+// loads at once need 128 registers here and spill).  A warp holding rows past the sequence's
 // end (its last slot) writes its valid rows itself instead: a box would
 // overwrite the next sequence's rows.  Out of line: it runs once per unit, and
 // its registers then do not constrain the softmax's per-tile code.
@@ -429,41 +432,46 @@ __device__ __noinline__ void pf_store_rows(const PrefillParams &p, const CUtenso
     const float inv = l > 0.f ? 16.f / l : 0.f;   // l accumulated P' = 16 P
     uint8_t *srow = pslot + r * 128;
     __nv_bfloat16 *orow = p.out + (qbase + r / G) * p.out_row_stride + (int64_t)(hkv * G + r % G) * D;
-#pragma unroll
-    for (int c = 0; c < D / 32; ++c) {
-        uint32_t o[32];
-        if (has_tiles) {
-            tmem_ld32(tO + (uint32_t)(c * 32), o);
-            tc_wait_ld();
-        } else {
-#pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] = 0u;
-        }
-        uint32_t pk[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i)
-            pk[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv, __uint_as_float(o[2 * i + 1]) * inv);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const uint4 v4 = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
-            const int ch = c * 4 + i;   // 16-byte chunk of the row
-            if (whole)
-                *reinterpret_cast<uint4 *>(srow + (ch >> 3) * kPPanelBytes + (((ch & 7) ^ (r & 7)) << 4)) = v4;
-            else if (row_valid)
-                reinterpret_cast<uint4 *>(orow)[ch] = v4;
-        }
-    }
     if (row_valid && p.lse)
         p.lse[(int64_t)(hkv * G + r % G) * p.total_q + qbase + r / G] =
             l > 0.f ? (m_ref + __log2f(l) - 4.0f) * 0.69314718055994531f : -INFINITY;
-    if (whole) {
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
+#pragma unroll 1
+    for (int pn = 0; pn < D / 64; ++pn) {
+        uint32_t o[2][32];
+        if (has_tiles) {
+            tmem_ld32(tO + (uint32_t)(pn * 64), o[0]);
+            tmem_ld32(tO + (uint32_t)(pn * 64 + 32), o[1]);
+            tc_wait_ld();
+        } else {
 #pragma unroll
-            for (int pn = 0; pn < D / 64; ++pn)
+            for (int i = 0; i < 32; ++i) o[0][i] = o[1][i] = 0u;
+        }
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+                pk[i] = pack_bf16x2(__uint_as_float(o[cc][2 * i]) * inv, __uint_as_float(o[cc][2 * i + 1]) * inv);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const uint4 v4 = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+                const int ch = (2 * pn + cc) * 4 + i;   // 16-byte chunk of the row
+                if (whole)
+                    *reinterpret_cast<uint4 *>(srow + (ch >> 3) * kPPanelBytes + (((ch & 7) ^ (r & 7)) << 4)) = v4;
+                else if (row_valid)
+                    reinterpret_cast<uint4 *>(orow)[ch] = v4;
+            }
+        }
+        if (whole) {
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0)
                 tma_store_3d(omap, pslot + pn * kPPanelBytes + wrow0 * 128, pn * 64, hkv * G + wrow0 % G,
                              (int)(qbase + wrow0 / G));
+        }
+    }
+    if (whole) {
+        if (lane == 0) {
             bulk_commit();
             bulk_wait_read();   // the staging rows are P' rows again right after
         }
