@@ -139,6 +139,55 @@ def test_one_pair_launch_takes_units_early_bitexact():
     assert bool((d <= 2.0 ** -7 * o1.float().abs() + 1e-6).all())
 
 
+ONE_SLOT_CASES = [
+    # seed, lens_q, lens_k, Hq, Hkv, causal: every sequence within one 128-row slot (Lq <= 128 / G)
+    (71, [128, 1, 0, 77], [900, 1, 5, 77], 16, 16, False),   # MHA: 128 tokens per slot, non-causal
+    (72, [128, 60, 3], [128, 2000, 3], 8, 8, True),
+    (73, [16, 9, 1, 16], [4000, 9, 300, 17], 32, 4, True),    # G = 8: 16 tokens per slot
+    (74, [32, 31, 5], [32, 600, 6000], 32, 8, False),
+]
+
+
+@pytest.mark.parametrize("seed,lq,lk,Hq,Hkv,causal", ONE_SLOT_CASES)
+def test_one_slot_instance_matches_oracle(seed, lq, lk, Hq, Hkv, causal):
+    """Launches whose sequences all fit one query slot run the instance in which
+    slot B's softmax warps take half of each of slot A's key tiles (the row max and
+    row sum exchanged between the two halves).  Against the oracle, and within a
+    bf16 ulp of the two-slot kernel (max_seqlen_q raised past one slot)."""
+    D = 128
+    cfg = workloads.small_varlen(seed, lq, lk, Hq, Hkv, D, causal)
+    q, k, v = cfg.q().cuda(), cfg.k().cuda(), cfg.v().cuda()
+    cu_q, cu_k = torch.from_numpy(cfg.cu_q).cuda(), torch.from_numpy(cfg.cu_k).cuda()
+    mq, mk = int(cfg.lens_q.max()), int(cfg.lens_k.max())
+    assert mq <= 128 // (Hq // Hkv)
+    av.get_last_device_error()
+    o1, l1 = av.attn_varlen_fwd(q, k, v, cu_q, cu_k, mq, mk, cfg.scale, causal=causal, return_lse=True)
+    o2, l2 = av.attn_varlen_fwd(q, k, v, cu_q, cu_k, 300, mk, cfg.scale, causal=causal, return_lse=True)
+    torch.cuda.synchronize()
+    assert av.get_last_device_error()[0] == 0
+    ref, ref_lse = oracle.attn_varlen(cfg.q(), cfg.k(), cfg.v(), cfg.cu_q, cfg.cu_k, Hq, Hkv, D, cfg.scale, causal)
+    what = f"one-slot s{seed} Hq{Hq}/{Hkv} causal={causal} {lq}/{lk}"
+    assert_close(o1, ref.reshape(o1.shape), what)
+    assert_lse_close(l1.t().contiguous(), ref_lse.reshape(-1, Hq), what + " lse")
+    d = (o1.float() - o2.float()).abs()
+    assert bool((d <= 2.0 ** -7 * o2.float().abs() + 1e-6).all()), what + ": differs from the two-slot kernel"
+
+
+def test_one_slot_instance_paged_v16_cache():
+    """The one-slot instance on the paged cache with the fp16 V / 16 cache (the kv-cache
+    route's case): a few new tokens per sequence against long contexts."""
+    cfg = workloads.small_paged(75, ctx=[3000, 0, 700, 129], new=[8, 8, 5, 1], Hq=32, Hkv=8, D=128, block_size=64)
+    q = cfg.q()
+    av.get_last_device_error()
+    kc, vc, k_new, v_new = _paged_device(cfg)
+    out, lse = _run_paged(cfg, q, kc, vc, v16=v16_of(vc))
+    torch.cuda.synchronize()
+    assert av.get_last_device_error()[0] == 0
+    ref, ref_lse, _ = _paged_oracle(cfg, q, k_new, v_new, list(range(cfg.batch)))
+    assert_close(out, ref.reshape(out.shape), "one-slot paged v16")
+    assert_lse_close(lse.t().contiguous(), ref_lse.reshape(-1, 32), "one-slot paged v16 lse")
+
+
 def test_varlen_strided_qkv_views():
     """q, k, v as views of one packed [tokens, Hq + 2 Hkv, D] projection."""
     lens = np.array([300, 129])
