@@ -179,8 +179,8 @@ bool kvcache_on_decode(int batch, int seqlen_q, int num_heads_q, int num_heads_k
     if (head_dim != 64 && head_dim != 128) return false;
     if (batch > 65535 || num_heads_kv > 65535) return false;
     const int G = num_heads_q / num_heads_kv;
-    // the prefill packs 128 / G tokens x G heads per query slot: other groups stay here
-    const bool prefill_ok = kPrefillSlotRows % G == 0;
+    // the prefill packs 128 / G tokens x G heads per query slot: larger groups stay here
+    const bool prefill_ok = G <= kPrefillSlotRows;
     return (int64_t)seqlen_q * G <= (v16 && prefill_ok ? kDecodeMaxColumnsV16 : kDecodeMaxColumns);
 }
 
@@ -406,7 +406,7 @@ static size_t kvcache_cu_bytes(int batch) { return ((size_t)2 * (batch + 1) * si
 static int64_t varlen_max_pairs(int num_heads_q, int num_heads_kv, int max_seqlen_q) {
     if (num_heads_kv <= 0 || num_heads_q <= 0 || num_heads_q % num_heads_kv || max_seqlen_q < 0) return -1;
     const int G = num_heads_q / num_heads_kv;
-    if (kPrefillSlotRows % G) return -1;
+    if (G > kPrefillSlotRows) return -1;   // a slot holds at least one token's G heads
     const int64_t tps = kPrefillSlotRows / G;
     return ((int64_t)max_seqlen_q + 2 * tps - 1) / (2 * tps);
 }
@@ -443,7 +443,7 @@ static attn_status varlen_impl(const void *q, const void *k, const void *v, void
     if (!(softmax_scale > 0.f) || !isfinite(softmax_scale)) return ATTN_ERR_INVALID_ARG;
     if (head_dim != 64 && head_dim != 128) return ATTN_ERR_UNSUPPORTED;
     const int G = num_heads_q / num_heads_kv;
-    if (kPrefillSlotRows % G != 0) return ATTN_ERR_UNSUPPORTED;
+    if (G > kPrefillSlotRows) return ATTN_ERR_UNSUPPORTED;
     if (batch > 65535 || num_heads_kv > 65535) return ATTN_ERR_UNSUPPORTED;
     const bool paged = block_table != nullptr;
     if (paged) {

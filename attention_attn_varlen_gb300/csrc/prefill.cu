@@ -421,14 +421,14 @@ __device__ __forceinline__ PfUnit pf_unit_k(const PrefillParams &p, int u) {
 // end (its last slot) writes its valid rows itself instead: a box would
 // overwrite the next sequence's rows.  Out of line: it runs once per unit, and
 // its registers then do not constrain the softmax's per-tile code.
-template <int D>
+template <int D, bool OBOX>
 __device__ __noinline__ void pf_store_rows(const PrefillParams &p, const CUtensorMap *omap, uint32_t tO,
                                               uint8_t *pslot, bool has_tiles, int64_t qbase, int ntok, int hkv,
                                               float l, float m_ref) {
     const int G = p.G, lane = threadIdx.x & 31, wrow0 = ((threadIdx.x >> 5) & 3) * 32;
     if (wrow0 / G >= ntok) return;   // no valid row in this warp
     const int r = wrow0 + lane;
-    const bool row_valid = r / G < ntok, whole = (wrow0 + 31) / G < ntok;
+    const bool row_valid = r / G < ntok, whole = OBOX && (wrow0 + 31) / G < ntok;
     const float inv = l > 0.f ? 16.f / l : 0.f;   // l accumulated P' = 16 P
     uint8_t *srow = pslot + r * 128;
     __nv_bfloat16 *orow = p.out + (qbase + r / G) * p.out_row_stride + (int64_t)(hkv * G + r % G) * D;
@@ -482,14 +482,14 @@ __device__ __noinline__ void pf_store_rows(const PrefillParams &p, const CUtenso
 // pf_store_rows for one half of the head dimension (HALF kernel): the warp's 32
 // rows, dims [64 h, 64 h + 64) from O's columns of that half, staged in panel h
 // of the slot's P' rows and written by one TMA store; half 0 writes the lse.
-template <int D>
+template <int D, bool OBOX>
 __device__ __noinline__ void pf_store_rows_half(const PrefillParams &p, const CUtensorMap *omap, uint32_t tO,
                                                 uint8_t *pslot, bool has_tiles, int64_t qbase, int ntok, int hkv,
                                                 float l, float m_ref, int h) {
     const int G = p.G, lane = threadIdx.x & 31, wrow0 = ((threadIdx.x >> 5) & 3) * 32;
     if (wrow0 / G >= ntok) return;   // no valid row in this warp
     const int r = wrow0 + lane;
-    const bool row_valid = r / G < ntok, whole = (wrow0 + 31) / G < ntok;
+    const bool row_valid = r / G < ntok, whole = OBOX && (wrow0 + 31) / G < ntok;
     const float inv = l > 0.f ? 16.f / l : 0.f;   // l accumulated P' = 16 P
     uint8_t *srow = pslot + r * 128;
     __nv_bfloat16 *orow = p.out + (qbase + r / G) * p.out_row_stride + (int64_t)(hkv * G + r % G) * D;
@@ -541,7 +541,10 @@ __device__ __noinline__ void pf_store_rows_half(const PrefillParams &p, const CU
 // that sharing is worth little and the boundary costs weigh most.
 // HALF: every sequence fits one query slot (at most 128 / G tokens), so slot B
 // never has rows; its softmax warps take half of each of slot A's key tiles.
-template <int D, bool EARLY, bool HALF>
+// OBOX: G divides 128, so a slot is 128 rows and a warp's 32 output rows form one
+// (heads x tokens) TMA store box.  Otherwise a slot is 128 / G * G rows, the rest
+// of its Q rows are zeroed once, and output rows are written row by row.
+template <int D, bool EARLY, bool HALF, bool OBOX>
 __global__ void __launch_bounds__(kPfThreads, 1)
     attn_prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                         const __grid_constant__ CUtensorMap vmap, const __grid_constant__ CUtensorMap omap,
@@ -604,6 +607,20 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     if (warp == 9) {
         tmem_alloc(tmem_slot, 512);
         tmem_relinquish();
+    }
+    // When G does not divide 128 the Q loads fill rows [128 / G * G, 128) of a
+    // slot with nothing: zero them once, so those rows' scores are 0 (their
+    // outputs are never written)
+    if constexpr (!OBOX) {
+        const int pad = BM - (BM / G) * G;
+        constexpr int kSlots = HALF ? 1 : 2;
+        const int per_panel = pad * 8;   // 16-byte chunks
+        for (int i = threadIdx.x; i < kSlots * S::kPanels * per_panel; i += kPfThreads) {
+            const int panel = i / per_panel, c = i % per_panel;
+            *reinterpret_cast<uint4 *>(sQ + panel * S::kPanelBytes + (BM - pad) * 128 + c * 16) =
+                make_uint4(0u, 0u, 0u, 0u);
+        }
+        fence_proxy_async_smem();   // seen by the tensor core's reads
     }
     tc_fence_before();
     __syncthreads();
@@ -675,7 +692,10 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             if (lane == 0) {
                 if (w.n > 0) {
                     const bool activeB = !HALF && w.t0B < w.Lq;   // HALF: no Q_B buffer
-                    mbar_arrive_expect_tx(q_full, (uint32_t)S::kTileBytes * (activeB ? 2u : 1u));
+                    // a Q box is 128 / G tokens x G heads: 128 rows unless G does not divide 128
+                    const uint32_t q_bytes =
+                        OBOX ? (uint32_t)S::kTileBytes : (uint32_t)((BM / G) * G) * 128u * S::kPanels;
+                    mbar_arrive_expect_tx(q_full, q_bytes * (activeB ? 2u : 1u));
 #pragma unroll
                     for (int pn = 0; pn < S::kPanels; ++pn)
                         tma_load_3d(sQ + pn * S::kPanelBytes, &qmap, q_full, pn * 64, w.hkv * G, w.qs + w.t0A);
@@ -977,7 +997,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                     tc_fence_after();
                 }
                 if (pend) {
-                    pf_store_rows_half<D>(p, &omap, tO, sP, pend_tiles, pend_qbase, pend_ntok, pend_hkv, pend_l,
+                    pf_store_rows_half<D, OBOX>(p, &omap, tO, sP, pend_tiles, pend_qbase, pend_ntok, pend_hkv, pend_l,
                                           pend_m, h);
                     pend = false;
                 }
@@ -1011,7 +1031,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                     if (!ok) break;
                     tc_fence_after();
                 }
-                pf_store_rows_half<D>(p, &omap, tO, sP, pend_tiles, pend_qbase, pend_ntok, pend_hkv, pend_l, pend_m,
+                pf_store_rows_half<D, OBOX>(p, &omap, tO, sP, pend_tiles, pend_qbase, pend_ntok, pend_hkv, pend_l, pend_m,
                                       h);
             }
             cX += nX;
@@ -1029,7 +1049,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                                                        SRC_PREFILL));
             if (ok) {
                 tc_fence_after();
-                pf_store_rows_half<D>(p, &omap, tO, sP, pend_tiles, pend_qbase, pend_ntok, pend_hkv, pend_l, pend_m,
+                pf_store_rows_half<D, OBOX>(p, &omap, tO, sP, pend_tiles, pend_qbase, pend_ntok, pend_hkv, pend_l, pend_m,
                                       h);
             }
         }
@@ -1131,7 +1151,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                     tc_fence_after();
                 }
                 if (pend) {   // j == 0: O_X holds the previous unit's result
-                    pf_store_rows<D>(p, &omap, tO, pslot, pend_tiles, pend_qbase, pend_ntok, pend_hkv, pend_l, pend_m);
+                    pf_store_rows<D, OBOX>(p, &omap, tO, pslot, pend_tiles, pend_qbase, pend_ntok, pend_hkv, pend_l, pend_m);
                     pend = false;
                 }
                 // O *= alpha where the reference moved (O of tile 0 is written, not accumulated)
@@ -1169,7 +1189,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                     if (!ok) break;
                     tc_fence_after();
                 }
-                pf_store_rows<D>(p, &omap, tO, pslot, pend_tiles, pend_qbase, pend_ntok, pend_hkv, pend_l, pend_m);
+                pf_store_rows<D, OBOX>(p, &omap, tO, pslot, pend_tiles, pend_qbase, pend_ntok, pend_hkv, pend_l, pend_m);
             }
             cX += nX;
             pend = true;
@@ -1187,7 +1207,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                                                        SRC_PREFILL));
             if (ok) {
                 tc_fence_after();
-                pf_store_rows<D>(p, &omap, tO, pslot, pend_tiles, pend_qbase, pend_ntok, pend_hkv, pend_l, pend_m);
+                pf_store_rows<D, OBOX>(p, &omap, tO, pslot, pend_tiles, pend_qbase, pend_ntok, pend_hkv, pend_l, pend_m);
             }
         }
         if (lane == 0) bulk_wait_all();   // this warp's output stores are complete before it exits
@@ -1276,7 +1296,7 @@ cudaError_t launch_kvcache_cu(const int32_t *cache_seqlens, int batch, int seqle
     return cudaGetLastError();
 }
 
-template <int D, bool EARLY, bool HALF = false>
+template <int D, bool EARLY, bool HALF = false, bool OBOX = true>
 static cudaError_t launch_prefill_t(const CUtensorMap &qmap, const CUtensorMap &kmap, const CUtensorMap &vmap,
                                     const CUtensorMap &omap, const PrefillParams &p, cudaStream_t stream) {
     using S = PfSmem<D, HALF>;
@@ -1288,7 +1308,7 @@ static cudaError_t launch_prefill_t(const CUtensorMap &qmap, const CUtensorMap &
     if (dev < 0 || dev >= kMaxDev) return cudaErrorInvalidDevice;
     std::call_once(attr_once[dev], [&] {
         attr_err[dev] =
-            cudaFuncSetAttribute(attn_prefill_kernel<D, EARLY, HALF>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+            cudaFuncSetAttribute(attn_prefill_kernel<D, EARLY, HALF, OBOX>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  S::kBytes);
     });
     if (attr_err[dev] != cudaSuccess) return attr_err[dev];
@@ -1310,10 +1330,10 @@ static cudaError_t launch_prefill_t(const CUtensorMap &qmap, const CUtensorMap &
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, attn_prefill_kernel<D, EARLY, HALF>, qmap, kmap, vmap, omap, p);
+    e = cudaLaunchKernelEx(&cfg, attn_prefill_kernel<D, EARLY, HALF, OBOX>, qmap, kmap, vmap, omap, p);
     if (e == cudaErrorNotSupported || e == cudaErrorInvalidValue) {
         (void)cudaGetLastError();
-        attn_prefill_kernel<D, EARLY, HALF><<<p.num_ctas, kPfThreads, S::kBytes, stream>>>(qmap, kmap, vmap, omap,
+        attn_prefill_kernel<D, EARLY, HALF, OBOX><<<p.num_ctas, kPfThreads, S::kBytes, stream>>>(qmap, kmap, vmap, omap,
                                                                                            p);
         e = cudaGetLastError();
     }
@@ -1327,6 +1347,14 @@ cudaError_t launch_prefill(const CUtensorMap &qmap, const CUtensorMap &kmap, con
     // small, so its siblings gain little from sharing it through L2) or when every
     // sequence is one query pair (a unit has no siblings)
     // every sequence fits one query slot: slot B's softmax warps share slot A's tiles
+    // a group that does not divide 128: slots of 128 / G * G rows, output rows
+    // written row by row (three instances; the next unit always taken early)
+    if (kPrefillSlotRows % p.G != 0) {
+        if (head_dim == 128)
+            return p.one_slot ? launch_prefill_t<128, true, true, false>(qmap, kmap, vmap, omap, p, stream)
+                              : launch_prefill_t<128, true, false, false>(qmap, kmap, vmap, omap, p, stream);
+        return launch_prefill_t<64, false, false, false>(qmap, kmap, vmap, omap, p, stream);
+    }
     if (head_dim == 128 && p.one_slot)
         return launch_prefill_t<128, true, true>(qmap, kmap, vmap, omap, p, stream);
     if (head_dim == 128)

@@ -30,11 +30,12 @@
  *  - head_dim must be 64 or 128; num_heads_q must be a multiple of
  *    num_heads_kv (GQA: query head h reads KV head h / (num_heads_q /
  *    num_heads_kv)).  The prefill kernels (attn_varlen_fwd, attn_padded_fwd,
- *    the prefill route of attn_kvcache_fwd) also need the group size
- *    G = num_heads_q / num_heads_kv to divide 128 (G in 1, 2, 4, 8, ..., 128):
- *    a 128-row query slot packs 128 / G tokens x G heads.  Other groups
- *    (3, 5, 6, 7, ...) return ATTN_ERR_UNSUPPORTED there; the decode kernels
- *    take any G up to 64.
+ *    the prefill route of attn_kvcache_fwd) take a group size
+ *    G = num_heads_q / num_heads_kv up to 128: a 128-row query slot packs
+ *    floor(128 / G) tokens x G heads (for G = 3, 5, 6, 7, ... the last
+ *    128 - floor(128 / G) G rows of a slot stay idle, and the slot's output
+ *    rows are written row by row instead of by TMA boxes).  Larger groups
+ *    return ATTN_ERR_UNSUPPORTED there; the decode kernels take any G up to 64.
  *  - No function aborts, throws or prints.
  */
 #ifndef ATTN_VARLEN_H
@@ -112,8 +113,8 @@ typedef enum attn_status {
  * Value range: the P V product runs in fp16 on 16 P and V / 16, so V entries
  * must satisfy |v| < 2^20; larger (or non-finite) entries are clamped and
  * reported as ATTN_ERR_DEVICE_RANGE by attn_get_last_device_error.
- * Limits: head_dim 64 or 128, and G = num_heads_q / num_heads_kv must divide
- * 128 (1, 2, 4, ..., 128); anything else returns ATTN_ERR_UNSUPPORTED.
+ * Limits: head_dim 64 or 128, and G = num_heads_q / num_heads_kv at most 128
+ * (any G, dividing 128 or not); anything else returns ATTN_ERR_UNSUPPORTED.
  * Returns ATTN_OK, ATTN_ERR_INVALID_ARG, ATTN_ERR_UNSUPPORTED,
  * ATTN_ERR_WORKSPACE_TOO_SMALL, ATTN_ERR_LAUNCH_FAILED or ATTN_ERR_NO_DEVICE.
  * ------------------------------------------------------------------------ */
@@ -318,8 +319,8 @@ ATTN_API size_t attn_padded_workspace_size(int batch, int seqlen_q, int seqlen_k
  * [B, seqlen_q, H, D] and seqlen_q >= 1: chunked append, speculative
  * verification).  Two routes, chosen from the sizes and from whether
  * v16_cache is given:
- *  - seqlen_q * (num_heads_q / num_heads_kv) <= 64 (<= 16 with v16_cache when
- *    the group divides 128) and head_dim 64 or 128: the split-KV decode kernel of attn_decode_paged with
+ *  - seqlen_q * (num_heads_q / num_heads_kv) <= 64 (<= 16 with v16_cache)
+ *    and head_dim 64 or 128: the split-KV decode kernel of attn_decode_paged with
  *    one query column per (new token, head), up to 16 columns per CTA; the
  *    cache is read from HBM once (CTAs holding other columns of the same KV
  *    head re-read it from L2).  With seqlen_q = 1 the result equals

@@ -45,7 +45,7 @@ def test_host_validation_without_device(L):
     assert L.attn_varlen_fwd(*args(scale=0.0)) == 1
     assert L.attn_varlen_fwd(*args(scale=float("nan"))) == 1
     assert L.attn_varlen_fwd(*args(D=96)) == 2
-    assert L.attn_varlen_fwd(*args(Hq=12, Hkv=4)) == 2       # group of 3 does not divide the 128-row slot
+    assert L.attn_varlen_fwd(*args(Hq=258, Hkv=2)) == 2      # a group of 129 heads exceeds the 128-row slot
     assert L.attn_varlen_fwd(*args(qs=4 * 64 + 3)) == 1        # row stride not 16-byte aligned
     assert L.attn_varlen_fwd(*args(B=0)) == 1
     assert L.attn_varlen_fwd(*args(v16=fake)) == 1            # a V / 16 cache needs a block table

@@ -19,8 +19,8 @@ pytestmark = pytest.mark.gpu
 
 
 def _heads(rng):
-    """(Hq, Hkv) with a group that divides 128 (every entry takes it)."""
-    G = int(rng.choice([1, 2, 4, 8]))
+    """(Hq, Hkv) with a group of up to 8 heads (every entry takes it), some not dividing 128."""
+    G = int(rng.choice([1, 2, 3, 4, 5, 6, 8]))
     Hkv = int(rng.choice([1, 2, 4, 8]))
     while G * Hkv > 32:
         Hkv //= 2

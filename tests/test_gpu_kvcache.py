@@ -26,7 +26,7 @@ CASES = [
     (77, [300, 1500, 7], 8, 32, 8, 128, 64),         # 32 columns: two column groups
     (78, [129, 640], 5, 64, 8, 128, 16),             # 40 columns: three groups, the last one half full
     (79, [2000, 33], 64, 8, 8, 64, 32),              # G = 1, 64 new tokens: four groups
-    (80, [400, 1300], 8, 24, 8, 128, 64),            # G = 3 (not a divisor of 128): decode kernel even with V/16
+    (80, [400, 1300], 8, 24, 8, 128, 64),            # G = 3: decode kernel; with V/16 the prefill (42-token slots)
     # larger Sq x G: the paged varlen prefill
     (64, [90, 700, 1], 64, 16, 2, 64, 32),
     (65, [3000, 129], 130, 32, 8, 128, 128),

@@ -52,6 +52,14 @@ VARLEN_CASES = [
     (8, [256], [256], 32, 2, 128, True),
     (9, [700, 45], [700, 45], 32, 8, 64, True),
     (10, [1, 1, 1], [1, 2, 1000], 8, 8, 128, True),
+    # groups that do not divide 128: a slot holds 128 // G tokens (126, 125, 126, 96 rows);
+    # the rows past them are never stored, and a warp's rows are written row by row
+    (11, [1, 42, 43, 300, 85], [1, 42, 43, 300, 90], 24, 8, 128, True),   # G = 3: 42 tokens
+    (12, [100, 126, 7, 0], [250, 126, 7, 4], 10, 2, 64, True),             # G = 5: 25 tokens
+    (13, [50, 200], [50, 260], 12, 2, 128, False),                          # G = 6: 21 tokens
+    (14, [36, 19, 250], [36, 40, 250], 28, 4, 128, True),                   # G = 7: 18 tokens
+    (15, [5, 3, 2], [5, 100, 2], 48, 1, 64, True),                          # G = 48: 2 tokens
+    (16, [3, 2], [40, 2], 96, 1, 128, True),                                # G = 96: 1 token
 ]
 
 
@@ -145,6 +153,7 @@ ONE_SLOT_CASES = [
     (72, [128, 60, 3], [128, 2000, 3], 8, 8, True),
     (73, [16, 9, 1, 16], [4000, 9, 300, 17], 32, 4, True),    # G = 8: 16 tokens per slot
     (74, [32, 31, 5], [32, 600, 6000], 32, 8, False),
+    (75, [25, 3, 0, 25], [25, 900, 0, 4000], 40, 8, True),   # G = 5: 25 tokens, 125 of 128 rows
 ]
 
 
@@ -276,6 +285,7 @@ PAGED_CASES = [
     (32, [1000, 257, 0], [200, 1, 64], 32, 8, 128, 256),
     (33, [511, 2048], [129, 3], 8, 8, 128, 64),
     (34, [90, 700], [40, 333], 16, 2, 64, 32),
+    (35, [300, 17, 1000], [50, 3, 130], 40, 8, 128, 16),   # G = 5
 ]
 
 
