@@ -116,6 +116,9 @@ constexpr int kDecodeMaxColumns = 64;   // Sq x G query columns per KV head on t
 // ... with the fp16 V / 16 cache: past one column group of 16 the paged prefill
 // (tcgen05, no conversion pass with that cache) streams the cache faster
 constexpr int kDecodeMaxColumnsV16 = 16;
+// ... and without it at head_dim 128: past two column groups the one-slot prefill,
+// converting each V tile in shared memory, streams the cache faster
+constexpr int kDecodeMaxColumnsCvt = 32;
 constexpr int kDecodeTile = 64;
 
 // Tokens a split streams at most when the library chooses the split count: long
@@ -172,8 +175,8 @@ size_t decode_partial_bytes(int batch, int seqlen_q, int num_heads_q, int head_d
 
 // The kv-cache entry runs on the decode kernel when the Sq x G query rows of a
 // KV head fit four column groups of 16 (one group when the fp16 V / 16 cache is
-// given and the prefill can take the group size); otherwise on the paged
-// varlen prefill.
+// given, two at head_dim 128 without it, where the prefill can take the group
+// size); otherwise on the paged varlen prefill.
 bool kvcache_on_decode(int batch, int seqlen_q, int num_heads_q, int num_heads_kv, int head_dim, bool v16) {
     if (num_heads_q <= 0 || num_heads_kv <= 0 || num_heads_q % num_heads_kv) return false;
     if (head_dim != 64 && head_dim != 128) return false;
@@ -181,7 +184,10 @@ bool kvcache_on_decode(int batch, int seqlen_q, int num_heads_q, int num_heads_k
     const int G = num_heads_q / num_heads_kv;
     // the prefill packs 128 / G tokens x G heads per query slot: larger groups stay here
     const bool prefill_ok = G <= kPrefillSlotRows;
-    return (int64_t)seqlen_q * G <= (v16 && prefill_ok ? kDecodeMaxColumnsV16 : kDecodeMaxColumns);
+    int cap = kDecodeMaxColumns;
+    if (prefill_ok && v16) cap = kDecodeMaxColumnsV16;
+    else if (prefill_ok && head_dim == 128) cap = kDecodeMaxColumnsCvt;
+    return (int64_t)seqlen_q * G <= cap;
 }
 
 struct DecodeCall {
@@ -411,6 +417,14 @@ static int64_t varlen_max_pairs(int num_heads_q, int num_heads_kv, int max_seqle
     return ((int64_t)max_seqlen_q + 2 * tps - 1) / (2 * tps);
 }
 
+// Launches whose sequences all fit one query slot (max_seqlen_q <= 128 / G) at
+// head_dim 128 run the one-slot instance, which converts bf16 V tiles to V' in
+// shared memory when no V' cache is given.
+static bool one_slot_cvt(int num_heads_q, int num_heads_kv, int head_dim, int max_seqlen_q) {
+    const int G = num_heads_q / num_heads_kv;
+    return head_dim == 128 && G >= 1 && G <= kPrefillSlotRows && max_seqlen_q <= kPrefillSlotRows / G;
+}
+
 static size_t v16_bytes(int num_heads_kv, int head_dim, int64_t total_k) {
     const size_t b = (size_t)total_k * (size_t)num_heads_kv * (size_t)head_dim * 2;
     return (b + 255) & ~(size_t)255;
@@ -420,6 +434,8 @@ size_t attn_varlen_workspace_size(int batch, int num_heads_q, int num_heads_kv, 
                                   int64_t total_k) {
     const int64_t mp = varlen_max_pairs(num_heads_q, num_heads_kv, max_seqlen_q);
     if (batch <= 0 || mp < 0 || head_dim <= 0 || total_k < 0) return 0;
+    // a one-slot launch at head_dim 128 converts V in the kernel: no V' copy
+    if (one_slot_cvt(num_heads_q, num_heads_kv, head_dim, max_seqlen_q)) total_k = 0;
     return kWsHeader + v16_bytes(num_heads_kv, head_dim, total_k) +
            (size_t)batch * (size_t)mp * (size_t)num_heads_kv * sizeof(int2);
 }
@@ -474,8 +490,12 @@ static attn_status varlen_impl(const void *q, const void *k, const void *v, void
     if (max_pairs <= 0 || max_pairs > 0xFFFF || num_heads_kv > 0x7FFF ||
         (int64_t)batch * max_pairs * num_heads_kv > (int64_t)INT32_MAX / 4)
         return ATTN_ERR_UNSUPPORTED;
-    // with a paged V' cache the workspace holds no V' copy (sized for total_k = 0)
-    const int64_t ws_keys = v16_cache ? 0 : total_k;
+    // the one-slot instance (head_dim 128, every sequence within one slot) converts
+    // bf16 V tiles to V' in shared memory itself: no conversion pass, no V' copy
+    const bool v_cvt = !v16_cache && one_slot_cvt(num_heads_q, num_heads_kv, head_dim, max_seqlen_q);
+    // with a paged V' cache, or converting in the kernel, the workspace holds no V'
+    // copy (sized for total_k = 0)
+    const int64_t ws_keys = (v16_cache || v_cvt) ? 0 : total_k;
     const size_t ws_need = attn_varlen_workspace_size(batch, num_heads_q, num_heads_kv, head_dim, max_seqlen_q, ws_keys);
     if (!workspace || workspace_bytes < ws_need) return ATTN_ERR_WORKSPACE_TOO_SMALL;
     if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return ATTN_ERR_INVALID_ARG;
@@ -490,11 +510,16 @@ static attn_status varlen_impl(const void *q, const void *k, const void *v, void
         !make_map(&kmap, k, kv_rows, num_heads_kv, head_dim, k_row_stride, 1, kv_box) ||
         !make_map(&omap, out, total_q, num_heads_q, head_dim, out_row_stride, obh, 32 / obh))
         return ATTN_ERR_LAUNCH_FAILED;
-    if (v16_cache ? !make_map(&vmap, v16_cache, kv_rows, num_heads_kv, head_dim, (int64_t)num_heads_kv * head_dim, 1,
-                              kv_box, CU_TENSOR_MAP_DATA_TYPE_FLOAT16)
-                  : !make_map(&vmap, v16, total_k, num_heads_kv, head_dim, (int64_t)num_heads_kv * head_dim, 1,
-                              kPrefillKeyTile, CU_TENSOR_MAP_DATA_TYPE_FLOAT16))
-        return ATTN_ERR_LAUNCH_FAILED;
+    bool vmap_ok;
+    if (v16_cache)
+        vmap_ok = make_map(&vmap, v16_cache, kv_rows, num_heads_kv, head_dim, (int64_t)num_heads_kv * head_dim, 1,
+                           kv_box, CU_TENSOR_MAP_DATA_TYPE_FLOAT16);
+    else if (v_cvt)
+        vmap_ok = make_map(&vmap, v, kv_rows, num_heads_kv, head_dim, v_row_stride, 1, kv_box);
+    else
+        vmap_ok = make_map(&vmap, v16, total_k, num_heads_kv, head_dim, (int64_t)num_heads_kv * head_dim, 1,
+                           kPrefillKeyTile, CU_TENSOR_MAP_DATA_TYPE_FLOAT16);
+    if (!vmap_ok) return ATTN_ERR_LAUNCH_FAILED;
 
     PrefillParams p;
     memset(&p, 0, sizeof p);
@@ -526,6 +551,7 @@ static attn_status varlen_impl(const void *q, const void *k, const void *v, void
     p.causal = causal ? 1 : 0;
     p.max_pairs = (int)max_pairs;
     p.one_slot = max_seqlen_q <= tps ? 1 : 0;
+    p.v_cvt = v_cvt ? 1 : 0;
     // persistent CTAs: one per SM (fewer when there are fewer possible units)
     const int64_t max_units = (int64_t)batch * max_pairs * num_heads_kv;
     p.num_ctas = (int)(max_units < d->num_sms ? max_units : d->num_sms);

@@ -54,6 +54,8 @@ struct PrefillParams {
                                  //    table (written by store_kvcache); no conversion pass
     int num_ctas;                // grid size: persistent CTAs (one per SM, at most the possible units)
     int one_slot;                // 1: max_seqlen_q <= 128 / G, every sequence fits one query slot
+    int v_cvt;                   // 1 (one-slot launches without a V' cache): V tiles are loaded as bf16
+                                 //    from v and converted to V' in shared memory; no conversion pass
     int2 *units;                 // workspace: (sequence, pair | kv_head << 16), scheduled order
     int *unit_count;             // workspace: [0] number of units
     float scale_log2;            // softmax_scale * log2(e), > 0

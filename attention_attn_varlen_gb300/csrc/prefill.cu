@@ -346,16 +346,16 @@ __device__ __forceinline__ void schedule_units(const PrefillParams &p) {
 // ---------------------------------------------------------------------------
 // Pre-pass before the attention kernel, one launch: CTA (0, 0) writes the unit
 // list (schedule_units); CTAs (x, b + 1) convert V of sequence b to V'
-// (v_to_f16_keys).  With a paged V' cache (v16_paged) the launch is the
-// scheduler's CTA alone.
+// (v_to_f16_keys).  With a paged V' cache (v16_paged), or when the one-slot
+// instance converts V tiles itself (v_cvt), the launch is the scheduler's CTA alone.
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(kCvtThreads) attn_prefill_prep_kernel(const PrefillParams p) {
     // the attention kernel may be scheduled now (it waits for this grid before
     // reading anything it writes)
     asm volatile("griddepcontrol.launch_dependents;");
-    if (p.v16_paged || blockIdx.y == 0) {
-        // the scheduler (grid row 0, dispatched first); with a paged V' cache there is
-        // nothing to convert and the launch is this one CTA
+    if (p.v16_paged || p.v_cvt || blockIdx.y == 0) {
+        // the scheduler (grid row 0, dispatched first); with a paged V' cache, or when
+        // the attention kernel converts V itself, the launch is this one CTA
         if (blockIdx.x == 0) schedule_units(p);
         return;
     }
@@ -533,6 +533,43 @@ __device__ __noinline__ void pf_store_rows_half(const PrefillParams &p, const CU
     }
 }
 
+// One-slot instance without a V' cache: the 256 softmax threads convert a bf16 V
+// tile in its ring stage to V' = fp16(V / 16) in place (the 128-byte swizzle only
+// permutes 16-byte chunks within a key row, so every chunk keeps its row and
+// its element order).  Rows at or past `valid` (keys past the sequence's end)
+// are zeroed; |v| >= 2^20 or non-finite is clamped and reported, as in the
+// conversion pass.  The caller's proxy fence and p_ready arrival publish it.
+template <int D>
+__device__ __forceinline__ void v_tile_to_f16(uint8_t *tile, int valid, uint32_t *err) {
+    constexpr int kChunks = (D / 64) * BN * 8;   // 16-byte chunks in the tile
+    uint32_t big = 0;
+#pragma unroll
+    for (int b0 = 0; b0 < kChunks / 256; b0 += 4) {
+        uint4 v[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            v[i] = *reinterpret_cast<const uint4 *>(tile + (size_t)(threadIdx.x + (b0 + i) * 256) * 16);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int c = threadIdx.x + (b0 + i) * 256;
+            uint4 w = v[i];
+            if (((c >> 3) & (BN - 1)) >= valid) {
+                w = make_uint4(0u, 0u, 0u, 0u);
+            } else {
+                big = __vmaxu2(big, __vmaxu2(w.x & 0x7FFF7FFFu, w.y & 0x7FFF7FFFu));
+                big = __vmaxu2(big, __vmaxu2(w.z & 0x7FFF7FFFu, w.w & 0x7FFF7FFFu));
+                w.x = bf16x2_to_f16x2_div16(w.x);
+                w.y = bf16x2_to_f16x2_div16(w.y);
+                w.z = bf16x2_to_f16x2_div16(w.z);
+                w.w = bf16x2_to_f16x2_div16(w.w);
+            }
+            *reinterpret_cast<uint4 *>(tile + (size_t)c * 16) = w;
+        }
+    }
+    if (__any_sync(0xffffffffu, (big & 0xFFFFu) >= 0x4980u || (big >> 16) >= 0x4980u) && (threadIdx.x & 31) == 0)
+        record_error(err, ERR_RANGE | SRC_PREFILL);
+}
+
 // EARLY: the producer takes and publishes the next unit's index at the start of
 // each unit, so every role has it a whole unit ahead (the unit boundary costs
 // less).  Otherwise it takes it when it starts the unit's loads, which keeps
@@ -544,7 +581,9 @@ __device__ __noinline__ void pf_store_rows_half(const PrefillParams &p, const CU
 // OBOX: G divides 128, so a slot is 128 rows and a warp's 32 output rows form one
 // (heads x tokens) TMA store box.  Otherwise a slot is 128 / G * G rows, the rest
 // of its Q rows are zeroed once, and output rows are written row by row.
-template <int D, bool EARLY, bool HALF, bool OBOX>
+// CVT (HALF only, no V' cache): V tiles are loaded as bf16 from v and the softmax
+// warps convert each to V' in its ring stage (no conversion pass).
+template <int D, bool EARLY, bool HALF, bool OBOX, bool CVT>
 __global__ void __launch_bounds__(kPfThreads, 1)
     attn_prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                         const __grid_constant__ CUtensorMap vmap, const __grid_constant__ CUtensorMap omap,
@@ -739,8 +778,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                         mbar_arrive_expect_tx(bar, (uint32_t)S::kTileBytes);
                         // V' converted by the pre-pass is contiguous by logical key (rows past
                         // the sequence hold the next sequence's keys or zeroed rows); a paged
-                        // V' cache is read through the block table like K
-                        if (!paged || (wv == 1 && !p.v16_paged)) {
+                        // V' cache, or bf16 V converted here, is read like K
+                        if (!paged || (wv == 1 && !p.v16_paged && !CVT)) {
 #pragma unroll
                             for (int pn = 0; pn < S::kPanels; ++pn)
                                 tma_load_3d(dst + pn * S::kPanelBytes, map, bar, pn * 64, w.hkv, w.ks0 + key0);
@@ -924,6 +963,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         int64_t pend_qbase = 0;
         int pend_ntok = 0, pend_hkv = 0;
         float pend_l = 0.f, pend_m = 0.f;
+        int itb = 0;          // CVT: ring items before this unit (the producer's order)
+        uint32_t vpar = 0;    // CVT: per stage, parity of the V tiles read from it
         for (;; ++k) {
             ok = __all_sync(0xffffffffu,
                             mbar_wait(&idx_full[k & 1], (uint32_t)(k >> 1) & 1u, abort_flag, p.err, SRC_PREFILL));
@@ -990,6 +1031,16 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                     pk[i] = pack_f16x2(x0, x1);
                 }
                 l += ((la[0] + lb[0]) + (la[1] + lb[1])) + ((la[2] + lb[2]) + (la[3] + lb[3]));
+                if constexpr (CVT) {
+                    // V tile j (bf16 as loaded) -> V' = fp16(V / 16) in place, before p_ready;
+                    // rows past the sequence's last key are zeroed
+                    const int itV = itb + (j < nX - 1 ? 2 * j + 2 : 2 * nX - 1), stV = itV % ST;
+                    ok = __all_sync(0xffffffffu, mbar_wait(&full_v[stV], (vpar >> stV) & 1u, abort_flag, p.err,
+                                                           SRC_PREFILL));
+                    vpar ^= 1u << stV;
+                    if (!ok) break;
+                    v_tile_to_f16<D>(sRing + stV * S::kTileBytes, w.Lk - j * BN, p.err);
+                }
                 if (t > 0) {
                     ok = __all_sync(0xffffffffu, mbar_wait(&pv_done[0], (uint32_t)(t - 1) & 1u, abort_flag, p.err,
                                                            SRC_PREFILL));
@@ -1035,6 +1086,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                                       h);
             }
             cX += nX;
+            if constexpr (CVT) itb += 2 * w.n;
             pend = true;
             pend_tiles = nX > 0;
             pend_qbase = (int64_t)w.qs + t0;
@@ -1296,7 +1348,7 @@ cudaError_t launch_kvcache_cu(const int32_t *cache_seqlens, int batch, int seqle
     return cudaGetLastError();
 }
 
-template <int D, bool EARLY, bool HALF = false, bool OBOX = true>
+template <int D, bool EARLY, bool HALF = false, bool OBOX = true, bool CVT = false>
 static cudaError_t launch_prefill_t(const CUtensorMap &qmap, const CUtensorMap &kmap, const CUtensorMap &vmap,
                                     const CUtensorMap &omap, const PrefillParams &p, cudaStream_t stream) {
     using S = PfSmem<D, HALF>;
@@ -1308,13 +1360,14 @@ static cudaError_t launch_prefill_t(const CUtensorMap &qmap, const CUtensorMap &
     if (dev < 0 || dev >= kMaxDev) return cudaErrorInvalidDevice;
     std::call_once(attr_once[dev], [&] {
         attr_err[dev] =
-            cudaFuncSetAttribute(attn_prefill_kernel<D, EARLY, HALF, OBOX>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+            cudaFuncSetAttribute(attn_prefill_kernel<D, EARLY, HALF, OBOX, CVT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  S::kBytes);
     });
     if (attr_err[dev] != cudaSuccess) return attr_err[dev];
     // unit list and V' in one launch: grid row 0 holds the scheduler (dispatched
     // before the conversion CTAs); with a paged V' cache the scheduler alone
-    const dim3 cgrid = p.v16_paged ? dim3(1, 1) : dim3((p.max_seqlen_k + kCvtKeys - 1) / kCvtKeys, p.batch + 1);
+    const dim3 cgrid = (p.v16_paged || p.v_cvt) ? dim3(1, 1)
+                                                : dim3((p.max_seqlen_k + kCvtKeys - 1) / kCvtKeys, p.batch + 1);
     attn_prefill_prep_kernel<<<cgrid, kCvtThreads, 0, stream>>>(p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
@@ -1330,10 +1383,10 @@ static cudaError_t launch_prefill_t(const CUtensorMap &qmap, const CUtensorMap &
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, attn_prefill_kernel<D, EARLY, HALF, OBOX>, qmap, kmap, vmap, omap, p);
+    e = cudaLaunchKernelEx(&cfg, attn_prefill_kernel<D, EARLY, HALF, OBOX, CVT>, qmap, kmap, vmap, omap, p);
     if (e == cudaErrorNotSupported || e == cudaErrorInvalidValue) {
         (void)cudaGetLastError();
-        attn_prefill_kernel<D, EARLY, HALF, OBOX><<<p.num_ctas, kPfThreads, S::kBytes, stream>>>(qmap, kmap, vmap, omap,
+        attn_prefill_kernel<D, EARLY, HALF, OBOX, CVT><<<p.num_ctas, kPfThreads, S::kBytes, stream>>>(qmap, kmap, vmap, omap,
                                                                                            p);
         e = cudaGetLastError();
     }
@@ -1343,20 +1396,23 @@ static cudaError_t launch_prefill_t(const CUtensorMap &qmap, const CUtensorMap &
 
 cudaError_t launch_prefill(const CUtensorMap &qmap, const CUtensorMap &kmap, const CUtensorMap &vmap,
                            const CUtensorMap &omap, const PrefillParams &p, int head_dim, cudaStream_t stream) {
+    // a group that does not divide 128: slots of 128 / G * G rows, output rows
+    // written row by row (the next unit always taken early; with a V' cache a
+    // one-slot launch takes the two-slot instance)
+    if (kPrefillSlotRows % p.G != 0) {
+        if (head_dim == 128)
+            return p.v_cvt ? launch_prefill_t<128, true, true, false, true>(qmap, kmap, vmap, omap, p, stream)
+                           : launch_prefill_t<128, true, false, false>(qmap, kmap, vmap, omap, p, stream);
+        return launch_prefill_t<64, false, false, false>(qmap, kmap, vmap, omap, p, stream);
+    }
+    // every sequence fits one query slot: slot B's softmax warps share slot A's
+    // tiles, and convert V tiles themselves unless a V' cache is read
+    if (head_dim == 128 && p.one_slot)
+        return p.v_cvt ? launch_prefill_t<128, true, true, true, true>(qmap, kmap, vmap, omap, p, stream)
+                       : launch_prefill_t<128, true, true>(qmap, kmap, vmap, omap, p, stream);
     // the next unit taken a unit ahead when keys are short (each unit's K / V is
     // small, so its siblings gain little from sharing it through L2) or when every
     // sequence is one query pair (a unit has no siblings)
-    // every sequence fits one query slot: slot B's softmax warps share slot A's tiles
-    // a group that does not divide 128: slots of 128 / G * G rows, output rows
-    // written row by row (three instances; the next unit always taken early)
-    if (kPrefillSlotRows % p.G != 0) {
-        if (head_dim == 128)
-            return p.one_slot ? launch_prefill_t<128, true, true, false>(qmap, kmap, vmap, omap, p, stream)
-                              : launch_prefill_t<128, true, false, false>(qmap, kmap, vmap, omap, p, stream);
-        return launch_prefill_t<64, false, false, false>(qmap, kmap, vmap, omap, p, stream);
-    }
-    if (head_dim == 128 && p.one_slot)
-        return launch_prefill_t<128, true, true>(qmap, kmap, vmap, omap, p, stream);
     if (head_dim == 128)
         return (p.max_seqlen_k <= kEarlyMaxKeys || p.max_pairs == 1)
                    ? launch_prefill_t<128, true>(qmap, kmap, vmap, omap, p, stream)

@@ -103,13 +103,18 @@ typedef enum attn_status {
  *                kept by store_kvcache (its v16_cache argument).  The P V
  *                product then reads V / 16 from it through the block table and
  *                the call converts nothing; without it each call writes an fp16
- *                copy of the V rows it reads into the workspace.  (A paged V
- *                tile past a sequence's last key is zeroed in shared memory, so
+ *                copy of the V rows it reads into the workspace, except when
+ *                head_dim is 128 and every sequence fits one query slot
+ *                (max_seqlen_q <= 128 / G): that kernel loads bf16 V tiles and
+ *                converts each to V / 16 in shared memory.  (A paged V tile
+ *                past a sequence's last key is zeroed in shared memory, so
  *                cache slots past the end may hold anything.)
  *   workspace    device scratch of at least attn_varlen_workspace_size(...)
- *                bytes, 256-byte aligned: without v16_cache it receives an fp16
- *                copy of V (V / 16) laid out by logical key, which the P V
- *                product reads; with v16_cache size it with total_k = 0
+ *                bytes, 256-byte aligned: without v16_cache (and outside the
+ *                one-slot case above) it receives an fp16 copy of V (V / 16)
+ *                laid out by logical key, which the P V product reads; with
+ *                v16_cache size it with total_k = 0 (the size function itself
+ *                leaves the copy out for one-slot sizes at head_dim 128)
  * Value range: the P V product runs in fp16 on 16 P and V / 16, so V entries
  * must satisfy |v| < 2^20; larger (or non-finite) entries are clamped and
  * reported as ATTN_ERR_DEVICE_RANGE by attn_get_last_device_error.
@@ -319,15 +324,17 @@ ATTN_API size_t attn_padded_workspace_size(int batch, int seqlen_q, int seqlen_k
  * [B, seqlen_q, H, D] and seqlen_q >= 1: chunked append, speculative
  * verification).  Two routes, chosen from the sizes and from whether
  * v16_cache is given:
- *  - seqlen_q * (num_heads_q / num_heads_kv) <= 64 (<= 16 with v16_cache)
- *    and head_dim 64 or 128: the split-KV decode kernel of attn_decode_paged with
+ *  - seqlen_q * (num_heads_q / num_heads_kv) <= 64 at head_dim 64, <= 32 at
+ *    head_dim 128, <= 16 with v16_cache: the split-KV decode kernel of attn_decode_paged with
  *    one query column per (new token, head), up to 16 columns per CTA; the
  *    cache is read from HBM once (CTAs holding other columns of the same KV
  *    head re-read it from L2).  With seqlen_q = 1 the result equals
  *    attn_decode_paged's bit for bit.
  *  - otherwise: cu_seqlens_q = b * seqlen_q and cu_seqlens_k = prefix sums of
  *    cache_seqlens are computed on the device, then the paged varlen prefill
- *    (attn_varlen_fwd) runs.
+ *    (attn_varlen_fwd) runs; up to 128 query rows per KV head at head_dim 128
+ *    that is the one-slot kernel, which converts V tiles itself when no
+ *    v16_cache is given.
  *
  *   q, out       [batch * seqlen_q, num_heads_q, head_dim] bf16, packed
  *                (the article's [B, seqlen_q, H, D])
@@ -348,8 +355,9 @@ ATTN_API size_t attn_padded_workspace_size(int batch, int seqlen_q, int seqlen_k
  *                either route, with or without v16_cache), 256-byte
  *                aligned.  On the decode route it holds the split partials
  *                (at most 64 splits of fp32 rows); on the prefill route without
- *                v16_cache the fp16 copy of V for batch * max_cache_seqlen keys,
- *                so there it grows with the cache length.
+ *                v16_cache and past one query slot (or at head_dim 64) the fp16
+ *                copy of V for batch * max_cache_seqlen keys, so there it grows
+ *                with the cache length.
  * Returns the statuses of attn_varlen_fwd.
  * ------------------------------------------------------------------------ */
 ATTN_API attn_status attn_kvcache_fwd(const void *q, const void *k_cache, const void *v_cache, void *out,

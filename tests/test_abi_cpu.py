@@ -94,9 +94,16 @@ def test_new_workspace_sizes_are_host_side(L):
     L.attn_padded_workspace_size.restype = ctypes.c_size_t
     assert L.attn_kvcache_workspace_size(0, 1, 32, 8, 128, 100) == 0
     assert L.attn_padded_workspace_size(2, 0, 16, 8, 8, 64) == 0
-    a = L.attn_kvcache_workspace_size(4, 17, 32, 8, 128, 1000)
-    b = L.attn_kvcache_workspace_size(4, 17, 32, 8, 128, 2000)
-    assert 0 < a < b            # prefill route (17 x 4 query rows per KV head): the fp16 V' copy grows with the cache
+    a = L.attn_kvcache_workspace_size(4, 40, 32, 8, 128, 1000)
+    b = L.attn_kvcache_workspace_size(4, 40, 32, 8, 128, 2000)
+    assert 0 < a < b            # two-slot prefill route (40 x 4 query rows per KV head): the fp16 V' copy grows with the cache
+    # one-slot prefill route at head_dim 128 (17 x 4 rows): V tiles are converted in the kernel, no V' copy
+    assert 0 < L.attn_kvcache_workspace_size(4, 17, 32, 8, 128, 1000) == L.attn_kvcache_workspace_size(4, 17, 32, 8, 128, 1 << 20)
+    L.attn_varlen_workspace_size.restype = ctypes.c_size_t
+    i64 = ctypes.c_int64
+    assert L.attn_varlen_workspace_size(4, 32, 8, 128, 32, i64(1000)) == L.attn_varlen_workspace_size(4, 32, 8, 128, 32, i64(10 ** 7))
+    assert L.attn_varlen_workspace_size(4, 32, 8, 128, 33, i64(1000)) < L.attn_varlen_workspace_size(4, 32, 8, 128, 33, i64(10 ** 7))
+    assert L.attn_varlen_workspace_size(4, 32, 8, 64, 32, i64(1000)) < L.attn_varlen_workspace_size(4, 32, 8, 64, 32, i64(10 ** 7))
     # decode route (3 x 4 rows): only split partials, at most 64 splits of fp32 rows, whatever the cache length
     for n in (0, 1000, 1 << 20):
         c = L.attn_kvcache_workspace_size(4, 3, 32, 8, 128, n)

@@ -24,10 +24,12 @@ CASES = [
     (71, [1200, 5, 64], 1, 32, 2, 128, 16),          # G = 16, one token
     (72, [64, 0, 191], 3, 16, 4, 64, 16),            # twelve live columns of sixteen
     (77, [300, 1500, 7], 8, 32, 8, 128, 64),         # 32 columns: two column groups
-    (78, [129, 640], 5, 64, 8, 128, 16),             # 40 columns: three groups, the last one half full
+    (78, [129, 640], 5, 64, 8, 64, 16),              # 40 columns at head_dim 64: three groups, the last one half full
     (79, [2000, 33], 64, 8, 8, 64, 32),              # G = 1, 64 new tokens: four groups
     (80, [400, 1300], 8, 24, 8, 128, 64),            # G = 3: decode kernel; with V/16 the prefill (42-token slots)
-    # larger Sq x G: the paged varlen prefill
+    # larger Sq x G: the paged varlen prefill (at head_dim 128 past 32 columns: one slot, V converted in the kernel)
+    (81, [129, 640, 3000], 5, 64, 8, 128, 16),       # 40 columns
+    (82, [2000, 17, 0, 900], 16, 32, 8, 128, 64),    # 64 columns
     (64, [90, 700, 1], 64, 16, 2, 64, 32),
     (65, [3000, 129], 130, 32, 8, 128, 128),
     (73, [400, 20], 17, 32, 8, 128, 64),

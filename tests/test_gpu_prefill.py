@@ -308,6 +308,41 @@ def test_paged_prefill_v16_cache_is_bitexact(seed, ctx, new, Hq, Hkv, D, bs):
     assert torch.equal(lse_a, lse_b)
 
 
+ONE_SLOT_PAGED_CASES = [
+    # seed, ctx, new, Hq, Hkv, block_size: head_dim 128, every sequence's new tokens within one slot
+    (36, [37, 900, 0, 300], [8, 8, 8, 1], 32, 8, 16),
+    (37, [5000, 129], [32, 3], 32, 8, 64),
+    (38, [700, 20, 3000], [25, 25, 2], 40, 8, 256),   # G = 5: 25-token slots
+]
+
+
+@pytest.mark.parametrize("seed,ctx,new,Hq,Hkv,bs", ONE_SLOT_PAGED_CASES)
+def test_one_slot_converts_v_in_the_kernel(seed, ctx, new, Hq, Hkv, bs):
+    """One-slot launches without a V / 16 cache load each bf16 V tile and convert it
+    to V / 16 in shared memory (no conversion pass, no V' copy): the oracle's
+    values, and for groups dividing 128 the bits of the call reading the fp16 V / 16
+    cache, although the bf16 cache slots past every sequence hold NaN (the converted
+    tile's rows past the sequence are zeroed)."""
+    cfg = workloads.small_paged(seed, ctx=ctx, new=new, Hq=Hq, Hkv=Hkv, D=128, block_size=bs)
+    assert max(new) <= 128 // (Hq // Hkv)
+    q = cfg.q()
+    kc, vc, k_new, v_new = _paged_device(cfg)
+    assert torch.isnan(vc.float()).any()
+    av.get_last_device_error()
+    out_a, lse_a = _run_paged(cfg, q, kc, vc)
+    out_b, lse_b = _run_paged(cfg, q, kc, vc, v16_of(vc))
+    torch.cuda.synchronize()
+    assert av.get_last_device_error()[0] == 0
+    ref, ref_lse, _ = _paged_oracle(cfg, q, k_new, v_new, list(range(cfg.batch)))
+    assert_close(out_a, ref.reshape(out_a.shape), f"one-slot in-kernel V' {ctx}+{new}")
+    assert_lse_close(lse_a.t().contiguous(), ref_lse.reshape(-1, Hq), "one-slot in-kernel V' lse")
+    if 128 % (Hq // Hkv) == 0:
+        assert torch.equal(out_a.view(torch.int16), out_b.view(torch.int16))
+        assert torch.equal(lse_a, lse_b)
+    else:   # with the V / 16 cache such a group runs the two-slot instance (other row-sum order)
+        assert_close(out_b, ref.reshape(out_b.shape), f"one-slot V' cache {ctx}+{new}")
+
+
 @pytest.mark.parametrize("seed,ctx,new,Hq,Hkv,D,bs", PAGED_CASES)
 def test_paged_prefill_matches_oracle(seed, ctx, new, Hq, Hkv, D, bs):
     cfg = workloads.small_paged(seed, ctx=ctx, new=new, Hq=Hq, Hkv=Hkv, D=D, block_size=bs)
@@ -444,8 +479,11 @@ def test_value_scale_of_v(vscale):
     assert rel <= 2e-3, rel
 
 
-def test_v_beyond_fp16_range_is_reported():
-    cfg = workloads.small_varlen(53, [100], [100], 4, 4, 128)
+@pytest.mark.parametrize("L", [100, 300])
+def test_v_beyond_fp16_range_is_reported(L):
+    """|v| >= 2^20 is clamped and reported: by the one-slot kernel's own conversion
+    (100 tokens) and by the conversion pass (300 tokens, two slots)."""
+    cfg = workloads.small_varlen(53, [L], [L], 4, 4, 128)
     q, k, v = cfg.q(), cfg.k(), cfg.v().clone()
     v[5, 0, 3] = 3.0e6
     av.get_last_device_error()
