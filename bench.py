@@ -173,6 +173,8 @@ KERNEL_SOURCES = {
     "decode_sq8": ["attention_attn_varlen_gb300/csrc/decode.cu", "attention_attn_varlen_gb300/csrc/common.cuh"],
     "kvcache_sq4_v16": ["attention_attn_varlen_gb300/csrc/decode.cu", "attention_attn_varlen_gb300/csrc/common.cuh"],
     "kvcache_sq8_v16": ["attention_attn_varlen_gb300/csrc/prefill.cu", "attention_attn_varlen_gb300/csrc/common.cuh"],
+    "kvcache_sq16": ["attention_attn_varlen_gb300/csrc/prefill.cu", "attention_attn_varlen_gb300/csrc/common.cuh"],
+    "kvcache_sq16_v16": ["attention_attn_varlen_gb300/csrc/prefill.cu", "attention_attn_varlen_gb300/csrc/common.cuh"],
     "store": ["attention_attn_varlen_gb300/csrc/store_kvcache.cu", "attention_attn_varlen_gb300/csrc/common.cuh"],
     "softmax_warp": ["attention_attn_varlen_gb300/csrc/softmax.cu", "attention_attn_varlen_gb300/csrc/common.cuh"],
     "softmax_cta_reg": ["attention_attn_varlen_gb300/csrc/softmax.cu", "attention_attn_varlen_gb300/csrc/common.cuh"],
@@ -343,7 +345,7 @@ def bench_decode(av, device, steps, warmup, flush, peaks, with_oracle=True):
     v16 = torch.empty(kc.shape, dtype=torch.float16, device=device)
     for i in range(0, cfg.num_blocks, 256):
         v16[i:i + 256] = (vc[i:i + 256].float() / 16.0).half()
-    for Sq in (4, 8):
+    for Sq in (4, 8, 16):
         qn = torch.randn(cfg.batch, Sq, cfg.Hq, cfg.D, device=device, generator=g).to(torch.bfloat16)
         wsn = torch.empty(av.lib().attn_kvcache_workspace_size(cfg.batch, Sq, cfg.Hq, cfg.Hkv, cfg.D, mx),
                           dtype=torch.uint8, device=device)
@@ -359,16 +361,24 @@ def bench_decode(av, device, steps, warmup, flush, peaks, with_oracle=True):
         tkn = float(np.mean(kmsn)) / 1e3
         fln = workloads.prefill_flops(np.full(cfg.batch, Sq), cfg.ctx, cfg.Hq, cfg.D)
         nbn = nbytes + 2 * cfg.batch * (Sq - 1) * cfg.Hq * cfg.D * 2    # the extra query and output rows
+        # past 32 query rows per KV head (head_dim 128) the entry runs the one-slot
+        # paged prefill, which converts the bf16 V tiles in shared memory
+        rows = Sq * cfg.Hq // cfg.Hkv
+        on_prefill_n = rows > 32
         res[f"kvcache_{Sq}_tokens"] = {
-            "workload": f"c4_decode cache, {Sq} new query tokens per sequence (attn_with_kvcache: split-KV decode "
-                        f"kernel, {Sq * cfg.Hq // cfg.Hkv} query rows per KV head, bottom-right causal)",
+            "workload": f"c4_decode cache, {Sq} new query tokens per sequence (attn_with_kvcache: " +
+                        ("one-slot paged prefill (tcgen05), V tiles converted in shared memory"
+                         if on_prefill_n else "split-KV decode kernel") +
+                        f", {rows} query rows per KV head, bottom-right causal)",
             "value": nbn / tn / 1e9, "unit": "GB/s", "tflops": fln / tn / 1e12, "ms_per_step": tn * 1e3,
             "algorithmic_bytes": nbn,
-            "roofline": {"bound": "hbm", "kernel": "attn_decode_split_kernel", "achieved": nbn / tkn / 1e9,
+            "roofline": {"bound": "hbm", "kernel": "attn_prefill_kernel" if on_prefill_n else "attn_decode_split_kernel",
+                         "achieved": nbn / tkn / 1e9,
                          "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": nbn / tkn / 1e9 / peaks["hbm_gbs"],
                          "kernel_ms": tkn * 1e3,
-                         "traffic": ncu_traffic(f"decode_sq{Sq}", float(cfg.ctx.sum()) * cfg.Hkv)},
-            "launches_per_step": 2 if splits > 1 else 1}
+                         "traffic": ncu_traffic(f"kvcache_sq{Sq}" if on_prefill_n else f"decode_sq{Sq}",
+                                                float(cfg.ctx.sum()) * cfg.Hkv)},
+            "launches_per_step": 3 if on_prefill_n else (2 if splits > 1 else 1)}
 
         def stepv():
             av.attn_with_kvcache(qn, kc, vc, cs, bt, cfg.scale, max_cache_seqlen=mx, out=outn, workspace=wsn,
@@ -796,6 +806,8 @@ def summary(line, peaks, peak_src):
         put("c4_sq8", c4.get("kvcache_8_tokens"))
         put("c4_sq4_v16", c4.get("kvcache_4_tokens_v16"))
         put("c4_sq8_v16", c4.get("kvcache_8_tokens_v16"))
+        put("c4_sq16", c4.get("kvcache_16_tokens"))
+        put("c4_sq16_v16", c4.get("kvcache_16_tokens_v16"))
     c5 = line.get("long_prefill")
     if c5:
         put("c5", c5, c5.get("oracle"), {"step_frac": _r(c5["value"] / peaks["bf16_tflops"], 3)})
