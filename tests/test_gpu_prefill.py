@@ -197,9 +197,11 @@ def test_one_slot_instance_paged_v16_cache():
     assert_lse_close(lse.t().contiguous(), ref_lse.reshape(-1, 32), "one-slot paged v16 lse")
 
 
-def test_varlen_strided_qkv_views():
-    """q, k, v as views of one packed [tokens, Hq + 2 Hkv, D] projection."""
-    lens = np.array([300, 129])
+@pytest.mark.parametrize("lens", [[300, 129], [32, 7, 20]])
+def test_varlen_strided_qkv_views(lens):
+    """q, k, v as views of one packed [tokens, Hq + 2 Hkv, D] projection (two query
+    slots with the conversion pass; one slot, V tiles converted in the kernel)."""
+    lens = np.array(lens)
     Hq, Hkv, D = 16, 4, 128
     T = int(lens.sum())
     qkv = workloads.normal_bf16((21, 1), T, (Hq + 2 * Hkv) * D).view(T, Hq + 2 * Hkv, D)
