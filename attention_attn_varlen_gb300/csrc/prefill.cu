@@ -33,7 +33,7 @@
 // per sequence against a cached context) slot B never has rows; the HALF
 // instance then gives warps 4-7 the keys [64, 128) of slot A's tiles, so each
 // softmax thread works on half a tile, and uses the freed Q_B / P'_B memory for
-// a fourth ring stage.
+// a fourth and a fifth ring stage.
 //
 // PV runs in fp16: the softmax threads write P' = 16 P as fp16 into shared
 // memory (one 128 x 128 tile per slot, K-major, 128-byte swizzle), and V comes
@@ -82,11 +82,12 @@ constexpr int BN = kPrefillKeyTile;    // 128 keys per tile
 constexpr int kPBytes = BM * BN * 2;   // one slot's P' tile (fp16)
 constexpr int kPPanelBytes = BM * 128; // 64 keys of P' per 128-byte-swizzled panel
 
-// HALF (one query slot per unit): no Q_B and no P'_B, a fourth ring stage and
-// the two softmax halves' exchange area instead
+// HALF (one query slot per unit): no Q_B and no P'_B; a fourth and a fifth ring
+// stage and the two softmax halves' exchange area instead (the fifth fits because
+// the dynamic shared memory is declared 1024-byte aligned, so no slack is kept)
 template <int D, bool HALF = false>
 struct PfSmem {
-    static constexpr int kStages = HALF ? 4 : (D == 128 ? 3 : 4);   // K / V' ring stages
+    static constexpr int kStages = HALF ? 5 : (D == 128 ? 3 : 4);   // K / V' ring stages
     static constexpr int kPanels = D / 64;
     static constexpr int kPanelBytes = 128 * 128;            // 128 rows x 128 B
     static constexpr int kTileBytes = kPanels * kPanelBytes; // one Q slot, K tile or V tile
@@ -95,7 +96,7 @@ struct PfSmem {
     static constexpr int kXchOff = kPOff + (HALF ? 1 : 2) * kPBytes;   // [parity][half][row] floats
     static constexpr int kBarOff = kXchOff + (HALF ? 2 * 2 * BM * 4 : 0);
     static constexpr int kNumBars = 3 * kStages + 24;
-    static constexpr int kBytes = kBarOff + kNumBars * 8 + 16 + 1024 /*align slack*/;
+    static constexpr int kBytes = kBarOff + kNumBars * 8 + 16 + (HALF ? 0 : 1024) /*align slack*/;
     static_assert(kBytes <= 227 * 1024, "shared memory");
 };
 
@@ -590,7 +591,14 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                         const PrefillParams p) {
     using S = PfSmem<D, HALF>;
     constexpr int ST = S::kStages;
-    extern __shared__ uint8_t psmem_raw[];
+    extern __shared__ __align__(1024) uint8_t psmem_raw[];
+    if constexpr (HALF) {
+        // no slack for aligning the base: a misaligned one is reported (no access made)
+        if (smem_u32(psmem_raw) & 1023u) {
+            if (threadIdx.x == 0) record_error(p.err, ERR_TIMEOUT | SRC_PREFILL);
+            return;
+        }
+    }
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(psmem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *sQ = sm;
     uint8_t *sRing = sm + S::kRingOff;
