@@ -16,9 +16,10 @@
 // Work unit (taken from the scheduler's list; persistent CTAs, one per SM,
 // take the next entry from a global counter when they start a unit): a
 // sequence b, a KV head, and two query "slots" A and B
-// of 128 rows each.  A slot packs 128/G consecutive tokens x the G query heads
-// that share the KV head (row r = token_offset * G + g), so one K/V stream
-// feeds 256 query rows.  Slot B holds the 128/G tokens after slot A.
+// of 128 rows each.  A slot packs floor(128 / G) consecutive tokens x the G query
+// heads that share the KV head (row r = token_offset * G + g), so one K/V stream
+// feeds 256 query rows (for a G that does not divide 128 a slot's last
+// 128 - floor(128 / G) G rows are idle).  Slot B holds the tokens after slot A's.
 //
 // Roles (352 threads):
 //   warps 0-3  softmax for slot A, one thread per row (TMEM lanes 0-127)
@@ -37,9 +38,11 @@
 //
 // PV runs in fp16: the softmax threads write P' = 16 P as fp16 into shared
 // memory (one 128 x 128 tile per slot, K-major, 128-byte swizzle), and V comes
-// from an fp16 copy V' = V / 16 made by attn_prefill_prep_kernel before the
-// attention kernel (laid out contiguously by sequence, also for a paged
-// cache).  The product P' V' equals P V, and the weights keep 11 significant
+// as V' = fp16(V / 16): from a copy made by attn_prefill_prep_kernel before the
+// attention kernel (laid out contiguously by sequence, also for a paged cache),
+// from the paged fp16 V / 16 cache that store_kvcache keeps, or, in the one-slot
+// instance without that cache, from bf16 V tiles that its softmax threads
+// convert in shared memory.  The product P' V' equals P V, and the weights keep 11 significant
 // bits: with bf16 weights (8 bits) the weight rounding adds about as much error
 // as the bf16 output rounding and the result exceeds a 2e-3 relative RMS error.
 // One MMA takes A and B of the same type, hence the fp16 copy of V.
