@@ -537,6 +537,24 @@ __device__ __noinline__ void pf_store_rows_half(const PrefillParams &p, const CU
     }
 }
 
+// One bf16 pair -> fp16(v / 16) pair: the scaling is exact in bf16 (a power of
+// two), then each half widens to fp32 exactly and the pair rounds to fp16 (RNE,
+// values past the fp16 range clamped).  The same values as scaling in fp32.
+__device__ __forceinline__ uint32_t bf16x2_div16_to_f16x2(uint32_t w) {
+    uint32_t q, r;
+    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(q) : "r"(w), "r"(0x3D803D80u));   // x 0.0625
+    asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;"
+        : "=r"(r)
+        : "f"(__uint_as_float(q & 0xFFFF0000u)), "f"(__uint_as_float(q << 16)));
+    return r;
+}
+
+// Bit 15 / 31 set where that bf16 half has |v| >= 2^20 or is not finite: its
+// magnitude bits plus 0x8000 - 0x4980 reach bit 15 (no carry crosses halves).
+__device__ __forceinline__ uint32_t bf16x2_past_2p20(uint32_t w) {
+    return ((w & 0x7FFF7FFFu) + 0x36803680u) & 0x80008000u;
+}
+
 // One-slot instance without a V' cache: the 256 softmax threads convert a bf16 V
 // tile in its ring stage to V' = fp16(V / 16) in place (the 128-byte swizzle only
 // permutes 16-byte chunks within a key row, so every chunk keeps its row and
@@ -546,45 +564,34 @@ __device__ __noinline__ void pf_store_rows_half(const PrefillParams &p, const CU
 template <int D>
 __device__ __forceinline__ void v_tile_to_f16(uint8_t *tile, int valid, uint32_t *err) {
     constexpr int kChunks = (D / 64) * BN * 8;   // 16-byte chunks in the tile
-    uint32_t big = 0;
+    const bool whole = valid >= BN;
+    uint32_t bad = 0;
 #pragma unroll
     for (int b0 = 0; b0 < kChunks / 256; b0 += 4) {
         uint4 v[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i)
-            v[i] = *reinterpret_cast<const uint4 *>(tile + (size_t)(threadIdx.x + (b0 + i) * 256) * 16);
+            v[i] = *reinterpret_cast<const uint4 *>(tile + (threadIdx.x + (b0 + i) * 256) * 16);
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             const int c = threadIdx.x + (b0 + i) * 256;
             uint4 w = v[i];
-            if (((c >> 3) & (BN - 1)) >= valid) {
+            if (!whole && ((c >> 3) & (BN - 1)) >= valid) {
                 w = make_uint4(0u, 0u, 0u, 0u);
             } else {
-                big = __vmaxu2(big, __vmaxu2(w.x & 0x7FFF7FFFu, w.y & 0x7FFF7FFFu));
-                big = __vmaxu2(big, __vmaxu2(w.z & 0x7FFF7FFFu, w.w & 0x7FFF7FFFu));
-                w.x = bf16x2_to_f16x2_div16(w.x);
-                w.y = bf16x2_to_f16x2_div16(w.y);
-                w.z = bf16x2_to_f16x2_div16(w.z);
-                w.w = bf16x2_to_f16x2_div16(w.w);
+                bad |= bf16x2_past_2p20(w.x) | bf16x2_past_2p20(w.y) | bf16x2_past_2p20(w.z) |
+                       bf16x2_past_2p20(w.w);
+                w.x = bf16x2_div16_to_f16x2(w.x);
+                w.y = bf16x2_div16_to_f16x2(w.y);
+                w.z = bf16x2_div16_to_f16x2(w.z);
+                w.w = bf16x2_div16_to_f16x2(w.w);
             }
-            *reinterpret_cast<uint4 *>(tile + (size_t)c * 16) = w;
+            *reinterpret_cast<uint4 *>(tile + c * 16) = w;
         }
     }
-    if (__any_sync(0xffffffffu, (big & 0xFFFFu) >= 0x4980u || (big >> 16) >= 0x4980u) && (threadIdx.x & 31) == 0)
-        record_error(err, ERR_RANGE | SRC_PREFILL);
+    if (__any_sync(0xffffffffu, bad != 0u) && (threadIdx.x & 31) == 0) record_error(err, ERR_RANGE | SRC_PREFILL);
 }
 
-// EARLY: the producer takes and publishes the next unit's index at the start of
-// each unit, so every role has it a whole unit ahead (the unit boundary costs
-// less).  Otherwise it takes it when it starts the unit's loads, which keeps
-// the units of one sequence and KV head side by side in time, sharing their
-// K / V tiles through L2: the launcher chooses EARLY for short keys only, where
-// that sharing is worth little and the boundary costs weigh most.
-// HALF: every sequence fits one query slot (at most 128 / G tokens), so slot B
-// never has rows; its softmax warps take half of each of slot A's key tiles.
-// OBOX: G divides 128, so a slot is 128 rows and a warp's 32 output rows form one
-// (heads x tokens) TMA store box.  Otherwise a slot is 128 / G * G rows, the rest
-// of its Q rows are zeroed once, and output rows are written row by row.
 // CVT (HALF only, no V' cache): V tiles are loaded as bf16 from v and the softmax
 // warps convert each to V' in its ring stage (no conversion pass).
 template <int D, bool EARLY, bool HALF, bool OBOX, bool CVT>
