@@ -769,11 +769,15 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             }
             // ring order K_0, K_1, V_0, K_2, V_1, ..., K_{n-1}, V_{n-2}, V_{n-1}: each K tile
             // one step ahead of the V' tile it pairs with, so the next QK^T's tile can land
-            // while the PV of the current one still holds its stage
+            // while the PV of the current one still holds its stage.  CVT: K_0, V_0, K_1,
+            // V_1, ...: a V tile lands before the softmax threads come to convert it
             for (int j = 0; j < w.n && ok; ++j) {
                 for (int step = 0; step < 3; ++step) {
                     int wv, tj;   // 0: K tile, 1: V tile; key tile index
-                    if (step == 0) {
+                    if constexpr (CVT) {   // K_j, V_j
+                        if (step == 1) continue;
+                        wv = step == 2 ? 1 : 0, tj = j;
+                    } else if (step == 0) {
                         if (j > 0) continue;
                         wv = 0, tj = 0;
                     } else if (step == 1) {
@@ -863,7 +867,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                 if (!ok) break;
                 tc_fence_after();
                 for (int j = 0; j < w.n && ok; ++j) {
-                    const int itK = itb + (j == 0 ? 0 : 2 * j - 1), stK = itK % ST;   // the producer's ring order
+                    const int itK = itb + (CVT ? 2 * j : (j == 0 ? 0 : 2 * j - 1)), stK = itK % ST;   // the producer's ring order
                     ok = mbar_wait(&full_k[stK], (kpar >> stK) & 1u, abort_flag, p.err, SRC_PREFILL);
                     kpar ^= 1u << stK;
                     if (!ok) break;
@@ -911,7 +915,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                 // PV_X(0) of a unit writes O_X afresh: its p_ready comes after the
                 // softmax threads have read O_X of the previous unit
                 for (int j = 0; j < w.n && ok; ++j) {
-                    const int itV = itb + (j < w.n - 1 ? 2 * j + 2 : 2 * w.n - 1), stV = itV % ST;
+                    const int itV = itb + (CVT ? 2 * j + 1 : (j < w.n - 1 ? 2 * j + 2 : 2 * w.n - 1)), stV = itV % ST;
                     ok = mbar_wait(&full_v[stV], (vpar >> stV) & 1u, abort_flag, p.err, SRC_PREFILL);
                     vpar ^= 1u << stV;
                     if (!ok) break;
@@ -1052,7 +1056,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                 if constexpr (CVT) {
                     // V tile j (bf16 as loaded) -> V' = fp16(V / 16) in place, before p_ready;
                     // rows past the sequence's last key are zeroed
-                    const int itV = itb + (j < nX - 1 ? 2 * j + 2 : 2 * nX - 1), stV = itV % ST;
+                    const int itV = itb + 2 * j + 1, stV = itV % ST;   // K_j, V_j order
                     ok = __all_sync(0xffffffffu, mbar_wait(&full_v[stV], (vpar >> stV) & 1u, abort_flag, p.err,
                                                            SRC_PREFILL));
                     vpar ^= 1u << stV;
