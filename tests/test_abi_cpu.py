@@ -139,3 +139,22 @@ def test_host_entry_checks_offsets_on_the_host(L):
     assert call([0, 100, 150], [0, 100, 150], ev=null) == 1
     # valid offsets reach the device query, which fails without a GPU
     assert call([0, 100, 150], [0, 100, 150]) == 7
+
+
+def test_group_sizes_that_do_not_divide_128(L):
+    """Prefill sizes for any group up to 128 heads per KV head: floor(128 / G) tokens
+    per slot, so the unit list grows with ceil(Lq / (2 floor(128 / G))); G > 128 is
+    refused (size 0)."""
+    L.attn_varlen_workspace_size.restype = ctypes.c_size_t
+    i64 = ctypes.c_int64
+    # head_dim 64 (no one-slot instance): header + V' copy + unit list
+    for G, tps in ((3, 42), (5, 25), (6, 21), (7, 18), (48, 2), (96, 1), (128, 1)):
+        one = L.attn_varlen_workspace_size(2, G, 1, 64, 2 * tps, i64(0))
+        two = L.attn_varlen_workspace_size(2, G, 1, 64, 2 * tps + 1, i64(0))
+        assert 0 < one < two, G   # one more query pair per sequence past 2 floor(128 / G) tokens
+    assert L.attn_varlen_workspace_size(2, 129, 1, 64, 8, i64(0)) == 0
+    # the kv-cache entry: G = 5 at head_dim 128, 8 new tokens = 40 rows -> one-slot prefill,
+    # no V' copy; 4 new tokens = 20 rows -> decode partials only
+    L.attn_kvcache_workspace_size.restype = ctypes.c_size_t
+    assert L.attn_kvcache_workspace_size(4, 8, 40, 8, 128, 1000) == L.attn_kvcache_workspace_size(4, 8, 40, 8, 128, 10 ** 6)
+    assert 0 < L.attn_kvcache_workspace_size(4, 4, 40, 8, 128, 10 ** 6) <= 4 * 4 * 40 * 64 * 129 * 4 + 256
