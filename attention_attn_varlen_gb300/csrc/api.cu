@@ -116,9 +116,9 @@ constexpr int kDecodeMaxColumns = 64;   // Sq x G query columns per KV head on t
 // ... with the fp16 V / 16 cache: past one column group of 16 the paged prefill
 // (tcgen05, no conversion pass with that cache) streams the cache faster
 constexpr int kDecodeMaxColumnsV16 = 16;
-// ... and without it at head_dim 128: past two column groups the one-slot prefill,
+// ... and without it at head_dim 128: past one column group the one-slot prefill,
 // converting each V tile in shared memory, streams the cache faster
-constexpr int kDecodeMaxColumnsCvt = 32;
+constexpr int kDecodeMaxColumnsCvt = 16;
 constexpr int kDecodeTile = 64;
 
 // Tokens a split streams at most when the library chooses the split count: long
@@ -174,9 +174,9 @@ size_t decode_partial_bytes(int batch, int seqlen_q, int num_heads_q, int head_d
 }
 
 // The kv-cache entry runs on the decode kernel when the Sq x G query rows of a
-// KV head fit four column groups of 16 (one group when the fp16 V / 16 cache is
-// given, two at head_dim 128 without it, where the prefill can take the group
-// size); otherwise on the paged varlen prefill.
+// KV head fit four column groups of 16 (one group at head_dim 128, with or without
+// the fp16 V / 16 cache, and with that cache at head_dim 64, where the prefill can
+// take the group size); otherwise on the paged varlen prefill.
 bool kvcache_on_decode(int batch, int seqlen_q, int num_heads_q, int num_heads_kv, int head_dim, bool v16) {
     if (num_heads_q <= 0 || num_heads_kv <= 0 || num_heads_q % num_heads_kv) return false;
     if (head_dim != 64 && head_dim != 128) return false;

@@ -562,19 +562,19 @@ __device__ __forceinline__ uint32_t bf16x2_past_2p20(uint32_t w) {
 // are zeroed; |v| >= 2^20 or non-finite is clamped and reported, as in the
 // conversion pass.  The caller's proxy fence and p_ready arrival publish it.
 template <int D>
-__device__ __forceinline__ void v_tile_to_f16(uint8_t *tile, int valid, uint32_t *err) {
+__device__ __forceinline__ void v_tile_to_f16(uint8_t *tile, int valid, uint32_t *err, int ci, int cs) {
     constexpr int kChunks = (D / 64) * BN * 8;   // 16-byte chunks in the tile
     const bool whole = valid >= BN;
     uint32_t bad = 0;
-#pragma unroll
-    for (int b0 = 0; b0 < kChunks / 256; b0 += 4) {
+    for (int c0 = ci; c0 < kChunks; c0 += 4 * cs) {
         uint4 v[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i)
-            v[i] = *reinterpret_cast<const uint4 *>(tile + (threadIdx.x + (b0 + i) * 256) * 16);
+            if (c0 + i * cs < kChunks) v[i] = *reinterpret_cast<const uint4 *>(tile + (c0 + i * cs) * 16);
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            const int c = threadIdx.x + (b0 + i) * 256;
+            const int c = c0 + i * cs;
+            if (c >= kChunks) break;
             uint4 w = v[i];
             if (!whole && ((c >> 3) & (BN - 1)) >= valid) {
                 w = make_uint4(0u, 0u, 0u, 0u);
@@ -999,8 +999,46 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             const int nX = w.nA;
             const int tok = t0 + r / G;
             const int lim = p.causal ? min(tok + w.off, w.Lk - 1) : w.Lk - 1;
+            // lane groups holding none of the unit's rows (a decode-like unit fills few
+            // of the slot's 128) skip the softmax and only keep the barriers' phases;
+            // with CVT their threads convert the V tiles, which all 256 threads do when
+            // every lane group holds rows
+            const int ngrp = (min(max(w.Lq - t0, 0), BM / G) * G + 31) / 32;
             float m_ref = -INFINITY;
             float l = 0.f;   // this half's share of d'
+            if (g4 >= ngrp) {
+                for (int j = 0; j < nX; ++j) {
+                    const int t = cX + j;
+                    ok = __all_sync(0xffffffffu,
+                                    mbar_wait(&s_full[0], (uint32_t)t & 1u, abort_flag, p.err, SRC_PREFILL));
+                    if (!ok) break;
+                    mbar_arrive(&s_free[0]);
+                    if constexpr (CVT) {
+                        const int itV = itb + 2 * j + 1, stV = itV % ST;   // K_j, V_j order
+                        const uint32_t vph = (vpar >> stV) & 1u;
+                        vpar ^= 1u << stV;
+                        ok = __all_sync(0xffffffffu, mbar_wait(&full_v[stV], vph, abort_flag, p.err, SRC_PREFILL));
+                        if (!ok) break;
+                        v_tile_to_f16<D>(sRing + stV * S::kTileBytes, w.Lk - j * BN, p.err,
+                                         (h * (4 - ngrp) + (g4 - ngrp)) * 32 + lane, (4 - ngrp) * 64);
+                    }
+                    // p_ready(t) only after p_ready(t - 1) has completed (PV(t - 1) done)
+                    if (t > 0) {
+                        ok = __all_sync(0xffffffffu, mbar_wait(&pv_done[0], (uint32_t)(t - 1) & 1u, abort_flag,
+                                                               p.err, SRC_PREFILL));
+                        if (!ok) break;
+                        tc_fence_after();
+                    }
+                    if (pend) {
+                        pf_store_rows_half<D, OBOX>(p, &omap, tO, sP, pend_tiles, pend_qbase, pend_ntok, pend_hkv,
+                                                    pend_l, pend_m, h);
+                        pend = false;
+                    }
+                    fence_proxy_async_smem();
+                    tc_fence_before();
+                    mbar_arrive(&p_ready[0]);
+                }
+            } else
             for (int j = 0; j < nX; ++j) {
                 const int t = cX + j;
                 ok = __all_sync(0xffffffffu,
@@ -1055,13 +1093,16 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                 l += ((la[0] + lb[0]) + (la[1] + lb[1])) + ((la[2] + lb[2]) + (la[3] + lb[3]));
                 if constexpr (CVT) {
                     // V tile j (bf16 as loaded) -> V' = fp16(V / 16) in place, before p_ready;
-                    // rows past the sequence's last key are zeroed
+                    // rows past the sequence's last key are zeroed.  Every thread keeps the
+                    // stage parities; these threads convert only when no lane group is idle.
                     const int itV = itb + 2 * j + 1, stV = itV % ST;   // K_j, V_j order
-                    ok = __all_sync(0xffffffffu, mbar_wait(&full_v[stV], (vpar >> stV) & 1u, abort_flag, p.err,
-                                                           SRC_PREFILL));
+                    const uint32_t vph = (vpar >> stV) & 1u;
                     vpar ^= 1u << stV;
-                    if (!ok) break;
-                    v_tile_to_f16<D>(sRing + stV * S::kTileBytes, w.Lk - j * BN, p.err);
+                    if (ngrp == 4) {
+                        ok = __all_sync(0xffffffffu, mbar_wait(&full_v[stV], vph, abort_flag, p.err, SRC_PREFILL));
+                        if (!ok) break;
+                        v_tile_to_f16<D>(sRing + stV * S::kTileBytes, w.Lk - j * BN, p.err, threadIdx.x, 256);
+                    }
                 }
                 if (t > 0) {
                     ok = __all_sync(0xffffffffu, mbar_wait(&pv_done[0], (uint32_t)(t - 1) & 1u, abort_flag, p.err,
@@ -1095,7 +1136,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                 mbar_arrive(&p_ready[0]);
             }
             if (!ok) break;
-            const float ltot = l + exchange(l);   // the unit's d' over both halves
+            const float ltot = g4 < ngrp ? l + exchange(l) : 0.f;   // the unit's d' over both halves
             if (!ok) break;
             if (pend) {   // no key tiles in this unit: store the previous unit's rows now
                 if (cX > 0) {

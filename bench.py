@@ -173,6 +173,7 @@ KERNEL_SOURCES = {
     "decode_sq8": ["attention_attn_varlen_gb300/csrc/decode.cu", "attention_attn_varlen_gb300/csrc/common.cuh"],
     "kvcache_sq4_v16": ["attention_attn_varlen_gb300/csrc/decode.cu", "attention_attn_varlen_gb300/csrc/common.cuh"],
     "kvcache_sq8_v16": ["attention_attn_varlen_gb300/csrc/prefill.cu", "attention_attn_varlen_gb300/csrc/common.cuh"],
+    "kvcache_sq8": ["attention_attn_varlen_gb300/csrc/prefill.cu", "attention_attn_varlen_gb300/csrc/common.cuh"],
     "kvcache_sq16": ["attention_attn_varlen_gb300/csrc/prefill.cu", "attention_attn_varlen_gb300/csrc/common.cuh"],
     "kvcache_sq16_v16": ["attention_attn_varlen_gb300/csrc/prefill.cu", "attention_attn_varlen_gb300/csrc/common.cuh"],
     "store": ["attention_attn_varlen_gb300/csrc/store_kvcache.cu", "attention_attn_varlen_gb300/csrc/common.cuh"],
@@ -361,10 +362,10 @@ def bench_decode(av, device, steps, warmup, flush, peaks, with_oracle=True):
         tkn = float(np.mean(kmsn)) / 1e3
         fln = workloads.prefill_flops(np.full(cfg.batch, Sq), cfg.ctx, cfg.Hq, cfg.D)
         nbn = nbytes + 2 * cfg.batch * (Sq - 1) * cfg.Hq * cfg.D * 2    # the extra query and output rows
-        # past 32 query rows per KV head (head_dim 128) the entry runs the one-slot
+        # past 16 query rows per KV head (head_dim 128) the entry runs the one-slot
         # paged prefill, which converts the bf16 V tiles in shared memory
         rows = Sq * cfg.Hq // cfg.Hkv
-        on_prefill_n = rows > 32
+        on_prefill_n = rows > 16
         res[f"kvcache_{Sq}_tokens"] = {
             "workload": f"c4_decode cache, {Sq} new query tokens per sequence (attn_with_kvcache: " +
                         ("one-slot paged prefill (tcgen05), V tiles converted in shared memory"

@@ -14,7 +14,7 @@ pytestmark = pytest.mark.gpu
 
 CASES = [
     # seed, ctx, Sq, Hq, Hkv, D, block_size
-    # Sq x G <= 16 query rows per KV head: the split-KV decode kernel
+    # Sq x G <= 16 query rows per KV head (<= 64 at head_dim 64): the split-KV decode kernel
     (61, [37, 5, 300], 1, 32, 8, 128, 16),
     (62, [1000, 257, 0], 2, 32, 8, 128, 256),
     (63, [511, 2048], 7, 8, 8, 128, 64),
@@ -23,11 +23,11 @@ CASES = [
     (70, [500, 77], 2, 64, 8, 128, 64),              # G = 8
     (71, [1200, 5, 64], 1, 32, 2, 128, 16),          # G = 16, one token
     (72, [64, 0, 191], 3, 16, 4, 64, 16),            # twelve live columns of sixteen
-    (77, [300, 1500, 7], 8, 32, 8, 128, 64),         # 32 columns: two column groups
+    (77, [300, 1500, 7], 8, 32, 8, 128, 64),         # 32 rows at head_dim 128: the one-slot prefill
     (78, [129, 640], 5, 64, 8, 64, 16),              # 40 columns at head_dim 64: three groups, the last one half full
     (79, [2000, 33], 64, 8, 8, 64, 32),              # G = 1, 64 new tokens: four groups
-    (80, [400, 1300], 8, 24, 8, 128, 64),            # G = 3: decode kernel; with V/16 the prefill (42-token slots)
-    # larger Sq x G: the paged varlen prefill (at head_dim 128 past 32 columns: one slot, V converted in the kernel)
+    (80, [400, 1300], 8, 24, 8, 128, 64),            # G = 3, 24 rows: the one-slot prefill (42-token slots)
+    # larger Sq x G: the paged varlen prefill (at head_dim 128 up to 128 rows: one slot, V converted in the kernel)
     (81, [129, 640, 3000], 5, 64, 8, 128, 16),       # 40 columns
     (82, [2000, 17, 0, 900], 16, 32, 8, 128, 64),    # 64 columns
     (64, [90, 700, 1], 64, 16, 2, 64, 32),
