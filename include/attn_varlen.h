@@ -324,8 +324,8 @@ ATTN_API size_t attn_padded_workspace_size(int batch, int seqlen_q, int seqlen_k
  * [B, seqlen_q, H, D] and seqlen_q >= 1: chunked append, speculative
  * verification).  Two routes, chosen from the sizes and from whether
  * v16_cache is given:
- *  - seqlen_q * (num_heads_q / num_heads_kv) <= 64 at head_dim 64, <= 32 at
- *    head_dim 128, <= 16 with v16_cache: the split-KV decode kernel of attn_decode_paged with
+ *  - seqlen_q * (num_heads_q / num_heads_kv) <= 64 at head_dim 64, <= 16 at
+ *    head_dim 128 or with v16_cache: the split-KV decode kernel of attn_decode_paged with
  *    one query column per (new token, head), up to 16 columns per CTA; the
  *    cache is read from HBM once (CTAs holding other columns of the same KV
  *    head re-read it from L2).  With seqlen_q = 1 the result equals
